@@ -1,0 +1,285 @@
+// api.cu — the extern "C" boundary of libnt.so (declared in include/nt.h):
+// context management and argument checking of every single-op entry point.
+// Nothing is launched until every check has passed.
+#include <cstring>
+
+#include "nt_internal.cuh"
+#include "ops.cuh"
+
+namespace nt {
+
+nt_status set_err(Ctx* c, nt_status s, const char* fmt, ...) {
+  if (c) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    c->last_error = buf;
+  }
+  return s;
+}
+
+nt_status cuda_check(Ctx* c, cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return NT_OK;
+  return set_err(c, e == cudaErrorMemoryAllocation ? NT_ERR_OOM : NT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace nt
+
+using namespace nt;
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    cudaGetDevice(&prev);
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (prev >= 0 && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+#define NT_REQUIRE(cond, code, ...)                         \
+  do {                                                      \
+    if (!(cond)) return set_err(ctx, code, __VA_ARGS__);    \
+  } while (0)
+
+nt_status check_fmt_cols(nt_ctx* ctx, int fmt, int64_t cols) {
+  NT_REQUIRE(fmt_ok(fmt), NT_ERR_UNSUPPORTED_FMT, "unknown format id %d", fmt);
+  NT_REQUIRE(cols > 0 && cols % block_elems(fmt) == 0, NT_ERR_INVALID_ARG,
+             "cols=%lld is not a positive multiple of the block size %d", (long long)cols, block_elems(fmt));
+  NT_REQUIRE(cols <= (int64_t(1) << 30), NT_ERR_INVALID_ARG, "cols=%lld too large", (long long)cols);
+  return NT_OK;
+}
+
+nt_status check_vec(nt_ctx* ctx, const void* p, const char* name) {
+  NT_REQUIRE(p != nullptr, NT_ERR_INVALID_ARG, "%s is NULL", name);
+  NT_REQUIRE(aligned(p, 16), NT_ERR_ALIGNMENT, "%s must be 16-byte aligned", name);
+  return NT_OK;
+}
+
+// surface a pending device error flag / sticky CUDA error before new work
+nt_status pre_call(nt_ctx* ctx) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  return NT_OK;
+}
+
+}  // namespace
+
+#define NT_TRY(expr)                  \
+  do {                                \
+    nt_status s_ = (expr);            \
+    if (s_ != NT_OK) return s_;       \
+  } while (0)
+
+extern "C" {
+
+int nt_block_bytes(int fmt) { return fmt_ok(fmt) ? block_bytes(fmt) : 0; }
+int nt_block_elems(int fmt) { return fmt_ok(fmt) ? block_elems(fmt) : 0; }
+
+nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes) {
+  if (!out) return NT_ERR_INVALID_ARG;
+  *out = nullptr;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    cudaGetLastError();
+    return NT_ERR_CUDA;
+  }
+  DeviceGuard g(device);
+  nt_ctx* c = new (std::nothrow) nt_ctx();
+  if (!c) return NT_ERR_OOM;
+  c->device = device;
+  int v = 0;
+  cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device);
+  c->num_sms = v;
+  cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  c->smem_optin = size_t(v);
+  c->scratch_bytes = scratch_bytes ? scratch_bytes : (size_t(64) << 20);
+  if (c->scratch_bytes < (size_t(1) << 20)) c->scratch_bytes = size_t(1) << 20;
+  if (cudaMalloc(&c->scratch, c->scratch_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    return NT_ERR_OOM;
+  }
+  if (cudaMemset(c->scratch, 0, c->scratch_bytes) != cudaSuccess) {
+    cudaFree(c->scratch);
+    delete c;
+    return NT_ERR_CUDA;
+  }
+  c->err_flag = reinterpret_cast<unsigned*>(c->scratch + kScratchErr);
+  *out = c;
+  return NT_OK;
+}
+
+nt_status nt_ctx_destroy(nt_ctx* ctx) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  {
+    DeviceGuard g(ctx->device);
+    cudaDeviceSynchronize();
+    cudaFree(ctx->scratch);
+  }
+  delete ctx;
+  return NT_OK;
+}
+
+nt_status nt_ctx_sync(nt_ctx* ctx) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_check(ctx, e, "device synchronize");
+  unsigned flag = 0;
+  e = cudaMemcpy(&flag, ctx->err_flag, sizeof flag, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_check(ctx, e, "read device error flag");
+  if (flag) {
+    cudaMemset(ctx->err_flag, 0, sizeof(unsigned));
+    return set_err(ctx, NT_ERR_TIMEOUT, "a device-side bounded wait ran out (flag 0x%x)", flag);
+  }
+  return NT_OK;
+}
+
+const char* nt_last_error(const nt_ctx* ctx) { return ctx ? ctx->last_error.c_str() : "null context"; }
+
+nt_status nt_dequant_rows(nt_ctx* ctx, int fmt, const void* W, int64_t row0, int64_t nrows, int64_t cols,
+                          float* out, void* stream) {
+  NT_TRY(pre_call(ctx));
+  NT_TRY(check_fmt_cols(ctx, fmt, cols));
+  NT_REQUIRE(W && out, NT_ERR_INVALID_ARG, "null pointer");
+  NT_REQUIRE(row0 >= 0 && nrows >= 0, NT_ERR_INVALID_ARG, "negative row range");
+  NT_REQUIRE(aligned(W, 2), NT_ERR_ALIGNMENT, "W must be 2-byte aligned");
+  NT_REQUIRE(aligned(out, 4), NT_ERR_ALIGNMENT, "out must be 4-byte aligned");
+  DeviceGuard g(ctx->device);
+  return launch_dequant(ctx, fmt, W, row0, nrows, cols, out, as_stream(stream));
+}
+
+nt_status nt_gemv_q_multi(nt_ctx* ctx, int fmt, const nt_gemv_job* jobs, int njobs, const float* x,
+                          const float* norm_g, float eps, int64_t cols, void* stream) {
+  NT_TRY(pre_call(ctx));
+  NT_TRY(check_fmt_cols(ctx, fmt, cols));
+  NT_REQUIRE(jobs && njobs >= 1 && njobs <= 3, NT_ERR_INVALID_ARG, "njobs must be 1..3");
+  NT_TRY(check_vec(ctx, x, "x"));
+  if (norm_g) NT_TRY(check_vec(ctx, norm_g, "norm_g"));
+  for (int j = 0; j < njobs; ++j) {
+    NT_REQUIRE(jobs[j].rows >= 0, NT_ERR_INVALID_ARG, "job %d: negative rows", j);
+    if (jobs[j].rows == 0) continue;
+    NT_REQUIRE(jobs[j].W_dev && jobs[j].y_dev, NT_ERR_INVALID_ARG, "job %d: null W or y", j);
+    NT_REQUIRE(aligned(jobs[j].W_dev, 2), NT_ERR_ALIGNMENT, "job %d: W must be 2-byte aligned", j);
+    NT_REQUIRE(aligned(jobs[j].y_dev, 4), NT_ERR_ALIGNMENT, "job %d: y must be 4-byte aligned", j);
+    NT_REQUIRE(!jobs[j].residual_dev || aligned(jobs[j].residual_dev, 4), NT_ERR_ALIGNMENT,
+               "job %d: residual must be 4-byte aligned", j);
+  }
+  DeviceGuard g(ctx->device);
+  return launch_gemv(ctx, fmt, jobs, njobs, nullptr, x, norm_g, eps, cols, false, as_stream(stream));
+}
+
+nt_status nt_gemv_q(nt_ctx* ctx, int fmt, const void* W, const float* x, float* y, int64_t rows, int64_t cols,
+                    const float* residual, void* stream) {
+  nt_gemv_job j{W, y, residual, rows};
+  return nt_gemv_q_multi(ctx, fmt, &j, 1, x, nullptr, 0.f, cols, stream);
+}
+
+nt_status nt_gemv_q_swiglu(nt_ctx* ctx, int fmt, const void* Wg, const void* Wu, const float* x, float* h,
+                           int64_t rows, int64_t cols, void* stream) {
+  NT_TRY(pre_call(ctx));
+  NT_TRY(check_fmt_cols(ctx, fmt, cols));
+  NT_TRY(check_vec(ctx, x, "x"));
+  NT_REQUIRE(rows >= 0, NT_ERR_INVALID_ARG, "negative rows");
+  if (rows == 0) return NT_OK;
+  NT_REQUIRE(Wg && Wu && h, NT_ERR_INVALID_ARG, "null pointer");
+  NT_REQUIRE(aligned(Wg, 2) && aligned(Wu, 2), NT_ERR_ALIGNMENT, "weights must be 2-byte aligned");
+  NT_REQUIRE(aligned(h, 4), NT_ERR_ALIGNMENT, "h must be 4-byte aligned");
+  nt_gemv_job j{Wg, h, nullptr, rows};
+  DeviceGuard g(ctx->device);
+  return launch_gemv(ctx, fmt, &j, 1, Wu, x, nullptr, 0.f, cols, true, as_stream(stream));
+}
+
+nt_status nt_rmsnorm(nt_ctx* ctx, const float* x, const float* g, float* y, int64_t n, float eps, void* stream) {
+  NT_TRY(pre_call(ctx));
+  NT_REQUIRE(x && g && y && n > 0, NT_ERR_INVALID_ARG, "null pointer or n <= 0");
+  NT_REQUIRE(aligned(x, 4) && aligned(g, 4) && aligned(y, 4), NT_ERR_ALIGNMENT, "vectors must be 4-byte aligned");
+  NT_REQUIRE(eps >= 0.f, NT_ERR_INVALID_ARG, "eps must be >= 0");
+  DeviceGuard gd(ctx->device);
+  return launch_rmsnorm(ctx, x, g, y, n, eps, as_stream(stream));
+}
+
+nt_status nt_rope(nt_ctx* ctx, float* q, float* k, int n_qh, int n_kvh, int head_dim, int64_t pos, float theta,
+                  void* stream) {
+  NT_TRY(pre_call(ctx));
+  NT_REQUIRE(q && n_qh > 0 && (!k || n_kvh > 0), NT_ERR_INVALID_ARG, "bad q/k or head counts");
+  NT_REQUIRE(head_dim > 0 && head_dim % 2 == 0 && head_dim <= 512, NT_ERR_INVALID_ARG, "head_dim must be even, <= 512");
+  NT_REQUIRE(pos >= 0 && theta > 0.f, NT_ERR_INVALID_ARG, "pos must be >= 0 and theta > 0");
+  DeviceGuard g(ctx->device);
+  return launch_rope(ctx, q, k, n_qh, n_kvh, head_dim, pos, theta, as_stream(stream));
+}
+
+nt_status nt_rope_kv_append(nt_ctx* ctx, float* q, const float* k, const float* v, void* kc, void* vc, int n_qh,
+                            int n_kvh, int head_dim, int64_t pos, int64_t kv_stride, float theta, void* stream) {
+  NT_TRY(pre_call(ctx));
+  NT_REQUIRE(q && k && v && kc && vc, NT_ERR_INVALID_ARG, "null pointer");
+  NT_REQUIRE(n_qh > 0 && n_kvh > 0, NT_ERR_INVALID_ARG, "bad head counts");
+  NT_REQUIRE(head_dim > 0 && head_dim % 2 == 0 && head_dim <= 512, NT_ERR_INVALID_ARG, "head_dim must be even, <= 512");
+  NT_REQUIRE(pos >= 0 && pos < kv_stride, NT_ERR_INVALID_ARG, "pos=%lld outside the cache (stride %lld)",
+             (long long)pos, (long long)kv_stride);
+  NT_REQUIRE(aligned(kc, 2) && aligned(vc, 2), NT_ERR_ALIGNMENT, "caches must be 2-byte aligned");
+  DeviceGuard g(ctx->device);
+  return launch_rope_append(ctx, q, k, v, kc, vc, n_qh, n_kvh, head_dim, pos, nullptr, kv_stride, theta,
+                            as_stream(stream));
+}
+
+nt_status nt_attn_decode(nt_ctx* ctx, const float* q, const void* kc, const void* vc, float* out, int n_qh,
+                         int n_kvh, int head_dim, int64_t n_pos, int64_t kv_stride, void* stream) {
+  NT_TRY(pre_call(ctx));
+  NT_REQUIRE(q && kc && vc && out, NT_ERR_INVALID_ARG, "null pointer");
+  NT_REQUIRE(head_dim == 128, NT_ERR_INVALID_ARG, "head_dim must be 128");
+  NT_REQUIRE(n_kvh > 0 && n_qh > 0 && n_qh % n_kvh == 0 && n_qh / n_kvh <= 16 && n_kvh <= 64, NT_ERR_INVALID_ARG,
+             "n_qh must be a multiple of n_kvh, group <= 16, n_kvh <= 64");
+  NT_REQUIRE(n_pos >= 1 && n_pos <= kv_stride, NT_ERR_INVALID_ARG, "need 1 <= n_pos <= kv_stride");
+  NT_TRY(check_vec(ctx, q, "q"));
+  NT_TRY(check_vec(ctx, out, "out"));
+  NT_REQUIRE(aligned(kc, 16) && aligned(vc, 16), NT_ERR_ALIGNMENT, "caches must be 16-byte aligned");
+  const int S = attn_splits(ctx, n_kvh, kv_stride);
+  const size_t need = attn_scratch_bytes(n_qh, n_kvh, S);
+  NT_REQUIRE(kScratchAttn + need <= ctx->scratch_bytes, NT_ERR_OOM, "attention needs %zu scratch bytes", need);
+  float* part = reinterpret_cast<float*>(ctx->scratch + kScratchAttn + 64 * sizeof(unsigned));
+  unsigned* counters = reinterpret_cast<unsigned*>(ctx->scratch + kScratchAttn);
+  DeviceGuard g(ctx->device);
+  return launch_attn(ctx, q, kc, vc, out, n_qh, n_kvh, n_pos, nullptr, kv_stride, part, counters, S,
+                     as_stream(stream));
+}
+
+nt_status nt_softmax(nt_ctx* ctx, const float* x, float* y, int64_t n, void* stream) {
+  NT_TRY(pre_call(ctx));
+  NT_REQUIRE(x && y && n > 0, NT_ERR_INVALID_ARG, "null pointer or n <= 0");
+  DeviceGuard g(ctx->device);
+  return launch_softmax(ctx, x, y, n, as_stream(stream));
+}
+
+nt_status nt_swiglu(nt_ctx* ctx, const float* gate, const float* up, float* h, int64_t n, void* stream) {
+  NT_TRY(pre_call(ctx));
+  NT_REQUIRE(gate && up && h && n >= 0, NT_ERR_INVALID_ARG, "null pointer or n < 0");
+  if (n == 0) return NT_OK;
+  DeviceGuard g(ctx->device);
+  return launch_swiglu(ctx, gate, up, h, n, as_stream(stream));
+}
+
+nt_status nt_argmax(nt_ctx* ctx, const float* v, int64_t n, int32_t* out, void* stream) {
+  NT_TRY(pre_call(ctx));
+  NT_REQUIRE(v && out && n > 0 && n < (int64_t(1) << 31), NT_ERR_INVALID_ARG, "null pointer or bad n");
+  auto* key = reinterpret_cast<unsigned long long*>(ctx->scratch + kScratchArgmax);
+  auto* counter = reinterpret_cast<unsigned*>(ctx->scratch + kScratchArgmax + 8);
+  DeviceGuard g(ctx->device);
+  return launch_argmax(ctx, v, n, out, key, counter, as_stream(stream));
+}
+
+nt_status nt_cos_sim(nt_ctx* ctx, const float* a, const float* b, int64_t n, float* out, void* stream) {
+  NT_TRY(pre_call(ctx));
+  NT_REQUIRE(a && b && out && n > 0, NT_ERR_INVALID_ARG, "null pointer or n <= 0");
+  DeviceGuard g(ctx->device);
+  return launch_cos(ctx, a, b, n, out, as_stream(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// nt_internal.cuh — shared internals of libnt.so: the context, status
+// helpers, and the inline-PTX wrappers for mbarriers and TMA bulk copies.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/nt.h"
+
+namespace nt {
+
+constexpr int kMaxSpin = 1 << 22;   // iteration cap of every device-side wait
+constexpr unsigned kErrWaitTimeout = 1u;
+
+struct Ctx {
+  int device = 0;
+  int num_sms = 0;
+  size_t smem_optin = 0;
+  char* scratch = nullptr;      // device scratch owned by the context
+  size_t scratch_bytes = 0;
+  unsigned* err_flag = nullptr; // device word, set by kernels whose bounded wait ran out
+  std::string last_error;
+  std::mutex mu;
+};
+
+// host-side status helpers ----------------------------------------------------
+nt_status set_err(Ctx* c, nt_status s, const char* fmt, ...);
+nt_status cuda_check(Ctx* c, cudaError_t e, const char* what);
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// scratch layout (bytes from ctx->scratch) ------------------------------------
+constexpr size_t kScratchErr = 0;            // unsigned err flag (also ctx->err_flag)
+constexpr size_t kScratchArgmax = 256;       // unsigned long long key + unsigned counter
+constexpr size_t kScratchAttn = 4096;        // attention partials + counters
+
+// format geometry ---------------------------------------------------------------
+__host__ __device__ constexpr int block_elems(int fmt) { return fmt <= NT_Q4_0 ? 32 : 256; }
+__host__ __device__ constexpr int block_bytes(int fmt) {
+  return fmt == NT_Q8_0 ? 34 : fmt == NT_Q4_0 ? 18 : fmt == NT_Q4_K ? 144 : fmt == NT_Q5_K ? 176 : 210;
+}
+inline bool fmt_ok(int fmt) { return fmt >= NT_Q8_0 && fmt <= NT_Q6_K; }
+
+// device helpers -----------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Bounded wait on phase `parity` of an mbarrier; false if the cap ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < kMaxSpin; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+// TMA bulk copy global -> shared, completion counted on mbarrier `bar`.
+// dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void flag_error(unsigned* err, unsigned code) {
+  if (err) atomicOr(err, code);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+
+// launch helpers (defined in the op files) -----------------------------------------
+nt_status launch_gemv(Ctx* c, int fmt, const nt_gemv_job* jobs, int njobs, const void* W2, const float* x,
+                      const float* norm_g, float eps, int64_t cols, bool swiglu, cudaStream_t st);
+
+}  // namespace nt
+
+struct nt_ctx : nt::Ctx {};

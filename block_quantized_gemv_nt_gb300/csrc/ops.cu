@@ -1,0 +1,445 @@
+// ops.cu — the small kernels around the quant GEMV: RMSNorm, RoPE (+ F16 KV
+// append), split-K GQA decode attention with its softmax, SwiGLU, greedy
+// argmax and cosine similarity.  Sources: "ntransformer - moteur d'inférence
+// NVMe-to-GPU…" (fr.news.hada.io), "Architecture et structure du code"
+// (cuda/: RMSNorm, RoPE, SwiGLU, softmax; inference/: sampler) and
+// "Fonctionnalités principales" (RoPE, GQA, SwiGLU, RMSNorm, KV cache);
+// "Performances et structure de cache" (cosine-similarity layer skip).
+#include <cfloat>
+
+#include "nt_internal.cuh"
+#include "ops.cuh"
+
+namespace nt {
+namespace {
+
+template <int NW>
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) t += red[w];
+  return t;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+template <int NW>
+__device__ __forceinline__ float block_max(float v, float* red) {
+  v = warp_max(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = -FLT_MAX;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) t = fmaxf(t, red[w]);
+  return t;
+}
+
+// ---- RMSNorm: y = x * rsqrt(mean(x^2) + eps) * g ------------------------------
+__global__ void __launch_bounds__(1024) rmsnorm_kernel(const float* x, const float* g, float* y, int64_t n,
+                                                       float eps) {
+  __shared__ float red[32];
+  float ss = 0.f;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+  ss = block_sum<32>(ss, red);
+  const float inv = rsqrtf(ss / float(n) + eps);
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) y[i] = x[i] * inv * g[i];
+}
+
+// ---- RoPE ----------------------------------------------------------------------
+// pair i of every head turns by pos * theta^(-2i/head_dim); angles in fp64.
+__device__ __forceinline__ void rope_table(float* cs, float* sn, int head_dim, int64_t pos, float theta) {
+  for (int i = threadIdx.x; i < head_dim / 2; i += blockDim.x) {
+    const double ang = double(pos) * pow(double(theta), -2.0 * double(i) / double(head_dim));
+    double s, c;
+    sincos(ang, &s, &c);
+    cs[i] = float(c);
+    sn[i] = float(s);
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ void rotate(float* v, int n_heads, int head_dim, const float* cs, const float* sn) {
+  const int half = head_dim / 2;
+  for (int t = threadIdx.x; t < n_heads * half; t += blockDim.x) {
+    const int h = t / half, i = t % half;
+    float* p = v + int64_t(h) * head_dim + 2 * i;
+    const float a = p[0], b = p[1];
+    p[0] = a * cs[i] - b * sn[i];
+    p[1] = a * sn[i] + b * cs[i];
+  }
+}
+
+__global__ void rope_kernel(float* q, float* k, int n_qh, int n_kvh, int head_dim, int64_t pos, float theta) {
+  __shared__ float cs[256], sn[256];
+  rope_table(cs, sn, head_dim, pos, theta);
+  rotate(q, n_qh, head_dim, cs, sn);
+  if (k) rotate(k, n_kvh, head_dim, cs, sn);
+}
+
+// RoPE q in place; rotate k and append f16(k), f16(v) at cache position pos.
+// pos_dev (nullable) overrides pos with a device value (graph replays).
+__global__ void rope_append_kernel(float* q, const float* k, const float* v, __half* kc, __half* vc, int n_qh,
+                                   int n_kvh, int head_dim, int64_t pos, const int64_t* pos_dev, int64_t kv_stride,
+                                   float theta) {
+  __shared__ float cs[256], sn[256];
+  if (pos_dev) pos = *pos_dev;
+  rope_table(cs, sn, head_dim, pos, theta);
+  rotate(q, n_qh, head_dim, cs, sn);
+  const int half = head_dim / 2;
+  for (int t = threadIdx.x; t < n_kvh * half; t += blockDim.x) {
+    const int h = t / half, i = t % half;
+    const float* p = k + int64_t(h) * head_dim + 2 * i;
+    const float a = p[0], b = p[1];
+    const int64_t at = (int64_t(h) * kv_stride + pos) * head_dim + 2 * i;
+    kc[at] = __float2half_rn(a * cs[i] - b * sn[i]);
+    kc[at + 1] = __float2half_rn(a * sn[i] + b * cs[i]);
+    vc[at] = __float2half_rn(v[int64_t(h) * head_dim + 2 * i]);
+    vc[at + 1] = __float2half_rn(v[int64_t(h) * head_dim + 2 * i + 1]);
+  }
+}
+
+// ---- split-K GQA decode attention ----------------------------------------------
+// grid (n_kvh, S); CTA (g, s) covers positions [s*chunk, (s+1)*chunk) of KV head
+// g for its whole group of G q heads, so K and V are read once per group.
+// Partials (m, l, o[128]) go to scratch; the last CTA of a KV head combines.
+constexpr int kAttnThreads = 256;
+constexpr int kHD = 128;
+constexpr int kMaxGroup = 16;
+constexpr int kMaxChunk = 512;
+
+struct AttnArgs {
+  const float* q;
+  const __half* K;
+  const __half* V;
+  float* out;
+  int n_qh, n_kvh, G, S;
+  int64_t n_pos;
+  const int64_t* pos_dev;  // nullable: n_pos = *pos_dev + 1
+  int64_t kv_stride;
+  float* part;             // [n_kvh][S][G][2 + 128]
+  unsigned* counters;      // [n_kvh]
+};
+
+__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
+  extern __shared__ float sm[];
+  const int G = a.G;
+  float* qs = sm;                       // [G][128], pre-scaled by 1/sqrt(128)
+  float* sc = qs + G * kHD;             // [G][kMaxChunk] scores, then probabilities
+  float* red = sc + G * kMaxChunk;      // [8 warps][G][128]
+  __shared__ float stat[2 * kMaxGroup];
+  __shared__ bool last;
+
+  const int g = blockIdx.x, s = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t n_pos = a.pos_dev ? *a.pos_dev + 1 : a.n_pos;
+  const int64_t chunk = (n_pos + a.S - 1) / a.S;
+  const int64_t p0 = int64_t(s) * chunk;
+  const int64_t p1 = min(n_pos, p0 + chunk);
+  const int np = p1 > p0 ? int(p1 - p0) : 0;
+
+  const float scale = rsqrtf(float(kHD));
+  for (int i = tid; i < G * kHD; i += kAttnThreads) qs[i] = a.q[int64_t(g) * G * kHD + i] * scale;
+  __syncthreads();
+
+  const __half* Kg = a.K + int64_t(g) * a.kv_stride * kHD;
+  const __half* Vg = a.V + int64_t(g) * a.kv_stride * kHD;
+
+  // scores: warp per position, lane owns dims 4*lane .. 4*lane+3
+  for (int j = warp; j < np; j += 8) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(Kg + (p0 + j) * kHD + 4 * lane);
+    const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    for (int h = 0; h < G; ++h) {
+      const float4 qv = *reinterpret_cast<const float4*>(qs + h * kHD + 4 * lane);
+      float d = qv.x * k01.x;
+      d = fmaf(qv.y, k01.y, d);
+      d = fmaf(qv.z, k23.x, d);
+      d = fmaf(qv.w, k23.y, d);
+      d = warp_sum(d);
+      if (lane == 0) sc[h * kMaxChunk + j] = d;
+    }
+  }
+  __syncthreads();
+
+  // local softmax statistics per head: warp h handles head h (and h + 8)
+  for (int h = warp; h < G; h += 8) {
+    float m = -FLT_MAX;
+    for (int j = lane; j < np; j += 32) m = fmaxf(m, sc[h * kMaxChunk + j]);
+    m = warp_max(m);
+    float l = 0.f;
+    for (int j = lane; j < np; j += 32) {
+      const float p = __expf(sc[h * kMaxChunk + j] - m);
+      sc[h * kMaxChunk + j] = p;
+      l += p;
+    }
+    l = warp_sum(l);
+    if (lane == 0) {
+      stat[2 * h] = np > 0 ? m : -INFINITY;
+      stat[2 * h + 1] = l;
+    }
+  }
+  __syncthreads();
+
+  // o = sum_j p_j V_j: warps split positions, lane owns 4 dims
+  float acc[kMaxGroup][4];
+#pragma unroll
+  for (int h = 0; h < kMaxGroup; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
+  for (int j = warp; j < np; j += 8) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(Vg + (p0 + j) * kHD + 4 * lane);
+    const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+#pragma unroll
+    for (int h = 0; h < kMaxGroup; ++h) {
+      if (h < G) {
+        const float p = sc[h * kMaxChunk + j];
+        acc[h][0] = fmaf(p, v01.x, acc[h][0]);
+        acc[h][1] = fmaf(p, v01.y, acc[h][1]);
+        acc[h][2] = fmaf(p, v23.x, acc[h][2]);
+        acc[h][3] = fmaf(p, v23.y, acc[h][3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < kMaxGroup; ++h)
+    if (h < G) *reinterpret_cast<float4*>(red + (warp * G + h) * kHD + 4 * lane) =
+        make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+  __syncthreads();
+
+  float* my = a.part + (int64_t(g) * a.S + s) * G * (2 + kHD);
+  for (int i = tid; i < G * kHD; i += kAttnThreads) {
+    const int h = i / kHD, d = i % kHD;
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += red[(w * G + h) * kHD + d];
+    my[h * (2 + kHD) + 2 + d] = t;
+  }
+  for (int h = tid; h < G; h += kAttnThreads) {
+    my[h * (2 + kHD)] = stat[2 * h];
+    my[h * (2 + kHD) + 1] = stat[2 * h + 1];
+  }
+
+  // the last CTA of this KV head combines the S partials
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(a.counters + g, 1u);
+    last = (prev == unsigned(a.S - 1));
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const float* base = a.part + int64_t(g) * a.S * G * (2 + kHD);
+  for (int i = tid; i < G * kHD; i += kAttnThreads) {
+    const int h = i / kHD, d = i % kHD;
+    float M = -INFINITY;
+    for (int t = 0; t < a.S; ++t) M = fmaxf(M, __ldcg(base + (int64_t(t) * G + h) * (2 + kHD)));
+    float L = 0.f, O = 0.f;
+    for (int t = 0; t < a.S; ++t) {
+      const float* pp = base + (int64_t(t) * G + h) * (2 + kHD);
+      const float mt = __ldcg(pp);
+      if (mt == -INFINITY) continue;
+      const float w = __expf(mt - M);
+      L = fmaf(__ldcg(pp + 1), w, L);
+      O = fmaf(__ldcg(pp + 2 + d), w, O);
+    }
+    a.out[(int64_t(g) * G + h) * kHD + d] = O / L;
+  }
+  if (tid == 0) a.counters[g] = 0u;  // ready for the next launch
+}
+
+// ---- softmax (standalone) --------------------------------------------------------
+__global__ void __launch_bounds__(1024) softmax_kernel(const float* x, float* y, int64_t n) {
+  __shared__ float red[32];
+  float m = -FLT_MAX;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, x[i]);
+  m = block_max<32>(m, red);
+  float l = 0.f;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) l += __expf(x[i] - m);
+  l = block_sum<32>(l, red);
+  const float inv = 1.0f / l;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) y[i] = __expf(x[i] - m) * inv;
+}
+
+// ---- SwiGLU (standalone) -----------------------------------------------------------
+__global__ void swiglu_kernel(const float* gate, const float* up, float* h, int64_t n) {
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
+    h[i] = silu(gate[i]) * up[i];
+}
+
+// ---- greedy argmax ------------------------------------------------------------------
+// key = (order-preserving bits of v) << 32 | (~index): the largest key is the
+// largest value with the lowest index.  NaN never wins.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int64_t i) {
+  if (v != v) return 0ull;
+  const unsigned b = __float_as_uint(v);
+  const unsigned o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<unsigned long long>(o) << 32) | (0xFFFFFFFFu - unsigned(i));
+}
+
+__global__ void argmax_kernel(const float* v, int64_t n, unsigned long long* key, unsigned* counter, int32_t* out) {
+  __shared__ unsigned long long wbest[32];
+  __shared__ bool last;
+  unsigned long long best = 0ull;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+    const unsigned long long k = argmax_key(v[i], i);
+    best = k > best ? k : best;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long t = __shfl_xor_sync(0xffffffffu, best, o);
+    best = t > best ? t : best;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) wbest[warp] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long b = 0ull;
+    for (int w = 0; w < int(blockDim.x >> 5); ++w) b = wbest[w] > b ? wbest[w] : b;
+    atomicMax(key, b);
+    __threadfence();
+    last = atomicAdd(counter, 1u) == gridDim.x - 1;
+    if (last) {
+      __threadfence();
+      const unsigned long long k = atomicAdd(key, 0ull);
+      *out = k ? int32_t(0xFFFFFFFFu - unsigned(k & 0xFFFFFFFFull)) : 0;
+      *key = 0ull;
+      *counter = 0u;
+    }
+  }
+}
+
+// ---- cosine similarity --------------------------------------------------------------
+__global__ void __launch_bounds__(1024) cos_kernel(const float* x, const float* y, int64_t n, float* out) {
+  __shared__ double red[3][32];
+  double ab = 0, aa = 0, bb = 0;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const double p = x[i], q = y[i];
+    ab += p * q;
+    aa += p * p;
+    bb += q * q;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ab += __shfl_xor_sync(0xffffffffu, ab, o);
+    aa += __shfl_xor_sync(0xffffffffu, aa, o);
+    bb += __shfl_xor_sync(0xffffffffu, bb, o);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    red[0][warp] = ab;
+    red[1][warp] = aa;
+    red[2][warp] = bb;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s0 = 0, s1 = 0, s2 = 0;
+    for (int w = 0; w < int(blockDim.x >> 5); ++w) {
+      s0 += red[0][w];
+      s1 += red[1][w];
+      s2 += red[2][w];
+    }
+    *out = float(s0 / (sqrt(s1) * sqrt(s2)));
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------------
+// launchers (arguments already validated by the C ABI layer)
+
+nt_status launch_rmsnorm(Ctx* c, const float* x, const float* g, float* y, int64_t n, float eps, cudaStream_t st) {
+  rmsnorm_kernel<<<1, 1024, 0, st>>>(x, g, y, n, eps);
+  return cuda_check(c, cudaGetLastError(), "rmsnorm launch");
+}
+
+nt_status launch_rope(Ctx* c, float* q, float* k, int n_qh, int n_kvh, int hd, int64_t pos, float theta,
+                      cudaStream_t st) {
+  rope_kernel<<<1, 256, 0, st>>>(q, k, n_qh, n_kvh, hd, pos, theta);
+  return cuda_check(c, cudaGetLastError(), "rope launch");
+}
+
+nt_status launch_rope_append(Ctx* c, float* q, const float* k, const float* v, void* kc, void* vc, int n_qh,
+                             int n_kvh, int hd, int64_t pos, const int64_t* pos_dev, int64_t kv_stride, float theta,
+                             cudaStream_t st) {
+  rope_append_kernel<<<1, 256, 0, st>>>(q, k, v, static_cast<__half*>(kc), static_cast<__half*>(vc), n_qh, n_kvh,
+                                        hd, pos, pos_dev, kv_stride, theta);
+  return cuda_check(c, cudaGetLastError(), "rope/append launch");
+}
+
+int attn_splits(const Ctx* c, int n_kvh, int64_t kv_stride) {
+  int S = (c->num_sms + n_kvh - 1) / n_kvh;
+  const int64_t need = (kv_stride + kMaxChunk - 1) / kMaxChunk;
+  if (need > S) S = int(need);
+  return S;
+}
+
+size_t attn_scratch_bytes(int n_qh, int n_kvh, int S) {
+  return size_t(n_kvh) * S * (n_qh / n_kvh) * (2 + kHD) * sizeof(float) + 64 * sizeof(unsigned);
+}
+
+nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, float* out, int n_qh, int n_kvh,
+                      int64_t n_pos, const int64_t* pos_dev, int64_t kv_stride, float* part, unsigned* counters,
+                      int S, cudaStream_t st) {
+  AttnArgs a{};
+  a.q = q;
+  a.K = static_cast<const __half*>(K);
+  a.V = static_cast<const __half*>(V);
+  a.out = out;
+  a.n_qh = n_qh;
+  a.n_kvh = n_kvh;
+  a.G = n_qh / n_kvh;
+  a.S = S;
+  a.n_pos = n_pos;
+  a.pos_dev = pos_dev;
+  a.kv_stride = kv_stride;
+  a.part = part;
+  a.counters = counters;
+  const size_t smem = size_t(a.G) * (kHD + kMaxChunk + 8 * kHD) * sizeof(float);
+  static size_t configured = 0;
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return cuda_check(c, e, "attention smem attribute");
+    configured = smem;
+  }
+  attn_kernel<<<dim3(n_kvh, S), kAttnThreads, smem, st>>>(a);
+  return cuda_check(c, cudaGetLastError(), "attention launch");
+}
+
+nt_status launch_softmax(Ctx* c, const float* x, float* y, int64_t n, cudaStream_t st) {
+  softmax_kernel<<<1, 1024, 0, st>>>(x, y, n);
+  return cuda_check(c, cudaGetLastError(), "softmax launch");
+}
+
+nt_status launch_swiglu(Ctx* c, const float* g, const float* u, float* h, int64_t n, cudaStream_t st) {
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  swiglu_kernel<<<int(blocks), 256, 0, st>>>(g, u, h, n);
+  return cuda_check(c, cudaGetLastError(), "swiglu launch");
+}
+
+nt_status launch_argmax(Ctx* c, const float* v, int64_t n, int32_t* out, unsigned long long* key, unsigned* counter,
+                        cudaStream_t st) {
+  int64_t blocks = (n + 1023) / 1024;
+  if (blocks > c->num_sms) blocks = c->num_sms;
+  if (blocks < 1) blocks = 1;
+  argmax_kernel<<<int(blocks), 1024, 0, st>>>(v, n, key, counter, out);
+  return cuda_check(c, cudaGetLastError(), "argmax launch");
+}
+
+nt_status launch_cos(Ctx* c, const float* a, const float* b, int64_t n, float* out, cudaStream_t st) {
+  cos_kernel<<<1, 1024, 0, st>>>(a, b, n, out);
+  return cuda_check(c, cudaGetLastError(), "cos launch");
+}
+
+}  // namespace nt

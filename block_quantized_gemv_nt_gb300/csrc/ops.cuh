@@ -1,0 +1,29 @@
+// ops.cuh — launchers of the kernels in qgemv.cu and ops.cu (arguments are
+// validated by the C ABI layer before any of these runs).
+#pragma once
+#include "nt_internal.cuh"
+
+namespace nt {
+
+nt_status launch_dequant(Ctx* c, int fmt, const void* W, int64_t row0, int64_t nrows, int64_t cols, float* out,
+                         cudaStream_t st);
+nt_status launch_embed(Ctx* c, int fmt, const void* W, int64_t cols, const int32_t* token_dev, float* out,
+                       cudaStream_t st);
+nt_status launch_rmsnorm(Ctx* c, const float* x, const float* g, float* y, int64_t n, float eps, cudaStream_t st);
+nt_status launch_rope(Ctx* c, float* q, float* k, int n_qh, int n_kvh, int hd, int64_t pos, float theta,
+                      cudaStream_t st);
+nt_status launch_rope_append(Ctx* c, float* q, const float* k, const float* v, void* kc, void* vc, int n_qh,
+                             int n_kvh, int hd, int64_t pos, const int64_t* pos_dev, int64_t kv_stride, float theta,
+                             cudaStream_t st);
+int attn_splits(const Ctx* c, int n_kvh, int64_t kv_stride);
+size_t attn_scratch_bytes(int n_qh, int n_kvh, int S);
+nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, float* out, int n_qh, int n_kvh,
+                      int64_t n_pos, const int64_t* pos_dev, int64_t kv_stride, float* part, unsigned* counters,
+                      int S, cudaStream_t st);
+nt_status launch_softmax(Ctx* c, const float* x, float* y, int64_t n, cudaStream_t st);
+nt_status launch_swiglu(Ctx* c, const float* g, const float* u, float* h, int64_t n, cudaStream_t st);
+nt_status launch_argmax(Ctx* c, const float* v, int64_t n, int32_t* out, unsigned long long* key, unsigned* counter,
+                        cudaStream_t st);
+nt_status launch_cos(Ctx* c, const float* a, const float* b, int64_t n, float* out, cudaStream_t st);
+
+}  // namespace nt

@@ -1,0 +1,200 @@
+"""ctypes binding of libnt.so — argument marshalling only.
+
+Every function keeps the C name from include/nt.h and takes torch tensors
+(device pointers via ``data_ptr()``) or plain ints; the stream defaults to
+torch's current stream on the tensor's device.  All computation runs in the
+CUDA kernels of libnt.so; if the library cannot be loaded, importing this
+module raises — there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+Q8_0, Q4_0, Q4_K, Q5_K, Q6_K = 0, 1, 2, 3, 4
+FMT_NAMES = {Q8_0: "Q8_0", Q4_0: "Q4_0", Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K"}
+
+NT_OK, NT_ERR_INVALID_ARG, NT_ERR_UNSUPPORTED_FMT, NT_ERR_ALIGNMENT, NT_ERR_CUDA, NT_ERR_OOM, NT_ERR_TIMEOUT = range(7)
+STATUS_NAMES = ["NT_OK", "NT_ERR_INVALID_ARG", "NT_ERR_UNSUPPORTED_FMT", "NT_ERR_ALIGNMENT", "NT_ERR_CUDA",
+                "NT_ERR_OOM", "NT_ERR_TIMEOUT"]
+
+
+class NtError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else status}: {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.SO
+
+
+def _load():
+    path = _build.SO
+    if not os.path.exists(path) or _build._stale():
+        _build.build()
+    return ctypes.CDLL(path)
+
+
+_lib = _load()
+
+_vp, _i64, _ci, _cf, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+class nt_gemv_job(ctypes.Structure):
+    _fields_ = [("W_dev", _vp), ("y_dev", _vp), ("residual_dev", _vp), ("rows", _i64)]
+
+
+def _sig(name, args, res=_ci):
+    f = getattr(_lib, name)
+    f.argtypes = args
+    f.restype = res
+    return f
+
+
+_sig("nt_ctx_create", [ctypes.POINTER(_vp), _ci, _sz])
+_sig("nt_ctx_destroy", [_vp])
+_sig("nt_ctx_sync", [_vp])
+_sig("nt_last_error", [_vp], ctypes.c_char_p)
+_sig("nt_block_bytes", [_ci])
+_sig("nt_block_elems", [_ci])
+_sig("nt_dequant_rows", [_vp, _ci, _vp, _i64, _i64, _i64, _vp, _vp])
+_sig("nt_gemv_q", [_vp, _ci, _vp, _vp, _vp, _i64, _i64, _vp, _vp])
+_sig("nt_gemv_q_swiglu", [_vp, _ci, _vp, _vp, _vp, _vp, _i64, _i64, _vp])
+_sig("nt_gemv_q_multi", [_vp, _ci, ctypes.POINTER(nt_gemv_job), _ci, _vp, _vp, _cf, _i64, _vp])
+_sig("nt_rmsnorm", [_vp, _vp, _vp, _vp, _i64, _cf, _vp])
+_sig("nt_rope", [_vp, _vp, _vp, _ci, _ci, _ci, _i64, _cf, _vp])
+_sig("nt_rope_kv_append", [_vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _i64, _i64, _cf, _vp])
+_sig("nt_attn_decode", [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _i64, _i64, _vp])
+_sig("nt_softmax", [_vp, _vp, _vp, _i64, _vp])
+_sig("nt_swiglu", [_vp, _vp, _vp, _vp, _i64, _vp])
+_sig("nt_argmax", [_vp, _vp, _i64, _vp, _vp])
+_sig("nt_cos_sim", [_vp, _vp, _vp, _i64, _vp, _vp])
+
+EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "nt_block_bytes", "nt_block_elems",
+            "nt_dequant_rows", "nt_gemv_q", "nt_gemv_q_swiglu", "nt_gemv_q_multi", "nt_rmsnorm", "nt_rope",
+            "nt_rope_kv_append", "nt_attn_decode", "nt_softmax", "nt_swiglu", "nt_argmax", "nt_cos_sim"]
+
+
+def lib():
+    return _lib
+
+
+# ---------------------------------------------------------------------------
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream, like=None):
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    dev = like.device if like is not None and hasattr(like, "device") else None
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+class Context:
+    """Owns one nt_ctx (device scratch, events, graphs)."""
+
+    def __init__(self, device: int = 0, scratch_bytes: int = 0):
+        h = _vp()
+        st = _lib.nt_ctx_create(ctypes.byref(h), device, scratch_bytes)
+        if st != NT_OK:
+            raise NtError(st, "nt_ctx_create failed")
+        self.handle = h.value
+        self.device = device
+
+    def check(self, status: int):
+        if status != NT_OK:
+            raise NtError(status, _lib.nt_last_error(self.handle).decode())
+        return status
+
+    def sync(self):
+        return self.check(_lib.nt_ctx_sync(self.handle))
+
+    def close(self):
+        if self.handle:
+            _lib.nt_ctx_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def nt_ctx_create(device: int = 0, scratch_bytes: int = 0) -> Context:
+    return Context(device, scratch_bytes)
+
+
+def nt_block_bytes(fmt: int) -> int:
+    return _lib.nt_block_bytes(fmt)
+
+
+def nt_block_elems(fmt: int) -> int:
+    return _lib.nt_block_elems(fmt)
+
+
+def nt_dequant_rows(ctx, fmt, W, row0, nrows, cols, out, stream=None):
+    return ctx.check(_lib.nt_dequant_rows(ctx.handle, fmt, _ptr(W), row0, nrows, cols, _ptr(out), _stream(stream, out)))
+
+
+def nt_gemv_q(ctx, fmt, W, x, y, rows, cols, residual=None, stream=None):
+    return ctx.check(_lib.nt_gemv_q(ctx.handle, fmt, _ptr(W), _ptr(x), _ptr(y), rows, cols, _ptr(residual),
+                                    _stream(stream, y)))
+
+
+def nt_gemv_q_swiglu(ctx, fmt, Wg, Wu, x, h, rows, cols, stream=None):
+    return ctx.check(_lib.nt_gemv_q_swiglu(ctx.handle, fmt, _ptr(Wg), _ptr(Wu), _ptr(x), _ptr(h), rows, cols,
+                                           _stream(stream, h)))
+
+
+def nt_gemv_q_multi(ctx, fmt, jobs, x, cols, norm_g=None, eps=0.0, stream=None):
+    """jobs: list of (W, y, residual_or_None, rows)."""
+    arr = (nt_gemv_job * max(1, len(jobs)))()
+    for i, (W, y, r, rows) in enumerate(jobs):
+        arr[i] = nt_gemv_job(_ptr(W), _ptr(y), _ptr(r), rows)
+    return ctx.check(_lib.nt_gemv_q_multi(ctx.handle, fmt, arr, len(jobs), _ptr(x), _ptr(norm_g), eps, cols,
+                                          _stream(stream, x)))
+
+
+def nt_rmsnorm(ctx, x, g, y, n, eps, stream=None):
+    return ctx.check(_lib.nt_rmsnorm(ctx.handle, _ptr(x), _ptr(g), _ptr(y), n, eps, _stream(stream, y)))
+
+
+def nt_rope(ctx, q, k, n_qh, n_kvh, head_dim, pos, theta, stream=None):
+    return ctx.check(_lib.nt_rope(ctx.handle, _ptr(q), _ptr(k), n_qh, n_kvh, head_dim, pos, theta,
+                                  _stream(stream, q)))
+
+
+def nt_rope_kv_append(ctx, q, k, v, kcache, vcache, n_qh, n_kvh, head_dim, pos, kv_stride, theta, stream=None):
+    return ctx.check(_lib.nt_rope_kv_append(ctx.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(kcache), _ptr(vcache), n_qh,
+                                            n_kvh, head_dim, pos, kv_stride, theta, _stream(stream, q)))
+
+
+def nt_attn_decode(ctx, q, kcache, vcache, out, n_qh, n_kvh, head_dim, n_pos, kv_stride, stream=None):
+    return ctx.check(_lib.nt_attn_decode(ctx.handle, _ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), n_qh, n_kvh,
+                                         head_dim, n_pos, kv_stride, _stream(stream, out)))
+
+
+def nt_softmax(ctx, x, y, n, stream=None):
+    return ctx.check(_lib.nt_softmax(ctx.handle, _ptr(x), _ptr(y), n, _stream(stream, y)))
+
+
+def nt_swiglu(ctx, gate, up, h, n, stream=None):
+    return ctx.check(_lib.nt_swiglu(ctx.handle, _ptr(gate), _ptr(up), _ptr(h), n, _stream(stream, h)))
+
+
+def nt_argmax(ctx, v, n, out, stream=None):
+    return ctx.check(_lib.nt_argmax(ctx.handle, _ptr(v), n, _ptr(out), _stream(stream, out)))
+
+
+def nt_cos_sim(ctx, a, b, n, out, stream=None):
+    return ctx.check(_lib.nt_cos_sim(ctx.handle, _ptr(a), _ptr(b), n, _ptr(out), _stream(stream, out)))

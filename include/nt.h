@@ -1,0 +1,159 @@
+/*
+ * nt.h — C ABI of libnt.so: batch-1 decode of a Llama-architecture
+ * transformer whose linear weights are GGUF-style block-quantized, on one
+ * GB300 (sm_103a).
+ *
+ * Passages the operations come from (page title, then section):
+ *  [about]  "Ntransformer" (en.unwiki.net), About — GGUF formats Q4_0, Q8_0,
+ *           Q4_K_M, Q5_K, Q6_K.
+ *  [code]   "ntransformer - moteur d'inférence NVMe-to-GPU…" (fr.news.hada.io),
+ *           "Architecture et structure du code" — cuda/: GEMV, RMSNorm, RoPE,
+ *           SwiGLU and softmax kernels; model/: transformer composition,
+ *           attention, FFN, normalisation; inference/: sampler, engine;
+ *           memory/: layer streaming engine.
+ *  [feat]   same page, "Fonctionnalités principales" — RoPE, GQA, SwiGLU,
+ *           RMSNorm, KV cache; SLEP double-buffered streaming; self-speculative
+ *           decoding with the VRAM-resident layers as the draft.
+ *  [cache]  same page, "Performances et structure de cache" — layer skip by
+ *           cosine similarity (20 of 80 layers); VRAM-resident layers and
+ *           pinned-RAM H2D tiers.
+ *  [road]   "Ntransformer" (en.unwiki.net), roadmap — F16 KV cache; public C
+ *           API planned.
+ *
+ * Conventions shared by every entry point:
+ *  - Every call returns nt_status.  Arguments are checked on the host first;
+ *    a call that fails its checks launches nothing and leaves outputs as they
+ *    were.  nt_last_error(ctx) then holds a one-line reason.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls only enqueue work; device-side faults and the device
+ *    error flag (a bounded wait inside a kernel that ran out) surface at
+ *    nt_ctx_sync() or at the next call on the context.
+ *  - Pointers named *_dev are device (HBM) pointers; pointers named *_host
+ *    are host pointers.  The caller owns every weight, activation, KV-cache
+ *    and output buffer; the context owns only its scratch, events, side
+ *    streams and captured graphs.
+ *  - Block-quantized matrices are row-major: row r is cols/block_elems
+ *    consecutive blocks.  cols must be a multiple of the format's block size
+ *    (32 for Q8_0/Q4_0, 256 for Q4_K/Q5_K/Q6_K).  Block bytes: Q8_0 34,
+ *    Q4_0 18, Q4_K 144, Q5_K 176, Q6_K 210; layouts are the GGUF ones.
+ *  - Weight pointers must be 2-byte aligned.  When the weight pointer is
+ *    16-byte aligned and each row is a multiple of 16 bytes, weights stream
+ *    through TMA bulk copies; otherwise a slower plain-load path runs.
+ *  - fp32 vectors must be 16-byte aligned.
+ */
+#ifndef NT_H
+#define NT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NT_OK = 0,
+  NT_ERR_INVALID_ARG = 1,     /* null pointer, bad size, ragged cols, ... */
+  NT_ERR_UNSUPPORTED_FMT = 2, /* format id outside nt_fmt */
+  NT_ERR_ALIGNMENT = 3,       /* pointer alignment rule broken */
+  NT_ERR_CUDA = 4,            /* a CUDA runtime call failed */
+  NT_ERR_OOM = 5,             /* device or pinned allocation failed */
+  NT_ERR_TIMEOUT = 6,         /* a host-side or device-side bounded wait ran out */
+} nt_status;
+
+typedef enum { NT_Q8_0 = 0, NT_Q4_0 = 1, NT_Q4_K = 2, NT_Q5_K = 3, NT_Q6_K = 4 } nt_fmt;
+
+typedef struct nt_ctx nt_ctx;
+typedef struct nt_model nt_model;
+
+/* ---- context ------------------------------------------------------------ */
+
+/* Create a context on CUDA device `device`.  scratch_bytes = 0 picks the
+ * default (64 MiB).  The context allocates its scratch on the device. */
+nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes);
+nt_status nt_ctx_destroy(nt_ctx* ctx);
+/* Wait for all work of this context's device, then report any asynchronous
+ * CUDA error or device-side timeout flag (NT_ERR_TIMEOUT) and clear the flag. */
+nt_status nt_ctx_sync(nt_ctx* ctx);
+const char* nt_last_error(const nt_ctx* ctx);
+/* Bytes per block / elements per block of a format (0 for an unknown id). */
+int nt_block_bytes(int fmt);
+int nt_block_elems(int fmt);
+
+/* ---- single ops ------------------------------------------------------------ */
+
+/* Dequantise rows [row0, row0+nrows) of a rows x cols matrix into fp32
+ * out_dev[nrows][cols].  Element values [about], GGUF reading:
+ *   Q8_0 d*q;  Q4_0 d*(q-8);  Q4_K/Q5_K (d*sc)*q - dmin*m;  Q6_K d*(sc*(q-32)).
+ * Each product is exact in fp32, so results are bit-identical to any
+ * implementation that rounds the same single subtraction. */
+nt_status nt_dequant_rows(nt_ctx* ctx, int fmt, const void* W_dev, int64_t row0, int64_t nrows, int64_t cols,
+                          float* out_dev, void* stream);
+
+/* Quant GEMV [code] cuda/ GEMV:  y[r] = sum_c deq(W[r,c]) * x[c]  (+ residual[r]),
+ * r < rows, fp32 accumulation.  residual_dev may be NULL or equal y_dev. */
+nt_status nt_gemv_q(nt_ctx* ctx, int fmt, const void* W_dev, const float* x_dev, float* y_dev, int64_t rows,
+                    int64_t cols, const float* residual_dev, void* stream);
+
+/* Gate/up GEMV with the SwiGLU epilogue [feat] SwiGLU:
+ *   h[r] = silu(Wg[r,:] . x) * (Wu[r,:] . x),  silu(z) = z / (1 + e^-z).
+ * Wg and Wu share format and shape. */
+nt_status nt_gemv_q_swiglu(nt_ctx* ctx, int fmt, const void* Wg_dev, const void* Wu_dev, const float* x_dev,
+                           float* h_dev, int64_t rows, int64_t cols, void* stream);
+
+/* One launch of several GEMVs sharing x (e.g. Q, K and V), optionally with the
+ * RMSNorm of x fused in front:  x' = x / sqrt(mean(x^2) + eps) * g  when
+ * norm_g_dev != NULL.  Up to 3 jobs, all of format fmt and width cols. */
+typedef struct {
+  const void* W_dev;
+  float* y_dev;
+  const float* residual_dev; /* nullable; may equal y_dev */
+  int64_t rows;
+} nt_gemv_job;
+nt_status nt_gemv_q_multi(nt_ctx* ctx, int fmt, const nt_gemv_job* jobs, int njobs, const float* x_dev,
+                          const float* norm_g_dev, float eps, int64_t cols, void* stream);
+
+/* RMSNorm [feat]:  y = x / sqrt(mean(x^2) + eps) * g, fp32, n elements. */
+nt_status nt_rmsnorm(nt_ctx* ctx, const float* x_dev, const float* g_dev, float* y_dev, int64_t n, float eps,
+                     void* stream);
+
+/* RoPE [feat] in place on q [n_qh][head_dim] and k [n_kvh][head_dim] (k may be
+ * NULL): adjacent pairs (2i, 2i+1) turn by pos * theta^(-2i/head_dim). */
+nt_status nt_rope(nt_ctx* ctx, float* q_dev, float* k_dev, int n_qh, int n_kvh, int head_dim, int64_t pos,
+                  float theta, void* stream);
+
+/* RoPE on q and k, then append k and v (fp32 -> binary16, round to nearest
+ * even) to the F16 KV cache [road] at position pos.  Caches are laid out
+ * [n_kvh][kv_stride][head_dim] (one layer). */
+nt_status nt_rope_kv_append(nt_ctx* ctx, float* q_dev, const float* k_dev, const float* v_dev, void* kcache_dev,
+                            void* vcache_dev, int n_qh, int n_kvh, int head_dim, int64_t pos, int64_t kv_stride,
+                            float theta, void* stream);
+
+/* Decode attention with grouped KV heads [feat] GQA over the F16 KV cache:
+ * for q head h, KV head g = h / (n_qh / n_kvh):
+ *   out_h = softmax_j(q_h . K_g[j] / sqrt(head_dim)) . V_g[j],  j < n_pos.
+ * Split over positions (flash-decoding), partials combined in the same
+ * launch through context scratch.  head_dim must be 128. */
+nt_status nt_attn_decode(nt_ctx* ctx, const float* q_dev, const void* kcache_dev, const void* vcache_dev,
+                         float* out_dev, int n_qh, int n_kvh, int head_dim, int64_t n_pos, int64_t kv_stride,
+                         void* stream);
+
+/* Softmax [code]: y = exp(x - max x) / sum, fp32, n elements (standalone). */
+nt_status nt_softmax(nt_ctx* ctx, const float* x_dev, float* y_dev, int64_t n, void* stream);
+
+/* SwiGLU [feat]: h = silu(gate) * up, fp32, n elements (standalone). */
+nt_status nt_swiglu(nt_ctx* ctx, const float* gate_dev, const float* up_dev, float* h_dev, int64_t n,
+                    void* stream);
+
+/* Greedy sampler [code] inference/: index of the largest of v[0..n), lowest
+ * index on ties (NaN never wins), written as int32 to out_dev. */
+nt_status nt_argmax(nt_ctx* ctx, const float* v_dev, int64_t n, int32_t* out_dev, void* stream);
+
+/* Cosine similarity [cache] of a and b: <a,b> / (|a| |b|), fp32 result. */
+nt_status nt_cos_sim(nt_ctx* ctx, const float* a_dev, const float* b_dev, int64_t n, float* out_dev,
+                     void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NT_H */

@@ -1,0 +1,50 @@
+"""The C-ABI library loads and exports every symbol include/nt.h declares, and
+rejects bad arguments before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "nt.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:nt_status|const char\*|int)\s+(nt_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("nt_ctx_create", "nt_gemv_q", "nt_rmsnorm", "nt_rope", "nt_attn_decode", "nt_swiglu"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    from block_quantized_gemv_nt_gb300 import nt
+    lib = ctypes.CDLL(nt.library_path())
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(_declared()) <= set(nt.EXPORTED)
+
+
+def test_geometry_and_null_context():
+    from block_quantized_gemv_nt_gb300 import nt
+    assert [nt.nt_block_bytes(f) for f in range(5)] == [34, 18, 144, 176, 210]
+    assert [nt.nt_block_elems(f) for f in range(5)] == [32, 32, 256, 256, 256]
+    assert nt.nt_block_bytes(9) == 0
+    L = nt.lib()
+    assert L.nt_gemv_q(None, 0, None, None, None, 1, 32, None, None) == nt.NT_ERR_INVALID_ARG
+    assert L.nt_ctx_sync(None) == nt.NT_ERR_INVALID_ARG
+    assert L.nt_ctx_destroy(None) == nt.NT_ERR_INVALID_ARG
+
+
+def test_no_gpu_context_fails_loudly():
+    import torch
+    from block_quantized_gemv_nt_gb300 import nt
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(nt.NtError):
+        nt.Context(0)
