@@ -65,6 +65,18 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def wait_first(self, timeout=5.0):
+        t0 = time.time()
+        while self.proc and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.02)
+        self.n0 = len(self.lines)
+
+    def wait_one_more(self, timeout=1.0):
+        t0 = time.time()
+        n = len(self.lines)
+        while self.proc and len(self.lines) == n and time.time() - t0 < timeout:
+            time.sleep(0.02)
+
     def __exit__(self, *a):
         if self.proc:
             self.proc.terminate()
@@ -158,11 +170,13 @@ def bench_gemv(args, rank, world):
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(torch.cuda.current_device()) as clk:
+            clk.wait_first()
             torch.cuda.synchronize()
             e0.record(st)
             g.replay()
             e1.record(st)
             e1.synchronize()
+            clk.wait_one_more()
         ms = e0.elapsed_time(e1)
     ms = max_over_ranks(ms, world)
     per_launch_s = ms / 1e3 / args.steps
@@ -224,6 +238,189 @@ def cpu_gemv(fmt, W, x, rows, cols, algo, budget_s=10.0):
 
 
 # ---------------------------------------------------------------------------
+# Decode workloads: the synthetic Llama shapes, one token per step
+def gemv_plan(spec):
+    """The quant-GEMV launches of one decode step, in order: (fmt, [(W, rows)], cols, x-tag, norm-tag, kind)."""
+    plan = []
+    for li in range(spec.n_layers):
+        f = spec.fmt
+        by = {}
+        for t in ("wq", "wk", "wv"):
+            by.setdefault(f[t], []).append(t)
+        for fm, ts in by.items():
+            plan.append((fm, [(li, t) for t in ts], spec.d_model, "x", ("attn_norm", li), "plain"))
+        plan.append((f["wo"], [(li, "wo")], spec.n_qh * spec.head_dim, "ao", None, "resid"))
+        plan.append((f["wg"], [(li, "wg"), (li, "wu")], spec.d_model, "x", ("ffn_norm", li), "swiglu"))
+        plan.append((f["wd"], [(li, "wd")], spec.ffn, "h", None, "resid"))
+    plan.append((spec.fmt["out"], [(-1, "out")], spec.d_model, "x", ("out_norm", -1), "plain"))
+    return plan
+
+
+def bench_decode(args, rank, world):
+    import torch
+
+    import synth
+    from block_quantized_gemv_nt_gb300 import engine, nt
+
+    spec = synth.model_spec(args.workload)
+    t0 = time.perf_counter()
+    hm = synth.make_host_model(spec)
+    t_gen = time.perf_counter() - t0
+    ctx = nt.Context(torch.cuda.current_device())
+    gm = engine.DeviceModel(ctx, spec, hm)
+    st = torch.cuda.Stream()
+    P = spec.n_prefill
+    window = spec.n_gen
+    with torch.cuda.stream(st):
+        gm.step(spec.first_token, P, stream=st)
+        for _ in range(max(3, args.warmup) - 1):
+            gm.step(-1, 0, stream=st)
+        st.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            clk.wait_first()
+            torch.cuda.synchronize()
+            e0.record(st)
+            for i in range(args.steps):
+                if i % window == 0:
+                    gm.step(spec.first_token, P, stream=st)      # restart the 128-token window
+                else:
+                    gm.step(-1, 0, stream=st)
+            e1.record(st)
+            e1.synchronize()
+            clk.wait_one_more()
+        ms = e0.elapsed_time(e1)
+    ms = max_over_ranks(ms, world)
+    tok_s = args.steps / (ms / 1e3)
+
+    # the step's quant-GEMV launches, same arguments, timed on their own (dominant kernel)
+    plan = gemv_plan(spec)
+    W = lambda li, t: gm.out if li < 0 else gm.layers[li][t]  # noqa: E731
+    norm = lambda tag: None if tag is None else (gm.out_norm if tag[1] < 0 else gm.layers[tag[1]][tag[0]])  # noqa
+    xbuf = {"x": torch.randn(spec.d_model, device="cuda"), "ao": torch.randn(spec.n_qh * spec.head_dim, device="cuda"),
+            "h": torch.randn(spec.ffn, device="cuda") * 0.01}
+    ybuf = torch.empty(max(spec.vocab, 3 * spec.ffn), device="cuda")
+    algo = 0
+    for fm, ws, cols, xt, nt_, kind in plan:
+        for li, t in ws:
+            algo += W(li, t).numel()
+        algo += 4 * cols
+    rows_out = sum(sum(W(li, t).shape[0] for li, t in ws) // (2 if kind == "swiglu" else 1) for _, ws, *_r in plan)
+    algo += 4 * rows_out
+
+    def run_plan():
+        for fm, ws, cols, xt, ntag, kind in plan:
+            g = norm(ntag)
+            if kind == "swiglu":
+                (li, tg), (_, tu) = ws
+                nt.nt_gemv_q_swiglu(ctx, fm, W(li, tg), W(li, tu), xbuf[xt], ybuf, W(li, tg).shape[0], cols,
+                                    norm_g=g, eps=spec.eps, stream=st)
+            else:
+                jobs, off = [], 0
+                for li, t in ws:
+                    r = W(li, t).shape[0]
+                    jobs.append((W(li, t), ybuf[off:], ybuf[off:] if kind == "resid" else None, r))
+                    off += ((r + 63) // 64) * 64
+                nt.nt_gemv_q_multi(ctx, fm, jobs, xbuf[xt], cols, norm_g=g, eps=spec.eps, stream=st)
+
+    with torch.cuda.stream(st):
+        run_plan()
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            run_plan()
+        g.replay()
+        st.synchronize()
+        k_reps = max(1, min(args.steps, 32))
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(st)
+        for _ in range(k_reps):
+            g.replay()
+        f1.record(st)
+        f1.synchronize()
+    gemv_ms = f0.elapsed_time(f1) / k_reps
+    n_launch = len(plan)
+    gemv_gbs = algo / (gemv_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    # e2e: host-driven loop through the C ABI: token in by value, logits + next token back to pinned host
+    logits_h = torch.empty(spec.vocab, dtype=torch.float32).pin_memory()
+    tok_h = torch.empty(1, dtype=torch.int32).pin_memory()
+    n_e2e = min(args.steps, window)
+    with torch.cuda.stream(st):
+        tok, pos = spec.first_token, P
+        st.synchronize()
+        h0 = time.perf_counter()
+        for i in range(n_e2e):
+            gm.step(tok, pos, stream=st)
+            logits_h.copy_(gm.logits, non_blocking=True)
+            tok_h.copy_(gm.next_token, non_blocking=True)
+            st.synchronize()
+            tok, pos = int(tok_h[0]), pos + 1
+        e2e_s = (time.perf_counter() - h0) / n_e2e
+    e2e_s = max_over_ranks(e2e_s, world)
+    ctx.sync()
+
+    per_step_bytes = step_bytes(spec)
+    kernels_per_step = 2 + spec.n_layers * (5 + len({spec.fmt[t] for t in ("wq", "wk", "wv")})) + 1
+    line = {
+        "metric": METRIC, "value": round(tok_s * world, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (block-quantized weights, f16 KV)",
+        "data": "synthetic: random weights of the named shape, seeded", "impl": "ours",
+        "config": {"workload": args.workload, "layers": spec.n_layers, "d_model": spec.d_model, "ffn": spec.ffn,
+                   "vocab": spec.vocab, "kv_prefill": P, "batch": 1, "seed": spec.seed,
+                   "weights": {k: synth.FMT_NAMES[v] for k, v in spec.fmt.items()},
+                   "l2": f"inputs larger than L2 ({per_step_bytes / 1e9:.2f} GB read per token)",
+                   "step_bytes": per_step_bytes,
+                   "step_hbm_gbs": round(per_step_bytes * tok_s / 1e9, 1),
+                   "step_frac_of_peak": round(per_step_bytes * tok_s / 1e9 / peak, 4)},
+        "roofline": {"bound": "hbm", "kernel": "qgemv", "achieved": round(gemv_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gemv_gbs / peak, 4), "peak_kind": peak_kind,
+                     "traffic": profile_traffic("qgemv", args.workload),
+                     "algo_bytes_per_launch": int(algo / n_launch), "launches_per_step": n_launch,
+                     "avg_launch_us": round(gemv_ms * 1e3 / n_launch, 3)},
+        "e2e": {"value": round(1.0 / e2e_s, 2), "unit": "tok/s", "h2d_bytes_per_step": 4,
+                "d2h_bytes_per_step": 4 * spec.vocab + 4},
+        "gpu_launches": args.steps * kernels_per_step + (args.steps + window - 1) // window,
+        "clocks": clk.summary(),
+        "host_generation_s": round(t_gen, 1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_decode(spec, hm, budget_s=args.cpu_budget)
+    gm.close()
+    return line
+
+
+def step_bytes(spec):
+    """Algorithmic HBM bytes of one decode token: every executed weight byte once,
+    the KV cache read (mean context of the window) and written, activations ignored
+    (they stay in L2)."""
+    import synth
+    w = spec.layer_bytes() * spec.n_layers
+    r, c = spec.tensor_shape("out")
+    w += r * synth.row_bytes(spec.fmt["out"], c)
+    w += synth.row_bytes(spec.fmt["embd"], spec.d_model)
+    ctxlen = spec.n_prefill + spec.n_gen / 2
+    kv = spec.n_layers * 2 * spec.n_kvh * spec.head_dim * 2 * (ctxlen + 1)
+    return int(w + kv)
+
+
+def cpu_decode(spec, hm, budget_s=15.0):
+    import oracle
+    om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
+    tok, pos, n = spec.first_token, spec.n_prefill, 0
+    t0 = time.perf_counter()
+    while n == 0 or time.perf_counter() - t0 < budget_s:
+        logits = om.step(tok, pos)
+        tok, pos, n = int(np.argmax(logits)), pos + 1, n + 1
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 4), "unit": "tok/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} greedy oracle decode steps of the full model in {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -266,15 +463,37 @@ def reference_arm(args, rank, world):
                 "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                                  "sample": f"{args.steps} full oracle GEMVs"},
                 "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    return {"impl": "reference", "unavailable": f"no reference arm for workload {args.workload}"}
+    spec = synth.model_spec(args.workload)
+    hm = synth.make_host_model(spec)
+    import oracle
+    om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
+    tok, pos = spec.first_token, spec.n_prefill
+    for _ in range(max(0, min(args.warmup, 1))):
+        om.step(tok, pos)
+    t0 = time.perf_counter()
+    n = max(1, min(args.steps, args.ref_max_steps))
+    for _ in range(n):
+        logits = om.step(tok, pos)
+        tok, pos = int(np.argmax(logits)), pos + 1
+    dt = (time.perf_counter() - t0) / n
+    v = round(1.0 / dt, 4)
+    return {"metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world, "steps": n, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 1), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic: random weights of the named shape, seeded", "impl": "reference",
+            "config": {"workload": args.workload, "batch": 1},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{n} greedy oracle decode steps (bounded sample of the workload)"},
+            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=128)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="gemv_q8_0_4096x4096")
+    ap.add_argument("--workload", default="llama8b_q8_0")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--ref-max-steps", type=int, default=8, help="oracle steps per reference-arm run")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -295,7 +514,7 @@ def main():
     if args.workload.startswith("gemv"):
         line = bench_gemv(args, rank, world)
     else:
-        raise SystemExit(f"unknown workload {args.workload}")
+        line = bench_decode(args, rank, world)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -112,6 +112,11 @@ nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes) {
     return NT_ERR_CUDA;
   }
   c->err_flag = reinterpret_cast<unsigned*>(c->scratch + kScratchErr);
+  if (configure_gemv(c) != NT_OK || configure_ops(c) != NT_OK) {
+    cudaFree(c->scratch);
+    delete c;
+    return NT_ERR_CUDA;
+  }
   *out = c;
   return NT_OK;
 }
@@ -182,11 +187,12 @@ nt_status nt_gemv_q(nt_ctx* ctx, int fmt, const void* W, const float* x, float* 
   return nt_gemv_q_multi(ctx, fmt, &j, 1, x, nullptr, 0.f, cols, stream);
 }
 
-nt_status nt_gemv_q_swiglu(nt_ctx* ctx, int fmt, const void* Wg, const void* Wu, const float* x, float* h,
-                           int64_t rows, int64_t cols, void* stream) {
+nt_status nt_gemv_q_swiglu(nt_ctx* ctx, int fmt, const void* Wg, const void* Wu, const float* x, const float* norm_g,
+                           float eps, float* h, int64_t rows, int64_t cols, void* stream) {
   NT_TRY(pre_call(ctx));
   NT_TRY(check_fmt_cols(ctx, fmt, cols));
   NT_TRY(check_vec(ctx, x, "x"));
+  if (norm_g) NT_TRY(check_vec(ctx, norm_g, "norm_g"));
   NT_REQUIRE(rows >= 0, NT_ERR_INVALID_ARG, "negative rows");
   if (rows == 0) return NT_OK;
   NT_REQUIRE(Wg && Wu && h, NT_ERR_INVALID_ARG, "null pointer");
@@ -194,7 +200,7 @@ nt_status nt_gemv_q_swiglu(nt_ctx* ctx, int fmt, const void* Wg, const void* Wu,
   NT_REQUIRE(aligned(h, 4), NT_ERR_ALIGNMENT, "h must be 4-byte aligned");
   nt_gemv_job j{Wg, h, nullptr, rows};
   DeviceGuard g(ctx->device);
-  return launch_gemv(ctx, fmt, &j, 1, Wu, x, nullptr, 0.f, cols, true, as_stream(stream));
+  return launch_gemv(ctx, fmt, &j, 1, Wu, x, norm_g, eps, cols, true, as_stream(stream));
 }
 
 nt_status nt_rmsnorm(nt_ctx* ctx, const float* x, const float* g, float* y, int64_t n, float eps, void* stream) {

@@ -287,7 +287,8 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int64_t i) {
   return (static_cast<unsigned long long>(o) << 32) | (0xFFFFFFFFu - unsigned(i));
 }
 
-__global__ void argmax_kernel(const float* v, int64_t n, unsigned long long* key, unsigned* counter, int32_t* out) {
+__global__ void argmax_kernel(const float* v, int64_t n, unsigned long long* key, unsigned* counter, int32_t* out,
+                              int32_t* tok_state, int64_t* pos_state) {
   __shared__ unsigned long long wbest[32];
   __shared__ bool last;
   unsigned long long best = 0ull;
@@ -312,7 +313,10 @@ __global__ void argmax_kernel(const float* v, int64_t n, unsigned long long* key
     if (last) {
       __threadfence();
       const unsigned long long k = atomicAdd(key, 0ull);
-      *out = k ? int32_t(0xFFFFFFFFu - unsigned(k & 0xFFFFFFFFull)) : 0;
+      const int32_t idx = k ? int32_t(0xFFFFFFFFu - unsigned(k & 0xFFFFFFFFull)) : 0;
+      if (out) *out = idx;
+      if (tok_state) *tok_state = idx;   // decode loop: next token and position
+      if (pos_state) *pos_state += 1;
       *key = 0ull;
       *counter = 0u;
     }
@@ -406,14 +410,14 @@ nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, floa
   a.part = part;
   a.counters = counters;
   const size_t smem = size_t(a.G) * (kHD + kMaxChunk + 8 * kHD) * sizeof(float);
-  static size_t configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return cuda_check(c, e, "attention smem attribute");
-    configured = smem;
-  }
   attn_kernel<<<dim3(n_kvh, S), kAttnThreads, smem, st>>>(a);
   return cuda_check(c, cudaGetLastError(), "attention launch");
+}
+
+nt_status configure_ops(Ctx* c) {
+  const size_t smem = size_t(kMaxGroup) * (kHD + kMaxChunk + 8 * kHD) * sizeof(float);
+  return cuda_check(c, cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
+                    "attention shared-memory attribute");
 }
 
 nt_status launch_softmax(Ctx* c, const float* x, float* y, int64_t n, cudaStream_t st) {
@@ -429,11 +433,11 @@ nt_status launch_swiglu(Ctx* c, const float* g, const float* u, float* h, int64_
 }
 
 nt_status launch_argmax(Ctx* c, const float* v, int64_t n, int32_t* out, unsigned long long* key, unsigned* counter,
-                        cudaStream_t st) {
+                        cudaStream_t st, int32_t* tok_state, int64_t* pos_state) {
   int64_t blocks = (n + 1023) / 1024;
   if (blocks > c->num_sms) blocks = c->num_sms;
   if (blocks < 1) blocks = 1;
-  argmax_kernel<<<int(blocks), 1024, 0, st>>>(v, n, key, counter, out);
+  argmax_kernel<<<int(blocks), 1024, 0, st>>>(v, n, key, counter, out, tok_state, pos_state);
   return cuda_check(c, cudaGetLastError(), "argmax launch");
 }
 

@@ -348,48 +348,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) qgemv_kernel(const GemvArgs a)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // ---- prologue: x (optionally RMS-normalised) and 16-column partial sums
-  {
-    __shared__ float red[kWarps];
-    float ss = 0.f;
-    for (int i = tid * 4; i < a.cols; i += blockDim.x * 4) {
-      const float4 v = *reinterpret_cast<const float4*>(a.x + i);
-      *reinterpret_cast<float4*>(xs + i) = v;
-      ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
-    }
-    if (a.norm_g) {
-      ss = warp_sum(ss);
-      if (lane == 0) red[warp] = ss;
-      __syncthreads();
-      float tot = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) tot += red[w];
-      const float inv = rsqrtf(tot / float(a.cols) + a.eps);
-      for (int i = tid * 4; i < a.cols; i += blockDim.x * 4) {
-        float4 v = *reinterpret_cast<float4*>(xs + i);
-        const float4 g = *reinterpret_cast<const float4*>(a.norm_g + i);
-        v.x = v.x * inv * g.x;
-        v.y = v.y * inv * g.y;
-        v.z = v.z * inv * g.z;
-        v.w = v.w * inv * g.w;
-        *reinterpret_cast<float4*>(xs + i) = v;
-      }
-    }
-    __syncthreads();
-    for (int i = tid; i < a.cols / 16; i += blockDim.x) {
-      float s = 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) s += xs[16 * i + k];
-      sx16[i] = s;
-    }
-    __syncthreads();
-  }
-
   // ---- per-warp pipeline
   const int64_t total_warps = int64_t(gridDim.x) * kWarps;
   const int64_t wg = int64_t(blockIdx.x) * kWarps + warp;
-  if (wg >= a.total_groups) return;
-  const int64_t my_groups = (a.total_groups - wg + total_warps - 1) / total_warps;
+  const int64_t my_groups = wg < a.total_groups ? (a.total_groups - wg + total_warps - 1) / total_warps : 0;
   const int64_t n_items = my_groups * a.nseg;
   uint8_t* st0 = stages + size_t(warp) * kStages * a.stb;
   const uint32_t bar0 = smem_u32(bars + warp * kStages);
@@ -464,10 +426,50 @@ __global__ void __launch_bounds__(kWarps * 32, 1) qgemv_kernel(const GemvArgs a)
     __syncwarp();
   };
 
+  // weights do not depend on x: start streaming them before the x prologue
   if (a.tma) {
     const int64_t pre = n_items < kStages - 1 ? n_items : kStages - 1;
     for (int64_t k = 0; k < pre; ++k) issue(k);
   }
+
+  // ---- prologue: x (optionally RMS-normalised) and 16-column partial sums
+  {
+    __shared__ float red[kWarps];
+    float ss = 0.f;
+    for (int i = tid * 4; i < a.cols; i += blockDim.x * 4) {
+      const float4 v = *reinterpret_cast<const float4*>(a.x + i);
+      *reinterpret_cast<float4*>(xs + i) = v;
+      ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+    }
+    if (a.norm_g) {
+      ss = warp_sum(ss);
+      if (lane == 0) red[warp] = ss;
+      __syncthreads();
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) tot += red[w];
+      const float inv = rsqrtf(tot / float(a.cols) + a.eps);
+      for (int i = tid * 4; i < a.cols; i += blockDim.x * 4) {
+        float4 v = *reinterpret_cast<float4*>(xs + i);
+        const float4 g = *reinterpret_cast<const float4*>(a.norm_g + i);
+        v.x = v.x * inv * g.x;
+        v.y = v.y * inv * g.y;
+        v.z = v.z * inv * g.z;
+        v.w = v.w * inv * g.w;
+        *reinterpret_cast<float4*>(xs + i) = v;
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < a.cols / 16; i += blockDim.x) {
+      float s = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) s += xs[16 * i + k];
+      sx16[i] = s;
+    }
+    __syncthreads();
+  }
+
+  if (my_groups == 0) return;
 
   float acc[R];
 #pragma unroll
@@ -533,14 +535,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1) qgemv_kernel(const GemvArgs a)
 
 template <int FMT, int R>
 cudaError_t launch_t(const GemvArgs& a, int grid, size_t smem, cudaStream_t st) {
-  static int configured_smem = 0;
-  if (configured_smem < int(smem)) {
-    cudaError_t e = cudaFuncSetAttribute(qgemv_kernel<FMT, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    configured_smem = int(smem);
-  }
   qgemv_kernel<FMT, R><<<grid, kWarps * 32, smem, st>>>(a);
   return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t configure_fmt(int smem) {
+  cudaError_t e = cudaFuncSetAttribute(qgemv_kernel<FMT, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(qgemv_kernel<FMT, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return e;
 }
 
 template <int FMT>
@@ -551,6 +555,18 @@ cudaError_t dispatch_r(int R, const GemvArgs& a, int grid, size_t smem, cudaStre
 constexpr int align_of(int fmt) { return (fmt == NT_Q4_K || fmt == NT_Q5_K) ? 1 : 8; }
 
 }  // namespace
+
+// Allow every GEMV instantiation the opt-in shared memory once, at context
+// creation (never during a stream capture).
+nt_status configure_gemv(Ctx* c) {
+  const int smem = int(c->smem_optin);
+  cudaError_t e = configure_fmt<NT_Q8_0>(smem);
+  if (e == cudaSuccess) e = configure_fmt<NT_Q4_0>(smem);
+  if (e == cudaSuccess) e = configure_fmt<NT_Q4_K>(smem);
+  if (e == cudaSuccess) e = configure_fmt<NT_Q5_K>(smem);
+  if (e == cudaSuccess) e = configure_fmt<NT_Q6_K>(smem);
+  return cuda_check(c, e, "gemv shared-memory attribute");
+}
 
 nt_status launch_gemv(Ctx* c, int fmt, const nt_gemv_job* jobs, int njobs, const void* W2, const float* x,
                       const float* norm_g, float eps, int64_t cols, bool swiglu, cudaStream_t st) {

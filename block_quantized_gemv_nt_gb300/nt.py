@@ -62,7 +62,7 @@ _sig("nt_block_bytes", [_ci])
 _sig("nt_block_elems", [_ci])
 _sig("nt_dequant_rows", [_vp, _ci, _vp, _i64, _i64, _i64, _vp, _vp])
 _sig("nt_gemv_q", [_vp, _ci, _vp, _vp, _vp, _i64, _i64, _vp, _vp])
-_sig("nt_gemv_q_swiglu", [_vp, _ci, _vp, _vp, _vp, _vp, _i64, _i64, _vp])
+_sig("nt_gemv_q_swiglu", [_vp, _ci, _vp, _vp, _vp, _vp, _cf, _vp, _i64, _i64, _vp])
 _sig("nt_gemv_q_multi", [_vp, _ci, ctypes.POINTER(nt_gemv_job), _ci, _vp, _vp, _cf, _i64, _vp])
 _sig("nt_rmsnorm", [_vp, _vp, _vp, _vp, _i64, _cf, _vp])
 _sig("nt_rope", [_vp, _vp, _vp, _ci, _ci, _ci, _i64, _cf, _vp])
@@ -73,9 +73,29 @@ _sig("nt_swiglu", [_vp, _vp, _vp, _vp, _i64, _vp])
 _sig("nt_argmax", [_vp, _vp, _i64, _vp, _vp])
 _sig("nt_cos_sim", [_vp, _vp, _vp, _i64, _vp, _vp])
 
+
+class nt_model_desc(ctypes.Structure):
+    _fields_ = [(n, _ci) for n in ("n_layers", "d_model", "n_qh", "n_kvh", "head_dim", "ffn", "vocab")] + [
+        ("eps", _cf), ("theta", _cf), ("kv_cap", _i64)] + [
+        (n, _ci) for n in ("fmt_q", "fmt_k", "fmt_v", "fmt_o", "fmt_gate", "fmt_up", "fmt_down", "fmt_embd",
+                           "fmt_out")]
+
+
+class nt_layer_ptrs(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "attn_norm", "ffn_norm", "kcache",
+                                   "vcache")]
+
+
+_sig("nt_model_init", [_vp, ctypes.POINTER(nt_model_desc), ctypes.POINTER(nt_layer_ptrs), _vp, _vp, _vp,
+                       ctypes.POINTER(_vp)])
+_sig("nt_model_destroy", [_vp, _vp])
+_sig("nt_decode_step", [_vp, _vp, ctypes.c_int32, _i64, _vp, _vp, _vp, _vp])
+_sig("nt_layer_skip_calibrate", [_vp, _vp, ctypes.c_int32, _i64, _ci, _vp, _vp, _vp, _vp, _vp])
+
 EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "nt_block_bytes", "nt_block_elems",
             "nt_dequant_rows", "nt_gemv_q", "nt_gemv_q_swiglu", "nt_gemv_q_multi", "nt_rmsnorm", "nt_rope",
-            "nt_rope_kv_append", "nt_attn_decode", "nt_softmax", "nt_swiglu", "nt_argmax", "nt_cos_sim"]
+            "nt_rope_kv_append", "nt_attn_decode", "nt_softmax", "nt_swiglu", "nt_argmax", "nt_cos_sim",
+            "nt_model_init", "nt_model_destroy", "nt_decode_step", "nt_layer_skip_calibrate"]
 
 
 def lib():
@@ -151,9 +171,9 @@ def nt_gemv_q(ctx, fmt, W, x, y, rows, cols, residual=None, stream=None):
                                     _stream(stream, y)))
 
 
-def nt_gemv_q_swiglu(ctx, fmt, Wg, Wu, x, h, rows, cols, stream=None):
-    return ctx.check(_lib.nt_gemv_q_swiglu(ctx.handle, fmt, _ptr(Wg), _ptr(Wu), _ptr(x), _ptr(h), rows, cols,
-                                           _stream(stream, h)))
+def nt_gemv_q_swiglu(ctx, fmt, Wg, Wu, x, h, rows, cols, norm_g=None, eps=0.0, stream=None):
+    return ctx.check(_lib.nt_gemv_q_swiglu(ctx.handle, fmt, _ptr(Wg), _ptr(Wu), _ptr(x), _ptr(norm_g), eps, _ptr(h),
+                                           rows, cols, _stream(stream, h)))
 
 
 def nt_gemv_q_multi(ctx, fmt, jobs, x, cols, norm_g=None, eps=0.0, stream=None):
@@ -198,3 +218,45 @@ def nt_argmax(ctx, v, n, out, stream=None):
 
 def nt_cos_sim(ctx, a, b, n, out, stream=None):
     return ctx.check(_lib.nt_cos_sim(ctx.handle, _ptr(a), _ptr(b), n, _ptr(out), _stream(stream, out)))
+
+
+def nt_model_init(ctx, desc: nt_model_desc, layers, embd, out, out_norm) -> int:
+    """layers: list of dicts with wq..wd, attn_norm, ffn_norm, kcache, vcache (tensors or int pointers)."""
+    arr = (nt_layer_ptrs * len(layers))()
+    for i, L in enumerate(layers):
+        arr[i] = nt_layer_ptrs(*[_ptr(L.get(n)) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "attn_norm",
+                                                          "ffn_norm", "kcache", "vcache")])
+    h = _vp()
+    ctx.check(_lib.nt_model_init(ctx.handle, ctypes.byref(desc), arr, _ptr(embd), _ptr(out), _ptr(out_norm),
+                                 ctypes.byref(h)))
+    return h.value
+
+
+def nt_model_destroy(ctx, model: int):
+    return ctx.check(_lib.nt_model_destroy(ctx.handle, model))
+
+
+def _mask_ptr(mask):
+    if mask is None:
+        return None, None
+    import numpy as np
+    m = np.ascontiguousarray(mask, dtype=np.uint8)
+    return m, m.ctypes.data
+
+
+def nt_decode_step(ctx, model: int, token: int, pos: int, skip_mask, logits, next_token=None, stream=None):
+    keep, mp = _mask_ptr(skip_mask)
+    return ctx.check(_lib.nt_decode_step(ctx.handle, model, token, pos, mp, _ptr(logits), _ptr(next_token),
+                                         _stream(stream, logits)))
+
+
+def nt_layer_skip_calibrate(ctx, model: int, token: int, pos: int, n_skip: int, n_layers: int, logits,
+                            next_token=None, stream=None):
+    """Returns (skip_mask uint8[n_layers], cos float32[n_layers])."""
+    import numpy as np
+    mask = np.zeros(n_layers, dtype=np.uint8)
+    cos = np.zeros(n_layers, dtype=np.float32)
+    ctx.check(_lib.nt_layer_skip_calibrate(ctx.handle, model, token, pos, n_skip, mask.ctypes.data,
+                                           cos.ctypes.data, _ptr(logits), _ptr(next_token),
+                                           _stream(stream, logits)))
+    return mask, cos

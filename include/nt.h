@@ -96,10 +96,12 @@ nt_status nt_gemv_q(nt_ctx* ctx, int fmt, const void* W_dev, const float* x_dev,
                     int64_t cols, const float* residual_dev, void* stream);
 
 /* Gate/up GEMV with the SwiGLU epilogue [feat] SwiGLU:
- *   h[r] = silu(Wg[r,:] . x) * (Wu[r,:] . x),  silu(z) = z / (1 + e^-z).
- * Wg and Wu share format and shape. */
+ *   h[r] = silu(Wg[r,:] . x') * (Wu[r,:] . x'),  silu(z) = z / (1 + e^-z),
+ * x' = x, or x / sqrt(mean(x^2) + eps) * g when norm_g_dev != NULL (the FFN
+ * RMSNorm fused in front).  Wg and Wu share format and shape. */
 nt_status nt_gemv_q_swiglu(nt_ctx* ctx, int fmt, const void* Wg_dev, const void* Wu_dev, const float* x_dev,
-                           float* h_dev, int64_t rows, int64_t cols, void* stream);
+                           const float* norm_g_dev, float eps, float* h_dev, int64_t rows, int64_t cols,
+                           void* stream);
 
 /* One launch of several GEMVs sharing x (e.g. Q, K and V), optionally with the
  * RMSNorm of x fused in front:  x' = x / sqrt(mean(x^2) + eps) * g  when
@@ -152,6 +154,59 @@ nt_status nt_argmax(nt_ctx* ctx, const float* v_dev, int64_t n, int32_t* out_dev
 /* Cosine similarity [cache] of a and b: <a,b> / (|a| |b|), fp32 result. */
 nt_status nt_cos_sim(nt_ctx* ctx, const float* a_dev, const float* b_dev, int64_t n, float* out_dev,
                      void* stream);
+
+
+/* ---- whole decode step ------------------------------------------------------ */
+
+/* Shapes and per-tensor formats of a Llama-architecture model [feat]
+ * (Q4_K_M = attn_v and ffn_down in Q6_K, the rest in Q4_K [about]). */
+typedef struct {
+  int n_layers, d_model, n_qh, n_kvh, head_dim, ffn, vocab;
+  float eps, theta;
+  int64_t kv_cap;                       /* positions per (layer, KV head) in the caches */
+  int fmt_q, fmt_k, fmt_v, fmt_o, fmt_gate, fmt_up, fmt_down, fmt_embd, fmt_out;
+} nt_model_desc;
+
+/* Device pointers of one layer.  Weights: row-major block matrices
+ * wq [n_qh*hd x d], wk/wv [n_kvh*hd x d], wo [d x n_qh*hd], wg/wu [ffn x d],
+ * wd [d x ffn]; norms fp32 [d]; caches binary16 [n_kvh][kv_cap][head_dim].
+ * A streamed layer may leave its weight pointers NULL: nt_stream_layer binds
+ * them per step. */
+typedef struct {
+  const void *wq, *wk, *wv, *wo, *wg, *wu, *wd;
+  const float *attn_norm, *ffn_norm;
+  void *kcache, *vcache;
+} nt_layer_ptrs;
+
+/* Bind a model: copies the descriptor and the pointer table (the buffers stay
+ * the caller's) and allocates the model's activations and step state on the
+ * device.  embd [vocab x d] and out [vocab x d] are block matrices, out_norm
+ * fp32 [d]. */
+nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_ptrs* layers, const void* embd_dev,
+                        const void* out_dev, const float* out_norm_dev, nt_model** out);
+nt_status nt_model_destroy(nt_ctx* ctx, nt_model* model);
+
+/* One batch-1 decode step [code] model/ + inference/:
+ *   x = embd[token];  per layer l with skip_mask_host[l] == 0:
+ *     q,k,v = W{q,k,v} rmsnorm(x, g_attn); rope(q, k, pos); K/V[l][:,pos] = f16(k, v)
+ *     x += Wo attn(q, K/V[l][:, :pos+1]);  x += Wd (silu(Wg xn) * (Wu xn)), xn = rmsnorm(x, g_ffn)
+ *   logits_dev = Wout rmsnorm(x, g_out);  next = argmax(logits) (lowest index on ties)
+ * token >= 0: start from (token, pos).  token < 0: continue on the device
+ * from the previous step (token = its argmax, pos = its pos + 1) with no host
+ * round trip.  next_token_dev (nullable) receives the argmax.  Each distinct
+ * (skip mask, logits, next_token) is captured once into a CUDA graph and
+ * replayed.  skip_mask_host is n_layers bytes or NULL. */
+nt_status nt_decode_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos, const uint8_t* skip_mask_host,
+                         float* logits_dev, int32_t* next_token_dev, void* stream);
+
+/* Layer-skip calibration [cache]: one full decode step (all layers) at
+ * (token, pos) that also measures cos(x before layer l, x after layer l) for
+ * every layer; marks the n_skip layers with the highest cosine (ties: lower
+ * index) in skip_mask_host[n_layers].  cos_host (nullable) gets the cosines.
+ * Synchronous on `stream`. */
+nt_status nt_layer_skip_calibrate(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos, int n_skip,
+                                  uint8_t* skip_mask_host, float* cos_host, float* logits_dev,
+                                  int32_t* next_token_dev, void* stream);
 
 #ifdef __cplusplus
 }

@@ -117,18 +117,21 @@ def test_gemv_residual_and_multi_with_norm(ctx, fmt):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-@pytest.mark.parametrize("rows,cols", [(333, 4096), (1, 256), (96, 28672)])
-def test_gemv_swiglu(ctx, fmt, rows, cols):
+@pytest.mark.parametrize("rows,cols,norm", [(333, 4096, False), (1, 256, False), (96, 28672, False),
+                                            (1001, 4096, True)])
+def test_gemv_swiglu(ctx, fmt, rows, cols, norm):
     nt = _nt()
     Wg = synth.quant_matrix(fmt, rows, cols, seed=5, stream=1)
     Wu = synth.quant_matrix(fmt, rows, cols, seed=5, stream=2)
     x = synth.normal_f32(cols, seed=5, stream=3) * 0.05
+    g = synth.normal_f32(cols, seed=5, stream=4, mean=1.0, std=0.02)
     h = torch.empty(rows, dtype=torch.float32, device="cuda")
-    nt.nt_gemv_q_swiglu(ctx, fmt, dev(Wg), dev(Wu), dev(x), h, rows, cols)
+    nt.nt_gemv_q_swiglu(ctx, fmt, dev(Wg), dev(Wu), dev(x), h, rows, cols, norm_g=dev(g) if norm else None, eps=1e-5)
     torch.cuda.synchronize()
-    g = oracle.gemv(fmt, Wg, x.astype(np.float64), rows, cols)
-    u = oracle.gemv(fmt, Wu, x.astype(np.float64), rows, cols)
-    assert rel_l2(host(h), oracle.swiglu(g, u)) <= TOL
+    xin = oracle.rmsnorm(x.astype(np.float64), g, 1e-5) if norm else x.astype(np.float64)
+    gg = oracle.gemv(fmt, Wg, xin, rows, cols)
+    u = oracle.gemv(fmt, Wu, xin, rows, cols)
+    assert rel_l2(host(h), oracle.swiglu(gg, u)) <= TOL
 
 
 @pytest.mark.parametrize("fmt", FMTS)
