@@ -25,6 +25,9 @@ nt_status cuda_check(Ctx* c, cudaError_t e, const char* what) {
   return set_err(c, e == cudaErrorMemoryAllocation ? NT_ERR_OOM : NT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// failures of nt_ctx_create have no context to hold their message
+thread_local std::string g_create_error;
+
 }  // namespace nt
 
 using namespace nt;
@@ -86,7 +89,10 @@ nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes) {
   if (!out) return NT_ERR_INVALID_ARG;
   *out = nullptr;
   int ndev = 0;
-  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+  cudaError_t ce = cudaGetDeviceCount(&ndev);
+  if (ce != cudaSuccess || device < 0 || device >= ndev) {
+    g_create_error = ce != cudaSuccess ? std::string("cudaGetDeviceCount: ") + cudaGetErrorString(ce)
+                                       : "device " + std::to_string(device) + " not present";
     cudaGetLastError();
     return NT_ERR_CUDA;
   }
@@ -103,16 +109,19 @@ nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes) {
   if (c->scratch_bytes < (size_t(1) << 20)) c->scratch_bytes = size_t(1) << 20;
   if (cudaMalloc(&c->scratch, c->scratch_bytes) != cudaSuccess) {
     cudaGetLastError();
+    g_create_error = "scratch allocation failed";
     delete c;
     return NT_ERR_OOM;
   }
   if (cudaMemset(c->scratch, 0, c->scratch_bytes) != cudaSuccess) {
+    g_create_error = "scratch memset failed";
     cudaFree(c->scratch);
     delete c;
     return NT_ERR_CUDA;
   }
   c->err_flag = reinterpret_cast<unsigned*>(c->scratch + kScratchErr);
   if (configure_gemv(c) != NT_OK || configure_ops(c) != NT_OK) {
+    g_create_error = c->last_error;
     cudaFree(c->scratch);
     delete c;
     return NT_ERR_CUDA;
@@ -147,7 +156,7 @@ nt_status nt_ctx_sync(nt_ctx* ctx) {
   return NT_OK;
 }
 
-const char* nt_last_error(const nt_ctx* ctx) { return ctx ? ctx->last_error.c_str() : "null context"; }
+const char* nt_last_error(const nt_ctx* ctx) { return ctx ? ctx->last_error.c_str() : g_create_error.c_str(); }
 
 nt_status nt_dequant_rows(nt_ctx* ctx, int fmt, const void* W, int64_t row0, int64_t nrows, int64_t cols,
                           float* out, void* stream) {

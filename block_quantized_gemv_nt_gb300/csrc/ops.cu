@@ -416,8 +416,11 @@ nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, floa
 
 nt_status configure_ops(Ctx* c) {
   const size_t smem = size_t(kMaxGroup) * (kHD + kMaxChunk + 8 * kHD) * sizeof(float);
-  return cuda_check(c, cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
-                    "attention shared-memory attribute");
+  cudaFuncAttributes fa{};
+  cudaError_t e = cudaFuncGetAttributes(&fa, attn_kernel);
+  if (e == cudaSuccess && smem + fa.sharedSizeBytes > c->smem_optin) e = cudaErrorInvalidValue;
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  return cuda_check(c, e, "attention shared-memory attribute");
 }
 
 nt_status launch_softmax(Ctx* c, const float* x, float* y, int64_t n, cudaStream_t st) {

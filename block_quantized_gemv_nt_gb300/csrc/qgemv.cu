@@ -539,11 +539,19 @@ cudaError_t launch_t(const GemvArgs& a, int grid, size_t smem, cudaStream_t st) 
   return cudaGetLastError();
 }
 
+// dynamic shared memory a kernel may use: the opt-in limit minus its static part
+template <typename K>
+cudaError_t allow_smem(K kernel, int optin) {
+  cudaFuncAttributes fa{};
+  cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - int(fa.sharedSizeBytes));
+}
+
 template <int FMT>
 cudaError_t configure_fmt(int smem) {
-  cudaError_t e = cudaFuncSetAttribute(qgemv_kernel<FMT, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(qgemv_kernel<FMT, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = allow_smem(qgemv_kernel<FMT, 4>, smem);
+  if (e == cudaSuccess) e = allow_smem(qgemv_kernel<FMT, 2>, smem);
   return e;
 }
 

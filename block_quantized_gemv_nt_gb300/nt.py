@@ -126,7 +126,7 @@ class Context:
         h = _vp()
         st = _lib.nt_ctx_create(ctypes.byref(h), device, scratch_bytes)
         if st != NT_OK:
-            raise NtError(st, "nt_ctx_create failed")
+            raise NtError(st, "nt_ctx_create failed: " + (_lib.nt_last_error(None) or b"").decode())
         self.handle = h.value
         self.device = device
 

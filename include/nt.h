@@ -72,6 +72,7 @@ typedef struct nt_model nt_model;
  * default (64 MiB).  The context allocates its scratch on the device. */
 nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes);
 nt_status nt_ctx_destroy(nt_ctx* ctx);
+/* nt_last_error(NULL) describes the last failed nt_ctx_create of this thread. */
 /* Wait for all work of this context's device, then report any asynchronous
  * CUDA error or device-side timeout flag (NT_ERR_TIMEOUT) and clear the flag. */
 nt_status nt_ctx_sync(nt_ctx* ctx);
