@@ -644,11 +644,11 @@ nt_status launch_gemv(Ctx* c, int fmt, const nt_gemv_job* jobs, int njobs, const
   a.total_groups = g;
   a.err = c->err_flag;
 
-  // balance whole groups over warps: every warp gets ceil or floor of g / warps
-  const int64_t max_warps = int64_t(c->num_sms) * kWarps;
-  const int64_t per = (g + max_warps - 1) / max_warps;
-  const int64_t warps = (g + per - 1) / per;
-  const int grid = int((warps + kWarps - 1) / kWarps);
+  // every SM gets a CTA (fewer only when there are fewer groups than warps);
+  // groups go round-robin, so warps differ by at most one group
+  int64_t grid64 = (g + kWarps - 1) / kWarps;
+  if (grid64 > c->num_sms) grid64 = c->num_sms;
+  const int grid = int(grid64);
   const size_t smem = size_t(head) + size_t(kWarps) * kStages * stb + pad;
 
   cudaError_t e;

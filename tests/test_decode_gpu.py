@@ -46,13 +46,15 @@ def _run(ctx, name, n_steps, skip=None, continue_on_device=False, layers=None):
         assert int(gm.next_token.item()) == g_arg
         tok, pos = g_arg, pos + 1
     ctx.sync()
-    # the KV written by the GPU matches the oracle's to within one f16 ulp
+    # the KV written by the GPU matches the oracle's: one f16 ulp of the value plus
+    # the fp32 GEMV rounding relative to the scale of the head (cancellation)
     kg = gm.layers[0]["kcache"].cpu().numpy().astype(np.float64)
     ko = om.kcache[0].astype(np.float64)
     P0 = spec.n_prefill
     if skip is None or not skip[0]:
-        d = np.abs(kg[:, P0:P0 + n_steps] - ko[:, P0:P0 + n_steps])
-        assert np.all(d <= np.abs(ko[:, P0:P0 + n_steps]) * 2 ** -9 + 1e-6)
+        new_o, new_g = ko[:, P0:P0 + n_steps], kg[:, P0:P0 + n_steps]
+        scale = np.sqrt(np.mean(new_o ** 2, axis=-1, keepdims=True))
+        assert np.all(np.abs(new_g - new_o) <= np.abs(new_o) * 2 ** -10 + 1e-4 * scale)
     gm.close()
     print(f"{name}: worst max|err|/std = {worst:.2e}, argmax agree {agree}/{n_steps}")
     return worst, agree
