@@ -1,6 +1,7 @@
 // api.cu — the extern "C" boundary of libnt.so (declared in include/nt.h):
 // context management and argument checking of every single-op entry point.
 // Nothing is launched until every check has passed.
+#include <cstdlib>
 #include <cstring>
 
 #include "nt_internal.cuh"
@@ -105,6 +106,16 @@ nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes) {
   c->num_sms = v;
   cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   c->smem_optin = size_t(v);
+  auto env_int = [](const char* name, int lo, int hi, int dflt) {
+    const char* v = getenv(name);
+    if (!v) return dflt;
+    const int x = atoi(v);
+    return (x >= lo && x <= hi) ? x : dflt;
+  };
+  c->gemv_warps = env_int("NT_GEMV_WARPS", 2, 8, 8);
+  c->gemv_stages = env_int("NT_GEMV_STAGES", 2, 8, 4);
+  c->gemv_stage_max = env_int("NT_GEMV_STAGE_MAX", 1024, 65536, 12288) / 16 * 16;
+  c->pdl = env_int("NT_PDL", 0, 1, 1) != 0;
   c->scratch_bytes = scratch_bytes ? scratch_bytes : (size_t(64) << 20);
   if (c->scratch_bytes < (size_t(1) << 20)) c->scratch_bytes = size_t(1) << 20;
   if (cudaMalloc(&c->scratch, c->scratch_bytes) != cudaSuccess) {

@@ -31,6 +31,7 @@ struct nt_model {
   char* buf = nullptr;           // one device allocation for everything below
   float *x = nullptr, *q = nullptr, *k = nullptr, *v = nullptr, *ao = nullptr, *h = nullptr, *xin = nullptr;
   float* cos = nullptr;
+  double* inv_freq = nullptr;    // RoPE frequencies theta^(-2i/head_dim), fp64
   int32_t* tok = nullptr;        // device step state
   int64_t* pos = nullptr;
   unsigned long long* amax_key = nullptr;
@@ -46,6 +47,7 @@ namespace nt {
 namespace {
 
 __global__ void set_state_kernel(int32_t* tok, int64_t* pos, int32_t t, int64_t p) {
+  pdl_wait();
   *tok = t;
   *pos = p;
 }
@@ -74,29 +76,28 @@ nt_status enqueue_step(Ctx* c, nt_model* m, const uint8_t* skip, float* logits, 
                      "copy x");
       if (s) return s;
     }
-    // Q, K, V: one launch per distinct format, attention RMSNorm fused in front
+    // Q, K, V: one launch per distinct format; attention RMSNorm fused in
+    // front, RoPE and the f16 KV append fused behind
     {
-      const void* W[3] = {L.wq, L.wk, L.wv};
-      float* Y[3] = {m->q, m->k, m->v};
-      const int64_t R[3] = {nq, nkv, nkv};
+      const RopeArgs ra{m->pos, m->inv_freq, hd, d.kv_cap};
+      const GemvJobEx J[3] = {GemvJobEx{nt_gemv_job{L.wq, m->q, nullptr, nq}, kEpiRope, nullptr},
+                              GemvJobEx{nt_gemv_job{L.wk, nullptr, nullptr, nkv}, kEpiRopeCache, L.kcache},
+                              GemvJobEx{nt_gemv_job{L.wv, nullptr, nullptr, nkv}, kEpiCache, L.vcache}};
       const int F[3] = {d.fmt_q, d.fmt_k, d.fmt_v};
       bool done[3] = {false, false, false};
       for (int i = 0; i < 3; ++i) {
         if (done[i]) continue;
-        nt_gemv_job jobs[3];
+        GemvJobEx jobs[3];
         int nj = 0;
         for (int j = i; j < 3; ++j)
           if (!done[j] && F[j] == F[i]) {
-            jobs[nj++] = nt_gemv_job{W[j], Y[j], nullptr, R[j]};
+            jobs[nj++] = J[j];
             done[j] = true;
           }
-        s = launch_gemv(c, F[i], jobs, nj, nullptr, m->x, L.attn_norm, d.eps, d.d_model, false, st);
+        s = launch_gemv_ex(c, F[i], jobs, nj, nullptr, m->x, L.attn_norm, d.eps, d.d_model, false, &ra, st);
         if (s) return s;
       }
     }
-    s = launch_rope_append(c, m->q, m->k, m->v, L.kcache, L.vcache, d.n_qh, d.n_kvh, hd, 0, m->pos, d.kv_cap,
-                           d.theta, st);
-    if (s) return s;
     s = launch_attn(c, m->q, L.kcache, L.vcache, m->ao, d.n_qh, d.n_kvh, 0, m->pos, d.kv_cap, m->attn_part,
                     m->attn_cnt, m->S, st);
     if (s) return s;
@@ -184,9 +185,9 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   m->S = attn_splits(ctx, d.n_kvh, d.kv_cap);
   const size_t fl = sizeof(float);
   const size_t nx = up256(fl * d.d_model), nqb = up256(fl * nq), nkb = up256(fl * d.n_kvh * d.head_dim),
-               nh = up256(fl * d.ffn), ncos = up256(fl * d.n_layers), nst = 256,
+               nh = up256(fl * d.ffn), ncos = up256(fl * d.n_layers), nst = 256, nfreq = up256(8 * d.head_dim),
                npart = up256(attn_scratch_bytes(d.n_qh, d.n_kvh, m->S));
-  const size_t total = 2 * nx + nqb * 2 + nkb * 2 + nh + ncos + nst + npart;
+  const size_t total = 2 * nx + nqb * 2 + nkb * 2 + nh + ncos + nst + npart + nfreq;
   int dev_prev = 0;
   cudaGetDevice(&dev_prev);
   cudaSetDevice(ctx->device);
@@ -218,9 +219,18 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   m->pos = reinterpret_cast<int64_t*>(stt + 8);
   m->amax_key = reinterpret_cast<unsigned long long*>(stt + 16);
   m->amax_cnt = reinterpret_cast<unsigned*>(stt + 24);
+  m->inv_freq = reinterpret_cast<double*>(take(nfreq));
   char* part = take(npart);
   m->attn_cnt = reinterpret_cast<unsigned*>(part);
   m->attn_part = reinterpret_cast<float*>(part + 64 * sizeof(unsigned));
+  cudaSetDevice(ctx->device);
+  nt_status st = launch_inv_freq(ctx, m->inv_freq, d.head_dim, d.theta, nullptr);
+  if (!st) st = cuda_check(ctx, cudaDeviceSynchronize(), "model init");
+  cudaSetDevice(dev_prev);
+  if (st) {
+    nt_model_destroy(ctx, m);
+    return st;
+  }
   *res = m;
   return NT_OK;
 }

@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <utility>
 
 #include "../../include/nt.h"
 
@@ -25,6 +26,10 @@ struct Ctx {
   char* scratch = nullptr;      // device scratch owned by the context
   size_t scratch_bytes = 0;
   unsigned* err_flag = nullptr; // device word, set by kernels whose bounded wait ran out
+  bool pdl = true;               // launch with programmatic stream serialization
+  int gemv_warps = 8;            // quant-GEMV launch shape (tuning knobs, env NT_GEMV_*)
+  int gemv_stages = 4;
+  int gemv_stage_max = 12288;
   std::string last_error;
   std::mutex mu;
 };
@@ -97,6 +102,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// Programmatic dependent launch: a kernel may start before its predecessor on
+// the stream has finished; pdl_wait() blocks until the predecessor grid has
+// completed and its writes are visible (a no-op without the launch attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void flag_error(unsigned* err, unsigned code) {
   if (err) atomicOr(err, code);
 }
@@ -109,9 +120,65 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
 
+// cos and sin of pos * inv_freq: the angle and its reduction modulo 2*pi in
+// fp64 (angles reach thousands of radians), the trigonometry in fp32 on
+// the reduced angle.
+__device__ __forceinline__ void rope_cs(int64_t pos, double inv_freq, float& c, float& s) {
+  const double ang = double(pos) * inv_freq;
+  const double k = rint(ang * 0.15915494309189533577);    // 1 / (2 pi)
+  double r = fma(-k, 6.283185307179586232, ang);          // 2 pi, high part
+  r = fma(-k, 2.4492935982947064e-16, r);                 // 2 pi, low part
+  sincosf(float(r), &s, &c);
+}
+
+__device__ __forceinline__ double rope_inv_freq(int pair, int head_dim, float theta) {
+  return pow(double(theta), -2.0 * double(pair) / double(head_dim));
+}
+
+// kernel launch with the programmatic-serialization attribute when enabled
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(const Ctx* c, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (c && c->pdl) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // launch helpers (defined in the op files) -----------------------------------------
+// epilogue of one GEMV job
+enum Epi : int {
+  kEpiPlain = 0,      // y = Wx (+ residual)
+  kEpiRope = 1,       // y = rope(Wx) on adjacent row pairs (fp32 q)
+  kEpiRopeCache = 2,  // cache[head][pos][d] = f16(rope(Wx))       (k)
+  kEpiCache = 3,      // cache[head][pos][d] = f16(Wx)              (v)
+};
+
+struct RopeArgs {
+  const int64_t* pos_dev;   // device position (decode step state)
+  const double* inv_freq;   // [head_dim/2]
+  int head_dim;
+  int64_t kv_stride;
+};
+
+struct GemvJobEx {
+  nt_gemv_job j;
+  int epi;
+  void* cache;  // f16 cache of one layer [n_kvh][kv_stride][head_dim] for kEpi*Cache
+};
+
 nt_status launch_gemv(Ctx* c, int fmt, const nt_gemv_job* jobs, int njobs, const void* W2, const float* x,
                       const float* norm_g, float eps, int64_t cols, bool swiglu, cudaStream_t st);
+nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobs, int njobs, const void* W2, const float* x,
+                         const float* norm_g, float eps, int64_t cols, bool swiglu, const RopeArgs* rope,
+                         cudaStream_t st);
 
 }  // namespace nt
 

@@ -57,15 +57,9 @@ __global__ void __launch_bounds__(1024) rmsnorm_kernel(const float* x, const flo
 }
 
 // ---- RoPE ----------------------------------------------------------------------
-// pair i of every head turns by pos * theta^(-2i/head_dim); angles in fp64.
+// pair i of every head turns by pos * theta^(-2i/head_dim)
 __device__ __forceinline__ void rope_table(float* cs, float* sn, int head_dim, int64_t pos, float theta) {
-  for (int i = threadIdx.x; i < head_dim / 2; i += blockDim.x) {
-    const double ang = double(pos) * pow(double(theta), -2.0 * double(i) / double(head_dim));
-    double s, c;
-    sincos(ang, &s, &c);
-    cs[i] = float(c);
-    sn[i] = float(s);
-  }
+  for (int i = threadIdx.x; i < head_dim / 2; i += blockDim.x) rope_cs(pos, rope_inv_freq(i, head_dim, theta), cs[i], sn[i]);
   __syncthreads();
 }
 
@@ -111,12 +105,13 @@ __global__ void rope_append_kernel(float* q, const float* k, const float* v, __h
 
 // ---- split-K GQA decode attention ----------------------------------------------
 // grid (n_kvh, S); CTA (g, s) covers positions [s*chunk, (s+1)*chunk) of KV head
-// g for its whole group of G q heads, so K and V are read once per group.
+// g for its whole group of G q heads, so K and V are read once per group.  The
+// chunk of K and of V (contiguous in the cache) arrive by two TMA bulk copies.
 // Partials (m, l, o[128]) go to scratch; the last CTA of a KV head combines.
 constexpr int kAttnThreads = 256;
 constexpr int kHD = 128;
 constexpr int kMaxGroup = 16;
-constexpr int kMaxChunk = 512;
+constexpr int kMaxChunk = 128;
 
 struct AttnArgs {
   const float* q;
@@ -129,35 +124,63 @@ struct AttnArgs {
   int64_t kv_stride;
   float* part;             // [n_kvh][S][G][2 + 128]
   unsigned* counters;      // [n_kvh]
+  unsigned* err;
 };
 
+__host__ __device__ constexpr size_t attn_smem_bytes(int G) {
+  return size_t(2) * kMaxChunk * kHD * 2 + size_t(G) * kHD * 4 + size_t(G) * kMaxChunk * 4 + size_t(8) * G * kHD * 4 +
+         16;
+}
+
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(128) uint8_t asmem[];
   const int G = a.G;
-  float* qs = sm;                       // [G][128], pre-scaled by 1/sqrt(128)
-  float* sc = qs + G * kHD;             // [G][kMaxChunk] scores, then probabilities
-  float* red = sc + G * kMaxChunk;      // [8 warps][G][128]
+  __half* Ks = reinterpret_cast<__half*>(asmem);                    // [kMaxChunk][128]
+  __half* Vs = Ks + kMaxChunk * kHD;                                 // [kMaxChunk][128]
+  float* qs = reinterpret_cast<float*>(Vs + kMaxChunk * kHD);        // [G][128], pre-scaled by 1/sqrt(128)
+  float* sc = qs + G * kHD;                                          // [G][kMaxChunk]
+  float* red = sc + G * kMaxChunk;                                   // [8 warps][G][128]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 8 * G * kHD);
   __shared__ float stat[2 * kMaxGroup];
   __shared__ bool last;
 
   const int g = blockIdx.x, s = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_trigger();
   const int64_t n_pos = a.pos_dev ? *a.pos_dev + 1 : a.n_pos;
   const int64_t chunk = (n_pos + a.S - 1) / a.S;
   const int64_t p0 = int64_t(s) * chunk;
   const int64_t p1 = min(n_pos, p0 + chunk);
   const int np = p1 > p0 ? int(p1 - p0) : 0;
+  const __half* Kg = a.K + int64_t(g) * a.kv_stride * kHD;
+  const __half* Vg = a.V + int64_t(g) * a.kv_stride * kHD;
+  const uint32_t b = smem_u32(bar);
 
+  if (tid == 0) {
+    mbar_init(b, 1);
+    fence_barrier_init();
+    if (np > 0) {
+      const uint32_t bytes = uint32_t(np) * kHD * 2;
+      mbar_arrive_expect_tx(b, 2 * bytes);
+      const uint64_t pol = policy_evict_first();
+      bulk_g2s(smem_u32(Ks), Kg + p0 * kHD, bytes, b, pol);
+      bulk_g2s(smem_u32(Vs), Vg + p0 * kHD, bytes, b, pol);
+    }
+  }
   const float scale = rsqrtf(float(kHD));
   for (int i = tid; i < G * kHD; i += kAttnThreads) qs[i] = a.q[int64_t(g) * G * kHD + i] * scale;
   __syncthreads();
-
-  const __half* Kg = a.K + int64_t(g) * a.kv_stride * kHD;
-  const __half* Vg = a.V + int64_t(g) * a.kv_stride * kHD;
+  bool ok = true;
+  if (np > 0) ok = mbar_wait(b, 0);
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) flag_error(a.err, kErrWaitTimeout);
+    return;
+  }
 
   // scores: warp per position, lane owns dims 4*lane .. 4*lane+3
   for (int j = warp; j < np; j += 8) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(Kg + (p0 + j) * kHD + 4 * lane);
+    const uint2 raw = *reinterpret_cast<const uint2*>(Ks + j * kHD + 4 * lane);
     const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
     const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
     for (int h = 0; h < G; ++h) {
@@ -196,7 +219,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
 #pragma unroll
   for (int h = 0; h < kMaxGroup; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
   for (int j = warp; j < np; j += 8) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(Vg + (p0 + j) * kHD + 4 * lane);
+    const uint2 raw = *reinterpret_cast<const uint2*>(Vs + j * kHD + 4 * lane);
     const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
     const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
 #pragma unroll
@@ -289,6 +312,8 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int64_t i) {
 
 __global__ void argmax_kernel(const float* v, int64_t n, unsigned long long* key, unsigned* counter, int32_t* out,
                               int32_t* tok_state, int64_t* pos_state) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ unsigned long long wbest[32];
   __shared__ bool last;
   unsigned long long best = 0ull;
@@ -325,6 +350,8 @@ __global__ void argmax_kernel(const float* v, int64_t n, unsigned long long* key
 
 // ---- cosine similarity --------------------------------------------------------------
 __global__ void __launch_bounds__(1024) cos_kernel(const float* x, const float* y, int64_t n, float* out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ double red[3][32];
   double ab = 0, aa = 0, bb = 0;
   for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
@@ -409,18 +436,28 @@ nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, floa
   a.kv_stride = kv_stride;
   a.part = part;
   a.counters = counters;
-  const size_t smem = size_t(a.G) * (kHD + kMaxChunk + 8 * kHD) * sizeof(float);
-  attn_kernel<<<dim3(n_kvh, S), kAttnThreads, smem, st>>>(a);
-  return cuda_check(c, cudaGetLastError(), "attention launch");
+  a.err = c->err_flag;
+  const size_t smem = attn_smem_bytes(a.G);
+  return cuda_check(c, launch_k(c, attn_kernel, dim3(n_kvh, S), dim3(kAttnThreads), smem, st, a),
+                    "attention launch");
 }
 
 nt_status configure_ops(Ctx* c) {
-  const size_t smem = size_t(kMaxGroup) * (kHD + kMaxChunk + 8 * kHD) * sizeof(float);
+  const size_t smem = attn_smem_bytes(kMaxGroup);
   cudaFuncAttributes fa{};
   cudaError_t e = cudaFuncGetAttributes(&fa, attn_kernel);
   if (e == cudaSuccess && smem + fa.sharedSizeBytes > c->smem_optin) e = cudaErrorInvalidValue;
   if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   return cuda_check(c, e, "attention shared-memory attribute");
+}
+
+__global__ void inv_freq_kernel(double* out, int head_dim, float theta) {
+  for (int i = threadIdx.x; i < head_dim / 2; i += blockDim.x) out[i] = rope_inv_freq(i, head_dim, theta);
+}
+
+nt_status launch_inv_freq(Ctx* c, double* out, int head_dim, float theta, cudaStream_t st) {
+  inv_freq_kernel<<<1, 128, 0, st>>>(out, head_dim, theta);
+  return cuda_check(c, cudaGetLastError(), "inv_freq launch");
 }
 
 nt_status launch_softmax(Ctx* c, const float* x, float* y, int64_t n, cudaStream_t st) {
@@ -440,8 +477,9 @@ nt_status launch_argmax(Ctx* c, const float* v, int64_t n, int32_t* out, unsigne
   int64_t blocks = (n + 1023) / 1024;
   if (blocks > c->num_sms) blocks = c->num_sms;
   if (blocks < 1) blocks = 1;
-  argmax_kernel<<<int(blocks), 1024, 0, st>>>(v, n, key, counter, out, tok_state, pos_state);
-  return cuda_check(c, cudaGetLastError(), "argmax launch");
+  return cuda_check(c, launch_k(c, argmax_kernel, dim3(int(blocks)), dim3(1024), 0, st, v, n, key, counter, out,
+                                tok_state, pos_state),
+                    "argmax launch");
 }
 
 nt_status launch_cos(Ctx* c, const float* a, const float* b, int64_t n, float* out, cudaStream_t st) {

@@ -25,6 +25,7 @@ nt_status launch_swiglu(Ctx* c, const float* g, const float* u, float* h, int64_
 nt_status launch_argmax(Ctx* c, const float* v, int64_t n, int32_t* out, unsigned long long* key, unsigned* counter,
                         cudaStream_t st, int32_t* tok_state = nullptr, int64_t* pos_state = nullptr);
 nt_status configure_gemv(Ctx* c);
+nt_status launch_inv_freq(Ctx* c, double* out, int head_dim, float theta, cudaStream_t st);
 nt_status configure_ops(Ctx* c);
 nt_status launch_cos(Ctx* c, const float* a, const float* b, int64_t n, float* out, cudaStream_t st);
 

@@ -23,16 +23,17 @@
 namespace nt {
 namespace {
 
-constexpr int kWarps = 8;   // warps per CTA (one CTA per SM)
-constexpr int kStages = 4;  // TMA stages per warp
+constexpr int kMaxWarps = 32;  // warps per CTA: a launch parameter (one CTA per SM)
 
 struct JobDev {
   const uint8_t* W;
   const uint8_t* W2;  // up-projection rows for the SwiGLU epilogue
   float* y;
   const float* res;
+  __half* cache;      // f16 KV cache for the cache epilogues
   int64_t rows;
   int64_t g0;         // first group index of this job
+  int epi;
 };
 
 struct GemvArgs {
@@ -48,11 +49,13 @@ struct GemvArgs {
   int nseg;           // segments per row
   int segStride;      // bytes between the rows of one stage
   int stb;            // bytes per stage
+  int nst;            // stages per warp
   int merged;         // one bulk copy per stage (whole consecutive rows)
   int tma;            // bulk-copy path (else plain loads)
   int swiglu;
   int64_t total_groups;
   unsigned* err;
+  RopeArgs rope;
 };
 
 // ---------------------------------------------------------------------------
@@ -115,15 +118,23 @@ __device__ __forceinline__ float h2f(uint32_t bits16) { return __half2float(__us
 template <int FMT>
 struct Q;
 
+// x lives in shared memory with 4 pad floats after every PADC columns, PADC
+// matched to the lane-to-column mapping of each format, so the float4 reads
+// of the 8 lanes of a quarter-warp land in 8 different bank groups.
+template <int PADC>
+__device__ __forceinline__ int xidx(int col) {
+  return col + 4 * (col / PADC);
+}
+
 // Q8_0: d (f16) | qs[32] int8.  value d*q.  unit = 16 quants, 2 per block.
 template <>
 struct Q<NT_Q8_0> {
-  static constexpr int BE = 32, BB = 34, ALIGN = 8, UPB = 2;
+  static constexpr int BE = 32, BB = 34, ALIGN = 8, UPB = 2, PADC = 16;
   struct X {
     float2 v[8];
   };
   __device__ static void load_x(X& x, const float* xs, const float*, int col0, int uu) {
-    const float* p = xs + col0 + 16 * uu;
+    const float* p = xs + xidx<PADC>(col0 + 16 * uu);
 #pragma unroll
     for (int k = 0; k < 4; ++k) ld_x4(p + 4 * k, x.v[2 * k], x.v[2 * k + 1]);
   }
@@ -149,14 +160,15 @@ struct Q<NT_Q8_0> {
 // value d*(q-8).  unit = one block.
 template <>
 struct Q<NT_Q4_0> {
-  static constexpr int BE = 32, BB = 18, ALIGN = 8, UPB = 1;
+  static constexpr int BE = 32, BB = 18, ALIGN = 8, UPB = 1, PADC = 32;
   struct X {
     float2 v[16];
     float k;  // -136 * sum(x over the block): removes the 0.5 offset and the -8
   };
   __device__ static void load_x(X& x, const float* xs, const float* sx16, int col0, int) {
+    const float* p = xs + xidx<PADC>(col0);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) ld_x4(xs + col0 + 4 * k, x.v[2 * k], x.v[2 * k + 1]);
+    for (int k = 0; k < 8; ++k) ld_x4(p + 4 * k, x.v[2 * k], x.v[2 * k + 1]);
     x.k = -136.0f * (sx16[col0 / 16] + sx16[col0 / 16 + 1]);
   }
   __device__ static float dot(const uint8_t* blk, int, const X& x) {
@@ -201,7 +213,7 @@ struct XK {
   float s0, s1;  // sum(x) over each sub-block
 };
 __device__ __forceinline__ void load_xk(XK& x, const float* xs, const float* sx16, int col0, int c) {
-  const float* p = xs + col0 + 64 * c;
+  const float* p = xs + xidx<64>(col0 + 64 * c);
 #pragma unroll
   for (int k = 0; k < 16; ++k) ld_x4(p + 4 * k, x.v[2 * k], x.v[2 * k + 1]);
   const float* s = sx16 + (col0 + 64 * c) / 16;
@@ -221,7 +233,7 @@ __device__ __forceinline__ float kq_combine(uint4 hdr, int c, float2 a0, float2 
 // Q4_K: d | dmin | scales[12] | qs[128].  value d*sc*q - dmin*m.
 template <>
 struct Q<NT_Q4_K> {
-  static constexpr int BE = 256, BB = 144, ALIGN = 1, UPB = 4;
+  static constexpr int BE = 256, BB = 144, ALIGN = 1, UPB = 4, PADC = 64;
   using X = XK;
   __device__ static void load_x(X& x, const float* xs, const float* sx16, int col0, int c) {
     load_xk(x, xs, sx16, col0, c);
@@ -245,7 +257,7 @@ struct Q<NT_Q4_K> {
 // sub-block j is bit j of qh[l].
 template <>
 struct Q<NT_Q5_K> {
-  static constexpr int BE = 256, BB = 176, ALIGN = 1, UPB = 4;
+  static constexpr int BE = 256, BB = 176, ALIGN = 1, UPB = 4, PADC = 64;
   using X = XK;
   __device__ static void load_x(X& x, const float* xs, const float* sx16, int col0, int c) {
     load_xk(x, xs, sx16, col0, c);
@@ -275,7 +287,7 @@ struct Q<NT_Q5_K> {
 // unit u = (half h = u>>1, s = u&1): elements 128h + 32g + 16s + l', g, l' < 16.
 template <>
 struct Q<NT_Q6_K> {
-  static constexpr int BE = 256, BB = 210, ALIGN = 8, UPB = 4;
+  static constexpr int BE = 256, BB = 210, ALIGN = 8, UPB = 4, PADC = 128;
   struct X {
     float2 v[32];  // v[8g + i]: the 16 columns of group g
     float k[4];    // -160 * sum(x) over group g: removes the 0.5 offset and the -32
@@ -285,8 +297,9 @@ struct Q<NT_Q6_K> {
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const int c = col0 + 128 * h + 32 * g + 16 * s;
+      const float* p = xs + xidx<PADC>(c);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) ld_x4(xs + c + 4 * k, x.v[8 * g + 2 * k], x.v[8 * g + 2 * k + 1]);
+      for (int k = 0; k < 4; ++k) ld_x4(p + 4 * k, x.v[8 * g + 2 * k], x.v[8 * g + 2 * k + 1]);
       x.k[g] = -160.0f * sx16[c / 16];
     }
   }
@@ -335,22 +348,27 @@ __device__ __forceinline__ void locate(const GemvArgs& a, int64_t g, int rpg, in
   nr = left < rpg ? int(left) : rpg;
 }
 
+__host__ __device__ constexpr int xs_bytes(int cols, int padc) {
+  return (((cols + 4 * ((cols + padc - 1) / padc)) * 4 + 15) / 16) * 16;
+}
+
 template <int FMT, int R>
-__global__ void __launch_bounds__(kWarps * 32, 1) qgemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
   using F = Q<FMT>;
   extern __shared__ __align__(128) uint8_t smem[];
+  const int nwarps = blockDim.x >> 5, kStages = a.nst;
   float* xs = reinterpret_cast<float*>(smem);
-  const int xsB = ((a.cols * 4 + 15) / 16) * 16;
+  const int xsB = xs_bytes(a.cols, F::PADC);
   float* sx16 = reinterpret_cast<float*>(smem + xsB);
   const int sxB = ((a.cols / 16 * 4 + 15) / 16) * 16;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + xsB + sxB);
-  uint8_t* stages = smem + ((xsB + sxB + kWarps * kStages * 8 + 127) / 128) * 128;
+  uint8_t* stages = smem + ((xsB + sxB + nwarps * kStages * 8 + 127) / 128) * 128;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   // ---- per-warp pipeline
-  const int64_t total_warps = int64_t(gridDim.x) * kWarps;
-  const int64_t wg = int64_t(blockIdx.x) * kWarps + warp;
+  const int64_t total_warps = int64_t(gridDim.x) * nwarps;
+  const int64_t wg = int64_t(blockIdx.x) * nwarps + warp;
   const int64_t my_groups = wg < a.total_groups ? (a.total_groups - wg + total_warps - 1) / total_warps : 0;
   const int64_t n_items = my_groups * a.nseg;
   uint8_t* st0 = stages + size_t(warp) * kStages * a.stb;
@@ -359,7 +377,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1) qgemv_kernel(const GemvArgs a)
 
   if (a.tma) {
     if (lane == 0) {
-#pragma unroll
       for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
       fence_barrier_init();
     }
@@ -426,19 +443,22 @@ __global__ void __launch_bounds__(kWarps * 32, 1) qgemv_kernel(const GemvArgs a)
     __syncwarp();
   };
 
-  // weights do not depend on x: start streaming them before the x prologue
+  // weights do not depend on x: start streaming them before waiting for the
+  // kernel that produces x
   if (a.tma) {
     const int64_t pre = n_items < kStages - 1 ? n_items : kStages - 1;
     for (int64_t k = 0; k < pre; ++k) issue(k);
   }
+  pdl_trigger();
+  pdl_wait();
 
-  // ---- prologue: x (optionally RMS-normalised) and 16-column partial sums
+  // ---- prologue: x (optionally RMS-normalised, padded layout) and 16-column partial sums
   {
-    __shared__ float red[kWarps];
+    __shared__ float red[kMaxWarps];
     float ss = 0.f;
     for (int i = tid * 4; i < a.cols; i += blockDim.x * 4) {
       const float4 v = *reinterpret_cast<const float4*>(a.x + i);
-      *reinterpret_cast<float4*>(xs + i) = v;
+      *reinterpret_cast<float4*>(xs + xidx<F::PADC>(i)) = v;
       ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
     }
     if (a.norm_g) {
@@ -446,24 +466,25 @@ __global__ void __launch_bounds__(kWarps * 32, 1) qgemv_kernel(const GemvArgs a)
       if (lane == 0) red[warp] = ss;
       __syncthreads();
       float tot = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) tot += red[w];
+      for (int w = 0; w < nwarps; ++w) tot += red[w];
       const float inv = rsqrtf(tot / float(a.cols) + a.eps);
       for (int i = tid * 4; i < a.cols; i += blockDim.x * 4) {
-        float4 v = *reinterpret_cast<float4*>(xs + i);
+        float4* px = reinterpret_cast<float4*>(xs + xidx<F::PADC>(i));
+        float4 v = *px;
         const float4 g = *reinterpret_cast<const float4*>(a.norm_g + i);
         v.x = v.x * inv * g.x;
         v.y = v.y * inv * g.y;
         v.z = v.z * inv * g.z;
         v.w = v.w * inv * g.w;
-        *reinterpret_cast<float4*>(xs + i) = v;
+        *px = v;
       }
     }
     __syncthreads();
     for (int i = tid; i < a.cols / 16; i += blockDim.x) {
+      const float* p = xs + xidx<F::PADC>(16 * i);
       float s = 0.f;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) s += xs[16 * i + k];
+      for (int k = 0; k < 16; ++k) s += p[k];
       sx16[i] = s;
     }
     __syncthreads();
@@ -517,13 +538,29 @@ __global__ void __launch_bounds__(kWarps * 32, 1) qgemv_kernel(const GemvArgs a)
       int j, nr;
       int64_t r0;
       locate(a, gi, rpg, j, r0, nr);
-      if (lane < nr) {
-        const int64_t r = r0 + lane;
-        if (a.swiglu) {
-          a.job[j].y[r] = silu(mine) * other;
-        } else {
-          const float* res = a.job[j].res;
-          a.job[j].y[r] = res ? mine + res[r] : mine;
+      const JobDev& J = a.job[j];
+      if (a.swiglu) {
+        if (lane < nr) J.y[r0 + lane] = silu(mine) * other;
+      } else if (J.epi == kEpiPlain) {
+        if (lane < nr) J.y[r0 + lane] = J.res ? mine + J.res[r0 + lane] : mine;
+      } else {
+        // rows come in adjacent (even, odd) pairs: lane i^1 holds the partner
+        const float partner = __shfl_xor_sync(0xffffffffu, mine, 1);
+        if (lane < nr) {
+          const int64_t r = r0 + lane;
+          const int hd = a.rope.head_dim;
+          const int64_t pos = *a.rope.pos_dev;
+          const int head = int(r / hd), d = int(r % hd);
+          float out = mine;
+          if (J.epi != kEpiCache) {
+            float cs, sn;
+            rope_cs(pos, a.rope.inv_freq[d >> 1], cs, sn);
+            out = (d & 1) ? fmaf(partner, sn, mine * cs) : fmaf(mine, cs, -partner * sn);
+          }
+          if (J.epi == kEpiRope)
+            J.y[r] = out;
+          else
+            J.cache[(int64_t(head) * a.rope.kv_stride + pos) * hd + d] = __float2half_rn(out);
         }
       }
     }
@@ -534,9 +571,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) qgemv_kernel(const GemvArgs a)
 // host side
 
 template <int FMT, int R>
-cudaError_t launch_t(const GemvArgs& a, int grid, size_t smem, cudaStream_t st) {
-  qgemv_kernel<FMT, R><<<grid, kWarps * 32, smem, st>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_t(const Ctx* c, const GemvArgs& a, int grid, size_t smem, cudaStream_t st) {
+  return launch_k(c, qgemv_kernel<FMT, R>, dim3(grid), dim3(c->gemv_warps * 32), smem, st, a);
 }
 
 // dynamic shared memory a kernel may use: the opt-in limit minus its static part
@@ -556,8 +592,8 @@ cudaError_t configure_fmt(int smem) {
 }
 
 template <int FMT>
-cudaError_t dispatch_r(int R, const GemvArgs& a, int grid, size_t smem, cudaStream_t st) {
-  return R == 4 ? launch_t<FMT, 4>(a, grid, smem, st) : launch_t<FMT, 2>(a, grid, smem, st);
+cudaError_t dispatch_r(const Ctx* c, int R, const GemvArgs& a, int grid, size_t smem, cudaStream_t st) {
+  return R == 4 ? launch_t<FMT, 4>(c, a, grid, smem, st) : launch_t<FMT, 2>(c, a, grid, smem, st);
 }
 
 constexpr int align_of(int fmt) { return (fmt == NT_Q4_K || fmt == NT_Q5_K) ? 1 : 8; }
@@ -578,20 +614,30 @@ nt_status configure_gemv(Ctx* c) {
 
 nt_status launch_gemv(Ctx* c, int fmt, const nt_gemv_job* jobs, int njobs, const void* W2, const float* x,
                       const float* norm_g, float eps, int64_t cols, bool swiglu, cudaStream_t st) {
+  GemvJobEx ex[3];
+  for (int j = 0; j < njobs && j < 3; ++j) ex[j] = GemvJobEx{jobs[j], kEpiPlain, nullptr};
+  return launch_gemv_ex(c, fmt, ex, njobs, W2, x, norm_g, eps, cols, swiglu, nullptr, st);
+}
+
+nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, const void* W2, const float* x,
+                         const float* norm_g, float eps, int64_t cols, bool swiglu, const RopeArgs* rope,
+                         cudaStream_t st) {
   const int BE = block_elems(fmt), BB = block_bytes(fmt);
   const int64_t nb = cols / BE;
   const int64_t rowB = nb * BB;
   bool tma = (rowB % 16) == 0;
-  for (int j = 0; j < njobs; ++j) tma = tma && aligned(jobs[j].W_dev, 16);
+  for (int j = 0; j < njobs; ++j) tma = tma && aligned(jobsx[j].j.W_dev, 16);
   if (swiglu) tma = tma && aligned(W2, 16);
 
-  const int xsB = int(((cols * 4 + 15) / 16) * 16);
+  static const int padc_of[5] = {16, 32, 64, 64, 128};
+  const int kWarps = c->gemv_warps, kStages = c->gemv_stages;
+  const int xsB = xs_bytes(int(cols), padc_of[fmt]);
   const int sxB = int(((cols / 16 * 4 + 15) / 16) * 16);
   const int head = ((xsB + sxB + kWarps * kStages * 8 + 127) / 128) * 128;
   const int pad = 16;  // the unaligned 16-byte reader may touch 4 bytes past a stage
   const long avail = long(c->smem_optin) - head - pad - 256;  // 256: static shared memory
   int stb = int(avail / (kWarps * kStages)) / 16 * 16;
-  if (stb > 12288) stb = 12288;
+  if (stb > c->gemv_stage_max) stb = c->gemv_stage_max;
 
   GemvArgs a{};
   int R = 0;
@@ -622,14 +668,18 @@ nt_status launch_gemv(Ctx* c, int fmt, const nt_gemv_job* jobs, int njobs, const
   const int rpg = swiglu ? R / 2 : R;
   int64_t g = 0;
   for (int j = 0; j < njobs; ++j) {
-    a.job[j].W = static_cast<const uint8_t*>(jobs[j].W_dev);
+    const nt_gemv_job& jb = jobsx[j].j;
+    a.job[j].W = static_cast<const uint8_t*>(jb.W_dev);
     a.job[j].W2 = static_cast<const uint8_t*>(W2);
-    a.job[j].y = jobs[j].y_dev;
-    a.job[j].res = jobs[j].residual_dev;
-    a.job[j].rows = jobs[j].rows;
+    a.job[j].y = jb.y_dev;
+    a.job[j].res = jb.residual_dev;
+    a.job[j].rows = jb.rows;
     a.job[j].g0 = g;
-    g += (jobs[j].rows + rpg - 1) / rpg;
+    a.job[j].epi = jobsx[j].epi;
+    a.job[j].cache = static_cast<__half*>(jobsx[j].cache);
+    g += (jb.rows + rpg - 1) / rpg;
   }
+  if (rope) a.rope = *rope;
   if (g == 0) return NT_OK;
   a.njobs = njobs;
   a.x = x;
@@ -639,6 +689,7 @@ nt_status launch_gemv(Ctx* c, int fmt, const nt_gemv_job* jobs, int njobs, const
   a.nb = int(nb);
   a.rowB = rowB;
   a.stb = stb;
+  a.nst = kStages;
   a.tma = tma;
   a.swiglu = swiglu;
   a.total_groups = g;
@@ -653,11 +704,11 @@ nt_status launch_gemv(Ctx* c, int fmt, const nt_gemv_job* jobs, int njobs, const
 
   cudaError_t e;
   switch (fmt) {
-    case NT_Q8_0: e = dispatch_r<NT_Q8_0>(R, a, grid, smem, st); break;
-    case NT_Q4_0: e = dispatch_r<NT_Q4_0>(R, a, grid, smem, st); break;
-    case NT_Q4_K: e = dispatch_r<NT_Q4_K>(R, a, grid, smem, st); break;
-    case NT_Q5_K: e = dispatch_r<NT_Q5_K>(R, a, grid, smem, st); break;
-    default: e = dispatch_r<NT_Q6_K>(R, a, grid, smem, st); break;
+    case NT_Q8_0: e = dispatch_r<NT_Q8_0>(c, R, a, grid, smem, st); break;
+    case NT_Q4_0: e = dispatch_r<NT_Q4_0>(c, R, a, grid, smem, st); break;
+    case NT_Q4_K: e = dispatch_r<NT_Q4_K>(c, R, a, grid, smem, st); break;
+    case NT_Q5_K: e = dispatch_r<NT_Q5_K>(c, R, a, grid, smem, st); break;
+    default: e = dispatch_r<NT_Q6_K>(c, R, a, grid, smem, st); break;
   }
   return cuda_check(c, e, "qgemv launch");
 }
@@ -736,6 +787,8 @@ __global__ void dequant_kernel(int fmt, const uint8_t* W, int64_t row0, int64_t 
 
 // row *token_dev of an embedding table, dequantised (token read on the device)
 __global__ void embed_kernel(int fmt, const uint8_t* W, int64_t cols, const int32_t* token_dev, float* out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t row = *token_dev;
   const int BE = block_elems(fmt), BB = block_bytes(fmt);
   const int64_t nb = cols / BE;
@@ -772,8 +825,9 @@ __global__ void embed_kernel(int fmt, const uint8_t* W, int64_t cols, const int3
 nt_status launch_embed(Ctx* c, int fmt, const void* W, int64_t cols, const int32_t* token_dev, float* out,
                        cudaStream_t st) {
   const int blocks = int((cols + 255) / 256);
-  embed_kernel<<<blocks, 256, 0, st>>>(fmt, static_cast<const uint8_t*>(W), cols, token_dev, out);
-  return cuda_check(c, cudaGetLastError(), "embed launch");
+  return cuda_check(c, launch_k(c, embed_kernel, dim3(blocks), dim3(256), 0, st, fmt, static_cast<const uint8_t*>(W),
+                                cols, token_dev, out),
+                    "embed launch");
 }
 
 nt_status launch_dequant(Ctx* c, int fmt, const void* W, int64_t row0, int64_t nrows, int64_t cols, float* out,
