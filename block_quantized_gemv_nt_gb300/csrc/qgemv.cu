@@ -1,29 +1,30 @@
 // qgemv.cu — dequantize-fused GEMV for the GGUF block formats named on
 // "Ntransformer" (en.unwiki.net), About (Q8_0, Q4_0, Q4_K_M = Q4_K + Q6_K,
 // Q5_K, Q6_K); the GEMV kernel of "Architecture et structure du code"
-// (fr.news.hada.io).  y[r] = sum_c deq(W[r,c]) x[c], fp32 accumulate.
+// (fr.news.hada.io).  y[r] = sum_c deq(W[r,c]) x[c].
 //
-// GB300 design (HBM-bound, M = 1):
-//  * x (optionally RMS-normalised in the prologue) lives in shared memory as
-//    fp32, with a table of 16-column partial sums used by the offset terms.
-//  * Every warp owns a private ring of NST shared-memory stages fed by TMA
-//    bulk copies (cp.async.bulk + mbarrier complete_tx, L2 evict-first) and
-//    works on groups of R consecutive rows, so each x value read from shared
-//    memory serves R rows.  Long rows are cut into column segments.
-//  * Quants become floats without the int->float converter: a byte or nibble
-//    is placed into the mantissa of a constant with PRMT, giving exactly
-//    2^23 + b (8-bit, then one subtract) or 0.5 + q/256 (4..6-bit; the 0.5
-//    offset is removed once per sub-block through the partial sums of x).
-//    Products use packed fp32x2 FMAs.
-//  * K-quant sub-block scale and min are applied once per 32 (16 for Q6_K)
-//    elements: sum (d sc q - dmin m) x = d sc sum(q x) - dmin m sum(x).
+// GB300 design (HBM-bound, M = 1, one CTA per SM):
+//  * Weights stream through a private ring of shared-memory stages per warp,
+//    filled by TMA bulk copies (cp.async.bulk + mbarrier complete_tx, L2
+//    evict-first).  A warp works on groups of R consecutive rows, so each x
+//    value it loads serves R rows; long rows are cut into column segments
+//    whose unit count is a multiple of 32 so every lane has work.
+//  * x (RMS-normalised in the prologue when asked) is held in shared memory
+//    as int16 fixed point with one power-of-two scale per 32 columns:
+//    x ~= x16 * 2^-s, |x - x16 2^-s| <= 2^-15 max|x over the 32 columns|.
+//    Quant x x16 products are then exact integer MACs: dp2a multiplies two
+//    int16 by two (u)int8 and accumulates in int32 — no per-weight
+//    int-to-float conversion.  Sub-block scales, mins and the group scale
+//    are applied once per 16 or 32 elements in fp32.
+//  * The x16 layout is padded by 16 bytes per unit width of each format so
+//    the 16-byte reads of a quarter-warp hit 8 distinct bank groups.
 #include "nt_internal.cuh"
 #include "ops.cuh"
 
 namespace nt {
 namespace {
 
-constexpr int kMaxWarps = 32;  // warps per CTA: a launch parameter (one CTA per SM)
+constexpr int kMaxWarps = 32;
 
 struct JobDev {
   const uint8_t* W;
@@ -59,100 +60,93 @@ struct GemvArgs {
 };
 
 // ---------------------------------------------------------------------------
-// small device helpers
+// device helpers
 
-// 16 bytes from a 2-byte-aligned shared address, as 4 little-endian words.
-__device__ __forceinline__ void lds16_a2(const uint8_t* p, uint32_t w[4]) {
+// d = c + a.lo16 * b.byte0 + a.hi16 * b.byte1  (signed 16-bit a, unsigned bytes b)
+__device__ __forceinline__ int dp2lo_u(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+// ... bytes 2 and 3 of b
+__device__ __forceinline__ int dp2hi_u(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+// signed bytes
+__device__ __forceinline__ int dp2lo_s(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2hi_s(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// N little-endian words from a 2-byte-aligned shared address
+template <int N>
+__device__ __forceinline__ void lds_a2(const uint8_t* p, uint32_t* w) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p);
   const uint32_t* b = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
   const uint32_t sh = uint32_t(a & 3) * 8;
-  const uint32_t t0 = b[0], t1 = b[1], t2 = b[2], t3 = b[3], t4 = b[4];
-  w[0] = __funnelshift_r(t0, t1, sh);
-  w[1] = __funnelshift_r(t1, t2, sh);
-  w[2] = __funnelshift_r(t2, t3, sh);
-  w[3] = __funnelshift_r(t3, t4, sh);
-}
-
-// 8 bytes from a 2-byte-aligned shared address.
-__device__ __forceinline__ void lds8_a2(const uint8_t* p, uint32_t w[2]) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  const uint32_t* b = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-  const uint32_t sh = uint32_t(a & 3) * 8;
-  const uint32_t t0 = b[0], t1 = b[1], t2 = b[2];
-  w[0] = __funnelshift_r(t0, t1, sh);
-  w[1] = __funnelshift_r(t1, t2, sh);
-}
-
-// byte k of v as the float 2^23 + byte (exact)
-template <int K>
-__device__ __forceinline__ float big(uint32_t v) {
-  return __int_as_float(__byte_perm(v, 0x4B000000u, 0x7650 | K));
-}
-// byte k of v (< 128) as the float 0.5 + byte/256 (exact)
-template <int K>
-__device__ __forceinline__ float half_q(uint32_t v) {
-  return __int_as_float(__byte_perm(v, 0x3F000000u, 0x7054 | (K << 8)));
-}
-
-__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
-
-// acc += (0.5 + q_k/256) * x_k for the four bytes of v against x pair p0, p1
-__device__ __forceinline__ float2 fma4(uint32_t v, float2 p0, float2 p1, float2 acc) {
-  acc = __ffma2_rn(f2(half_q<0>(v), half_q<1>(v)), p0, acc);
-  acc = __ffma2_rn(f2(half_q<2>(v), half_q<3>(v)), p1, acc);
-  return acc;
-}
-
-__device__ __forceinline__ void ld_x4(const float* p, float2& a, float2& b) {
-  const float4 t = *reinterpret_cast<const float4*>(p);
-  a = f2(t.x, t.y);
-  b = f2(t.z, t.w);
+  uint32_t t[N + 1];
+#pragma unroll
+  for (int i = 0; i <= N; ++i) t[i] = b[i];
+#pragma unroll
+  for (int i = 0; i < N; ++i) w[i] = __funnelshift_r(t[i], t[i + 1], sh);
 }
 
 __device__ __forceinline__ float h2f(uint32_t bits16) { return __half2float(__ushort_as_half((unsigned short)bits16)); }
 
+__device__ __forceinline__ void ld4(const int16_t* p, uint32_t* w) {
+  const uint4 t = *reinterpret_cast<const uint4*>(p);
+  w[0] = t.x;
+  w[1] = t.y;
+  w[2] = t.z;
+  w[3] = t.w;
+}
+
 // ---------------------------------------------------------------------------
-// per-format traits.  A "unit" is one lane's share of one block; X holds the
-// unit's x values (and offset terms), loaded once and reused for R rows.
+// Shared x: x16[phys(col)], scale[col/32] = 2^-s, sum16[col/16] = sum of x16
+// over 16 columns.  phys(col) = col + 8 * pads(col) (8 int16 = 16 bytes).
+struct XS {
+  const int16_t* x16;
+  const float* scale;
+  const int* sum16;
+};
 
 template <int FMT>
 struct Q;
 
-// x lives in shared memory with 4 pad floats after every PADC columns, PADC
-// matched to the lane-to-column mapping of each format, so the float4 reads
-// of the 8 lanes of a quarter-warp land in 8 different bank groups.
-template <int PADC>
-__device__ __forceinline__ int xidx(int col) {
-  return col + 4 * (col / PADC);
-}
-
-// Q8_0: d (f16) | qs[32] int8.  value d*q.  unit = 16 quants, 2 per block.
+// Q8_0: d (f16) | qs[32] int8.  value d*q.  unit = one block.
 template <>
 struct Q<NT_Q8_0> {
-  static constexpr int BE = 32, BB = 34, ALIGN = 8, UPB = 2, PADC = 16;
+  static constexpr int BE = 32, BB = 34, ALIGN = 32, UPB = 1;
+  __host__ __device__ static constexpr int pads(int col) { return col / 32; }
   struct X {
-    float2 v[8];
+    uint32_t v[16];
+    float s;
   };
-  __device__ static void load_x(X& x, const float* xs, const float*, int col0, int uu) {
-    const float* p = xs + xidx<PADC>(col0 + 16 * uu);
+  __device__ static void load_x(X& x, const XS& xs, int col0, int) {
+    const int16_t* p = xs.x16 + col0 + 8 * pads(col0);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) ld_x4(p + 4 * k, x.v[2 * k], x.v[2 * k + 1]);
+    for (int k = 0; k < 4; ++k) ld4(p + 8 * k, x.v + 4 * k);
+    x.s = xs.scale[col0 / 32];
   }
-  __device__ static float dot(const uint8_t* blk, int uu, const X& x) {
-    uint32_t w[4];
-    lds16_a2(blk + 2 + 16 * uu, w);
-    const float d = __half2float(*reinterpret_cast<const __half*>(blk));
-    const float2 c = f2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
-    float2 a = f2(0.f, 0.f);
+  __device__ static float dot(const uint8_t* blk, int, const X& x) {
+    uint32_t w[8];
+    lds_a2<8>(blk + 2, w);
+    int acc = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t v = w[i] ^ 0x80808080u;  // q + 128 as an unsigned byte
-      const float2 q01 = __fadd2_rn(f2(big<0>(v), big<1>(v)), c);
-      const float2 q23 = __fadd2_rn(f2(big<2>(v), big<3>(v)), c);
-      a = __ffma2_rn(q01, x.v[2 * i], a);
-      a = __ffma2_rn(q23, x.v[2 * i + 1], a);
+    for (int i = 0; i < 8; ++i) {
+      acc = dp2lo_s(x.v[2 * i], w[i], acc);
+      acc = dp2hi_s(x.v[2 * i + 1], w[i], acc);
     }
-    return d * (a.x + a.y);
+    const float d = __half2float(*reinterpret_cast<const __half*>(blk));
+    return float(acc) * (d * x.s);
   }
 };
 
@@ -160,30 +154,34 @@ struct Q<NT_Q8_0> {
 // value d*(q-8).  unit = one block.
 template <>
 struct Q<NT_Q4_0> {
-  static constexpr int BE = 32, BB = 18, ALIGN = 8, UPB = 1, PADC = 32;
+  static constexpr int BE = 32, BB = 18, ALIGN = 32, UPB = 1;
+  __host__ __device__ static constexpr int pads(int col) { return col / 32; }
   struct X {
-    float2 v[16];
-    float k;  // -136 * sum(x over the block): removes the 0.5 offset and the -8
+    uint32_t v[16];
+    float s;
+    int off;  // -8 * sum(x16 over the block)
   };
-  __device__ static void load_x(X& x, const float* xs, const float* sx16, int col0, int) {
-    const float* p = xs + xidx<PADC>(col0);
+  __device__ static void load_x(X& x, const XS& xs, int col0, int) {
+    const int16_t* p = xs.x16 + col0 + 8 * pads(col0);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) ld_x4(p + 4 * k, x.v[2 * k], x.v[2 * k + 1]);
-    x.k = -136.0f * (sx16[col0 / 16] + sx16[col0 / 16 + 1]);
+    for (int k = 0; k < 4; ++k) ld4(p + 8 * k, x.v + 4 * k);
+    x.s = xs.scale[col0 / 32];
+    x.off = -8 * (xs.sum16[col0 / 16] + xs.sum16[col0 / 16 + 1]);
   }
   __device__ static float dot(const uint8_t* blk, int, const X& x) {
     uint32_t w[4];
-    lds16_a2(blk + 2, w);
-    const float d = __half2float(*reinterpret_cast<const __half*>(blk));
-    float2 a = f2(0.f, 0.f), b = f2(0.f, 0.f);
+    lds_a2<4>(blk + 2, w);
+    int acc = x.off;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
-      a = fma4(lo, x.v[2 * i], x.v[2 * i + 1], a);
-      b = fma4(hi, x.v[8 + 2 * i], x.v[8 + 2 * i + 1], b);
+      acc = dp2lo_u(x.v[2 * i], lo, acc);
+      acc = dp2hi_u(x.v[2 * i + 1], lo, acc);
+      acc = dp2lo_u(x.v[8 + 2 * i], hi, acc);
+      acc = dp2hi_u(x.v[8 + 2 * i + 1], hi, acc);
     }
-    // sum (q-8) x = 256 * sum((0.5 + q/256) x) - 136 * sum(x)
-    return d * fmaf(256.0f, (a.x + a.y) + (b.x + b.y), x.k);
+    const float d = __half2float(*reinterpret_cast<const __half*>(blk));
+    return float(acc) * (d * x.s);
   }
 };
 
@@ -207,61 +205,66 @@ __device__ __forceinline__ void kq_scales(uint32_t h1, uint32_t h2, uint32_t h3,
   m1 = float((mp >> 8) & 0xFFu);
 }
 
-// Shared X of the 4/5-bit K formats: unit c = 64 columns (sub-blocks 2c, 2c+1).
+// X of the 4/5-bit K formats: unit c = 64 columns = sub-blocks 2c, 2c+1.
 struct XK {
-  float2 v[32];
-  float s0, s1;  // sum(x) over each sub-block
+  uint32_t v[32];
+  float s0, s1;  // group scales of the two sub-blocks
+  float t0, t1;  // sum(x) of each sub-block (= sum16 * scale)
 };
-__device__ __forceinline__ void load_xk(XK& x, const float* xs, const float* sx16, int col0, int c) {
-  const float* p = xs + xidx<64>(col0 + 64 * c);
+__host__ __device__ constexpr int kq_pads(int col) { return col / 64; }
+__device__ __forceinline__ void load_xk(XK& x, const XS& xs, int col0, int c) {
+  const int col = col0 + 64 * c;
+  const int16_t* p = xs.x16 + col + 8 * kq_pads(col);
 #pragma unroll
-  for (int k = 0; k < 16; ++k) ld_x4(p + 4 * k, x.v[2 * k], x.v[2 * k + 1]);
-  const float* s = sx16 + (col0 + 64 * c) / 16;
-  x.s0 = s[0] + s[1];
-  x.s1 = s[2] + s[3];
+  for (int k = 0; k < 8; ++k) ld4(p + 8 * k, x.v + 4 * k);
+  x.s0 = xs.scale[col / 32];
+  x.s1 = xs.scale[col / 32 + 1];
+  const int* s = xs.sum16 + col / 16;
+  x.t0 = float(s[0] + s[1]) * x.s0;
+  x.t1 = float(s[2] + s[3]) * x.s1;
 }
 
-__device__ __forceinline__ float kq_combine(uint4 hdr, int c, float2 a0, float2 a1, const XK& x) {
+__device__ __forceinline__ float kq_combine(uint4 hdr, int c, int acc0, int acc1, const XK& x) {
   float sc0, sc1, m0, m1;
   kq_scales(hdr.y, hdr.z, hdr.w, c, sc0, sc1, m0, m1);
   const float d = h2f(hdr.x & 0xFFFFu), dmin = h2f(hdr.x >> 16);
-  const float t0 = fmaf(256.0f, a0.x + a0.y, -128.0f * x.s0);  // sum q x, sub-block 2c
-  const float t1 = fmaf(256.0f, a1.x + a1.y, -128.0f * x.s1);  // sum q x, sub-block 2c+1
-  return d * fmaf(sc0, t0, sc1 * t1) - dmin * fmaf(m0, x.s0, m1 * x.s1);
+  // sum_j (d sc_j q - dmin m_j) x = d (sc0 s0 acc0 + sc1 s1 acc1) - dmin (m0 t0 + m1 t1)
+  return d * fmaf(sc0 * x.s0, float(acc0), sc1 * x.s1 * float(acc1)) - dmin * fmaf(m0, x.t0, m1 * x.t1);
 }
 
 // Q4_K: d | dmin | scales[12] | qs[128].  value d*sc*q - dmin*m.
 template <>
 struct Q<NT_Q4_K> {
-  static constexpr int BE = 256, BB = 144, ALIGN = 1, UPB = 4, PADC = 64;
+  static constexpr int BE = 256, BB = 144, ALIGN = 8, UPB = 4;
+  __host__ __device__ static constexpr int pads(int col) { return kq_pads(col); }
   using X = XK;
-  __device__ static void load_x(X& x, const float* xs, const float* sx16, int col0, int c) {
-    load_xk(x, xs, sx16, col0, c);
-  }
+  __device__ static void load_x(X& x, const XS& xs, int col0, int c) { load_xk(x, xs, col0, c); }
   __device__ static float dot(const uint8_t* blk, int c, const X& x) {
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const uint4* qp = reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
     const uint4 q0 = qp[0], q1 = qp[1];
     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    float2 a0 = f2(0.f, 0.f), a1 = f2(0.f, 0.f);
+    int a0 = 0, a1 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      a0 = fma4(w[i] & 0x0F0F0F0Fu, x.v[2 * i], x.v[2 * i + 1], a0);
-      a1 = fma4((w[i] >> 4) & 0x0F0F0F0Fu, x.v[16 + 2 * i], x.v[16 + 2 * i + 1], a1);
+      const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
+      a0 = dp2lo_u(x.v[2 * i], lo, a0);
+      a0 = dp2hi_u(x.v[2 * i + 1], lo, a0);
+      a1 = dp2lo_u(x.v[16 + 2 * i], hi, a1);
+      a1 = dp2hi_u(x.v[16 + 2 * i + 1], hi, a1);
     }
     return kq_combine(hdr, c, a0, a1, x);
   }
 };
 
-// Q5_K: d | dmin | scales[12] | qh[32] | qs[128]; fifth bit of element l of
-// sub-block j is bit j of qh[l].
+// Q5_K: d | dmin | scales[12] | qh[32] | qs[128]; the fifth bit of element l
+// of sub-block j is bit j of qh[l].
 template <>
 struct Q<NT_Q5_K> {
-  static constexpr int BE = 256, BB = 176, ALIGN = 1, UPB = 4, PADC = 64;
+  static constexpr int BE = 256, BB = 176, ALIGN = 8, UPB = 4;
+  __host__ __device__ static constexpr int pads(int col) { return kq_pads(col); }
   using X = XK;
-  __device__ static void load_x(X& x, const float* xs, const float* sx16, int col0, int c) {
-    load_xk(x, xs, sx16, col0, c);
-  }
+  __device__ static void load_x(X& x, const XS& xs, int col0, int c) { load_xk(x, xs, col0, c); }
   __device__ static float dot(const uint8_t* blk, int c, const X& x) {
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const uint4* hp = reinterpret_cast<const uint4*>(blk + 16);
@@ -271,72 +274,81 @@ struct Q<NT_Q5_K> {
     const uint4 q0 = qp[0], q1 = qp[1];
     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
     const int b0 = 2 * c;
-    float2 a0 = f2(0.f, 0.f), a1 = f2(0.f, 0.f);
+    int a0 = 0, a1 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t lo = (w[i] & 0x0F0F0F0Fu) | (((hw[i] >> b0) & 0x01010101u) << 4);
       const uint32_t hi = ((w[i] >> 4) & 0x0F0F0F0Fu) | (((hw[i] >> (b0 + 1)) & 0x01010101u) << 4);
-      a0 = fma4(lo, x.v[2 * i], x.v[2 * i + 1], a0);
-      a1 = fma4(hi, x.v[16 + 2 * i], x.v[16 + 2 * i + 1], a1);
+      a0 = dp2lo_u(x.v[2 * i], lo, a0);
+      a0 = dp2hi_u(x.v[2 * i + 1], lo, a0);
+      a1 = dp2lo_u(x.v[16 + 2 * i], hi, a1);
+      a1 = dp2hi_u(x.v[16 + 2 * i + 1], hi, a1);
     }
     return kq_combine(hdr, c, a0, a1, x);
   }
 };
 
 // Q6_K: ql[128] | qh[64] | scales[16] int8 | d.  value d*sc*(q-32).
-// unit u = (half h = u>>1, s = u&1): elements 128h + 32g + 16s + l', g, l' < 16.
+// unit u = (half h = u>>1, s = u&1): groups g = 0..3 of 16 elements at block
+// columns 128h + 32g + 16s + l', l' < 16; group g has scale scales[8h+2g+s].
 template <>
 struct Q<NT_Q6_K> {
-  static constexpr int BE = 256, BB = 210, ALIGN = 8, UPB = 4, PADC = 128;
+  static constexpr int BE = 256, BB = 210, ALIGN = 8, UPB = 4;
+  __host__ __device__ static constexpr int pads(int col) { return 4 * (col / 256) + (col / 128) % 2; }
   struct X {
-    float2 v[32];  // v[8g + i]: the 16 columns of group g
-    float k[4];    // -160 * sum(x) over group g: removes the 0.5 offset and the -32
+    uint32_t v[32];  // v[8g + i]: x16 pairs of group g
+    float s[4];      // group scales
+    int off[4];      // -32 * sum(x16 over group g)
   };
-  __device__ static void load_x(X& x, const float* xs, const float* sx16, int col0, int u) {
+  __device__ static void load_x(X& x, const XS& xs, int col0, int u) {
     const int h = u >> 1, s = u & 1;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      const int c = col0 + 128 * h + 32 * g + 16 * s;
-      const float* p = xs + xidx<PADC>(c);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) ld_x4(p + 4 * k, x.v[8 * g + 2 * k], x.v[8 * g + 2 * k + 1]);
-      x.k[g] = -160.0f * sx16[c / 16];
+      const int col = col0 + 128 * h + 32 * g + 16 * s;
+      const int16_t* p = xs.x16 + col + 8 * pads(col);
+      ld4(p, x.v + 8 * g);
+      ld4(p + 8, x.v + 8 * g + 4);
+      x.s[g] = xs.scale[col / 32];
+      x.off[g] = -32 * xs.sum16[col / 16];
     }
   }
   __device__ static float dot(const uint8_t* blk, int u, const X& x) {
     const int h = u >> 1, s = u & 1;
     uint32_t A[4], B[4], H[4], S[2];
-    lds16_a2(blk + 64 * h + 16 * s, A);       // low nibble: group 0, high: group 2
-    lds16_a2(blk + 64 * h + 32 + 16 * s, B);  // low nibble: group 1, high: group 3
-    lds16_a2(blk + 128 + 32 * h + 16 * s, H); // bits 2g..2g+1: top bits of group g
-    lds8_a2(blk + 192 + 8 * h, S);            // scales[8h .. 8h+7]
-    const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
-    float2 a[4];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) a[g] = f2(0.f, 0.f);
+    lds_a2<4>(blk + 64 * h + 16 * s, A);        // low nibble: group 0, high: group 2
+    lds_a2<4>(blk + 64 * h + 32 + 16 * s, B);   // low nibble: group 1, high: group 3
+    lds_a2<4>(blk + 128 + 32 * h + 16 * s, H);  // bits 2g..2g+1: top bits of group g
+    lds_a2<2>(blk + 192 + 8 * h, S);            // scales[8h .. 8h+7]
+    int a[4] = {x.off[0], x.off[1], x.off[2], x.off[3]};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t q0 = (A[i] & 0x0F0F0F0Fu) | ((H[i] << 4) & 0x30303030u);
       const uint32_t q1 = (B[i] & 0x0F0F0F0Fu) | ((H[i] << 2) & 0x30303030u);
       const uint32_t q2 = ((A[i] >> 4) & 0x0F0F0F0Fu) | (H[i] & 0x30303030u);
       const uint32_t q3 = ((B[i] >> 4) & 0x0F0F0F0Fu) | ((H[i] >> 2) & 0x30303030u);
-      a[0] = fma4(q0, x.v[2 * i], x.v[2 * i + 1], a[0]);
-      a[1] = fma4(q1, x.v[8 + 2 * i], x.v[8 + 2 * i + 1], a[1]);
-      a[2] = fma4(q2, x.v[16 + 2 * i], x.v[16 + 2 * i + 1], a[2]);
-      a[3] = fma4(q3, x.v[24 + 2 * i], x.v[24 + 2 * i + 1], a[3]);
+      a[0] = dp2hi_u(x.v[2 * i + 1], q0, dp2lo_u(x.v[2 * i], q0, a[0]));
+      a[1] = dp2hi_u(x.v[8 + 2 * i + 1], q1, dp2lo_u(x.v[8 + 2 * i], q1, a[1]));
+      a[2] = dp2hi_u(x.v[16 + 2 * i + 1], q2, dp2lo_u(x.v[16 + 2 * i], q2, a[2]));
+      a[3] = dp2hi_u(x.v[24 + 2 * i + 1], q3, dp2lo_u(x.v[24 + 2 * i], q3, a[3]));
     }
     // scale of group g: scales[8h + 2g + s] = byte (2g + s) of the 8-byte window
     const float sc0 = float(int8_t(S[0] >> (8 * s)));
     const float sc1 = float(int8_t(S[0] >> (8 * s + 16)));
     const float sc2 = float(int8_t(S[1] >> (8 * s)));
     const float sc3 = float(int8_t(S[1] >> (8 * s + 16)));
-    float t = sc0 * fmaf(256.0f, a[0].x + a[0].y, x.k[0]);
-    t = fmaf(sc1, fmaf(256.0f, a[1].x + a[1].y, x.k[1]), t);
-    t = fmaf(sc2, fmaf(256.0f, a[2].x + a[2].y, x.k[2]), t);
-    t = fmaf(sc3, fmaf(256.0f, a[3].x + a[3].y, x.k[3]), t);
+    float t = sc0 * x.s[0] * float(a[0]);
+    t = fmaf(sc1 * x.s[1], float(a[1]), t);
+    t = fmaf(sc2 * x.s[2], float(a[2]), t);
+    t = fmaf(sc3 * x.s[3], float(a[3]), t);
+    const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
     return d * t;
   }
 };
+
+template <int FMT>
+__host__ __device__ constexpr int x16_bytes(int cols) {
+  return ((2 * (cols + 8 * Q<FMT>::pads(cols)) + 16 + 15) / 16) * 16;
+}
 
 // ---------------------------------------------------------------------------
 
@@ -348,25 +360,20 @@ __device__ __forceinline__ void locate(const GemvArgs& a, int64_t g, int rpg, in
   nr = left < rpg ? int(left) : rpg;
 }
 
-__host__ __device__ constexpr int xs_bytes(int cols, int padc) {
-  return (((cols + 4 * ((cols + padc - 1) / padc)) * 4 + 15) / 16) * 16;
-}
-
 template <int FMT, int R>
 __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
   using F = Q<FMT>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int nwarps = blockDim.x >> 5, kStages = a.nst;
-  float* xs = reinterpret_cast<float*>(smem);
-  const int xsB = xs_bytes(a.cols, F::PADC);
-  float* sx16 = reinterpret_cast<float*>(smem + xsB);
-  const int sxB = ((a.cols / 16 * 4 + 15) / 16) * 16;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + xsB + sxB);
-  uint8_t* stages = smem + ((xsB + sxB + nwarps * kStages * 8 + 127) / 128) * 128;
+  const int xB = x16_bytes<FMT>(a.cols);
+  const int ng = a.cols / 32;
+  int16_t* x16 = reinterpret_cast<int16_t*>(smem);
+  float* gscale = reinterpret_cast<float*>(smem + xB);
+  int* sum16 = reinterpret_cast<int*>(smem + xB + 4 * ng);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ((xB + 12 * ng + 7) / 8) * 8);
+  uint8_t* stages = smem + ((xB + 12 * ng + 8 + nwarps * kStages * 8 + 127) / 128) * 128;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-  // ---- per-warp pipeline
   const int64_t total_warps = int64_t(gridDim.x) * nwarps;
   const int64_t wg = int64_t(blockIdx.x) * nwarps + warp;
   const int64_t my_groups = wg < a.total_groups ? (a.total_groups - wg + total_warps - 1) / total_warps : 0;
@@ -452,45 +459,66 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
   pdl_trigger();
   pdl_wait();
 
-  // ---- prologue: x (optionally RMS-normalised, padded layout) and 16-column partial sums
+  // ---- prologue: x (optionally RMS-normalised) -> int16 per 32-column group
   {
     __shared__ float red[kMaxWarps];
-    float ss = 0.f;
-    for (int i = tid * 4; i < a.cols; i += blockDim.x * 4) {
-      const float4 v = *reinterpret_cast<const float4*>(a.x + i);
-      *reinterpret_cast<float4*>(xs + xidx<F::PADC>(i)) = v;
-      ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
-    }
+    float inv = 1.f;
     if (a.norm_g) {
+      float ss = 0.f;
+      for (int i = tid * 4; i < a.cols; i += blockDim.x * 4) {
+        const float4 v = *reinterpret_cast<const float4*>(a.x + i);
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+      }
       ss = warp_sum(ss);
       if (lane == 0) red[warp] = ss;
       __syncthreads();
       float tot = 0.f;
       for (int w = 0; w < nwarps; ++w) tot += red[w];
-      const float inv = rsqrtf(tot / float(a.cols) + a.eps);
-      for (int i = tid * 4; i < a.cols; i += blockDim.x * 4) {
-        float4* px = reinterpret_cast<float4*>(xs + xidx<F::PADC>(i));
-        float4 v = *px;
-        const float4 g = *reinterpret_cast<const float4*>(a.norm_g + i);
-        v.x = v.x * inv * g.x;
-        v.y = v.y * inv * g.y;
-        v.z = v.z * inv * g.z;
-        v.w = v.w * inv * g.w;
-        *px = v;
+      inv = rsqrtf(tot / float(a.cols) + a.eps);
+    }
+    // 8 lanes per group of 32 columns, 4 columns per lane
+    for (int base = warp * 4; base < ng; base += nwarps * 4) {
+      const int grp = base + (lane >> 3), sub = lane & 7;
+      const bool live = grp < ng;
+      const int col = 32 * grp + 4 * sub;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (live) {
+        v = *reinterpret_cast<const float4*>(a.x + col);
+        if (a.norm_g) {
+          const float4 g = *reinterpret_cast<const float4*>(a.norm_g + col);
+          v.x = v.x * inv * g.x;
+          v.y = v.y * inv * g.y;
+          v.z = v.z * inv * g.z;
+          v.w = v.w * inv * g.w;
+        }
+      }
+      float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+      int e = 0;
+      if (m > 0.f) frexpf(m, &e);  // m = f * 2^e, f in [0.5, 1)
+      const int sh = 15 - e;       // max |x| * 2^sh < 2^15
+      const int q0 = max(-32767, min(32767, __float2int_rn(ldexpf(v.x, sh))));
+      const int q1 = max(-32767, min(32767, __float2int_rn(ldexpf(v.y, sh))));
+      const int q2 = max(-32767, min(32767, __float2int_rn(ldexpf(v.z, sh))));
+      const int q3 = max(-32767, min(32767, __float2int_rn(ldexpf(v.w, sh))));
+      int s4 = q0 + q1 + q2 + q3;
+      s4 += __shfl_xor_sync(0xffffffffu, s4, 1);
+      s4 += __shfl_xor_sync(0xffffffffu, s4, 2);
+      if (live) {
+        uint2 pk;
+        pk.x = (uint32_t(q0) & 0xFFFFu) | (uint32_t(q1) << 16);
+        pk.y = (uint32_t(q2) & 0xFFFFu) | (uint32_t(q3) << 16);
+        *reinterpret_cast<uint2*>(x16 + col + 8 * F::pads(col)) = pk;
+        if ((sub & 3) == 0) sum16[2 * grp + (sub >> 2)] = s4;
+        if (sub == 0) gscale[grp] = ldexpf(1.0f, -sh);
       }
     }
     __syncthreads();
-    for (int i = tid; i < a.cols / 16; i += blockDim.x) {
-      const float* p = xs + xidx<F::PADC>(16 * i);
-      float s = 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) s += p[k];
-      sx16[i] = s;
-    }
-    __syncthreads();
   }
-
   if (my_groups == 0) return;
+  const XS xs{x16, gscale, sum16};
 
   float acc[R];
 #pragma unroll
@@ -518,14 +546,14 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
     for (int u = lane; u < units; u += 32) {
       const int b = u / F::UPB, uu = u % F::UPB;
       typename F::X x;
-      F::load_x(x, xs, sx16, (blk0 + b) * F::BE, uu);
+      F::load_x(x, xs, (blk0 + b) * F::BE, uu);
       const uint8_t* bp = st + b * F::BB;
 #pragma unroll
       for (int i = 0; i < R; ++i) acc[i] += F::dot(bp + i * a.segStride, uu, x);
     }
     __syncwarp();
     if (s == a.nseg - 1) {
-      // group done: reduce across lanes, lane i writes row i
+      // group done: reduce across lanes, lane i holds row i
       float mine = 0.f, other = 0.f;
 #pragma unroll
       for (int i = 0; i < R; ++i) {
@@ -596,7 +624,20 @@ cudaError_t dispatch_r(const Ctx* c, int R, const GemvArgs& a, int grid, size_t 
   return R == 4 ? launch_t<FMT, 4>(c, a, grid, smem, st) : launch_t<FMT, 2>(c, a, grid, smem, st);
 }
 
-constexpr int align_of(int fmt) { return (fmt == NT_Q4_K || fmt == NT_Q5_K) ? 1 : 8; }
+struct FmtInfo {
+  int align;   // blocks per segment unit: 16-byte aligned and a multiple of 32 lane units
+  int xbytes;  // shared bytes of x16
+};
+
+FmtInfo fmt_info(int fmt, int cols) {
+  switch (fmt) {
+    case NT_Q8_0: return {Q<NT_Q8_0>::ALIGN, x16_bytes<NT_Q8_0>(cols)};
+    case NT_Q4_0: return {Q<NT_Q4_0>::ALIGN, x16_bytes<NT_Q4_0>(cols)};
+    case NT_Q4_K: return {Q<NT_Q4_K>::ALIGN, x16_bytes<NT_Q4_K>(cols)};
+    case NT_Q5_K: return {Q<NT_Q5_K>::ALIGN, x16_bytes<NT_Q5_K>(cols)};
+    default: return {Q<NT_Q6_K>::ALIGN, x16_bytes<NT_Q6_K>(cols)};
+  }
+}
 
 }  // namespace
 
@@ -622,27 +663,27 @@ nt_status launch_gemv(Ctx* c, int fmt, const nt_gemv_job* jobs, int njobs, const
 nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, const void* W2, const float* x,
                          const float* norm_g, float eps, int64_t cols, bool swiglu, const RopeArgs* rope,
                          cudaStream_t st) {
-  const int BE = block_elems(fmt), BB = block_bytes(fmt);
-  const int64_t nb = cols / BE;
+  const int BB = block_bytes(fmt);
+  const int64_t nb = cols / block_elems(fmt);
   const int64_t rowB = nb * BB;
   bool tma = (rowB % 16) == 0;
   for (int j = 0; j < njobs; ++j) tma = tma && aligned(jobsx[j].j.W_dev, 16);
   if (swiglu) tma = tma && aligned(W2, 16);
 
-  static const int padc_of[5] = {16, 32, 64, 64, 128};
+  const FmtInfo fi = fmt_info(fmt, int(cols));
   const int kWarps = c->gemv_warps, kStages = c->gemv_stages;
-  const int xsB = xs_bytes(int(cols), padc_of[fmt]);
-  const int sxB = int(((cols / 16 * 4 + 15) / 16) * 16);
-  const int head = ((xsB + sxB + kWarps * kStages * 8 + 127) / 128) * 128;
-  const int pad = 16;  // the unaligned 16-byte reader may touch 4 bytes past a stage
+  const int ng = int(cols / 32);
+  const int head = ((fi.xbytes + 12 * ng + 8 + kWarps * kStages * 8 + 127) / 128) * 128;
+  const int pad = 16;  // the unaligned readers may touch 4 bytes past a stage
   const long avail = long(c->smem_optin) - head - pad - 256;  // 256: static shared memory
   int stb = int(avail / (kWarps * kStages)) / 16 * 16;
   if (stb > c->gemv_stage_max) stb = c->gemv_stage_max;
 
   GemvArgs a{};
   int R = 0;
-  const int al = align_of(fmt);
+  const int al = fi.align;
   for (int r : {4, 2}) {
+    // whole rows when R of them fit a stage
     if (int64_t(r) * (tma ? rowB : ((rowB + 15) / 16) * 16) <= stb) {
       R = r;
       a.seg = int(nb);
@@ -711,134 +752,6 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
     default: e = dispatch_r<NT_Q6_K>(c, R, a, grid, smem, st); break;
   }
   return cuda_check(c, e, "qgemv launch");
-}
-
-// ---------------------------------------------------------------------------
-// dequantisation of whole rows (embedding lookup; bit-exact parity checks)
-
-namespace {
-
-__device__ __forceinline__ int quant_of(int fmt, const uint8_t* b, int i) {
-  switch (fmt) {
-    case NT_Q8_0: return int(int8_t(b[2 + i]));
-    case NT_Q4_0: return i < 16 ? (b[2 + i] & 15) : (b[2 + i - 16] >> 4);
-    case NT_Q4_K: {
-      const int j = i >> 5, l = i & 31, c = j >> 1;
-      const uint8_t v = b[16 + 32 * c + l];
-      return (j & 1) ? (v >> 4) : (v & 15);
-    }
-    case NT_Q5_K: {
-      const int j = i >> 5, l = i & 31, c = j >> 1;
-      const uint8_t v = b[48 + 32 * c + l];
-      return ((j & 1) ? (v >> 4) : (v & 15)) | (((b[16 + l] >> j) & 1) << 4);
-    }
-    default: {
-      const int h = i >> 7, e = i & 127, g = e >> 5, l = e & 31;
-      const uint8_t* ql = b + 64 * h;
-      const uint8_t lo = (g & 1) ? ql[l + 32] : ql[l];
-      const int q4 = (g >= 2) ? (lo >> 4) : (lo & 15);
-      return q4 | (((b[128 + 32 * h + l] >> (2 * g)) & 3) << 4);
-    }
-  }
-}
-
-__device__ __forceinline__ void kq_sm(const uint8_t* s, int j, int& sc, int& m) {
-  if (j < 4) {
-    sc = s[j] & 63;
-    m = s[j + 4] & 63;
-  } else {
-    sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
-    m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
-  }
-}
-
-__global__ void dequant_kernel(int fmt, const uint8_t* W, int64_t row0, int64_t nrows, int64_t cols, float* out) {
-  const int BE = block_elems(fmt), BB = block_bytes(fmt);
-  const int64_t nb = cols / BE;
-  const int64_t total = nrows * cols;
-  for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = e / cols, col = e % cols;
-    const uint8_t* b = W + ((row0 + r) * nb + col / BE) * BB;
-    const int i = int(col % BE);
-    float v;
-    switch (fmt) {
-      case NT_Q8_0: v = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b)), float(quant_of(fmt, b, i))); break;
-      case NT_Q4_0:
-        v = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b)), float(quant_of(fmt, b, i) - 8));
-        break;
-      case NT_Q4_K:
-      case NT_Q5_K: {
-        int sc, m;
-        kq_sm(b + 4, i >> 5, sc, m);
-        const float d = __half2float(*reinterpret_cast<const __half*>(b));
-        const float dm = __half2float(*reinterpret_cast<const __half*>(b + 2));
-        v = __fsub_rn(__fmul_rn(__fmul_rn(d, float(sc)), float(quant_of(fmt, b, i))), __fmul_rn(dm, float(m)));
-        break;
-      }
-      default: {
-        const int s = int(int8_t(b[192 + (i >> 7) * 8 + ((i & 127) >> 4)]));
-        v = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b + 208)), float(s * (quant_of(fmt, b, i) - 32)));
-        break;
-      }
-    }
-    out[e] = v;
-  }
-}
-
-// row *token_dev of an embedding table, dequantised (token read on the device)
-__global__ void embed_kernel(int fmt, const uint8_t* W, int64_t cols, const int32_t* token_dev, float* out) {
-  pdl_wait();
-  pdl_trigger();
-  const int64_t row = *token_dev;
-  const int BE = block_elems(fmt), BB = block_bytes(fmt);
-  const int64_t nb = cols / BE;
-  for (int64_t col = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; col < cols; col += int64_t(gridDim.x) * blockDim.x) {
-    const uint8_t* b = W + (row * nb + col / BE) * BB;
-    const int i = int(col % BE);
-    float v;
-    switch (fmt) {
-      case NT_Q8_0: v = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b)), float(quant_of(fmt, b, i))); break;
-      case NT_Q4_0:
-        v = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b)), float(quant_of(fmt, b, i) - 8));
-        break;
-      case NT_Q4_K:
-      case NT_Q5_K: {
-        int sc, m;
-        kq_sm(b + 4, i >> 5, sc, m);
-        const float d = __half2float(*reinterpret_cast<const __half*>(b));
-        const float dm = __half2float(*reinterpret_cast<const __half*>(b + 2));
-        v = __fsub_rn(__fmul_rn(__fmul_rn(d, float(sc)), float(quant_of(fmt, b, i))), __fmul_rn(dm, float(m)));
-        break;
-      }
-      default: {
-        const int s = int(int8_t(b[192 + (i >> 7) * 8 + ((i & 127) >> 4)]));
-        v = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b + 208)), float(s * (quant_of(fmt, b, i) - 32)));
-        break;
-      }
-    }
-    out[col] = v;
-  }
-}
-
-}  // namespace
-
-nt_status launch_embed(Ctx* c, int fmt, const void* W, int64_t cols, const int32_t* token_dev, float* out,
-                       cudaStream_t st) {
-  const int blocks = int((cols + 255) / 256);
-  return cuda_check(c, launch_k(c, embed_kernel, dim3(blocks), dim3(256), 0, st, fmt, static_cast<const uint8_t*>(W),
-                                cols, token_dev, out),
-                    "embed launch");
-}
-
-nt_status launch_dequant(Ctx* c, int fmt, const void* W, int64_t row0, int64_t nrows, int64_t cols, float* out,
-                         cudaStream_t st) {
-  const int64_t total = nrows * cols;
-  if (total == 0) return NT_OK;
-  int64_t blocks = (total + 255) / 256;
-  const int64_t cap = int64_t(c->num_sms) * 8;
-  if (blocks > cap) blocks = cap;
-  dequant_kernel<<<int(blocks), 256, 0, st>>>(fmt, static_cast<const uint8_t*>(W), row0, nrows, cols, out);
-  return cuda_check(c, cudaGetLastError(), "dequant launch");
 }
 
 }  // namespace nt
