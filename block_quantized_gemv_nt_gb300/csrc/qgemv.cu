@@ -10,14 +10,15 @@
 //    value it loads serves R rows; long rows are cut into column segments
 //    whose unit count is a multiple of 32 so every lane has work.
 //  * x (RMS-normalised in the prologue when asked) is held in shared memory
-//    as int16 fixed point with one power-of-two scale per 32 columns:
-//    x ~= x16 * 2^-s, |x - x16 2^-s| <= 2^-15 max|x over the 32 columns|.
-//    Quant x x16 products are then exact integer MACs: dp2a multiplies two
-//    int16 by two (u)int8 and accumulates in int32 — no per-weight
-//    int-to-float conversion.  Sub-block scales, mins and the group scale
-//    are applied once per 16 or 32 elements in fp32.
-//  * The x16 layout is padded by 16 bytes per unit width of each format so
-//    the 16-byte reads of a quarter-warp hit 8 distinct bank groups.
+//    as 24-bit fixed point with one power-of-two scale per 32 columns,
+//    split into three byte planes: |x - x24 2^-s| <= 2^-23 max|x over the
+//    32 columns|, the order of fp32 rounding.  Quant x plane products are
+//    exact integer MACs: dp4a multiplies four (u)int8 pairs and accumulates
+//    in int32 — no per-weight int-to-float conversion.  The three plane
+//    sums, sub-block scales, mins and the group scale are applied once per
+//    16 or 32 elements in fp32.
+//  * The plane layout is padded per format so the 16-byte reads of a
+//    quarter-warp hit 8 distinct bank groups.
 #include "nt_internal.cuh"
 #include "ops.cuh"
 
@@ -62,29 +63,18 @@ struct GemvArgs {
 // ---------------------------------------------------------------------------
 // device helpers
 
-// d = c + a.lo16 * b.byte0 + a.hi16 * b.byte1  (signed 16-bit a, unsigned bytes b)
-__device__ __forceinline__ int dp2lo_u(uint32_t a, uint32_t b, int c) {
-  int d;
-  asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-// ... bytes 2 and 3 of b
-__device__ __forceinline__ int dp2hi_u(uint32_t a, uint32_t b, int c) {
-  int d;
-  asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-// signed bytes
-__device__ __forceinline__ int dp2lo_s(uint32_t a, uint32_t b, int c) {
-  int d;
-  asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-__device__ __forceinline__ int dp2hi_s(uint32_t a, uint32_t b, int c) {
-  int d;
-  asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
+// dp4a: d = c + sum_i a.byte_i * b.byte_i.  Suffixes: signedness of a, then b.
+#define NT_DP4A(name, ta, tb)                                                        \
+  __device__ __forceinline__ int name(uint32_t a, uint32_t b, int c) {               \
+    int d;                                                                           \
+    asm("dp4a." ta "." tb " %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));     \
+    return d;                                                                        \
+  }
+NT_DP4A(dp4_su, "s32", "u32")
+NT_DP4A(dp4_uu, "u32", "u32")
+NT_DP4A(dp4_ss, "s32", "s32")
+NT_DP4A(dp4_us, "u32", "s32")
+#undef NT_DP4A
 
 // N little-endian words from a 2-byte-aligned shared address
 template <int N>
@@ -101,7 +91,7 @@ __device__ __forceinline__ void lds_a2(const uint8_t* p, uint32_t* w) {
 
 __device__ __forceinline__ float h2f(uint32_t bits16) { return __half2float(__ushort_as_half((unsigned short)bits16)); }
 
-__device__ __forceinline__ void ld4(const int16_t* p, uint32_t* w) {
+__device__ __forceinline__ void ld4(const uint8_t* p, uint32_t* w) {
   const uint4 t = *reinterpret_cast<const uint4*>(p);
   w[0] = t.x;
   w[1] = t.y;
@@ -110,78 +100,92 @@ __device__ __forceinline__ void ld4(const int16_t* p, uint32_t* w) {
 }
 
 // ---------------------------------------------------------------------------
-// Shared x: x16[phys(col)], scale[col/32] = 2^-s, sum16[col/16] = sum of x16
-// over 16 columns.  phys(col) = col + 8 * pads(col) (8 int16 = 16 bytes).
+// Shared x.  Each 32-column group g holds x as 24-bit fixed point,
+// x24 = rint(x * 2^sh_g), split into three byte planes
+//   x24 = p2 * 2^16 + p1 * 2^8 + p0   (p2 signed, p1 and p0 unsigned)
+// stored as [p0: 32 B][p1: 32 B][p2: 32 B][16 B pad] at goff(g), plus
+// scale[g] = 2^-sh_g and psum[3 * (col/16) + k] = sum of plane k over 16
+// columns (for the constant offsets of Q4_0 and Q6_K).  |x - x24 2^-sh| is
+// at most 2^-23 of the group's largest |x|.
 struct XS {
-  const int16_t* x16;
+  const uint8_t* x;
   const float* scale;
-  const int* sum16;
+  const int* psum;
 };
+
+// sum of the three planes' integer dot products: 65536 a2 + 256 a1 + a0
+__device__ __forceinline__ float planes(int a2, int a1, int a0) {
+  return fmaf(float(a2), 65536.0f, fmaf(float(a1), 256.0f, float(a0)));
+}
 
 template <int FMT>
 struct Q;
 
-// Q8_0: d (f16) | qs[32] int8.  value d*q.  unit = one block.
+// Q8_0: d (f16) | qs[32] int8.  value d*q.  unit = one block (one group).
 template <>
 struct Q<NT_Q8_0> {
-  static constexpr int BE = 32, BB = 34, ALIGN = 32, UPB = 1;
-  __host__ __device__ static constexpr int pads(int col) { return col / 32; }
+  static constexpr int BE = 32, BB = 34, ALIGN = 32, UPB = 1, PB = 0;
   struct X {
-    uint32_t v[16];
+    uint32_t v[3][8];
     float s;
   };
-  __device__ static void load_x(X& x, const XS& xs, int col0, int) {
-    const int16_t* p = xs.x16 + col0 + 8 * pads(col0);
+  __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) ld4(p + 8 * k, x.v + 4 * k);
+    for (int k = 0; k < 3; ++k) {
+      ld4(g + 32 * k, x.v[k]);
+      ld4(g + 32 * k + 16, x.v[k] + 4);
+    }
     x.s = xs.scale[col0 / 32];
   }
   __device__ static float dot(const uint8_t* blk, int, const X& x) {
     uint32_t w[8];
     lds_a2<8>(blk + 2, w);
-    int acc = 0;
+    int a0 = 0, a1 = 0, a2 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      acc = dp2lo_s(x.v[2 * i], w[i], acc);
-      acc = dp2hi_s(x.v[2 * i + 1], w[i], acc);
+      a0 = dp4_us(x.v[0][i], w[i], a0);
+      a1 = dp4_us(x.v[1][i], w[i], a1);
+      a2 = dp4_ss(x.v[2][i], w[i], a2);
     }
     const float d = __half2float(*reinterpret_cast<const __half*>(blk));
-    return float(acc) * (d * x.s);
+    return planes(a2, a1, a0) * (d * x.s);
   }
 };
 
 // Q4_0: d | qs[16]; element i<16 = low nibble of qs[i], i+16 = high nibble.
-// value d*(q-8).  unit = one block.
+// value d*(q-8).  unit = one block (one group).
 template <>
 struct Q<NT_Q4_0> {
-  static constexpr int BE = 32, BB = 18, ALIGN = 32, UPB = 1;
-  __host__ __device__ static constexpr int pads(int col) { return col / 32; }
+  static constexpr int BE = 32, BB = 18, ALIGN = 32, UPB = 1, PB = 0;
   struct X {
-    uint32_t v[16];
+    uint32_t v[3][8];
     float s;
-    int off;  // -8 * sum(x16 over the block)
+    int off[3];  // -8 * sum of each plane over the block
   };
-  __device__ static void load_x(X& x, const XS& xs, int col0, int) {
-    const int16_t* p = xs.x16 + col0 + 8 * pads(col0);
+  __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) ld4(p + 8 * k, x.v + 4 * k);
+    for (int k = 0; k < 3; ++k) {
+      ld4(g + 32 * k, x.v[k]);
+      ld4(g + 32 * k + 16, x.v[k] + 4);
+    }
     x.s = xs.scale[col0 / 32];
-    x.off = -8 * (xs.sum16[col0 / 16] + xs.sum16[col0 / 16 + 1]);
+    const int* ps = xs.psum + 3 * (col0 / 16);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) x.off[k] = -8 * (ps[k] + ps[3 + k]);
   }
   __device__ static float dot(const uint8_t* blk, int, const X& x) {
     uint32_t w[4];
     lds_a2<4>(blk + 2, w);
-    int acc = x.off;
+    int a0 = x.off[0], a1 = x.off[1], a2 = x.off[2];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
-      acc = dp2lo_u(x.v[2 * i], lo, acc);
-      acc = dp2hi_u(x.v[2 * i + 1], lo, acc);
-      acc = dp2lo_u(x.v[8 + 2 * i], hi, acc);
-      acc = dp2hi_u(x.v[8 + 2 * i + 1], hi, acc);
+      a0 = dp4_uu(x.v[0][4 + i], hi, dp4_uu(x.v[0][i], lo, a0));
+      a1 = dp4_uu(x.v[1][4 + i], hi, dp4_uu(x.v[1][i], lo, a1));
+      a2 = dp4_su(x.v[2][4 + i], hi, dp4_su(x.v[2][i], lo, a2));
     }
     const float d = __half2float(*reinterpret_cast<const __half*>(blk));
-    return float(acc) * (d * x.s);
+    return planes(a2, a1, a0) * (d * x.s);
   }
 };
 
@@ -205,55 +209,68 @@ __device__ __forceinline__ void kq_scales(uint32_t h1, uint32_t h2, uint32_t h3,
   m1 = float((mp >> 8) & 0xFFu);
 }
 
-// X of the 4/5-bit K formats: unit c = 64 columns = sub-blocks 2c, 2c+1.
+// X of the 4/5-bit K formats: unit c = 64 columns = sub-blocks 2c, 2c+1 =
+// groups A (low nibbles) and B (high nibbles).
 struct XK {
-  uint32_t v[32];
-  float s0, s1;  // group scales of the two sub-blocks
-  float t0, t1;  // sum(x) of each sub-block (= sum16 * scale)
+  uint32_t a[3][8], b[3][8];
+  float s0, s1;  // group scales
+  float t0, t1;  // sum(x) over each sub-block
 };
-__host__ __device__ constexpr int kq_pads(int col) { return col / 64; }
-__device__ __forceinline__ void load_xk(XK& x, const XS& xs, int col0, int c) {
-  const int col = col0 + 64 * c;
-  const int16_t* p = xs.x16 + col + 8 * kq_pads(col);
+__device__ __forceinline__ void load_xk(XK& x, const uint8_t* g, const uint8_t* g2, const XS& xs, int col0, int c) {
 #pragma unroll
-  for (int k = 0; k < 8; ++k) ld4(p + 8 * k, x.v + 4 * k);
+  for (int k = 0; k < 3; ++k) {
+    ld4(g + 32 * k, x.a[k]);
+    ld4(g + 32 * k + 16, x.a[k] + 4);
+    ld4(g2 + 32 * k, x.b[k]);
+    ld4(g2 + 32 * k + 16, x.b[k] + 4);
+  }
+  const int col = col0 + 64 * c;
   x.s0 = xs.scale[col / 32];
   x.s1 = xs.scale[col / 32 + 1];
-  const int* s = xs.sum16 + col / 16;
-  x.t0 = float(s[0] + s[1]) * x.s0;
-  x.t1 = float(s[2] + s[3]) * x.s1;
+  const int* ps = xs.psum + 3 * (col / 16);
+  x.t0 = planes(ps[2] + ps[5], ps[1] + ps[4], ps[0] + ps[3]) * x.s0;
+  x.t1 = planes(ps[8] + ps[11], ps[7] + ps[10], ps[6] + ps[9]) * x.s1;
 }
 
-__device__ __forceinline__ float kq_combine(uint4 hdr, int c, int acc0, int acc1, const XK& x) {
+__device__ __forceinline__ float kq_combine(uint4 hdr, int c, float qa, float qb, const XK& x) {
   float sc0, sc1, m0, m1;
   kq_scales(hdr.y, hdr.z, hdr.w, c, sc0, sc1, m0, m1);
   const float d = h2f(hdr.x & 0xFFFFu), dmin = h2f(hdr.x >> 16);
-  // sum_j (d sc_j q - dmin m_j) x = d (sc0 s0 acc0 + sc1 s1 acc1) - dmin (m0 t0 + m1 t1)
-  return d * fmaf(sc0 * x.s0, float(acc0), sc1 * x.s1 * float(acc1)) - dmin * fmaf(m0, x.t0, m1 * x.t1);
+  // sum_j (d sc_j q - dmin m_j) x = d (sc0 s0 qa + sc1 s1 qb) - dmin (m0 t0 + m1 t1)
+  return d * fmaf(sc0 * x.s0, qa, sc1 * x.s1 * qb) - dmin * fmaf(m0, x.t0, m1 * x.t1);
 }
+
+// nibble bytes lo/hi of one qs word against plane words of groups A and B
+#define NT_KQ_MAC(i, lo, hi)                                          \
+  do {                                                                \
+    A0 = dp4_uu(x.a[0][i], lo, A0);                                   \
+    A1 = dp4_uu(x.a[1][i], lo, A1);                                   \
+    A2 = dp4_su(x.a[2][i], lo, A2);                                   \
+    B0 = dp4_uu(x.b[0][i], hi, B0);                                   \
+    B1 = dp4_uu(x.b[1][i], hi, B1);                                   \
+    B2 = dp4_su(x.b[2][i], hi, B2);                                   \
+  } while (0)
 
 // Q4_K: d | dmin | scales[12] | qs[128].  value d*sc*q - dmin*m.
 template <>
 struct Q<NT_Q4_K> {
-  static constexpr int BE = 256, BB = 144, ALIGN = 8, UPB = 4;
-  __host__ __device__ static constexpr int pads(int col) { return kq_pads(col); }
+  static constexpr int BE = 256, BB = 144, ALIGN = 8, UPB = 4, PB = 1;
   using X = XK;
-  __device__ static void load_x(X& x, const XS& xs, int col0, int c) { load_xk(x, xs, col0, c); }
+  __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int c) {
+    load_xk(x, g, g + 112, xs, col0, c);
+  }
   __device__ static float dot(const uint8_t* blk, int c, const X& x) {
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const uint4* qp = reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
     const uint4 q0 = qp[0], q1 = qp[1];
     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    int a0 = 0, a1 = 0;
+    int A0 = 0, A1 = 0, A2 = 0, B0 = 0, B1 = 0, B2 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
-      a0 = dp2lo_u(x.v[2 * i], lo, a0);
-      a0 = dp2hi_u(x.v[2 * i + 1], lo, a0);
-      a1 = dp2lo_u(x.v[16 + 2 * i], hi, a1);
-      a1 = dp2hi_u(x.v[16 + 2 * i + 1], hi, a1);
+      NT_KQ_MAC(i, lo, hi);
     }
-    return kq_combine(hdr, c, a0, a1, x);
+    return kq_combine(hdr, c, planes(A2, A1, A0), planes(B2, B1, B0), x);
   }
 };
 
@@ -261,10 +278,11 @@ struct Q<NT_Q4_K> {
 // of sub-block j is bit j of qh[l].
 template <>
 struct Q<NT_Q5_K> {
-  static constexpr int BE = 256, BB = 176, ALIGN = 8, UPB = 4;
-  __host__ __device__ static constexpr int pads(int col) { return kq_pads(col); }
+  static constexpr int BE = 256, BB = 176, ALIGN = 8, UPB = 4, PB = 1;
   using X = XK;
-  __device__ static void load_x(X& x, const XS& xs, int col0, int c) { load_xk(x, xs, col0, c); }
+  __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int c) {
+    load_xk(x, g, g + 112, xs, col0, c);
+  }
   __device__ static float dot(const uint8_t* blk, int c, const X& x) {
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const uint4* hp = reinterpret_cast<const uint4*>(blk + 16);
@@ -274,80 +292,94 @@ struct Q<NT_Q5_K> {
     const uint4 q0 = qp[0], q1 = qp[1];
     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
     const int b0 = 2 * c;
-    int a0 = 0, a1 = 0;
+    int A0 = 0, A1 = 0, A2 = 0, B0 = 0, B1 = 0, B2 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t lo = (w[i] & 0x0F0F0F0Fu) | (((hw[i] >> b0) & 0x01010101u) << 4);
       const uint32_t hi = ((w[i] >> 4) & 0x0F0F0F0Fu) | (((hw[i] >> (b0 + 1)) & 0x01010101u) << 4);
-      a0 = dp2lo_u(x.v[2 * i], lo, a0);
-      a0 = dp2hi_u(x.v[2 * i + 1], lo, a0);
-      a1 = dp2lo_u(x.v[16 + 2 * i], hi, a1);
-      a1 = dp2hi_u(x.v[16 + 2 * i + 1], hi, a1);
+      NT_KQ_MAC(i, lo, hi);
     }
-    return kq_combine(hdr, c, a0, a1, x);
+    return kq_combine(hdr, c, planes(A2, A1, A0), planes(B2, B1, B0), x);
   }
 };
+#undef NT_KQ_MAC
 
 // Q6_K: ql[128] | qh[64] | scales[16] int8 | d.  value d*sc*(q-32).
-// unit u = (half h = u>>1, s = u&1): groups g = 0..3 of 16 elements at block
-// columns 128h + 32g + 16s + l', l' < 16; group g has scale scales[8h+2g+s].
+// unit u = (half h = u>>1, s = u&1): chunks g = 0..3 of 16 elements at block
+// columns 128h + 32g + 16s + l', l' < 16 (the s-th half of group 4h+g);
+// chunk g has scale scales[8h+2g+s].
 template <>
 struct Q<NT_Q6_K> {
-  static constexpr int BE = 256, BB = 210, ALIGN = 8, UPB = 4;
-  __host__ __device__ static constexpr int pads(int col) { return 4 * (col / 256) + (col / 128) % 2; }
+  static constexpr int BE = 256, BB = 210, ALIGN = 8, UPB = 4, PB = 2;
   struct X {
-    uint32_t v[32];  // v[8g + i]: x16 pairs of group g
-    float s[4];      // group scales
-    int off[4];      // -32 * sum(x16 over group g)
+    uint32_t v[4][3][4];  // chunk g, plane k, 4 words (16 columns)
+    float s[4];           // group scales
+    int off[4][3];        // -32 * plane sums over the chunk
   };
-  __device__ static void load_x(X& x, const XS& xs, int col0, int u) {
+  __device__ static void load_x(X& x, const uint8_t* g0, const XS& xs, int col0, int u) {
     const int h = u >> 1, s = u & 1;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
+      const uint8_t* p = g0 + 112 * (4 * h + g) + 16 * s;
+#pragma unroll
+      for (int k = 0; k < 3; ++k) ld4(p + 32 * k, x.v[g][k]);
       const int col = col0 + 128 * h + 32 * g + 16 * s;
-      const int16_t* p = xs.x16 + col + 8 * pads(col);
-      ld4(p, x.v + 8 * g);
-      ld4(p + 8, x.v + 8 * g + 4);
       x.s[g] = xs.scale[col / 32];
-      x.off[g] = -32 * xs.sum16[col / 16];
+      const int* ps = xs.psum + 3 * (col / 16);
+#pragma unroll
+      for (int k = 0; k < 3; ++k) x.off[g][k] = -32 * ps[k];
     }
   }
   __device__ static float dot(const uint8_t* blk, int u, const X& x) {
     const int h = u >> 1, s = u & 1;
     uint32_t A[4], B[4], H[4], S[2];
-    lds_a2<4>(blk + 64 * h + 16 * s, A);        // low nibble: group 0, high: group 2
-    lds_a2<4>(blk + 64 * h + 32 + 16 * s, B);   // low nibble: group 1, high: group 3
-    lds_a2<4>(blk + 128 + 32 * h + 16 * s, H);  // bits 2g..2g+1: top bits of group g
+    lds_a2<4>(blk + 64 * h + 16 * s, A);        // low nibble: chunk 0, high: chunk 2
+    lds_a2<4>(blk + 64 * h + 32 + 16 * s, B);   // low nibble: chunk 1, high: chunk 3
+    lds_a2<4>(blk + 128 + 32 * h + 16 * s, H);  // bits 2g..2g+1: top bits of chunk g
     lds_a2<2>(blk + 192 + 8 * h, S);            // scales[8h .. 8h+7]
-    int a[4] = {x.off[0], x.off[1], x.off[2], x.off[3]};
+    int a[4][3];
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int k = 0; k < 3; ++k) a[g][k] = x.off[g][k];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t q0 = (A[i] & 0x0F0F0F0Fu) | ((H[i] << 4) & 0x30303030u);
-      const uint32_t q1 = (B[i] & 0x0F0F0F0Fu) | ((H[i] << 2) & 0x30303030u);
-      const uint32_t q2 = ((A[i] >> 4) & 0x0F0F0F0Fu) | (H[i] & 0x30303030u);
-      const uint32_t q3 = ((B[i] >> 4) & 0x0F0F0F0Fu) | ((H[i] >> 2) & 0x30303030u);
-      a[0] = dp2hi_u(x.v[2 * i + 1], q0, dp2lo_u(x.v[2 * i], q0, a[0]));
-      a[1] = dp2hi_u(x.v[8 + 2 * i + 1], q1, dp2lo_u(x.v[8 + 2 * i], q1, a[1]));
-      a[2] = dp2hi_u(x.v[16 + 2 * i + 1], q2, dp2lo_u(x.v[16 + 2 * i], q2, a[2]));
-      a[3] = dp2hi_u(x.v[24 + 2 * i + 1], q3, dp2lo_u(x.v[24 + 2 * i], q3, a[3]));
+      const uint32_t q[4] = {(A[i] & 0x0F0F0F0Fu) | ((H[i] << 4) & 0x30303030u),
+                             (B[i] & 0x0F0F0F0Fu) | ((H[i] << 2) & 0x30303030u),
+                             ((A[i] >> 4) & 0x0F0F0F0Fu) | (H[i] & 0x30303030u),
+                             ((B[i] >> 4) & 0x0F0F0F0Fu) | ((H[i] >> 2) & 0x30303030u)};
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        a[g][0] = dp4_uu(x.v[g][0][i], q[g], a[g][0]);
+        a[g][1] = dp4_uu(x.v[g][1][i], q[g], a[g][1]);
+        a[g][2] = dp4_su(x.v[g][2][i], q[g], a[g][2]);
+      }
     }
-    // scale of group g: scales[8h + 2g + s] = byte (2g + s) of the 8-byte window
+    // scale of chunk g: scales[8h + 2g + s] = byte (2g + s) of the 8-byte window
     const float sc0 = float(int8_t(S[0] >> (8 * s)));
     const float sc1 = float(int8_t(S[0] >> (8 * s + 16)));
     const float sc2 = float(int8_t(S[1] >> (8 * s)));
     const float sc3 = float(int8_t(S[1] >> (8 * s + 16)));
-    float t = sc0 * x.s[0] * float(a[0]);
-    t = fmaf(sc1 * x.s[1], float(a[1]), t);
-    t = fmaf(sc2 * x.s[2], float(a[2]), t);
-    t = fmaf(sc3 * x.s[3], float(a[3]), t);
+    float t = sc0 * x.s[0] * planes(a[0][2], a[0][1], a[0][0]);
+    t = fmaf(sc1 * x.s[1], planes(a[1][2], a[1][1], a[1][0]), t);
+    t = fmaf(sc2 * x.s[2], planes(a[2][2], a[2][1], a[2][0]), t);
+    t = fmaf(sc3 * x.s[3], planes(a[3][2], a[3][1], a[3][0]), t);
     const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
     return d * t;
   }
 };
 
+// byte offset of 32-column group g: 112 bytes per group, plus PB*16 bytes
+// per 8 groups (one K block), chosen per format so that the 16-byte plane
+// reads of a quarter-warp fall into 8 distinct bank groups
 template <int FMT>
-__host__ __device__ constexpr int x16_bytes(int cols) {
-  return ((2 * (cols + 8 * Q<FMT>::pads(cols)) + 16 + 15) / 16) * 16;
+__host__ __device__ constexpr int goff(int g) {
+  return 112 * g + 16 * Q<FMT>::PB * (g / 8);
+}
+
+template <int FMT>
+__host__ __device__ constexpr int x_bytes(int cols) {
+  return ((goff<FMT>(cols / 32 + 1) + 15) / 16) * 16;
 }
 
 // ---------------------------------------------------------------------------
@@ -365,13 +397,13 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
   using F = Q<FMT>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int nwarps = blockDim.x >> 5, kStages = a.nst;
-  const int xB = x16_bytes<FMT>(a.cols);
+  const int xB = x_bytes<FMT>(a.cols);
   const int ng = a.cols / 32;
-  int16_t* x16 = reinterpret_cast<int16_t*>(smem);
+  uint8_t* xsm = smem;
   float* gscale = reinterpret_cast<float*>(smem + xB);
-  int* sum16 = reinterpret_cast<int*>(smem + xB + 4 * ng);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ((xB + 12 * ng + 7) / 8) * 8);
-  uint8_t* stages = smem + ((xB + 12 * ng + 8 + nwarps * kStages * 8 + 127) / 128) * 128;
+  int* psum = reinterpret_cast<int*>(smem + xB + 4 * ng);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ((xB + 28 * ng + 7) / 8) * 8);
+  uint8_t* stages = smem + ((xB + 28 * ng + 8 + nwarps * kStages * 8 + 127) / 128) * 128;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t total_warps = int64_t(gridDim.x) * nwarps;
@@ -459,7 +491,7 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
   pdl_trigger();
   pdl_wait();
 
-  // ---- prologue: x (optionally RMS-normalised) -> int16 per 32-column group
+  // ---- prologue: x (optionally RMS-normalised) -> 24-bit fixed point per 32-column group
   {
     __shared__ float red[kMaxWarps];
     float inv = 1.f;
@@ -498,27 +530,46 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
       int e = 0;
       if (m > 0.f) frexpf(m, &e);  // m = f * 2^e, f in [0.5, 1)
-      const int sh = 15 - e;       // max |x| * 2^sh < 2^15
-      const int q0 = max(-32767, min(32767, __float2int_rn(ldexpf(v.x, sh))));
-      const int q1 = max(-32767, min(32767, __float2int_rn(ldexpf(v.y, sh))));
-      const int q2 = max(-32767, min(32767, __float2int_rn(ldexpf(v.z, sh))));
-      const int q3 = max(-32767, min(32767, __float2int_rn(ldexpf(v.w, sh))));
-      int s4 = q0 + q1 + q2 + q3;
-      s4 += __shfl_xor_sync(0xffffffffu, s4, 1);
-      s4 += __shfl_xor_sync(0xffffffffu, s4, 2);
+      const int sh = 23 - e;       // max |x| * 2^sh < 2^23
+      constexpr int kLim = (1 << 23) - 1;
+      const int q[4] = {max(-kLim, min(kLim, __float2int_rn(ldexpf(v.x, sh)))),
+                        max(-kLim, min(kLim, __float2int_rn(ldexpf(v.y, sh)))),
+                        max(-kLim, min(kLim, __float2int_rn(ldexpf(v.z, sh)))),
+                        max(-kLim, min(kLim, __float2int_rn(ldexpf(v.w, sh))))};
+      uint32_t pw[3] = {0u, 0u, 0u};
+      int ps[3] = {0, 0, 0};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int b0 = q[c] & 255, b1 = (q[c] >> 8) & 255, b2 = q[c] >> 16;  // b2 signed
+        pw[0] |= uint32_t(b0) << (8 * c);
+        pw[1] |= uint32_t(b1) << (8 * c);
+        pw[2] |= (uint32_t(b2) & 255u) << (8 * c);
+        ps[0] += b0;
+        ps[1] += b1;
+        ps[2] += b2;
+      }
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        ps[k] += __shfl_xor_sync(0xffffffffu, ps[k], 1);
+        ps[k] += __shfl_xor_sync(0xffffffffu, ps[k], 2);
+      }
       if (live) {
-        uint2 pk;
-        pk.x = (uint32_t(q0) & 0xFFFFu) | (uint32_t(q1) << 16);
-        pk.y = (uint32_t(q2) & 0xFFFFu) | (uint32_t(q3) << 16);
-        *reinterpret_cast<uint2*>(x16 + col + 8 * F::pads(col)) = pk;
-        if ((sub & 3) == 0) sum16[2 * grp + (sub >> 2)] = s4;
+        uint8_t* gp = xsm + goff<FMT>(grp) + 4 * sub;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) *reinterpret_cast<uint32_t*>(gp + 32 * k) = pw[k];
+        if ((sub & 3) == 0) {
+          int* dst = psum + 3 * (2 * grp + (sub >> 2));
+          dst[0] = ps[0];
+          dst[1] = ps[1];
+          dst[2] = ps[2];
+        }
         if (sub == 0) gscale[grp] = ldexpf(1.0f, -sh);
       }
     }
     __syncthreads();
   }
   if (my_groups == 0) return;
-  const XS xs{x16, gscale, sum16};
+  const XS xs{xsm, gscale, psum};
 
   float acc[R];
 #pragma unroll
@@ -546,7 +597,8 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
     for (int u = lane; u < units; u += 32) {
       const int b = u / F::UPB, uu = u % F::UPB;
       typename F::X x;
-      F::load_x(x, xs, (blk0 + b) * F::BE, uu);
+      const int col0 = (blk0 + b) * F::BE;
+      F::load_x(x, xsm + goff<FMT>(col0 / 32 + (F::UPB == 4 && FMT != NT_Q6_K ? 2 * uu : 0)), xs, col0, uu);
       const uint8_t* bp = st + b * F::BB;
 #pragma unroll
       for (int i = 0; i < R; ++i) acc[i] += F::dot(bp + i * a.segStride, uu, x);
@@ -626,16 +678,16 @@ cudaError_t dispatch_r(const Ctx* c, int R, const GemvArgs& a, int grid, size_t 
 
 struct FmtInfo {
   int align;   // blocks per segment unit: 16-byte aligned and a multiple of 32 lane units
-  int xbytes;  // shared bytes of x16
+  int xbytes;  // shared bytes of x
 };
 
 FmtInfo fmt_info(int fmt, int cols) {
   switch (fmt) {
-    case NT_Q8_0: return {Q<NT_Q8_0>::ALIGN, x16_bytes<NT_Q8_0>(cols)};
-    case NT_Q4_0: return {Q<NT_Q4_0>::ALIGN, x16_bytes<NT_Q4_0>(cols)};
-    case NT_Q4_K: return {Q<NT_Q4_K>::ALIGN, x16_bytes<NT_Q4_K>(cols)};
-    case NT_Q5_K: return {Q<NT_Q5_K>::ALIGN, x16_bytes<NT_Q5_K>(cols)};
-    default: return {Q<NT_Q6_K>::ALIGN, x16_bytes<NT_Q6_K>(cols)};
+    case NT_Q8_0: return {Q<NT_Q8_0>::ALIGN, x_bytes<NT_Q8_0>(cols)};
+    case NT_Q4_0: return {Q<NT_Q4_0>::ALIGN, x_bytes<NT_Q4_0>(cols)};
+    case NT_Q4_K: return {Q<NT_Q4_K>::ALIGN, x_bytes<NT_Q4_K>(cols)};
+    case NT_Q5_K: return {Q<NT_Q5_K>::ALIGN, x_bytes<NT_Q5_K>(cols)};
+    default: return {Q<NT_Q6_K>::ALIGN, x_bytes<NT_Q6_K>(cols)};
   }
 }
 
@@ -673,7 +725,7 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
   const FmtInfo fi = fmt_info(fmt, int(cols));
   const int kWarps = c->gemv_warps, kStages = c->gemv_stages;
   const int ng = int(cols / 32);
-  const int head = ((fi.xbytes + 12 * ng + 8 + kWarps * kStages * 8 + 127) / 128) * 128;
+  const int head = ((fi.xbytes + 28 * ng + 8 + kWarps * kStages * 8 + 127) / 128) * 128;
   const int pad = 16;  // the unaligned readers may touch 4 bytes past a stage
   const long avail = long(c->smem_optin) - head - pad - 256;  // 256: static shared memory
   int stb = int(avail / (kWarps * kStages)) / 16 * 16;
