@@ -723,39 +723,43 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
   if (swiglu) tma = tma && aligned(W2, 16);
 
   const FmtInfo fi = fmt_info(fmt, int(cols));
-  const int kWarps = c->gemv_warps, kStages = c->gemv_stages;
+  const int kWarps = c->gemv_warps;
   const int ng = int(cols / 32);
-  const int head = ((fi.xbytes + 28 * ng + 8 + kWarps * kStages * 8 + 127) / 128) * 128;
   const int pad = 16;  // the unaligned readers may touch 4 bytes past a stage
-  const long avail = long(c->smem_optin) - head - pad - 256;  // 256: static shared memory
-  int stb = int(avail / (kWarps * kStages)) / 16 * 16;
-  if (stb > c->gemv_stage_max) stb = c->gemv_stage_max;
-
   GemvArgs a{};
-  int R = 0;
+  int R = 0, kStages = 0, head = 0, stb = 0;
   const int al = fi.align;
-  for (int r : {4, 2}) {
-    // whole rows when R of them fit a stage
-    if (int64_t(r) * (tma ? rowB : ((rowB + 15) / 16) * 16) <= stb) {
-      R = r;
-      a.seg = int(nb);
-      a.nseg = 1;
-      a.merged = tma && !swiglu;
-      a.segStride = int(a.merged ? rowB : ((rowB + 15) / 16) * 16);
-      break;
+  // the configured stage count, fewer when x leaves too little shared memory
+  for (int ns = c->gemv_stages; ns >= 2 && R == 0; --ns) {
+    head = ((fi.xbytes + 28 * ng + 8 + kWarps * ns * 8 + 127) / 128) * 128;
+    const long avail = long(c->smem_optin) - head - pad - 256;  // 256: static shared memory
+    stb = int(avail / (kWarps * ns)) / 16 * 16;
+    if (stb > c->gemv_stage_max) stb = c->gemv_stage_max;
+    if (stb < 256) continue;
+    for (int r : {4, 2}) {
+      // whole rows when R of them fit a stage
+      if (int64_t(r) * (tma ? rowB : ((rowB + 15) / 16) * 16) <= stb) {
+        R = r;
+        a.seg = int(nb);
+        a.nseg = 1;
+        a.merged = tma && !swiglu;
+        a.segStride = int(a.merged ? rowB : ((rowB + 15) / 16) * 16);
+        break;
+      }
+      int seg = int(stb / (int64_t(r) * BB)) / al * al;
+      while (seg >= al && int64_t(r) * (((seg * BB + 15) / 16) * 16) > stb) seg -= al;
+      if (seg >= al) {
+        R = r;
+        a.seg = seg;
+        a.nseg = int((nb + seg - 1) / seg);
+        a.merged = 0;
+        a.segStride = ((seg * BB + 15) / 16) * 16;
+        break;
+      }
     }
-    int seg = int(stb / (int64_t(r) * BB)) / al * al;
-    while (seg >= al && int64_t(r) * (((seg * BB + 15) / 16) * 16) > stb) seg -= al;
-    if (seg >= al) {
-      R = r;
-      a.seg = seg;
-      a.nseg = int((nb + seg - 1) / seg);
-      a.merged = 0;
-      a.segStride = ((seg * BB + 15) / 16) * 16;
-      break;
-    }
+    if (R) kStages = ns;
   }
-  if (R == 0 || stb < 256)
+  if (R == 0)
     return set_err(c, NT_ERR_INVALID_ARG, "gemv: cols=%lld too large for the shared-memory plan", (long long)cols);
 
   const int rpg = swiglu ? R / 2 : R;
