@@ -392,8 +392,8 @@ __device__ __forceinline__ void locate(const GemvArgs& a, int64_t g, int rpg, in
   nr = left < rpg ? int(left) : rpg;
 }
 
-template <int FMT, int R>
-__global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
+template <int FMT, int R, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
   using F = Q<FMT>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int nwarps = blockDim.x >> 5, kStages = a.nst;
@@ -408,8 +408,8 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t total_warps = int64_t(gridDim.x) * nwarps;
   const int64_t wg = int64_t(blockIdx.x) * nwarps + warp;
-  const int64_t my_groups = wg < a.total_groups ? (a.total_groups - wg + total_warps - 1) / total_warps : 0;
-  const int64_t n_items = my_groups * a.nseg;
+  const int my_groups = wg < a.total_groups ? int((a.total_groups - wg + total_warps - 1) / total_warps) : 0;
+  const int n_items = my_groups * a.nseg;
   uint8_t* st0 = stages + size_t(warp) * kStages * a.stb;
   const uint32_t bar0 = smem_u32(bars + warp * kStages);
   const int rpg = a.swiglu ? R / 2 : R;
@@ -423,70 +423,71 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
   }
   const uint64_t pol = policy_evict_first();
 
-  // row pointer of local row i of a group (nullptr when the row is past the end)
-  auto row_ptr = [&](int j, int64_t r0, int nr, int i) -> const uint8_t* {
-    if (a.swiglu) {
-      const int h = R / 2;
-      const int k = i < h ? i : i - h;
-      if (k >= nr) return nullptr;
-      return (i < h ? a.job[j].W : a.job[j].W2) + (r0 + k) * a.rowB;
+  // ---- issue cursor: group ordinal, segment, stage slot; rows of the group cached
+  int it_t = 0, it_s = 0, it_slot = 0;
+  int g_j = 0, g_nr = 0;
+  int64_t g_r0 = 0;
+  const uint8_t* my_row = nullptr;  // lane i < R: row i of the current issue group (null past the end)
+
+  auto load_group = [&](int t) {
+    locate(a, wg + int64_t(t) * total_warps, rpg, g_j, g_r0, g_nr);
+    my_row = nullptr;
+    if (lane < R) {
+      const JobDev& J = a.job[g_j];
+      if (a.swiglu) {
+        const int h = R / 2, k = lane < h ? lane : lane - h;
+        if (k < g_nr) my_row = (lane < h ? J.W : J.W2) + (g_r0 + k) * a.rowB;
+      } else if (lane < g_nr) {
+        my_row = J.W + (g_r0 + lane) * a.rowB;
+      }
     }
-    if (i >= nr) return nullptr;
-    return a.job[j].W + (r0 + i) * a.rowB;
   };
 
-  auto issue = [&](int64_t k) {
-    const int64_t gi = wg + (k / a.nseg) * total_warps;
-    const int s = int(k % a.nseg);
-    int j, nr;
-    int64_t r0;
-    locate(a, gi, rpg, j, r0, nr);
+  auto fill = [&](uint8_t* st, uint32_t bar, int s) {
     const int blk0 = s * a.seg;
     const int nblk = min(a.seg, a.nb - blk0);
     const uint32_t bytes_row = uint32_t(nblk) * F::BB;
-    uint8_t* st = st0 + size_t(k % kStages) * a.stb;
-    const uint32_t bar = bar0 + 8 * uint32_t(k % kStages);
-    if (a.merged) {
-      if (lane == 0) {
-        const uint32_t tot = uint32_t(nr) * uint32_t(a.rowB);
-        mbar_arrive_expect_tx(bar, tot);
-        bulk_g2s(smem_u32(st), a.job[j].W + r0 * a.rowB, tot, bar, pol);
+    if (a.tma) {
+      if (a.merged) {
+        if (lane == 0) {
+          const uint32_t tot = uint32_t(g_nr) * uint32_t(a.rowB);
+          mbar_arrive_expect_tx(bar, tot);
+          bulk_g2s(smem_u32(st), a.job[g_j].W + g_r0 * a.rowB, tot, bar, pol);
+        }
+      } else {
+        const int nvalid = a.swiglu ? 2 * g_nr : g_nr;
+        if (lane == 0) mbar_arrive_expect_tx(bar, uint32_t(nvalid) * bytes_row);
+        __syncwarp();
+        if (my_row) bulk_g2s(smem_u32(st + lane * a.segStride), my_row + size_t(blk0) * F::BB, bytes_row, bar, pol);
       }
     } else {
-      const int nvalid = a.swiglu ? 2 * nr : nr;
-      if (lane == 0) mbar_arrive_expect_tx(bar, uint32_t(nvalid) * bytes_row);
-      __syncwarp();
-      if (lane < R) {
-        const uint8_t* src = row_ptr(j, r0, nr, lane);
-        if (src) bulk_g2s(smem_u32(st + lane * a.segStride), src + size_t(blk0) * F::BB, bytes_row, bar, pol);
+      // plain-load path for weights that break the bulk-copy alignment rules
+      for (int i = 0; i < R; ++i) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(
+            __shfl_sync(0xffffffffu, static_cast<unsigned long long>(reinterpret_cast<uintptr_t>(my_row)), i));
+        if (!src) continue;
+        src += size_t(blk0) * F::BB;
+        for (int b = lane; b < int(bytes_row); b += 32) st[i * a.segStride + b] = src[b];
       }
+      __syncwarp();
     }
   };
 
-  // plain-load path for weights that break the bulk-copy alignment rules
-  auto fill_plain = [&](int64_t k, uint8_t* st) {
-    const int64_t gi = wg + (k / a.nseg) * total_warps;
-    const int s = int(k % a.nseg);
-    int j, nr;
-    int64_t r0;
-    locate(a, gi, rpg, j, r0, nr);
-    const int blk0 = s * a.seg;
-    const int nblk = min(a.seg, a.nb - blk0);
-    const int bytes_row = nblk * F::BB;
-    for (int i = 0; i < R; ++i) {
-      const uint8_t* src = row_ptr(j, r0, nr, i);
-      if (!src) continue;
-      src += size_t(blk0) * F::BB;
-      for (int b = lane; b < bytes_row; b += 32) st[i * a.segStride + b] = src[b];
+  auto issue_next = [&]() {
+    if (it_s == 0) load_group(it_t);
+    fill(st0 + size_t(it_slot) * a.stb, bar0 + 8 * uint32_t(it_slot), it_s);
+    if (++it_s == a.nseg) {
+      it_s = 0;
+      ++it_t;
     }
-    __syncwarp();
+    if (++it_slot == kStages) it_slot = 0;
   };
 
   // weights do not depend on x: start streaming them before waiting for the
   // kernel that produces x
   if (a.tma) {
-    const int64_t pre = n_items < kStages - 1 ? n_items : kStages - 1;
-    for (int64_t k = 0; k < pre; ++k) issue(k);
+    const int pre = n_items < kStages - 1 ? n_items : kStages - 1;
+    for (int k = 0; k < pre; ++k) issue_next();
   }
   pdl_trigger();
   pdl_wait();
@@ -575,23 +576,32 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
 #pragma unroll
   for (int i = 0; i < R; ++i) acc[i] = 0.f;
 
-  for (int64_t k = 0; k < n_items; ++k) {
-    uint8_t* st = st0 + size_t(k % kStages) * a.stb;
+  // ---- consume cursor
+  int cs = 0, ct = 0, cseg = 0;
+  uint32_t cph = 0;
+  for (int k = 0; k < n_items; ++k) {
+    uint8_t* st = st0 + size_t(cs) * a.stb;
     if (a.tma) {
-      if (k + kStages - 1 < n_items) issue(k + kStages - 1);
-      const bool ok = mbar_wait(bar0 + 8 * uint32_t(k % kStages), uint32_t((k / kStages) & 1));
+      if (k + kStages - 1 < n_items) issue_next();
+      const bool ok = mbar_wait(bar0 + 8 * uint32_t(cs), cph);
       if (!__all_sync(0xffffffffu, ok)) {
         // a copy never landed: flag it, wait (bounded) for what is in flight, stop
         if (lane == 0) flag_error(a.err, kErrWaitTimeout);
-        const int64_t last = min(n_items, k + kStages - 1);
-        for (int64_t q = k + 1; q < last; ++q) mbar_wait(bar0 + 8 * uint32_t(q % kStages), uint32_t((q / kStages) & 1));
+        int q = cs;
+        uint32_t ph = cph;
+        for (int n = k + 1; n < min(n_items, k + kStages - 1); ++n) {
+          if (++q == kStages) {
+            q = 0;
+            ph ^= 1u;
+          }
+          mbar_wait(bar0 + 8 * uint32_t(q), ph);
+        }
         return;
       }
     } else {
-      fill_plain(k, st);
+      issue_next();
     }
-    const int s = int(k % a.nseg);
-    const int blk0 = s * a.seg;
+    const int blk0 = cseg * a.seg;
     const int nblk = min(a.seg, a.nb - blk0);
     const int units = nblk * F::UPB;
     for (int u = lane; u < units; u += 32) {
@@ -604,7 +614,7 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
       for (int i = 0; i < R; ++i) acc[i] += F::dot(bp + i * a.segStride, uu, x);
     }
     __syncwarp();
-    if (s == a.nseg - 1) {
+    if (cseg == a.nseg - 1) {
       // group done: reduce across lanes, lane i holds row i
       float mine = 0.f, other = 0.f;
 #pragma unroll
@@ -614,10 +624,9 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
         if (a.swiglu && lane + R / 2 == i) other = v;
         acc[i] = 0.f;
       }
-      const int64_t gi = wg + (k / a.nseg) * total_warps;
       int j, nr;
       int64_t r0;
-      locate(a, gi, rpg, j, r0, nr);
+      locate(a, wg + int64_t(ct) * total_warps, rpg, j, r0, nr);
       const JobDev& J = a.job[j];
       if (a.swiglu) {
         if (lane < nr) J.y[r0 + lane] = silu(mine) * other;
@@ -633,9 +642,9 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
           const int head = int(r / hd), d = int(r % hd);
           float out = mine;
           if (J.epi != kEpiCache) {
-            float cs, sn;
-            rope_cs(pos, a.rope.inv_freq[d >> 1], cs, sn);
-            out = (d & 1) ? fmaf(partner, sn, mine * cs) : fmaf(mine, cs, -partner * sn);
+            float cs_, sn;
+            rope_cs(pos, a.rope.inv_freq[d >> 1], cs_, sn);
+            out = (d & 1) ? fmaf(partner, sn, mine * cs_) : fmaf(mine, cs_, -partner * sn);
           }
           if (J.epi == kEpiRope)
             J.y[r] = out;
@@ -643,6 +652,14 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
             J.cache[(int64_t(head) * a.rope.kv_stride + pos) * hd + d] = __float2half_rn(out);
         }
       }
+    }
+    if (++cs == kStages) {
+      cs = 0;
+      cph ^= 1u;
+    }
+    if (++cseg == a.nseg) {
+      cseg = 0;
+      ++ct;
     }
   }
 }
@@ -652,7 +669,9 @@ __global__ void __launch_bounds__(256, 1) qgemv_kernel(const GemvArgs a) {
 
 template <int FMT, int R>
 cudaError_t launch_t(const Ctx* c, const GemvArgs& a, int grid, size_t smem, cudaStream_t st) {
-  return launch_k(c, qgemv_kernel<FMT, R>, dim3(grid), dim3(c->gemv_warps * 32), smem, st, a);
+  if (c->gemv_warps > 8)
+    return launch_k(c, qgemv_kernel<FMT, R, 512>, dim3(grid), dim3(c->gemv_warps * 32), smem, st, a);
+  return launch_k(c, qgemv_kernel<FMT, R, 256>, dim3(grid), dim3(c->gemv_warps * 32), smem, st, a);
 }
 
 // dynamic shared memory a kernel may use: the opt-in limit minus its static part
@@ -666,8 +685,10 @@ cudaError_t allow_smem(K kernel, int optin) {
 
 template <int FMT>
 cudaError_t configure_fmt(int smem) {
-  cudaError_t e = allow_smem(qgemv_kernel<FMT, 4>, smem);
-  if (e == cudaSuccess) e = allow_smem(qgemv_kernel<FMT, 2>, smem);
+  cudaError_t e = allow_smem(qgemv_kernel<FMT, 4, 256>, smem);
+  if (e == cudaSuccess) e = allow_smem(qgemv_kernel<FMT, 2, 256>, smem);
+  if (e == cudaSuccess) e = allow_smem(qgemv_kernel<FMT, 4, 512>, smem);
+  if (e == cudaSuccess) e = allow_smem(qgemv_kernel<FMT, 2, 512>, smem);
   return e;
 }
 
