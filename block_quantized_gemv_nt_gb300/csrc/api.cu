@@ -112,8 +112,8 @@ nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes) {
     const int x = atoi(v);
     return (x >= lo && x <= hi) ? x : dflt;
   };
-  c->gemv_warps = env_int("NT_GEMV_WARPS", 2, 16, 8);
-  c->gemv_stages = env_int("NT_GEMV_STAGES", 2, 8, 4);
+  c->gemv_warps = env_int("NT_GEMV_WARPS", 4, 16, 16);
+  c->gemv_stages = env_int("NT_GEMV_STAGES", 2, 8, 2);
   c->gemv_stage_max = env_int("NT_GEMV_STAGE_MAX", 1024, 65536, 12288) / 16 * 16;
   c->pdl = env_int("NT_PDL", 0, 1, 1) != 0;
   c->scratch_bytes = scratch_bytes ? scratch_bytes : (size_t(64) << 20);

@@ -27,8 +27,8 @@ struct Ctx {
   size_t scratch_bytes = 0;
   unsigned* err_flag = nullptr; // device word, set by kernels whose bounded wait ran out
   bool pdl = true;               // launch with programmatic stream serialization
-  int gemv_warps = 8;            // quant-GEMV launch shape (tuning knobs, env NT_GEMV_*)
-  int gemv_stages = 4;
+  int gemv_warps = 16;           // quant-GEMV launch shape (tuning knobs, env NT_GEMV_*)
+  int gemv_stages = 2;
   int gemv_stage_max = 12288;
   std::string last_error;
   std::mutex mu;

@@ -668,10 +668,9 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
 // host side
 
 template <int FMT, int R>
-cudaError_t launch_t(const Ctx* c, const GemvArgs& a, int grid, size_t smem, cudaStream_t st) {
-  if (c->gemv_warps > 8)
-    return launch_k(c, qgemv_kernel<FMT, R, 512>, dim3(grid), dim3(c->gemv_warps * 32), smem, st, a);
-  return launch_k(c, qgemv_kernel<FMT, R, 256>, dim3(grid), dim3(c->gemv_warps * 32), smem, st, a);
+cudaError_t launch_t(const Ctx* c, const GemvArgs& a, int warps, int grid, size_t smem, cudaStream_t st) {
+  if (warps > 8) return launch_k(c, qgemv_kernel<FMT, R, 512>, dim3(grid), dim3(warps * 32), smem, st, a);
+  return launch_k(c, qgemv_kernel<FMT, R, 256>, dim3(grid), dim3(warps * 32), smem, st, a);
 }
 
 // dynamic shared memory a kernel may use: the opt-in limit minus its static part
@@ -693,8 +692,8 @@ cudaError_t configure_fmt(int smem) {
 }
 
 template <int FMT>
-cudaError_t dispatch_r(const Ctx* c, int R, const GemvArgs& a, int grid, size_t smem, cudaStream_t st) {
-  return R == 4 ? launch_t<FMT, 4>(c, a, grid, smem, st) : launch_t<FMT, 2>(c, a, grid, smem, st);
+cudaError_t dispatch_r(const Ctx* c, int R, const GemvArgs& a, int warps, int grid, size_t smem, cudaStream_t st) {
+  return R == 4 ? launch_t<FMT, 4>(c, a, warps, grid, smem, st) : launch_t<FMT, 2>(c, a, warps, grid, smem, st);
 }
 
 struct FmtInfo {
@@ -744,41 +743,45 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
   if (swiglu) tma = tma && aligned(W2, 16);
 
   const FmtInfo fi = fmt_info(fmt, int(cols));
-  const int kWarps = c->gemv_warps;
   const int ng = int(cols / 32);
   const int pad = 16;  // the unaligned readers may touch 4 bytes past a stage
   GemvArgs a{};
-  int R = 0, kStages = 0, head = 0, stb = 0;
+  int R = 0, kStages = 0, kWarps = 0, head = 0, stb = 0;
   const int al = fi.align;
-  // the configured stage count, fewer when x leaves too little shared memory
-  for (int ns = c->gemv_stages; ns >= 2 && R == 0; --ns) {
-    head = ((fi.xbytes + 28 * ng + 8 + kWarps * ns * 8 + 127) / 128) * 128;
-    const long avail = long(c->smem_optin) - head - pad - 256;  // 256: static shared memory
-    stb = int(avail / (kWarps * ns)) / 16 * 16;
-    if (stb > c->gemv_stage_max) stb = c->gemv_stage_max;
-    if (stb < 256) continue;
-    for (int r : {4, 2}) {
-      // whole rows when R of them fit a stage
-      if (int64_t(r) * (tma ? rowB : ((rowB + 15) / 16) * 16) <= stb) {
-        R = r;
-        a.seg = int(nb);
-        a.nseg = 1;
-        a.merged = tma && !swiglu;
-        a.segStride = int(a.merged ? rowB : ((rowB + 15) / 16) * 16);
-        break;
+  // the configured warps and stages; fewer when x leaves too little shared memory
+  for (int nw = c->gemv_warps; nw >= 4 && R == 0; nw /= 2) {
+    for (int ns = c->gemv_stages; ns >= 2 && R == 0; --ns) {
+      head = ((fi.xbytes + 28 * ng + 8 + nw * ns * 8 + 127) / 128) * 128;
+      const long avail = long(c->smem_optin) - head - pad - 256;  // 256: static shared memory
+      stb = int(avail / (nw * ns)) / 16 * 16;
+      if (stb > c->gemv_stage_max) stb = c->gemv_stage_max;
+      if (stb < 256) continue;
+      for (int r : {4, 2}) {
+        // whole rows when R of them fit a stage
+        if (int64_t(r) * (tma ? rowB : ((rowB + 15) / 16) * 16) <= stb) {
+          R = r;
+          a.seg = int(nb);
+          a.nseg = 1;
+          a.merged = tma && !swiglu;
+          a.segStride = int(a.merged ? rowB : ((rowB + 15) / 16) * 16);
+          break;
+        }
+        int seg = int(stb / (int64_t(r) * BB)) / al * al;
+        while (seg >= al && int64_t(r) * (((seg * BB + 15) / 16) * 16) > stb) seg -= al;
+        if (seg >= al) {
+          R = r;
+          a.seg = seg;
+          a.nseg = int((nb + seg - 1) / seg);
+          a.merged = 0;
+          a.segStride = ((seg * BB + 15) / 16) * 16;
+          break;
+        }
       }
-      int seg = int(stb / (int64_t(r) * BB)) / al * al;
-      while (seg >= al && int64_t(r) * (((seg * BB + 15) / 16) * 16) > stb) seg -= al;
-      if (seg >= al) {
-        R = r;
-        a.seg = seg;
-        a.nseg = int((nb + seg - 1) / seg);
-        a.merged = 0;
-        a.segStride = ((seg * BB + 15) / 16) * 16;
-        break;
+      if (R) {
+        kStages = ns;
+        kWarps = nw;
       }
     }
-    if (R) kStages = ns;
   }
   if (R == 0)
     return set_err(c, NT_ERR_INVALID_ARG, "gemv: cols=%lld too large for the shared-memory plan", (long long)cols);
@@ -822,11 +825,11 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
 
   cudaError_t e;
   switch (fmt) {
-    case NT_Q8_0: e = dispatch_r<NT_Q8_0>(c, R, a, grid, smem, st); break;
-    case NT_Q4_0: e = dispatch_r<NT_Q4_0>(c, R, a, grid, smem, st); break;
-    case NT_Q4_K: e = dispatch_r<NT_Q4_K>(c, R, a, grid, smem, st); break;
-    case NT_Q5_K: e = dispatch_r<NT_Q5_K>(c, R, a, grid, smem, st); break;
-    default: e = dispatch_r<NT_Q6_K>(c, R, a, grid, smem, st); break;
+    case NT_Q8_0: e = dispatch_r<NT_Q8_0>(c, R, a, kWarps, grid, smem, st); break;
+    case NT_Q4_0: e = dispatch_r<NT_Q4_0>(c, R, a, kWarps, grid, smem, st); break;
+    case NT_Q4_K: e = dispatch_r<NT_Q4_K>(c, R, a, kWarps, grid, smem, st); break;
+    case NT_Q5_K: e = dispatch_r<NT_Q5_K>(c, R, a, kWarps, grid, smem, st); break;
+    default: e = dispatch_r<NT_Q6_K>(c, R, a, kWarps, grid, smem, st); break;
   }
   return cuda_check(c, e, "qgemv launch");
 }
