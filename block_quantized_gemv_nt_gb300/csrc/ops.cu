@@ -6,6 +6,7 @@
 // "Fonctionnalités principales" (RoPE, GQA, SwiGLU, RMSNorm, KV cache);
 // "Performances et structure de cache" (cosine-similarity layer skip).
 #include <cfloat>
+#include <mutex>
 
 #include "nt_internal.cuh"
 #include "ops.cuh"
@@ -487,4 +488,91 @@ nt_status launch_cos(Ctx* c, const float* a, const float* b, int64_t n, float* o
   return cuda_check(c, cudaGetLastError(), "cos launch");
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the decode attention.  Its scratch (split
+// partials, combine counters, error word) is this file-scope array instead
+// of context memory, so the entry point needs no nt_ctx and calls neither
+// cudaMalloc nor cudaFree.  Every GPU that loads the library holds the array
+// until the process exits.
+namespace {
+constexpr size_t kAttnStaticBytes = size_t(4) << 20;  // 4 MiB
+constexpr size_t kAttnStaticCounters = 0;             // 64 unsigned
+constexpr size_t kAttnStaticErr = 256;                // unsigned error word
+constexpr size_t kAttnStaticPart = 512;               // split partials
+static __device__ __align__(256) unsigned char g_attn_static_scratch[kAttnStaticBytes];
+
+struct StaticAttnDevice {
+  bool ready = false;
+  unsigned char* scratch = nullptr;  // device address of g_attn_static_scratch
+  int num_sms = 0;
+};
+constexpr int kMaxDevices = 64;
+StaticAttnDevice g_static_dev[kMaxDevices];
+std::mutex g_static_mu;
+}  // namespace
+
 }  // namespace nt
+
+extern "C" nt_status nt_attn_decode_static(const float* q, const void* kc, const void* vc, float* out, int n_qh,
+                                           int n_kvh, int head_dim, int64_t n_pos, int64_t kv_stride,
+                                           void* stream) {
+  using namespace nt;
+  if (!q || !kc || !vc || !out) return NT_ERR_INVALID_ARG;
+  if (head_dim != kHD) return NT_ERR_INVALID_ARG;
+  if (n_kvh <= 0 || n_qh <= 0 || n_qh % n_kvh || n_qh / n_kvh > kMaxGroup || n_kvh > 64) return NT_ERR_INVALID_ARG;
+  if (n_pos < 1 || n_pos > kv_stride) return NT_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(kc, 16) || !aligned(vc, 16)) return NT_ERR_ALIGNMENT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NT_ERR_CUDA;
+  StaticAttnDevice* sd = &g_static_dev[dev];
+  {
+    // once per device, with that device current: the device address of the
+    // scratch array, the SM count and the kernel's shared-memory allowance
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!sd->ready) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_attn_static_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return NT_ERR_CUDA;
+      }
+      int sms = 0, optin = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return NT_ERR_CUDA;
+      const size_t smem = attn_smem_bytes(kMaxGroup);
+      cudaFuncAttributes fa{};
+      if (cudaFuncGetAttributes(&fa, attn_kernel) != cudaSuccess || smem + fa.sharedSizeBytes > size_t(optin) ||
+          cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+        return NT_ERR_CUDA;
+      sd->scratch = static_cast<unsigned char*>(ptr);
+      sd->num_sms = sms;
+      sd->ready = true;
+    }
+  }
+  int S = (sd->num_sms + n_kvh - 1) / n_kvh;
+  const int64_t need_s = (kv_stride + kMaxChunk - 1) / kMaxChunk;
+  if (need_s > S) S = int(need_s);
+  const size_t part_bytes = size_t(n_kvh) * S * (n_qh / n_kvh) * (2 + kHD) * sizeof(float);
+  if (kAttnStaticPart + part_bytes > kAttnStaticBytes) return NT_ERR_INVALID_ARG;  // beyond the fixed scratch
+  cudaStream_t st = as_stream(stream);
+  // the combine counters must start at zero; a call cut short may have left them set
+  if (cudaMemsetAsync(sd->scratch + kAttnStaticCounters, 0, kAttnStaticPart, st) != cudaSuccess) return NT_ERR_CUDA;
+  AttnArgs a{};
+  a.q = q;
+  a.K = static_cast<const __half*>(kc);
+  a.V = static_cast<const __half*>(vc);
+  a.out = out;
+  a.n_qh = n_qh;
+  a.n_kvh = n_kvh;
+  a.G = n_qh / n_kvh;
+  a.S = S;
+  a.n_pos = n_pos;
+  a.pos_dev = nullptr;
+  a.kv_stride = kv_stride;
+  a.part = reinterpret_cast<float*>(sd->scratch + kAttnStaticPart);
+  a.counters = reinterpret_cast<unsigned*>(sd->scratch + kAttnStaticCounters);
+  a.err = reinterpret_cast<unsigned*>(sd->scratch + kAttnStaticErr);
+  attn_kernel<<<dim3(n_kvh, S), kAttnThreads, attn_smem_bytes(a.G), st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? NT_OK : NT_ERR_CUDA;
+}
+

@@ -91,11 +91,13 @@ _sig("nt_model_init", [_vp, ctypes.POINTER(nt_model_desc), ctypes.POINTER(nt_lay
 _sig("nt_model_destroy", [_vp, _vp])
 _sig("nt_decode_step", [_vp, _vp, ctypes.c_int32, _i64, _vp, _vp, _vp, _vp])
 _sig("nt_layer_skip_calibrate", [_vp, _vp, ctypes.c_int32, _i64, _ci, _vp, _vp, _vp, _vp, _vp])
+_sig("nt_attn_decode_static", [_vp, _vp, _vp, _vp, _ci, _ci, _ci, _i64, _i64, _vp])
 
 EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "nt_block_bytes", "nt_block_elems",
             "nt_dequant_rows", "nt_gemv_q", "nt_gemv_q_swiglu", "nt_gemv_q_multi", "nt_rmsnorm", "nt_rope",
             "nt_rope_kv_append", "nt_attn_decode", "nt_softmax", "nt_swiglu", "nt_argmax", "nt_cos_sim",
-            "nt_model_init", "nt_model_destroy", "nt_decode_step", "nt_layer_skip_calibrate"]
+            "nt_model_init", "nt_model_destroy", "nt_decode_step", "nt_layer_skip_calibrate",
+            "nt_attn_decode_static"]
 
 
 def lib():
@@ -260,3 +262,13 @@ def nt_layer_skip_calibrate(ctx, model: int, token: int, pos: int, n_skip: int, 
                                            cos.ctypes.data, _ptr(logits), _ptr(next_token),
                                            _stream(stream, logits)))
     return mask, cos
+
+
+def nt_attn_decode_static(q, kcache, vcache, out, n_qh, n_kvh, head_dim, n_pos, kv_stride, stream=None):
+    """Decode attention without a context or any allocation (fixed scratch inside
+    the library); raises NtError on a non-OK status."""
+    st = _lib.nt_attn_decode_static(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), n_qh, n_kvh, head_dim, n_pos,
+                                    kv_stride, _stream(stream, out))
+    if st != NT_OK:
+        raise NtError(st, "nt_attn_decode_static failed")
+    return st

@@ -209,6 +209,34 @@ nt_status nt_layer_skip_calibrate(nt_ctx* ctx, nt_model* model, int32_t token, i
                                   uint8_t* skip_mask_host, float* cos_host, float* logits_dev,
                                   int32_t* next_token_dev, void* stream);
 
+/* ---- allocation-free attention ------------------------------------------------ */
+
+/* nt_attn_decode without a context and without any device allocation: the
+ * pages have no counterpart; it exists for callers that cannot call
+ * cudaMalloc — code running while a stream is captured into a CUDA graph in
+ * a mode that forbids allocation, and hosts whose device memory is handed
+ * out only by their own pool (an nt_ctx allocates its scratch, so such
+ * callers cannot create one).
+ *
+ * Same operation, arguments and result as nt_attn_decode, on the calling
+ * thread's current device.  The split partials, the combine counters and the
+ * error word live in one fixed 4 MiB array compiled into the library
+ * (every GPU that loads the library holds it until the process exits);
+ * n_kvh * S * (n_qh / n_kvh) * 130 * 4 + 512 bytes must fit in it, where
+ * S = max(ceil(SMs / n_kvh), ceil(kv_stride / 128)) — e.g. 64 q heads over
+ * 8 KV heads fit for kv_stride up to 16,128 positions.  Larger shapes return
+ * NT_ERR_INVALID_ARG before any launch.
+ *  - The first call on a device looks up the array's device address and sets
+ *    the kernel's shared-memory limit; make that first call before any stream
+ *    capture.
+ *  - Every call shares the array and clears its counters on `stream` first;
+ *    calls whose work overlaps on the GPU (different streams, or devices
+ *    sharing nothing but the symbol) race on it — serialize them.
+ *  - Returns NT_OK once the work is enqueued; a device-side wait that runs out
+ *    is recorded only in the array, not reported. */
+nt_status nt_attn_decode_static(const float* q_dev, const void* kcache_dev, const void* vcache_dev, float* out_dev,
+                                int n_qh, int n_kvh, int head_dim, int64_t n_pos, int64_t kv_stride, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
