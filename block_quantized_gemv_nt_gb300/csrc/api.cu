@@ -264,6 +264,7 @@ nt_status nt_attn_decode(nt_ctx* ctx, const float* q, const void* kc, const void
   NT_REQUIRE(n_kvh > 0 && n_qh > 0 && n_qh % n_kvh == 0 && n_qh / n_kvh <= 16 && n_kvh <= 64, NT_ERR_INVALID_ARG,
              "n_qh must be a multiple of n_kvh, group <= 16, n_kvh <= 64");
   NT_REQUIRE(n_pos >= 1 && n_pos <= kv_stride, NT_ERR_INVALID_ARG, "need 1 <= n_pos <= kv_stride");
+  NT_REQUIRE(kv_stride <= attn_max_stride(), NT_ERR_INVALID_ARG, "kv_stride above %lld", (long long)attn_max_stride());
   NT_TRY(check_vec(ctx, q, "q"));
   NT_TRY(check_vec(ctx, out, "out"));
   NT_REQUIRE(aligned(kc, 16) && aligned(vc, 16), NT_ERR_ALIGNMENT, "caches must be 16-byte aligned");

@@ -158,6 +158,7 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   NT_REQUIRE(d.n_kvh > 0 && d.n_qh % d.n_kvh == 0 && d.n_qh / d.n_kvh <= 16 && d.n_kvh <= 64, NT_ERR_INVALID_ARG,
              "bad head counts");
   NT_REQUIRE(d.kv_cap > 0 && d.eps >= 0.f && d.theta > 0.f, NT_ERR_INVALID_ARG, "bad kv_cap/eps/theta");
+  NT_REQUIRE(d.kv_cap <= attn_max_stride(), NT_ERR_INVALID_ARG, "kv_cap above %lld", (long long)attn_max_stride());
   const int fm[9] = {d.fmt_q, d.fmt_k, d.fmt_v, d.fmt_o, d.fmt_gate, d.fmt_up, d.fmt_down, d.fmt_embd, d.fmt_out};
   for (int f : fm) NT_REQUIRE(fmt_ok(f), NT_ERR_UNSUPPORTED_FMT, "unknown format id %d", f);
   NT_REQUIRE(d.fmt_gate == d.fmt_up, NT_ERR_INVALID_ARG, "gate and up must share a format");

@@ -263,21 +263,46 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   __syncthreads();
   if (!last) return;
   __threadfence();
+  // combine: stage every split's (max, sum) in shared memory, turn them into
+  // per-split weights w_t = e^(m_t - M) / L, then each output element is an
+  // independent sum over the splits
   const float* base = a.part + int64_t(g) * a.S * G * (2 + kHD);
+  float* wts = sc;  // [G][S] (the score buffer is free now; S <= kMaxChunk)
+  for (int i = tid; i < G * a.S; i += kAttnThreads) {
+    const int h = i / a.S, t = i % a.S;
+    wts[h * kMaxChunk + t] = __ldcg(base + (int64_t(t) * G + h) * (2 + kHD));
+  }
+  __syncthreads();
+  for (int h = warp; h < G; h += 8) {
+    float M = -INFINITY;
+    for (int t = lane; t < a.S; t += 32) M = fmaxf(M, wts[h * kMaxChunk + t]);
+    M = warp_max(M);
+    float L = 0.f;
+    for (int t = lane; t < a.S; t += 32) {
+      const float mt = wts[h * kMaxChunk + t];
+      const float w = mt == -INFINITY ? 0.f : __expf(mt - M);
+      L = fmaf(__ldcg(base + (int64_t(t) * G + h) * (2 + kHD) + 1), w, L);
+      wts[h * kMaxChunk + t] = w;
+    }
+    L = warp_sum(L);
+    const float inv = 1.0f / L;
+    for (int t = lane; t < a.S; t += 32) wts[h * kMaxChunk + t] *= inv;
+  }
+  __syncthreads();
   for (int i = tid; i < G * kHD; i += kAttnThreads) {
     const int h = i / kHD, d = i % kHD;
-    float M = -INFINITY;
-    for (int t = 0; t < a.S; ++t) M = fmaxf(M, __ldcg(base + (int64_t(t) * G + h) * (2 + kHD)));
-    float L = 0.f, O = 0.f;
-    for (int t = 0; t < a.S; ++t) {
-      const float* pp = base + (int64_t(t) * G + h) * (2 + kHD);
-      const float mt = __ldcg(pp);
-      if (mt == -INFINITY) continue;
-      const float w = __expf(mt - M);
-      L = fmaf(__ldcg(pp + 1), w, L);
-      O = fmaf(__ldcg(pp + 2 + d), w, O);
+    const float* pp = base + int64_t(h) * (2 + kHD) + 2 + d;
+    const int64_t stride = int64_t(G) * (2 + kHD);
+    float O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
+    int t = 0;
+    for (; t + 4 <= a.S; t += 4) {
+      O0 = fmaf(__ldcg(pp + (t + 0) * stride), wts[h * kMaxChunk + t + 0], O0);
+      O1 = fmaf(__ldcg(pp + (t + 1) * stride), wts[h * kMaxChunk + t + 1], O1);
+      O2 = fmaf(__ldcg(pp + (t + 2) * stride), wts[h * kMaxChunk + t + 2], O2);
+      O3 = fmaf(__ldcg(pp + (t + 3) * stride), wts[h * kMaxChunk + t + 3], O3);
     }
-    a.out[(int64_t(g) * G + h) * kHD + d] = O / L;
+    for (; t < a.S; ++t) O0 = fmaf(__ldcg(pp + t * stride), wts[h * kMaxChunk + t], O0);
+    a.out[(int64_t(g) * G + h) * kHD + d] = (O0 + O1) + (O2 + O3);
   }
   if (tid == 0) a.counters[g] = 0u;  // ready for the next launch
 }
@@ -409,12 +434,17 @@ nt_status launch_rope_append(Ctx* c, float* q, const float* k, const float* v, v
   return cuda_check(c, cudaGetLastError(), "rope/append launch");
 }
 
+// splits per KV head: enough CTAs to cover the SMs, chunks of at most
+// kMaxChunk positions, and at most kMaxChunk splits (the combine stages one
+// weight per split in a kMaxChunk-long row), so kv_stride <= kMaxChunk^2
 int attn_splits(const Ctx* c, int n_kvh, int64_t kv_stride) {
   int S = (c->num_sms + n_kvh - 1) / n_kvh;
   const int64_t need = (kv_stride + kMaxChunk - 1) / kMaxChunk;
   if (need > S) S = int(need);
-  return S;
+  return S < kMaxChunk ? S : kMaxChunk;
 }
+
+int64_t attn_max_stride() { return int64_t(kMaxChunk) * kMaxChunk; }
 
 size_t attn_scratch_bytes(int n_qh, int n_kvh, int S) {
   return size_t(n_kvh) * S * (n_qh / n_kvh) * (2 + kHD) * sizeof(float) + 64 * sizeof(unsigned);
@@ -549,9 +579,11 @@ extern "C" nt_status nt_attn_decode_static(const float* q, const void* kc, const
       sd->ready = true;
     }
   }
+  if (kv_stride > int64_t(kMaxChunk) * kMaxChunk) return NT_ERR_INVALID_ARG;
   int S = (sd->num_sms + n_kvh - 1) / n_kvh;
   const int64_t need_s = (kv_stride + kMaxChunk - 1) / kMaxChunk;
   if (need_s > S) S = int(need_s);
+  if (S > kMaxChunk) S = kMaxChunk;
   const size_t part_bytes = size_t(n_kvh) * S * (n_qh / n_kvh) * (2 + kHD) * sizeof(float);
   if (kAttnStaticPart + part_bytes > kAttnStaticBytes) return NT_ERR_INVALID_ARG;  // beyond the fixed scratch
   cudaStream_t st = as_stream(stream);

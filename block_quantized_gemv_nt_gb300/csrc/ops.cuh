@@ -16,6 +16,7 @@ nt_status launch_rope_append(Ctx* c, float* q, const float* k, const float* v, v
                              int n_kvh, int hd, int64_t pos, const int64_t* pos_dev, int64_t kv_stride, float theta,
                              cudaStream_t st);
 int attn_splits(const Ctx* c, int n_kvh, int64_t kv_stride);
+int64_t attn_max_stride();
 size_t attn_scratch_bytes(int n_qh, int n_kvh, int S);
 nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, float* out, int n_qh, int n_kvh,
                       int64_t n_pos, const int64_t* pos_dev, int64_t kv_stride, float* part, unsigned* counters,

@@ -58,6 +58,8 @@ struct GemvArgs {
   int64_t total_groups;
   unsigned* err;
   RopeArgs rope;
+  int ks;             // warps sharing a row group, each over a column part
+  int pblk[5];        // part p covers blocks [pblk[p], pblk[p+1])
 };
 
 // ---------------------------------------------------------------------------
@@ -87,6 +89,10 @@ __device__ __forceinline__ void lds_a2(const uint8_t* p, uint32_t* w) {
   for (int i = 0; i <= N; ++i) t[i] = b[i];
 #pragma unroll
   for (int i = 0; i < N; ++i) w[i] = __funnelshift_r(t[i], t[i + 1], sh);
+}
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ float h2f(uint32_t bits16) { return __half2float(__ushort_as_half((unsigned short)bits16)); }
@@ -406,10 +412,16 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
   uint8_t* stages = smem + ((xB + 28 * ng + 8 + nwarps * kStages * 8 + 127) / 128) * 128;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t total_warps = int64_t(gridDim.x) * nwarps;
-  const int64_t wg = int64_t(blockIdx.x) * nwarps + warp;
+  // warps come in slots of a.ks; the warps of a slot share row groups, warp
+  // `part` of a slot covers the blocks [pblk[part], pblk[part+1]) of each row
+  const int KS = a.ks, slots = nwarps / KS, slot = warp / KS, part = warp % KS;
+  const int pb0 = a.pblk[part], pb1 = a.pblk[part + 1];
+  const int nseg = (pb1 - pb0 + a.seg - 1) / a.seg;
+  const int64_t total_warps = int64_t(gridDim.x) * slots;  // group stride
+  const int64_t wg = int64_t(blockIdx.x) * slots + slot;   // first group
   const int my_groups = wg < a.total_groups ? int((a.total_groups - wg + total_warps - 1) / total_warps) : 0;
-  const int n_items = my_groups * a.nseg;
+  const int n_items = my_groups * nseg;
+  __shared__ float xchg[2 * 4 * kMaxWarps];  // [2][slots][KS][R] partial sums of split groups
   uint8_t* st0 = stages + size_t(warp) * kStages * a.stb;
   const uint32_t bar0 = smem_u32(bars + warp * kStages);
   const int rpg = a.swiglu ? R / 2 : R;
@@ -444,8 +456,8 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
   };
 
   auto fill = [&](uint8_t* st, uint32_t bar, int s) {
-    const int blk0 = s * a.seg;
-    const int nblk = min(a.seg, a.nb - blk0);
+    const int blk0 = pb0 + s * a.seg;
+    const int nblk = min(a.seg, pb1 - blk0);
     const uint32_t bytes_row = uint32_t(nblk) * F::BB;
     if (a.tma) {
       if (a.merged) {
@@ -476,7 +488,7 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
   auto issue_next = [&]() {
     if (it_s == 0) load_group(it_t);
     fill(st0 + size_t(it_slot) * a.stb, bar0 + 8 * uint32_t(it_slot), it_s);
-    if (++it_s == a.nseg) {
+    if (++it_s == nseg) {
       it_s = 0;
       ++it_t;
     }
@@ -579,13 +591,15 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
   // ---- consume cursor
   int cs = 0, ct = 0, cseg = 0;
   uint32_t cph = 0;
+  bool dead = false;  // a copy never landed: stop streaming, keep the group barriers
   for (int k = 0; k < n_items; ++k) {
     uint8_t* st = st0 + size_t(cs) * a.stb;
-    if (a.tma) {
+    if (dead) {
+    } else if (a.tma) {
       if (k + kStages - 1 < n_items) issue_next();
       const bool ok = mbar_wait(bar0 + 8 * uint32_t(cs), cph);
       if (!__all_sync(0xffffffffu, ok)) {
-        // a copy never landed: flag it, wait (bounded) for what is in flight, stop
+        // flag it, wait (bounded) for the copies still in flight, stream no more
         if (lane == 0) flag_error(a.err, kErrWaitTimeout);
         int q = cs;
         uint32_t ph = cph;
@@ -596,60 +610,72 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
           }
           mbar_wait(bar0 + 8 * uint32_t(q), ph);
         }
-        return;
+        dead = true;
       }
     } else {
       issue_next();
     }
-    const int blk0 = cseg * a.seg;
-    const int nblk = min(a.seg, a.nb - blk0);
-    const int units = nblk * F::UPB;
-    for (int u = lane; u < units; u += 32) {
-      const int b = u / F::UPB, uu = u % F::UPB;
-      typename F::X x;
-      const int col0 = (blk0 + b) * F::BE;
-      F::load_x(x, xsm + goff<FMT>(col0 / 32 + (F::UPB == 4 && FMT != NT_Q6_K ? 2 * uu : 0)), xs, col0, uu);
-      const uint8_t* bp = st + b * F::BB;
+    if (!dead) {
+      const int blk0 = pb0 + cseg * a.seg;
+      const int nblk = min(a.seg, pb1 - blk0);
+      const int units = nblk * F::UPB;
+      for (int u = lane; u < units; u += 32) {
+        const int b = u / F::UPB, uu = u % F::UPB;
+        typename F::X x;
+        const int col0 = (blk0 + b) * F::BE;
+        F::load_x(x, xsm + goff<FMT>(col0 / 32 + (F::UPB == 4 && FMT != NT_Q6_K ? 2 * uu : 0)), xs, col0, uu);
+        const uint8_t* bp = st + b * F::BB;
 #pragma unroll
-      for (int i = 0; i < R; ++i) acc[i] += F::dot(bp + i * a.segStride, uu, x);
+        for (int i = 0; i < R; ++i) acc[i] += F::dot(bp + i * a.segStride, uu, x);
+      }
     }
     __syncwarp();
-    if (cseg == a.nseg - 1) {
+    if (cseg == nseg - 1) {
       // group done: reduce across lanes, lane i holds row i
-      float mine = 0.f, other = 0.f;
+      float mine = 0.f;
 #pragma unroll
       for (int i = 0; i < R; ++i) {
         const float v = warp_sum(acc[i]);
         if (lane == i) mine = v;
-        if (a.swiglu && lane + R / 2 == i) other = v;
         acc[i] = 0.f;
       }
-      int j, nr;
-      int64_t r0;
-      locate(a, wg + int64_t(ct) * total_warps, rpg, j, r0, nr);
-      const JobDev& J = a.job[j];
-      if (a.swiglu) {
-        if (lane < nr) J.y[r0 + lane] = silu(mine) * other;
-      } else if (J.epi == kEpiPlain) {
-        if (lane < nr) J.y[r0 + lane] = J.res ? mine + J.res[r0 + lane] : mine;
-      } else {
-        // rows come in adjacent (even, odd) pairs: lane i^1 holds the partner
-        const float partner = __shfl_xor_sync(0xffffffffu, mine, 1);
-        if (lane < nr) {
-          const int64_t r = r0 + lane;
-          const int hd = a.rope.head_dim;
-          const int64_t pos = *a.rope.pos_dev;
-          const int head = int(r / hd), d = int(r % hd);
-          float out = mine;
-          if (J.epi != kEpiCache) {
-            float cs_, sn;
-            rope_cs(pos, a.rope.inv_freq[d >> 1], cs_, sn);
-            out = (d & 1) ? fmaf(partner, sn, mine * cs_) : fmaf(mine, cs_, -partner * sn);
+      if (KS > 1) {
+        // the parts of a split group meet in shared memory (double-buffered by group parity)
+        float* xb = xchg + ((ct & 1) * slots + slot) * KS * R;
+        if (part > 0 && lane < R) xb[part * R + lane] = mine;
+        named_sync(1 + slot, 32 * KS);
+        if (part == 0 && lane < R)
+          for (int p = 1; p < KS; ++p) mine += xb[p * R + lane];
+      }
+      if (part == 0) {
+        const float other = __shfl_down_sync(0xffffffffu, mine, R / 2);  // lane i: row i + R/2
+        int j, nr;
+        int64_t r0;
+        locate(a, wg + int64_t(ct) * total_warps, rpg, j, r0, nr);
+        const JobDev& J = a.job[j];
+        if (a.swiglu) {
+          if (lane < nr) J.y[r0 + lane] = silu(mine) * other;
+        } else if (J.epi == kEpiPlain) {
+          if (lane < nr) J.y[r0 + lane] = J.res ? mine + J.res[r0 + lane] : mine;
+        } else {
+          // rows come in adjacent (even, odd) pairs: lane i^1 holds the partner
+          const float partner = __shfl_xor_sync(0xffffffffu, mine, 1);
+          if (lane < nr) {
+            const int64_t r = r0 + lane;
+            const int hd = a.rope.head_dim;
+            const int64_t pos = *a.rope.pos_dev;
+            const int head = int(r / hd), d = int(r % hd);
+            float out = mine;
+            if (J.epi != kEpiCache) {
+              float cs_, sn;
+              rope_cs(pos, a.rope.inv_freq[d >> 1], cs_, sn);
+              out = (d & 1) ? fmaf(partner, sn, mine * cs_) : fmaf(mine, cs_, -partner * sn);
+            }
+            if (J.epi == kEpiRope)
+              J.y[r] = out;
+            else
+              J.cache[(int64_t(head) * a.rope.kv_stride + pos) * hd + d] = __float2half_rn(out);
           }
-          if (J.epi == kEpiRope)
-            J.y[r] = out;
-          else
-            J.cache[(int64_t(head) * a.rope.kv_stride + pos) * hd + d] = __float2half_rn(out);
         }
       }
     }
@@ -657,7 +683,7 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
       cs = 0;
       cph ^= 1u;
     }
-    if (++cseg == a.nseg) {
+    if (++cseg == nseg) {
       cseg = 0;
       ++ct;
     }
@@ -802,6 +828,39 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
   }
   if (rope) a.rope = *rope;
   if (g == 0) return NT_OK;
+
+  // split row groups over KS warps (column parts) when there are too few
+  // groups to give every warp of every SM the same amount of work
+  int ks = 1;
+  {
+    const int64_t T = int64_t(c->num_sms) * kWarps;
+    double best = 0.0;
+    const int units = int(nb / al);  // ALIGN-block units per row
+    for (int cand : {1, 2, 4}) {
+      if (kWarps % cand || (cand > 1 && units < cand)) continue;
+      const int64_t u = g * cand;
+      const int64_t per = (u + T - 1) / T;
+      const double eff = double(u) / double(T * per);
+      if (eff > best + 0.02) {
+        best = eff;
+        ks = cand;
+      }
+    }
+  }
+  a.ks = ks;
+  if (ks == 1) {
+    a.pblk[0] = 0;
+    a.pblk[1] = int(nb);
+  } else {
+    const int units = int(nb / al);
+    for (int p = 0; p <= ks; ++p) a.pblk[p] = (p * units / ks) * al;
+    a.pblk[ks] = int(nb);
+    const int plen = a.pblk[1] - a.pblk[0];
+    if (a.seg > plen) a.seg = plen;  // a part fits one stage
+    a.merged = 0;
+    a.segStride = ((a.seg * BB + 15) / 16) * 16;
+  }
+  a.nseg = 0;  // per part, computed in the kernel
   a.njobs = njobs;
   a.x = x;
   a.norm_g = norm_g;
@@ -818,7 +877,8 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
 
   // every SM gets a CTA (fewer only when there are fewer groups than warps);
   // groups go round-robin, so warps differ by at most one group
-  int64_t grid64 = (g + kWarps - 1) / kWarps;
+  const int slots = kWarps / ks;
+  int64_t grid64 = (g + slots - 1) / slots;
   if (grid64 > c->num_sms) grid64 = c->num_sms;
   const int grid = int(grid64);
   const size_t smem = size_t(head) + size_t(kWarps) * kStages * stb + pad;

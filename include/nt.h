@@ -136,7 +136,8 @@ nt_status nt_rope_kv_append(nt_ctx* ctx, float* q_dev, const float* k_dev, const
  * for q head h, KV head g = h / (n_qh / n_kvh):
  *   out_h = softmax_j(q_h . K_g[j] / sqrt(head_dim)) . V_g[j],  j < n_pos.
  * Split over positions (flash-decoding), partials combined in the same
- * launch through context scratch.  head_dim must be 128. */
+ * launch through context scratch.  head_dim must be 128; kv_stride at most
+ * 16384 positions. */
 nt_status nt_attn_decode(nt_ctx* ctx, const float* q_dev, const void* kcache_dev, const void* vcache_dev,
                          float* out_dev, int n_qh, int n_kvh, int head_dim, int64_t n_pos, int64_t kv_stride,
                          void* stream);
@@ -164,7 +165,7 @@ nt_status nt_cos_sim(nt_ctx* ctx, const float* a_dev, const float* b_dev, int64_
 typedef struct {
   int n_layers, d_model, n_qh, n_kvh, head_dim, ffn, vocab;
   float eps, theta;
-  int64_t kv_cap;                       /* positions per (layer, KV head) in the caches */
+  int64_t kv_cap;                       /* positions per (layer, KV head) in the caches, <= 16384 */
   int fmt_q, fmt_k, fmt_v, fmt_o, fmt_gate, fmt_up, fmt_down, fmt_embd, fmt_out;
 } nt_model_desc;
 
@@ -223,9 +224,9 @@ nt_status nt_layer_skip_calibrate(nt_ctx* ctx, nt_model* model, int32_t token, i
  * error word live in one fixed 4 MiB array compiled into the library
  * (every GPU that loads the library holds it until the process exits);
  * n_kvh * S * (n_qh / n_kvh) * 130 * 4 + 512 bytes must fit in it, where
- * S = max(ceil(SMs / n_kvh), ceil(kv_stride / 128)) — e.g. 64 q heads over
- * 8 KV heads fit for kv_stride up to 16,128 positions.  Larger shapes return
- * NT_ERR_INVALID_ARG before any launch.
+ * S = min(128, max(ceil(SMs / n_kvh), ceil(kv_stride / 128))) — e.g. 64 q
+ * heads over 8 KV heads fit for kv_stride up to 16,128 positions.  Larger
+ * shapes return NT_ERR_INVALID_ARG before any launch.
  *  - The first call on a device looks up the array's device address and sets
  *    the kernel's shared-memory limit; make that first call before any stream
  *    capture.
