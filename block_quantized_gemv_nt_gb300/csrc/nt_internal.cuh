@@ -30,6 +30,7 @@ struct Ctx {
   int gemv_warps = 16;           // quant-GEMV launch shape (tuning knobs, env NT_GEMV_*)
   int gemv_stages = 2;
   int gemv_stage_max = 12288;
+  int gemv_static_smem = 2048;   // largest static shared memory of the GEMV kernels
   std::string last_error;
   std::mutex mu;
 };

@@ -699,21 +699,23 @@ cudaError_t launch_t(const Ctx* c, const GemvArgs& a, int warps, int grid, size_
   return launch_k(c, qgemv_kernel<FMT, R, 256>, dim3(grid), dim3(warps * 32), smem, st, a);
 }
 
-// dynamic shared memory a kernel may use: the opt-in limit minus its static part
+// dynamic shared memory a kernel may use: the opt-in limit minus its static
+// part; the largest static part is remembered for the launch plans
 template <typename K>
-cudaError_t allow_smem(K kernel, int optin) {
+cudaError_t allow_smem(K kernel, int optin, int* max_static) {
   cudaFuncAttributes fa{};
   cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
+  if (int(fa.sharedSizeBytes) > *max_static) *max_static = int(fa.sharedSizeBytes);
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - int(fa.sharedSizeBytes));
 }
 
 template <int FMT>
-cudaError_t configure_fmt(int smem) {
-  cudaError_t e = allow_smem(qgemv_kernel<FMT, 4, 256>, smem);
-  if (e == cudaSuccess) e = allow_smem(qgemv_kernel<FMT, 2, 256>, smem);
-  if (e == cudaSuccess) e = allow_smem(qgemv_kernel<FMT, 4, 512>, smem);
-  if (e == cudaSuccess) e = allow_smem(qgemv_kernel<FMT, 2, 512>, smem);
+cudaError_t configure_fmt(int smem, int* st) {
+  cudaError_t e = allow_smem(qgemv_kernel<FMT, 4, 256>, smem, st);
+  if (e == cudaSuccess) e = allow_smem(qgemv_kernel<FMT, 2, 256>, smem, st);
+  if (e == cudaSuccess) e = allow_smem(qgemv_kernel<FMT, 4, 512>, smem, st);
+  if (e == cudaSuccess) e = allow_smem(qgemv_kernel<FMT, 2, 512>, smem, st);
   return e;
 }
 
@@ -743,11 +745,13 @@ FmtInfo fmt_info(int fmt, int cols) {
 // creation (never during a stream capture).
 nt_status configure_gemv(Ctx* c) {
   const int smem = int(c->smem_optin);
-  cudaError_t e = configure_fmt<NT_Q8_0>(smem);
-  if (e == cudaSuccess) e = configure_fmt<NT_Q4_0>(smem);
-  if (e == cudaSuccess) e = configure_fmt<NT_Q4_K>(smem);
-  if (e == cudaSuccess) e = configure_fmt<NT_Q5_K>(smem);
-  if (e == cudaSuccess) e = configure_fmt<NT_Q6_K>(smem);
+  int st = 0;
+  cudaError_t e = configure_fmt<NT_Q8_0>(smem, &st);
+  if (e == cudaSuccess) e = configure_fmt<NT_Q4_0>(smem, &st);
+  if (e == cudaSuccess) e = configure_fmt<NT_Q4_K>(smem, &st);
+  if (e == cudaSuccess) e = configure_fmt<NT_Q5_K>(smem, &st);
+  if (e == cudaSuccess) e = configure_fmt<NT_Q6_K>(smem, &st);
+  c->gemv_static_smem = st;
   return cuda_check(c, e, "gemv shared-memory attribute");
 }
 
@@ -778,7 +782,7 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
   for (int nw = c->gemv_warps; nw >= 4 && R == 0; nw /= 2) {
     for (int ns = c->gemv_stages; ns >= 2 && R == 0; --ns) {
       head = ((fi.xbytes + 28 * ng + 8 + nw * ns * 8 + 127) / 128) * 128;
-      const long avail = long(c->smem_optin) - head - pad - 256;  // 256: static shared memory
+      const long avail = long(c->smem_optin) - head - pad - c->gemv_static_smem;
       stb = int(avail / (nw * ns)) / 16 * 16;
       if (stb > c->gemv_stage_max) stb = c->gemv_stage_max;
       if (stb < 256) continue;
