@@ -238,6 +238,60 @@ def cpu_gemv(fmt, W, x, rows, cols, algo, budget_s=10.0):
 
 
 # ---------------------------------------------------------------------------
+# Attention workload attn_<n_qh>x<n_kvh>x<n_pos>: one decode attention over an
+# f16 KV cache of n_pos positions per step, rotating over enough caches to
+# exceed 4x L2.
+def bench_attn(args, rank, world):
+    import torch
+
+    import synth
+    from block_quantized_gemv_nt_gb300 import nt
+
+    H, G, P = (int(v) for v in args.workload.split("_")[1].split("x"))
+    hd, stride = 128, P
+    ctx = nt.Context(torch.cuda.current_device())
+    kv_bytes = 2 * G * stride * hd * 2
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    ncopy = max(1, -(-4 * l2 // kv_bytes))
+    K = torch.from_numpy(synth.normal_f16(G * stride * hd, 5, 1)).cuda()
+    V = torch.from_numpy(synth.normal_f16(G * stride * hd, 5, 2)).cuda()
+    Ks = [K.clone() for _ in range(ncopy)]
+    Vs = [V.clone() for _ in range(ncopy)]
+    q = torch.from_numpy(synth.normal_f32(H * hd, 5, 3)).cuda()
+    out = torch.empty(H * hd, device="cuda")
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        for i in range(max(3, args.warmup)):
+            nt.nt_attn_decode(ctx, q, Ks[i % ncopy], Vs[i % ncopy], out, H, G, hd, P, stride)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for i in range(args.steps):
+                nt.nt_attn_decode(ctx, q, Ks[i % ncopy], Vs[i % ncopy], out, H, G, hd, P, stride)
+        g.replay()
+        st.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            clk.wait_first()
+            e0.record(st)
+            g.replay()
+            e1.record(st)
+            e1.synchronize()
+            clk.wait_one_more()
+    per = e0.elapsed_time(e1) / 1e3 / args.steps
+    gbs = kv_bytes / per / 1e9
+    peak, kind = measured_peaks()
+    ctx.sync()
+    return {"metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(per * 1e3, 6), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16 KV, f32 math", "data": "synthetic N(0,1) KV", "impl": "ours",
+            "config": {"workload": args.workload, "l2": f"rotating {ncopy} KV caches"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_kind": kind, "traffic": None,
+                         "algo_bytes_per_launch": kv_bytes},
+            "gpu_launches": args.steps, "clocks": clk.summary()}
+
+
+# ---------------------------------------------------------------------------
 # Decode workloads: the synthetic Llama shapes, one token per step
 def gemv_plan(spec):
     """The quant-GEMV launches of one decode step, in order: (fmt, [(W, rows)], cols, x-tag, norm-tag, kind)."""
@@ -513,6 +567,8 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     if args.workload.startswith("gemv"):
         line = bench_gemv(args, rank, world)
+    elif args.workload.startswith("attn"):
+        line = bench_attn(args, rank, world)
     else:
         line = bench_decode(args, rank, world)
     if rank == 0:

@@ -179,19 +179,30 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     return;
   }
 
-  // scores: warp per position, lane owns dims 4*lane .. 4*lane+3
+  // scores: warp per position, lane owns dims 4*lane .. 4*lane+3; the heads
+  // of the group are independent reductions, unrolled for ILP
   for (int j = warp; j < np; j += 8) {
     const uint2 raw = *reinterpret_cast<const uint2*>(Ks + j * kHD + 4 * lane);
     const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
     const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-    for (int h = 0; h < G; ++h) {
-      const float4 qv = *reinterpret_cast<const float4*>(qs + h * kHD + 4 * lane);
-      float d = qv.x * k01.x;
-      d = fmaf(qv.y, k01.y, d);
-      d = fmaf(qv.z, k23.x, d);
-      d = fmaf(qv.w, k23.y, d);
-      d = warp_sum(d);
-      if (lane == 0) sc[h * kMaxChunk + j] = d;
+    for (int h0 = 0; h0 < G; h0 += 8) {
+      float d[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        d[u] = 0.f;
+        if (h0 + u < G) {
+          const float4 qv = *reinterpret_cast<const float4*>(qs + (h0 + u) * kHD + 4 * lane);
+          d[u] = fmaf(qv.w, k23.y, fmaf(qv.z, k23.x, fmaf(qv.y, k01.y, qv.x * k01.x)));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) d[u] += __shfl_xor_sync(0xffffffffu, d[u], o);
+      if (lane == 0)
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (h0 + u < G) sc[(h0 + u) * kMaxChunk + j] = d[u];
     }
   }
   __syncthreads();
