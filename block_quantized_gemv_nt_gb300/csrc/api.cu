@@ -261,8 +261,13 @@ nt_status nt_attn_decode(nt_ctx* ctx, const float* q, const void* kc, const void
   NT_TRY(pre_call(ctx));
   NT_REQUIRE(q && kc && vc && out, NT_ERR_INVALID_ARG, "null pointer");
   NT_REQUIRE(head_dim == 128, NT_ERR_INVALID_ARG, "head_dim must be 128");
-  NT_REQUIRE(n_kvh > 0 && n_qh > 0 && n_qh % n_kvh == 0 && n_qh / n_kvh <= 16 && n_kvh <= 64, NT_ERR_INVALID_ARG,
-             "n_qh must be a multiple of n_kvh, group <= 16, n_kvh <= 64");
+  NT_REQUIRE(n_kvh > 0 && n_qh > 0 && n_qh % n_kvh == 0 && n_kvh <= 64, NT_ERR_INVALID_ARG,
+             "n_qh must be a multiple of n_kvh, n_kvh <= 64");
+  {
+    const int grp = n_qh / n_kvh;
+    NT_REQUIRE(grp == 1 || grp == 2 || grp == 4 || grp == 8 || grp == 16, NT_ERR_INVALID_ARG,
+               "n_qh / n_kvh must be 1, 2, 4, 8 or 16");
+  }
   NT_REQUIRE(n_pos >= 1 && n_pos <= kv_stride, NT_ERR_INVALID_ARG, "need 1 <= n_pos <= kv_stride");
   NT_REQUIRE(kv_stride <= attn_max_stride(), NT_ERR_INVALID_ARG, "kv_stride above %lld", (long long)attn_max_stride());
   NT_TRY(check_vec(ctx, q, "q"));

@@ -155,8 +155,12 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   const nt_model_desc& d = *desc;
   NT_REQUIRE(d.n_layers > 0 && d.d_model > 0 && d.ffn > 0 && d.vocab > 0, NT_ERR_INVALID_ARG, "bad dims");
   NT_REQUIRE(d.head_dim == 128, NT_ERR_INVALID_ARG, "head_dim must be 128");
-  NT_REQUIRE(d.n_kvh > 0 && d.n_qh % d.n_kvh == 0 && d.n_qh / d.n_kvh <= 16 && d.n_kvh <= 64, NT_ERR_INVALID_ARG,
-             "bad head counts");
+  NT_REQUIRE(d.n_kvh > 0 && d.n_qh % d.n_kvh == 0 && d.n_kvh <= 64, NT_ERR_INVALID_ARG, "bad head counts");
+  {
+    const int grp = d.n_qh / d.n_kvh;
+    NT_REQUIRE(grp == 1 || grp == 2 || grp == 4 || grp == 8 || grp == 16, NT_ERR_INVALID_ARG,
+               "n_qh / n_kvh must be 1, 2, 4, 8 or 16");
+  }
   NT_REQUIRE(d.kv_cap > 0 && d.eps >= 0.f && d.theta > 0.f, NT_ERR_INVALID_ARG, "bad kv_cap/eps/theta");
   NT_REQUIRE(d.kv_cap <= attn_max_stride(), NT_ERR_INVALID_ARG, "kv_cap above %lld", (long long)attn_max_stride());
   const int fm[9] = {d.fmt_q, d.fmt_k, d.fmt_v, d.fmt_o, d.fmt_gate, d.fmt_up, d.fmt_down, d.fmt_embd, d.fmt_out};

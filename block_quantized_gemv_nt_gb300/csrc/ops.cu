@@ -108,8 +108,14 @@ __global__ void rope_append_kernel(float* q, const float* k, const float* v, __h
 // grid (n_kvh, S); CTA (g, s) covers positions [s*chunk, (s+1)*chunk) of KV head
 // g for its whole group of G q heads, so K and V are read once per group.  The
 // chunk of K and of V (contiguous in the cache) arrive by two TMA bulk copies.
-// Partials (m, l, o[128]) go to scratch; the last CTA of a KV head combines.
-constexpr int kAttnThreads = 256;
+// Each of the 4 warps runs an online softmax over 32-position tiles: scores
+// with one lane per position (dims visited in a lane-rotated order so the
+// shared-memory reads of a warp hit distinct banks), P.V with one lane per 4
+// dims and the probabilities broadcast by shuffle.  The warps merge in shared
+// memory; partials (m, l, o[128]) go to scratch; the last CTA of a KV head
+// combines the S partials.
+constexpr int kAttnThreads = 128;
+constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kHD = 128;
 constexpr int kMaxGroup = 16;
 constexpr int kMaxChunk = 128;
@@ -128,21 +134,27 @@ struct AttnArgs {
   unsigned* err;
 };
 
+// shared memory: K and V chunks, q (scaled), combine weights, warp partials
 __host__ __device__ constexpr size_t attn_smem_bytes(int G) {
-  return size_t(2) * kMaxChunk * kHD * 2 + size_t(G) * kHD * 4 + size_t(G) * kMaxChunk * 4 + size_t(8) * G * kHD * 4 +
-         16;
+  return size_t(2) * kMaxChunk * kHD * 2 + size_t(G) * kHD * 4 + size_t(G) * kMaxChunk * 4 +
+         size_t(kAttnWarps) * G * (2 + kHD) * 4 + 16;
 }
 
+__device__ __forceinline__ float4 h4(uint2 raw) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <int G>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   extern __shared__ __align__(128) uint8_t asmem[];
-  const int G = a.G;
-  __half* Ks = reinterpret_cast<__half*>(asmem);                    // [kMaxChunk][128]
-  __half* Vs = Ks + kMaxChunk * kHD;                                 // [kMaxChunk][128]
-  float* qs = reinterpret_cast<float*>(Vs + kMaxChunk * kHD);        // [G][128], pre-scaled by 1/sqrt(128)
-  float* sc = qs + G * kHD;                                          // [G][kMaxChunk]
-  float* red = sc + G * kMaxChunk;                                   // [8 warps][G][128]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 8 * G * kHD);
-  __shared__ float stat[2 * kMaxGroup];
+  __half* Ks = reinterpret_cast<__half*>(asmem);                  // [kMaxChunk][128]
+  __half* Vs = Ks + kMaxChunk * kHD;                               // [kMaxChunk][128]
+  float* qs = reinterpret_cast<float*>(Vs + kMaxChunk * kHD);      // [G][128], pre-scaled by 1/sqrt(128)
+  float* wts = qs + G * kHD;                                       // [G][kMaxChunk] combine weights
+  float* wp = wts + G * kMaxChunk;                                 // [warps][G][2 + 128] warp partials
+  uint64_t* bar = reinterpret_cast<uint64_t*>(wp + kAttnWarps * G * (2 + kHD));
   __shared__ bool last;
 
   const int g = blockIdx.x, s = blockIdx.y;
@@ -179,89 +191,92 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     return;
   }
 
-  // scores: warp per position, lane owns dims 4*lane .. 4*lane+3; the heads
-  // of the group are independent reductions, unrolled for ILP
-  for (int j = warp; j < np; j += 8) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(Ks + j * kHD + 4 * lane);
-    const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-    const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-    for (int h0 = 0; h0 < G; h0 += 8) {
-      float d[8];
+  // ---- per-warp online softmax over 32-position tiles
+  float m[G], l[G], o[G][4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        d[u] = 0.f;
-        if (h0 + u < G) {
-          const float4 qv = *reinterpret_cast<const float4*>(qs + (h0 + u) * kHD + 4 * lane);
-          d[u] = fmaf(qv.w, k23.y, fmaf(qv.z, k23.x, fmaf(qv.y, k01.y, qv.x * k01.x)));
+  for (int h = 0; h < G; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+    o[h][0] = o[h][1] = o[h][2] = o[h][3] = 0.f;
+  }
+  for (int t0 = 32 * warp; t0 < np; t0 += 32 * kAttnWarps) {
+    const int j = t0 + lane;
+    const bool valid = j < np;
+    float sc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) sc[h] = 0.f;
+    if (valid) {
+      const __half* krow = Ks + j * kHD;
+#pragma unroll 4
+      for (int c = 0; c < 32; ++c) {
+        const int cc = (c + lane) & 31;  // lane-rotated 4-dim chunk: distinct banks across the warp
+        const float4 k = h4(*reinterpret_cast<const uint2*>(krow + 4 * cc));
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float4 qv = *reinterpret_cast<const float4*>(qs + h * kHD + 4 * cc);
+          sc[h] = fmaf(qv.x, k.x, fmaf(qv.y, k.y, fmaf(qv.z, k.z, fmaf(qv.w, k.w, sc[h]))));
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) d[u] += __shfl_xor_sync(0xffffffffu, d[u], o);
-      if (lane == 0)
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (h0 + u < G) sc[(h0 + u) * kMaxChunk + j] = d[u];
     }
-  }
-  __syncthreads();
-
-  // local softmax statistics per head: warp h handles head h (and h + 8)
-  for (int h = warp; h < G; h += 8) {
-    float m = -FLT_MAX;
-    for (int j = lane; j < np; j += 32) m = fmaxf(m, sc[h * kMaxChunk + j]);
-    m = warp_max(m);
-    float l = 0.f;
-    for (int j = lane; j < np; j += 32) {
-      const float p = __expf(sc[h * kMaxChunk + j] - m);
-      sc[h * kMaxChunk + j] = p;
-      l += p;
-    }
-    l = warp_sum(l);
-    if (lane == 0) {
-      stat[2 * h] = np > 0 ? m : -INFINITY;
-      stat[2 * h + 1] = l;
-    }
-  }
-  __syncthreads();
-
-  // o = sum_j p_j V_j: warps split positions, lane owns 4 dims
-  float acc[kMaxGroup][4];
+    float pj[G];
 #pragma unroll
-  for (int h = 0; h < kMaxGroup; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
-  for (int j = warp; j < np; j += 8) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(Vs + j * kHD + 4 * lane);
-    const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-    const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    for (int h = 0; h < G; ++h) {
+      const float sv = valid ? sc[h] : -INFINITY;
+      const float mn = fmaxf(m[h], warp_max(sv));
+      const float corr = m[h] == -INFINITY ? 0.f : __expf(m[h] - mn);
+      pj[h] = valid ? __expf(sv - mn) : 0.f;
+      l[h] = fmaf(l[h], corr, warp_sum(pj[h]));
+      o[h][0] *= corr;
+      o[h][1] *= corr;
+      o[h][2] *= corr;
+      o[h][3] *= corr;
+      m[h] = mn;
+    }
+    const int nt = min(32, np - t0);
+    for (int jj = 0; jj < nt; ++jj) {
+      const float4 v = h4(*reinterpret_cast<const uint2*>(Vs + (t0 + jj) * kHD + 4 * lane));
 #pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h) {
-      if (h < G) {
-        const float p = sc[h * kMaxChunk + j];
-        acc[h][0] = fmaf(p, v01.x, acc[h][0]);
-        acc[h][1] = fmaf(p, v01.y, acc[h][1]);
-        acc[h][2] = fmaf(p, v23.x, acc[h][2]);
-        acc[h][3] = fmaf(p, v23.y, acc[h][3]);
+      for (int h = 0; h < G; ++h) {
+        const float p = __shfl_sync(0xffffffffu, pj[h], jj);
+        o[h][0] = fmaf(p, v.x, o[h][0]);
+        o[h][1] = fmaf(p, v.y, o[h][1]);
+        o[h][2] = fmaf(p, v.z, o[h][2]);
+        o[h][3] = fmaf(p, v.w, o[h][3]);
       }
     }
   }
+  // ---- merge the warps: (m, l, o) of each warp -> one CTA partial
+  {
+    float* mine = wp + warp * G * (2 + kHD);
 #pragma unroll
-  for (int h = 0; h < kMaxGroup; ++h)
-    if (h < G) *reinterpret_cast<float4*>(red + (warp * G + h) * kHD + 4 * lane) =
-        make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-  __syncthreads();
-
-  float* my = a.part + (int64_t(g) * a.S + s) * G * (2 + kHD);
-  for (int i = tid; i < G * kHD; i += kAttnThreads) {
-    const int h = i / kHD, d = i % kHD;
-    float t = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) t += red[(w * G + h) * kHD + d];
-    my[h * (2 + kHD) + 2 + d] = t;
+    for (int h = 0; h < G; ++h) {
+      if (lane == 0) {
+        mine[h * (2 + kHD)] = m[h];
+        mine[h * (2 + kHD) + 1] = l[h];
+      }
+      *reinterpret_cast<float4*>(mine + h * (2 + kHD) + 2 + 4 * lane) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+    }
   }
-  for (int h = tid; h < G; h += kAttnThreads) {
-    my[h * (2 + kHD)] = stat[2 * h];
-    my[h * (2 + kHD) + 1] = stat[2 * h + 1];
+  __syncthreads();
+  float* my = a.part + (int64_t(g) * a.S + s) * G * (2 + kHD);
+  for (int i = tid; i < G * (kHD + 1); i += kAttnThreads) {
+    const int h = i / (kHD + 1), d = i % (kHD + 1);  // d == kHD: the (m, l) pair
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wp[(w * G + h) * (2 + kHD)]);
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const float* pw = wp + (w * G + h) * (2 + kHD);
+      const float c = pw[0] == -INFINITY ? 0.f : __expf(pw[0] - M);
+      acc = fmaf(d < kHD ? pw[2 + d] : pw[1], c, acc);
+    }
+    if (d < kHD) {
+      my[h * (2 + kHD) + 2 + d] = acc;
+    } else {
+      my[h * (2 + kHD)] = M;
+      my[h * (2 + kHD) + 1] = acc;
+    }
   }
 
   // the last CTA of this KV head combines the S partials
@@ -274,17 +289,16 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   __syncthreads();
   if (!last) return;
   __threadfence();
-  // combine: stage every split's (max, sum) in shared memory, turn them into
-  // per-split weights w_t = e^(m_t - M) / L, then each output element is an
-  // independent sum over the splits
+  // stage every split's (max, sum) in shared memory, turn them into per-split
+  // weights w_t = e^(m_t - M) / L, then each output element is an independent
+  // sum over the splits
   const float* base = a.part + int64_t(g) * a.S * G * (2 + kHD);
-  float* wts = sc;  // [G][S] (the score buffer is free now; S <= kMaxChunk)
   for (int i = tid; i < G * a.S; i += kAttnThreads) {
     const int h = i / a.S, t = i % a.S;
     wts[h * kMaxChunk + t] = __ldcg(base + (int64_t(t) * G + h) * (2 + kHD));
   }
   __syncthreads();
-  for (int h = warp; h < G; h += 8) {
+  for (int h = warp; h < G; h += kAttnWarps) {
     float M = -INFINITY;
     for (int t = lane; t < a.S; t += 32) M = fmaxf(M, wts[h * kMaxChunk + t]);
     M = warp_max(M);
@@ -316,6 +330,18 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     a.out[(int64_t(g) * G + h) * kHD + d] = (O0 + O1) + (O2 + O3);
   }
   if (tid == 0) a.counters[g] = 0u;  // ready for the next launch
+}
+
+using AttnKernel = void (*)(AttnArgs);
+AttnKernel attn_kernel_for(int G) {
+  switch (G) {
+    case 1: return attn_kernel<1>;
+    case 2: return attn_kernel<2>;
+    case 4: return attn_kernel<4>;
+    case 8: return attn_kernel<8>;
+    case 16: return attn_kernel<16>;
+    default: return nullptr;
+  }
 }
 
 // ---- softmax (standalone) --------------------------------------------------------
@@ -480,17 +506,26 @@ nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, floa
   a.counters = counters;
   a.err = c->err_flag;
   const size_t smem = attn_smem_bytes(a.G);
-  return cuda_check(c, launch_k(c, attn_kernel, dim3(n_kvh, S), dim3(kAttnThreads), smem, st, a),
-                    "attention launch");
+  AttnKernel k = attn_kernel_for(a.G);
+  if (!k) return set_err(c, NT_ERR_INVALID_ARG, "attention: group size %d not in {1,2,4,8,16}", a.G);
+  return cuda_check(c, launch_k(c, k, dim3(n_kvh, S), dim3(kAttnThreads), smem, st, a), "attention launch");
+}
+
+cudaError_t configure_attn(size_t optin) {
+  for (int G : {1, 2, 4, 8, 16}) {
+    const size_t smem = attn_smem_bytes(G);
+    AttnKernel k = attn_kernel_for(G);
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, k);
+    if (e == cudaSuccess && smem + fa.sharedSizeBytes > optin) e = cudaErrorInvalidValue;
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 nt_status configure_ops(Ctx* c) {
-  const size_t smem = attn_smem_bytes(kMaxGroup);
-  cudaFuncAttributes fa{};
-  cudaError_t e = cudaFuncGetAttributes(&fa, attn_kernel);
-  if (e == cudaSuccess && smem + fa.sharedSizeBytes > c->smem_optin) e = cudaErrorInvalidValue;
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  return cuda_check(c, e, "attention shared-memory attribute");
+  return cuda_check(c, configure_attn(c->smem_optin), "attention shared-memory attribute");
 }
 
 __global__ void inv_freq_kernel(double* out, int head_dim, float theta) {
@@ -560,7 +595,7 @@ extern "C" nt_status nt_attn_decode_static(const float* q, const void* kc, const
   using namespace nt;
   if (!q || !kc || !vc || !out) return NT_ERR_INVALID_ARG;
   if (head_dim != kHD) return NT_ERR_INVALID_ARG;
-  if (n_kvh <= 0 || n_qh <= 0 || n_qh % n_kvh || n_qh / n_kvh > kMaxGroup || n_kvh > 64) return NT_ERR_INVALID_ARG;
+  if (n_kvh <= 0 || n_qh <= 0 || n_qh % n_kvh || n_kvh > 64 || !attn_kernel_for(n_qh / n_kvh)) return NT_ERR_INVALID_ARG;
   if (n_pos < 1 || n_pos > kv_stride) return NT_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(kc, 16) || !aligned(vc, 16)) return NT_ERR_ALIGNMENT;
   int dev = 0;
@@ -580,11 +615,7 @@ extern "C" nt_status nt_attn_decode_static(const float* q, const void* kc, const
       if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
           cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return NT_ERR_CUDA;
-      const size_t smem = attn_smem_bytes(kMaxGroup);
-      cudaFuncAttributes fa{};
-      if (cudaFuncGetAttributes(&fa, attn_kernel) != cudaSuccess || smem + fa.sharedSizeBytes > size_t(optin) ||
-          cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
-        return NT_ERR_CUDA;
+      if (configure_attn(size_t(optin)) != cudaSuccess) return NT_ERR_CUDA;
       sd->scratch = static_cast<unsigned char*>(ptr);
       sd->num_sms = sms;
       sd->ready = true;
@@ -615,7 +646,9 @@ extern "C" nt_status nt_attn_decode_static(const float* q, const void* kc, const
   a.part = reinterpret_cast<float*>(sd->scratch + kAttnStaticPart);
   a.counters = reinterpret_cast<unsigned*>(sd->scratch + kAttnStaticCounters);
   a.err = reinterpret_cast<unsigned*>(sd->scratch + kAttnStaticErr);
-  attn_kernel<<<dim3(n_kvh, S), kAttnThreads, attn_smem_bytes(a.G), st>>>(a);
+  AttnKernel k = attn_kernel_for(a.G);
+  if (!k) return NT_ERR_INVALID_ARG;
+  k<<<dim3(n_kvh, S), kAttnThreads, attn_smem_bytes(a.G), st>>>(a);
   return cudaGetLastError() == cudaSuccess ? NT_OK : NT_ERR_CUDA;
 }
 

@@ -136,8 +136,8 @@ nt_status nt_rope_kv_append(nt_ctx* ctx, float* q_dev, const float* k_dev, const
  * for q head h, KV head g = h / (n_qh / n_kvh):
  *   out_h = softmax_j(q_h . K_g[j] / sqrt(head_dim)) . V_g[j],  j < n_pos.
  * Split over positions (flash-decoding), partials combined in the same
- * launch through context scratch.  head_dim must be 128; kv_stride at most
- * 16384 positions. */
+ * launch through context scratch.  head_dim must be 128, n_qh / n_kvh one of
+ * 1, 2, 4, 8, 16, kv_stride at most 16384 positions. */
 nt_status nt_attn_decode(nt_ctx* ctx, const float* q_dev, const void* kcache_dev, const void* vcache_dev,
                          float* out_dev, int n_qh, int n_kvh, int head_dim, int64_t n_pos, int64_t kv_stride,
                          void* stream);
