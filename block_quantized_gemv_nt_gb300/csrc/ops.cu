@@ -134,10 +134,14 @@ struct AttnArgs {
   unsigned* err;
 };
 
+// a warp partial row in shared memory: o[128] (16-byte aligned), then m, l, 2 pad
+constexpr int kWpStride = kHD + 4;
+constexpr int kWpM = kHD, kWpL = kHD + 1;
+
 // shared memory: K and V chunks, q (scaled), combine weights, warp partials
 __host__ __device__ constexpr size_t attn_smem_bytes(int G) {
   return size_t(2) * kMaxChunk * kHD * 2 + size_t(G) * kHD * 4 + size_t(G) * kMaxChunk * 4 +
-         size_t(kAttnWarps) * G * (2 + kHD) * 4 + 16;
+         size_t(kAttnWarps) * G * kWpStride * 4 + 16;
 }
 
 __device__ __forceinline__ float4 h4(uint2 raw) {
@@ -153,8 +157,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   __half* Vs = Ks + kMaxChunk * kHD;                               // [kMaxChunk][128]
   float* qs = reinterpret_cast<float*>(Vs + kMaxChunk * kHD);      // [G][128], pre-scaled by 1/sqrt(128)
   float* wts = qs + G * kHD;                                       // [G][kMaxChunk] combine weights
-  float* wp = wts + G * kMaxChunk;                                 // [warps][G][2 + 128] warp partials
-  uint64_t* bar = reinterpret_cast<uint64_t*>(wp + kAttnWarps * G * (2 + kHD));
+  float* wp = wts + G * kMaxChunk;                                 // [warps][G][kWpStride] warp partials
+  uint64_t* bar = reinterpret_cast<uint64_t*>(wp + kAttnWarps * G * kWpStride);
   __shared__ bool last;
 
   const int g = blockIdx.x, s = blockIdx.y;
@@ -247,14 +251,14 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   }
   // ---- merge the warps: (m, l, o) of each warp -> one CTA partial
   {
-    float* mine = wp + warp * G * (2 + kHD);
+    float* mine = wp + warp * G * kWpStride;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       if (lane == 0) {
-        mine[h * (2 + kHD)] = m[h];
-        mine[h * (2 + kHD) + 1] = l[h];
+        mine[h * kWpStride + kWpM] = m[h];
+        mine[h * kWpStride + kWpL] = l[h];
       }
-      *reinterpret_cast<float4*>(mine + h * (2 + kHD) + 2 + 4 * lane) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+      *reinterpret_cast<float4*>(mine + h * kWpStride + 4 * lane) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
     }
   }
   __syncthreads();
@@ -263,13 +267,13 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     const int h = i / (kHD + 1), d = i % (kHD + 1);  // d == kHD: the (m, l) pair
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wp[(w * G + h) * (2 + kHD)]);
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wp[(w * G + h) * kWpStride + kWpM]);
     float acc = 0.f;
 #pragma unroll
     for (int w = 0; w < kAttnWarps; ++w) {
-      const float* pw = wp + (w * G + h) * (2 + kHD);
-      const float c = pw[0] == -INFINITY ? 0.f : __expf(pw[0] - M);
-      acc = fmaf(d < kHD ? pw[2 + d] : pw[1], c, acc);
+      const float* pw = wp + (w * G + h) * kWpStride;
+      const float c = pw[kWpM] == -INFINITY ? 0.f : __expf(pw[kWpM] - M);
+      acc = fmaf(d < kHD ? pw[d] : pw[kWpL], c, acc);
     }
     if (d < kHD) {
       my[h * (2 + kHD) + 2 + d] = acc;
