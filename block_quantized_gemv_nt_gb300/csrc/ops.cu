@@ -163,13 +163,18 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
 
   const int g = blockIdx.x, s = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait();
   pdl_trigger();
+  // In the decode step (pos_dev set) the cached positions before pos were
+  // written by earlier tokens and are stable, so their K/V chunk streams in
+  // before waiting for the kernel that writes q and position pos.  Called
+  // standalone, everything waits: the caller may have just written the cache.
+  if (!a.pos_dev) pdl_wait();
   const int64_t n_pos = a.pos_dev ? *a.pos_dev + 1 : a.n_pos;
   const int64_t chunk = (n_pos + a.S - 1) / a.S;
   const int64_t p0 = int64_t(s) * chunk;
   const int64_t p1 = min(n_pos, p0 + chunk);
   const int np = p1 > p0 ? int(p1 - p0) : 0;
+  const int np_early = a.pos_dev ? max(0, int(min(p1, n_pos - 1) - p0)) : np;  // positions safe before the wait
   const __half* Kg = a.K + int64_t(g) * a.kv_stride * kHD;
   const __half* Vg = a.V + int64_t(g) * a.kv_stride * kHD;
   const uint32_t b = smem_u32(bar);
@@ -178,11 +183,23 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     mbar_init(b, 1);
     fence_barrier_init();
     if (np > 0) {
-      const uint32_t bytes = uint32_t(np) * kHD * 2;
-      mbar_arrive_expect_tx(b, 2 * bytes);
+      mbar_arrive_expect_tx(b, uint32_t(np) * kHD * 2 * 2);
+      if (np_early > 0) {
+        const uint32_t bytes = uint32_t(np_early) * kHD * 2;
+        const uint64_t pol = policy_evict_first();
+        bulk_g2s(smem_u32(Ks), Kg + p0 * kHD, bytes, b, pol);
+        bulk_g2s(smem_u32(Vs), Vg + p0 * kHD, bytes, b, pol);
+      }
+    }
+  }
+  if (a.pos_dev) {
+    pdl_wait();
+    if (tid == 0 && np > np_early) {
+      // the rest (the new position pos) after the producer has finished
+      const uint32_t off = uint32_t(np_early) * kHD, bytes = uint32_t(np - np_early) * kHD * 2;
       const uint64_t pol = policy_evict_first();
-      bulk_g2s(smem_u32(Ks), Kg + p0 * kHD, bytes, b, pol);
-      bulk_g2s(smem_u32(Vs), Vg + p0 * kHD, bytes, b, pol);
+      bulk_g2s(smem_u32(Ks + off), Kg + (p0 + np_early) * kHD, bytes, b, pol);
+      bulk_g2s(smem_u32(Vs + off), Vg + (p0 + np_early) * kHD, bytes, b, pol);
     }
   }
   const float scale = rsqrtf(float(kHD));
