@@ -16,7 +16,8 @@
 
 namespace nt {
 
-constexpr int kMaxSpin = 1 << 22;   // iteration cap of every device-side wait
+constexpr int kMaxSpin = 1 << 16;   // iteration cap of every device-side wait
+constexpr unsigned kWaitHintNs = 50000;  // each try_wait may sleep this long (cap ~3 s in all)
 constexpr unsigned kErrWaitTimeout = 1u;
 
 struct Ctx {
@@ -76,10 +77,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kWaitHintNs)
         : "memory");
     if (ok) return true;
   }

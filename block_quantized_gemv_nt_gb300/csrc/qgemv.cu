@@ -78,12 +78,13 @@ NT_DP4A(dp4_ss, "s32", "s32")
 NT_DP4A(dp4_us, "u32", "s32")
 #undef NT_DP4A
 
-// N little-endian words from a 2-byte-aligned shared address
+// N little-endian words from a 2-byte-aligned shared address (the aligned
+// base is formed from p itself so the loads stay shared-memory loads)
 template <int N>
 __device__ __forceinline__ void lds_a2(const uint8_t* p, uint32_t* w) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  const uint32_t* b = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-  const uint32_t sh = uint32_t(a & 3) * 8;
+  const uint32_t mis = smem_u32(p) & 3u;
+  const uint32_t* b = reinterpret_cast<const uint32_t*>(p - mis);
+  const uint32_t sh = mis * 8;
   uint32_t t[N + 1];
 #pragma unroll
   for (int i = 0; i <= N; ++i) t[i] = b[i];
