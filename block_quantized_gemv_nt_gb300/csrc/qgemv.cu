@@ -505,15 +505,39 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
   pdl_trigger();
   pdl_wait();
 
-  // ---- prologue: x (optionally RMS-normalised) -> 24-bit fixed point per 32-column group
+  // ---- prologue: x (optionally RMS-normalised) -> 24-bit fixed point per 32-column group.
+  // 8 lanes per group of 32 columns, 4 columns per lane; a warp covers 4 groups
+  // per pass.  All of a lane's x loads are issued first (one memory round
+  // trip), the RMSNorm sum of squares comes from the same registers.
   {
     __shared__ float red[kMaxWarps];
+    constexpr int kPF = 16;  // passes held in registers
+    const int sub = lane & 7;
+    const int pass_stride = nwarps * 4;
+    const int npass = (ng - warp * 4 + pass_stride - 1) / pass_stride;  // passes of this warp (may be <= 0)
+    const bool whole = (ng + pass_stride - 1) / pass_stride <= kPF;      // CTA-uniform: all of x in registers
+    float4 v[kPF];
+    auto load_passes = [&](int p0) {
+#pragma unroll
+      for (int k = 0; k < kPF; ++k) {
+        const int grp = warp * 4 + (p0 + k) * pass_stride + (lane >> 3);
+        v[k] = (p0 + k < npass && grp < ng) ? *reinterpret_cast<const float4*>(a.x + 32 * grp + 4 * sub)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    };
+    if (whole) load_passes(0);
     float inv = 1.f;
     if (a.norm_g) {
       float ss = 0.f;
-      for (int i = tid * 4; i < a.cols; i += blockDim.x * 4) {
-        const float4 v = *reinterpret_cast<const float4*>(a.x + i);
-        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+      if (whole) {
+#pragma unroll
+        for (int k = 0; k < kPF; ++k)
+          ss = fmaf(v[k].x, v[k].x, fmaf(v[k].y, v[k].y, fmaf(v[k].z, v[k].z, fmaf(v[k].w, v[k].w, ss))));
+      } else {
+        for (int i = tid * 4; i < a.cols; i += blockDim.x * 4) {
+          const float4 t = *reinterpret_cast<const float4*>(a.x + i);
+          ss = fmaf(t.x, t.x, fmaf(t.y, t.y, fmaf(t.z, t.z, fmaf(t.w, t.w, ss))));
+        }
       }
       ss = warp_sum(ss);
       if (lane == 0) red[warp] = ss;
@@ -522,62 +546,62 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
       for (int w = 0; w < nwarps; ++w) tot += red[w];
       inv = rsqrtf(tot / float(a.cols) + a.eps);
     }
-    // 8 lanes per group of 32 columns, 4 columns per lane
-    for (int base = warp * 4; base < ng; base += nwarps * 4) {
-      const int grp = base + (lane >> 3), sub = lane & 7;
-      const bool live = grp < ng;
-      const int col = 32 * grp + 4 * sub;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (live) {
-        v = *reinterpret_cast<const float4*>(a.x + col);
-        if (a.norm_g) {
+    for (int p0 = 0; p0 < npass; p0 += kPF) {
+      if (!whole) load_passes(p0);
+#pragma unroll
+      for (int k = 0; k < kPF; ++k) {
+        if (p0 + k >= npass) break;  // warp-uniform
+        const int grp = warp * 4 + (p0 + k) * pass_stride + (lane >> 3);
+        const bool live = grp < ng;
+        const int col = 32 * grp + 4 * sub;
+        float4 x4 = v[k];
+        if (a.norm_g && live) {
           const float4 g = *reinterpret_cast<const float4*>(a.norm_g + col);
-          v.x = v.x * inv * g.x;
-          v.y = v.y * inv * g.y;
-          v.z = v.z * inv * g.z;
-          v.w = v.w * inv * g.w;
+          x4.x = x4.x * inv * g.x;
+          x4.y = x4.y * inv * g.y;
+          x4.z = x4.z * inv * g.z;
+          x4.w = x4.w * inv * g.w;
         }
-      }
-      float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-      int e = 0;
-      if (m > 0.f) frexpf(m, &e);  // m = f * 2^e, f in [0.5, 1)
-      const int sh = 23 - e;       // max |x| * 2^sh < 2^23
-      constexpr int kLim = (1 << 23) - 1;
-      const int q[4] = {max(-kLim, min(kLim, __float2int_rn(ldexpf(v.x, sh)))),
-                        max(-kLim, min(kLim, __float2int_rn(ldexpf(v.y, sh)))),
-                        max(-kLim, min(kLim, __float2int_rn(ldexpf(v.z, sh)))),
-                        max(-kLim, min(kLim, __float2int_rn(ldexpf(v.w, sh))))};
-      uint32_t pw[3] = {0u, 0u, 0u};
-      int ps[3] = {0, 0, 0};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int b0 = q[c] & 255, b1 = (q[c] >> 8) & 255, b2 = q[c] >> 16;  // b2 signed
-        pw[0] |= uint32_t(b0) << (8 * c);
-        pw[1] |= uint32_t(b1) << (8 * c);
-        pw[2] |= (uint32_t(b2) & 255u) << (8 * c);
-        ps[0] += b0;
-        ps[1] += b1;
-        ps[2] += b2;
-      }
-#pragma unroll
-      for (int k = 0; k < 3; ++k) {
-        ps[k] += __shfl_xor_sync(0xffffffffu, ps[k], 1);
-        ps[k] += __shfl_xor_sync(0xffffffffu, ps[k], 2);
-      }
-      if (live) {
-        uint8_t* gp = xsm + goff<FMT>(grp) + 4 * sub;
-#pragma unroll
-        for (int k = 0; k < 3; ++k) *reinterpret_cast<uint32_t*>(gp + 32 * k) = pw[k];
-        if ((sub & 3) == 0) {
-          int* dst = psum + 3 * (2 * grp + (sub >> 2));
-          dst[0] = ps[0];
-          dst[1] = ps[1];
-          dst[2] = ps[2];
+        float m = fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w)));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        // m = f * 2^e with f in [0.5, 1): e from the exponent field; scale = 2^(23 - e)
+        const int e = int((__float_as_uint(m) >> 23) & 0xFFu) - 126;
+        const int sh = min(126, max(-126, 23 - e));
+        const float scl = __uint_as_float(uint32_t(127 + sh) << 23);
+        constexpr int kLim = (1 << 23) - 1;
+        const int q0 = max(-kLim, min(kLim, __float2int_rn(x4.x * scl)));
+        const int q1 = max(-kLim, min(kLim, __float2int_rn(x4.y * scl)));
+        const int q2 = max(-kLim, min(kLim, __float2int_rn(x4.z * scl)));
+        const int q3 = max(-kLim, min(kLim, __float2int_rn(x4.w * scl)));
+        // byte planes: plane k holds byte k of the four 24-bit values
+        const uint32_t lo01 = __byte_perm(q0, q1, 0x5410), lo23 = __byte_perm(q2, q3, 0x5410);  // bytes 0,1 of each
+        const uint32_t hi01 = __byte_perm(q0, q1, 0x7632), hi23 = __byte_perm(q2, q3, 0x7632);  // bytes 2,3 of each
+        const uint32_t pw0 = __byte_perm(lo01, lo23, 0x6420);
+        const uint32_t pw1 = __byte_perm(lo01, lo23, 0x7531);
+        const uint32_t pw2 = __byte_perm(hi01, hi23, 0x6420);
+        int ps0 = __dp4a(pw0, 0x01010101u, 0u), ps1 = __dp4a(pw1, 0x01010101u, 0u);
+        int ps2 = __dp4a(int(pw2), 0x01010101, 0);  // plane 2 is signed
+        ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
+        ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
+        ps2 += __shfl_xor_sync(0xffffffffu, ps2, 1);
+        ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
+        ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
+        ps2 += __shfl_xor_sync(0xffffffffu, ps2, 2);
+        if (live) {
+          uint8_t* gp = xsm + goff<FMT>(grp) + 4 * sub;
+          *reinterpret_cast<uint32_t*>(gp) = pw0;
+          *reinterpret_cast<uint32_t*>(gp + 32) = pw1;
+          *reinterpret_cast<uint32_t*>(gp + 64) = pw2;
+          if ((sub & 3) == 0) {
+            int* dst = psum + 3 * (2 * grp + (sub >> 2));
+            dst[0] = ps0;
+            dst[1] = ps1;
+            dst[2] = ps2;
+          }
+          if (sub == 0) gscale[grp] = __uint_as_float(uint32_t(127 - sh) << 23);
         }
-        if (sub == 0) gscale[grp] = ldexpf(1.0f, -sh);
       }
     }
     __syncthreads();
