@@ -6,11 +6,12 @@
 // similarity ("Performances et structure de cache").
 //
 // GB300 shape of the step: per layer four quant-GEMV launches (Q/K/V with the
-// attention RMSNorm fused in front, O with the residual add, gate/up with the
-// FFN RMSNorm in front and SwiGLU behind, down with the residual add), one
-// RoPE + KV-append kernel and one split-K attention kernel; then the LM head
-// (final RMSNorm fused) and the argmax, which also advances the device-side
-// (token, pos) state.  The whole sequence is captured once into a CUDA graph
+// attention RMSNorm fused in front and RoPE plus the f16 KV append fused
+// behind; a second launch for V when its format differs, as in Q4_K_M; O with
+// the residual add; gate/up with the FFN RMSNorm in front and SwiGLU behind;
+// down with the residual add) and one split attention kernel; then the LM
+// head (final RMSNorm fused) and the argmax, which also advances the
+// device-side (token, pos) state.  The whole sequence is captured once into a CUDA graph
 // per skip mask and replayed, so a token costs one graph launch and no host
 // round trip.
 #include <algorithm>
