@@ -293,10 +293,12 @@ def bench_attn(args, rank, world):
 
 # ---------------------------------------------------------------------------
 # Decode workloads: the synthetic Llama shapes, one token per step
-def gemv_plan(spec):
+def gemv_plan(spec, skip=None):
     """The quant-GEMV launches of one decode step, in order: (fmt, [(W, rows)], cols, x-tag, norm-tag, kind)."""
     plan = []
     for li in range(spec.n_layers):
+        if skip is not None and skip[li]:
+            continue
         f = spec.fmt
         by = {}
         for t in ("wq", "wk", "wv"):
@@ -310,13 +312,24 @@ def gemv_plan(spec):
     return plan
 
 
+def parse_decode(name):
+    """<model>[_skip<N>]: a synthetic model, optionally decoding with the N
+    layers of highest calibration cosine skipped."""
+    import synth
+    n_skip = 0
+    if "_skip" in name:
+        name, n = name.rsplit("_skip", 1)
+        n_skip = int(n)
+    return synth.model_spec(name), n_skip
+
+
 def bench_decode(args, rank, world):
     import torch
 
     import synth
     from block_quantized_gemv_nt_gb300 import engine, nt
 
-    spec = synth.model_spec(args.workload)
+    spec, n_skip = parse_decode(args.workload)
     t0 = time.perf_counter()
     hm = synth.make_host_model(spec)
     t_gen = time.perf_counter() - t0
@@ -325,10 +338,14 @@ def bench_decode(args, rank, world):
     st = torch.cuda.Stream()
     P = spec.n_prefill
     window = spec.n_gen
+    skip = None
     with torch.cuda.stream(st):
-        gm.step(spec.first_token, P, stream=st)
+        if n_skip:
+            # calibration on the first token (all layers run), then the mask is frozen
+            skip, _ = gm.calibrate(spec.first_token, P, n_skip, stream=st)
+        gm.step(spec.first_token, P, skip, stream=st)
         for _ in range(max(3, args.warmup) - 1):
-            gm.step(-1, 0, stream=st)
+            gm.step(-1, 0, skip, stream=st)
         st.synchronize()
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -338,9 +355,9 @@ def bench_decode(args, rank, world):
             e0.record(st)
             for i in range(args.steps):
                 if i % window == 0:
-                    gm.step(spec.first_token, P, stream=st)      # restart the 128-token window
+                    gm.step(spec.first_token, P, skip, stream=st)  # restart the generation window
                 else:
-                    gm.step(-1, 0, stream=st)
+                    gm.step(-1, 0, skip, stream=st)
             e1.record(st)
             e1.synchronize()
             clk.wait_one_more()
@@ -349,7 +366,7 @@ def bench_decode(args, rank, world):
     tok_s = args.steps / (ms / 1e3)
 
     # the step's quant-GEMV launches, same arguments, timed on their own (dominant kernel)
-    plan = gemv_plan(spec)
+    plan = gemv_plan(spec, skip)
     W = lambda li, t: gm.out if li < 0 else gm.layers[li][t]  # noqa: E731
     norm = lambda tag: None if tag is None else (gm.out_norm if tag[1] < 0 else gm.layers[tag[1]][tag[0]])  # noqa
     xbuf = {"x": torch.randn(spec.d_model, device="cuda"), "ao": torch.randn(spec.n_qh * spec.head_dim, device="cuda"),
@@ -407,7 +424,7 @@ def bench_decode(args, rank, world):
         st.synchronize()
         h0 = time.perf_counter()
         for i in range(n_e2e):
-            gm.step(tok, pos, stream=st)
+            gm.step(tok, pos, skip, stream=st)
             logits_h.copy_(gm.logits, non_blocking=True)
             tok_h.copy_(gm.next_token, non_blocking=True)
             st.synchronize()
@@ -416,14 +433,16 @@ def bench_decode(args, rank, world):
     e2e_s = max_over_ranks(e2e_s, world)
     ctx.sync()
 
-    per_step_bytes = step_bytes(spec)
-    kernels_per_step = 2 + spec.n_layers * (5 + len({spec.fmt[t] for t in ("wq", "wk", "wv")})) + 1
+    per_step_bytes = step_bytes(spec, skip)
+    n_exec = spec.n_layers - (int(np.sum(skip)) if skip is not None else 0)
+    kernels_per_step = 2 + n_exec * (4 + len({spec.fmt[t] for t in ("wq", "wk", "wv")})) + 1
     line = {
         "metric": METRIC, "value": round(tok_s * world, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32 (block-quantized weights, f16 KV)",
         "data": "synthetic: random weights of the named shape, seeded", "impl": "ours",
-        "config": {"workload": args.workload, "layers": spec.n_layers, "d_model": spec.d_model, "ffn": spec.ffn,
+        "config": {"workload": args.workload, "layers": spec.n_layers, "layers_executed": n_exec,
+                   "d_model": spec.d_model, "ffn": spec.ffn,
                    "vocab": spec.vocab, "kv_prefill": P, "batch": 1, "seed": spec.seed,
                    "weights": {k: synth.FMT_NAMES[v] for k, v in spec.fmt.items()},
                    "l2": f"inputs larger than L2 ({per_step_bytes / 1e9:.2f} GB read per token)",
@@ -442,36 +461,38 @@ def bench_decode(args, rank, world):
         "host_generation_s": round(t_gen, 1),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_decode(spec, hm, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cpu_decode(spec, hm, budget_s=args.cpu_budget, skip=skip)
     gm.close()
     return line
 
 
-def step_bytes(spec):
+def step_bytes(spec, skip=None):
     """Algorithmic HBM bytes of one decode token: every executed weight byte once,
-    the KV cache read (mean context of the window) and written, activations ignored
-    (they stay in L2)."""
+    the KV cache of the executed layers read (mean context of the window) and
+    written, activations ignored (they stay in L2)."""
     import synth
-    w = spec.layer_bytes() * spec.n_layers
+    n_exec = spec.n_layers - (int(np.sum(skip)) if skip is not None else 0)
+    w = spec.layer_bytes() * n_exec
     r, c = spec.tensor_shape("out")
     w += r * synth.row_bytes(spec.fmt["out"], c)
     w += synth.row_bytes(spec.fmt["embd"], spec.d_model)
     ctxlen = spec.n_prefill + spec.n_gen / 2
-    kv = spec.n_layers * 2 * spec.n_kvh * spec.head_dim * 2 * (ctxlen + 1)
+    kv = n_exec * 2 * spec.n_kvh * spec.head_dim * 2 * (ctxlen + 1)
     return int(w + kv)
 
 
-def cpu_decode(spec, hm, budget_s=15.0):
+def cpu_decode(spec, hm, budget_s=15.0, skip=None):
     import oracle
     om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
     tok, pos, n = spec.first_token, spec.n_prefill, 0
     t0 = time.perf_counter()
     while n == 0 or time.perf_counter() - t0 < budget_s:
-        logits = om.step(tok, pos)
+        logits = om.step(tok, pos, skip)
         tok, pos, n = int(np.argmax(logits)), pos + 1, n + 1
     dt = time.perf_counter() - t0
+    what = "the full model" if skip is None else f"the model with {int(np.sum(skip))} layers skipped"
     return {"value": round(n / dt, 4), "unit": "tok/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} greedy oracle decode steps of the full model in {dt:.1f} s"}
+            "sample": f"{n} greedy oracle decode steps of {what} in {dt:.1f} s"}
 
 
 # ---------------------------------------------------------------------------
@@ -517,17 +538,22 @@ def reference_arm(args, rank, world):
                 "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                                  "sample": f"{args.steps} full oracle GEMVs"},
                 "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    spec = synth.model_spec(args.workload)
+    spec, n_skip = parse_decode(args.workload)
     hm = synth.make_host_model(spec)
     import oracle
     om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
     tok, pos = spec.first_token, spec.n_prefill
+    skip = None
+    if n_skip:
+        # calibration step (all layers), then the frozen mask
+        _, cos_l = om.step(tok, pos, want_cos=True)
+        skip = oracle.layer_skip_select(cos_l, n_skip)
     for _ in range(max(0, min(args.warmup, 1))):
-        om.step(tok, pos)
+        om.step(tok, pos, skip)
     t0 = time.perf_counter()
     n = max(1, min(args.steps, args.ref_max_steps))
     for _ in range(n):
-        logits = om.step(tok, pos)
+        logits = om.step(tok, pos, skip)
         tok, pos = int(np.argmax(logits)), pos + 1
     dt = (time.perf_counter() - t0) / n
     v = round(1.0 / dt, 4)

@@ -138,3 +138,37 @@ def test_decode_llama8b_q8_0_full_size(ctx):
     greedy steps at full size against the oracle."""
     worst, agree = _run(ctx, "llama8b_q8_0", 2)
     assert worst <= 2e-2 and agree == 2
+
+
+@pytest.mark.slow
+def test_decode_llama70b_q4_k_m_full_size(ctx):
+    """The 70B Q4_K_M workload (seed 2, 4096 prefilled positions, attn_v and
+    ffn_down in Q6_K): two greedy steps at full size against the oracle; then
+    the 20-of-80 layer skip: calibration cosines against the oracle's, the
+    mask from the selection rule, and one masked step against the oracle
+    running that mask."""
+    from block_quantized_gemv_nt_gb300 import engine
+    spec = synth.model_spec("llama70b_q4_k_m")
+    hm = synth.make_host_model(spec)
+    om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
+    gm = engine.DeviceModel(ctx, spec, hm)
+    P = spec.n_prefill
+    tok = spec.first_token
+    for i in range(2):
+        got = gm.step(tok, P + i).cpu().numpy().astype(np.float64)
+        ref = om.step(tok, P + i)
+        assert np.max(np.abs(got - ref)) <= 2e-2 * ref.std()
+        assert int(np.argmax(got)) == int(np.argmax(ref))
+        tok = int(np.argmax(got))
+    # calibration on the next position (all layers run), then one masked step
+    mask, cos = gm.calibrate(tok, P + 2, n_skip=20)
+    ref_logits, ref_cos = om.step(tok, P + 2, want_cos=True)
+    assert np.max(np.abs(cos - ref_cos)) <= 1e-4
+    assert int(mask.sum()) == 20
+    assert np.array_equal(mask, oracle.layer_skip_select(cos.astype(np.float64), 20))
+    tok = int(np.argmax(gm.logits.cpu().numpy()))
+    got = gm.step(tok, P + 3, mask).cpu().numpy().astype(np.float64)
+    ref = om.step(tok, P + 3, mask)
+    assert np.max(np.abs(got - ref)) <= 2e-2 * ref.std()
+    assert int(np.argmax(got)) == int(np.argmax(ref))
+    gm.close()
