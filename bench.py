@@ -313,14 +313,18 @@ def gemv_plan(spec, skip=None):
 
 
 def parse_decode(name):
-    """<model>[_skip<N>]: a synthetic model, optionally decoding with the N
-    layers of highest calibration cosine skipped."""
+    """<model>[_skip<N>][_spec<K>]: a synthetic model, optionally decoding with
+    the N layers of highest calibration cosine skipped, or self-speculatively
+    with K drafted tokens per step.  Returns (spec, n_skip, k)."""
     import synth
-    n_skip = 0
+    n_skip = k = 0
+    if "_spec" in name:
+        name, n = name.rsplit("_spec", 1)
+        k = int(n)
     if "_skip" in name:
         name, n = name.rsplit("_skip", 1)
         n_skip = int(n)
-    return synth.model_spec(name), n_skip
+    return synth.model_spec(name), n_skip, k
 
 
 def bench_decode(args, rank, world):
@@ -329,7 +333,7 @@ def bench_decode(args, rank, world):
     import synth
     from block_quantized_gemv_nt_gb300 import engine, nt
 
-    spec, n_skip = parse_decode(args.workload)
+    spec, n_skip, _ = parse_decode(args.workload)
     t0 = time.perf_counter()
     hm = synth.make_host_model(spec)
     t_gen = time.perf_counter() - t0
@@ -466,6 +470,150 @@ def bench_decode(args, rank, world):
     return line
 
 
+def h2d_peak(src, nbytes, reps=5):
+    """Best pinned host -> HBM copy bandwidth (GB/s) of one nbytes copy."""
+    import torch
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.Stream()
+    best = 0.0
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(st):
+            e0.record(st)
+            dst.copy_(src[:nbytes], non_blocking=True)
+            e1.record(st)
+        e1.synchronize()
+        best = max(best, nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del dst
+    return best
+
+
+def bench_streamed(args, rank, world):
+    """Decode of a model whose layers n_resident.. stream from page-locked
+    host memory each pass; greedy, or self-speculative with k drafts (the
+    resident layers draft, all layers verify)."""
+    import torch
+
+    import synth
+    from block_quantized_gemv_nt_gb300 import engine, nt
+
+    spec, n_skip, k = parse_decode(args.workload)
+    assert n_skip == 0, "layer skip is not combined with streaming here"
+    t0 = time.perf_counter()
+    blobs = engine.HostBlobs(spec)
+    hm = synth.make_host_model(spec, out_view=blobs.view)
+    t_gen = time.perf_counter() - t0
+    ctx = nt.Context(torch.cuda.current_device())
+    gm = engine.DeviceModel(ctx, spec, hm, blobs=blobs)
+    st = torch.cuda.Stream()
+    P = spec.n_prefill
+    n_streamed = len(blobs.layers)
+    # one step emits up to k + 1 tokens: restart the window before the KV capacity runs out
+    window = max(1, spec.n_gen // (k + 1)) if k else spec.n_gen
+    counts = torch.zeros(max(1, args.steps), dtype=torch.int32, device="cuda")
+
+    def one(i, timed):
+        first = i % window == 0
+        if k:
+            _, cnt, _ = gm.spec_step(spec.first_token if first else -1, P, k, stream=st)
+            if timed:
+                counts[i:i + 1].copy_(cnt, non_blocking=True)
+        else:
+            gm.step(spec.first_token if first else -1, P, stream=st)
+
+    with torch.cuda.stream(st):
+        for i in range(max(3, args.warmup)):
+            one(i, False)
+        st.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            clk.wait_first()
+            torch.cuda.synchronize()
+            e0.record(st)
+            for i in range(args.steps):
+                one(i, True)
+            e1.record(st)
+            e1.synchronize()
+            clk.wait_one_more()
+        ms = e0.elapsed_time(e1)
+    ms = max_over_ranks(ms, world)
+    n_tok = int(counts[:args.steps].sum().item()) if k else args.steps
+    tok_s = n_tok / (ms / 1e3)
+    pass_s = ms / 1e3 / args.steps
+    link_bytes = n_streamed * blobs.nbytes          # host -> HBM bytes of one pass
+    b_h2d = h2d_peak(blobs.blob[blobs.layers[0]], blobs.nbytes)
+    link_gbs = link_bytes / pass_s / 1e9
+
+    # e2e: host-driven loop through the C ABI, results back to pinned host memory each step
+    n_e2e = min(args.steps, 4)
+    out_h = torch.empty(spec.vocab, dtype=torch.float32).pin_memory()
+    tok_h = torch.empty(8, dtype=torch.int32).pin_memory()
+    cnt_h = torch.empty(1, dtype=torch.int32).pin_memory()
+    with torch.cuda.stream(st):
+        st.synchronize()
+        tok, pos, got = spec.first_token, P, 0
+        h0 = time.perf_counter()
+        for i in range(n_e2e):
+            if k:
+                toks, cnt, _ = gm.spec_step(tok, pos, k, stream=st)
+                tok_h.copy_(toks, non_blocking=True)
+                cnt_h.copy_(cnt, non_blocking=True)
+                st.synchronize()
+                n = int(cnt_h[0])
+                tok, pos, got = int(tok_h[n - 1]), pos + n, got + n
+            else:
+                gm.step(tok, pos, stream=st)
+                out_h.copy_(gm.logits, non_blocking=True)
+                tok_h[:1].copy_(gm.next_token, non_blocking=True)
+                st.synchronize()
+                tok, pos, got = int(tok_h[0]), pos + 1, got + 1
+        e2e_s = time.perf_counter() - h0
+    e2e_tok_s = got / max_over_ranks(e2e_s, world)
+    ctx.sync()
+    hbm_w = gm.hbm_weight_bytes()
+    peak, peak_kind = measured_peaks()
+    per_pass = n_tok / args.steps
+    line = {
+        "metric": METRIC, "value": round(tok_s * world, 3), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(pass_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 (block-quantized weights, f16 KV)",
+        "data": "synthetic: random weights of the named shape, seeded", "impl": "ours",
+        "config": {"workload": args.workload, "layers": spec.n_layers, "resident_layers": spec.n_resident,
+                   "streamed_layers": n_streamed, "stream_slots": gm.n_slots, "layer_blob_bytes": blobs.nbytes,
+                   "hbm_weight_bytes": hbm_w, "d_model": spec.d_model, "ffn": spec.ffn, "vocab": spec.vocab,
+                   "kv_prefill": P, "batch": 1, "seed": spec.seed,
+                   "weights": {kk: synth.FMT_NAMES[v] for kk, v in spec.fmt.items()},
+                   "decode": f"self-speculative, k={k} drafts by the resident layers" if k else "greedy",
+                   "tokens_per_pass": round(per_pass, 3),
+                   "draft_acceptance": round((per_pass - 1) / k, 4) if k else None,
+                   "l2": f"inputs larger than L2 ({link_bytes / 1e9:.1f} GB streamed per pass)"},
+        "roofline": {"bound": "h2d", "kernel": "host-to-HBM layer copies", "achieved": round(link_gbs, 1),
+                     "peak": round(b_h2d, 1), "unit": "GB/s", "frac": round(link_gbs / b_h2d, 4),
+                     "peak_kind": "measured in this run: best pinned copy of one layer blob",
+                     "traffic": None, "algo_bytes_per_launch": link_bytes, "hbm_peak": peak},
+        "e2e": {"value": round(e2e_tok_s, 3), "unit": "tok/s", "h2d_bytes_per_step": 4,
+                "d2h_bytes_per_step": 4 * (k + 2) if k else 4 * spec.vocab + 4},
+        "gpu_launches": None,
+        "clocks": clk.summary(),
+        "host_generation_s": round(t_gen, 1),
+    }
+    n_exec = spec.n_layers
+    per_layer = 4 + len({spec.fmt[t] for t in ("wq", "wk", "wv")})
+    if k:
+        # per pass: setup, k drafts (resident layers), verify (GEMM + epilogue per GEMV, attention), accept
+        n_res = spec.n_resident
+        draft = 2 + n_res * per_layer + 1
+        verify = 1 + n_exec * (2 * (per_layer - 1) + 1) + 2 + k + 1
+        line["gpu_launches"] = args.steps * (2 + k * draft + verify)
+    else:
+        line["gpu_launches"] = args.steps * (3 + n_exec * per_layer) + (args.steps + window - 1) // window
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_decode(spec, hm, budget_s=args.cpu_budget)
+    gm.close()
+    return line
+
+
 def step_bytes(spec, skip=None):
     """Algorithmic HBM bytes of one decode token: every executed weight byte once,
     the KV cache of the executed layers read (mean context of the window) and
@@ -538,7 +686,7 @@ def reference_arm(args, rank, world):
                 "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                                  "sample": f"{args.steps} full oracle GEMVs"},
                 "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    spec, n_skip = parse_decode(args.workload)
+    spec, n_skip, _ = parse_decode(args.workload)
     hm = synth.make_host_model(spec)
     import oracle
     om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
@@ -595,6 +743,8 @@ def main():
         line = bench_gemv(args, rank, world)
     elif args.workload.startswith("attn"):
         line = bench_attn(args, rank, world)
+    elif parse_decode(args.workload)[0].n_resident >= 0:
+        line = bench_streamed(args, rank, world)
     else:
         line = bench_decode(args, rank, world)
     if rank == 0:

@@ -131,7 +131,7 @@ nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes) {
     return NT_ERR_CUDA;
   }
   c->err_flag = reinterpret_cast<unsigned*>(c->scratch + kScratchErr);
-  if (configure_gemv(c) != NT_OK || configure_ops(c) != NT_OK) {
+  if (configure_gemv(c) != NT_OK || configure_ops(c) != NT_OK || configure_gemm(c) != NT_OK) {
     g_create_error = c->last_error;
     cudaFree(c->scratch);
     delete c;
@@ -162,7 +162,9 @@ nt_status nt_ctx_sync(nt_ctx* ctx) {
   if (e != cudaSuccess) return cuda_check(ctx, e, "read device error flag");
   if (flag) {
     cudaMemset(ctx->err_flag, 0, sizeof(unsigned));
-    return set_err(ctx, NT_ERR_TIMEOUT, "a device-side bounded wait ran out (flag 0x%x)", flag);
+    if (flag & kErrWaitTimeout)
+      return set_err(ctx, NT_ERR_TIMEOUT, "a device-side bounded wait ran out (flag 0x%x)", flag);
+    return set_err(ctx, NT_ERR_INVALID_ARG, "a device-side position ran past the KV cache (flag 0x%x)", flag);
   }
   return NT_OK;
 }
@@ -205,6 +207,28 @@ nt_status nt_gemv_q(nt_ctx* ctx, int fmt, const void* W, const float* x, float* 
                     const float* residual, void* stream) {
   nt_gemv_job j{W, y, residual, rows};
   return nt_gemv_q_multi(ctx, fmt, &j, 1, x, nullptr, 0.f, cols, stream);
+}
+
+nt_status nt_gemm_q(nt_ctx* ctx, int fmt, const void* W, const float* X, float* Y, int64_t rows, int64_t cols, int M,
+                    const float* residual, const float* norm_g, float eps, void* stream) {
+  NT_TRY(pre_call(ctx));
+  NT_TRY(check_fmt_cols(ctx, fmt, cols));
+  NT_REQUIRE(M >= 1 && M <= kMaxVerify, NT_ERR_INVALID_ARG, "M must be 1..%d", kMaxVerify);
+  NT_REQUIRE(rows >= 0, NT_ERR_INVALID_ARG, "negative rows");
+  if (rows == 0) return NT_OK;
+  NT_REQUIRE(W && Y, NT_ERR_INVALID_ARG, "null W or Y");
+  NT_REQUIRE(aligned(W, 2), NT_ERR_ALIGNMENT, "W must be 2-byte aligned");
+  NT_TRY(check_vec(ctx, X, "X"));
+  NT_REQUIRE(cols % 4 == 0, NT_ERR_INVALID_ARG, "cols must be a multiple of 4");
+  NT_REQUIRE(aligned(Y, 4) && (!residual || aligned(residual, 4)), NT_ERR_ALIGNMENT,
+             "Y and residual must be 4-byte aligned");
+  if (norm_g) NT_TRY(check_vec(ctx, norm_g, "norm_g"));
+  NT_REQUIRE(ctx->scratch_bytes > kScratchGemm, NT_ERR_OOM, "the context scratch has no room for partial sums");
+  const GemmJobEx job{W, rows, Y, rows, residual, nullptr, kEpiPlain};
+  DeviceGuard g(ctx->device);
+  return launch_gemm(ctx, fmt, &job, 1, false, X, cols, M, norm_g, eps, cols, nullptr,
+                     reinterpret_cast<float*>(ctx->scratch + kScratchGemm), ctx->scratch_bytes - kScratchGemm,
+                     as_stream(stream));
 }
 
 nt_status nt_gemv_q_swiglu(nt_ctx* ctx, int fmt, const void* Wg, const void* Wu, const float* x, const float* norm_g,
@@ -256,10 +280,12 @@ nt_status nt_rope_kv_append(nt_ctx* ctx, float* q, const float* k, const float* 
                             as_stream(stream));
 }
 
-nt_status nt_attn_decode(nt_ctx* ctx, const float* q, const void* kc, const void* vc, float* out, int n_qh,
-                         int n_kvh, int head_dim, int64_t n_pos, int64_t kv_stride, void* stream) {
+namespace {
+nt_status attn_entry(nt_ctx* ctx, const float* q, const void* kc, const void* vc, float* out, int n_qh, int n_kvh,
+                     int head_dim, int64_t n_pos, int nq, int64_t kv_stride, void* stream) {
   NT_TRY(pre_call(ctx));
   NT_REQUIRE(q && kc && vc && out, NT_ERR_INVALID_ARG, "null pointer");
+  NT_REQUIRE(nq >= 1 && nq <= kMaxVerify, NT_ERR_INVALID_ARG, "n_query must be 1..%d", kMaxVerify);
   NT_REQUIRE(head_dim == 128, NT_ERR_INVALID_ARG, "head_dim must be 128");
   NT_REQUIRE(n_kvh > 0 && n_qh > 0 && n_qh % n_kvh == 0 && n_kvh <= 64, NT_ERR_INVALID_ARG,
              "n_qh must be a multiple of n_kvh, n_kvh <= 64");
@@ -268,19 +294,32 @@ nt_status nt_attn_decode(nt_ctx* ctx, const float* q, const void* kc, const void
     NT_REQUIRE(grp == 1 || grp == 2 || grp == 4 || grp == 8 || grp == 16, NT_ERR_INVALID_ARG,
                "n_qh / n_kvh must be 1, 2, 4, 8 or 16");
   }
-  NT_REQUIRE(n_pos >= 1 && n_pos <= kv_stride, NT_ERR_INVALID_ARG, "need 1 <= n_pos <= kv_stride");
+  NT_REQUIRE(n_pos >= 1 && n_pos + nq - 1 <= kv_stride, NT_ERR_INVALID_ARG,
+             "need 1 <= n_pos and n_pos + n_query - 1 <= kv_stride");
   NT_REQUIRE(kv_stride <= attn_max_stride(), NT_ERR_INVALID_ARG, "kv_stride above %lld", (long long)attn_max_stride());
   NT_TRY(check_vec(ctx, q, "q"));
   NT_TRY(check_vec(ctx, out, "out"));
   NT_REQUIRE(aligned(kc, 16) && aligned(vc, 16), NT_ERR_ALIGNMENT, "caches must be 16-byte aligned");
   const int S = attn_splits(ctx, n_kvh, kv_stride);
-  const size_t need = attn_scratch_bytes(n_qh, n_kvh, S);
-  NT_REQUIRE(kScratchAttn + need <= ctx->scratch_bytes, NT_ERR_OOM, "attention needs %zu scratch bytes", need);
-  float* part = reinterpret_cast<float*>(ctx->scratch + kScratchAttn + 64 * sizeof(unsigned));
+  const size_t need = attn_scratch_bytes(n_qh, n_kvh, S, nq);
+  NT_REQUIRE(kScratchAttn + need <= kScratchGemm && kScratchAttn + need <= ctx->scratch_bytes, NT_ERR_OOM,
+             "attention needs %zu scratch bytes", need);
+  float* part = reinterpret_cast<float*>(ctx->scratch + kScratchAttn + kAttnCounterBytes);
   unsigned* counters = reinterpret_cast<unsigned*>(ctx->scratch + kScratchAttn);
   DeviceGuard g(ctx->device);
   return launch_attn(ctx, q, kc, vc, out, n_qh, n_kvh, n_pos, nullptr, kv_stride, part, counters, S,
-                     as_stream(stream));
+                     as_stream(stream), nq);
+}
+}  // namespace
+
+nt_status nt_attn_decode(nt_ctx* ctx, const float* q, const void* kc, const void* vc, float* out, int n_qh,
+                         int n_kvh, int head_dim, int64_t n_pos, int64_t kv_stride, void* stream) {
+  return attn_entry(ctx, q, kc, vc, out, n_qh, n_kvh, head_dim, n_pos, 1, kv_stride, stream);
+}
+
+nt_status nt_attn_verify(nt_ctx* ctx, const float* q, const void* kc, const void* vc, float* out, int n_qh,
+                         int n_kvh, int head_dim, int64_t n_pos0, int n_query, int64_t kv_stride, void* stream) {
+  return attn_entry(ctx, q, kc, vc, out, n_qh, n_kvh, head_dim, n_pos0, n_query, kv_stride, stream);
 }
 
 nt_status nt_softmax(nt_ctx* ctx, const float* x, float* y, int64_t n, void* stream) {

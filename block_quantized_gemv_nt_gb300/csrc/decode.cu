@@ -1,9 +1,10 @@
 // decode.cu — the batch-1 decode step of a Llama-architecture model with
 // block-quantized weights ("ntransformer - moteur d'inférence NVMe-to-GPU…",
 // fr.news.hada.io: "Architecture et structure du code" — model/ transformer
-// composition, inference/ engine and sampler; "Fonctionnalités principales" —
-// RoPE, GQA, SwiGLU, RMSNorm, KV cache), and layer-skip calibration by cosine
-// similarity ("Performances et structure de cache").
+// composition, inference/ engine and sampler, memory/ layer streaming;
+// "Fonctionnalités principales" — RoPE, GQA, SwiGLU, RMSNorm, KV cache, SLEP
+// double-buffered streaming, self-speculative decoding), and layer-skip
+// calibration by cosine similarity ("Performances et structure de cache").
 //
 // GB300 shape of the step: per layer four quant-GEMV launches (Q/K/V with the
 // attention RMSNorm fused in front and RoPE plus the f16 KV append fused
@@ -11,9 +12,16 @@
 // the residual add; gate/up with the FFN RMSNorm in front and SwiGLU behind;
 // down with the residual add) and one split attention kernel; then the LM
 // head (final RMSNorm fused) and the argmax, which also advances the
-// device-side (token, pos) state.  The whole sequence is captured once into a CUDA graph
-// per skip mask and replayed, so a token costs one graph launch and no host
-// round trip.
+// device-side (token, pos) state.  The whole sequence is captured once into
+// a CUDA graph per skip mask and replayed, so a token costs one graph launch
+// and no host round trip.
+//
+// Streamed layers (weights in page-locked host memory) are copied into HBM
+// slots on a side stream inside the same graph, each copy overlapping the
+// compute of earlier layers.  The self-speculative step drafts k tokens with
+// the first layers, then verifies the k + 1 tokens in one pass of all layers
+// (M = k + 1 GEMMs, causal multi-query attention) and keeps the longest
+// agreeing prefix plus one token — all on the device, one graph per step.
 #include <algorithm>
 #include <cstring>
 #include <map>
@@ -42,6 +50,24 @@ struct nt_model {
   int S = 0;
   cudaStream_t cap = nullptr;
   std::map<std::string, cudaGraphExec_t> graphs;
+  // streaming: layers whose weights stay in page-locked host memory
+  std::vector<const void*> host_blob;  // per layer; null = resident
+  int n_slots = 0;
+  size_t blob_bytes = 0, blob_off[7] = {};
+  char* slots = nullptr;               // n_slots HBM slots of blob_bytes
+  std::vector<int> slot_layer;         // last layer copied into each slot
+  cudaStream_t copy_st = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaEvent_t ev_ready[8] = {}, ev_free[8] = {};
+  // self-speculative verify: up to kMaxVerify tokens per pass
+  int32_t* spec_tok = nullptr;         // [kMaxVerify]: the step's token, then the drafts
+  int64_t* spec_pos = nullptr;         // [kMaxVerify]: pos + i
+  int32_t* vtok = nullptr;             // [kMaxVerify]: argmax of each verify row
+  unsigned long long* vkey = nullptr;  // [kMaxVerify] argmax keys and counters
+  unsigned* vcnt = nullptr;
+  float *xv = nullptr, *qv = nullptr, *aov = nullptr, *hv = nullptr, *lv = nullptr, *dlogits = nullptr;
+  float* gpart = nullptr;              // verify-GEMM partial sums
+  size_t gpart_bytes = 0;
 };
 
 namespace nt {
@@ -55,23 +81,130 @@ __global__ void set_state_kernel(int32_t* tok, int64_t* pos, int32_t t, int64_t 
 
 size_t up256(size_t n) { return (n + 255) / 256 * 256; }
 
-struct Launch {
+constexpr int kMaxSlots = 8;
+
+// rows x cols of the seven layer matrices, in blob order wq wk wv wo wg wu wd
+void layer_shapes(const nt_model_desc& d, int64_t rows[7], int64_t cols[7], int fmt[7]) {
+  const int64_t nq = int64_t(d.n_qh) * d.head_dim, nkv = int64_t(d.n_kvh) * d.head_dim;
+  const int64_t r[7] = {nq, nkv, nkv, d.d_model, d.ffn, d.ffn, d.d_model};
+  const int64_t c[7] = {d.d_model, d.d_model, d.d_model, nq, d.d_model, d.d_model, d.ffn};
+  const int f[7] = {d.fmt_q, d.fmt_k, d.fmt_v, d.fmt_o, d.fmt_gate, d.fmt_up, d.fmt_down};
+  for (int i = 0; i < 7; ++i) {
+    rows[i] = r[i];
+    cols[i] = c[i];
+    fmt[i] = f[i];
+  }
+}
+
+void blob_layout(const nt_model_desc& d, size_t off[7], size_t* total) {
+  int64_t rows[7], cols[7];
+  int fmt[7];
+  layer_shapes(d, rows, cols, fmt);
+  size_t o = 0;
+  for (int i = 0; i < 7; ++i) {
+    off[i] = o;
+    o += up256(size_t(rows[i]) * size_t(cols[i] / block_elems(fmt[i])) * size_t(block_bytes(fmt[i])));
+  }
+  *total = o;
+}
+
+char* slot_ptr(const nt_model* m, int slot) { return m->slots + size_t(slot) * m->blob_bytes; }
+
+// the layer's weight pointers when its blob sits in `slot`
+void bind_slot(const nt_model* m, int slot, nt_layer_ptrs& L) {
+  const char* b = slot_ptr(m, slot);
+  const void** w[7] = {&L.wq, &L.wk, &L.wv, &L.wo, &L.wg, &L.wu, &L.wd};
+  for (int i = 0; i < 7; ++i) *w[i] = b + m->blob_off[i];
+}
+
+// the copy step of the streaming engine: layer blob host -> HBM slot on st
+nt_status copy_layer(Ctx* c, nt_model* m, int layer, const void* src, int slot, cudaStream_t st) {
+  nt_status s = cuda_check(c, cudaMemcpyAsync(slot_ptr(m, slot), src, m->blob_bytes, cudaMemcpyHostToDevice, st),
+                           "stream layer copy");
+  if (!s) m->slot_layer[slot] = layer;
+  return s;
+}
+
+// Streaming schedule of one pass over the layers: the executed streamed
+// layers, in order, go through slot i % n_slots on the copy stream; the
+// first n_slots copies start with the pass, each later copy waits for the
+// compute of the layer that last used its slot, and each streamed layer's
+// compute waits for its copy.  Works eagerly and under stream capture (the
+// copy stream joins the capture through the fork event).
+struct Streamer {
   Ctx* c;
   nt_model* m;
   cudaStream_t st;
+  std::vector<int> sl;
+  int si = 0;  // ordinal of the next streamed layer
+
+  nt_status copy(int i) {
+    const int NS = m->n_slots, slot = i % NS;
+    nt_status r = NT_OK;
+    if (i >= NS) r = cuda_check(c, cudaStreamWaitEvent(m->copy_st, m->ev_free[slot], 0), "copy waits for its slot");
+    if (!r) r = copy_layer(c, m, sl[i], m->host_blob[sl[i]], slot, m->copy_st);
+    if (!r) r = cuda_check(c, cudaEventRecord(m->ev_ready[slot], m->copy_st), "slot ready");
+    return r;
+  }
+  nt_status begin(const uint8_t* skip) {
+    for (int l = 0; l < m->d.n_layers; ++l)
+      if (!(skip && skip[l]) && m->host_blob[l]) sl.push_back(l);
+    if (sl.empty()) return NT_OK;
+    nt_status s = cuda_check(c, cudaEventRecord(m->ev_fork, st), "fork copy stream");
+    if (!s) s = cuda_check(c, cudaStreamWaitEvent(m->copy_st, m->ev_fork, 0), "fork copy stream");
+    for (int i = 0; i < m->n_slots && i < int(sl.size()) && !s; ++i) s = copy(i);
+    return s;
+  }
+  // layer l's pointers (bound to its slot when streamed); slot = -1 when resident
+  nt_status before(int l, nt_layer_ptrs& L, int& slot) {
+    L = m->layers[l];
+    slot = -1;
+    if (!m->host_blob[l]) return NT_OK;
+    slot = si % m->n_slots;
+    bind_slot(m, slot, L);
+    return cuda_check(c, cudaStreamWaitEvent(st, m->ev_ready[slot], 0), "compute waits for its layer copy");
+  }
+  nt_status after(int slot) {
+    if (slot < 0) return NT_OK;
+    // the slot is free once this layer's kernels are done: the copy that reuses it may start
+    nt_status s = cuda_check(c, cudaEventRecord(m->ev_free[slot], st), "slot free");
+    if (!s && si + m->n_slots < int(sl.size())) s = copy(si + m->n_slots);
+    ++si;
+    return s;
+  }
+  nt_status end() {
+    if (sl.empty()) return NT_OK;
+    nt_status s = cuda_check(c, cudaEventRecord(m->ev_join, m->copy_st), "join copy stream");
+    if (!s) s = cuda_check(c, cudaStreamWaitEvent(st, m->ev_join, 0), "join copy stream");
+    return s;
+  }
+};
+
+// where one decode pass reads its token and position and puts its result
+struct StepIO {
+  const int32_t* tok;  // device token
+  const int64_t* pos;  // device position
+  float* logits;
+  int32_t* next_tok;   // nullable: receives the argmax
+  bool advance;        // the argmax also moves the model state: tok = argmax, pos += 1
 };
 
 // all kernels of one decode step, enqueued on st
-nt_status enqueue_step(Ctx* c, nt_model* m, const uint8_t* skip, float* logits, int32_t* next_tok, cudaStream_t st,
-                       bool want_cos) {
+nt_status enqueue_step(Ctx* c, nt_model* m, const uint8_t* skip, const StepIO& io, cudaStream_t st, bool want_cos) {
   const nt_model_desc& d = m->d;
   const int hd = d.head_dim;
   const int64_t nq = int64_t(d.n_qh) * hd, nkv = int64_t(d.n_kvh) * hd;
-  nt_status s = launch_embed(c, d.fmt_embd, m->embd, d.d_model, m->tok, m->x, st);
+  Streamer sm{c, m, st};
+  nt_status s = sm.begin(skip);
+  if (s) return s;
+  s = launch_embed(c, d.fmt_embd, m->embd, d.d_model, io.tok, m->x, st);
   if (s) return s;
   for (int l = 0; l < d.n_layers; ++l) {
     if (skip && skip[l]) continue;
-    const nt_layer_ptrs& L = m->layers[l];
+    nt_layer_ptrs L;
+    int slot;
+    s = sm.before(l, L, slot);
+    if (s) return s;
     if (want_cos) {
       s = cuda_check(c, cudaMemcpyAsync(m->xin, m->x, sizeof(float) * d.d_model, cudaMemcpyDeviceToDevice, st),
                      "copy x");
@@ -80,7 +213,7 @@ nt_status enqueue_step(Ctx* c, nt_model* m, const uint8_t* skip, float* logits, 
     // Q, K, V: one launch per distinct format; attention RMSNorm fused in
     // front, RoPE and the f16 KV append fused behind
     {
-      const RopeArgs ra{m->pos, m->inv_freq, hd, d.kv_cap};
+      const RopeArgs ra{io.pos, m->inv_freq, hd, d.kv_cap};
       const GemvJobEx J[3] = {GemvJobEx{nt_gemv_job{L.wq, m->q, nullptr, nq}, kEpiRope, nullptr},
                               GemvJobEx{nt_gemv_job{L.wk, nullptr, nullptr, nkv}, kEpiRopeCache, L.kcache},
                               GemvJobEx{nt_gemv_job{L.wv, nullptr, nullptr, nkv}, kEpiCache, L.vcache}};
@@ -99,7 +232,7 @@ nt_status enqueue_step(Ctx* c, nt_model* m, const uint8_t* skip, float* logits, 
         if (s) return s;
       }
     }
-    s = launch_attn(c, m->q, L.kcache, L.vcache, m->ao, d.n_qh, d.n_kvh, 0, m->pos, d.kv_cap, m->attn_part,
+    s = launch_attn(c, m->q, L.kcache, L.vcache, m->ao, d.n_qh, d.n_kvh, 0, io.pos, d.kv_cap, m->attn_part,
                     m->attn_cnt, m->S, st);
     if (s) return s;
     {
@@ -121,20 +254,182 @@ nt_status enqueue_step(Ctx* c, nt_model* m, const uint8_t* skip, float* logits, 
       s = launch_cos(c, m->xin, m->x, d.d_model, m->cos + l, st);
       if (s) return s;
     }
+    s = sm.after(slot);
+    if (s) return s;
   }
+  s = sm.end();
+  if (s) return s;
   {
-    nt_gemv_job j{m->out, logits, nullptr, d.vocab};
+    nt_gemv_job j{m->out, io.logits, nullptr, d.vocab};
     s = launch_gemv(c, d.fmt_out, &j, 1, nullptr, m->x, m->out_norm, d.eps, d.d_model, false, st);
     if (s) return s;
   }
-  return launch_argmax(c, logits, d.vocab, next_tok, m->amax_key, m->amax_cnt, st, m->tok, m->pos);
+  return launch_argmax(c, io.logits, d.vocab, io.next_tok, m->amax_key, m->amax_cnt, st,
+                       io.advance ? m->tok : nullptr, io.advance ? m->pos : nullptr);
+}
+
+// the verify pass: tokens spec_tok[0..M) at positions spec_pos[0] + i
+// through every layer (M-vector GEMMs, causal M-query attention), logits
+// [M][vocab], row argmaxes into vtok
+nt_status enqueue_verify(Ctx* c, nt_model* m, int M, float* logits, cudaStream_t st) {
+  const nt_model_desc& d = m->d;
+  const int hd = d.head_dim;
+  const int64_t nq = int64_t(d.n_qh) * hd, nkv = int64_t(d.n_kvh) * hd;
+  Streamer sm{c, m, st};
+  nt_status s = sm.begin(nullptr);
+  if (s) return s;
+  s = launch_embed(c, d.fmt_embd, m->embd, d.d_model, m->spec_tok, m->xv, st, M);
+  if (s) return s;
+  const RopeArgs ra{m->spec_pos, m->inv_freq, hd, d.kv_cap};
+  for (int l = 0; l < d.n_layers; ++l) {
+    nt_layer_ptrs L;
+    int slot;
+    s = sm.before(l, L, slot);
+    if (s) return s;
+    {
+      const GemmJobEx J[3] = {GemmJobEx{L.wq, nq, m->qv, nq, nullptr, nullptr, kEpiRope},
+                              GemmJobEx{L.wk, nkv, nullptr, 0, nullptr, L.kcache, kEpiRopeCache},
+                              GemmJobEx{L.wv, nkv, nullptr, 0, nullptr, L.vcache, kEpiCache}};
+      const int F[3] = {d.fmt_q, d.fmt_k, d.fmt_v};
+      bool done[3] = {false, false, false};
+      for (int i = 0; i < 3; ++i) {
+        if (done[i]) continue;
+        GemmJobEx jobs[3];
+        int nj = 0;
+        for (int j = i; j < 3; ++j)
+          if (!done[j] && F[j] == F[i]) {
+            jobs[nj++] = J[j];
+            done[j] = true;
+          }
+        s = launch_gemm(c, F[i], jobs, nj, false, m->xv, d.d_model, M, L.attn_norm, d.eps, d.d_model, &ra,
+                        m->gpart, m->gpart_bytes, st);
+        if (s) return s;
+      }
+    }
+    s = launch_attn(c, m->qv, L.kcache, L.vcache, m->aov, d.n_qh, d.n_kvh, 0, m->spec_pos, d.kv_cap, m->attn_part,
+                    m->attn_cnt, m->S, st, M);
+    if (s) return s;
+    {
+      const GemmJobEx j{L.wo, d.d_model, m->xv, d.d_model, m->xv, nullptr, kEpiPlain};
+      s = launch_gemm(c, d.fmt_o, &j, 1, false, m->aov, nq, M, nullptr, 0.f, nq, nullptr, m->gpart, m->gpart_bytes,
+                      st);
+      if (s) return s;
+    }
+    {
+      const GemmJobEx j[2] = {GemmJobEx{L.wg, d.ffn, m->hv, d.ffn, nullptr, nullptr, kEpiPlain},
+                              GemmJobEx{L.wu, d.ffn, nullptr, 0, nullptr, nullptr, kEpiPlain}};
+      s = launch_gemm(c, d.fmt_gate, j, 2, true, m->xv, d.d_model, M, L.ffn_norm, d.eps, d.d_model, nullptr,
+                      m->gpart, m->gpart_bytes, st);
+      if (s) return s;
+    }
+    {
+      const GemmJobEx j{L.wd, d.d_model, m->xv, d.d_model, m->xv, nullptr, kEpiPlain};
+      s = launch_gemm(c, d.fmt_down, &j, 1, false, m->hv, d.ffn, M, nullptr, 0.f, d.ffn, nullptr, m->gpart,
+                      m->gpart_bytes, st);
+      if (s) return s;
+    }
+    s = sm.after(slot);
+    if (s) return s;
+  }
+  s = sm.end();
+  if (s) return s;
+  {
+    const GemmJobEx j{m->out, d.vocab, logits, d.vocab, nullptr, nullptr, kEpiPlain};
+    s = launch_gemm(c, d.fmt_out, &j, 1, false, m->xv, d.d_model, M, m->out_norm, d.eps, d.d_model, nullptr,
+                    m->gpart, m->gpart_bytes, st);
+    if (s) return s;
+  }
+  for (int i = 0; i < M && !s; ++i)
+    s = launch_argmax(c, logits + int64_t(i) * d.vocab, d.vocab, m->vtok + i, m->vkey + i, m->vcnt + i, st);
+  return s;
+}
+
+// start of a speculative step: the step's token and the positions of the
+// verify rows, from the model state
+__global__ void spec_setup_kernel(const int32_t* tok, const int64_t* pos, int32_t* spec_tok, int64_t* spec_pos,
+                                  int M) {
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) spec_tok[0] = *tok;
+  if (int(threadIdx.x) < M) spec_pos[threadIdx.x] = *pos + threadIdx.x;
+}
+
+// end of a speculative step: draft i + 1 is kept while it equals the verify
+// argmax of row i; the kept drafts plus the verify argmax after them are the
+// step's tokens, and the model state moves past them
+__global__ void spec_accept_kernel(const int32_t* spec_tok, const int32_t* vtok, int k, int32_t* out, int32_t* n_out,
+                                   int32_t* tok, int64_t* pos, const int64_t* spec_pos) {
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x != 0) return;
+  int n = 0;
+  while (n < k && spec_tok[n + 1] == vtok[n]) ++n;
+  for (int i = 0; i <= n; ++i) out[i] = vtok[i];
+  *n_out = n + 1;
+  *tok = vtok[n];
+  *pos = spec_pos[0] + n + 1;
+}
+
+// draft layers: [0, n_draft) when n_draft > 0, else every resident layer
+std::vector<uint8_t> draft_mask(const nt_model* m, int n_draft) {
+  std::vector<uint8_t> mask(m->d.n_layers, 0);
+  for (int l = 0; l < m->d.n_layers; ++l) mask[l] = n_draft > 0 ? (l >= n_draft) : (m->host_blob[l] != nullptr);
+  return mask;
+}
+
+nt_status enqueue_spec(Ctx* c, nt_model* m, int k, int n_draft, int32_t* out, int32_t* n_out, float* logits,
+                       cudaStream_t st) {
+  const int M = k + 1;
+  nt_status s = cuda_check(c, launch_k(c, spec_setup_kernel, dim3(1), dim3(32), 0, st, m->tok, m->pos, m->spec_tok,
+                                       m->spec_pos, M),
+                           "spec setup launch");
+  if (s) return s;
+  const std::vector<uint8_t> mask = draft_mask(m, n_draft);
+  for (int i = 0; i < k && !s; ++i)
+    s = enqueue_step(c, m, mask.data(), StepIO{m->spec_tok + i, m->spec_pos + i, m->dlogits, m->spec_tok + i + 1, false},
+                     st, false);
+  if (!s) s = enqueue_verify(c, m, M, logits ? logits : m->lv, st);
+  if (!s)
+    s = cuda_check(c, launch_k(c, spec_accept_kernel, dim3(1), dim3(32), 0, st, m->spec_tok, m->vtok, k, out, n_out,
+                               m->tok, m->pos, m->spec_pos),
+                   "spec accept launch");
+  return s;
+}
+
+template <typename T>
+void key_append(std::string& k, const T& v) {
+  k.append(reinterpret_cast<const char*>(&v), sizeof v);
 }
 
 std::string graph_key(const nt_model* m, const uint8_t* skip, const float* logits, const int32_t* next_tok) {
-  std::string k(reinterpret_cast<const char*>(&logits), sizeof logits);
-  k.append(reinterpret_cast<const char*>(&next_tok), sizeof next_tok);
+  std::string k("d");
+  key_append(k, logits);
+  key_append(k, next_tok);
   for (int l = 0; l < m->d.n_layers; ++l) k.push_back(skip && skip[l] ? '1' : '0');
   return k;
+}
+
+// replay the graph under `key`, capturing it first with `enqueue` on the
+// model's capture stream
+template <typename F>
+nt_status run_graph(Ctx* c, nt_model* m, const std::string& key, cudaStream_t st, F enqueue) {
+  auto it = m->graphs.find(key);
+  nt_status s = NT_OK;
+  if (it == m->graphs.end()) {
+    cudaGraph_t g = nullptr;
+    cudaGraphExec_t ge = nullptr;
+    s = cuda_check(c, cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeThreadLocal), "begin capture");
+    if (!s) {
+      nt_status s2 = enqueue(m->cap);
+      cudaError_t e = cudaStreamEndCapture(m->cap, &g);
+      s = s2 ? s2 : cuda_check(c, e, "end capture");
+    }
+    if (!s) s = cuda_check(c, cudaGraphInstantiate(&ge, g, 0), "graph instantiate");
+    if (g) cudaGraphDestroy(g);
+    if (s) return s;
+    it = m->graphs.emplace(key, ge).first;
+  }
+  return cuda_check(c, cudaGraphLaunch(it->second, st), "graph launch");
 }
 
 }  // namespace
@@ -173,18 +468,49 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
                  d.d_model % block_elems(d.fmt_embd) == 0 && d.d_model % block_elems(d.fmt_out) == 0 &&
                  nq % block_elems(d.fmt_o) == 0 && d.ffn % block_elems(d.fmt_down) == 0,
              NT_ERR_INVALID_ARG, "a matrix width is not a multiple of its block size");
+  const int n_slots = d.stream_slots == 0 ? 2 : d.stream_slots;
+  NT_REQUIRE(n_slots >= 1 && n_slots <= kMaxSlots, NT_ERR_INVALID_ARG, "stream_slots must be 0..%d", kMaxSlots);
+  int n_streamed = 0;
   for (int l = 0; l < d.n_layers; ++l) {
     const nt_layer_ptrs& L = layers[l];
     NT_REQUIRE(L.attn_norm && L.ffn_norm && L.kcache && L.vcache, NT_ERR_INVALID_ARG, "layer %d: null norm/cache", l);
     NT_REQUIRE(aligned(L.kcache, 16) && aligned(L.vcache, 16) && aligned(L.attn_norm, 16) && aligned(L.ffn_norm, 16),
                NT_ERR_ALIGNMENT, "layer %d: caches and norms must be 16-byte aligned", l);
+    const void* w[7] = {L.wq, L.wk, L.wv, L.wo, L.wg, L.wu, L.wd};
+    int nw = 0;
+    for (const void* p : w) nw += p != nullptr;
+    if (nw == 7) {
+      NT_REQUIRE(!L.host_blob, NT_ERR_INVALID_ARG, "layer %d: resident weights and a host blob", l);
+    } else {
+      NT_REQUIRE(nw == 0 && L.host_blob, NT_ERR_INVALID_ARG,
+                 "layer %d: set all seven weight pointers, or none and a host blob", l);
+      cudaPointerAttributes pa{};
+      const cudaError_t pe = cudaPointerGetAttributes(&pa, L.host_blob);
+      NT_REQUIRE(pe == cudaSuccess && pa.type == cudaMemoryTypeHost, NT_ERR_INVALID_ARG,
+                 "layer %d: host_blob must be page-locked host memory", l);
+      ++n_streamed;
+    }
   }
   NT_REQUIRE(aligned(out_norm, 16), NT_ERR_ALIGNMENT, "out_norm must be 16-byte aligned");
+  // an embedding table in page-locked host memory is read through its device alias
+  {
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, embd) == cudaSuccess && pa.type == cudaMemoryTypeHost) {
+      NT_REQUIRE(pa.devicePointer, NT_ERR_INVALID_ARG, "embd: host memory without a device mapping");
+      embd = pa.devicePointer;
+    }
+    cudaGetLastError();
+  }
 
   nt_model* m = new (std::nothrow) nt_model();
   if (!m) return NT_ERR_OOM;
   m->d = d;
   m->layers.assign(layers, layers + d.n_layers);
+  m->host_blob.resize(d.n_layers);
+  for (int l = 0; l < d.n_layers; ++l) m->host_blob[l] = layers[l].host_blob;
+  blob_layout(d, m->blob_off, &m->blob_bytes);
+  m->n_slots = n_streamed ? n_slots : 0;
+  m->slot_layer.assign(m->n_slots, -1);
   m->embd = embd;
   m->out = out;
   m->out_norm = out_norm;
@@ -192,19 +518,40 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   const size_t fl = sizeof(float);
   const size_t nx = up256(fl * d.d_model), nqb = up256(fl * nq), nkb = up256(fl * d.n_kvh * d.head_dim),
                nh = up256(fl * d.ffn), ncos = up256(fl * d.n_layers), nst = 256, nfreq = up256(8 * d.head_dim),
-               npart = up256(attn_scratch_bytes(d.n_qh, d.n_kvh, m->S));
-  const size_t total = 2 * nx + nqb * 2 + nkb * 2 + nh + ncos + nst + npart + nfreq;
+               npart = up256(attn_scratch_bytes(d.n_qh, d.n_kvh, m->S, kMaxVerify)), nspec = 1024,
+               nvx = up256(fl * kMaxVerify * d.d_model), nvq = up256(fl * kMaxVerify * nq),
+               nvh = up256(fl * kMaxVerify * d.ffn), nvl = up256(fl * kMaxVerify * d.vocab), ndl = up256(fl * d.vocab);
+  {
+    // partial sums of the largest verify GEMM
+    const int64_t nkv = int64_t(d.n_kvh) * d.head_dim;
+    const int64_t rc[5][2] = {{nq + 2 * nkv, d.d_model}, {d.d_model, nq}, {2 * int64_t(d.ffn), d.d_model},
+                              {d.d_model, d.ffn}, {d.vocab, d.d_model}};
+    for (auto& x : rc) m->gpart_bytes = std::max(m->gpart_bytes, gemm_scratch_bytes(x[0], x[1], kMaxVerify));
+    m->gpart_bytes = up256(m->gpart_bytes);
+  }
+  const size_t total = 2 * nx + nqb * 2 + nkb * 2 + nh + ncos + nst + npart + nfreq + nspec + nvx + 2 * nvq + nvh +
+                       nvl + ndl + m->gpart_bytes;
   int dev_prev = 0;
   cudaGetDevice(&dev_prev);
   cudaSetDevice(ctx->device);
   cudaError_t e = cudaMalloc(&m->buf, total);
   if (e == cudaSuccess) e = cudaMemset(m->buf, 0, total);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->cap, cudaStreamNonBlocking);
+  if (e == cudaSuccess && m->n_slots) {
+    e = cudaMalloc(&m->slots, size_t(m->n_slots) * m->blob_bytes);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->copy_st, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_join, cudaEventDisableTiming);
+    for (int i = 0; i < m->n_slots && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&m->ev_ready[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_free[i], cudaEventDisableTiming);
+    }
+  }
   cudaSetDevice(dev_prev);
   if (e != cudaSuccess) {
-    if (m->buf) cudaFree(m->buf);
-    delete m;
-    return cuda_check(ctx, e, "model allocation");
+    const nt_status st = cuda_check(ctx, e, "model allocation");
+    nt_model_destroy(ctx, m);
+    return e == cudaErrorMemoryAllocation ? set_err(ctx, NT_ERR_OOM, "model allocation: out of device memory") : st;
   }
   char* p = m->buf;
   auto take = [&](size_t n) {
@@ -228,7 +575,20 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   m->inv_freq = reinterpret_cast<double*>(take(nfreq));
   char* part = take(npart);
   m->attn_cnt = reinterpret_cast<unsigned*>(part);
-  m->attn_part = reinterpret_cast<float*>(part + 64 * sizeof(unsigned));
+  m->attn_part = reinterpret_cast<float*>(part + kAttnCounterBytes);
+  char* sp = take(nspec);
+  m->spec_tok = reinterpret_cast<int32_t*>(sp);
+  m->spec_pos = reinterpret_cast<int64_t*>(sp + 64);
+  m->vtok = reinterpret_cast<int32_t*>(sp + 128);
+  m->vkey = reinterpret_cast<unsigned long long*>(sp + 192);
+  m->vcnt = reinterpret_cast<unsigned*>(sp + 256);
+  m->xv = reinterpret_cast<float*>(take(nvx));
+  m->qv = reinterpret_cast<float*>(take(nvq));
+  m->aov = reinterpret_cast<float*>(take(nvq));
+  m->hv = reinterpret_cast<float*>(take(nvh));
+  m->lv = reinterpret_cast<float*>(take(nvl));
+  m->dlogits = reinterpret_cast<float*>(take(ndl));
+  m->gpart = reinterpret_cast<float*>(take(m->gpart_bytes));
   cudaSetDevice(ctx->device);
   nt_status st = launch_inv_freq(ctx, m->inv_freq, d.head_dim, d.theta, nullptr);
   if (!st) st = cuda_check(ctx, cudaDeviceSynchronize(), "model init");
@@ -249,7 +609,15 @@ nt_status nt_model_destroy(nt_ctx* ctx, nt_model* m) {
   cudaDeviceSynchronize();
   for (auto& kv : m->graphs) cudaGraphExecDestroy(kv.second);
   if (m->cap) cudaStreamDestroy(m->cap);
-  cudaFree(m->buf);
+  if (m->copy_st) cudaStreamDestroy(m->copy_st);
+  for (cudaEvent_t ev : {m->ev_fork, m->ev_join})
+    if (ev) cudaEventDestroy(ev);
+  for (int i = 0; i < kMaxSlots; ++i) {
+    if (m->ev_ready[i]) cudaEventDestroy(m->ev_ready[i]);
+    if (m->ev_free[i]) cudaEventDestroy(m->ev_free[i]);
+  }
+  if (m->slots) cudaFree(m->slots);
+  if (m->buf) cudaFree(m->buf);
   cudaSetDevice(dev_prev);
   delete m;
   return NT_OK;
@@ -265,12 +633,6 @@ nt_status nt_decode_step(nt_ctx* ctx, nt_model* m, int32_t token, int64_t pos, c
     NT_REQUIRE(pos >= 0 && pos < m->d.kv_cap, NT_ERR_INVALID_ARG, "pos %lld outside the KV cache",
                (long long)pos);
   }
-  for (int l = 0; l < m->d.n_layers; ++l) {
-    if (skip && skip[l]) continue;
-    const nt_layer_ptrs& L = m->layers[l];
-    NT_REQUIRE(L.wq && L.wk && L.wv && L.wo && L.wg && L.wu && L.wd, NT_ERR_INVALID_ARG,
-               "layer %d has no weights bound", l);
-  }
   int dev_prev = 0;
   cudaGetDevice(&dev_prev);
   if (dev_prev != ctx->device) cudaSetDevice(ctx->device);
@@ -281,22 +643,9 @@ nt_status nt_decode_step(nt_ctx* ctx, nt_model* m, int32_t token, int64_t pos, c
     s = cuda_check(ctx, cudaGetLastError(), "set step state");
   }
   if (!s) {
-    const std::string key = graph_key(m, skip, logits, next_tok);
-    auto it = m->graphs.find(key);
-    if (it == m->graphs.end()) {
-      cudaGraph_t g = nullptr;
-      cudaGraphExec_t ge = nullptr;
-      s = cuda_check(ctx, cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeThreadLocal), "begin capture");
-      if (!s) {
-        nt_status s2 = enqueue_step(ctx, m, skip, logits, next_tok, m->cap, false);
-        cudaError_t e = cudaStreamEndCapture(m->cap, &g);
-        s = s2 ? s2 : cuda_check(ctx, e, "end capture");
-      }
-      if (!s) s = cuda_check(ctx, cudaGraphInstantiate(&ge, g, 0), "graph instantiate");
-      if (g) cudaGraphDestroy(g);
-      if (!s) it = m->graphs.emplace(key, ge).first;
-    }
-    if (!s) s = cuda_check(ctx, cudaGraphLaunch(it->second, st), "graph launch");
+    const StepIO io{m->tok, m->pos, logits, next_tok, true};
+    s = run_graph(ctx, m, graph_key(m, skip, logits, next_tok), st,
+                  [&](cudaStream_t cs) { return enqueue_step(ctx, m, skip, io, cs, false); });
   }
   if (dev_prev != ctx->device) cudaSetDevice(dev_prev);
   return s;
@@ -316,7 +665,7 @@ nt_status nt_layer_skip_calibrate(nt_ctx* ctx, nt_model* m, int32_t token, int64
   std::vector<float> cs(m->d.n_layers, 0.f);
   set_state_kernel<<<1, 1, 0, st>>>(m->tok, m->pos, token, pos);
   nt_status s = cuda_check(ctx, cudaGetLastError(), "set step state");
-  if (!s) s = enqueue_step(ctx, m, nullptr, logits, next_tok, st, true);
+  if (!s) s = enqueue_step(ctx, m, nullptr, StepIO{m->tok, m->pos, logits, next_tok, true}, st, true);
   if (!s)
     s = cuda_check(ctx, cudaMemcpyAsync(cs.data(), m->cos, sizeof(float) * cs.size(), cudaMemcpyDeviceToHost, st),
                    "read cosines");
@@ -330,6 +679,86 @@ nt_status nt_layer_skip_calibrate(nt_ctx* ctx, nt_model* m, int32_t token, int64
   std::memset(mask, 0, size_t(m->d.n_layers));
   for (int i = 0; i < n_skip; ++i) mask[idx[i]] = 1;
   if (cos_host) std::memcpy(cos_host, cs.data(), sizeof(float) * cs.size());
+  return NT_OK;
+}
+
+nt_status nt_spec_step(nt_ctx* ctx, nt_model* m, int32_t token, int64_t pos, int k, int n_draft_layers,
+                       int32_t* tokens_out, int32_t* n_out, float* logits, void* stream) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  NT_REQUIRE(m && tokens_out && n_out, NT_ERR_INVALID_ARG, "null model or outputs");
+  NT_REQUIRE(k >= 1 && k < kMaxVerify, NT_ERR_INVALID_ARG, "k must be 1..%d", kMaxVerify - 1);
+  NT_REQUIRE(n_draft_layers >= 0 && n_draft_layers <= m->d.n_layers, NT_ERR_INVALID_ARG,
+             "n_draft_layers outside 0..n_layers");
+  NT_REQUIRE(aligned(tokens_out, 4) && aligned(n_out, 4), NT_ERR_ALIGNMENT, "outputs must be 4-byte aligned");
+  NT_REQUIRE(!logits || aligned(logits, 16), NT_ERR_ALIGNMENT, "logits must be 16-byte aligned");
+  if (token >= 0) {
+    NT_REQUIRE(token < m->d.vocab, NT_ERR_INVALID_ARG, "token %d outside the vocabulary", token);
+    NT_REQUIRE(pos >= 0 && pos + k < m->d.kv_cap, NT_ERR_INVALID_ARG, "pos %lld: pos + k outside the KV cache",
+               (long long)pos);
+  }
+  int dev_prev = 0;
+  cudaGetDevice(&dev_prev);
+  if (dev_prev != ctx->device) cudaSetDevice(ctx->device);
+  cudaStream_t st = as_stream(stream);
+  nt_status s = NT_OK;
+  if (token >= 0) {
+    set_state_kernel<<<1, 1, 0, st>>>(m->tok, m->pos, token, pos);
+    s = cuda_check(ctx, cudaGetLastError(), "set step state");
+  }
+  if (!s) {
+    std::string key("s");
+    key_append(key, k);
+    key_append(key, n_draft_layers);
+    key_append(key, tokens_out);
+    key_append(key, n_out);
+    key_append(key, logits);
+    s = run_graph(ctx, m, key, st,
+                  [&](cudaStream_t cs) { return enqueue_spec(ctx, m, k, n_draft_layers, tokens_out, n_out, logits, cs); });
+  }
+  if (dev_prev != ctx->device) cudaSetDevice(dev_prev);
+  return s;
+}
+
+nt_status nt_layer_blob_layout(const nt_model_desc* d, size_t* off, size_t* bytes) {
+  if (!d || !off || !bytes) return NT_ERR_INVALID_ARG;
+  const int fm[7] = {d->fmt_q, d->fmt_k, d->fmt_v, d->fmt_o, d->fmt_gate, d->fmt_up, d->fmt_down};
+  for (int f : fm)
+    if (!fmt_ok(f)) return NT_ERR_UNSUPPORTED_FMT;
+  if (d->d_model <= 0 || d->n_qh <= 0 || d->n_kvh <= 0 || d->head_dim <= 0 || d->ffn <= 0) return NT_ERR_INVALID_ARG;
+  blob_layout(*d, off, bytes);
+  return NT_OK;
+}
+
+nt_status nt_stream_layer(nt_ctx* ctx, nt_model* m, int layer, const void* src, size_t bytes, int slot,
+                          void* copy_stream) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  NT_REQUIRE(m && src, NT_ERR_INVALID_ARG, "null model or source");
+  NT_REQUIRE(m->n_slots > 0, NT_ERR_INVALID_ARG, "the model streams no layer");
+  NT_REQUIRE(layer >= 0 && layer < m->d.n_layers && m->host_blob[layer], NT_ERR_INVALID_ARG,
+             "layer %d is not a streamed layer", layer);
+  NT_REQUIRE(slot >= 0 && slot < m->n_slots, NT_ERR_INVALID_ARG, "slot %d outside 0..%d", slot, m->n_slots - 1);
+  NT_REQUIRE(bytes == m->blob_bytes, NT_ERR_INVALID_ARG, "bytes %zu, the layer blob is %zu", bytes, m->blob_bytes);
+  cudaPointerAttributes pa{};
+  const cudaError_t pe = cudaPointerGetAttributes(&pa, src);
+  cudaGetLastError();
+  NT_REQUIRE(pe == cudaSuccess && pa.type == cudaMemoryTypeHost, NT_ERR_INVALID_ARG,
+             "the source must be page-locked host memory");
+  int dev_prev = 0;
+  cudaGetDevice(&dev_prev);
+  if (dev_prev != ctx->device) cudaSetDevice(ctx->device);
+  const nt_status s = copy_layer(ctx, m, layer, src, slot, as_stream(copy_stream));
+  if (dev_prev != ctx->device) cudaSetDevice(dev_prev);
+  return s;
+}
+
+nt_status nt_model_slot(nt_ctx* ctx, nt_model* m, int slot, void** dev, size_t* bytes, int* layer) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  NT_REQUIRE(m, NT_ERR_INVALID_ARG, "null model");
+  NT_REQUIRE(m->n_slots > 0, NT_ERR_INVALID_ARG, "the model streams no layer");
+  NT_REQUIRE(slot >= 0 && slot < m->n_slots, NT_ERR_INVALID_ARG, "slot %d outside 0..%d", slot, m->n_slots - 1);
+  if (dev) *dev = slot_ptr(m, slot);
+  if (bytes) *bytes = m->blob_bytes;
+  if (layer) *layer = m->slot_layer[slot];
   return NT_OK;
 }
 

@@ -77,11 +77,13 @@ __global__ void dequant_kernel(int fmt, const uint8_t* W, int64_t row0, int64_t 
   }
 }
 
-// row *token_dev of an embedding table, dequantised (token read on the device)
+// rows token_dev[m] of an embedding table, dequantised into out[m][cols]
+// (m = blockIdx.y; tokens read on the device)
 __global__ void embed_kernel(int fmt, const uint8_t* W, int64_t cols, const int32_t* token_dev, float* out) {
   pdl_wait();
   pdl_trigger();
-  const int64_t row = *token_dev;
+  const int64_t row = token_dev[blockIdx.y];
+  out += int64_t(blockIdx.y) * cols;
   const int BE = block_elems(fmt), BB = block_bytes(fmt);
   const int64_t nb = cols / BE;
   for (int64_t col = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; col < cols; col += int64_t(gridDim.x) * blockDim.x) {
@@ -115,9 +117,9 @@ __global__ void embed_kernel(int fmt, const uint8_t* W, int64_t cols, const int3
 }  // namespace
 
 nt_status launch_embed(Ctx* c, int fmt, const void* W, int64_t cols, const int32_t* token_dev, float* out,
-                       cudaStream_t st) {
+                       cudaStream_t st, int M) {
   const int blocks = int((cols + 255) / 256);
-  return cuda_check(c, launch_k(c, embed_kernel, dim3(blocks), dim3(256), 0, st, fmt, static_cast<const uint8_t*>(W),
+  return cuda_check(c, launch_k(c, embed_kernel, dim3(blocks, M), dim3(256), 0, st, fmt, static_cast<const uint8_t*>(W),
                                 cols, token_dev, out),
                     "embed launch");
 }

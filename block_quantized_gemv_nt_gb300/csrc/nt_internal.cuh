@@ -19,6 +19,7 @@ namespace nt {
 constexpr int kMaxSpin = 1 << 16;   // iteration cap of every device-side wait
 constexpr unsigned kWaitHintNs = 50000;  // each try_wait may sleep this long (cap ~3 s in all)
 constexpr unsigned kErrWaitTimeout = 1u;
+constexpr unsigned kErrPosRange = 2u;  // a device-side position fell outside the KV cache: nothing written there
 
 struct Ctx {
   int device = 0;
@@ -32,6 +33,7 @@ struct Ctx {
   int gemv_stages = 2;
   int gemv_stage_max = 12288;
   int gemv_static_smem = 2048;   // largest static shared memory of the GEMV kernels
+  int gemm_static_smem = 1024;   // same for the verify-GEMM kernels
   std::string last_error;
   std::mutex mu;
 };
@@ -45,7 +47,9 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 // scratch layout (bytes from ctx->scratch) ------------------------------------
 constexpr size_t kScratchErr = 0;            // unsigned err flag (also ctx->err_flag)
 constexpr size_t kScratchArgmax = 256;       // unsigned long long key + unsigned counter
-constexpr size_t kScratchAttn = 4096;        // attention partials + counters
+constexpr size_t kScratchAttn = 4096;        // attention counters (kAttnCounterBytes), then partials
+constexpr size_t kAttnCounterBytes = 2048;   // [queries <= 8][KV heads <= 64] unsigned
+constexpr size_t kScratchGemm = size_t(32) << 20;  // verify-GEMM partial sums, to the end of the scratch
 
 // format geometry ---------------------------------------------------------------
 __host__ __device__ constexpr int block_elems(int fmt) { return fmt <= NT_Q4_0 ? 32 : 256; }
@@ -174,6 +178,19 @@ struct GemvJobEx {
   nt_gemv_job j;
   int epi;
   void* cache;  // f16 cache of one layer [n_kvh][kv_stride][head_dim] for kEpi*Cache
+};
+
+// one job of the M-vector verify GEMM: Y[m] = W X[m], with the epilogue applied
+// per vector m (RoPE and the cache append at position pos + m)
+constexpr int kMaxVerify = 8;  // vectors per verify GEMM (draft length + 1)
+struct GemmJobEx {
+  const void* W;
+  int64_t rows;
+  float* y;            // [M][ldy]
+  int64_t ldy;
+  const float* res;    // [M][ldy] residual, nullable (kEpiPlain)
+  void* cache;         // f16 cache of one layer for kEpi*Cache
+  int epi;
 };
 
 nt_status launch_gemv(Ctx* c, int fmt, const nt_gemv_job* jobs, int njobs, const void* W2, const float* x,

@@ -129,9 +129,11 @@ struct AttnArgs {
   int64_t n_pos;
   const int64_t* pos_dev;  // nullable: n_pos = *pos_dev + 1
   int64_t kv_stride;
-  float* part;             // [n_kvh][S][G][2 + 128]
-  unsigned* counters;      // [n_kvh]
+  float* part;             // [nq][n_kvh][S][G][2 + 128]
+  unsigned* counters;      // [nq][n_kvh]
   unsigned* err;
+  int64_t q_stride;        // floats between the q (and out) vectors of consecutive queries
+  int64_t part_stride;     // floats between the partials of consecutive queries
 };
 
 // a warp partial row in shared memory: o[128] (16-byte aligned), then m, l, 2 pad
@@ -163,18 +165,32 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
 
   const int g = blockIdx.x, s = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // query qi (blockIdx.z) sees one position more than query qi - 1: causal
+  // attention of consecutive tokens (the verify pass); one query in decode
+  const int qi = blockIdx.z;
+  const float* qv = a.q + int64_t(qi) * a.q_stride;
+  float* outv = a.out + int64_t(qi) * a.q_stride;
+  float* partv = a.part + int64_t(qi) * a.part_stride;
+  unsigned* cnt = a.counters + qi * a.n_kvh;
   pdl_trigger();
   // In the decode step (pos_dev set) the cached positions before pos were
   // written by earlier tokens and are stable, so their K/V chunk streams in
-  // before waiting for the kernel that writes q and position pos.  Called
+  // before waiting for the kernel that writes q and positions pos.. .  Called
   // standalone, everything waits: the caller may have just written the cache.
   if (!a.pos_dev) pdl_wait();
-  const int64_t n_pos = a.pos_dev ? *a.pos_dev + 1 : a.n_pos;
+  const int64_t pos0 = a.pos_dev ? __ldcg(a.pos_dev) : 0;  // read before the wait: bypass L1
+  int64_t n_pos = (a.pos_dev ? pos0 + 1 : a.n_pos) + qi;
+  if (n_pos < 1 || n_pos > a.kv_stride) {
+    // a device-side position outside the cache: read nothing beyond it
+    if (tid == 0 && s == 0) flag_error(a.err, kErrPosRange);
+    n_pos = n_pos < 1 ? 1 : a.kv_stride;
+  }
+  const int64_t stable = a.pos_dev ? pos0 : n_pos;  // positions written before this step
   const int64_t chunk = (n_pos + a.S - 1) / a.S;
   const int64_t p0 = int64_t(s) * chunk;
   const int64_t p1 = min(n_pos, p0 + chunk);
   const int np = p1 > p0 ? int(p1 - p0) : 0;
-  const int np_early = a.pos_dev ? max(0, int(min(p1, n_pos - 1) - p0)) : np;  // positions safe before the wait
+  const int np_early = a.pos_dev ? max(0, int(min(p1, stable) - p0)) : np;  // positions safe before the wait
   const __half* Kg = a.K + int64_t(g) * a.kv_stride * kHD;
   const __half* Vg = a.V + int64_t(g) * a.kv_stride * kHD;
   const uint32_t b = smem_u32(bar);
@@ -203,7 +219,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     }
   }
   const float scale = rsqrtf(float(kHD));
-  for (int i = tid; i < G * kHD; i += kAttnThreads) qs[i] = a.q[int64_t(g) * G * kHD + i] * scale;
+  for (int i = tid; i < G * kHD; i += kAttnThreads) qs[i] = qv[int64_t(g) * G * kHD + i] * scale;
   __syncthreads();
   bool ok = true;
   if (np > 0) ok = mbar_wait(b, 0);
@@ -279,7 +295,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     }
   }
   __syncthreads();
-  float* my = a.part + (int64_t(g) * a.S + s) * G * (2 + kHD);
+  float* my = partv + (int64_t(g) * a.S + s) * G * (2 + kHD);
   for (int i = tid; i < G * (kHD + 1); i += kAttnThreads) {
     const int h = i / (kHD + 1), d = i % (kHD + 1);  // d == kHD: the (m, l) pair
     float M = -INFINITY;
@@ -304,7 +320,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    const unsigned prev = atomicAdd(a.counters + g, 1u);
+    const unsigned prev = atomicAdd(cnt + g, 1u);
     last = (prev == unsigned(a.S - 1));
   }
   __syncthreads();
@@ -313,7 +329,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   // stage every split's (max, sum) in shared memory, turn them into per-split
   // weights w_t = e^(m_t - M) / L, then each output element is an independent
   // sum over the splits
-  const float* base = a.part + int64_t(g) * a.S * G * (2 + kHD);
+  const float* base = partv + int64_t(g) * a.S * G * (2 + kHD);
   for (int i = tid; i < G * a.S; i += kAttnThreads) {
     const int h = i / a.S, t = i % a.S;
     wts[h * kMaxChunk + t] = __ldcg(base + (int64_t(t) * G + h) * (2 + kHD));
@@ -348,9 +364,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       O3 = fmaf(__ldcg(pp + (t + 3) * stride), wts[h * kMaxChunk + t + 3], O3);
     }
     for (; t < a.S; ++t) O0 = fmaf(__ldcg(pp + t * stride), wts[h * kMaxChunk + t], O0);
-    a.out[(int64_t(g) * G + h) * kHD + d] = (O0 + O1) + (O2 + O3);
+    outv[(int64_t(g) * G + h) * kHD + d] = (O0 + O1) + (O2 + O3);
   }
-  if (tid == 0) a.counters[g] = 0u;  // ready for the next launch
+  if (tid == 0) cnt[g] = 0u;  // ready for the next launch
 }
 
 using AttnKernel = void (*)(AttnArgs);
@@ -504,14 +520,18 @@ int attn_splits(const Ctx* c, int n_kvh, int64_t kv_stride) {
 
 int64_t attn_max_stride() { return int64_t(kMaxChunk) * kMaxChunk; }
 
-size_t attn_scratch_bytes(int n_qh, int n_kvh, int S) {
-  return size_t(n_kvh) * S * (n_qh / n_kvh) * (2 + kHD) * sizeof(float) + 64 * sizeof(unsigned);
+size_t attn_scratch_bytes(int n_qh, int n_kvh, int S, int nq) {
+  return size_t(nq) * size_t(n_kvh) * S * (n_qh / n_kvh) * (2 + kHD) * sizeof(float) + kAttnCounterBytes;
 }
+
+size_t attn_part_floats(int n_qh, int n_kvh, int S) { return size_t(n_kvh) * S * (n_qh / n_kvh) * (2 + kHD); }
 
 nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, float* out, int n_qh, int n_kvh,
                       int64_t n_pos, const int64_t* pos_dev, int64_t kv_stride, float* part, unsigned* counters,
-                      int S, cudaStream_t st) {
+                      int S, cudaStream_t st, int nq) {
   AttnArgs a{};
+  a.q_stride = int64_t(n_qh) * kHD;
+  a.part_stride = int64_t(attn_part_floats(n_qh, n_kvh, S));
   a.q = q;
   a.K = static_cast<const __half*>(K);
   a.V = static_cast<const __half*>(V);
@@ -529,7 +549,7 @@ nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, floa
   const size_t smem = attn_smem_bytes(a.G);
   AttnKernel k = attn_kernel_for(a.G);
   if (!k) return set_err(c, NT_ERR_INVALID_ARG, "attention: group size %d not in {1,2,4,8,16}", a.G);
-  return cuda_check(c, launch_k(c, k, dim3(n_kvh, S), dim3(kAttnThreads), smem, st, a), "attention launch");
+  return cuda_check(c, launch_k(c, k, dim3(n_kvh, S, nq), dim3(kAttnThreads), smem, st, a), "attention launch");
 }
 
 cudaError_t configure_attn(size_t optin) {

@@ -7,8 +7,9 @@ namespace nt {
 
 nt_status launch_dequant(Ctx* c, int fmt, const void* W, int64_t row0, int64_t nrows, int64_t cols, float* out,
                          cudaStream_t st);
+// out[m][cols] = dequantised row token_dev[m], m < M
 nt_status launch_embed(Ctx* c, int fmt, const void* W, int64_t cols, const int32_t* token_dev, float* out,
-                       cudaStream_t st);
+                       cudaStream_t st, int M = 1);
 nt_status launch_rmsnorm(Ctx* c, const float* x, const float* g, float* y, int64_t n, float eps, cudaStream_t st);
 nt_status launch_rope(Ctx* c, float* q, float* k, int n_qh, int n_kvh, int hd, int64_t pos, float theta,
                       cudaStream_t st);
@@ -17,15 +18,25 @@ nt_status launch_rope_append(Ctx* c, float* q, const float* k, const float* v, v
                              cudaStream_t st);
 int attn_splits(const Ctx* c, int n_kvh, int64_t kv_stride);
 int64_t attn_max_stride();
-size_t attn_scratch_bytes(int n_qh, int n_kvh, int S);
+// counters (kAttnCounterBytes) followed by the partials of nq queries
+size_t attn_scratch_bytes(int n_qh, int n_kvh, int S, int nq = 1);
+size_t attn_part_floats(int n_qh, int n_kvh, int S);
+// nq queries: query i sees n_pos + i positions (pos_dev set: *pos_dev + 1 + i);
+// q, out [nq][n_qh * 128]; part [nq][attn_part_floats]; counters [nq][n_kvh], zero
 nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, float* out, int n_qh, int n_kvh,
                       int64_t n_pos, const int64_t* pos_dev, int64_t kv_stride, float* part, unsigned* counters,
-                      int S, cudaStream_t st);
+                      int S, cudaStream_t st, int nq = 1);
 nt_status launch_softmax(Ctx* c, const float* x, float* y, int64_t n, cudaStream_t st);
 nt_status launch_swiglu(Ctx* c, const float* g, const float* u, float* h, int64_t n, cudaStream_t st);
 nt_status launch_argmax(Ctx* c, const float* v, int64_t n, int32_t* out, unsigned long long* key, unsigned* counter,
                         cudaStream_t st, int32_t* tok_state = nullptr, int64_t* pos_state = nullptr);
 nt_status configure_gemv(Ctx* c);
+nt_status configure_gemm(Ctx* c);
+int gemm_parts(int64_t cols);
+size_t gemm_scratch_bytes(int64_t total_rows, int64_t cols, int M);
+nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool swiglu, const float* X, int64_t ldx,
+                      int M, const float* norm_g, float eps, int64_t cols, const RopeArgs* rope, float* part,
+                      size_t part_bytes, cudaStream_t st);
 nt_status launch_inv_freq(Ctx* c, double* out, int head_dim, float theta, cudaStream_t st);
 nt_status configure_ops(Ctx* c);
 nt_status launch_cos(Ctx* c, const float* a, const float* b, int64_t n, float* out, cudaStream_t st);

@@ -1,0 +1,386 @@
+// qformats.cuh — the GGUF block formats as seen by the quant-GEMV kernels:
+// per-format dot products of one block unit against x held in shared memory
+// as 24-bit fixed point in three byte planes, and the x prologue that builds
+// those planes.  Formats and element values ("Ntransformer" (en.unwiki.net),
+// About; GGUF layouts): Q8_0 d*q; Q4_0 d*(q-8); Q4_K/Q5_K d*sc*q - dmin*m;
+// Q6_K d*sc*(q-32).
+#pragma once
+#include "nt_internal.cuh"
+
+namespace nt {
+namespace qf {
+
+// dp4a: d = c + sum_i a.byte_i * b.byte_i.  Suffixes: signedness of a, then b.
+#define NT_DP4A(name, ta, tb)                                                        \
+  __device__ __forceinline__ int name(uint32_t a, uint32_t b, int c) {               \
+    int d;                                                                           \
+    asm("dp4a." ta "." tb " %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));     \
+    return d;                                                                        \
+  }
+NT_DP4A(dp4_su, "s32", "u32")
+NT_DP4A(dp4_uu, "u32", "u32")
+NT_DP4A(dp4_ss, "s32", "s32")
+NT_DP4A(dp4_us, "u32", "s32")
+#undef NT_DP4A
+
+// N little-endian words from a 2-byte-aligned shared address (the aligned
+// base is formed from p itself so the loads stay shared-memory loads)
+template <int N>
+__device__ __forceinline__ void lds_a2(const uint8_t* p, uint32_t* w) {
+  const uint32_t mis = smem_u32(p) & 3u;
+  const uint32_t* b = reinterpret_cast<const uint32_t*>(p - mis);
+  const uint32_t sh = mis * 8;
+  uint32_t t[N + 1];
+#pragma unroll
+  for (int i = 0; i <= N; ++i) t[i] = b[i];
+#pragma unroll
+  for (int i = 0; i < N; ++i) w[i] = __funnelshift_r(t[i], t[i + 1], sh);
+}
+
+__device__ __forceinline__ float h2f(uint32_t bits16) { return __half2float(__ushort_as_half((unsigned short)bits16)); }
+
+__device__ __forceinline__ void ld4(const uint8_t* p, uint32_t* w) {
+  const uint4 t = *reinterpret_cast<const uint4*>(p);
+  w[0] = t.x;
+  w[1] = t.y;
+  w[2] = t.z;
+  w[3] = t.w;
+}
+
+// ---------------------------------------------------------------------------
+// Shared x.  Each 32-column group g holds x as 24-bit fixed point,
+// x24 = rint(x * 2^sh_g), split into three byte planes
+//   x24 = p2 * 2^16 + p1 * 2^8 + p0   (p2 signed, p1 and p0 unsigned)
+// stored as [p0: 32 B][p1: 32 B][p2: 32 B][16 B pad] at goff(g), plus
+// scale[g] = 2^-sh_g and psum[3 * (col/16) + k] = sum of plane k over 16
+// columns (for the constant offsets of Q4_0 and Q6_K).  |x - x24 2^-sh| is
+// at most 2^-23 of the group's largest |x|.
+struct XS {
+  const uint8_t* x;
+  const float* scale;
+  const int* psum;
+};
+
+// sum of the three planes' integer dot products: 65536 a2 + 256 a1 + a0
+__device__ __forceinline__ float planes(int a2, int a1, int a0) {
+  return fmaf(float(a2), 65536.0f, fmaf(float(a1), 256.0f, float(a0)));
+}
+
+template <int FMT>
+struct Q;
+
+// Q8_0: d (f16) | qs[32] int8.  value d*q.  unit = one block (one group).
+template <>
+struct Q<NT_Q8_0> {
+  static constexpr int BE = 32, BB = 34, ALIGN = 32, UPB = 1, PB = 0;
+  struct X {
+    uint32_t v[3][8];
+    float s;
+  };
+  __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      ld4(g + 32 * k, x.v[k]);
+      ld4(g + 32 * k + 16, x.v[k] + 4);
+    }
+    x.s = xs.scale[col0 / 32];
+  }
+  __device__ static float dot(const uint8_t* blk, int, const X& x) {
+    uint32_t w[8];
+    lds_a2<8>(blk + 2, w);
+    int a0 = 0, a1 = 0, a2 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      a0 = dp4_us(x.v[0][i], w[i], a0);
+      a1 = dp4_us(x.v[1][i], w[i], a1);
+      a2 = dp4_ss(x.v[2][i], w[i], a2);
+    }
+    const float d = __half2float(*reinterpret_cast<const __half*>(blk));
+    return planes(a2, a1, a0) * (d * x.s);
+  }
+};
+
+// Q4_0: d | qs[16]; element i<16 = low nibble of qs[i], i+16 = high nibble.
+// value d*(q-8).  unit = one block (one group).
+template <>
+struct Q<NT_Q4_0> {
+  static constexpr int BE = 32, BB = 18, ALIGN = 32, UPB = 1, PB = 0;
+  struct X {
+    uint32_t v[3][8];
+    float s;
+    int off[3];  // -8 * sum of each plane over the block
+  };
+  __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      ld4(g + 32 * k, x.v[k]);
+      ld4(g + 32 * k + 16, x.v[k] + 4);
+    }
+    x.s = xs.scale[col0 / 32];
+    const int* ps = xs.psum + 3 * (col0 / 16);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) x.off[k] = -8 * (ps[k] + ps[3 + k]);
+  }
+  __device__ static float dot(const uint8_t* blk, int, const X& x) {
+    uint32_t w[4];
+    lds_a2<4>(blk + 2, w);
+    int a0 = x.off[0], a1 = x.off[1], a2 = x.off[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
+      a0 = dp4_uu(x.v[0][4 + i], hi, dp4_uu(x.v[0][i], lo, a0));
+      a1 = dp4_uu(x.v[1][4 + i], hi, dp4_uu(x.v[1][i], lo, a1));
+      a2 = dp4_su(x.v[2][4 + i], hi, dp4_su(x.v[2][i], lo, a2));
+    }
+    const float d = __half2float(*reinterpret_cast<const __half*>(blk));
+    return planes(a2, a1, a0) * (d * x.s);
+  }
+};
+
+// K-quant scale/min pairs of the two sub-blocks 2c, 2c+1 from header words
+// h1 = scales[0..3], h2 = scales[4..7], h3 = scales[8..11].
+__device__ __forceinline__ void kq_scales(uint32_t h1, uint32_t h2, uint32_t h3, int c, float& sc0, float& sc1,
+                                          float& m0, float& m1) {
+  const int sh = (c & 1) * 16;
+  const uint32_t a1 = h1 >> sh, a2 = h2 >> sh, a3 = h3 >> sh;
+  uint32_t scp, mp;
+  if (c < 2) {
+    scp = a1 & 0x3F3Fu;
+    mp = a2 & 0x3F3Fu;
+  } else {
+    scp = (a3 & 0x0F0Fu) | ((a1 >> 2) & 0x3030u);
+    mp = ((a3 >> 4) & 0x0F0Fu) | ((a2 >> 2) & 0x3030u);
+  }
+  sc0 = float(scp & 0xFFu);
+  sc1 = float((scp >> 8) & 0xFFu);
+  m0 = float(mp & 0xFFu);
+  m1 = float((mp >> 8) & 0xFFu);
+}
+
+// X of the 4/5-bit K formats: unit c = 64 columns = sub-blocks 2c, 2c+1 =
+// groups A (low nibbles) and B (high nibbles).
+struct XK {
+  uint32_t a[3][8], b[3][8];
+  float s0, s1;  // group scales
+  float t0, t1;  // sum(x) over each sub-block
+};
+__device__ __forceinline__ void load_xk(XK& x, const uint8_t* g, const uint8_t* g2, const XS& xs, int col0, int c) {
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    ld4(g + 32 * k, x.a[k]);
+    ld4(g + 32 * k + 16, x.a[k] + 4);
+    ld4(g2 + 32 * k, x.b[k]);
+    ld4(g2 + 32 * k + 16, x.b[k] + 4);
+  }
+  const int col = col0 + 64 * c;
+  x.s0 = xs.scale[col / 32];
+  x.s1 = xs.scale[col / 32 + 1];
+  const int* ps = xs.psum + 3 * (col / 16);
+  x.t0 = planes(ps[2] + ps[5], ps[1] + ps[4], ps[0] + ps[3]) * x.s0;
+  x.t1 = planes(ps[8] + ps[11], ps[7] + ps[10], ps[6] + ps[9]) * x.s1;
+}
+
+__device__ __forceinline__ float kq_combine(uint4 hdr, int c, float qa, float qb, const XK& x) {
+  float sc0, sc1, m0, m1;
+  kq_scales(hdr.y, hdr.z, hdr.w, c, sc0, sc1, m0, m1);
+  const float d = h2f(hdr.x & 0xFFFFu), dmin = h2f(hdr.x >> 16);
+  // sum_j (d sc_j q - dmin m_j) x = d (sc0 s0 qa + sc1 s1 qb) - dmin (m0 t0 + m1 t1)
+  return d * fmaf(sc0 * x.s0, qa, sc1 * x.s1 * qb) - dmin * fmaf(m0, x.t0, m1 * x.t1);
+}
+
+// nibble bytes lo/hi of one qs word against plane words of groups A and B
+#define NT_KQ_MAC(i, lo, hi)                                          \
+  do {                                                                \
+    A0 = dp4_uu(x.a[0][i], lo, A0);                                   \
+    A1 = dp4_uu(x.a[1][i], lo, A1);                                   \
+    A2 = dp4_su(x.a[2][i], lo, A2);                                   \
+    B0 = dp4_uu(x.b[0][i], hi, B0);                                   \
+    B1 = dp4_uu(x.b[1][i], hi, B1);                                   \
+    B2 = dp4_su(x.b[2][i], hi, B2);                                   \
+  } while (0)
+
+// Q4_K: d | dmin | scales[12] | qs[128].  value d*sc*q - dmin*m.
+template <>
+struct Q<NT_Q4_K> {
+  static constexpr int BE = 256, BB = 144, ALIGN = 8, UPB = 4, PB = 1;
+  using X = XK;
+  __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int c) {
+    load_xk(x, g, g + 112, xs, col0, c);
+  }
+  __device__ static float dot(const uint8_t* blk, int c, const X& x) {
+    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+    const uint4* qp = reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
+    const uint4 q0 = qp[0], q1 = qp[1];
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    int A0 = 0, A1 = 0, A2 = 0, B0 = 0, B1 = 0, B2 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
+      NT_KQ_MAC(i, lo, hi);
+    }
+    return kq_combine(hdr, c, planes(A2, A1, A0), planes(B2, B1, B0), x);
+  }
+};
+
+// Q5_K: d | dmin | scales[12] | qh[32] | qs[128]; the fifth bit of element l
+// of sub-block j is bit j of qh[l].
+template <>
+struct Q<NT_Q5_K> {
+  static constexpr int BE = 256, BB = 176, ALIGN = 8, UPB = 4, PB = 1;
+  using X = XK;
+  __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int c) {
+    load_xk(x, g, g + 112, xs, col0, c);
+  }
+  __device__ static float dot(const uint8_t* blk, int c, const X& x) {
+    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+    const uint4* hp = reinterpret_cast<const uint4*>(blk + 16);
+    const uint4 h0 = hp[0], h1 = hp[1];
+    const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    const uint4* qp = reinterpret_cast<const uint4*>(blk + 48 + 32 * c);
+    const uint4 q0 = qp[0], q1 = qp[1];
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const int b0 = 2 * c;
+    int A0 = 0, A1 = 0, A2 = 0, B0 = 0, B1 = 0, B2 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t lo = (w[i] & 0x0F0F0F0Fu) | (((hw[i] >> b0) & 0x01010101u) << 4);
+      const uint32_t hi = ((w[i] >> 4) & 0x0F0F0F0Fu) | (((hw[i] >> (b0 + 1)) & 0x01010101u) << 4);
+      NT_KQ_MAC(i, lo, hi);
+    }
+    return kq_combine(hdr, c, planes(A2, A1, A0), planes(B2, B1, B0), x);
+  }
+};
+#undef NT_KQ_MAC
+
+// Q6_K: ql[128] | qh[64] | scales[16] int8 | d.  value d*sc*(q-32).
+// unit u = (half h = u>>1, s = u&1): chunks g = 0..3 of 16 elements at block
+// columns 128h + 32g + 16s + l', l' < 16 (the s-th half of group 4h+g);
+// chunk g has scale scales[8h+2g+s].
+template <>
+struct Q<NT_Q6_K> {
+  static constexpr int BE = 256, BB = 210, ALIGN = 8, UPB = 4, PB = 2;
+  struct X {
+    uint32_t v[4][3][4];  // chunk g, plane k, 4 words (16 columns)
+    float s[4];           // group scales
+    int off[4][3];        // -32 * plane sums over the chunk
+  };
+  __device__ static void load_x(X& x, const uint8_t* g0, const XS& xs, int col0, int u) {
+    const int h = u >> 1, s = u & 1;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint8_t* p = g0 + 112 * (4 * h + g) + 16 * s;
+#pragma unroll
+      for (int k = 0; k < 3; ++k) ld4(p + 32 * k, x.v[g][k]);
+      const int col = col0 + 128 * h + 32 * g + 16 * s;
+      x.s[g] = xs.scale[col / 32];
+      const int* ps = xs.psum + 3 * (col / 16);
+#pragma unroll
+      for (int k = 0; k < 3; ++k) x.off[g][k] = -32 * ps[k];
+    }
+  }
+  __device__ static float dot(const uint8_t* blk, int u, const X& x) {
+    const int h = u >> 1, s = u & 1;
+    uint32_t A[4], B[4], H[4], S[2];
+    lds_a2<4>(blk + 64 * h + 16 * s, A);        // low nibble: chunk 0, high: chunk 2
+    lds_a2<4>(blk + 64 * h + 32 + 16 * s, B);   // low nibble: chunk 1, high: chunk 3
+    lds_a2<4>(blk + 128 + 32 * h + 16 * s, H);  // bits 2g..2g+1: top bits of chunk g
+    lds_a2<2>(blk + 192 + 8 * h, S);            // scales[8h .. 8h+7]
+    int a[4][3];
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int k = 0; k < 3; ++k) a[g][k] = x.off[g][k];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t q[4] = {(A[i] & 0x0F0F0F0Fu) | ((H[i] << 4) & 0x30303030u),
+                             (B[i] & 0x0F0F0F0Fu) | ((H[i] << 2) & 0x30303030u),
+                             ((A[i] >> 4) & 0x0F0F0F0Fu) | (H[i] & 0x30303030u),
+                             ((B[i] >> 4) & 0x0F0F0F0Fu) | ((H[i] >> 2) & 0x30303030u)};
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        a[g][0] = dp4_uu(x.v[g][0][i], q[g], a[g][0]);
+        a[g][1] = dp4_uu(x.v[g][1][i], q[g], a[g][1]);
+        a[g][2] = dp4_su(x.v[g][2][i], q[g], a[g][2]);
+      }
+    }
+    // scale of chunk g: scales[8h + 2g + s] = byte (2g + s) of the 8-byte window
+    const float sc0 = float(int8_t(S[0] >> (8 * s)));
+    const float sc1 = float(int8_t(S[0] >> (8 * s + 16)));
+    const float sc2 = float(int8_t(S[1] >> (8 * s)));
+    const float sc3 = float(int8_t(S[1] >> (8 * s + 16)));
+    float t = sc0 * x.s[0] * planes(a[0][2], a[0][1], a[0][0]);
+    t = fmaf(sc1 * x.s[1], planes(a[1][2], a[1][1], a[1][0]), t);
+    t = fmaf(sc2 * x.s[2], planes(a[2][2], a[2][1], a[2][0]), t);
+    t = fmaf(sc3 * x.s[3], planes(a[3][2], a[3][1], a[3][0]), t);
+    const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
+    return d * t;
+  }
+};
+
+// byte offset of 32-column group g: 112 bytes per group, plus PB*16 bytes
+// per 8 groups (one K block), chosen per format so that the 16-byte plane
+// reads of a quarter-warp fall into 8 distinct bank groups
+template <int FMT>
+__host__ __device__ constexpr int goff(int g) {
+  return 112 * g + 16 * Q<FMT>::PB * (g / 8);
+}
+
+template <int FMT>
+__host__ __device__ constexpr int x_bytes(int cols) {
+  return ((goff<FMT>(cols / 32 + 1) + 15) / 16) * 16;
+}
+
+
+// One pass of the x prologue for one warp: 8 lanes per 32-column group, 4
+// columns (x4) per lane, lane `sub` = lane & 7 of group `grp`.  Converts the
+// group to 24-bit fixed point with scale 2^-sh (sh from the exponent of the
+// group's largest |x|), writes its three byte planes, the plane sums of each
+// 16 columns and the scale.  Every lane of the warp must call it (shuffles);
+// `live` = grp is a real group.
+template <int FMT>
+__device__ __forceinline__ void put_x4(float4 x4, bool live, int grp, int sub, uint8_t* xsm, int* psum,
+                                       float* gscale) {
+  float m = fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w)));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+  // m = f * 2^e with f in [0.5, 1): e from the exponent field; scale = 2^(23 - e)
+  const int e = int((__float_as_uint(m) >> 23) & 0xFFu) - 126;
+  const int sh = min(126, max(-126, 23 - e));
+  const float scl = __uint_as_float(uint32_t(127 + sh) << 23);
+  constexpr int kLim = (1 << 23) - 1;
+  const int q0 = max(-kLim, min(kLim, __float2int_rn(x4.x * scl)));
+  const int q1 = max(-kLim, min(kLim, __float2int_rn(x4.y * scl)));
+  const int q2 = max(-kLim, min(kLim, __float2int_rn(x4.z * scl)));
+  const int q3 = max(-kLim, min(kLim, __float2int_rn(x4.w * scl)));
+  // byte planes: plane k holds byte k of the four 24-bit values
+  const uint32_t lo01 = __byte_perm(q0, q1, 0x5410), lo23 = __byte_perm(q2, q3, 0x5410);  // bytes 0,1 of each
+  const uint32_t hi01 = __byte_perm(q0, q1, 0x7632), hi23 = __byte_perm(q2, q3, 0x7632);  // bytes 2,3 of each
+  const uint32_t pw0 = __byte_perm(lo01, lo23, 0x6420);
+  const uint32_t pw1 = __byte_perm(lo01, lo23, 0x7531);
+  const uint32_t pw2 = __byte_perm(hi01, hi23, 0x6420);
+  int ps0 = __dp4a(pw0, 0x01010101u, 0u), ps1 = __dp4a(pw1, 0x01010101u, 0u);
+  int ps2 = __dp4a(int(pw2), 0x01010101, 0);  // plane 2 is signed
+  ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
+  ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
+  ps2 += __shfl_xor_sync(0xffffffffu, ps2, 1);
+  ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
+  ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
+  ps2 += __shfl_xor_sync(0xffffffffu, ps2, 2);
+  if (live) {
+    uint8_t* gp = xsm + goff<FMT>(grp) + 4 * sub;
+    *reinterpret_cast<uint32_t*>(gp) = pw0;
+    *reinterpret_cast<uint32_t*>(gp + 32) = pw1;
+    *reinterpret_cast<uint32_t*>(gp + 64) = pw2;
+    if ((sub & 3) == 0) {
+      int* dst = psum + 3 * (2 * grp + (sub >> 2));
+      dst[0] = ps0;
+      dst[1] = ps1;
+      dst[2] = ps2;
+    }
+    if (sub == 0) gscale[grp] = __uint_as_float(uint32_t(127 - sh) << 23);
+  }
+}
+
+}  // namespace qf
+}  // namespace nt

@@ -78,12 +78,12 @@ class nt_model_desc(ctypes.Structure):
     _fields_ = [(n, _ci) for n in ("n_layers", "d_model", "n_qh", "n_kvh", "head_dim", "ffn", "vocab")] + [
         ("eps", _cf), ("theta", _cf), ("kv_cap", _i64)] + [
         (n, _ci) for n in ("fmt_q", "fmt_k", "fmt_v", "fmt_o", "fmt_gate", "fmt_up", "fmt_down", "fmt_embd",
-                           "fmt_out")]
+                           "fmt_out", "stream_slots")]
 
 
 class nt_layer_ptrs(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "attn_norm", "ffn_norm", "kcache",
-                                   "vcache")]
+                                   "vcache", "host_blob")]
 
 
 _sig("nt_model_init", [_vp, ctypes.POINTER(nt_model_desc), ctypes.POINTER(nt_layer_ptrs), _vp, _vp, _vp,
@@ -92,12 +92,19 @@ _sig("nt_model_destroy", [_vp, _vp])
 _sig("nt_decode_step", [_vp, _vp, ctypes.c_int32, _i64, _vp, _vp, _vp, _vp])
 _sig("nt_layer_skip_calibrate", [_vp, _vp, ctypes.c_int32, _i64, _ci, _vp, _vp, _vp, _vp, _vp])
 _sig("nt_attn_decode_static", [_vp, _vp, _vp, _vp, _ci, _ci, _ci, _i64, _i64, _vp])
+_sig("nt_layer_blob_layout", [ctypes.POINTER(nt_model_desc), ctypes.POINTER(_sz), ctypes.POINTER(_sz)])
+_sig("nt_spec_step", [_vp, _vp, ctypes.c_int32, _i64, _ci, _ci, _vp, _vp, _vp, _vp])
+_sig("nt_gemm_q", [_vp, _ci, _vp, _vp, _vp, _i64, _i64, _ci, _vp, _vp, _cf, _vp])
+_sig("nt_attn_verify", [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _i64, _ci, _i64, _vp])
+_sig("nt_stream_layer", [_vp, _vp, _ci, _vp, _sz, _ci, _vp])
+_sig("nt_model_slot", [_vp, _vp, _ci, ctypes.POINTER(_vp), ctypes.POINTER(_sz), ctypes.POINTER(_ci)])
 
 EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "nt_block_bytes", "nt_block_elems",
             "nt_dequant_rows", "nt_gemv_q", "nt_gemv_q_swiglu", "nt_gemv_q_multi", "nt_rmsnorm", "nt_rope",
             "nt_rope_kv_append", "nt_attn_decode", "nt_softmax", "nt_swiglu", "nt_argmax", "nt_cos_sim",
             "nt_model_init", "nt_model_destroy", "nt_decode_step", "nt_layer_skip_calibrate",
-            "nt_attn_decode_static"]
+            "nt_attn_decode_static", "nt_layer_blob_layout", "nt_stream_layer", "nt_model_slot", "nt_spec_step",
+            "nt_gemm_q", "nt_attn_verify"]
 
 
 def lib():
@@ -227,11 +234,49 @@ def nt_model_init(ctx, desc: nt_model_desc, layers, embd, out, out_norm) -> int:
     arr = (nt_layer_ptrs * len(layers))()
     for i, L in enumerate(layers):
         arr[i] = nt_layer_ptrs(*[_ptr(L.get(n)) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "attn_norm",
-                                                          "ffn_norm", "kcache", "vcache")])
+                                                          "ffn_norm", "kcache", "vcache", "host_blob")])
     h = _vp()
     ctx.check(_lib.nt_model_init(ctx.handle, ctypes.byref(desc), arr, _ptr(embd), _ptr(out), _ptr(out_norm),
                                  ctypes.byref(h)))
     return h.value
+
+
+def nt_gemm_q(ctx, fmt, W, X, Y, rows, cols, M, residual=None, norm_g=None, eps=0.0, stream=None):
+    return ctx.check(_lib.nt_gemm_q(ctx.handle, fmt, _ptr(W), _ptr(X), _ptr(Y), rows, cols, M, _ptr(residual),
+                                    _ptr(norm_g), eps, _stream(stream, Y)))
+
+
+def nt_attn_verify(ctx, q, kcache, vcache, out, n_qh, n_kvh, head_dim, n_pos0, n_query, kv_stride, stream=None):
+    return ctx.check(_lib.nt_attn_verify(ctx.handle, _ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), n_qh, n_kvh,
+                                         head_dim, n_pos0, n_query, kv_stride, _stream(stream, out)))
+
+
+def nt_spec_step(ctx, model: int, token: int, pos: int, k: int, n_draft_layers: int, tokens_out, n_out,
+                 logits=None, stream=None):
+    return ctx.check(_lib.nt_spec_step(ctx.handle, model, token, pos, k, n_draft_layers, _ptr(tokens_out),
+                                       _ptr(n_out), _ptr(logits), _stream(stream, tokens_out)))
+
+
+def nt_layer_blob_layout(desc: nt_model_desc):
+    """Returns (offsets of wq..wd [7 ints], blob bytes)."""
+    off = (_sz * 7)()
+    n = _sz()
+    st = _lib.nt_layer_blob_layout(ctypes.byref(desc), off, ctypes.byref(n))
+    if st != NT_OK:
+        raise NtError(st, "nt_layer_blob_layout failed")
+    return list(off), n.value
+
+
+def nt_stream_layer(ctx, model: int, layer: int, host_src, nbytes: int, slot: int, copy_stream=None):
+    return ctx.check(_lib.nt_stream_layer(ctx.handle, model, layer, _ptr(host_src), nbytes, slot,
+                                          _stream(copy_stream)))
+
+
+def nt_model_slot(ctx, model: int, slot: int):
+    """Returns (slot device address, slot bytes, layer last copied into it)."""
+    p, n, layer = _vp(), _sz(), _ci()
+    ctx.check(_lib.nt_model_slot(ctx.handle, model, slot, ctypes.byref(p), ctypes.byref(n), ctypes.byref(layer)))
+    return p.value, n.value, layer.value
 
 
 def nt_model_destroy(ctx, model: int):

@@ -74,7 +74,10 @@ nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes);
 nt_status nt_ctx_destroy(nt_ctx* ctx);
 /* nt_last_error(NULL) describes the last failed nt_ctx_create of this thread. */
 /* Wait for all work of this context's device, then report any asynchronous
- * CUDA error or device-side timeout flag (NT_ERR_TIMEOUT) and clear the flag. */
+ * CUDA error or device-side flag and clear the flag: NT_ERR_TIMEOUT when a
+ * bounded wait inside a kernel ran out; NT_ERR_INVALID_ARG when a position
+ * held on the device (a decode step continued with token < 0) ran past the
+ * KV cache — the kernels then wrote nothing outside the caches. */
 nt_status nt_ctx_sync(nt_ctx* ctx);
 const char* nt_last_error(const nt_ctx* ctx);
 /* Bytes per block / elements per block of a format (0 for an unknown id). */
@@ -142,11 +145,35 @@ nt_status nt_attn_decode(nt_ctx* ctx, const float* q_dev, const void* kcache_dev
                          float* out_dev, int n_qh, int n_kvh, int head_dim, int64_t n_pos, int64_t kv_stride,
                          void* stream);
 
+/* Causal multi-query decode attention, the attention of the verify pass of
+ * self-speculative decoding [feat]: n_query consecutive tokens whose K/V
+ * are already in the caches; query i (0 <= i < n_query) attends to
+ * positions 0 .. n_pos0 - 1 + i.  q_dev, out_dev fp32 [n_query][n_qh][128];
+ * other arguments as nt_attn_decode; n_query 1..8, n_pos0 + n_query - 1 <=
+ * kv_stride.  n_query = 1 is nt_attn_decode. */
+nt_status nt_attn_verify(nt_ctx* ctx, const float* q_dev, const void* kcache_dev, const void* vcache_dev,
+                         float* out_dev, int n_qh, int n_kvh, int head_dim, int64_t n_pos0, int n_query,
+                         int64_t kv_stride, void* stream);
+
 /* Softmax [code]: y = exp(x - max x) / sum, fp32, n elements (standalone). */
 nt_status nt_softmax(nt_ctx* ctx, const float* x_dev, float* y_dev, int64_t n, void* stream);
 
 /* SwiGLU [feat]: h = silu(gate) * up, fp32, n elements (standalone). */
 nt_status nt_swiglu(nt_ctx* ctx, const float* gate_dev, const float* up_dev, float* h_dev, int64_t n,
+                    void* stream);
+
+/* Verify GEMM of self-speculative decoding [feat] (M = draft length + 1
+ * tokens through one layer's weights at once): for m < M,
+ *   Y_dev[m][r] = sum_c deq(W[r, c]) * xn_m[c] (+ residual_dev[m][r]),
+ * xn_m = rmsnorm(X_dev[m], norm_g_dev, eps) when norm_g_dev is non-NULL,
+ * else X_dev[m].  X_dev fp32 [M][cols] (16-byte aligned, cols a multiple of
+ * 4), Y_dev and residual_dev fp32 [M][rows] (residual may equal Y).  Every
+ * weight byte is read once for all M vectors.  Precision and layout rules
+ * as nt_gemv_q.  M 1..8.  Uses the context scratch beyond its first 32 MiB
+ * for partial sums: NT_ERR_OOM when 4 * M * rows * ceil(cols / 2048) bytes
+ * do not fit. */
+nt_status nt_gemm_q(nt_ctx* ctx, int fmt, const void* W_dev, const float* X_dev, float* Y_dev, int64_t rows,
+                    int64_t cols, int M, const float* residual_dev, const float* norm_g_dev, float eps,
                     void* stream);
 
 /* Greedy sampler [code] inference/: index of the largest of v[0..n), lowest
@@ -167,28 +194,42 @@ typedef struct {
   float eps, theta;
   int64_t kv_cap;                       /* positions per (layer, KV head) in the caches, <= 16384 */
   int fmt_q, fmt_k, fmt_v, fmt_o, fmt_gate, fmt_up, fmt_down, fmt_embd, fmt_out;
+  int stream_slots;                     /* HBM slots for streamed layers: 0 = 2 (double buffering), max 8 */
 } nt_model_desc;
 
-/* Device pointers of one layer.  Weights: row-major block matrices
+/* Pointers of one layer.  Weights: row-major block matrices
  * wq [n_qh*hd x d], wk/wv [n_kvh*hd x d], wo [d x n_qh*hd], wg/wu [ffn x d],
- * wd [d x ffn]; norms fp32 [d]; caches binary16 [n_kvh][kv_cap][head_dim].
- * A streamed layer may leave its weight pointers NULL: nt_stream_layer binds
- * them per step. */
+ * wd [d x ffn]; norms fp32 [d]; caches binary16 [n_kvh][kv_cap][head_dim];
+ * norms and caches always in HBM.
+ * A resident layer sets all seven weight pointers (HBM) and host_blob NULL.
+ * A streamed layer [feat] (pinned-RAM tier [cache]) sets the seven weight
+ * pointers NULL and host_blob to page-locked host memory holding its weights
+ * in the blob layout of nt_layer_blob_layout; every decode step copies it
+ * into one of the model's HBM slots while earlier layers compute. */
 typedef struct {
   const void *wq, *wk, *wv, *wo, *wg, *wu, *wd;
   const float *attn_norm, *ffn_norm;
   void *kcache, *vcache;
+  const void* host_blob;
 } nt_layer_ptrs;
+
+/* Byte layout of one layer's weights as one contiguous blob (the unit the
+ * streaming engine copies): offsets_out[0..6] = offsets of wq, wk, wv, wo,
+ * wg, wu, wd, each a multiple of 256; *blob_bytes_out = total size (a
+ * multiple of 256).  Pure host computation from the descriptor. */
+nt_status nt_layer_blob_layout(const nt_model_desc* desc, size_t offsets_out[7], size_t* blob_bytes_out);
 
 /* Bind a model: copies the descriptor and the pointer table (the buffers stay
  * the caller's) and allocates the model's activations and step state on the
- * device.  embd [vocab x d] and out [vocab x d] are block matrices, out_norm
- * fp32 [d]. */
+ * device, plus, when a layer is streamed, desc->stream_slots HBM slots of
+ * one blob each, a copy stream and its events.  embd [vocab x d] and out
+ * [vocab x d] are block matrices, out_norm fp32 [d].  embd may live in
+ * page-locked host memory: the step reads one row of it per token. */
 nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_ptrs* layers, const void* embd_dev,
                         const void* out_dev, const float* out_norm_dev, nt_model** out);
 nt_status nt_model_destroy(nt_ctx* ctx, nt_model* model);
 
-/* One batch-1 decode step [code] model/ + inference/:
+/* One batch-1 decode step [code] model/ + inference/ + memory/:
  *   x = embd[token];  per layer l with skip_mask_host[l] == 0:
  *     q,k,v = W{q,k,v} rmsnorm(x, g_attn); rope(q, k, pos); K/V[l][:,pos] = f16(k, v)
  *     x += Wo attn(q, K/V[l][:, :pos+1]);  x += Wd (silu(Wg xn) * (Wu xn)), xn = rmsnorm(x, g_ffn)
@@ -197,7 +238,13 @@ nt_status nt_model_destroy(nt_ctx* ctx, nt_model* model);
  * from the previous step (token = its argmax, pos = its pos + 1) with no host
  * round trip.  next_token_dev (nullable) receives the argmax.  Each distinct
  * (skip mask, logits, next_token) is captured once into a CUDA graph and
- * replayed.  skip_mask_host is n_layers bytes or NULL. */
+ * replayed.  skip_mask_host is n_layers bytes or NULL.
+ * Streamed layers: inside the same graph, executed streamed layer i (in layer
+ * order) is copied into slot i mod stream_slots on the model's copy stream;
+ * the first stream_slots copies start with the step and overlap the
+ * resident layers, every later copy waits for the compute of the layer that
+ * last occupied its slot, and each streamed layer's compute waits for its
+ * copy (double buffering with 2 slots).  Skipped layers are not copied. */
 nt_status nt_decode_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos, const uint8_t* skip_mask_host,
                          float* logits_dev, int32_t* next_token_dev, void* stream);
 
@@ -209,6 +256,41 @@ nt_status nt_decode_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t po
 nt_status nt_layer_skip_calibrate(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos, int n_skip,
                                   uint8_t* skip_mask_host, float* cos_host, float* logits_dev,
                                   int32_t* next_token_dev, void* stream);
+
+/* Streaming-engine copy step [feat] (SLEP double buffering), [cache]
+ * (pinned-RAM H2D tier): enqueue on copy_stream the host-to-HBM copy of one
+ * layer blob of `bytes` (= the model's blob size) from page-locked
+ * host_pinned_src into HBM slot `slot`.  `layer` must be a streamed layer of
+ * the model; it is recorded as the slot's occupant.  Ordering is the
+ * caller's: copy_stream must already wait for every kernel still reading the
+ * slot.  nt_decode_step runs this copy itself for each streamed layer; the
+ * call is for staging a layer outside a step (read the slot through
+ * nt_model_slot). */
+nt_status nt_stream_layer(nt_ctx* ctx, nt_model* model, int layer, const void* host_pinned_src, size_t bytes,
+                          int slot, void* copy_stream);
+
+/* HBM address and size of streaming slot `slot`, and the layer last copied
+ * into it (-1: none yet).  NT_ERR_INVALID_ARG when the model streams no
+ * layer or slot is out of range. */
+nt_status nt_model_slot(nt_ctx* ctx, nt_model* model, int slot, void** slot_dev_out, size_t* bytes_out,
+                        int* layer_out);
+
+/* Self-speculative decoding step [feat] (the VRAM-resident layers are the
+ * draft model): from (token, pos) — or, token < 0, from the device state
+ * left by the previous step — draft k tokens greedily with layers
+ * [0, n_draft_layers) (n_draft_layers = 0: every resident, i.e. not
+ * streamed, layer) followed by the final norm, LM head and argmax; then
+ * verify [token, d_1 .. d_k] at positions pos .. pos + k in one pass of all
+ * layers (M = k + 1 GEMMs, causal attention among the k + 1 queries).  With
+ * v_i the argmax of verify row i, d_{i+1} is accepted while d_{i+1} == v_i;
+ * with n accepted, tokens_out_dev[0..n] = v_0 .. v_n (the greedy tokens) and
+ * *n_out_dev = n + 1, and the device state moves to (v_n, pos + n + 1).  The
+ * KV entries written past the accepted ones are overwritten by later steps.
+ * logits_dev (nullable) receives the verify logits [k + 1][vocab].  k is
+ * 1..7; pos + k < kv_cap.  Streamed layers stream in the verify pass as in
+ * nt_decode_step.  One CUDA graph per (k, n_draft_layers, outputs). */
+nt_status nt_spec_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos, int k, int n_draft_layers,
+                       int32_t* tokens_out_dev, int32_t* n_out_dev, float* logits_dev, void* stream);
 
 /* ---- allocation-free attention ------------------------------------------------ */
 

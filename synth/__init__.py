@@ -174,6 +174,12 @@ def _q4_k_m() -> dict:
 
 
 def model_spec(name: str) -> ModelSpec:
+    # "<tiny_* or small_*>_r<N>": the same model with only layers 0..N-1 resident
+    base, sep, tail = name.rpartition("_r")
+    if sep and tail.isdigit() and (base.startswith("tiny_") or base.startswith("small_")):
+        spec = model_spec(base)
+        spec.name, spec.n_resident = name, int(tail)
+        return spec
     if name == "llama8b_q8_0":
         return ModelSpec(name, 32, 4096, 32, 8, 128, 14336, 128256, 1e-5, 500000.0, seed=1,
                          n_prefill=1024, n_gen=128, fmt=_uniform_fmt(Q8_0))
@@ -188,12 +194,12 @@ def model_spec(name: str) -> ModelSpec:
         f = FMT_BY_NAME[name[5:].upper()] if name[5:].upper() in FMT_BY_NAME else None
         fm = _q4_k_m() if name == "tiny_q4_k_m" else _uniform_fmt(f)
         return ModelSpec(name, 3, 512, 8, 2, 128, 768, 1000, 1e-5, 500000.0, seed=7,
-                         n_prefill=37, n_gen=8, fmt=fm)
+                         n_prefill=37, n_gen=32, fmt=fm)
     if name.startswith("small_"):
         f = FMT_BY_NAME[name[6:].upper()] if name[6:].upper() in FMT_BY_NAME else None
         fm = _q4_k_m() if name == "small_q4_k_m" else _uniform_fmt(f)
         return ModelSpec(name, 4, 2048, 16, 4, 128, 6144, 32000, 1e-5, 500000.0, seed=11,
-                         n_prefill=300, n_gen=8, fmt=fm)
+                         n_prefill=300, n_gen=32, fmt=fm)
     raise KeyError(name)
 
 
@@ -209,21 +215,26 @@ class HostModel:
     vcache: np.ndarray
 
 
-def make_host_model(spec: ModelSpec, layers: range | None = None, with_kv: bool = True) -> HostModel:
+def make_host_model(spec: ModelSpec, layers: range | None = None, with_kv: bool = True,
+                    out_view=None) -> HostModel:
+    """out_view(layer, name) may return a preallocated uint8 array [rows,
+    row_bytes] to generate a weight matrix into (layer -1 for "embd"/"out"),
+    or None for a fresh array."""
     s = spec.seed
     Ls = range(spec.n_layers) if layers is None else layers
+    dst = (lambda li, t: None) if out_view is None else out_view
     lay = []
     for li in Ls:
         d = {}
         for t in LAYER_TENSORS:
             r, c = spec.tensor_shape(t)
-            d[t] = quant_matrix(spec.fmt[t], r, c, s, spec.stream_of(t, li))
+            d[t] = quant_matrix(spec.fmt[t], r, c, s, spec.stream_of(t, li), out=dst(li, t))
         d["attn_norm"] = normal_f32(spec.d_model, s, spec.stream_of("attn_norm", li), 1.0, 0.02)
         d["ffn_norm"] = normal_f32(spec.d_model, s, spec.stream_of("ffn_norm", li), 1.0, 0.02)
         lay.append(d)
     r, c = spec.tensor_shape("embd")
-    embd = quant_matrix(spec.fmt["embd"], r, c, s, spec.stream_of("embd"))
-    out = quant_matrix(spec.fmt["out"], r, c, s, spec.stream_of("out"))
+    embd = quant_matrix(spec.fmt["embd"], r, c, s, spec.stream_of("embd"), out=dst(-1, "embd"))
+    out = quant_matrix(spec.fmt["out"], r, c, s, spec.stream_of("out"), out=dst(-1, "out"))
     out_norm = normal_f32(spec.d_model, s, spec.stream_of("out_norm"), 1.0, 0.02)
     if with_kv:
         kc, vc = make_kv_cache(spec)

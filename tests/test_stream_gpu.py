@@ -1,0 +1,166 @@
+"""Layer streaming from page-locked host memory (the SLEP double-buffered
+pipeline and the pinned-RAM tier of "ntransformer - moteur d'inférence
+NVMe-to-GPU…", "Fonctionnalités principales" and "Performances et structure
+de cache"), on the GPU.
+
+Pins: a streamed model runs the same kernels on the same bytes as the
+resident one, so its logits are bit-identical to the resident model's, for
+any slot count; and it matches the fp64 oracle within the decode tolerance.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import need_gpu, torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    need_gpu()
+    from block_quantized_gemv_nt_gb300 import nt
+    c = nt.Context(0)
+    yield c
+    c.sync()
+    c.close()
+
+
+def _models(ctx, name, stream_slots=0):
+    """(spec, host model, streamed device model): the streamed layers' host
+    arrays are views of the page-locked blobs."""
+    from block_quantized_gemv_nt_gb300 import engine
+    spec = synth.model_spec(name)
+    blobs = engine.HostBlobs(spec, stream_slots)
+    hm = synth.make_host_model(spec, out_view=blobs.view)
+    gm = engine.DeviceModel(ctx, spec, hm, blobs=blobs, stream_slots=stream_slots)
+    return spec, hm, gm
+
+
+def _greedy(gm, spec, n, skip=None):
+    out = []
+    tok, pos = spec.first_token, spec.n_prefill
+    for i in range(n):
+        lg = gm.step(tok, pos, skip) if i == 0 else gm.step(-1, 0, skip)
+        out.append(lg.clone())
+        tok, pos = int(gm.next_token.item()), pos + 1
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("name,slots", [("tiny_q4_k_m_r0", 0), ("small_q6_k_r1", 0), ("small_q6_k_r1", 3),
+                                        ("small_q4_k_m_r2", 1)])
+def test_streamed_equals_resident_bit_exact(ctx, name, slots):
+    from block_quantized_gemv_nt_gb300 import engine
+    spec, hm, gs = _models(ctx, name, slots)
+    rspec = synth.model_spec(name.rsplit("_r", 1)[0])
+    gr = engine.DeviceModel(ctx, rspec, hm)
+    a = _greedy(gs, spec, 4)
+    b = _greedy(gr, rspec, 4)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    # the streamed layers' KV went to the same caches as the resident model's
+    for li in range(spec.n_layers):
+        assert torch.equal(gs.layers[li]["kcache"], gr.layers[li]["kcache"])
+        assert torch.equal(gs.layers[li]["vcache"], gr.layers[li]["vcache"])
+    gs.close()
+    gr.close()
+
+
+@pytest.mark.parametrize("name", ["tiny_q4_k_m_r0", "small_q6_k_r1"])
+def test_streamed_decode_matches_oracle(ctx, name):
+    spec, hm, gm = _models(ctx, name)
+    om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
+    tok, pos = spec.first_token, spec.n_prefill
+    for _ in range(5):
+        got = gm.step(tok, pos).cpu().numpy().astype(np.float64)
+        ref = om.step(tok, pos)
+        assert np.max(np.abs(got - ref)) <= 2e-2 * ref.std()
+        assert int(np.argmax(got)) == int(np.argmax(ref))
+        tok, pos = int(np.argmax(got)), pos + 1
+    gm.close()
+
+
+def test_streamed_decode_with_skip_mask(ctx):
+    """Skipped streamed layers are not copied; the rest still match the oracle
+    running the same mask."""
+    spec, hm, gm = _models(ctx, "small_q4_k_m_r1")
+    om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
+    skip = np.zeros(spec.n_layers, np.uint8)
+    skip[2] = 1
+    tok, pos = spec.first_token, spec.n_prefill
+    for _ in range(3):
+        got = gm.step(tok, pos, skip).cpu().numpy().astype(np.float64)
+        ref = om.step(tok, pos, skip)
+        assert np.max(np.abs(got - ref)) <= 2e-2 * ref.std()
+        assert int(np.argmax(got)) == int(np.argmax(ref))
+        tok, pos = int(np.argmax(got)), pos + 1
+    gm.close()
+
+
+def test_streamed_calibration(ctx):
+    """Calibration runs the streaming schedule eagerly (no graph)."""
+    spec, hm, gm = _models(ctx, "small_q6_k_r1")
+    om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
+    mask, cos = gm.calibrate(spec.first_token, spec.n_prefill, n_skip=1)
+    _, ref_cos = om.step(spec.first_token, spec.n_prefill, want_cos=True)
+    assert np.max(np.abs(cos - ref_cos)) <= 1e-4
+    gm.close()
+
+
+def test_stream_layer_copies_the_blob(ctx):
+    """nt_stream_layer lands the blob bytes in the slot: every matrix read back
+    from the slot dequantises exactly like the host copy."""
+    from block_quantized_gemv_nt_gb300 import engine, nt
+    spec, hm, gm = _models(ctx, "small_q4_k_m_r1")
+    blobs = gm.blobs
+    st = torch.cuda.Stream()
+    nt.nt_stream_layer(ctx, gm.handle, 3, blobs.blob[3], blobs.nbytes, 1, st)
+    st.synchronize()
+    base, nbytes, occupant = nt.nt_model_slot(ctx, gm.handle, 1)
+    assert nbytes == blobs.nbytes and occupant == 3
+    for i, name in enumerate(engine.LAYER):
+        rows, cols = spec.tensor_shape(name)
+        n = min(rows, 64)
+        got = torch.empty(n * cols, device="cuda")
+        ref = torch.empty(n * cols, device="cuda")
+        host = torch.from_numpy(hm.layers[3][name][:n]).cuda()
+        nt.nt_dequant_rows(ctx, spec.fmt[name], base + blobs.offsets[i], 0, n, cols, got)
+        nt.nt_dequant_rows(ctx, spec.fmt[name], host, 0, n, cols, ref)
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref), name
+    gm.close()
+
+
+def test_stream_bad_args(ctx):
+    from block_quantized_gemv_nt_gb300 import engine, nt
+    spec, hm, gm = _models(ctx, "tiny_q8_0_r1")
+    blobs = gm.blobs
+    st = torch.cuda.Stream()
+    cases = [
+        dict(layer=0, slot=0, nbytes=blobs.nbytes),        # resident layer
+        dict(layer=1, slot=2, nbytes=blobs.nbytes),        # slot out of range
+        dict(layer=1, slot=0, nbytes=blobs.nbytes - 256),  # wrong size
+    ]
+    for c in cases:
+        with pytest.raises(nt.NtError) as ei:
+            nt.nt_stream_layer(ctx, gm.handle, c["layer"], blobs.blob[1], c["nbytes"], c["slot"], st)
+        assert ei.value.status == nt.NT_ERR_INVALID_ARG
+    pageable = torch.empty(blobs.nbytes, dtype=torch.uint8)
+    with pytest.raises(nt.NtError) as ei:
+        nt.nt_stream_layer(ctx, gm.handle, 1, pageable, blobs.nbytes, 0, st)
+    assert ei.value.status == nt.NT_ERR_INVALID_ARG
+    # a layer with some weight pointers and a host blob is refused at model init
+    layers = [dict(L) for L in gm.layers]
+    layers[1]["wq"] = gm.layers[0]["wq"]
+    with pytest.raises(nt.NtError) as ei:
+        nt.nt_model_init(ctx, engine.model_desc(spec), layers, gm.embd, gm.out, gm.out_norm)
+    assert ei.value.status == nt.NT_ERR_INVALID_ARG
+    # a pageable host blob is refused too
+    layers = [dict(L) for L in gm.layers]
+    layers[1]["host_blob"] = pageable
+    with pytest.raises(nt.NtError) as ei:
+        nt.nt_model_init(ctx, engine.model_desc(spec), layers, gm.embd, gm.out, gm.out_norm)
+    assert ei.value.status == nt.NT_ERR_INVALID_ARG
+    gm.close()
