@@ -129,12 +129,15 @@ def profile_traffic(kernel_tag: str, workload: str):
 # ---------------------------------------------------------------------------
 # GEMV workloads: Q8_0 4096x4096 (seed 0) and the format sweep shapes
 def parse_gemv(name):
-    """gemv_<fmt>_<rows>x<cols>, e.g. gemv_q8_0_4096x4096, gemv_q4_k_8192x28672"""
+    """gemv_<fmt>_<rows>x<cols>, e.g. gemv_q8_0_4096x4096, gemv_q4_k_8192x28672;
+    gemm_<fmt>_<rows>x<cols>_m<M> for the M-vector verify GEMM.  Returns
+    (fmt, rows, cols, M)."""
     import synth
     parts = name.split("_")
     fmt = synth.FMT_BY_NAME[(parts[1] + "_" + parts[2]).upper()]
     rows, cols = (int(v) for v in parts[3].split("x"))
-    return fmt, rows, cols
+    M = int(parts[4][1:]) if len(parts) > 4 else 1
+    return fmt, rows, cols, M
 
 
 def bench_gemv(args, rank, world):
@@ -143,28 +146,36 @@ def bench_gemv(args, rank, world):
     import synth
     from block_quantized_gemv_nt_gb300 import nt
 
-    fmt, rows, cols = parse_gemv(args.workload)
+    fmt, rows, cols, M = parse_gemv(args.workload)
+    gemm = args.workload.startswith("gemm")
     seed = 0 if (fmt == synth.Q8_0 and rows == 4096 and cols == 4096) else 100 + fmt
     W = synth.quant_matrix(fmt, rows, cols, seed=seed, stream=0)
-    x = synth.normal_f32(cols, seed=seed, stream=1)
+    x = synth.normal_f32(M * cols, seed=seed, stream=1)
     ctx = nt.Context(torch.cuda.current_device())
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     wbytes = W.nbytes
     ncopy = max(1, -(-4 * l2 // wbytes))          # rotate copies so the set is >= 4x L2
     Wd = [torch.from_numpy(W).cuda() for _ in range(ncopy)]
     xd = torch.from_numpy(x).cuda()
-    y = torch.empty(rows, dtype=torch.float32, device="cuda")
+    y = torch.empty(M * rows, dtype=torch.float32, device="cuda")
     st = torch.cuda.Stream()
-    algo = wbytes + 4 * cols + 4 * rows
+    algo = wbytes + 4 * M * (cols + rows)
+
+    def launch(i, xin):
+        if gemm:
+            nt.nt_gemm_q(ctx, fmt, Wd[i % ncopy], xin, y, rows, cols, M)
+        else:
+            nt.nt_gemv_q(ctx, fmt, Wd[i % ncopy], xin, y, rows, cols)
+
     with torch.cuda.stream(st):
         for i in range(max(3, args.warmup)):
-            nt.nt_gemv_q(ctx, fmt, Wd[i % ncopy], xd, y, rows, cols)
+            launch(i, xd)
         st.synchronize()
         # CUDA graph of K launches over the rotating copies (launch overhead out of the way)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=st):
             for i in range(args.steps):
-                nt.nt_gemv_q(ctx, fmt, Wd[i % ncopy], xd, y, rows, cols)
+                launch(i, xd)
         g.replay()
         st.synchronize()
         barrier(world)
@@ -185,19 +196,19 @@ def bench_gemv(args, rank, world):
 
     # e2e through the C ABI with host buffers: x from pinned host in, y back to pinned host
     xh = torch.from_numpy(x).pin_memory()
-    yh = torch.empty(rows, dtype=torch.float32).pin_memory()
+    yh = torch.empty(M * rows, dtype=torch.float32).pin_memory()
     xdev = torch.empty_like(xd)
     with torch.cuda.stream(st):
         for i in range(3):
             xdev.copy_(xh, non_blocking=True)
-            nt.nt_gemv_q(ctx, fmt, Wd[i % ncopy], xdev, y, rows, cols)
+            launch(i, xdev)
             yh.copy_(y, non_blocking=True)
         st.synchronize()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(st)
         for i in range(args.steps):
             xdev.copy_(xh, non_blocking=True)
-            nt.nt_gemv_q(ctx, fmt, Wd[i % ncopy], xdev, y, rows, cols)
+            launch(i, xdev)
             yh.copy_(y, non_blocking=True)
         f1.record(st)
         f1.synchronize()
@@ -209,32 +220,47 @@ def bench_gemv(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(per_launch_s * 1e3, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32 (block-quantized weights)",
         "data": "synthetic seeded blocks", "impl": "ours",
-        "config": {"workload": args.workload, "fmt": synth.FMT_NAMES[fmt], "rows": rows, "cols": cols,
+        "config": {"workload": args.workload, "fmt": synth.FMT_NAMES[fmt], "rows": rows, "cols": cols, "M": M,
                    "seed": seed, "l2": f"rotating {ncopy} weight copies ({ncopy * wbytes / 2**20:.0f} MiB >= 4x L2)"},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
                      "traffic": profile_traffic("qgemv", args.workload), "algo_bytes_per_launch": algo},
-        "e2e": {"value": round(algo / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": 4 * cols,
-                "d2h_bytes_per_step": 4 * rows},
-        "gpu_launches": args.steps,
+        "e2e": {"value": round(algo / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": 4 * M * cols,
+                "d2h_bytes_per_step": 4 * M * rows},
+        "gpu_launches": args.steps * (2 if gemm else 1),
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_gemv(fmt, W, x, rows, cols, algo)
+        line["cpu_baseline"] = cpu_gemv(fmt, W, x.reshape(M, cols), rows, cols, algo)
     return line
 
 
-def cpu_gemv(fmt, W, x, rows, cols, algo, budget_s=10.0):
+def cpu_gemv(fmt, W, X, rows, cols, algo, budget_s=10.0):
+    """The oracle's GEMV over the same inputs (M vectors: M oracle GEMVs),
+    with all host cores and, on a shorter sample, one thread."""
     import oracle
-    xd = x.astype(np.float64)
-    n = 0
-    t0 = time.perf_counter()
-    while time.perf_counter() - t0 < budget_s or n == 0:
-        oracle.gemv(fmt, W, xd, rows, cols)
-        n += 1
-    dt = (time.perf_counter() - t0) / n
-    return {"value": round(algo / dt / 1e9, 3), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} full oracle GEMVs ({rows}x{cols}) in {n * dt:.1f} s"}
+    Xd = X.astype(np.float64)
+
+    def rate(budget):
+        n = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < budget or n == 0:
+            for xv in Xd:
+                oracle.gemv(fmt, W, xv, rows, cols)
+            n += 1
+        return (time.perf_counter() - t0) / n, n
+
+    dt, n = rate(budget_s)
+    cores = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        dt1, n1 = rate(budget_s / 4)
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": round(algo / dt / 1e9, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "value_1_thread": round(algo / dt1 / 1e9, 3),
+            "sample": f"{n} full oracle passes ({len(Xd)} x {rows}x{cols}) in {n * dt:.1f} s; "
+                      f"{n1} on one thread in {n1 * dt1:.1f} s"}
 
 
 # ---------------------------------------------------------------------------
@@ -504,7 +530,13 @@ def bench_streamed(args, rank, world):
     hm = synth.make_host_model(spec, out_view=blobs.view)
     t_gen = time.perf_counter() - t0
     ctx = nt.Context(torch.cuda.current_device())
-    gm = engine.DeviceModel(ctx, spec, hm, blobs=blobs)
+    slots = args.stream_slots
+    if slots <= 0:
+        # as many slots as the weight cap leaves room for (2..8)
+        r, c = spec.tensor_shape("out")
+        fixed = spec.n_resident * spec.layer_bytes() + r * synth.row_bytes(spec.fmt["out"], c)
+        slots = int(max(2, min(8, (args.hbm_weight_cap * 1e9 - fixed) // blobs.nbytes)))
+    gm = engine.DeviceModel(ctx, spec, hm, blobs=blobs, stream_slots=slots)
     st = torch.cuda.Stream()
     P = spec.n_prefill
     n_streamed = len(blobs.layers)
@@ -581,7 +613,7 @@ def bench_streamed(args, rank, world):
         "data": "synthetic: random weights of the named shape, seeded", "impl": "ours",
         "config": {"workload": args.workload, "layers": spec.n_layers, "resident_layers": spec.n_resident,
                    "streamed_layers": n_streamed, "stream_slots": gm.n_slots, "layer_blob_bytes": blobs.nbytes,
-                   "hbm_weight_bytes": hbm_w, "d_model": spec.d_model, "ffn": spec.ffn, "vocab": spec.vocab,
+                   "hbm_weight_bytes": hbm_w, "hbm_weight_cap_gb": args.hbm_weight_cap, "d_model": spec.d_model, "ffn": spec.ffn, "vocab": spec.vocab,
                    "kv_prefill": P, "batch": 1, "seed": spec.seed,
                    "weights": {kk: synth.FMT_NAMES[v] for kk, v in spec.fmt.items()},
                    "decode": f"self-speculative, k={k} drafts by the resident layers" if k else "greedy",
@@ -665,18 +697,19 @@ def reference_arm(args, rank, world):
     if rank != 0:
         return None
     import synth
-    if args.workload.startswith("gemv"):
-        fmt, rows, cols = parse_gemv(args.workload)
+    if args.workload.startswith("gem"):
+        fmt, rows, cols, M = parse_gemv(args.workload)
         seed = 0 if (fmt == synth.Q8_0 and rows == 4096 and cols == 4096) else 100 + fmt
         W = synth.quant_matrix(fmt, rows, cols, seed=seed, stream=0)
-        x = synth.normal_f32(cols, seed=seed, stream=1)
-        algo = W.nbytes + 4 * cols + 4 * rows
+        X = synth.normal_f32(M * cols, seed=seed, stream=1).reshape(M, cols).astype(np.float64)
+        algo = W.nbytes + 4 * M * (cols + rows)
         import oracle
         for _ in range(max(1, min(args.warmup, 2))):
-            oracle.gemv(fmt, W, x.astype(np.float64), rows, cols)
+            oracle.gemv(fmt, W, X[0], rows, cols)
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            oracle.gemv(fmt, W, x.astype(np.float64), rows, cols)
+            for xv in X:
+                oracle.gemv(fmt, W, xv, rows, cols)
         dt = (time.perf_counter() - t0) / args.steps
         v = round(algo / dt / 1e9, 3)
         return {"metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -724,6 +757,9 @@ def main():
     ap.add_argument("--ref-max-steps", type=int, default=8, help="oracle steps per reference-arm run")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stream-slots", type=int, default=0,
+                    help="HBM slots for streamed layers (0: as many as --hbm-weight-cap allows, 2..8)")
+    ap.add_argument("--hbm-weight-cap", type=float, default=24.0, help="GB of HBM for weights, streamed models")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -739,7 +775,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    if args.workload.startswith("gemv"):
+    if args.workload.startswith("gemv") or args.workload.startswith("gemm"):
         line = bench_gemv(args, rank, world)
     elif args.workload.startswith("attn"):
         line = bench_attn(args, rank, world)

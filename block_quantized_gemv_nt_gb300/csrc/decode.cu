@@ -271,14 +271,13 @@ nt_status enqueue_step(Ctx* c, nt_model* m, const uint8_t* skip, const StepIO& i
 // the verify pass: tokens spec_tok[0..M) at positions spec_pos[0] + i
 // through every layer (M-vector GEMMs, causal M-query attention), logits
 // [M][vocab], row argmaxes into vtok
-nt_status enqueue_verify(Ctx* c, nt_model* m, int M, float* logits, cudaStream_t st) {
+// sm: the pass's streaming schedule, begun by the caller (its first copies
+// may overlap the drafts)
+nt_status enqueue_verify(Ctx* c, nt_model* m, int M, float* logits, Streamer& sm, cudaStream_t st) {
   const nt_model_desc& d = m->d;
   const int hd = d.head_dim;
   const int64_t nq = int64_t(d.n_qh) * hd, nkv = int64_t(d.n_kvh) * hd;
-  Streamer sm{c, m, st};
-  nt_status s = sm.begin(nullptr);
-  if (s) return s;
-  s = launch_embed(c, d.fmt_embd, m->embd, d.d_model, m->spec_tok, m->xv, st, M);
+  nt_status s = launch_embed(c, d.fmt_embd, m->embd, d.d_model, m->spec_tok, m->xv, st, M);
   if (s) return s;
   const RopeArgs ra{m->spec_pos, m->inv_freq, hd, d.kv_cap};
   for (int l = 0; l < d.n_layers; ++l) {
@@ -385,10 +384,18 @@ nt_status enqueue_spec(Ctx* c, nt_model* m, int k, int n_draft, int32_t* out, in
                            "spec setup launch");
   if (s) return s;
   const std::vector<uint8_t> mask = draft_mask(m, n_draft);
+  // the verify pass's first layer copies start now and overlap the drafts
+  // (drafts that run streamed layers stream them themselves, so then the
+  // verify's copies start after the drafts)
+  bool drafts_stream = false;
+  for (int l = 0; l < m->d.n_layers; ++l) drafts_stream = drafts_stream || (!mask[l] && m->host_blob[l]);
+  Streamer sm{c, m, st};
+  if (!drafts_stream) s = sm.begin(nullptr);
   for (int i = 0; i < k && !s; ++i)
     s = enqueue_step(c, m, mask.data(), StepIO{m->spec_tok + i, m->spec_pos + i, m->dlogits, m->spec_tok + i + 1, false},
                      st, false);
-  if (!s) s = enqueue_verify(c, m, M, logits ? logits : m->lv, st);
+  if (!s && drafts_stream) s = sm.begin(nullptr);
+  if (!s) s = enqueue_verify(c, m, M, logits ? logits : m->lv, sm, st);
   if (!s)
     s = cuda_check(c, launch_k(c, spec_accept_kernel, dim3(1), dim3(32), 0, st, m->spec_tok, m->vtok, k, out, n_out,
                                m->tok, m->pos, m->spec_pos),

@@ -136,9 +136,11 @@ struct AttnArgs {
   int64_t part_stride;     // floats between the partials of consecutive queries
 };
 
-// a warp partial row in shared memory: o[128] (16-byte aligned), then m, l, 2 pad
+// a partial row (a warp's in shared memory, a CTA's in scratch): o[128]
+// (16-byte aligned), then m, l, 2 pad
 constexpr int kWpStride = kHD + 4;
 constexpr int kWpM = kHD, kWpL = kHD + 1;
+constexpr int kPS = kWpStride;  // floats per (split, head) partial in scratch
 
 // shared memory: K and V chunks, q (scaled), combine weights, warp partials
 __host__ __device__ constexpr size_t attn_smem_bytes(int G) {
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     }
   }
   __syncthreads();
-  float* my = partv + (int64_t(g) * a.S + s) * G * (2 + kHD);
+  float* my = partv + (int64_t(g) * a.S + s) * G * kPS;
   for (int i = tid; i < G * (kHD + 1); i += kAttnThreads) {
     const int h = i / (kHD + 1), d = i % (kHD + 1);  // d == kHD: the (m, l) pair
     float M = -INFINITY;
@@ -309,10 +311,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       acc = fmaf(d < kHD ? pw[d] : pw[kWpL], c, acc);
     }
     if (d < kHD) {
-      my[h * (2 + kHD) + 2 + d] = acc;
+      my[h * kPS + d] = acc;
     } else {
-      my[h * (2 + kHD)] = M;
-      my[h * (2 + kHD) + 1] = acc;
+      my[h * kPS + kWpM] = M;
+      my[h * kPS + kWpL] = acc;
     }
   }
 
@@ -329,10 +331,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   // stage every split's (max, sum) in shared memory, turn them into per-split
   // weights w_t = e^(m_t - M) / L, then each output element is an independent
   // sum over the splits
-  const float* base = partv + int64_t(g) * a.S * G * (2 + kHD);
+  const float* base = partv + int64_t(g) * a.S * G * kPS;
   for (int i = tid; i < G * a.S; i += kAttnThreads) {
     const int h = i / a.S, t = i % a.S;
-    wts[h * kMaxChunk + t] = __ldcg(base + (int64_t(t) * G + h) * (2 + kHD));
+    wts[h * kMaxChunk + t] = __ldcg(base + (int64_t(t) * G + h) * kPS + kWpM);
   }
   __syncthreads();
   for (int h = warp; h < G; h += kAttnWarps) {
@@ -343,7 +345,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     for (int t = lane; t < a.S; t += 32) {
       const float mt = wts[h * kMaxChunk + t];
       const float w = mt == -INFINITY ? 0.f : __expf(mt - M);
-      L = fmaf(__ldcg(base + (int64_t(t) * G + h) * (2 + kHD) + 1), w, L);
+      L = fmaf(__ldcg(base + (int64_t(t) * G + h) * kPS + kWpL), w, L);
       wts[h * kMaxChunk + t] = w;
     }
     L = warp_sum(L);
@@ -351,20 +353,29 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     for (int t = lane; t < a.S; t += 32) wts[h * kMaxChunk + t] *= inv;
   }
   __syncthreads();
-  for (int i = tid; i < G * kHD; i += kAttnThreads) {
-    const int h = i / kHD, d = i % kHD;
-    const float* pp = base + int64_t(h) * (2 + kHD) + 2 + d;
-    const int64_t stride = int64_t(G) * (2 + kHD);
-    float O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
+  // each thread: 4 dims of one head, 16-byte loads, two splits per round
+  for (int it = tid; it < G * (kHD / 4); it += kAttnThreads) {
+    const int h = it / (kHD / 4), d4 = 4 * (it % (kHD / 4));
+    const float* pp = base + int64_t(h) * kPS + d4;
+    const int64_t stride = int64_t(G) * kPS;
+    const float* w = wts + h * kMaxChunk;
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f), B = A;
     int t = 0;
-    for (; t + 4 <= a.S; t += 4) {
-      O0 = fmaf(__ldcg(pp + (t + 0) * stride), wts[h * kMaxChunk + t + 0], O0);
-      O1 = fmaf(__ldcg(pp + (t + 1) * stride), wts[h * kMaxChunk + t + 1], O1);
-      O2 = fmaf(__ldcg(pp + (t + 2) * stride), wts[h * kMaxChunk + t + 2], O2);
-      O3 = fmaf(__ldcg(pp + (t + 3) * stride), wts[h * kMaxChunk + t + 3], O3);
+#pragma unroll 4
+    for (; t + 2 <= a.S; t += 2) {
+      const float4 u = __ldcg(reinterpret_cast<const float4*>(pp + t * stride));
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(pp + (t + 1) * stride));
+      const float wu = w[t], wv = w[t + 1];
+      A = make_float4(fmaf(u.x, wu, A.x), fmaf(u.y, wu, A.y), fmaf(u.z, wu, A.z), fmaf(u.w, wu, A.w));
+      B = make_float4(fmaf(v.x, wv, B.x), fmaf(v.y, wv, B.y), fmaf(v.z, wv, B.z), fmaf(v.w, wv, B.w));
     }
-    for (; t < a.S; ++t) O0 = fmaf(__ldcg(pp + t * stride), wts[h * kMaxChunk + t], O0);
-    outv[(int64_t(g) * G + h) * kHD + d] = (O0 + O1) + (O2 + O3);
+    if (t < a.S) {
+      const float4 u = __ldcg(reinterpret_cast<const float4*>(pp + t * stride));
+      const float wu = w[t];
+      A = make_float4(fmaf(u.x, wu, A.x), fmaf(u.y, wu, A.y), fmaf(u.z, wu, A.z), fmaf(u.w, wu, A.w));
+    }
+    *reinterpret_cast<float4*>(outv + (int64_t(g) * G + h) * kHD + d4) =
+        make_float4(A.x + B.x, A.y + B.y, A.z + B.z, A.w + B.w);
   }
   if (tid == 0) cnt[g] = 0u;  // ready for the next launch
 }
@@ -521,10 +532,10 @@ int attn_splits(const Ctx* c, int n_kvh, int64_t kv_stride) {
 int64_t attn_max_stride() { return int64_t(kMaxChunk) * kMaxChunk; }
 
 size_t attn_scratch_bytes(int n_qh, int n_kvh, int S, int nq) {
-  return size_t(nq) * size_t(n_kvh) * S * (n_qh / n_kvh) * (2 + kHD) * sizeof(float) + kAttnCounterBytes;
+  return size_t(nq) * size_t(n_kvh) * S * (n_qh / n_kvh) * kPS * sizeof(float) + kAttnCounterBytes;
 }
 
-size_t attn_part_floats(int n_qh, int n_kvh, int S) { return size_t(n_kvh) * S * (n_qh / n_kvh) * (2 + kHD); }
+size_t attn_part_floats(int n_qh, int n_kvh, int S) { return size_t(n_kvh) * S * (n_qh / n_kvh) * kPS; }
 
 nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, float* out, int n_qh, int n_kvh,
                       int64_t n_pos, const int64_t* pos_dev, int64_t kv_stride, float* part, unsigned* counters,
@@ -667,7 +678,7 @@ extern "C" nt_status nt_attn_decode_static(const float* q, const void* kc, const
   const int64_t need_s = (kv_stride + kMaxChunk - 1) / kMaxChunk;
   if (need_s > S) S = int(need_s);
   if (S > kMaxChunk) S = kMaxChunk;
-  const size_t part_bytes = size_t(n_kvh) * S * (n_qh / n_kvh) * (2 + kHD) * sizeof(float);
+  const size_t part_bytes = size_t(n_kvh) * S * (n_qh / n_kvh) * kPS * sizeof(float);
   if (kAttnStaticPart + part_bytes > kAttnStaticBytes) return NT_ERR_INVALID_ARG;  // beyond the fixed scratch
   cudaStream_t st = as_stream(stream);
   // the combine counters must start at zero; a call cut short may have left them set

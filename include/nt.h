@@ -305,9 +305,9 @@ nt_status nt_spec_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos,
  * thread's current device.  The split partials, the combine counters and the
  * error word live in one fixed 4 MiB array compiled into the library
  * (every GPU that loads the library holds it until the process exits);
- * n_kvh * S * (n_qh / n_kvh) * 130 * 4 + 512 bytes must fit in it, where
+ * n_kvh * S * (n_qh / n_kvh) * 132 * 4 + 512 bytes must fit in it, where
  * S = min(128, max(ceil(SMs / n_kvh), ceil(kv_stride / 128))) — e.g. 64 q
- * heads over 8 KV heads fit for kv_stride up to 16,128 positions.  Larger
+ * heads over 8 KV heads fit for kv_stride up to 15,872 positions.  Larger
  * shapes return NT_ERR_INVALID_ARG before any launch.
  *  - The first call on a device looks up the array's device address and sets
  *    the kernel's shared-memory limit; make that first call before any stream

@@ -208,3 +208,40 @@ def test_spec_step_bad_args(ctx):
             nt.nt_spec_step(ctx, gm.handle, tok, pos, k, nd, t, n)
         assert ei.value.status == nt.NT_ERR_INVALID_ARG
     gm.close()
+
+
+@pytest.mark.parametrize("name,k,n_draft", [("tiny_q4_k_m", 4, 1), ("small_q8_0", 3, 2)])
+def test_spec_accept_rule_with_the_draft_chain(ctx, name, k, n_draft):
+    """The drafts are greedy decode steps of the first n_draft layers (the
+    same kernels as a decode step with the deeper layers skipped), and the
+    step keeps draft i+1 exactly while it equals verify output i: emitted
+    tokens 0..n-1 are drafts 1..n, and draft n+1 (if any) differs from
+    emitted token n."""
+    from block_quantized_gemv_nt_gb300 import engine
+    spec = synth.model_spec(name)
+    hm = synth.make_host_model(spec)
+    gd = engine.DeviceModel(ctx, spec, hm)   # runs the draft chain alone
+    gs = engine.DeviceModel(ctx, spec, hm)   # runs the speculative steps
+    skip = np.zeros(spec.n_layers, np.uint8)
+    skip[n_draft:] = 1
+    tok, pos = spec.first_token, spec.n_prefill
+    for step in range(4):
+        drafts, t = [tok], tok
+        for i in range(k):
+            gd.step(t, pos + i, skip)
+            t = int(gd.next_token.item())
+            drafts.append(t)
+        toks, cnt, _ = gs.spec_step(tok, pos, k, n_draft)
+        n_out = int(cnt.item())
+        out = host(toks)[:n_out].tolist()
+        n = n_out - 1
+        assert out[:n] == drafts[1:n + 1]
+        if n < k:
+            assert drafts[n + 1] != out[n]
+        # the draft model's KV at the accepted positions must hold the real
+        # tokens before the next draft chain: replay them through it
+        for i, t in enumerate([tok] + out[:-1]):
+            gd.step(t, pos + i, skip)
+        tok, pos = out[-1], pos + n_out
+    gd.close()
+    gs.close()

@@ -164,3 +164,31 @@ def test_stream_bad_args(ctx):
         nt.nt_model_init(ctx, engine.model_desc(spec), layers, gm.embd, gm.out, gm.out_norm)
     assert ei.value.status == nt.NT_ERR_INVALID_ARG
     gm.close()
+
+
+@pytest.mark.slow
+def test_llama70b_q6_k_streamed_full_size(ctx):
+    """The streamed 70B all-Q6_K workload (seed 3, 4096 prefilled positions,
+    layers 0..25 resident, 26..79 streamed from page-locked host memory):
+    the weights kept in HBM fit the 24 GB cap; one greedy streamed step, then
+    one self-speculative step (k = 4, the resident layers draft) against the
+    oracle, teacher-forced on the emitted tokens."""
+    spec, hm, gm = _models(ctx, "llama70b_q6_k_streamed")
+    assert gm.hbm_weight_bytes() <= 24e9
+    om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
+    P = spec.n_prefill
+    got = gm.step(spec.first_token, P).cpu().numpy().astype(np.float64)
+    ref = om.step(spec.first_token, P)
+    assert np.max(np.abs(got - ref)) <= 2e-2 * ref.std()
+    assert int(np.argmax(got)) == int(np.argmax(ref))
+    tok = int(np.argmax(got))
+    toks, cnt, vl = gm.spec_step(tok, P + 1, 4)
+    n = int(cnt.item())
+    out = toks.cpu().numpy()[:n].tolist()
+    vl = vl.cpu().numpy().astype(np.float64)
+    seq = [tok] + out[:-1]
+    for i in range(n):
+        ref = om.step(seq[i], P + 1 + i)
+        assert np.max(np.abs(vl[i] - ref)) <= 2e-2 * ref.std()
+        assert int(np.argmax(ref)) == out[i]
+    gm.close()
