@@ -532,10 +532,12 @@ def bench_streamed(args, rank, world):
     ctx = nt.Context(torch.cuda.current_device())
     slots = args.stream_slots
     if slots <= 0:
-        # as many slots as the weight cap leaves room for (2..8)
+        # greedy: double buffering (per-layer compute is far below a layer copy);
+        # speculative: as many slots as the weight cap allows (2..8), so copies
+        # run ahead during the drafts and the resident part of the verify pass
         r, c = spec.tensor_shape("out")
         fixed = spec.n_resident * spec.layer_bytes() + r * synth.row_bytes(spec.fmt["out"], c)
-        slots = int(max(2, min(8, (args.hbm_weight_cap * 1e9 - fixed) // blobs.nbytes)))
+        slots = int(max(2, min(8, (args.hbm_weight_cap * 1e9 - fixed) // blobs.nbytes))) if k else 2
     gm = engine.DeviceModel(ctx, spec, hm, blobs=blobs, stream_slots=slots)
     st = torch.cuda.Stream()
     P = spec.n_prefill
@@ -758,7 +760,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stream-slots", type=int, default=0,
-                    help="HBM slots for streamed layers (0: as many as --hbm-weight-cap allows, 2..8)")
+                    help="HBM slots for streamed layers (0: 2 for greedy decoding; for speculative decoding as "
+                         "many as --hbm-weight-cap allows, 2..8)")
     ap.add_argument("--hbm-weight-cap", type=float, default=24.0, help="GB of HBM for weights, streamed models")
     args = ap.parse_args()
 

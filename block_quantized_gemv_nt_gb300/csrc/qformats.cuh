@@ -52,9 +52,10 @@ __device__ __forceinline__ void ld4(const uint8_t* p, uint32_t* w) {
 // x24 = rint(x * 2^sh_g), split into three byte planes
 //   x24 = p2 * 2^16 + p1 * 2^8 + p0   (p2 signed, p1 and p0 unsigned)
 // stored as [p0: 32 B][p1: 32 B][p2: 32 B][16 B pad] at goff(g), plus
-// scale[g] = 2^-sh_g and psum[3 * (col/16) + k] = sum of plane k over 16
-// columns (for the constant offsets of Q4_0 and Q6_K).  |x - x24 2^-sh| is
-// at most 2^-23 of the group's largest |x|.
+// scale[g] = 2^-sh_g and psum[col/16] = sum of x24 over 16 columns (for the
+// constant offsets of Q4_0 and Q6_K and the mins of the K formats; at most
+// 2^27 in magnitude).  |x - x24 2^-sh| is at most 2^-23 of the group's
+// largest |x|.
 struct XS {
   const uint8_t* x;
   const float* scale;
@@ -64,6 +65,14 @@ struct XS {
 // sum of the three planes' integer dot products: 65536 a2 + 256 a1 + a0
 __device__ __forceinline__ float planes(int a2, int a1, int a0) {
   return fmaf(float(a2), 65536.0f, fmaf(float(a1), 256.0f, float(a0)));
+}
+
+// -c * S split over the planes (S = 65536 (S >> 16) + 256 ((S >> 8) & 255) +
+// (S & 255)), so the constant offset folds exactly into the integer sums
+__device__ __forceinline__ void plane_offsets(int S, int c, int off[3]) {
+  off[0] = -c * (S & 255);
+  off[1] = -c * ((S >> 8) & 255);
+  off[2] = -c * (S >> 16);
 }
 
 template <int FMT>
@@ -85,18 +94,29 @@ struct Q<NT_Q8_0> {
     }
     x.s = xs.scale[col0 / 32];
   }
-  __device__ static float dot(const uint8_t* blk, int, const X& x) {
-    uint32_t w[8];
-    lds_a2<8>(blk + 2, w);
+  // one unit of one row, unpacked: quants and scale
+  struct W {
+    uint32_t q[8];
+    float d;
+  };
+  __device__ static void unpack(const uint8_t* blk, int, W& w) {
+    lds_a2<8>(blk + 2, w.q);
+    w.d = __half2float(*reinterpret_cast<const __half*>(blk));
+  }
+  __device__ static float dotw(const W& w, int, const X& x) {
     int a0 = 0, a1 = 0, a2 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      a0 = dp4_us(x.v[0][i], w[i], a0);
-      a1 = dp4_us(x.v[1][i], w[i], a1);
-      a2 = dp4_ss(x.v[2][i], w[i], a2);
+      a0 = dp4_us(x.v[0][i], w.q[i], a0);
+      a1 = dp4_us(x.v[1][i], w.q[i], a1);
+      a2 = dp4_ss(x.v[2][i], w.q[i], a2);
     }
-    const float d = __half2float(*reinterpret_cast<const __half*>(blk));
-    return planes(a2, a1, a0) * (d * x.s);
+    return planes(a2, a1, a0) * (w.d * x.s);
+  }
+  __device__ static float dot(const uint8_t* blk, int u, const X& x) {
+    W w;
+    unpack(blk, u, w);
+    return dotw(w, u, x);
   }
 };
 
@@ -108,7 +128,7 @@ struct Q<NT_Q4_0> {
   struct X {
     uint32_t v[3][8];
     float s;
-    int off[3];  // -8 * sum of each plane over the block
+    int off[3];  // -8 * sum(x24) over the block, split over the planes
   };
   __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int) {
 #pragma unroll
@@ -117,23 +137,37 @@ struct Q<NT_Q4_0> {
       ld4(g + 32 * k + 16, x.v[k] + 4);
     }
     x.s = xs.scale[col0 / 32];
-    const int* ps = xs.psum + 3 * (col0 / 16);
-#pragma unroll
-    for (int k = 0; k < 3; ++k) x.off[k] = -8 * (ps[k] + ps[3 + k]);
+    const int* ps = xs.psum + col0 / 16;
+    plane_offsets(ps[0] + ps[1], 8, x.off);
   }
-  __device__ static float dot(const uint8_t* blk, int, const X& x) {
-    uint32_t w[4];
-    lds_a2<4>(blk + 2, w);
+  struct W {
+    uint32_t lo[4], hi[4];
+    float d;
+  };
+  __device__ static void unpack(const uint8_t* blk, int, W& w) {
+    uint32_t q[4];
+    lds_a2<4>(blk + 2, q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w.lo[i] = q[i] & 0x0F0F0F0Fu;
+      w.hi[i] = (q[i] >> 4) & 0x0F0F0F0Fu;
+    }
+    w.d = __half2float(*reinterpret_cast<const __half*>(blk));
+  }
+  __device__ static float dotw(const W& w, int, const X& x) {
     int a0 = x.off[0], a1 = x.off[1], a2 = x.off[2];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
-      a0 = dp4_uu(x.v[0][4 + i], hi, dp4_uu(x.v[0][i], lo, a0));
-      a1 = dp4_uu(x.v[1][4 + i], hi, dp4_uu(x.v[1][i], lo, a1));
-      a2 = dp4_su(x.v[2][4 + i], hi, dp4_su(x.v[2][i], lo, a2));
+      a0 = dp4_uu(x.v[0][4 + i], w.hi[i], dp4_uu(x.v[0][i], w.lo[i], a0));
+      a1 = dp4_uu(x.v[1][4 + i], w.hi[i], dp4_uu(x.v[1][i], w.lo[i], a1));
+      a2 = dp4_su(x.v[2][4 + i], w.hi[i], dp4_su(x.v[2][i], w.lo[i], a2));
     }
-    const float d = __half2float(*reinterpret_cast<const __half*>(blk));
-    return planes(a2, a1, a0) * (d * x.s);
+    return planes(a2, a1, a0) * (w.d * x.s);
+  }
+  __device__ static float dot(const uint8_t* blk, int u, const X& x) {
+    W w;
+    unpack(blk, u, w);
+    return dotw(w, u, x);
   }
 };
 
@@ -175,17 +209,22 @@ __device__ __forceinline__ void load_xk(XK& x, const uint8_t* g, const uint8_t* 
   const int col = col0 + 64 * c;
   x.s0 = xs.scale[col / 32];
   x.s1 = xs.scale[col / 32 + 1];
-  const int* ps = xs.psum + 3 * (col / 16);
-  x.t0 = planes(ps[2] + ps[5], ps[1] + ps[4], ps[0] + ps[3]) * x.s0;
-  x.t1 = planes(ps[8] + ps[11], ps[7] + ps[10], ps[6] + ps[9]) * x.s1;
+  const int* ps = xs.psum + col / 16;
+  x.t0 = float(ps[0] + ps[1]) * x.s0;
+  x.t1 = float(ps[2] + ps[3]) * x.s1;
 }
 
-__device__ __forceinline__ float kq_combine(uint4 hdr, int c, float qa, float qb, const XK& x) {
-  float sc0, sc1, m0, m1;
-  kq_scales(hdr.y, hdr.z, hdr.w, c, sc0, sc1, m0, m1);
-  const float d = h2f(hdr.x & 0xFFFFu), dmin = h2f(hdr.x >> 16);
-  // sum_j (d sc_j q - dmin m_j) x = d (sc0 s0 qa + sc1 s1 qb) - dmin (m0 t0 + m1 t1)
-  return d * fmaf(sc0 * x.s0, qa, sc1 * x.s1 * qb) - dmin * fmaf(m0, x.t0, m1 * x.t1);
+// one unit of one row of a 4/5-bit K format, unpacked: the quants of
+// sub-blocks 2c (lo) and 2c+1 (hi) as bytes, their scales and mins, d, dmin
+struct WK {
+  uint32_t lo[8], hi[8];
+  float sc0, sc1, m0, m1, d, dmin;
+};
+__device__ __forceinline__ void kq_header(const uint8_t* blk, int c, WK& w) {
+  const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+  kq_scales(hdr.y, hdr.z, hdr.w, c, w.sc0, w.sc1, w.m0, w.m1);
+  w.d = h2f(hdr.x & 0xFFFFu);
+  w.dmin = h2f(hdr.x >> 16);
 }
 
 // nibble bytes lo/hi of one qs word against plane words of groups A and B
@@ -199,6 +238,16 @@ __device__ __forceinline__ float kq_combine(uint4 hdr, int c, float qa, float qb
     B2 = dp4_su(x.b[2][i], hi, B2);                                   \
   } while (0)
 
+__device__ __forceinline__ float kq_dotw(const WK& w, const XK& x) {
+  int A0 = 0, A1 = 0, A2 = 0, B0 = 0, B1 = 0, B2 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) NT_KQ_MAC(i, w.lo[i], w.hi[i]);
+  const float qa = planes(A2, A1, A0), qb = planes(B2, B1, B0);
+  // sum_j (d sc_j q - dmin m_j) x = d (sc0 s0 qa + sc1 s1 qb) - dmin (m0 t0 + m1 t1)
+  return w.d * fmaf(w.sc0 * x.s0, qa, w.sc1 * x.s1 * qb) - w.dmin * fmaf(w.m0, x.t0, w.m1 * x.t1);
+}
+#undef NT_KQ_MAC
+
 // Q4_K: d | dmin | scales[12] | qs[128].  value d*sc*q - dmin*m.
 template <>
 struct Q<NT_Q4_K> {
@@ -207,18 +256,23 @@ struct Q<NT_Q4_K> {
   __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int c) {
     load_xk(x, g, g + 112, xs, col0, c);
   }
-  __device__ static float dot(const uint8_t* blk, int c, const X& x) {
-    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+  using W = WK;
+  __device__ static void unpack(const uint8_t* blk, int c, W& w) {
+    kq_header(blk, c, w);
     const uint4* qp = reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
     const uint4 q0 = qp[0], q1 = qp[1];
-    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    int A0 = 0, A1 = 0, A2 = 0, B0 = 0, B1 = 0, B2 = 0;
+    const uint32_t q[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
-      NT_KQ_MAC(i, lo, hi);
+      w.lo[i] = q[i] & 0x0F0F0F0Fu;
+      w.hi[i] = (q[i] >> 4) & 0x0F0F0F0Fu;
     }
-    return kq_combine(hdr, c, planes(A2, A1, A0), planes(B2, B1, B0), x);
+  }
+  __device__ static float dotw(const W& w, int, const X& x) { return kq_dotw(w, x); }
+  __device__ static float dot(const uint8_t* blk, int c, const X& x) {
+    W w;
+    unpack(blk, c, w);
+    return dotw(w, c, x);
   }
 };
 
@@ -231,27 +285,29 @@ struct Q<NT_Q5_K> {
   __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int c) {
     load_xk(x, g, g + 112, xs, col0, c);
   }
-  __device__ static float dot(const uint8_t* blk, int c, const X& x) {
-    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+  using W = WK;
+  __device__ static void unpack(const uint8_t* blk, int c, W& w) {
+    kq_header(blk, c, w);
     const uint4* hp = reinterpret_cast<const uint4*>(blk + 16);
     const uint4 h0 = hp[0], h1 = hp[1];
     const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
     const uint4* qp = reinterpret_cast<const uint4*>(blk + 48 + 32 * c);
     const uint4 q0 = qp[0], q1 = qp[1];
-    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t q[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
     const int b0 = 2 * c;
-    int A0 = 0, A1 = 0, A2 = 0, B0 = 0, B1 = 0, B2 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t lo = (w[i] & 0x0F0F0F0Fu) | (((hw[i] >> b0) & 0x01010101u) << 4);
-      const uint32_t hi = ((w[i] >> 4) & 0x0F0F0F0Fu) | (((hw[i] >> (b0 + 1)) & 0x01010101u) << 4);
-      NT_KQ_MAC(i, lo, hi);
+      w.lo[i] = (q[i] & 0x0F0F0F0Fu) | (((hw[i] >> b0) & 0x01010101u) << 4);
+      w.hi[i] = ((q[i] >> 4) & 0x0F0F0F0Fu) | (((hw[i] >> (b0 + 1)) & 0x01010101u) << 4);
     }
-    return kq_combine(hdr, c, planes(A2, A1, A0), planes(B2, B1, B0), x);
+  }
+  __device__ static float dotw(const W& w, int, const X& x) { return kq_dotw(w, x); }
+  __device__ static float dot(const uint8_t* blk, int c, const X& x) {
+    W w;
+    unpack(blk, c, w);
+    return dotw(w, c, x);
   }
 };
-#undef NT_KQ_MAC
-
 // Q6_K: ql[128] | qh[64] | scales[16] int8 | d.  value d*sc*(q-32).
 // unit u = (half h = u>>1, s = u&1): chunks g = 0..3 of 16 elements at block
 // columns 128h + 32g + 16s + l', l' < 16 (the s-th half of group 4h+g);
@@ -262,7 +318,7 @@ struct Q<NT_Q6_K> {
   struct X {
     uint32_t v[4][3][4];  // chunk g, plane k, 4 words (16 columns)
     float s[4];           // group scales
-    int off[4][3];        // -32 * plane sums over the chunk
+    int off[4][3];        // -32 * sum(x24) over the chunk, split over the planes
   };
   __device__ static void load_x(X& x, const uint8_t* g0, const XS& xs, int col0, int u) {
     const int h = u >> 1, s = u & 1;
@@ -273,47 +329,61 @@ struct Q<NT_Q6_K> {
       for (int k = 0; k < 3; ++k) ld4(p + 32 * k, x.v[g][k]);
       const int col = col0 + 128 * h + 32 * g + 16 * s;
       x.s[g] = xs.scale[col / 32];
-      const int* ps = xs.psum + 3 * (col / 16);
-#pragma unroll
-      for (int k = 0; k < 3; ++k) x.off[g][k] = -32 * ps[k];
+      plane_offsets(xs.psum[col / 16], 32, x.off[g]);
     }
   }
-  __device__ static float dot(const uint8_t* blk, int u, const X& x) {
+  // one unit of one row, unpacked: the 6-bit quants of chunks 0..3 (4 words
+  // each, as bytes), their scales, d
+  struct W {
+    uint32_t q[4][4];  // word i of chunk g: q[i][g]
+    float sc[4];
+    float d;
+  };
+  __device__ static void unpack(const uint8_t* blk, int u, W& w) {
     const int h = u >> 1, s = u & 1;
     uint32_t A[4], B[4], H[4], S[2];
     lds_a2<4>(blk + 64 * h + 16 * s, A);        // low nibble: chunk 0, high: chunk 2
     lds_a2<4>(blk + 64 * h + 32 + 16 * s, B);   // low nibble: chunk 1, high: chunk 3
     lds_a2<4>(blk + 128 + 32 * h + 16 * s, H);  // bits 2g..2g+1: top bits of chunk g
     lds_a2<2>(blk + 192 + 8 * h, S);            // scales[8h .. 8h+7]
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w.q[i][0] = (A[i] & 0x0F0F0F0Fu) | ((H[i] << 4) & 0x30303030u);
+      w.q[i][1] = (B[i] & 0x0F0F0F0Fu) | ((H[i] << 2) & 0x30303030u);
+      w.q[i][2] = ((A[i] >> 4) & 0x0F0F0F0Fu) | (H[i] & 0x30303030u);
+      w.q[i][3] = ((B[i] >> 4) & 0x0F0F0F0Fu) | ((H[i] >> 2) & 0x30303030u);
+    }
+    // scale of chunk g: scales[8h + 2g + s] = byte (2g + s) of the 8-byte window
+    w.sc[0] = float(int8_t(S[0] >> (8 * s)));
+    w.sc[1] = float(int8_t(S[0] >> (8 * s + 16)));
+    w.sc[2] = float(int8_t(S[1] >> (8 * s)));
+    w.sc[3] = float(int8_t(S[1] >> (8 * s + 16)));
+    w.d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
+  }
+  __device__ static float dotw(const W& w, int, const X& x) {
     int a[4][3];
 #pragma unroll
     for (int g = 0; g < 4; ++g)
 #pragma unroll
       for (int k = 0; k < 3; ++k) a[g][k] = x.off[g][k];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t q[4] = {(A[i] & 0x0F0F0F0Fu) | ((H[i] << 4) & 0x30303030u),
-                             (B[i] & 0x0F0F0F0Fu) | ((H[i] << 2) & 0x30303030u),
-                             ((A[i] >> 4) & 0x0F0F0F0Fu) | (H[i] & 0x30303030u),
-                             ((B[i] >> 4) & 0x0F0F0F0Fu) | ((H[i] >> 2) & 0x30303030u)};
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        a[g][0] = dp4_uu(x.v[g][0][i], q[g], a[g][0]);
-        a[g][1] = dp4_uu(x.v[g][1][i], q[g], a[g][1]);
-        a[g][2] = dp4_su(x.v[g][2][i], q[g], a[g][2]);
+        a[g][0] = dp4_uu(x.v[g][0][i], w.q[i][g], a[g][0]);
+        a[g][1] = dp4_uu(x.v[g][1][i], w.q[i][g], a[g][1]);
+        a[g][2] = dp4_su(x.v[g][2][i], w.q[i][g], a[g][2]);
       }
-    }
-    // scale of chunk g: scales[8h + 2g + s] = byte (2g + s) of the 8-byte window
-    const float sc0 = float(int8_t(S[0] >> (8 * s)));
-    const float sc1 = float(int8_t(S[0] >> (8 * s + 16)));
-    const float sc2 = float(int8_t(S[1] >> (8 * s)));
-    const float sc3 = float(int8_t(S[1] >> (8 * s + 16)));
-    float t = sc0 * x.s[0] * planes(a[0][2], a[0][1], a[0][0]);
-    t = fmaf(sc1 * x.s[1], planes(a[1][2], a[1][1], a[1][0]), t);
-    t = fmaf(sc2 * x.s[2], planes(a[2][2], a[2][1], a[2][0]), t);
-    t = fmaf(sc3 * x.s[3], planes(a[3][2], a[3][1], a[3][0]), t);
-    const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
-    return d * t;
+    float t = w.sc[0] * x.s[0] * planes(a[0][2], a[0][1], a[0][0]);
+    t = fmaf(w.sc[1] * x.s[1], planes(a[1][2], a[1][1], a[1][0]), t);
+    t = fmaf(w.sc[2] * x.s[2], planes(a[2][2], a[2][1], a[2][0]), t);
+    t = fmaf(w.sc[3] * x.s[3], planes(a[3][2], a[3][1], a[3][0]), t);
+    return w.d * t;
+  }
+  __device__ static float dot(const uint8_t* blk, int u, const X& x) {
+    W w;
+    unpack(blk, u, w);
+    return dotw(w, u, x);
   }
 };
 
@@ -334,8 +404,8 @@ __host__ __device__ constexpr int x_bytes(int cols) {
 // One pass of the x prologue for one warp: 8 lanes per 32-column group, 4
 // columns (x4) per lane, lane `sub` = lane & 7 of group `grp`.  Converts the
 // group to 24-bit fixed point with scale 2^-sh (sh from the exponent of the
-// group's largest |x|), writes its three byte planes, the plane sums of each
-// 16 columns and the scale.  Every lane of the warp must call it (shuffles);
+// group's largest |x|), writes its three byte planes, the sum of x24 over
+// each 16 columns and the scale.  Every lane of the warp must call it (shuffles);
 // `live` = grp is a real group.
 template <int FMT>
 __device__ __forceinline__ void put_x4(float4 x4, bool live, int grp, int sub, uint8_t* xsm, int* psum,
@@ -359,25 +429,16 @@ __device__ __forceinline__ void put_x4(float4 x4, bool live, int grp, int sub, u
   const uint32_t pw0 = __byte_perm(lo01, lo23, 0x6420);
   const uint32_t pw1 = __byte_perm(lo01, lo23, 0x7531);
   const uint32_t pw2 = __byte_perm(hi01, hi23, 0x6420);
-  int ps0 = __dp4a(pw0, 0x01010101u, 0u), ps1 = __dp4a(pw1, 0x01010101u, 0u);
-  int ps2 = __dp4a(int(pw2), 0x01010101, 0);  // plane 2 is signed
-  ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
-  ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
-  ps2 += __shfl_xor_sync(0xffffffffu, ps2, 1);
-  ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
-  ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
-  ps2 += __shfl_xor_sync(0xffffffffu, ps2, 2);
+  // sum of x24 over the 16 columns of this lane's quarter-group (4 lanes)
+  int ps = (q0 + q1) + (q2 + q3);
+  ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+  ps += __shfl_xor_sync(0xffffffffu, ps, 2);
   if (live) {
     uint8_t* gp = xsm + goff<FMT>(grp) + 4 * sub;
     *reinterpret_cast<uint32_t*>(gp) = pw0;
     *reinterpret_cast<uint32_t*>(gp + 32) = pw1;
     *reinterpret_cast<uint32_t*>(gp + 64) = pw2;
-    if ((sub & 3) == 0) {
-      int* dst = psum + 3 * (2 * grp + (sub >> 2));
-      dst[0] = ps0;
-      dst[1] = ps1;
-      dst[2] = ps2;
-    }
+    if ((sub & 3) == 0) psum[2 * grp + (sub >> 2)] = ps;
     if (sub == 0) gscale[grp] = __uint_as_float(uint32_t(127 - sh) << 23);
   }
 }

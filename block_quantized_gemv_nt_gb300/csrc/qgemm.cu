@@ -213,6 +213,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qgemm_kernel(const GemmArgs a
         const int b = u / F::UPB, uu = u % F::UPB;
         const int col0 = b * F::BE;  // column within the part
         const uint8_t* bp = st + b * F::BB;
+        // the R rows' weights of this unit are unpacked once and serve all M vectors
+        typename F::W w[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) F::unpack(bp + i * a.segStride, uu, w[i]);
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
           if (m < a.M) {
@@ -221,7 +225,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) qgemm_kernel(const GemmArgs a
             typename F::X x;
             F::load_x(x, xm + goff<FMT>(col0 / 32 + (F::UPB == 4 && FMT != NT_Q6_K ? 2 * uu : 0)), xs, col0, uu);
 #pragma unroll
-            for (int i = 0; i < R; ++i) acc[i][m] += F::dot(bp + i * a.segStride, uu, x);
+            for (int i = 0; i < R; ++i) acc[i][m] += F::dotw(w[i], uu, x);
           }
         }
       }
@@ -344,7 +348,7 @@ int gemm_cwb() {
 template <int FMT>
 int gemm_vstride() {
   const int ng = kPartCols / 32;
-  return ((x_bytes<FMT>(kPartCols) + 28 * ng) + 15) / 16 * 16;
+  return ((x_bytes<FMT>(kPartCols) + 12 * ng) + 15) / 16 * 16;
 }
 
 int fmt_vstride(int fmt) {

@@ -89,8 +89,8 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
   uint8_t* xsm = smem;
   float* gscale = reinterpret_cast<float*>(smem + xB);
   int* psum = reinterpret_cast<int*>(smem + xB + 4 * ng);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ((xB + 28 * ng + 7) / 8) * 8);
-  uint8_t* stages = smem + ((xB + 28 * ng + 8 + nwarps * kStages * 8 + 127) / 128) * 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ((xB + 12 * ng + 7) / 8) * 8);
+  uint8_t* stages = smem + ((xB + 12 * ng + 8 + nwarps * kStages * 8 + 127) / 128) * 128;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // warps come in slots of a.ks; the warps of a slot share row groups, warp
@@ -447,9 +447,12 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
   int R = 0, kStages = 0, kWarps = 0, head = 0, stb = 0;
   const int al = fi.align;
   // the configured warps and stages; fewer when x leaves too little shared memory
-  for (int nw = c->gemv_warps; nw >= 4 && R == 0; nw /= 2) {
+  const int warp_opts[4] = {c->gemv_warps, 12, 8, 4};
+  for (int wi = 0; wi < 4 && R == 0; ++wi) {
+    const int nw = warp_opts[wi];
+    if (nw > c->gemv_warps || (wi > 0 && nw >= warp_opts[0])) continue;
     for (int ns = c->gemv_stages; ns >= 2 && R == 0; --ns) {
-      head = ((fi.xbytes + 28 * ng + 8 + nw * ns * 8 + 127) / 128) * 128;
+      head = ((fi.xbytes + 12 * ng + 8 + nw * ns * 8 + 127) / 128) * 128;
       const long avail = long(c->smem_optin) - head - pad - c->gemv_static_smem;
       stb = int(avail / (nw * ns)) / 16 * 16;
       if (stb > c->gemv_stage_max) stb = c->gemv_stage_max;
