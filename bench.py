@@ -105,14 +105,22 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def kernel_source_sha() -> str:
+    """First 16 hex digits of the SHA-256 of the quant-GEMV sources (the
+    kernel file and the block-format header it includes)."""
+    h = hashlib.sha256()
+    for f in ("qgemv.cu", "qformats.cuh"):
+        h.update(open(os.path.join(ROOT, "block_quantized_gemv_nt_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def profile_traffic(kernel_tag: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary for this kernel and
     workload, if its recorded source hash still matches the kernel source."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
     if not os.path.exists(path):
         return None
-    src = os.path.join(ROOT, "block_quantized_gemv_nt_gb300", "csrc", "qgemv.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = kernel_source_sha()
     got = {}
     for ln in open(path):
         if ":" in ln:

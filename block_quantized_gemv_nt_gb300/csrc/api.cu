@@ -116,6 +116,8 @@ nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes) {
   c->gemv_stages = env_int("NT_GEMV_STAGES", 2, 8, 2);
   c->gemv_stage_max = env_int("NT_GEMV_STAGE_MAX", 1024, 65536, 12288) / 16 * 16;
   c->pdl = env_int("NT_PDL", 0, 1, 1) != 0;
+  c->gemv_tune = env_int("NT_GEMV_TUNE", 0, 1, 1) != 0;
+  c->attn_fill = env_int("NT_ATTN_FILL", 0, 1, 1) != 0;
   c->scratch_bytes = scratch_bytes ? scratch_bytes : (size_t(64) << 20);
   if (c->scratch_bytes < (size_t(1) << 20)) c->scratch_bytes = size_t(1) << 20;
   if (cudaMalloc(&c->scratch, c->scratch_bytes) != cudaSuccess) {
@@ -302,7 +304,7 @@ nt_status attn_entry(nt_ctx* ctx, const float* q, const void* kc, const void* vc
   NT_REQUIRE(aligned(kc, 16) && aligned(vc, 16), NT_ERR_ALIGNMENT, "caches must be 16-byte aligned");
   const int S = attn_splits(ctx, n_kvh, kv_stride);
   const size_t need = attn_scratch_bytes(n_qh, n_kvh, S, nq);
-  NT_REQUIRE(kScratchAttn + need <= kScratchGemm && kScratchAttn + need <= ctx->scratch_bytes, NT_ERR_OOM,
+  NT_REQUIRE(kScratchAttn + need <= kScratchTune && kScratchAttn + need <= ctx->scratch_bytes, NT_ERR_OOM,
              "attention needs %zu scratch bytes", need);
   float* part = reinterpret_cast<float*>(ctx->scratch + kScratchAttn + kAttnCounterBytes);
   unsigned* counters = reinterpret_cast<unsigned*>(ctx->scratch + kScratchAttn);

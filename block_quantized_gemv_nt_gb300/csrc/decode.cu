@@ -139,6 +139,7 @@ struct Streamer {
   int si = 0;  // ordinal of the next streamed layer
 
   nt_status copy(int i) {
+    if (c->dry) return NT_OK;
     const int NS = m->n_slots, slot = i % NS;
     nt_status r = NT_OK;
     if (i >= NS) r = cuda_check(c, cudaStreamWaitEvent(m->copy_st, m->ev_free[slot], 0), "copy waits for its slot");
@@ -149,7 +150,7 @@ struct Streamer {
   nt_status begin(const uint8_t* skip) {
     for (int l = 0; l < m->d.n_layers; ++l)
       if (!(skip && skip[l]) && m->host_blob[l]) sl.push_back(l);
-    if (sl.empty()) return NT_OK;
+    if (sl.empty() || c->dry) return NT_OK;
     nt_status s = cuda_check(c, cudaEventRecord(m->ev_fork, st), "fork copy stream");
     if (!s) s = cuda_check(c, cudaStreamWaitEvent(m->copy_st, m->ev_fork, 0), "fork copy stream");
     for (int i = 0; i < m->n_slots && i < int(sl.size()) && !s; ++i) s = copy(i);
@@ -162,10 +163,15 @@ struct Streamer {
     if (!m->host_blob[l]) return NT_OK;
     slot = si % m->n_slots;
     bind_slot(m, slot, L);
+    if (c->dry) return NT_OK;
     return cuda_check(c, cudaStreamWaitEvent(st, m->ev_ready[slot], 0), "compute waits for its layer copy");
   }
   nt_status after(int slot) {
     if (slot < 0) return NT_OK;
+    if (c->dry) {
+      ++si;
+      return NT_OK;
+    }
     // the slot is free once this layer's kernels are done: the copy that reuses it may start
     nt_status s = cuda_check(c, cudaEventRecord(m->ev_free[slot], st), "slot free");
     if (!s && si + m->n_slots < int(sl.size())) s = copy(si + m->n_slots);
@@ -173,7 +179,7 @@ struct Streamer {
     return s;
   }
   nt_status end() {
-    if (sl.empty()) return NT_OK;
+    if (sl.empty() || c->dry) return NT_OK;
     nt_status s = cuda_check(c, cudaEventRecord(m->ev_join, m->copy_st), "join copy stream");
     if (!s) s = cuda_check(c, cudaStreamWaitEvent(st, m->ev_join, 0), "join copy stream");
     return s;
@@ -205,7 +211,7 @@ nt_status enqueue_step(Ctx* c, nt_model* m, const uint8_t* skip, const StepIO& i
     int slot;
     s = sm.before(l, L, slot);
     if (s) return s;
-    if (want_cos) {
+    if (want_cos && !c->dry) {
       s = cuda_check(c, cudaMemcpyAsync(m->xin, m->x, sizeof(float) * d.d_model, cudaMemcpyDeviceToDevice, st),
                      "copy x");
       if (s) return s;
@@ -379,9 +385,10 @@ std::vector<uint8_t> draft_mask(const nt_model* m, int n_draft) {
 nt_status enqueue_spec(Ctx* c, nt_model* m, int k, int n_draft, int32_t* out, int32_t* n_out, float* logits,
                        cudaStream_t st) {
   const int M = k + 1;
-  nt_status s = cuda_check(c, launch_k(c, spec_setup_kernel, dim3(1), dim3(32), 0, st, m->tok, m->pos, m->spec_tok,
-                                       m->spec_pos, M),
-                           "spec setup launch");
+  nt_status s = c->dry ? NT_OK
+                       : cuda_check(c, launch_k(c, spec_setup_kernel, dim3(1), dim3(32), 0, st, m->tok, m->pos,
+                                                m->spec_tok, m->spec_pos, M),
+                                    "spec setup launch");
   if (s) return s;
   const std::vector<uint8_t> mask = draft_mask(m, n_draft);
   // the verify pass's first layer copies start now and overlap the drafts
@@ -396,7 +403,7 @@ nt_status enqueue_spec(Ctx* c, nt_model* m, int k, int n_draft, int32_t* out, in
                      st, false);
   if (!s && drafts_stream) s = sm.begin(nullptr);
   if (!s) s = enqueue_verify(c, m, M, logits ? logits : m->lv, sm, st);
-  if (!s)
+  if (!s && !c->dry)
     s = cuda_check(c, launch_k(c, spec_accept_kernel, dim3(1), dim3(32), 0, st, m->spec_tok, m->vtok, k, out, n_out,
                                m->tok, m->pos, m->spec_pos),
                    "spec accept launch");
@@ -423,6 +430,14 @@ nt_status run_graph(Ctx* c, nt_model* m, const std::string& key, cudaStream_t st
   auto it = m->graphs.find(key);
   nt_status s = NT_OK;
   if (it == m->graphs.end()) {
+    if (c->gemv_tune) {
+      // a dry pass first: every GEMV shape of the sequence gets its plan
+      // tuned eagerly on st, so the captured graph holds tuned launches
+      c->dry = true;
+      s = enqueue(st);
+      c->dry = false;
+      if (s) return s;
+    }
     cudaGraph_t g = nullptr;
     cudaGraphExec_t ge = nullptr;
     s = cuda_check(c, cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeThreadLocal), "begin capture");

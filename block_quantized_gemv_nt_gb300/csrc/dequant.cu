@@ -118,6 +118,7 @@ __global__ void embed_kernel(int fmt, const uint8_t* W, int64_t cols, const int3
 
 nt_status launch_embed(Ctx* c, int fmt, const void* W, int64_t cols, const int32_t* token_dev, float* out,
                        cudaStream_t st, int M) {
+  if (c->dry) return NT_OK;
   const int blocks = int((cols + 255) / 256);
   return cuda_check(c, launch_k(c, embed_kernel, dim3(blocks, M), dim3(256), 0, st, fmt, static_cast<const uint8_t*>(W),
                                 cols, token_dev, out),

@@ -8,6 +8,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <map>
 #include <mutex>
 #include <string>
 #include <utility>
@@ -20,6 +21,11 @@ constexpr int kMaxSpin = 1 << 16;   // iteration cap of every device-side wait
 constexpr unsigned kWaitHintNs = 50000;  // each try_wait may sleep this long (cap ~3 s in all)
 constexpr unsigned kErrWaitTimeout = 1u;
 constexpr unsigned kErrPosRange = 2u;  // a device-side position fell outside the KV cache: nothing written there
+
+// a GEMV launch configuration: warps per CTA, stage-size cap, split-K (0 = by balance)
+struct PlanChoice {
+  int warps, stage_max, ks;
+};
 
 struct Ctx {
   int device = 0;
@@ -36,6 +42,10 @@ struct Ctx {
   int gemm_static_smem = 1024;   // same for the verify-GEMM kernels
   std::string last_error;
   std::mutex mu;
+  bool attn_fill = true;         // attention splits: also one CTA per SM (else by positions only)
+  bool gemv_tune = true;         // time candidate plans on a shape's first eager launch
+  bool dry = false;              // enqueue nothing: launchers only tune (a dry pass before a capture)
+  std::map<std::string, PlanChoice> gemv_plans;  // tuned plan per launch shape
 };
 
 // host-side status helpers ----------------------------------------------------
@@ -49,6 +59,7 @@ constexpr size_t kScratchErr = 0;            // unsigned err flag (also ctx->err
 constexpr size_t kScratchArgmax = 256;       // unsigned long long key + unsigned counter
 constexpr size_t kScratchAttn = 4096;        // attention counters (kAttnCounterBytes), then partials
 constexpr size_t kAttnCounterBytes = 2048;   // [queries <= 8][KV heads <= 64] unsigned
+constexpr size_t kScratchTune = size_t(24) << 20;  // GEMV plan tuning outputs (8 MiB)
 constexpr size_t kScratchGemm = size_t(32) << 20;  // verify-GEMM partial sums, to the end of the scratch
 
 // format geometry ---------------------------------------------------------------

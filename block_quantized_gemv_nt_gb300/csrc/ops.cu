@@ -332,9 +332,12 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   // weights w_t = e^(m_t - M) / L, then each output element is an independent
   // sum over the splits
   const float* base = partv + int64_t(g) * a.S * G * kPS;
+  float* lsum = wp;  // the warp partials are merged: their space holds each split's sum
   for (int i = tid; i < G * a.S; i += kAttnThreads) {
     const int h = i / a.S, t = i % a.S;
-    wts[h * kMaxChunk + t] = __ldcg(base + (int64_t(t) * G + h) * kPS + kWpM);
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + (int64_t(t) * G + h) * kPS + kWpM));
+    wts[h * kMaxChunk + t] = ml.x;
+    lsum[h * kMaxChunk + t] = ml.y;
   }
   __syncthreads();
   for (int h = warp; h < G; h += kAttnWarps) {
@@ -345,7 +348,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     for (int t = lane; t < a.S; t += 32) {
       const float mt = wts[h * kMaxChunk + t];
       const float w = mt == -INFINITY ? 0.f : __expf(mt - M);
-      L = fmaf(__ldcg(base + (int64_t(t) * G + h) * kPS + kWpL), w, L);
+      L = fmaf(lsum[h * kMaxChunk + t], w, L);
       wts[h * kMaxChunk + t] = w;
     }
     L = warp_sum(L);
@@ -361,15 +364,20 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     const float* w = wts + h * kMaxChunk;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f), B = A;
     int t = 0;
-#pragma unroll 4
-    for (; t + 2 <= a.S; t += 2) {
-      const float4 u = __ldcg(reinterpret_cast<const float4*>(pp + t * stride));
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(pp + (t + 1) * stride));
-      const float wu = w[t], wv = w[t + 1];
-      A = make_float4(fmaf(u.x, wu, A.x), fmaf(u.y, wu, A.y), fmaf(u.z, wu, A.z), fmaf(u.w, wu, A.w));
-      B = make_float4(fmaf(v.x, wv, B.x), fmaf(v.y, wv, B.y), fmaf(v.z, wv, B.z), fmaf(v.w, wv, B.w));
+    // eight splits' loads in flight before their sums
+    for (; t + 8 <= a.S; t += 8) {
+      float4 u[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) u[j] = __ldcg(reinterpret_cast<const float4*>(pp + (t + j) * stride));
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+        const float wu = w[t + j], wv = w[t + j + 1];
+        A = make_float4(fmaf(u[j].x, wu, A.x), fmaf(u[j].y, wu, A.y), fmaf(u[j].z, wu, A.z), fmaf(u[j].w, wu, A.w));
+        B = make_float4(fmaf(u[j + 1].x, wv, B.x), fmaf(u[j + 1].y, wv, B.y), fmaf(u[j + 1].z, wv, B.z),
+                        fmaf(u[j + 1].w, wv, B.w));
+      }
     }
-    if (t < a.S) {
+    for (; t < a.S; ++t) {
       const float4 u = __ldcg(reinterpret_cast<const float4*>(pp + t * stride));
       const float wu = w[t];
       A = make_float4(fmaf(u.x, wu, A.x), fmaf(u.y, wu, A.y), fmaf(u.z, wu, A.z), fmaf(u.w, wu, A.w));
@@ -523,7 +531,9 @@ nt_status launch_rope_append(Ctx* c, float* q, const float* k, const float* v, v
 // kMaxChunk positions, and at most kMaxChunk splits (the combine stages one
 // weight per split in a kMaxChunk-long row), so kv_stride <= kMaxChunk^2
 int attn_splits(const Ctx* c, int n_kvh, int64_t kv_stride) {
-  int S = (c->num_sms + n_kvh - 1) / n_kvh;
+  // chunks of up to kMaxChunk positions keep every warp on a full 32-position
+  // tile; with attn_fill, also at least one CTA per SM
+  int S = c->attn_fill ? (c->num_sms + n_kvh - 1) / n_kvh : 1;
   const int64_t need = (kv_stride + kMaxChunk - 1) / kMaxChunk;
   if (need > S) S = int(need);
   return S < kMaxChunk ? S : kMaxChunk;
@@ -540,6 +550,7 @@ size_t attn_part_floats(int n_qh, int n_kvh, int S) { return size_t(n_kvh) * S *
 nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, float* out, int n_qh, int n_kvh,
                       int64_t n_pos, const int64_t* pos_dev, int64_t kv_stride, float* part, unsigned* counters,
                       int S, cudaStream_t st, int nq) {
+  if (c->dry) return NT_OK;
   AttnArgs a{};
   a.q_stride = int64_t(n_qh) * kHD;
   a.part_stride = int64_t(attn_part_floats(n_qh, n_kvh, S));
@@ -603,6 +614,7 @@ nt_status launch_swiglu(Ctx* c, const float* g, const float* u, float* h, int64_
 
 nt_status launch_argmax(Ctx* c, const float* v, int64_t n, int32_t* out, unsigned long long* key, unsigned* counter,
                         cudaStream_t st, int32_t* tok_state, int64_t* pos_state) {
+  if (c->dry) return NT_OK;
   int64_t blocks = (n + 1023) / 1024;
   if (blocks > c->num_sms) blocks = c->num_sms;
   if (blocks < 1) blocks = 1;
@@ -612,6 +624,7 @@ nt_status launch_argmax(Ctx* c, const float* v, int64_t n, int32_t* out, unsigne
 }
 
 nt_status launch_cos(Ctx* c, const float* a, const float* b, int64_t n, float* out, cudaStream_t st) {
+  if (c->dry) return NT_OK;
   cos_kernel<<<1, 1024, 0, st>>>(a, b, n, out);
   return cuda_check(c, cudaGetLastError(), "cos launch");
 }

@@ -62,9 +62,11 @@ struct XS {
   const int* psum;
 };
 
-// sum of the three planes' integer dot products: 65536 a2 + 256 a1 + a0
+// sum of the three planes' integer dot products: 65536 a2 + 256 a1 + a0.
+// 256 a1 + a0 is formed in int32 (every format keeps |a1|, |a0| below 2^22,
+// so it cannot overflow), then one fp32 rounding per step.
 __device__ __forceinline__ float planes(int a2, int a1, int a0) {
-  return fmaf(float(a2), 65536.0f, fmaf(float(a1), 256.0f, float(a0)));
+  return fmaf(float(a2), 65536.0f, float(a1 * 256 + a0));
 }
 
 // -c * S split over the planes (S = 65536 (S >> 16) + 256 ((S >> 8) & 255) +
@@ -265,8 +267,9 @@ struct Q<NT_Q4_K> {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       w.lo[i] = q[i] & 0x0F0F0F0Fu;
-      w.hi[i] = (q[i] >> 4) & 0x0F0F0F0Fu;
+      w.hi[i] = q[i] & 0xF0F0F0F0u;  // 16 x the high nibble: no shift; 1/16 in the combine
     }
+    w.sc1 *= 0.0625f;
   }
   __device__ static float dotw(const W& w, int, const X& x) { return kq_dotw(w, x); }
   __device__ static float dot(const uint8_t* blk, int c, const X& x) {

@@ -402,6 +402,7 @@ nt_status configure_gemm(Ctx* c) {
 nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool swiglu, const float* X, int64_t ldx,
                       int M, const float* norm_g, float eps, int64_t cols, const RopeArgs* rope, float* part,
                       size_t part_bytes, cudaStream_t st) {
+  if (c->dry) return NT_OK;
   if (M < 1 || M > kMaxVerify) return set_err(c, NT_ERR_INVALID_ARG, "gemm: M must be 1..%d", kMaxVerify);
   const int BB = block_bytes(fmt), BE = block_elems(fmt);
   const int64_t nb = cols / BE;

@@ -19,6 +19,10 @@
 //    16 or 32 elements in fp32.
 //  * The plane layout is padded per format so the 16-byte reads of a
 //    quarter-warp hit 8 distinct bank groups.
+#include <algorithm>
+#include <string>
+#include <vector>
+
 #include "nt_internal.cuh"
 #include "ops.cuh"
 #include "qformats.cuh"
@@ -430,9 +434,20 @@ nt_status launch_gemv(Ctx* c, int fmt, const nt_gemv_job* jobs, int njobs, const
   return launch_gemv_ex(c, fmt, ex, njobs, W2, x, norm_g, eps, cols, swiglu, nullptr, st);
 }
 
-nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, const void* W2, const float* x,
-                         const float* norm_g, float eps, int64_t cols, bool swiglu, const RopeArgs* rope,
-                         cudaStream_t st) {
+namespace {
+
+// one launch configuration of the GEMV
+struct Plan {
+  GemvArgs a{};
+  int R = 0, warps = 0, grid = 0;
+  size_t smem = 0;
+};
+
+// the launch plan for `pc` (warps, stage size cap, split-K: 0 = by balance);
+// false when x leaves no shared-memory room for it
+bool make_plan(const Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, const void* W2, const float* x,
+               const float* norm_g, float eps, int64_t cols, bool swiglu, const RopeArgs* rope, PlanChoice pc,
+               Plan& P) {
   const int BB = block_bytes(fmt);
   const int64_t nb = cols / block_elems(fmt);
   const int64_t rowB = nb * BB;
@@ -443,49 +458,44 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
   const FmtInfo fi = fmt_info(fmt, int(cols));
   const int ng = int(cols / 32);
   const int pad = 16;  // the unaligned readers may touch 4 bytes past a stage
-  GemvArgs a{};
+  GemvArgs& a = P.a;
+  a = GemvArgs{};
   int R = 0, kStages = 0, kWarps = 0, head = 0, stb = 0;
   const int al = fi.align;
-  // the configured warps and stages; fewer when x leaves too little shared memory
-  const int warp_opts[4] = {c->gemv_warps, 12, 8, 4};
-  for (int wi = 0; wi < 4 && R == 0; ++wi) {
-    const int nw = warp_opts[wi];
-    if (nw > c->gemv_warps || (wi > 0 && nw >= warp_opts[0])) continue;
-    for (int ns = c->gemv_stages; ns >= 2 && R == 0; --ns) {
-      head = ((fi.xbytes + 12 * ng + 8 + nw * ns * 8 + 127) / 128) * 128;
-      const long avail = long(c->smem_optin) - head - pad - c->gemv_static_smem;
-      stb = int(avail / (nw * ns)) / 16 * 16;
-      if (stb > c->gemv_stage_max) stb = c->gemv_stage_max;
-      if (stb < 256) continue;
-      for (int r : {4, 2}) {
-        // whole rows when R of them fit a stage
-        if (int64_t(r) * (tma ? rowB : ((rowB + 15) / 16) * 16) <= stb) {
-          R = r;
-          a.seg = int(nb);
-          a.nseg = 1;
-          a.merged = tma && !swiglu;
-          a.segStride = int(a.merged ? rowB : ((rowB + 15) / 16) * 16);
-          break;
-        }
-        int seg = int(stb / (int64_t(r) * BB)) / al * al;
-        while (seg >= al && int64_t(r) * (((seg * BB + 15) / 16) * 16) > stb) seg -= al;
-        if (seg >= al) {
-          R = r;
-          a.seg = seg;
-          a.nseg = int((nb + seg - 1) / seg);
-          a.merged = 0;
-          a.segStride = ((seg * BB + 15) / 16) * 16;
-          break;
-        }
+  const int nw = pc.warps;
+  for (int ns = c->gemv_stages; ns >= 2 && R == 0; --ns) {
+    head = ((fi.xbytes + 12 * ng + 8 + nw * ns * 8 + 127) / 128) * 128;
+    const long avail = long(c->smem_optin) - head - pad - c->gemv_static_smem;
+    stb = int(avail / (nw * ns)) / 16 * 16;
+    if (stb > pc.stage_max) stb = pc.stage_max;
+    if (stb < 256) continue;
+    for (int r : {4, 2}) {
+      // whole rows when R of them fit a stage
+      if (int64_t(r) * (tma ? rowB : ((rowB + 15) / 16) * 16) <= stb) {
+        R = r;
+        a.seg = int(nb);
+        a.nseg = 1;
+        a.merged = tma && !swiglu;
+        a.segStride = int(a.merged ? rowB : ((rowB + 15) / 16) * 16);
+        break;
       }
-      if (R) {
-        kStages = ns;
-        kWarps = nw;
+      int seg = int(stb / (int64_t(r) * BB)) / al * al;
+      while (seg >= al && int64_t(r) * (((seg * BB + 15) / 16) * 16) > stb) seg -= al;
+      if (seg >= al) {
+        R = r;
+        a.seg = seg;
+        a.nseg = int((nb + seg - 1) / seg);
+        a.merged = 0;
+        a.segStride = ((seg * BB + 15) / 16) * 16;
+        break;
       }
     }
+    if (R) {
+      kStages = ns;
+      kWarps = nw;
+    }
   }
-  if (R == 0)
-    return set_err(c, NT_ERR_INVALID_ARG, "gemv: cols=%lld too large for the shared-memory plan", (long long)cols);
+  if (R == 0) return false;
 
   const int rpg = swiglu ? R / 2 : R;
   int64_t g = 0;
@@ -502,15 +512,16 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
     g += (jb.rows + rpg - 1) / rpg;
   }
   if (rope) a.rope = *rope;
-  if (g == 0) return NT_OK;
 
   // split row groups over KS warps (column parts) when there are too few
   // groups to give every warp of every SM the same amount of work
-  int ks = 1;
-  {
+  int ks = pc.ks;
+  const int units = int(nb / al);  // ALIGN-block units per row
+  if (ks > 1 && (kWarps % ks || units < ks)) return false;
+  if (ks == 0) {
+    ks = 1;
     const int64_t T = int64_t(c->num_sms) * kWarps;
     double best = 0.0;
-    const int units = int(nb / al);  // ALIGN-block units per row
     for (int cand : {1, 2, 4}) {
       if (kWarps % cand || (cand > 1 && units < cand)) continue;
       const int64_t u = g * cand;
@@ -527,7 +538,6 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
     a.pblk[0] = 0;
     a.pblk[1] = int(nb);
   } else {
-    const int units = int(nb / al);
     for (int p = 0; p <= ks; ++p) a.pblk[p] = (p * units / ks) * al;
     a.pblk[ks] = int(nb);
     const int plen = a.pblk[1] - a.pblk[0];
@@ -555,18 +565,132 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
   const int slots = kWarps / ks;
   int64_t grid64 = (g + slots - 1) / slots;
   if (grid64 > c->num_sms) grid64 = c->num_sms;
-  const int grid = int(grid64);
-  const size_t smem = size_t(head) + size_t(kWarps) * kStages * stb + pad;
+  P.R = R;
+  P.warps = kWarps;
+  P.grid = int(grid64 > 0 ? grid64 : 1);
+  P.smem = size_t(head) + size_t(kWarps) * kStages * stb + pad;
+  return true;
+}
 
-  cudaError_t e;
+cudaError_t launch_plan(const Ctx* c, int fmt, const Plan& P, cudaStream_t st) {
   switch (fmt) {
-    case NT_Q8_0: e = dispatch_r<NT_Q8_0>(c, R, a, kWarps, grid, smem, st); break;
-    case NT_Q4_0: e = dispatch_r<NT_Q4_0>(c, R, a, kWarps, grid, smem, st); break;
-    case NT_Q4_K: e = dispatch_r<NT_Q4_K>(c, R, a, kWarps, grid, smem, st); break;
-    case NT_Q5_K: e = dispatch_r<NT_Q5_K>(c, R, a, kWarps, grid, smem, st); break;
-    default: e = dispatch_r<NT_Q6_K>(c, R, a, kWarps, grid, smem, st); break;
+    case NT_Q8_0: return dispatch_r<NT_Q8_0>(c, P.R, P.a, P.warps, P.grid, P.smem, st);
+    case NT_Q4_0: return dispatch_r<NT_Q4_0>(c, P.R, P.a, P.warps, P.grid, P.smem, st);
+    case NT_Q4_K: return dispatch_r<NT_Q4_K>(c, P.R, P.a, P.warps, P.grid, P.smem, st);
+    case NT_Q5_K: return dispatch_r<NT_Q5_K>(c, P.R, P.a, P.warps, P.grid, P.smem, st);
+    default: return dispatch_r<NT_Q6_K>(c, P.R, P.a, P.warps, P.grid, P.smem, st);
   }
-  return cuda_check(c, e, "qgemv launch");
+}
+
+// the shape of a launch: what the plan depends on
+std::string plan_key(int fmt, const GemvJobEx* jobsx, int njobs, const void* W2, int64_t cols, bool swiglu) {
+  char buf[160];
+  bool tma = true;
+  for (int j = 0; j < njobs; ++j) tma = tma && aligned(jobsx[j].j.W_dev, 16);
+  if (swiglu) tma = tma && aligned(W2, 16);
+  snprintf(buf, sizeof buf, "%d/%lld/%d/%d/%lld/%lld/%lld", fmt, (long long)cols, int(swiglu), int(tma),
+           (long long)jobsx[0].j.rows, (long long)(njobs > 1 ? jobsx[1].j.rows : -1),
+           (long long)(njobs > 2 ? jobsx[2].j.rows : -1));
+  return buf;
+}
+
+// time the candidate plans of one launch shape on `st` (outputs to scratch,
+// plain epilogue, no residual) and remember the fastest
+nt_status tune(Ctx* c, const std::string& key, int fmt, const GemvJobEx* jobsx, int njobs, const void* W2,
+               const float* x, const float* norm_g, float eps, int64_t cols, bool swiglu, cudaStream_t st) {
+  GemvJobEx tj[3];
+  size_t off = 0;
+  for (int j = 0; j < njobs; ++j) {
+    tj[j] = jobsx[j];
+    tj[j].j.y_dev = reinterpret_cast<float*>(c->scratch + kScratchTune + off);
+    tj[j].j.residual_dev = nullptr;
+    tj[j].epi = kEpiPlain;
+    tj[j].cache = nullptr;
+    off += (size_t(jobsx[j].j.rows) * 4 + 255) / 256 * 256;
+  }
+  if (kScratchTune + off > kScratchGemm || kScratchGemm > c->scratch_bytes) {
+    std::lock_guard<std::mutex> lk(c->mu);  // no room to tune: keep the default
+    c->gemv_plans[key] = PlanChoice{c->gemv_warps, c->gemv_stage_max, 0};
+    return NT_OK;
+  }
+  const PlanChoice cands[] = {{c->gemv_warps, c->gemv_stage_max, 0}, {12, 16384, 0}, {8, 24576, 0},
+                              {16, 12288, 1},  {12, 12288, 0},      {16, 16384, 0}, {12, 16384, 1},
+                              {8, 16384, 0},   {16, 8192, 0}};
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  cudaError_t ce = cudaEventCreate(&e0);
+  if (ce == cudaSuccess) ce = cudaEventCreate(&e1);
+  float best_ms = 1e30f;
+  PlanChoice best = cands[0];
+  std::vector<std::string> seen;
+  for (const PlanChoice& pc : cands) {
+    if (ce != cudaSuccess) break;
+    if (pc.warps > 16 || pc.warps < 4) continue;
+    Plan P;
+    if (!make_plan(c, fmt, tj, njobs, W2, x, norm_g, eps, cols, swiglu, nullptr, pc, P)) continue;
+    char sig[96];
+    snprintf(sig, sizeof sig, "%d/%d/%d/%d/%d/%d", P.R, P.warps, P.a.seg, P.a.ks, P.a.stb, P.a.nst);
+    if (std::find(seen.begin(), seen.end(), std::string(sig)) != seen.end()) continue;
+    seen.push_back(sig);
+    ce = launch_plan(c, fmt, P, st);  // warm-up
+    if (ce == cudaSuccess) ce = cudaEventRecord(e0, st);
+    for (int r = 0; r < 3 && ce == cudaSuccess; ++r) ce = launch_plan(c, fmt, P, st);
+    if (ce == cudaSuccess) ce = cudaEventRecord(e1, st);
+    if (ce == cudaSuccess) ce = cudaEventSynchronize(e1);
+    float ms = 0.f;
+    if (ce == cudaSuccess) ce = cudaEventElapsedTime(&ms, e0, e1);
+    if (ce == cudaSuccess && ms < best_ms) {
+      best_ms = ms;
+      best = pc;
+    }
+  }
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  if (ce != cudaSuccess) return cuda_check(c, ce, "gemv plan tuning");
+  std::lock_guard<std::mutex> lk(c->mu);
+  c->gemv_plans[key] = best;
+  return NT_OK;
+}
+
+}  // namespace
+
+nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, const void* W2, const float* x,
+                         const float* norm_g, float eps, int64_t cols, bool swiglu, const RopeArgs* rope,
+                         cudaStream_t st) {
+  int64_t rows = 0;
+  for (int j = 0; j < njobs; ++j) rows += jobsx[j].j.rows;
+  if (rows == 0) return NT_OK;
+  const std::string key = plan_key(fmt, jobsx, njobs, W2, cols, swiglu);
+  PlanChoice pc{c->gemv_warps, c->gemv_stage_max, 0};
+  bool known = false;
+  {
+    std::lock_guard<std::mutex> lk(c->mu);
+    auto it = c->gemv_plans.find(key);
+    if (it != c->gemv_plans.end()) {
+      pc = it->second;
+      known = true;
+    }
+  }
+  if (!known && c->gemv_tune) {
+    // tune on the first eager call of a shape (never inside a stream capture)
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone) {
+      nt_status s = tune(c, key, fmt, jobsx, njobs, W2, x, norm_g, eps, cols, swiglu, st);
+      if (s) return s;
+      std::lock_guard<std::mutex> lk(c->mu);
+      pc = c->gemv_plans[key];
+    }
+    cudaGetLastError();
+  }
+  if (c->dry) return NT_OK;
+  // the chosen plan, else fewer warps when x leaves too little shared memory
+  Plan P;
+  bool ok = make_plan(c, fmt, jobsx, njobs, W2, x, norm_g, eps, cols, swiglu, rope, pc, P);
+  for (int nw : {12, 8, 4})
+    if (!ok && nw < pc.warps)
+      ok = make_plan(c, fmt, jobsx, njobs, W2, x, norm_g, eps, cols, swiglu, rope, PlanChoice{nw, pc.stage_max, 0}, P);
+  if (!ok)
+    return set_err(c, NT_ERR_INVALID_ARG, "gemv: cols=%lld too large for the shared-memory plan", (long long)cols);
+  return cuda_check(c, launch_plan(c, fmt, P, st), "qgemv launch");
 }
 
 }  // namespace nt

@@ -95,7 +95,13 @@ nt_status nt_dequant_rows(nt_ctx* ctx, int fmt, const void* W_dev, int64_t row0,
                           float* out_dev, void* stream);
 
 /* Quant GEMV [code] cuda/ GEMV:  y[r] = sum_c deq(W[r,c]) * x[c]  (+ residual[r]),
- * r < rows, fp32 accumulation.  residual_dev may be NULL or equal y_dev. */
+ * r < rows, fp32 accumulation.  residual_dev may be NULL or equal y_dev.
+ * Launch plans (warps per CTA, stage size, split of each row over warps)
+ * are tuned per launch shape: the first call of a shape on a stream that is
+ * not being captured times a few plans, writing only context scratch, then
+ * synchronizes the stream and keeps the fastest.  Later calls, captured or
+ * not, use that plan; a shape first seen inside a capture uses the default
+ * plan.  The plan changes only the summation order (fp32 rounding). */
 nt_status nt_gemv_q(nt_ctx* ctx, int fmt, const void* W_dev, const float* x_dev, float* y_dev, int64_t rows,
                     int64_t cols, const float* residual_dev, void* stream);
 
@@ -238,7 +244,9 @@ nt_status nt_model_destroy(nt_ctx* ctx, nt_model* model);
  * from the previous step (token = its argmax, pos = its pos + 1) with no host
  * round trip.  next_token_dev (nullable) receives the argmax.  Each distinct
  * (skip mask, logits, next_token) is captured once into a CUDA graph and
- * replayed.  skip_mask_host is n_layers bytes or NULL.
+ * replayed.  skip_mask_host is n_layers bytes or NULL.  Before the first
+ * capture of a graph, a dry pass tunes the GEMV plans of its shapes on
+ * `stream` (see nt_gemv_q), which synchronizes that stream once.
  * Streamed layers: inside the same graph, executed streamed layer i (in layer
  * order) is copied into slot i mod stream_slots on the model's copy stream;
  * the first stream_slots copies start with the step and overlap the
