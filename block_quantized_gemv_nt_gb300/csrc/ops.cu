@@ -114,8 +114,9 @@ __global__ void rope_append_kernel(float* q, const float* k, const float* v, __h
 // dims and the probabilities broadcast by shuffle.  The warps merge in shared
 // memory; partials (m, l, o[128]) go to scratch; the last CTA of a KV head
 // combines the S partials.
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kTiles = 4;  // 32-position tiles per chunk (kMaxChunk / 32)
 constexpr int kHD = 128;
 constexpr int kMaxGroup = 16;
 constexpr int kMaxChunk = 128;
@@ -145,7 +146,7 @@ constexpr int kPS = kWpStride;  // floats per (split, head) partial in scratch
 // shared memory: K and V chunks, q (scaled), combine weights, warp partials
 __host__ __device__ constexpr size_t attn_smem_bytes(int G) {
   return size_t(2) * kMaxChunk * kHD * 2 + size_t(G) * kHD * 4 + size_t(G) * kMaxChunk * 4 +
-         size_t(kAttnWarps) * G * kWpStride * 4 + 16;
+         size_t(kTiles) * G * kWpStride * 4 + 16;
 }
 
 __device__ __forceinline__ float4 h4(uint2 raw) {
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   float* qs = reinterpret_cast<float*>(Vs + kMaxChunk * kHD);      // [G][128], pre-scaled by 1/sqrt(128)
   float* wts = qs + G * kHD;                                       // [G][kMaxChunk] combine weights
   float* wp = wts + G * kMaxChunk;                                 // [warps][G][kWpStride] warp partials
-  uint64_t* bar = reinterpret_cast<uint64_t*>(wp + kAttnWarps * G * kWpStride);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(wp + kTiles * G * kWpStride);
   __shared__ bool last;
 
   const int g = blockIdx.x, s = blockIdx.y;
@@ -230,20 +231,25 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     return;
   }
 
-  // ---- per-warp online softmax over 32-position tiles
-  float m[G], l[G], o[G][4];
+  // ---- per-warp online softmax over one 32-position tile: warp w takes tile
+  // w % 4 of the chunk and half of the group's heads (all of them when G = 1)
+  constexpr int NH = G >= 2 ? 2 : 1;  // head halves
+  constexpr int HS = G / NH;           // heads per warp
+  const int tile = warp % kTiles, hh = warp / kTiles;
+  float m[HS], l[HS], o[HS][4];
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
+  for (int h = 0; h < HS; ++h) {
     m[h] = -INFINITY;
     l[h] = 0.f;
     o[h][0] = o[h][1] = o[h][2] = o[h][3] = 0.f;
   }
-  for (int t0 = 32 * warp; t0 < np; t0 += 32 * kAttnWarps) {
+  const float* qh = qs + hh * HS * kHD;
+  for (int t0 = 32 * tile; hh < NH && t0 < np; t0 += 32 * kTiles) {
     const int j = t0 + lane;
     const bool valid = j < np;
-    float sc[G];
+    float sc[HS];
 #pragma unroll
-    for (int h = 0; h < G; ++h) sc[h] = 0.f;
+    for (int h = 0; h < HS; ++h) sc[h] = 0.f;
     if (valid) {
       const __half* krow = Ks + j * kHD;
 #pragma unroll 4
@@ -251,15 +257,15 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
         const int cc = (c + lane) & 31;  // lane-rotated 4-dim chunk: distinct banks across the warp
         const float4 k = h4(*reinterpret_cast<const uint2*>(krow + 4 * cc));
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float4 qv = *reinterpret_cast<const float4*>(qs + h * kHD + 4 * cc);
+        for (int h = 0; h < HS; ++h) {
+          const float4 qv = *reinterpret_cast<const float4*>(qh + h * kHD + 4 * cc);
           sc[h] = fmaf(qv.x, k.x, fmaf(qv.y, k.y, fmaf(qv.z, k.z, fmaf(qv.w, k.w, sc[h]))));
         }
       }
     }
-    float pj[G];
+    float pj[HS];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < HS; ++h) {
       const float sv = valid ? sc[h] : -INFINITY;
       const float mn = fmaxf(m[h], warp_max(sv));
       const float corr = m[h] == -INFINITY ? 0.f : __expf(m[h] - mn);
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     for (int jj = 0; jj < nt; ++jj) {
       const float4 v = h4(*reinterpret_cast<const uint2*>(Vs + (t0 + jj) * kHD + 4 * lane));
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
+      for (int h = 0; h < HS; ++h) {
         const float p = __shfl_sync(0xffffffffu, pj[h], jj);
         o[h][0] = fmaf(p, v.x, o[h][0]);
         o[h][1] = fmaf(p, v.y, o[h][1]);
@@ -284,16 +290,18 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       }
     }
   }
-  // ---- merge the warps: (m, l, o) of each warp -> one CTA partial
-  {
-    float* mine = wp + warp * G * kWpStride;
+  // ---- merge the tiles: (m, l, o) of each (tile, head) -> one CTA partial
+  if (hh < NH) {
+    float* mine = wp + tile * G * kWpStride;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int hl = 0; hl < HS; ++hl) {
+      const int h = hh * HS + hl;
       if (lane == 0) {
-        mine[h * kWpStride + kWpM] = m[h];
-        mine[h * kWpStride + kWpL] = l[h];
+        mine[h * kWpStride + kWpM] = m[hl];
+        mine[h * kWpStride + kWpL] = l[hl];
       }
-      *reinterpret_cast<float4*>(mine + h * kWpStride + 4 * lane) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+      *reinterpret_cast<float4*>(mine + h * kWpStride + 4 * lane) =
+          make_float4(o[hl][0], o[hl][1], o[hl][2], o[hl][3]);
     }
   }
   __syncthreads();
@@ -302,10 +310,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     const int h = i / (kHD + 1), d = i % (kHD + 1);  // d == kHD: the (m, l) pair
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wp[(w * G + h) * kWpStride + kWpM]);
+    for (int w = 0; w < kTiles; ++w) M = fmaxf(M, wp[(w * G + h) * kWpStride + kWpM]);
     float acc = 0.f;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) {
+    for (int w = 0; w < kTiles; ++w) {
       const float* pw = wp + (w * G + h) * kWpStride;
       const float c = pw[kWpM] == -INFINITY ? 0.f : __expf(pw[kWpM] - M);
       acc = fmaf(d < kHD ? pw[d] : pw[kWpL], c, acc);
