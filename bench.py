@@ -141,10 +141,12 @@ def parse_gemv(name):
     gemm_<fmt>_<rows>x<cols>_m<M> for the M-vector verify GEMM.  Returns
     (fmt, rows, cols, M)."""
     import synth
-    parts = name.split("_")
-    fmt = synth.FMT_BY_NAME[(parts[1] + "_" + parts[2]).upper()]
-    rows, cols = (int(v) for v in parts[3].split("x"))
-    M = int(parts[4][1:]) if len(parts) > 4 else 1
+    parts = name.split("_")[1:]
+    # the format name is one or two parts: q8_0, q4_k, f16, ...
+    nf = 2 if (parts[0] + "_" + parts[1]).upper() in synth.FMT_BY_NAME else 1
+    fmt = synth.FMT_BY_NAME["_".join(parts[:nf]).upper()]
+    rows, cols = (int(v) for v in parts[nf].split("x"))
+    M = int(parts[nf + 1][1:]) if len(parts) > nf + 1 else 1
     return fmt, rows, cols, M
 
 

@@ -179,7 +179,8 @@ nt_status nt_dequant_rows(nt_ctx* ctx, int fmt, const void* W, int64_t row0, int
   NT_TRY(check_fmt_cols(ctx, fmt, cols));
   NT_REQUIRE(W && out, NT_ERR_INVALID_ARG, "null pointer");
   NT_REQUIRE(row0 >= 0 && nrows >= 0, NT_ERR_INVALID_ARG, "negative row range");
-  NT_REQUIRE(aligned(W, 2), NT_ERR_ALIGNMENT, "W must be 2-byte aligned");
+  NT_REQUIRE(aligned(W, fmt == NT_F32 ? 4 : 2), NT_ERR_ALIGNMENT, "W must be %d-byte aligned",
+             fmt == NT_F32 ? 4 : 2);
   NT_REQUIRE(aligned(out, 4), NT_ERR_ALIGNMENT, "out must be 4-byte aligned");
   DeviceGuard g(ctx->device);
   return launch_dequant(ctx, fmt, W, row0, nrows, cols, out, as_stream(stream));

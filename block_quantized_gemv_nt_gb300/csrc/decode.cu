@@ -514,6 +514,7 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
     }
   }
   NT_REQUIRE(aligned(out_norm, 16), NT_ERR_ALIGNMENT, "out_norm must be 16-byte aligned");
+  NT_REQUIRE(aligned(embd, d.fmt_embd == NT_F32 ? 4 : 2), NT_ERR_ALIGNMENT, "embd is misaligned for its format");
   // an embedding table in page-locked host memory is read through its device alias
   {
     cudaPointerAttributes pa{};
@@ -546,9 +547,12 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   {
     // partial sums of the largest verify GEMM
     const int64_t nkv = int64_t(d.n_kvh) * d.head_dim;
-    const int64_t rc[5][2] = {{nq + 2 * nkv, d.d_model}, {d.d_model, nq}, {2 * int64_t(d.ffn), d.d_model},
-                              {d.d_model, d.ffn}, {d.vocab, d.d_model}};
-    for (auto& x : rc) m->gpart_bytes = std::max(m->gpart_bytes, gemm_scratch_bytes(x[0], x[1], kMaxVerify));
+    const int64_t rc[7][3] = {{nq + 2 * nkv, d.d_model, d.fmt_q}, {nq + 2 * nkv, d.d_model, d.fmt_k},
+                              {nq + 2 * nkv, d.d_model, d.fmt_v}, {d.d_model, nq, d.fmt_o},
+                              {2 * int64_t(d.ffn), d.d_model, d.fmt_gate}, {d.d_model, d.ffn, d.fmt_down},
+                              {d.vocab, d.d_model, d.fmt_out}};
+    for (auto& x : rc)
+      m->gpart_bytes = std::max(m->gpart_bytes, gemm_scratch_bytes(int(x[2]), x[0], x[1], kMaxVerify));
     m->gpart_bytes = up256(m->gpart_bytes);
   }
   const size_t total = 2 * nx + nqb * 2 + nkb * 2 + nh + ncos + nst + npart + nfreq + nspec + nvx + 2 * nvq + nvh +
@@ -748,6 +752,39 @@ nt_status nt_layer_blob_layout(const nt_model_desc* d, size_t* off, size_t* byte
     if (!fmt_ok(f)) return NT_ERR_UNSUPPORTED_FMT;
   if (d->d_model <= 0 || d->n_qh <= 0 || d->n_kvh <= 0 || d->head_dim <= 0 || d->ffn <= 0) return NT_ERR_INVALID_ARG;
   blob_layout(*d, off, bytes);
+  return NT_OK;
+}
+
+nt_status nt_plan_residency(const nt_model_desc* d, size_t budget, int embd_in_hbm, nt_residency_plan* out) {
+  if (!d || !out) return NT_ERR_INVALID_ARG;
+  const int fm[9] = {d->fmt_q, d->fmt_k, d->fmt_v, d->fmt_o, d->fmt_gate, d->fmt_up, d->fmt_down, d->fmt_embd,
+                     d->fmt_out};
+  for (int f : fm)
+    if (!fmt_ok(f)) return NT_ERR_UNSUPPORTED_FMT;
+  if (d->n_layers <= 0 || d->d_model <= 0 || d->vocab <= 0 || d->d_model % block_elems(d->fmt_out) ||
+      d->d_model % block_elems(d->fmt_embd) || d->stream_slots < 0 || d->stream_slots > kMaxSlots)
+    return NT_ERR_INVALID_ARG;
+  size_t off[7], layer = 0;
+  blob_layout(*d, off, &layer);
+  const auto mat = [&](int fmt) {
+    return size_t(d->vocab) * size_t(d->d_model / block_elems(fmt)) * size_t(block_bytes(fmt));
+  };
+  const size_t fixed = mat(d->fmt_out) + (embd_in_hbm ? mat(d->fmt_embd) : 0);
+  const int slots = d->stream_slots ? d->stream_slots : 2;
+  nt_residency_plan p{};
+  p.layer_bytes = layer;
+  p.fixed_bytes = fixed;
+  if (fixed + size_t(d->n_layers) * layer <= budget) {
+    p.n_resident = d->n_layers;  // everything fits: nothing streams
+    p.stream_slots = 0;
+  } else {
+    const size_t need = fixed + size_t(slots) * layer;
+    const size_t room = budget > need ? budget - need : 0;
+    p.n_resident = int(std::min<size_t>(room / layer, size_t(d->n_layers - 1)));
+    p.stream_slots = slots;
+  }
+  p.total_bytes = fixed + size_t(p.n_resident) * layer + size_t(p.stream_slots) * layer;
+  *out = p;
   return NT_OK;
 }
 

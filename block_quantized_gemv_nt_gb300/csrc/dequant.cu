@@ -1,9 +1,9 @@
-// dequant.cu — dequantisation of whole rows of the GGUF block formats named
-// on "Ntransformer" (en.unwiki.net), About: the embedding-row lookup of the
+// dequant.cu — dequantisation of whole rows of the weight formats named on
+// "Ntransformer" (en.unwiki.net), About: the embedding-row lookup of the
 // decode step and the bit-exact dequantisation entry point.  Element values
 // (GGUF reading): Q8_0 d*q; Q4_0 d*(q-8); Q4_K/Q5_K (d*sc)*q - dmin*m;
-// Q6_K d*(sc*(q-32)); every product is exact in fp32, only the K-quant
-// subtraction rounds.
+// Q6_K d*(sc*(q-32)); F16 / F32 the value itself.  Every product is exact in
+// fp32, only the K-quant subtraction rounds.
 #include "nt_internal.cuh"
 #include "ops.cuh"
 
@@ -44,36 +44,37 @@ __device__ __forceinline__ void kq_sm(const uint8_t* s, int j, int& sc, int& m) 
   }
 }
 
+// element i of block b, exactly as the formats define it (every product exact
+// in fp32; only the K-quant subtraction rounds)
+__device__ __forceinline__ float elem_value(int fmt, const uint8_t* b, int i) {
+  switch (fmt) {
+    case NT_Q8_0: return __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b)), float(quant_of(fmt, b, i)));
+    case NT_Q4_0:
+      return __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b)), float(quant_of(fmt, b, i) - 8));
+    case NT_Q4_K:
+    case NT_Q5_K: {
+      int sc, m;
+      kq_sm(b + 4, i >> 5, sc, m);
+      const float d = __half2float(*reinterpret_cast<const __half*>(b));
+      const float dm = __half2float(*reinterpret_cast<const __half*>(b + 2));
+      return __fsub_rn(__fmul_rn(__fmul_rn(d, float(sc)), float(quant_of(fmt, b, i))), __fmul_rn(dm, float(m)));
+    }
+    case NT_Q6_K: {
+      const int s = int(int8_t(b[192 + (i >> 7) * 8 + ((i & 127) >> 4)]));
+      return __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b + 208)), float(s * (quant_of(fmt, b, i) - 32)));
+    }
+    case NT_F16: return __half2float(*reinterpret_cast<const __half*>(b + 2 * i));
+    default: return *reinterpret_cast<const float*>(b + 4 * i);
+  }
+}
+
 __global__ void dequant_kernel(int fmt, const uint8_t* W, int64_t row0, int64_t nrows, int64_t cols, float* out) {
   const int BE = block_elems(fmt), BB = block_bytes(fmt);
   const int64_t nb = cols / BE;
   const int64_t total = nrows * cols;
   for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += int64_t(gridDim.x) * blockDim.x) {
     const int64_t r = e / cols, col = e % cols;
-    const uint8_t* b = W + ((row0 + r) * nb + col / BE) * BB;
-    const int i = int(col % BE);
-    float v;
-    switch (fmt) {
-      case NT_Q8_0: v = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b)), float(quant_of(fmt, b, i))); break;
-      case NT_Q4_0:
-        v = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b)), float(quant_of(fmt, b, i) - 8));
-        break;
-      case NT_Q4_K:
-      case NT_Q5_K: {
-        int sc, m;
-        kq_sm(b + 4, i >> 5, sc, m);
-        const float d = __half2float(*reinterpret_cast<const __half*>(b));
-        const float dm = __half2float(*reinterpret_cast<const __half*>(b + 2));
-        v = __fsub_rn(__fmul_rn(__fmul_rn(d, float(sc)), float(quant_of(fmt, b, i))), __fmul_rn(dm, float(m)));
-        break;
-      }
-      default: {
-        const int s = int(int8_t(b[192 + (i >> 7) * 8 + ((i & 127) >> 4)]));
-        v = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b + 208)), float(s * (quant_of(fmt, b, i) - 32)));
-        break;
-      }
-    }
-    out[e] = v;
+    out[e] = elem_value(fmt, W + ((row0 + r) * nb + col / BE) * BB, int(col % BE));
   }
 }
 
@@ -86,32 +87,8 @@ __global__ void embed_kernel(int fmt, const uint8_t* W, int64_t cols, const int3
   out += int64_t(blockIdx.y) * cols;
   const int BE = block_elems(fmt), BB = block_bytes(fmt);
   const int64_t nb = cols / BE;
-  for (int64_t col = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; col < cols; col += int64_t(gridDim.x) * blockDim.x) {
-    const uint8_t* b = W + (row * nb + col / BE) * BB;
-    const int i = int(col % BE);
-    float v;
-    switch (fmt) {
-      case NT_Q8_0: v = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b)), float(quant_of(fmt, b, i))); break;
-      case NT_Q4_0:
-        v = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b)), float(quant_of(fmt, b, i) - 8));
-        break;
-      case NT_Q4_K:
-      case NT_Q5_K: {
-        int sc, m;
-        kq_sm(b + 4, i >> 5, sc, m);
-        const float d = __half2float(*reinterpret_cast<const __half*>(b));
-        const float dm = __half2float(*reinterpret_cast<const __half*>(b + 2));
-        v = __fsub_rn(__fmul_rn(__fmul_rn(d, float(sc)), float(quant_of(fmt, b, i))), __fmul_rn(dm, float(m)));
-        break;
-      }
-      default: {
-        const int s = int(int8_t(b[192 + (i >> 7) * 8 + ((i & 127) >> 4)]));
-        v = __fmul_rn(__half2float(*reinterpret_cast<const __half*>(b + 208)), float(s * (quant_of(fmt, b, i) - 32)));
-        break;
-      }
-    }
-    out[col] = v;
-  }
+  for (int64_t col = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; col < cols; col += int64_t(gridDim.x) * blockDim.x)
+    out[col] = elem_value(fmt, W + (row * nb + col / BE) * BB, int(col % BE));
 }
 
 }  // namespace

@@ -63,11 +63,19 @@ constexpr size_t kScratchTune = size_t(24) << 20;  // GEMV plan tuning outputs (
 constexpr size_t kScratchGemm = size_t(32) << 20;  // verify-GEMM partial sums, to the end of the scratch
 
 // format geometry ---------------------------------------------------------------
-__host__ __device__ constexpr int block_elems(int fmt) { return fmt <= NT_Q4_0 ? 32 : 256; }
-__host__ __device__ constexpr int block_bytes(int fmt) {
-  return fmt == NT_Q8_0 ? 34 : fmt == NT_Q4_0 ? 18 : fmt == NT_Q4_K ? 144 : fmt == NT_Q5_K ? 176 : 210;
+__host__ __device__ constexpr int block_elems(int fmt) {
+  return (fmt == NT_Q4_K || fmt == NT_Q5_K || fmt == NT_Q6_K) ? 256 : 32;
 }
-inline bool fmt_ok(int fmt) { return fmt >= NT_Q8_0 && fmt <= NT_Q6_K; }
+__host__ __device__ constexpr int block_bytes(int fmt) {
+  return fmt == NT_Q8_0   ? 34
+         : fmt == NT_Q4_0 ? 18
+         : fmt == NT_Q4_K ? 144
+         : fmt == NT_Q5_K ? 176
+         : fmt == NT_Q6_K ? 210
+         : fmt == NT_F16  ? 64
+                          : 128;
+}
+inline bool fmt_ok(int fmt) { return fmt >= NT_Q8_0 && fmt <= NT_F32; }
 
 // device helpers -----------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

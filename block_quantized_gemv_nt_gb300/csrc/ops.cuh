@@ -32,8 +32,8 @@ nt_status launch_argmax(Ctx* c, const float* v, int64_t n, int32_t* out, unsigne
                         cudaStream_t st, int32_t* tok_state = nullptr, int64_t* pos_state = nullptr);
 nt_status configure_gemv(Ctx* c);
 nt_status configure_gemm(Ctx* c);
-int gemm_parts(int64_t cols);
-size_t gemm_scratch_bytes(int64_t total_rows, int64_t cols, int M);
+int gemm_parts(int fmt, int64_t cols);
+size_t gemm_scratch_bytes(int fmt, int64_t total_rows, int64_t cols, int M);
 nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool swiglu, const float* X, int64_t ldx,
                       int M, const float* norm_g, float eps, int64_t cols, const RopeArgs* rope, float* part,
                       size_t part_bytes, cudaStream_t st);

@@ -84,6 +84,7 @@ struct Q;
 template <>
 struct Q<NT_Q8_0> {
   static constexpr int BE = 32, BB = 34, ALIGN = 32, UPB = 1, PB = 0;
+  static constexpr bool FLOATX = false;  // x as 24-bit byte planes
   struct X {
     uint32_t v[3][8];
     float s;
@@ -127,6 +128,7 @@ struct Q<NT_Q8_0> {
 template <>
 struct Q<NT_Q4_0> {
   static constexpr int BE = 32, BB = 18, ALIGN = 32, UPB = 1, PB = 0;
+  static constexpr bool FLOATX = false;  // x as 24-bit byte planes
   struct X {
     uint32_t v[3][8];
     float s;
@@ -254,6 +256,7 @@ __device__ __forceinline__ float kq_dotw(const WK& w, const XK& x) {
 template <>
 struct Q<NT_Q4_K> {
   static constexpr int BE = 256, BB = 144, ALIGN = 8, UPB = 4, PB = 1;
+  static constexpr bool FLOATX = false;  // x as 24-bit byte planes
   using X = XK;
   __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int c) {
     load_xk(x, g, g + 112, xs, col0, c);
@@ -284,6 +287,7 @@ struct Q<NT_Q4_K> {
 template <>
 struct Q<NT_Q5_K> {
   static constexpr int BE = 256, BB = 176, ALIGN = 8, UPB = 4, PB = 1;
+  static constexpr bool FLOATX = false;  // x as 24-bit byte planes
   using X = XK;
   __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int c) {
     load_xk(x, g, g + 112, xs, col0, c);
@@ -318,6 +322,7 @@ struct Q<NT_Q5_K> {
 template <>
 struct Q<NT_Q6_K> {
   static constexpr int BE = 256, BB = 210, ALIGN = 8, UPB = 4, PB = 2;
+  static constexpr bool FLOATX = false;  // x as 24-bit byte planes
   struct X {
     uint32_t v[4][3][4];  // chunk g, plane k, 4 words (16 columns)
     float s[4];           // group scales
@@ -390,12 +395,83 @@ struct Q<NT_Q6_K> {
   }
 };
 
+// F16 / F32: plain weights, so x stays fp32 in shared memory (32 floats per
+// 32-column group at a 144-byte pitch: a quarter-warp's 16-byte reads of
+// consecutive groups fall into 8 distinct bank groups) and the dot product
+// is fp32 FMA.  unit = 32 values of one row.
+struct XF {
+  float v[32];
+};
+
+template <>
+struct Q<NT_F16> {
+  static constexpr int BE = 32, BB = 64, ALIGN = 8, UPB = 1, PB = 0;
+  static constexpr bool FLOATX = true;
+  using X = XF;
+  __device__ static void load_x(X& x, const uint8_t* g, const XS&, int, int) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) *reinterpret_cast<float4*>(x.v + 4 * k) = *reinterpret_cast<const float4*>(g + 16 * k);
+  }
+  struct W {
+    uint32_t h[16];  // 32 binary16 values, two per word
+  };
+  __device__ static void unpack(const uint8_t* blk, int, W& w) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ld4(blk + 16 * k, w.h + 4 * k);
+  }
+  __device__ static float dotw(const W& w, int, const X& x) {
+    float a = 0.f, b = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w.h[i]));
+      a = fmaf(f.x, x.v[2 * i], a);
+      b = fmaf(f.y, x.v[2 * i + 1], b);
+    }
+    return a + b;
+  }
+  __device__ static float dot(const uint8_t* blk, int u, const X& x) {
+    W w;
+    unpack(blk, u, w);
+    return dotw(w, u, x);
+  }
+};
+
+template <>
+struct Q<NT_F32> {
+  static constexpr int BE = 32, BB = 128, ALIGN = 8, UPB = 1, PB = 0;
+  static constexpr bool FLOATX = true;
+  using X = XF;
+  __device__ static void load_x(X& x, const uint8_t* g, const XS&, int, int) { Q<NT_F16>::load_x(x, g, XS{}, 0, 0); }
+  struct W {
+    float f[32];
+  };
+  __device__ static void unpack(const uint8_t* blk, int, W& w) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) *reinterpret_cast<float4*>(w.f + 4 * k) = *reinterpret_cast<const float4*>(blk + 16 * k);
+  }
+  __device__ static float dotw(const W& w, int, const X& x) {
+    float a = 0.f, b = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      a = fmaf(w.f[2 * i], x.v[2 * i], a);
+      b = fmaf(w.f[2 * i + 1], x.v[2 * i + 1], b);
+    }
+    return a + b;
+  }
+  __device__ static float dot(const uint8_t* blk, int u, const X& x) {
+    W w;
+    unpack(blk, u, w);
+    return dotw(w, u, x);
+  }
+};
+
 // byte offset of 32-column group g: 112 bytes per group, plus PB*16 bytes
 // per 8 groups (one K block), chosen per format so that the 16-byte plane
-// reads of a quarter-warp fall into 8 distinct bank groups
+// reads of a quarter-warp fall into 8 distinct bank groups; 144 bytes per
+// group for fp32 x
 template <int FMT>
 __host__ __device__ constexpr int goff(int g) {
-  return 112 * g + 16 * Q<FMT>::PB * (g / 8);
+  return Q<FMT>::FLOATX ? 144 * g : 112 * g + 16 * Q<FMT>::PB * (g / 8);
 }
 
 template <int FMT>
@@ -413,6 +489,10 @@ __host__ __device__ constexpr int x_bytes(int cols) {
 template <int FMT>
 __device__ __forceinline__ void put_x4(float4 x4, bool live, int grp, int sub, uint8_t* xsm, int* psum,
                                        float* gscale) {
+  if constexpr (Q<FMT>::FLOATX) {
+    if (live) *reinterpret_cast<float4*>(xsm + goff<FMT>(grp) + 16 * sub) = x4;
+    return;
+  }
   float m = fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w)));
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));

@@ -8,9 +8,9 @@
 // 16 or 32 weights, so the contraction stays on the integer pipes: the same
 // 24-bit fixed-point x planes and dp4a dot products as the M = 1 GEMV, with
 // the weights staged once per CTA and reused for all M vectors.
-//  * grid (X, P): the columns are cut into P parts of 2048 so that M
-//    vectors of x planes fit in shared memory; CTA (x, p) holds the planes
-//    of part p of every vector and walks row groups of R = 2 rows.
+//  * grid (X, P): the columns are cut into P parts (2048 columns; 1024 /
+//    512 for F16 / F32) so that M vectors of x fit in shared memory; CTA
+//    (x, p) holds part p of every vector and walks row groups of R = 2 rows.
 //  * each warp streams its rows' part through a private ring of TMA bulk
 //    copies (mbarrier completion, L2 evict-first), as the GEMV does.
 //  * partial sums go to scratch [P][M][rows]; a second kernel adds the P
@@ -30,7 +30,9 @@ constexpr int kGemmWarps = 8;
 constexpr int kGemmThreads = kGemmWarps * 32;
 constexpr int kGemmStages = 4;  // per warp
 constexpr int kGemmR = 2;       // rows per group
-constexpr int kPartCols = 2048; // columns per part
+// columns per part: 2048 for the quantized formats; the float formats carry
+// 2 or 4 bytes per weight, so their parts are narrower (2 KB of each row)
+__host__ __device__ constexpr int part_cols(int fmt) { return fmt == NT_F32 ? 512 : fmt == NT_F16 ? 1024 : 2048; }
 
 struct GemmJobDev {
   const uint8_t* W;
@@ -341,14 +343,9 @@ cudaError_t gemm_launch_t(const Ctx* c, const GemmArgs& a, dim3 grid, size_t sme
 }
 
 template <int FMT>
-int gemm_cwb() {
-  return kPartCols / Q<FMT>::BE;
-}
-
-template <int FMT>
 int gemm_vstride() {
-  const int ng = kPartCols / 32;
-  return ((x_bytes<FMT>(kPartCols) + 12 * ng) + 15) / 16 * 16;
+  const int ng = part_cols(FMT) / 32;
+  return ((x_bytes<FMT>(part_cols(FMT)) + 12 * ng) + 15) / 16 * 16;
 }
 
 int fmt_vstride(int fmt) {
@@ -357,12 +354,14 @@ int fmt_vstride(int fmt) {
     case NT_Q4_0: return gemm_vstride<NT_Q4_0>();
     case NT_Q4_K: return gemm_vstride<NT_Q4_K>();
     case NT_Q5_K: return gemm_vstride<NT_Q5_K>();
-    default: return gemm_vstride<NT_Q6_K>();
+    case NT_Q6_K: return gemm_vstride<NT_Q6_K>();
+    case NT_F16: return gemm_vstride<NT_F16>();
+    default: return gemm_vstride<NT_F32>();
   }
 }
 
 size_t gemm_smem(int fmt, int M) {
-  const int cwb = kPartCols / block_elems(fmt);
+  const int cwb = part_cols(fmt) / block_elems(fmt);
   const int segStride = ((cwb * block_bytes(fmt) + 15) / 16) * 16;
   const int stb = kGemmR * segStride + 16;  // the unaligned readers may touch 4 bytes past a row
   const size_t head = ((size_t(M) * fmt_vstride(fmt) + kGemmWarps * kGemmStages * 8 + 127) / 128) * 128;
@@ -371,10 +370,10 @@ size_t gemm_smem(int fmt, int M) {
 
 }  // namespace
 
-int gemm_parts(int64_t cols) { return int((cols + kPartCols - 1) / kPartCols); }
+int gemm_parts(int fmt, int64_t cols) { return int((cols + part_cols(fmt) - 1) / part_cols(fmt)); }
 
-size_t gemm_scratch_bytes(int64_t total_rows, int64_t cols, int M) {
-  return size_t(gemm_parts(cols)) * size_t(M) * size_t(total_rows) * sizeof(float);
+size_t gemm_scratch_bytes(int fmt, int64_t total_rows, int64_t cols, int M) {
+  return size_t(gemm_parts(fmt, cols)) * size_t(M) * size_t(total_rows) * sizeof(float);
 }
 
 nt_status configure_gemm(Ctx* c) {
@@ -395,6 +394,8 @@ nt_status configure_gemm(Ctx* c) {
   allow(qgemm_kernel<NT_Q4_K>);
   allow(qgemm_kernel<NT_Q5_K>);
   allow(qgemm_kernel<NT_Q6_K>);
+  allow(qgemm_kernel<NT_F16>);
+  allow(qgemm_kernel<NT_F32>);
   c->gemm_static_smem = st;
   return cuda_check(c, e, "gemm shared-memory attribute");
 }
@@ -425,7 +426,7 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
     pb += (J.rows + 1) / 2;
   }
   if (g == 0) return NT_OK;
-  const int cwb = kPartCols / BE;
+  const int cwb = part_cols(fmt) / BE;
   const int nparts = int((nb + cwb - 1) / cwb);
   const size_t need = size_t(nparts) * M * size_t(rb) * sizeof(float);
   if (need > part_bytes)
@@ -464,7 +465,9 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
     case NT_Q4_0: err = gemm_launch_t<NT_Q4_0>(c, a, grid, smem, st); break;
     case NT_Q4_K: err = gemm_launch_t<NT_Q4_K>(c, a, grid, smem, st); break;
     case NT_Q5_K: err = gemm_launch_t<NT_Q5_K>(c, a, grid, smem, st); break;
-    default: err = gemm_launch_t<NT_Q6_K>(c, a, grid, smem, st); break;
+    case NT_Q6_K: err = gemm_launch_t<NT_Q6_K>(c, a, grid, smem, st); break;
+    case NT_F16: err = gemm_launch_t<NT_F16>(c, a, grid, smem, st); break;
+    default: err = gemm_launch_t<NT_F32>(c, a, grid, smem, st); break;
   }
   nt_status s = cuda_check(c, err, "qgemm launch");
   if (s) return s;

@@ -407,7 +407,9 @@ FmtInfo fmt_info(int fmt, int cols) {
     case NT_Q4_0: return {Q<NT_Q4_0>::ALIGN, x_bytes<NT_Q4_0>(cols)};
     case NT_Q4_K: return {Q<NT_Q4_K>::ALIGN, x_bytes<NT_Q4_K>(cols)};
     case NT_Q5_K: return {Q<NT_Q5_K>::ALIGN, x_bytes<NT_Q5_K>(cols)};
-    default: return {Q<NT_Q6_K>::ALIGN, x_bytes<NT_Q6_K>(cols)};
+    case NT_Q6_K: return {Q<NT_Q6_K>::ALIGN, x_bytes<NT_Q6_K>(cols)};
+    case NT_F16: return {Q<NT_F16>::ALIGN, x_bytes<NT_F16>(cols)};
+    default: return {Q<NT_F32>::ALIGN, x_bytes<NT_F32>(cols)};
   }
 }
 
@@ -423,6 +425,8 @@ nt_status configure_gemv(Ctx* c) {
   if (e == cudaSuccess) e = configure_fmt<NT_Q4_K>(smem, &st);
   if (e == cudaSuccess) e = configure_fmt<NT_Q5_K>(smem, &st);
   if (e == cudaSuccess) e = configure_fmt<NT_Q6_K>(smem, &st);
+  if (e == cudaSuccess) e = configure_fmt<NT_F16>(smem, &st);
+  if (e == cudaSuccess) e = configure_fmt<NT_F32>(smem, &st);
   c->gemv_static_smem = st;
   return cuda_check(c, e, "gemv shared-memory attribute");
 }
@@ -578,7 +582,9 @@ cudaError_t launch_plan(const Ctx* c, int fmt, const Plan& P, cudaStream_t st) {
     case NT_Q4_0: return dispatch_r<NT_Q4_0>(c, P.R, P.a, P.warps, P.grid, P.smem, st);
     case NT_Q4_K: return dispatch_r<NT_Q4_K>(c, P.R, P.a, P.warps, P.grid, P.smem, st);
     case NT_Q5_K: return dispatch_r<NT_Q5_K>(c, P.R, P.a, P.warps, P.grid, P.smem, st);
-    default: return dispatch_r<NT_Q6_K>(c, P.R, P.a, P.warps, P.grid, P.smem, st);
+    case NT_Q6_K: return dispatch_r<NT_Q6_K>(c, P.R, P.a, P.warps, P.grid, P.smem, st);
+    case NT_F16: return dispatch_r<NT_F16>(c, P.R, P.a, P.warps, P.grid, P.smem, st);
+    default: return dispatch_r<NT_F32>(c, P.R, P.a, P.warps, P.grid, P.smem, st);
   }
 }
 

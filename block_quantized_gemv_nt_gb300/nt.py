@@ -13,8 +13,8 @@ import os
 
 from . import build as _build
 
-Q8_0, Q4_0, Q4_K, Q5_K, Q6_K = 0, 1, 2, 3, 4
-FMT_NAMES = {Q8_0: "Q8_0", Q4_0: "Q4_0", Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K"}
+Q8_0, Q4_0, Q4_K, Q5_K, Q6_K, F16, F32 = 0, 1, 2, 3, 4, 5, 6
+FMT_NAMES = {Q8_0: "Q8_0", Q4_0: "Q4_0", Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K", F16: "F16", F32: "F32"}
 
 NT_OK, NT_ERR_INVALID_ARG, NT_ERR_UNSUPPORTED_FMT, NT_ERR_ALIGNMENT, NT_ERR_CUDA, NT_ERR_OOM, NT_ERR_TIMEOUT = range(7)
 STATUS_NAMES = ["NT_OK", "NT_ERR_INVALID_ARG", "NT_ERR_UNSUPPORTED_FMT", "NT_ERR_ALIGNMENT", "NT_ERR_CUDA",
@@ -93,6 +93,12 @@ _sig("nt_decode_step", [_vp, _vp, ctypes.c_int32, _i64, _vp, _vp, _vp, _vp])
 _sig("nt_layer_skip_calibrate", [_vp, _vp, ctypes.c_int32, _i64, _ci, _vp, _vp, _vp, _vp, _vp])
 _sig("nt_attn_decode_static", [_vp, _vp, _vp, _vp, _ci, _ci, _ci, _i64, _i64, _vp])
 _sig("nt_layer_blob_layout", [ctypes.POINTER(nt_model_desc), ctypes.POINTER(_sz), ctypes.POINTER(_sz)])
+class nt_residency_plan(ctypes.Structure):
+    _fields_ = [("n_resident", _ci), ("stream_slots", _ci), ("layer_bytes", _sz), ("fixed_bytes", _sz),
+                ("total_bytes", _sz)]
+
+
+_sig("nt_plan_residency", [ctypes.POINTER(nt_model_desc), _sz, _ci, ctypes.POINTER(nt_residency_plan)])
 _sig("nt_spec_step", [_vp, _vp, ctypes.c_int32, _i64, _ci, _ci, _vp, _vp, _vp, _vp])
 _sig("nt_gemm_q", [_vp, _ci, _vp, _vp, _vp, _i64, _i64, _ci, _vp, _vp, _cf, _vp])
 _sig("nt_attn_verify", [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _i64, _ci, _i64, _vp])
@@ -104,7 +110,7 @@ EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "
             "nt_rope_kv_append", "nt_attn_decode", "nt_softmax", "nt_swiglu", "nt_argmax", "nt_cos_sim",
             "nt_model_init", "nt_model_destroy", "nt_decode_step", "nt_layer_skip_calibrate",
             "nt_attn_decode_static", "nt_layer_blob_layout", "nt_stream_layer", "nt_model_slot", "nt_spec_step",
-            "nt_gemm_q", "nt_attn_verify"]
+            "nt_gemm_q", "nt_attn_verify", "nt_plan_residency"]
 
 
 def lib():
@@ -255,6 +261,14 @@ def nt_spec_step(ctx, model: int, token: int, pos: int, k: int, n_draft_layers: 
                  logits=None, stream=None):
     return ctx.check(_lib.nt_spec_step(ctx.handle, model, token, pos, k, n_draft_layers, _ptr(tokens_out),
                                        _ptr(n_out), _ptr(logits), _stream(stream, tokens_out)))
+
+
+def nt_plan_residency(desc: nt_model_desc, hbm_weight_budget: int, embd_in_hbm: bool = False) -> nt_residency_plan:
+    p = nt_residency_plan()
+    st = _lib.nt_plan_residency(ctypes.byref(desc), int(hbm_weight_budget), int(bool(embd_in_hbm)), ctypes.byref(p))
+    if st != NT_OK:
+        raise NtError(st, "nt_plan_residency failed")
+    return p
 
 
 def nt_layer_blob_layout(desc: nt_model_desc):

@@ -34,8 +34,9 @@
  *    streams and captured graphs.
  *  - Block-quantized matrices are row-major: row r is cols/block_elems
  *    consecutive blocks.  cols must be a multiple of the format's block size
- *    (32 for Q8_0/Q4_0, 256 for Q4_K/Q5_K/Q6_K).  Block bytes: Q8_0 34,
- *    Q4_0 18, Q4_K 144, Q5_K 176, Q6_K 210; layouts are the GGUF ones.
+ *    (32 for Q8_0/Q4_0/F16/F32, 256 for Q4_K/Q5_K/Q6_K).  Block bytes: Q8_0
+ *    34, Q4_0 18, Q4_K 144, Q5_K 176, Q6_K 210, F16 64, F32 128; layouts are
+ *    the GGUF ones.
  *  - Weight pointers must be 2-byte aligned.  When the weight pointer is
  *    16-byte aligned and each row is a multiple of 16 bytes, weights stream
  *    through TMA bulk copies; otherwise a slower plain-load path runs.
@@ -61,7 +62,10 @@ typedef enum {
   NT_ERR_TIMEOUT = 6,         /* a host-side or device-side bounded wait ran out */
 } nt_status;
 
-typedef enum { NT_Q8_0 = 0, NT_Q4_0 = 1, NT_Q4_K = 2, NT_Q5_K = 3, NT_Q6_K = 4 } nt_fmt;
+/* Weight formats [about].  The quantized ones are GGUF blocks (block bytes
+ * below); F16 / F32 rows are plain little-endian binary16 / binary32 values,
+ * handled in units of 32 (their "block": 32 values, 64 / 128 bytes). */
+typedef enum { NT_Q8_0 = 0, NT_Q4_0 = 1, NT_Q4_K = 2, NT_Q5_K = 3, NT_Q6_K = 4, NT_F16 = 5, NT_F32 = 6 } nt_fmt;
 
 typedef struct nt_ctx nt_ctx;
 typedef struct nt_model nt_model;
@@ -176,8 +180,8 @@ nt_status nt_swiglu(nt_ctx* ctx, const float* gate_dev, const float* up_dev, flo
  * 4), Y_dev and residual_dev fp32 [M][rows] (residual may equal Y).  Every
  * weight byte is read once for all M vectors.  Precision and layout rules
  * as nt_gemv_q.  M 1..8.  Uses the context scratch beyond its first 32 MiB
- * for partial sums: NT_ERR_OOM when 4 * M * rows * ceil(cols / 2048) bytes
- * do not fit. */
+ * for partial sums: NT_ERR_OOM when 4 * M * rows * ceil(cols / P) bytes do
+ * not fit (P = 2048 columns; 1024 for F16, 512 for F32). */
 nt_status nt_gemm_q(nt_ctx* ctx, int fmt, const void* W_dev, const float* X_dev, float* Y_dev, int64_t rows,
                     int64_t cols, int M, const float* residual_dev, const float* norm_g_dev, float eps,
                     void* stream);
@@ -264,6 +268,24 @@ nt_status nt_decode_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t po
 nt_status nt_layer_skip_calibrate(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos, int n_skip,
                                   uint8_t* skip_mask_host, float* cos_host, float* logits_dev,
                                   int32_t* next_token_dev, void* stream);
+
+/* Resident-layer planner [about] (3-tier adaptive caching: VRAM-resident
+ * layers first, the rest from pinned RAM) [cache] (the format decides how
+ * many layers fit: "36 vs 26" for Q4_K_M vs Q6_K on the pages' card): how
+ * many leading layers keep their weights in HBM when the weights may use
+ * at most hbm_weight_budget bytes — the LM head, the embedding table when
+ * embd_in_hbm, the resident layers and, if any layer is streamed,
+ * stream_slots (0 = 2) slots of one layer blob.  KV caches and activations
+ * are outside this budget.  Pure host arithmetic from the descriptor. */
+typedef struct {
+  int n_resident;      /* layers 0..n_resident-1 resident, the rest streamed */
+  int stream_slots;    /* slots the plan reserves (0 when nothing streams) */
+  size_t layer_bytes;  /* one layer's weights: the blob of nt_layer_blob_layout */
+  size_t fixed_bytes;  /* LM head (+ embedding table) */
+  size_t total_bytes;  /* fixed + resident layers + slots, <= the budget unless nothing fits */
+} nt_residency_plan;
+nt_status nt_plan_residency(const nt_model_desc* desc, size_t hbm_weight_budget, int embd_in_hbm,
+                            nt_residency_plan* plan_out);
 
 /* Streaming-engine copy step [feat] (SLEP double buffering), [cache]
  * (pinned-RAM H2D tier): enqueue on copy_stream the host-to-HBM copy of one

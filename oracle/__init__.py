@@ -23,7 +23,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _BUILD = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD, "liboracle.so")
 
-Q8_0, Q4_0, Q4_K, Q5_K, Q6_K = 0, 1, 2, 3, 4
+Q8_0, Q4_0, Q4_K, Q5_K, Q6_K, F16, F32 = 0, 1, 2, 3, 4, 5, 6
 
 
 def build(force: bool = False) -> str:

@@ -42,11 +42,11 @@
 #include <omp.h>
 #endif
 
-enum { OR_Q8_0 = 0, OR_Q4_0 = 1, OR_Q4_K = 2, OR_Q5_K = 3, OR_Q6_K = 4 };
+enum { OR_Q8_0 = 0, OR_Q4_0 = 1, OR_Q4_K = 2, OR_Q5_K = 3, OR_Q6_K = 4, OR_F16 = 5, OR_F32 = 6 };
 
 int or_block_elems(int fmt) {
   switch (fmt) {
-    case OR_Q8_0: case OR_Q4_0: return 32;
+    case OR_Q8_0: case OR_Q4_0: case OR_F16: case OR_F32: return 32;  /* F16/F32: 32 plain values */
     case OR_Q4_K: case OR_Q5_K: case OR_Q6_K: return 256;
     default: return 0;
   }
@@ -59,6 +59,8 @@ int or_block_bytes(int fmt) {
     case OR_Q4_K: return 2 + 2 + 12 + 128;   /* d, dmin, scales[12], qs[128]   */
     case OR_Q5_K: return 2 + 2 + 12 + 32 + 128; /* + qh[32]                    */
     case OR_Q6_K: return 128 + 64 + 16 + 2;  /* ql[128], qh[64], sc[16], d     */
+    case OR_F16: return 32 * 2;              /* binary16 values                */
+    case OR_F32: return 32 * 4;              /* binary32 values                */
     default: return 0;
   }
 }
@@ -178,6 +180,17 @@ void or_dequant_block(int fmt, const uint8_t* b, float* out) {
         int s = sc[(i / 128) * 8 + (i % 128) / 16];
         int q = or_quant_of(fmt, b, i) - 32;
         out[i] = d * (float)(s * q);   /* |s*q| <= 4096: exact product */
+      }
+      break;
+    }
+    case OR_F16:   /* every binary16 value is exact in fp32 */
+      for (int i = 0; i < 32; ++i) out[i] = half_f(b + 2 * i);
+      break;
+    case OR_F32: { /* little-endian binary32 */
+      for (int i = 0; i < 32; ++i) {
+        uint32_t u = (uint32_t)b[4 * i] | ((uint32_t)b[4 * i + 1] << 8) | ((uint32_t)b[4 * i + 2] << 16) |
+                     ((uint32_t)b[4 * i + 3] << 24);
+        memcpy(&out[i], &u, 4);
       }
       break;
     }

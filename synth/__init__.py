@@ -19,11 +19,12 @@ _BUILD = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD, "libsynth.so")
 
 # format ids (same numbering as the public C ABI's nt_fmt)
-Q8_0, Q4_0, Q4_K, Q5_K, Q6_K = 0, 1, 2, 3, 4
-FMT_NAMES = {Q8_0: "Q8_0", Q4_0: "Q4_0", Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K"}
+Q8_0, Q4_0, Q4_K, Q5_K, Q6_K, F16, F32 = 0, 1, 2, 3, 4, 5, 6
+FMT_NAMES = {Q8_0: "Q8_0", Q4_0: "Q4_0", Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K", F16: "F16", F32: "F32"}
 FMT_BY_NAME = {v: k for k, v in FMT_NAMES.items()}
-BLOCK_ELEMS = {Q8_0: 32, Q4_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256}
-BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q4_K: 144, Q5_K: 176, Q6_K: 210}
+# F16 / F32 rows are plain arrays, handled in units of 32 values
+BLOCK_ELEMS = {Q8_0: 32, Q4_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256, F16: 32, F32: 32}
+BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q4_K: 144, Q5_K: 176, Q6_K: 210, F16: 64, F32: 128}
 
 
 def build(force: bool = False) -> str:
@@ -66,7 +67,9 @@ def row_bytes(fmt: int, cols: int) -> int:
 
 def quant_matrix(fmt: int, rows: int, cols: int, seed: int, stream: int, scale_std: float = 0.02,
                  out: np.ndarray | None = None) -> np.ndarray:
-    """rows x cols block-quantized matrix as raw bytes, shape [rows, row_bytes]."""
+    """rows x cols block-quantized matrix as raw bytes, shape [rows, row_bytes].
+    Block scales are f16(|N(0,1)| * scale_std); F16 / F32 weights are plain
+    N(0, scale_std^2) values."""
     if cols % BLOCK_ELEMS[fmt]:
         raise ValueError("cols must be a multiple of the block size")
     rb = row_bytes(fmt, cols)

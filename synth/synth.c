@@ -11,7 +11,8 @@
  * Normals: Box & Muller (1958), z = sqrt(-2 ln u1) cos(2 pi u2).
  *
  * Block byte layouts follow the GGUF-style formats named on the pages
- * ("Ntransformer", en.unwiki.net — About: Q4_0, Q8_0, Q4_K_M, Q5_K, Q6_K);
+ * ("Ntransformer", en.unwiki.net — About: Q4_0, Q8_0, Q4_K_M, Q5_K, Q6_K, F16,
+ * F32; the float formats are handled as "blocks" of 32 plain values);
  * this file only needs to know where the fp16 scale fields sit and which
  * bytes carry quants, because every other byte is drawn uniformly.
  */
@@ -24,7 +25,7 @@
 #endif
 
 /* format ids — kept identical to the numbering of the public C ABI */
-enum { SY_Q8_0 = 0, SY_Q4_0 = 1, SY_Q4_K = 2, SY_Q5_K = 3, SY_Q6_K = 4 };
+enum { SY_Q8_0 = 0, SY_Q4_0 = 1, SY_Q4_K = 2, SY_Q5_K = 3, SY_Q6_K = 4, SY_F16 = 5, SY_F32 = 6 };
 
 static inline uint64_t sm64(uint64_t z) {
   z += 0x9E3779B97F4A7C15ull;
@@ -77,7 +78,7 @@ static void rand_bytes(uint8_t* p, int n, uint64_t seed, uint64_t stream, uint64
 
 int sy_block_elems(int fmt) {
   switch (fmt) {
-    case SY_Q8_0: case SY_Q4_0: return 32;
+    case SY_Q8_0: case SY_Q4_0: case SY_F16: case SY_F32: return 32;
     case SY_Q4_K: case SY_Q5_K: case SY_Q6_K: return 256;
     default: return 0;
   }
@@ -89,6 +90,8 @@ int sy_block_bytes(int fmt) {
     case SY_Q4_K: return 144;
     case SY_Q5_K: return 176;
     case SY_Q6_K: return 210;
+    case SY_F16: return 64;   /* 32 binary16 values, no scale */
+    case SY_F32: return 128;  /* 32 binary32 values */
     default: return 0;
   }
 }
@@ -133,6 +136,20 @@ static void fill_block(int fmt, uint8_t* b, uint64_t seed, uint64_t stream, uint
     case SY_Q6_K:
       rand_bytes(b, 208, seed, stream, c + 4);
       put_u16(b + 208, to_half_bits(n0));
+      break;
+    case SY_F16:
+    case SY_F32:
+      /* plain weights N(0, scale_std^2): element i from counters c + 2i, c + 2i + 1 */
+      for (int i = 0; i < 32; ++i) {
+        double v = box_muller(draw(seed, stream, c + 2u * (uint64_t)i), draw(seed, stream, c + 2u * (uint64_t)i + 1u)) *
+                   scale_std;
+        if (fmt == SY_F16) {
+          put_u16(b + 2 * i, to_half_bits(v));
+        } else {
+          float f = (float)v;
+          memcpy(b + 4 * i, &f, 4);  /* little-endian on every supported host */
+        }
+      }
       break;
     default: break;
   }

@@ -32,8 +32,8 @@ def test_library_exports_every_declared_symbol():
 
 def test_geometry_and_null_context():
     from block_quantized_gemv_nt_gb300 import nt
-    assert [nt.nt_block_bytes(f) for f in range(5)] == [34, 18, 144, 176, 210]
-    assert [nt.nt_block_elems(f) for f in range(5)] == [32, 32, 256, 256, 256]
+    assert [nt.nt_block_bytes(f) for f in range(7)] == [34, 18, 144, 176, 210, 64, 128]
+    assert [nt.nt_block_elems(f) for f in range(7)] == [32, 32, 256, 256, 256, 32, 32]
     assert nt.nt_block_bytes(9) == 0
     L = nt.lib()
     assert L.nt_gemv_q(None, 0, None, None, None, 1, 32, None, None) == nt.NT_ERR_INVALID_ARG

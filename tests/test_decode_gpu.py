@@ -60,7 +60,8 @@ def _run(ctx, name, n_steps, skip=None, continue_on_device=False, layers=None):
     return worst, agree
 
 
-@pytest.mark.parametrize("name", ["tiny_q8_0", "tiny_q4_0", "tiny_q4_k", "tiny_q5_k", "tiny_q6_k", "tiny_q4_k_m"])
+@pytest.mark.parametrize("name", ["tiny_q8_0", "tiny_q4_0", "tiny_q4_k", "tiny_q5_k", "tiny_q6_k", "tiny_q4_k_m",
+                                  "tiny_f16", "tiny_f32"])
 def test_decode_tiny(ctx, name):
     worst, agree = _run(ctx, name, 6)
     assert worst <= 2e-2 and agree == 6

@@ -1,7 +1,8 @@
 """Quant GEMV and dequantisation on the GPU vs the fp64 oracle, through the C ABI.
 
-Bar: dequantised weights bit-exact (all five formats); GEMV relative L2 error
-<= 1e-3 of the fp64 oracle (the stated tolerance)."""
+Bar: dequantised weights bit-exact (all seven formats: the five block formats
+and plain F16 / F32); GEMV relative L2 error <= 1e-3 of the fp64 oracle (the
+stated tolerance)."""
 import numpy as np
 import pytest
 
@@ -11,7 +12,7 @@ from gpu_util import dev, host, need_gpu, rel_l2, torch
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-3
-FMTS = [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q5_K, synth.Q6_K]
+FMTS = [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q5_K, synth.Q6_K, synth.F16, synth.F32]
 
 
 @pytest.fixture(scope="module")

@@ -41,10 +41,52 @@ def test_float_to_half_rne_matches_numpy():
 
 # --- block layouts --------------------------------------------------------
 @pytest.mark.parametrize("name,elems,nbytes", [("Q8_0", 32, 34), ("Q4_0", 32, 18), ("Q4_K", 256, 144),
-                                               ("Q5_K", 256, 176), ("Q6_K", 256, 210)])
+                                               ("Q5_K", 256, 176), ("Q6_K", 256, 210), ("F16", 32, 64),
+                                               ("F32", 32, 128)])
 def test_block_geometry(name, elems, nbytes):
-    assert oracle.block_elems(FMTS[name]) == elems
-    assert oracle.block_bytes(FMTS[name]) == nbytes
+    fmt = FMTS.get(name, {"F16": 5, "F32": 6}.get(name))
+    assert oracle.block_elems(fmt) == elems
+    assert oracle.block_bytes(fmt) == nbytes
+
+
+# --- the float formats ("Ntransformer" (en.unwiki.net), About: F16, F32) -----
+def test_f16_rows_decode_like_numpy():
+    """F16 weights are IEEE binary16 values, row-major: numpy's float16 view of
+    the same bytes (every bit pattern but NaN) is the reference."""
+    bits = np.arange(65536, dtype=np.uint16)
+    bits = bits[~np.isnan(bits.view(np.float16))]
+    n = len(bits) // 32 * 32
+    W = bits[:n].view(np.uint8).reshape(n // 32, 64)
+    got = oracle.dequant(5, W, n // 32, 32)
+    ref = bits[:n].view(np.float16).astype(np.float32).reshape(n // 32, 32)
+    assert np.array_equal(got, ref)
+
+
+def test_f32_rows_are_the_bytes():
+    x = synth.normal_f32(4 * 96, seed=9, stream=9)
+    got = oracle.dequant(6, x.view(np.uint8).reshape(4, 96 * 4), 4, 96)
+    assert np.array_equal(got, x.reshape(4, 96))
+
+
+@pytest.mark.parametrize("fmt", [5, 6])
+def test_float_format_gemv_is_plain_matvec(fmt):
+    """y = W x with W the float matrix itself (numpy fp64 matvec, same column order)."""
+    rows, cols = 9, 160
+    W = synth.quant_matrix(fmt, rows, cols, seed=5, stream=fmt)
+    x = synth.normal_f32(cols, seed=5, stream=50).astype(np.float64)
+    dense = (W.view(np.float16) if fmt == 5 else W.view(np.float32)).astype(np.float64).reshape(rows, cols)
+    y = oracle.gemv(fmt, W, x, rows, cols)
+    assert np.allclose(y, dense @ x, rtol=1e-13, atol=1e-15)
+
+
+def test_float_format_generator_statistics():
+    """The generator's plain weights are N(0, scale^2): mean and std within a
+    few standard errors at 64k samples."""
+    for fmt, view in ((5, np.float16), (6, np.float32)):
+        W = synth.quant_matrix(fmt, 256, 256, seed=11, stream=1, scale_std=0.5)
+        v = W.view(view).astype(np.float64).ravel()
+        assert abs(v.mean()) < 4 * 0.5 / np.sqrt(v.size)
+        assert abs(v.std() - 0.5) < 0.01
 
 
 def test_q6_k_layer_size_matches_page():
@@ -126,7 +168,7 @@ def test_kquant_scale_bits_are_a_bijection():
 
 
 # --- GEMV -----------------------------------------------------------------
-@pytest.mark.parametrize("fmt", range(5))
+@pytest.mark.parametrize("fmt", range(7))
 def test_gemv_brute_force_small(fmt):
     be = oracle.block_elems(fmt)
     rows, cols = 5, 2 * be
@@ -138,7 +180,7 @@ def test_gemv_brute_force_small(fmt):
     assert np.allclose(y, ref, rtol=1e-13, atol=1e-12 * np.abs(ref).max())
 
 
-@pytest.mark.parametrize("fmt", range(5))
+@pytest.mark.parametrize("fmt", range(7))
 def test_gemv_one_hot_returns_column(fmt):
     be = oracle.block_elems(fmt)
     rows, cols = 7, 3 * be

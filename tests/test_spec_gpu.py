@@ -28,7 +28,7 @@ def ctx():
 
 
 # ---- verify GEMM ----------------------------------------------------------
-@pytest.mark.parametrize("fmt", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q5_K, synth.Q6_K])
+@pytest.mark.parametrize("fmt", [synth.Q8_0, synth.Q4_0, synth.Q4_K, synth.Q5_K, synth.Q6_K, synth.F16, synth.F32])
 @pytest.mark.parametrize("rows,cols,M", [(300, 2304, 5), (257, 4608, 1), (64, 2048, 8), (1000, 512, 3)])
 def test_gemm_q_matches_oracle(ctx, fmt, rows, cols, M):
     """Y[m] = W X[m] for M vectors; columns cut into 2048-wide parts (ragged
