@@ -63,6 +63,7 @@ struct nt_model {
   int32_t* spec_tok = nullptr;         // [kMaxVerify]: the step's token, then the drafts
   int64_t* spec_pos = nullptr;         // [kMaxVerify]: pos + i
   int32_t* vtok = nullptr;             // [kMaxVerify]: argmax of each verify row
+  int32_t* prompt = nullptr;           // [kv_cap]: prefill tokens
   unsigned long long* vkey = nullptr;  // [kMaxVerify] argmax keys and counters
   unsigned* vcnt = nullptr;
   float *xv = nullptr, *qv = nullptr, *aov = nullptr, *hv = nullptr, *lv = nullptr, *dlogits = nullptr;
@@ -277,15 +278,17 @@ nt_status enqueue_step(Ctx* c, nt_model* m, const uint8_t* skip, const StepIO& i
 // the verify pass: tokens spec_tok[0..M) at positions spec_pos[0] + i
 // through every layer (M-vector GEMMs, causal M-query attention), logits
 // [M][vocab], row argmaxes into vtok
-// sm: the pass's streaming schedule, begun by the caller (its first copies
-// may overlap the drafts)
-nt_status enqueue_verify(Ctx* c, nt_model* m, int M, float* logits, Streamer& sm, cudaStream_t st) {
+// the M tokens tok_dev[0..M) at positions pos_dev[0] + i; sm: the pass's
+// streaming schedule, begun by the caller (its first copies may overlap the
+// drafts); logits == nullptr: no LM head (a prefill chunk before the last)
+nt_status enqueue_multi(Ctx* c, nt_model* m, int M, const int32_t* tok_dev, const int64_t* pos_dev, float* logits,
+                        bool argmax, Streamer& sm, cudaStream_t st) {
   const nt_model_desc& d = m->d;
   const int hd = d.head_dim;
   const int64_t nq = int64_t(d.n_qh) * hd, nkv = int64_t(d.n_kvh) * hd;
-  nt_status s = launch_embed(c, d.fmt_embd, m->embd, d.d_model, m->spec_tok, m->xv, st, M);
+  nt_status s = launch_embed(c, d.fmt_embd, m->embd, d.d_model, tok_dev, m->xv, st, M);
   if (s) return s;
-  const RopeArgs ra{m->spec_pos, m->inv_freq, hd, d.kv_cap};
+  const RopeArgs ra{pos_dev, m->inv_freq, hd, d.kv_cap};
   for (int l = 0; l < d.n_layers; ++l) {
     nt_layer_ptrs L;
     int slot;
@@ -311,7 +314,7 @@ nt_status enqueue_verify(Ctx* c, nt_model* m, int M, float* logits, Streamer& sm
         if (s) return s;
       }
     }
-    s = launch_attn(c, m->qv, L.kcache, L.vcache, m->aov, d.n_qh, d.n_kvh, 0, m->spec_pos, d.kv_cap, m->attn_part,
+    s = launch_attn(c, m->qv, L.kcache, L.vcache, m->aov, d.n_qh, d.n_kvh, 0, pos_dev, d.kv_cap, m->attn_part,
                     m->attn_cnt, m->S, st, M);
     if (s) return s;
     {
@@ -337,16 +340,26 @@ nt_status enqueue_verify(Ctx* c, nt_model* m, int M, float* logits, Streamer& sm
     if (s) return s;
   }
   s = sm.end();
-  if (s) return s;
+  if (s || !logits) return s;
   {
     const GemmJobEx j{m->out, d.vocab, logits, d.vocab, nullptr, nullptr, kEpiPlain};
     s = launch_gemm(c, d.fmt_out, &j, 1, false, m->xv, d.d_model, M, m->out_norm, d.eps, d.d_model, nullptr,
                     m->gpart, m->gpart_bytes, st);
     if (s) return s;
   }
-  for (int i = 0; i < M && !s; ++i)
+  for (int i = 0; argmax && i < M && !s; ++i)
     s = launch_argmax(c, logits + int64_t(i) * d.vocab, d.vocab, m->vtok + i, m->vkey + i, m->vcnt + i, st);
   return s;
+}
+
+// one prefill chunk: tokens prompt[0..M) at positions base + i
+__global__ void prefill_setup_kernel(const int32_t* prompt, int64_t base, int32_t* tok, int64_t* pos, int M) {
+  pdl_wait();
+  pdl_trigger();
+  if (int(threadIdx.x) < M) {
+    tok[threadIdx.x] = prompt[threadIdx.x];
+    pos[threadIdx.x] = base + threadIdx.x;
+  }
 }
 
 // start of a speculative step: the step's token and the positions of the
@@ -402,7 +415,7 @@ nt_status enqueue_spec(Ctx* c, nt_model* m, int k, int n_draft, int32_t* out, in
     s = enqueue_step(c, m, mask.data(), StepIO{m->spec_tok + i, m->spec_pos + i, m->dlogits, m->spec_tok + i + 1, false},
                      st, false);
   if (!s && drafts_stream) s = sm.begin(nullptr);
-  if (!s) s = enqueue_verify(c, m, M, logits ? logits : m->lv, sm, st);
+  if (!s) s = enqueue_multi(c, m, M, m->spec_tok, m->spec_pos, logits ? logits : m->lv, true, sm, st);
   if (!s && !c->dry)
     s = cuda_check(c, launch_k(c, spec_accept_kernel, dim3(1), dim3(32), 0, st, m->spec_tok, m->vtok, k, out, n_out,
                                m->tok, m->pos, m->spec_pos),
@@ -543,7 +556,8 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
                nh = up256(fl * d.ffn), ncos = up256(fl * d.n_layers), nst = 256, nfreq = up256(8 * d.head_dim),
                npart = up256(attn_scratch_bytes(d.n_qh, d.n_kvh, m->S, kMaxVerify)), nspec = 1024,
                nvx = up256(fl * kMaxVerify * d.d_model), nvq = up256(fl * kMaxVerify * nq),
-               nvh = up256(fl * kMaxVerify * d.ffn), nvl = up256(fl * kMaxVerify * d.vocab), ndl = up256(fl * d.vocab);
+               nvh = up256(fl * kMaxVerify * d.ffn), nvl = up256(fl * kMaxVerify * d.vocab), ndl = up256(fl * d.vocab),
+               nprompt = up256(sizeof(int32_t) * size_t(d.kv_cap));
   {
     // partial sums of the largest verify GEMM
     const int64_t nkv = int64_t(d.n_kvh) * d.head_dim;
@@ -556,7 +570,7 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
     m->gpart_bytes = up256(m->gpart_bytes);
   }
   const size_t total = 2 * nx + nqb * 2 + nkb * 2 + nh + ncos + nst + npart + nfreq + nspec + nvx + 2 * nvq + nvh +
-                       nvl + ndl + m->gpart_bytes;
+                       nvl + ndl + nprompt + m->gpart_bytes;
   int dev_prev = 0;
   cudaGetDevice(&dev_prev);
   cudaSetDevice(ctx->device);
@@ -614,6 +628,7 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   m->hv = reinterpret_cast<float*>(take(nvh));
   m->lv = reinterpret_cast<float*>(take(nvl));
   m->dlogits = reinterpret_cast<float*>(take(ndl));
+  m->prompt = reinterpret_cast<int32_t*>(take(nprompt));
   m->gpart = reinterpret_cast<float*>(take(m->gpart_bytes));
   cudaSetDevice(ctx->device);
   nt_status st = launch_inv_freq(ctx, m->inv_freq, d.head_dim, d.theta, nullptr);
@@ -753,6 +768,49 @@ nt_status nt_layer_blob_layout(const nt_model_desc* d, size_t* off, size_t* byte
   if (d->d_model <= 0 || d->n_qh <= 0 || d->n_kvh <= 0 || d->head_dim <= 0 || d->ffn <= 0) return NT_ERR_INVALID_ARG;
   blob_layout(*d, off, bytes);
   return NT_OK;
+}
+
+nt_status nt_prefill(nt_ctx* ctx, nt_model* m, const int32_t* tokens_host, int64_t n, int64_t pos0, float* logits,
+                     int32_t* next_tok, void* stream) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  NT_REQUIRE(m && tokens_host && logits, NT_ERR_INVALID_ARG, "null model, tokens or logits");
+  NT_REQUIRE(aligned(logits, 16), NT_ERR_ALIGNMENT, "logits must be 16-byte aligned");
+  NT_REQUIRE(n >= 1 && pos0 >= 0 && pos0 + n <= m->d.kv_cap, NT_ERR_INVALID_ARG,
+             "need n >= 1 and pos0 + n <= kv_cap (%lld)", (long long)m->d.kv_cap);
+  for (int64_t i = 0; i < n; ++i)
+    NT_REQUIRE(tokens_host[i] >= 0 && tokens_host[i] < m->d.vocab, NT_ERR_INVALID_ARG,
+               "token %lld outside the vocabulary", (long long)i);
+  int dev_prev = 0;
+  cudaGetDevice(&dev_prev);
+  if (dev_prev != ctx->device) cudaSetDevice(ctx->device);
+  cudaStream_t st = as_stream(stream);
+  nt_status s = cuda_check(ctx, cudaMemcpyAsync(m->prompt, tokens_host, sizeof(int32_t) * size_t(n),
+                                                cudaMemcpyHostToDevice, st),
+                           "prompt upload");
+  for (int64_t base = 0; base < n && !s; base += kMaxVerify) {
+    const int M = int(std::min<int64_t>(kMaxVerify, n - base));
+    const bool last = base + M == n;
+    s = cuda_check(ctx, launch_k(ctx, prefill_setup_kernel, dim3(1), dim3(32), 0, st, m->prompt + base, pos0 + base,
+                                 m->spec_tok, m->spec_pos, M),
+                   "prefill chunk setup");
+    Streamer sm{ctx, m, st};
+    if (!s) s = sm.begin(nullptr);
+    if (!s) s = enqueue_multi(ctx, m, M, m->spec_tok, m->spec_pos, last ? m->lv : nullptr, false, sm, st);
+    if (!s && last) {
+      // the last token's logits; greedy next token and the device state for decoding on
+      s = cuda_check(ctx, cudaMemcpyAsync(logits, m->lv + int64_t(M - 1) * m->d.vocab, sizeof(float) * m->d.vocab,
+                                          cudaMemcpyDeviceToDevice, st),
+                     "prefill logits");
+      if (!s) {
+        set_state_kernel<<<1, 1, 0, st>>>(m->tok, m->pos, 0, pos0 + n - 1);
+        s = cuda_check(ctx, cudaGetLastError(), "prefill state");
+      }
+      if (!s)
+        s = launch_argmax(ctx, logits, m->d.vocab, next_tok, m->amax_key, m->amax_cnt, st, m->tok, m->pos);
+    }
+  }
+  if (dev_prev != ctx->device) cudaSetDevice(dev_prev);
+  return s;
 }
 
 nt_status nt_plan_residency(const nt_model_desc* d, size_t budget, int embd_in_hbm, nt_residency_plan* out) {

@@ -69,6 +69,33 @@ struct GemvArgs {
   int pblk[5];        // part p covers blocks [pblk[p], pblk[p+1])
 };
 
+// the R per-lane partial sums of a row group, summed over the warp: lane
+// i < R returns row i.  A butterfly that halves the rows each lane carries
+// before the plain tree: 7 shuffles for R = 4 and 6 for R = 2, against 5 per
+// row for R separate warp sums.
+__device__ __forceinline__ float rows_reduce(float (&a)[4], int lane) {
+  const bool b4 = lane & 16, b3 = lane & 8;
+  float k0 = b4 ? a[2] : a[0], k1 = b4 ? a[3] : a[1];  // rows 2*b4 and 2*b4 + 1 stay
+  k0 += __shfl_xor_sync(0xffffffffu, b4 ? a[0] : a[2], 16);
+  k1 += __shfl_xor_sync(0xffffffffu, b4 ? a[1] : a[3], 16);
+  float k = b3 ? k1 : k0;                               // row 2*b4 + b3 stays
+  k += __shfl_xor_sync(0xffffffffu, b3 ? k0 : k1, 8);
+  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  return __shfl_sync(0xffffffffu, k, (lane & 3) * 8);  // row r lives on lane 8r
+}
+__device__ __forceinline__ float rows_reduce(float (&a)[2], int lane) {
+  const bool b4 = lane & 16;
+  float k = b4 ? a[1] : a[0];
+  k += __shfl_xor_sync(0xffffffffu, b4 ? a[0] : a[1], 16);
+  k += __shfl_xor_sync(0xffffffffu, k, 8);
+  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  return __shfl_sync(0xffffffffu, k, (lane & 1) * 16);  // row r lives on lane 16r
+}
+
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -302,13 +329,9 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
     __syncwarp();
     if (cseg == nseg - 1) {
       // group done: reduce across lanes, lane i holds row i
-      float mine = 0.f;
+      float mine = rows_reduce(acc, lane);
 #pragma unroll
-      for (int i = 0; i < R; ++i) {
-        const float v = warp_sum(acc[i]);
-        if (lane == i) mine = v;
-        acc[i] = 0.f;
-      }
+      for (int i = 0; i < R; ++i) acc[i] = 0.f;
       if (KS > 1) {
         // the parts of a split group meet in shared memory (double-buffered by group parity)
         float* xb = xchg + ((ct & 1) * slots + slot) * KS * R;

@@ -97,6 +97,12 @@ class DeviceModel:
         nt.nt_decode_step(self.ctx, self.handle, token, pos, skip, self.logits, self.next_token, stream)
         return self.logits
 
+    def prefill(self, tokens, pos0: int, stream=None):
+        """Run a prompt through the model (KV written for pos0 ..); returns the
+        logits after its last token.  Decoding continues with step(-1, 0)."""
+        nt.nt_prefill(self.ctx, self.handle, tokens, pos0, self.logits, self.next_token, stream)
+        return self.logits
+
     def spec_step(self, token: int, pos: int, k: int, n_draft_layers: int = 0, stream=None):
         """One self-speculative step (token < 0 continues from the device
         state); returns (tokens [k + 1] int32 device tensor, count [1] int32

@@ -269,6 +269,18 @@ nt_status nt_layer_skip_calibrate(nt_ctx* ctx, nt_model* model, int32_t token, i
                                   uint8_t* skip_mask_host, float* cos_host, float* logits_dev,
                                   int32_t* next_token_dev, void* stream);
 
+/* Prompt prefill [feat] (KV cache): run tokens_host[0..n) at positions
+ * pos0 .. pos0 + n - 1 through every layer, writing their K/V into the
+ * caches, in chunks of up to 8 tokens — each chunk one pass of the M-vector
+ * GEMMs and the causal multi-query attention of the verify step (weights
+ * read once per chunk).  logits_dev receives the logits after the last
+ * token, next_token_dev (nullable) their argmax, and the device state
+ * becomes (that argmax, pos0 + n): nt_decode_step with token < 0 continues
+ * from there.  Runs eagerly on `stream` (no graph); streamed layers stream
+ * once per chunk.  tokens_host is read before the call returns. */
+nt_status nt_prefill(nt_ctx* ctx, nt_model* model, const int32_t* tokens_host, int64_t n, int64_t pos0,
+                     float* logits_dev, int32_t* next_token_dev, void* stream);
+
 /* Resident-layer planner [about] (3-tier adaptive caching: VRAM-resident
  * layers first, the rest from pinned RAM) [cache] (the format decides how
  * many layers fit: "36 vs 26" for Q4_K_M vs Q6_K on the pages' card): how

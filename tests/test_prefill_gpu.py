@@ -1,0 +1,77 @@
+"""Prompt prefill on the GPU (the step before decoding: "ntransformer - moteur
+d'inférence NVMe-to-GPU…", "Fonctionnalités principales", KV cache): chunks of
+up to 8 prompt tokens through the M-vector GEMMs and causal multi-query
+attention, against the fp64 oracle run token by token (teacher-forced).
+
+Pins: the K/V the prefill writes for every prompt position match the
+oracle's (one f16 ulp plus the fp32 GEMV rounding), the logits after the last
+prompt token match the oracle's within the decode tolerance, and decoding
+continues from the prefilled state like the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import need_gpu, torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    need_gpu()
+    from block_quantized_gemv_nt_gb300 import nt
+    c = nt.Context(0)
+    yield c
+    c.sync()
+    c.close()
+
+
+def _prompt(spec, n, stream):
+    raw = synth.random_bytes(4 * n, seed=spec.seed, stream=stream).view(np.uint32)
+    return (raw % spec.vocab).astype(np.int32)
+
+
+@pytest.mark.parametrize("name,n,pos0", [("tiny_q4_k_m", 20, 37), ("tiny_q8_0", 8, 0), ("small_q6_k", 13, 300),
+                                         ("tiny_f16", 3, 40), ("small_q4_k_m_r1", 11, 290)])
+def test_prefill_matches_oracle(ctx, name, n, pos0):
+    from block_quantized_gemv_nt_gb300 import engine
+    spec = synth.model_spec(name)
+    blobs = engine.HostBlobs(spec) if spec.n_resident >= 0 else None
+    hm = synth.make_host_model(spec, out_view=blobs.view if blobs else None)
+    om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
+    gm = engine.DeviceModel(ctx, spec, hm, blobs=blobs)
+    prompt = _prompt(spec, n, 777)
+    got = gm.prefill(prompt, pos0).cpu().numpy().astype(np.float64)
+    for i, t in enumerate(prompt):
+        ref = om.step(int(t), pos0 + i)
+    assert np.max(np.abs(got - ref)) <= 2e-2 * ref.std()
+    assert int(gm.next_token.item()) == int(np.argmax(got)) == int(np.argmax(ref))
+    # the K/V of every prompt position, every layer
+    torch.cuda.synchronize()
+    for li in range(spec.n_layers):
+        for which in ("kcache", "vcache"):
+            g = gm.layers[li][which].cpu().numpy().astype(np.float64)[:, pos0:pos0 + n]
+            o = getattr(om, which)[li].astype(np.float64)[:, pos0:pos0 + n]
+            scale = np.sqrt(np.mean(o ** 2, axis=-1, keepdims=True))
+            assert np.all(np.abs(g - o) <= np.abs(o) * 2 ** -10 + 1e-4 * scale), (li, which)
+    # decoding continues from the prefilled state
+    tok = int(np.argmax(got))
+    for step in range(3):
+        g = gm.step(-1, 0).cpu().numpy().astype(np.float64)
+        r = om.step(tok, pos0 + n + step)
+        assert np.max(np.abs(g - r)) <= 2e-2 * r.std()
+        assert int(np.argmax(g)) == int(np.argmax(r))
+        tok = int(np.argmax(r))
+    gm.close()
+
+
+def test_prefill_bad_args(ctx):
+    from block_quantized_gemv_nt_gb300 import engine, nt
+    spec = synth.model_spec("tiny_q8_0")
+    gm = engine.DeviceModel(ctx, spec, synth.make_host_model(spec))
+    for toks, pos0 in [([], 0), ([1, 2], spec.kv_cap - 1), ([spec.vocab], 0), ([-1], 0), ([1], -1)]:
+        with pytest.raises(nt.NtError) as ei:
+            nt.nt_prefill(ctx, gm.handle, toks, pos0, gm.logits)
+        assert ei.value.status == nt.NT_ERR_INVALID_ARG
+    gm.close()
