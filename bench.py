@@ -348,6 +348,56 @@ def gemv_plan(spec, skip=None):
     return plan
 
 
+def bench_prefill(args, rank, world):
+    """<model>_prefill<N>: one N-token prompt through nt_prefill (chunks of 8
+    tokens through the verify GEMMs), repeated; tokens/s of prompt."""
+    import torch
+
+    import synth
+    from block_quantized_gemv_nt_gb300 import engine, nt
+
+    base, n = args.workload.rsplit("_prefill", 1)
+    n = int(n)
+    spec = synth.model_spec(base)
+    hm = synth.make_host_model(spec)
+    ctx = nt.Context(torch.cuda.current_device())
+    gm = engine.DeviceModel(ctx, spec, hm)
+    raw = synth.random_bytes(4 * n, seed=spec.seed, stream=777).view(np.uint32)
+    prompt = (raw % spec.vocab).astype(np.int32)
+    pos0 = max(0, min(spec.n_prefill, spec.kv_cap - n))
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        for _ in range(max(1, min(args.warmup, 2))):
+            gm.prefill(prompt, pos0, stream=st)
+        st.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            clk.wait_first()
+            e0.record(st)
+            for _ in range(args.steps):
+                gm.prefill(prompt, pos0, stream=st)
+            e1.record(st)
+            e1.synchronize()
+            clk.wait_one_more()
+    ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    chunks = -(-n // 8)
+    wbytes = spec.layer_bytes() * spec.n_layers
+    gbs = chunks * wbytes / (ms / 1e3) / 1e9
+    peak, kind = measured_peaks()
+    ctx.sync()
+    gm.close()
+    return {"metric": METRIC, "value": round(n / (ms / 1e3) * world, 2), "unit": "prompt tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32 (block-quantized weights, f16 KV)",
+            "data": "synthetic: random weights of the named shape, seeded", "impl": "ours",
+            "config": {"workload": args.workload, "prompt_tokens": n, "chunks_of_8": chunks, "pos0": pos0},
+            "roofline": {"bound": "alu", "kernel": "qgemm (M = 8)", "achieved": round(gbs, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_kind": kind + " (HBM copy; the M = 8 "
+                         "GEMM is integer-issue-bound, see DESIGN)", "traffic": None,
+                         "algo_bytes_per_launch": wbytes},
+            "gpu_launches": None, "clocks": clk.summary()}
+
+
 def parse_decode(name):
     """<model>[_skip<N>][_spec<K>]: a synthetic model, optionally decoding with
     the N layers of highest calibration cosine skipped, or self-speculatively
@@ -731,7 +781,12 @@ def reference_arm(args, rank, world):
                 "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                                  "sample": f"{args.steps} full oracle GEMVs"},
                 "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    spec, n_skip, _ = parse_decode(args.workload)
+    prefill_n = 0
+    if "_prefill" in args.workload:
+        base, n = args.workload.rsplit("_prefill", 1)
+        spec, n_skip, prefill_n = synth.model_spec(base), 0, int(n)
+    else:
+        spec, n_skip, _ = parse_decode(args.workload)
     hm = synth.make_host_model(spec)
     import oracle
     om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
@@ -747,7 +802,8 @@ def reference_arm(args, rank, world):
     n = max(1, min(args.steps, args.ref_max_steps))
     for _ in range(n):
         logits = om.step(tok, pos, skip)
-        tok, pos = int(np.argmax(logits)), pos + 1
+        # a prompt is fed token by token (teacher-forced); decoding feeds back the argmax
+        tok, pos = (int(np.argmax(logits)) if not prefill_n else (tok * 7 + 3) % spec.vocab), pos + 1
     dt = (time.perf_counter() - t0) / n
     v = round(1.0 / dt, 4)
     return {"metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world, "steps": n, "warmup": args.warmup,
@@ -792,6 +848,8 @@ def main():
         line = bench_gemv(args, rank, world)
     elif args.workload.startswith("attn"):
         line = bench_attn(args, rank, world)
+    elif "_prefill" in args.workload:
+        line = bench_prefill(args, rank, world)
     elif parse_decode(args.workload)[0].n_resident >= 0:
         line = bench_streamed(args, rank, world)
     else:

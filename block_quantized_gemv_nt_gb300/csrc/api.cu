@@ -349,6 +349,16 @@ nt_status nt_argmax(nt_ctx* ctx, const float* v, int64_t n, int32_t* out, void* 
   return launch_argmax(ctx, v, n, out, key, counter, as_stream(stream));
 }
 
+nt_status nt_sample(nt_ctx* ctx, const float* z, int64_t n, float T, float P, uint64_t seed, uint64_t counter,
+                    int32_t* out, void* stream) {
+  NT_TRY(pre_call(ctx));
+  NT_REQUIRE(z && out && n >= 1 && n <= (int64_t(1) << 31) - 1, NT_ERR_INVALID_ARG, "null pointer or bad n");
+  NT_REQUIRE(aligned(z, 4) && aligned(out, 4), NT_ERR_ALIGNMENT, "logits and out must be 4-byte aligned");
+  NT_REQUIRE(P > 0.f && P <= 1.f && !(T != T) && T < 3.0e38f, NT_ERR_INVALID_ARG, "top_p in (0, 1], finite temperature");
+  DeviceGuard g(ctx->device);
+  return launch_sample(ctx, z, n, T, P, seed, nullptr, int64_t(counter), out, as_stream(stream));
+}
+
 nt_status nt_cos_sim(nt_ctx* ctx, const float* a, const float* b, int64_t n, float* out, void* stream) {
   NT_TRY(pre_call(ctx));
   NT_REQUIRE(a && b && out && n > 0, NT_ERR_INVALID_ARG, "null pointer or n <= 0");

@@ -69,6 +69,8 @@ struct nt_model {
   float *xv = nullptr, *qv = nullptr, *aov = nullptr, *hv = nullptr, *lv = nullptr, *dlogits = nullptr;
   float* gpart = nullptr;              // verify-GEMM partial sums
   size_t gpart_bytes = 0;
+  float temperature = 0.f, top_p = 1.f;  // decode-step sampler (temperature <= 0: greedy)
+  uint64_t seed = 0;
 };
 
 namespace nt {
@@ -165,6 +167,7 @@ struct Streamer {
     slot = si % m->n_slots;
     bind_slot(m, slot, L);
     if (c->dry) return NT_OK;
+    c->pdl_hold = true;  // the layer's first kernel must not prefetch the slot before the copy lands
     return cuda_check(c, cudaStreamWaitEvent(st, m->ev_ready[slot], 0), "compute waits for its layer copy");
   }
   nt_status after(int slot) {
@@ -271,6 +274,9 @@ nt_status enqueue_step(Ctx* c, nt_model* m, const uint8_t* skip, const StepIO& i
     s = launch_gemv(c, d.fmt_out, &j, 1, nullptr, m->x, m->out_norm, d.eps, d.d_model, false, st);
     if (s) return s;
   }
+  if (io.advance && m->temperature > 0.f)  // counter: the position of this step's input token
+    return launch_sample(c, io.logits, d.vocab, m->temperature, m->top_p, m->seed, io.pos, 0, io.next_tok, st, m->tok,
+                         m->pos);
   return launch_argmax(c, io.logits, d.vocab, io.next_tok, m->amax_key, m->amax_cnt, st,
                        io.advance ? m->tok : nullptr, io.advance ? m->pos : nullptr);
 }
@@ -432,6 +438,9 @@ std::string graph_key(const nt_model* m, const uint8_t* skip, const float* logit
   std::string k("d");
   key_append(k, logits);
   key_append(k, next_tok);
+  key_append(k, m->temperature);
+  key_append(k, m->top_p);
+  key_append(k, m->seed);
   for (int l = 0; l < m->d.n_layers; ++l) k.push_back(skip && skip[l] ? '1' : '0');
   return k;
 }
@@ -811,6 +820,16 @@ nt_status nt_prefill(nt_ctx* ctx, nt_model* m, const int32_t* tokens_host, int64
   }
   if (dev_prev != ctx->device) cudaSetDevice(dev_prev);
   return s;
+}
+
+nt_status nt_model_set_sampler(nt_ctx* ctx, nt_model* m, float T, float P, uint64_t seed) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  NT_REQUIRE(m, NT_ERR_INVALID_ARG, "null model");
+  NT_REQUIRE(P > 0.f && P <= 1.f && !(T != T) && T < 3.0e38f, NT_ERR_INVALID_ARG, "top_p in (0, 1], finite temperature");
+  m->temperature = T > 0.f ? T : 0.f;
+  m->top_p = P;
+  m->seed = seed;
+  return NT_OK;
 }
 
 nt_status nt_plan_residency(const nt_model_desc* d, size_t budget, int embd_in_hbm, nt_residency_plan* out) {

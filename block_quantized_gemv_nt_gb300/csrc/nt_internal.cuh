@@ -35,6 +35,7 @@ struct Ctx {
   size_t scratch_bytes = 0;
   unsigned* err_flag = nullptr; // device word, set by kernels whose bounded wait ran out
   bool pdl = true;               // launch with programmatic stream serialization
+  mutable bool pdl_hold = false; // the next launch waits for everything before it (set after an event wait)
   int gemv_warps = 16;           // quant-GEMV launch shape (tuning knobs, env NT_GEMV_*)
   int gemv_stages = 2;
   int gemv_stage_max = 12288;
@@ -173,7 +174,10 @@ cudaError_t launch_k(const Ctx* c, void (*kernel)(KArgs...), dim3 grid, dim3 blo
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = (c && c->pdl) ? 1 : 0;
+  // a launch that follows a cross-stream event wait is not programmatic: its
+  // early part (weight prefetch) must not run before the awaited work
+  cfg.numAttrs = (c && c->pdl && !c->pdl_hold) ? 1 : 0;
+  if (c) c->pdl_hold = false;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

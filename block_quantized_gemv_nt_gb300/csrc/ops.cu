@@ -475,6 +475,210 @@ __global__ void argmax_kernel(const float* v, int64_t n, unsigned long long* key
   }
 }
 
+// ---- non-greedy sampler: temperature + nucleus (top-p) -------------------------------
+// Token weights are integers, w = rint(exp((z - max z) / T) * 2^40), so every
+// sum is exact and independent of the order of addition.  The nucleus is the
+// shortest prefix of the tokens ordered by logit (descending, ties by lower
+// index) whose weight reaches ceil(top_p * sum w), found by a 4-round radix
+// select on the order-preserving 32-bit key of the logit; the token is the
+// one of the nucleus, in index order, whose cumulative weight first exceeds
+// floor(u * nucleus weight), u from SplitMix64 (Steele, Lea & Flood 2014) of
+// (seed, counter).  One CTA of 1024 threads, each owning a contiguous index
+// range; T <= 0 is greedy.
+constexpr int kSampThreads = 1024;
+
+__device__ __forceinline__ uint64_t splitmix64(uint64_t z) {
+  z += 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// order-preserving key of a logit; NaN ranks below everything
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  if (v != v) return 0u;
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// exclusive prefix sum over the block (1024 threads); total in *total
+__device__ __forceinline__ unsigned long long block_excl_scan(unsigned long long v, unsigned long long* sm,
+                                                              unsigned long long* total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long w = sm[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    sm[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const unsigned long long before = (warp ? sm[warp - 1] : 0ull) + x - v;
+  *total = sm[31];
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(kSampThreads) sample_kernel(const float* z, int64_t n, float T, float P,
+                                                              uint64_t seed, const int64_t* ctr_dev, int64_t ctr,
+                                                              int32_t* out, int32_t* tok_state, int64_t* pos_state) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ unsigned long long sm[32];
+  __shared__ unsigned long long hist[256];
+  __shared__ unsigned long long s_above;
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_pick;
+  __shared__ float s_max;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t per = (n + kSampThreads - 1) / kSampThreads;
+  const int64_t i0 = min(n, int64_t(tid) * per), i1 = min(n, i0 + per);
+  const uint64_t counter = ctr_dev ? uint64_t(*ctr_dev) : uint64_t(ctr);
+
+  // largest logit (NaN never wins)
+  float mx = -INFINITY;
+  for (int64_t i = i0; i < i1; ++i) mx = fmaxf(mx, z[i]);  // fmaxf ignores a NaN operand
+  mx = warp_max(mx);
+  if (lane == 0) reinterpret_cast<float*>(sm)[warp] = mx;
+  __syncthreads();
+  if (warp == 0) {
+    float v = reinterpret_cast<float*>(sm)[lane];
+    v = warp_max(v);
+    if (lane == 0) s_max = v;
+  }
+  __syncthreads();
+  const float M = s_max;
+  int64_t pick = -1;
+
+  if (!(T > 0.f)) {
+    // greedy: lowest index holding the maximum
+    int64_t first = n;
+    for (int64_t i = i0; i < i1; ++i)
+      if (z[i] == M) {
+        first = i;
+        break;
+      }
+    unsigned long long f = static_cast<unsigned long long>(first);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long t = __shfl_xor_sync(0xffffffffu, f, o);
+      f = t < f ? t : f;
+    }
+    if (lane == 0) sm[warp] = f;
+    __syncthreads();
+    if (tid == 0) {
+      unsigned long long b = sm[0];
+      for (int w = 1; w < 32; ++w) b = sm[w] < b ? sm[w] : b;
+      s_pick = int(b < static_cast<unsigned long long>(n) ? b : 0ull);
+    }
+    __syncthreads();
+    pick = s_pick;
+  } else {
+    auto weight = [&](float v) -> unsigned long long {
+      if (!(v >= -3.0e38f)) return 0ull;  // NaN and -inf weigh nothing
+      return __float2ull_rn(expf((v - M) / T) * 1099511627776.0f);  // 2^40
+    };
+    unsigned long long part = 0;
+    for (int64_t i = i0; i < i1; ++i) part += weight(z[i]);
+    unsigned long long Z;
+    block_excl_scan(part, sm, &Z);
+    const double tgt = ceil(double(P) * double(Z));
+    const unsigned long long target = tgt < 1.0 ? 1ull : (tgt > double(Z) ? Z : static_cast<unsigned long long>(tgt));
+
+    // radix select: the key tau of the last token the nucleus needs, and the
+    // weight of all keys above it
+    uint32_t prefix = 0, mask = 0;
+    unsigned long long above = 0;
+    for (int round = 0; round < 4; ++round) {
+      const int shift = 24 - 8 * round;
+      if (tid < 256) hist[tid] = 0ull;
+      __syncthreads();
+      for (int64_t i = i0; i < i1; ++i) {
+        const uint32_t k = logit_key(z[i]);
+        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], weight(z[i]));
+      }
+      __syncthreads();
+      if (tid == 0) {
+        unsigned long long cum = above;
+        int d = 255;
+        for (; d > 0; --d) {
+          if (cum + hist[d] >= target) break;
+          cum += hist[d];
+        }
+        s_above = cum;
+        s_prefix = prefix | (uint32_t(d) << shift);
+      }
+      __syncthreads();
+      above = s_above;
+      prefix = s_prefix;
+      mask |= 0xFFu << shift;
+      __syncthreads();
+    }
+    const uint32_t tau = prefix;
+    // the weight of one token at the threshold key, and how many of those ties the nucleus takes
+    float tv = 0.f;
+    {
+      const uint32_t b = (tau & 0x80000000u) ? (tau & 0x7FFFFFFFu) : ~tau;
+      tv = __uint_as_float(b);
+    }
+    const unsigned long long wt = weight(tv);
+    const unsigned long long need = target - above;
+    const unsigned long long j = wt ? (need + wt - 1) / wt : 0ull;
+    const unsigned long long Mn = above + j * wt;
+    const double u = double(splitmix64(seed ^ (counter << 1)) >> 40) * 0x1.0p-24;
+    const unsigned long long r = static_cast<unsigned long long>(u * double(Mn));
+
+    // tie ranks in index order, then the nucleus weight of each thread's range
+    unsigned long long ties = 0;
+    for (int64_t i = i0; i < i1; ++i) ties += logit_key(z[i]) == tau;
+    unsigned long long tmp;
+    const unsigned long long tie0 = block_excl_scan(ties, sm, &tmp);
+    unsigned long long mass = 0, seen = tie0;
+    for (int64_t i = i0; i < i1; ++i) {
+      const uint32_t k = logit_key(z[i]);
+      const bool in = k > tau || (k == tau && seen < j);
+      seen += k == tau;
+      if (in) mass += weight(z[i]);
+    }
+    const unsigned long long base = block_excl_scan(mass, sm, &tmp);
+    if (tid == 0) s_pick = -1;
+    __syncthreads();
+    if (mass && base <= r && r < base + mass) {
+      unsigned long long acc = base;
+      seen = tie0;
+      for (int64_t i = i0; i < i1; ++i) {
+        const uint32_t k = logit_key(z[i]);
+        const bool in = k > tau || (k == tau && seen < j);
+        seen += k == tau;
+        if (!in) continue;
+        acc += weight(z[i]);
+        if (acc > r) {
+          s_pick = int(i);
+          break;
+        }
+      }
+    }
+    __syncthreads();
+    pick = s_pick;
+  }
+  if (tid == 0) {
+    const int32_t t = pick < 0 ? 0 : int32_t(pick);
+    if (out) *out = t;
+    if (tok_state) *tok_state = t;
+    if (pos_state) *pos_state += 1;
+  }
+}
+
 // ---- cosine similarity --------------------------------------------------------------
 __global__ void __launch_bounds__(1024) cos_kernel(const float* x, const float* y, int64_t n, float* out) {
   pdl_wait();
@@ -629,6 +833,14 @@ nt_status launch_argmax(Ctx* c, const float* v, int64_t n, int32_t* out, unsigne
   return cuda_check(c, launch_k(c, argmax_kernel, dim3(int(blocks)), dim3(1024), 0, st, v, n, key, counter, out,
                                 tok_state, pos_state),
                     "argmax launch");
+}
+
+nt_status launch_sample(Ctx* c, const float* z, int64_t n, float T, float P, uint64_t seed, const int64_t* ctr_dev,
+                        int64_t ctr, int32_t* out, cudaStream_t st, int32_t* tok_state, int64_t* pos_state) {
+  if (c->dry) return NT_OK;
+  return cuda_check(c, launch_k(c, sample_kernel, dim3(1), dim3(kSampThreads), 0, st, z, n, T, P, seed, ctr_dev, ctr, out,
+                                tok_state, pos_state),
+                    "sample launch");
 }
 
 nt_status launch_cos(Ctx* c, const float* a, const float* b, int64_t n, float* out, cudaStream_t st) {

@@ -97,6 +97,10 @@ class DeviceModel:
         nt.nt_decode_step(self.ctx, self.handle, token, pos, skip, self.logits, self.next_token, stream)
         return self.logits
 
+    def set_sampler(self, temperature: float, top_p: float = 1.0, seed: int = 0):
+        """Later decode steps sample (temperature, top-p); temperature <= 0 is greedy."""
+        nt.nt_model_set_sampler(self.ctx, self.handle, temperature, top_p, seed)
+
     def prefill(self, tokens, pos0: int, stream=None):
         """Run a prompt through the model (KV written for pos0 ..); returns the
         logits after its last token.  Decoding continues with step(-1, 0)."""

@@ -99,6 +99,8 @@ class nt_residency_plan(ctypes.Structure):
 
 
 _sig("nt_plan_residency", [ctypes.POINTER(nt_model_desc), _sz, _ci, ctypes.POINTER(nt_residency_plan)])
+_sig("nt_sample", [_vp, _vp, _i64, _cf, _cf, ctypes.c_uint64, ctypes.c_uint64, _vp, _vp])
+_sig("nt_model_set_sampler", [_vp, _vp, _cf, _cf, ctypes.c_uint64])
 _sig("nt_prefill", [_vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp])
 _sig("nt_spec_step", [_vp, _vp, ctypes.c_int32, _i64, _ci, _ci, _vp, _vp, _vp, _vp])
 _sig("nt_gemm_q", [_vp, _ci, _vp, _vp, _vp, _i64, _i64, _ci, _vp, _vp, _cf, _vp])
@@ -111,7 +113,7 @@ EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "
             "nt_rope_kv_append", "nt_attn_decode", "nt_softmax", "nt_swiglu", "nt_argmax", "nt_cos_sim",
             "nt_model_init", "nt_model_destroy", "nt_decode_step", "nt_layer_skip_calibrate",
             "nt_attn_decode_static", "nt_layer_blob_layout", "nt_stream_layer", "nt_model_slot", "nt_spec_step",
-            "nt_gemm_q", "nt_attn_verify", "nt_plan_residency", "nt_prefill"]
+            "nt_gemm_q", "nt_attn_verify", "nt_plan_residency", "nt_prefill", "nt_sample", "nt_model_set_sampler"]
 
 
 def lib():
@@ -256,6 +258,15 @@ def nt_gemm_q(ctx, fmt, W, X, Y, rows, cols, M, residual=None, norm_g=None, eps=
 def nt_attn_verify(ctx, q, kcache, vcache, out, n_qh, n_kvh, head_dim, n_pos0, n_query, kv_stride, stream=None):
     return ctx.check(_lib.nt_attn_verify(ctx.handle, _ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), n_qh, n_kvh,
                                          head_dim, n_pos0, n_query, kv_stride, _stream(stream, out)))
+
+
+def nt_sample(ctx, logits, n: int, temperature: float, top_p: float, seed: int, counter: int, out, stream=None):
+    return ctx.check(_lib.nt_sample(ctx.handle, _ptr(logits), n, temperature, top_p, seed, counter, _ptr(out),
+                                    _stream(stream, out)))
+
+
+def nt_model_set_sampler(ctx, model: int, temperature: float, top_p: float, seed: int):
+    return ctx.check(_lib.nt_model_set_sampler(ctx.handle, model, temperature, top_p, seed))
 
 
 def nt_prefill(ctx, model: int, tokens, pos0: int, logits, next_token=None, stream=None):

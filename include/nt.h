@@ -190,6 +190,19 @@ nt_status nt_gemm_q(nt_ctx* ctx, int fmt, const void* W_dev, const float* X_dev,
  * index on ties (NaN never wins), written as int32 to out_dev. */
 nt_status nt_argmax(nt_ctx* ctx, const float* v_dev, int64_t n, int32_t* out_dev, void* stream);
 
+/* Non-greedy sampler [code] inference/ (sampler): temperature and nucleus
+ * (top-p) sampling of logits_dev[0..n) into *out_dev.  Definition:
+ * w_i = rint(exp((z_i - max z) / temperature) * 2^40) (integer weights);
+ * the nucleus is the shortest prefix of the tokens ordered by logit
+ * (descending, ties by lower index) whose weight reaches
+ * ceil(top_p * sum w); with u = (splitmix64(seed ^ (counter << 1)) >> 40) *
+ * 2^-24 (SplitMix64 output function: Steele, Lea & Flood 2014) and
+ * r = floor(u * nucleus weight), the pick is the nucleus token, in index
+ * order, whose cumulative weight first exceeds r.  temperature <= 0 is
+ * greedy (nt_argmax).  top_p in (0, 1]. */
+nt_status nt_sample(nt_ctx* ctx, const float* logits_dev, int64_t n, float temperature, float top_p, uint64_t seed,
+                    uint64_t counter, int32_t* out_dev, void* stream);
+
 /* Cosine similarity [cache] of a and b: <a,b> / (|a| |b|), fp32 result. */
 nt_status nt_cos_sim(nt_ctx* ctx, const float* a_dev, const float* b_dev, int64_t n, float* out_dev,
                      void* stream);
@@ -259,6 +272,13 @@ nt_status nt_model_destroy(nt_ctx* ctx, nt_model* model);
  * copy (double buffering with 2 slots).  Skipped layers are not copied. */
 nt_status nt_decode_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos, const uint8_t* skip_mask_host,
                          float* logits_dev, int32_t* next_token_dev, void* stream);
+
+/* Sampling for the model's decode steps (nt_decode_step, nt_prefill's next
+ * token stays greedy): every later step draws its next token with nt_sample's
+ * definition, counter = the position of the step's input token, so a
+ * sequence is reproducible from (seed, start).  temperature <= 0 restores
+ * greedy decoding.  nt_spec_step always decodes greedily. */
+nt_status nt_model_set_sampler(nt_ctx* ctx, nt_model* model, float temperature, float top_p, uint64_t seed);
 
 /* Layer-skip calibration [cache]: one full decode step (all layers) at
  * (token, pos) that also measures cos(x before layer l, x after layer l) for

@@ -90,6 +90,13 @@ def lib():
         L.or_layer_skip_select.argtypes = [vp, ci, ci, vp]
         L.or_decode_step.argtypes = [ctypes.POINTER(_Model), ctypes.c_int32, i64, vp, vp, vp]
         L.or_set_num_threads.argtypes = [ci]
+        L.or_splitmix64.argtypes = [ctypes.c_uint64]
+        L.or_splitmix64.restype = ctypes.c_uint64
+        L.or_sample_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+        L.or_sample_uniform.restype = ctypes.c_double
+        L.or_sample.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                ctypes.POINTER(ctypes.c_int64)]
+        L.or_sample.restype = ctypes.c_int64
         _lib = L
     return _lib
 
@@ -198,6 +205,24 @@ def swiglu(gate, up) -> np.ndarray:
 def argmax(v) -> int:
     v, vp_ = _c(v, np.float64)
     return int(lib().or_argmax(vp_, v.size))
+
+
+def splitmix64(z: int) -> int:
+    return int(lib().or_splitmix64(ctypes.c_uint64(z & 0xFFFFFFFFFFFFFFFF)))
+
+
+def sample_uniform(seed: int, counter: int) -> float:
+    return float(lib().or_sample_uniform(ctypes.c_uint64(seed), ctypes.c_uint64(counter)))
+
+
+def sample(logits, temperature: float, top_p: float, u: float):
+    """Nucleus sample of fp32 logits with uniform u; returns (token, nucleus size)."""
+    z = np.ascontiguousarray(np.asarray(logits, dtype=np.float32))
+    k = ctypes.c_int64(0)
+    t = int(lib().or_sample(z.ctypes.data, z.size, float(temperature), float(top_p), float(u), ctypes.byref(k)))
+    if t < 0:
+        raise RuntimeError("or_sample failed")
+    return t, int(k.value)
 
 
 def cos_sim(a, b) -> float:

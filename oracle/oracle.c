@@ -310,6 +310,85 @@ int64_t or_argmax(const double* v, int64_t n) {
   return best;
 }
 
+/* ---- non-greedy sampler ([P-code] inference/: sampler) --------------------
+ * Reading: temperature softmax followed by nucleus (top-p) truncation, the
+ * usual non-greedy decoding of a Llama engine.  Written out as the plain
+ * definition:
+ *   w_i   = rint(exp((z_i - max z) / T) * 2^40)   (token weights, integers)
+ *   order = tokens by logit descending, ties by lower index
+ *   N     = the shortest prefix of that order whose weight sum reaches
+ *           target = ceil(top_p * sum_i w_i)
+ *   pick  = with r = floor(u * sum_{N} w), the token of N, taken in index
+ *           order, whose cumulative weight first exceeds r.
+ * T <= 0 is greedy (argmax, lowest index).  Integer weights make every sum
+ * exact and independent of the order of addition. */
+
+/* SplitMix64 output function (Steele, Lea & Flood, OOPSLA 2014): the state
+ * advanced by the golden-ratio increment, then two xor-shift-multiply steps. */
+uint64_t or_splitmix64(uint64_t z) {
+  z += 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+/* the sampler's uniform for (seed, counter): the top 24 bits of
+ * splitmix64(seed xor 2 counter), as a multiple of 2^-24 in [0, 1) */
+double or_sample_uniform(uint64_t seed, uint64_t counter) {
+  return (double)(or_splitmix64(seed ^ (counter << 1)) >> 40) * 0x1.0p-24;
+}
+
+static const float* g_sort_z;  /* comparison context of the sort below */
+static int cmp_desc(const void* a, const void* b) {
+  int64_t i = *(const int64_t*)a, j = *(const int64_t*)b;
+  float zi = g_sort_z[i], zj = g_sort_z[j];
+  if (zi > zj) return -1;
+  if (zi < zj) return 1;
+  return (i > j) - (i < j);
+}
+
+int64_t or_sample(const float* z, int64_t n, double temperature, double top_p, double u, int64_t* nucleus_out) {
+  if (n <= 0) return -1;
+  if (temperature <= 0.0) {
+    int64_t best = 0;
+    for (int64_t i = 1; i < n; ++i)
+      if (z[i] > z[best]) best = i;
+    if (nucleus_out) *nucleus_out = 1;
+    return best;
+  }
+  double mx = z[0];
+  for (int64_t i = 1; i < n; ++i)
+    if (z[i] > mx) mx = z[i];
+  uint64_t* w = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)n);
+  int64_t* idx = (int64_t*)malloc(sizeof(int64_t) * (size_t)n);
+  uint8_t* in = (uint8_t*)calloc((size_t)n, 1);
+  if (!w || !idx || !in) { free(w); free(idx); free(in); return -2; }
+  uint64_t Z = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    w[i] = (uint64_t)nearbyint(exp(((double)z[i] - mx) / temperature) * 0x1.0p40);
+    Z += w[i];
+    idx[i] = i;
+  }
+  double t = ceil(top_p * (double)Z);
+  uint64_t target = t < 1.0 ? 1 : (t > (double)Z ? Z : (uint64_t)t);
+  g_sort_z = z;
+  qsort(idx, (size_t)n, sizeof(int64_t), cmp_desc);
+  uint64_t M = 0;
+  int64_t k = 0;
+  while (k < n && M < target) { M += w[idx[k]]; in[idx[k]] = 1; ++k; }
+  uint64_t r = (uint64_t)floor(u * (double)M);
+  uint64_t acc = 0;
+  int64_t pick = -1;
+  for (int64_t i = 0; i < n; ++i) {
+    if (!in[i]) continue;
+    acc += w[i];
+    if (acc > r) { pick = i; break; }
+  }
+  if (nucleus_out) *nucleus_out = k;
+  free(w); free(idx); free(in);
+  return pick;
+}
+
 /* cosine similarity <a,b> / (|a| |b|)   ([P-cache] layer skip) */
 double or_cos_sim(const double* a, const double* b, int64_t n) {
   double ab = 0.0, aa = 0.0, bb = 0.0;

@@ -1,0 +1,124 @@
+"""The non-greedy sampler (temperature + nucleus; inference/ sampler of
+"ntransformer - moteur d'inférence NVMe-to-GPU…", "Architecture et structure
+du code") on the GPU vs the oracle's plain definition, standalone and inside
+the decode step.
+
+The GPU computes the token weights with fp32 exp, the oracle with fp64 exp,
+so when u lands within rounding of a boundary of the cumulative weights the
+two may pick neighbouring tokens.  The bar: the GPU's token equals the
+oracle's for almost every draw, and always equals the oracle's pick for u
+moved by at most 1e-6 (a valid sample)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import dev, host, need_gpu, torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    need_gpu()
+    from block_quantized_gemv_nt_gb300 import nt
+    c = nt.Context(0)
+    yield c
+    c.sync()
+    c.close()
+
+
+def _valid(z, T, P, u, tok, delta):
+    return tok in {oracle.sample(z, T, P, min(max(u + d, 0.0), 1 - 2**-24))[0] for d in (-delta, 0.0, delta)}
+
+
+@pytest.mark.parametrize("n", [7, 1000, 32000, 128256])
+def test_sample_matches_oracle(ctx, n):
+    from block_quantized_gemv_nt_gb300 import nt
+    z = synth.normal_f32(n, seed=3, stream=n % 1000) * 3.0
+    zd = dev(z)
+    out = torch.zeros(1, dtype=torch.int32, device="cuda")
+    exact, trials = 0, 0
+    for T, P in [(1.0, 0.9), (0.7, 0.5), (1.5, 1.0), (0.3, 0.95)]:
+        for counter in range(6):
+            seed = 1000 + counter
+            nt.nt_sample(ctx, zd, n, T, P, seed, counter, out)
+            tok = int(out.item())
+            u = oracle.sample_uniform(seed, counter)
+            ref, _ = oracle.sample(z, T, P, u)
+            exact += tok == ref
+            trials += 1
+            assert _valid(z, T, P, u, tok, 1e-6), (T, P, counter, tok, ref)
+    assert exact >= trials - 1
+
+
+def test_sample_greedy_and_ties(ctx):
+    from block_quantized_gemv_nt_gb300 import nt
+    out = torch.zeros(1, dtype=torch.int32, device="cuda")
+    z = synth.normal_f32(5000, seed=4, stream=1)
+    nt.nt_sample(ctx, dev(z), 5000, 0.0, 0.9, 7, 0, out)
+    assert int(out.item()) == int(np.argmax(z))
+    ties = np.ones(8, dtype=np.float32)
+    for counter in range(20):
+        nt.nt_sample(ctx, dev(ties), 8, 1.0, 0.5, 11, counter, out)
+        u = oracle.sample_uniform(11, counter)
+        assert int(out.item()) == oracle.sample(ties, 1.0, 0.5, u)[0] == (0 if u < 0.25 else 1 if u < 0.5 else
+                                                                          2 if u < 0.75 else 3)
+
+
+def test_sample_frequencies(ctx):
+    """Many counters: the GPU's picks follow the renormalised nucleus."""
+    from block_quantized_gemv_nt_gb300 import nt
+    z = np.array([1.5, 0.2, -0.4, 0.9, -2.0, 0.0], dtype=np.float32)
+    zd = dev(z)
+    T, P, n = 0.8, 0.85, 3000
+    outs = torch.zeros(n, dtype=torch.int32, device="cuda")
+    for c in range(n):
+        nt.nt_sample(ctx, zd, 6, T, P, 5, c, outs[c:])
+    got = np.bincount(host(outs), minlength=6)
+    p = np.exp((z - z.max()) / T)
+    p /= p.sum()
+    order = np.argsort(-z, kind="stable")
+    keep = order[:np.searchsorted(np.cumsum(p[order]), P) + 1]
+    q = np.zeros(6)
+    q[keep] = p[keep] / p[keep].sum()
+    assert np.all(got[q == 0] == 0)
+    chi2 = np.sum((got[q > 0] - n * q[q > 0]) ** 2 / (n * q[q > 0]))
+    assert chi2 < 20.0
+
+
+def test_sample_bad_args(ctx):
+    from block_quantized_gemv_nt_gb300 import nt
+    z = torch.zeros(10, device="cuda")
+    out = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for n, T, P in [(0, 1.0, 0.9), (10, 1.0, 0.0), (10, 1.0, 1.5), (10, float("nan"), 0.9)]:
+        with pytest.raises(nt.NtError) as ei:
+            nt.nt_sample(ctx, z, n, T, P, 0, 0, out)
+        assert ei.value.status == nt.NT_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["tiny_q8_0", "small_q4_k_m"])
+def test_decode_with_sampler(ctx, name):
+    """Sampled decoding (T = 0.8, top-p 0.9) continued on the device: each
+    token is a valid draw from the oracle's distribution at that step
+    (teacher-forced), with u from (seed, position)."""
+    from block_quantized_gemv_nt_gb300 import engine
+    spec = synth.model_spec(name)
+    hm = synth.make_host_model(spec)
+    om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
+    gm = engine.DeviceModel(ctx, spec, hm)
+    T, P, seed = 0.8, 0.9, 2024
+    gm.set_sampler(T, P, seed)
+    tok, pos = spec.first_token, spec.n_prefill
+    for step in range(6):
+        lg = gm.step(tok if step == 0 else -1, pos).cpu().numpy()
+        g = int(gm.next_token.item())
+        ref_logits = om.step(tok, pos)
+        u = oracle.sample_uniform(seed, pos)
+        # the GPU's own logits give the same pick as the oracle's definition...
+        assert _valid(lg, T, P, u, g, 1e-6)
+        # ...and the oracle's logits agree up to the logit tolerance's effect on the cumulative weights
+        assert _valid(ref_logits.astype(np.float32), T, P, u, g, 1e-3)
+        tok, pos = g, pos + 1
+    gm.set_sampler(0.0)
+    gm.close()
