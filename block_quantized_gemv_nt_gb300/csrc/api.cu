@@ -359,6 +359,27 @@ nt_status nt_sample(nt_ctx* ctx, const float* z, int64_t n, float T, float P, ui
   return launch_sample(ctx, z, n, T, P, seed, nullptr, int64_t(counter), out, as_stream(stream));
 }
 
+nt_status nt_host_register(nt_ctx* ctx, const void* p, size_t bytes, int read_only) {
+  NT_TRY(pre_call(ctx));
+  NT_REQUIRE(p && bytes, NT_ERR_INVALID_ARG, "null pointer or zero bytes");
+  NT_REQUIRE(aligned(p, 4096) && bytes % 4096 == 0, NT_ERR_ALIGNMENT, "pointer and size must be multiples of 4096");
+  DeviceGuard g(ctx->device);
+  unsigned flags = cudaHostRegisterPortable | cudaHostRegisterMapped;
+  if (read_only) flags |= cudaHostRegisterReadOnly;
+  const cudaError_t e = cudaHostRegister(const_cast<void*>(p), bytes, flags);
+  if (e != cudaSuccess) cudaGetLastError();  // a refused registration leaves no error behind for later calls
+  return cuda_check(ctx, e, "host register");
+}
+
+nt_status nt_host_unregister(nt_ctx* ctx, const void* p) {
+  NT_TRY(pre_call(ctx));
+  NT_REQUIRE(p, NT_ERR_INVALID_ARG, "null pointer");
+  DeviceGuard g(ctx->device);
+  const cudaError_t e = cudaHostUnregister(const_cast<void*>(p));
+  if (e != cudaSuccess) cudaGetLastError();
+  return cuda_check(ctx, e, "host unregister");
+}
+
 nt_status nt_cos_sim(nt_ctx* ctx, const float* a, const float* b, int64_t n, float* out, void* stream) {
   NT_TRY(pre_call(ctx));
   NT_REQUIRE(a && b && out && n > 0, NT_ERR_INVALID_ARG, "null pointer or n <= 0");

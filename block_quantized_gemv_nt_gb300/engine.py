@@ -11,6 +11,11 @@ from . import nt
 LAYER = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
 
 
+def _h(a) -> torch.Tensor:
+    """A host array as a tensor (read-only views, e.g. of a mapped file, are copied)."""
+    return torch.from_numpy(a if a.flags.writeable else np.array(a))
+
+
 def model_desc(spec, stream_slots: int = 0) -> nt.nt_model_desc:
     f = spec.fmt
     return nt.nt_model_desc(spec.n_layers, spec.d_model, spec.n_qh, spec.n_kvh, spec.head_dim, spec.ffn, spec.vocab,
@@ -67,19 +72,19 @@ class DeviceModel:
         self.layers = []
         for i, L in enumerate(hm.layers):
             if blobs is not None and i in blobs.blob:
-                d = {n: torch.from_numpy(L[n]).to(dev) for n in ("attn_norm", "ffn_norm")}
+                d = {n: _h(L[n]).to(dev) for n in ("attn_norm", "ffn_norm")}
                 d["host_blob"] = blobs.blob[i]
             else:
-                d = {n: torch.from_numpy(L[n]).to(dev) for n in LAYER + ("attn_norm", "ffn_norm")}
+                d = {n: _h(L[n]).to(dev) for n in LAYER + ("attn_norm", "ffn_norm")}
             d["kcache"] = torch.from_numpy(np.ascontiguousarray(hm.kcache[i])).to(dev)
             d["vcache"] = torch.from_numpy(np.ascontiguousarray(hm.vcache[i])).to(dev)
             self.layers.append(d)
         if blobs is not None and blobs.embd is not None:
             self.embd = blobs.embd
         else:
-            self.embd = torch.from_numpy(hm.embd).to(dev)
-        self.out = torch.from_numpy(hm.out).to(dev)
-        self.out_norm = torch.from_numpy(hm.out_norm).to(dev)
+            self.embd = _h(hm.embd).to(dev)
+        self.out = _h(hm.out).to(dev)
+        self.out_norm = _h(hm.out_norm).to(dev)
         self.logits = torch.empty(spec.vocab, dtype=torch.float32, device=dev)
         self.next_token = torch.zeros(1, dtype=torch.int32, device=dev)
         self.handle = nt.nt_model_init(ctx, model_desc(spec, stream_slots), self.layers, self.embd, self.out,
@@ -89,7 +94,7 @@ class DeviceModel:
         """Weight bytes this model keeps in HBM: resident layers, LM head,
         embedding table when resident, streaming slots."""
         n = sum(t.numel() for L in self.layers for k, t in L.items() if k in LAYER)
-        n += self.out.numel() + (self.embd.numel() if self.embd.is_cuda else 0)
+        n += self.out.numel() + (self.embd.numel() if isinstance(self.embd, torch.Tensor) and self.embd.is_cuda else 0)
         return n + self.n_slots * (self.blobs.nbytes if self.blobs is not None else 0)
 
     def step(self, token: int, pos: int, skip=None, stream=None):

@@ -1,0 +1,215 @@
+"""Model files: the host-file tier of the 3-tier cache ("Ntransformer"
+(en.unwiki.net), About: VRAM-resident layers, pinned RAM, NVMe/mmap
+fallback; the "mmap pinned" data path).
+
+A GGUF-style single-file container of a model's weights, laid out so that a
+streamed layer is one contiguous, page-aligned range of the file:
+
+    offset 0   b"NTQF", u32 version (1), u64 header length H
+    offset 16  H bytes of UTF-8 JSON: the model description, the blob layout
+               and every entry's (offset, bytes)
+    data       entries at 4096-byte-aligned offsets: "embd", "out",
+               "out_norm", and per layer l: "blob.l" (its seven weight
+               matrices in the library's blob layout, nt_layer_blob_layout),
+               "attn_norm.l", "ffn_norm.l"
+
+``ModelFile`` maps the file read-only.  Resident layers are uploaded from
+the mapping; the streamed layers' blobs (and the embedding table) stay in the
+mapping, page-locked with nt_host_register ("mmap pinned"), so the streaming
+engine copies them to HBM exactly as it copies pinned RAM.  Where the
+operating system refuses to page-lock file-backed memory, ``FileBlobs`` falls
+back to one CPU copy of those ranges into page-locked buffers ("CPU memcpy").
+The KV cache is runtime state, not part of the file.
+"""
+from __future__ import annotations
+
+import json
+import mmap
+import os
+import struct
+from dataclasses import asdict
+
+import numpy as np
+
+from . import nt
+
+MAGIC = b"NTQF"
+VERSION = 1
+ALIGN = 4096
+LAYER = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
+
+
+def _up(n: int, a: int = ALIGN) -> int:
+    return (n + a - 1) // a * a
+
+
+def _row_bytes(fmt: int, cols: int) -> int:
+    return cols // nt.nt_block_elems(fmt) * nt.nt_block_bytes(fmt)
+
+
+class FileSpec:
+    """The model description stored in a file: the fields of the spec it was
+    written from, with the shape helpers the engine uses."""
+
+    def __init__(self, fields: dict):
+        self.__dict__.update(fields)
+        self.fmt = {k: int(v) for k, v in self.fmt.items()}
+
+    def tensor_shape(self, name: str):
+        d, hd = self.d_model, self.head_dim
+        return {"wq": (self.n_qh * hd, d), "wk": (self.n_kvh * hd, d), "wv": (self.n_kvh * hd, d),
+                "wo": (d, self.n_qh * hd), "wg": (self.ffn, d), "wu": (self.ffn, d), "wd": (d, self.ffn),
+                "embd": (self.vocab, d), "out": (self.vocab, d)}[name]
+
+    @property
+    def kv_cap(self) -> int:
+        return self.n_prefill + self.n_gen + 8
+
+    def layer_bytes(self) -> int:
+        return sum(self.tensor_shape(t)[0] * _row_bytes(self.fmt[t], self.tensor_shape(t)[1]) for t in LAYER)
+
+
+def write_model(path: str, spec, hm) -> None:
+    """Write host model `hm` (synth.HostModel layout) of `spec` to `path`."""
+    from .engine import model_desc
+    offsets, blob_bytes = nt.nt_layer_blob_layout(model_desc(spec))
+    entries = {}
+    pieces = []  # (name, offset, writer)
+    pos = 0
+
+    def add(name, nbytes, fill):
+        nonlocal pos
+        entries[name] = [pos, int(nbytes)]
+        pieces.append((pos, fill))
+        pos = _up(pos + int(nbytes))
+
+    add("embd", hm.embd.nbytes, lambda f: f.write(hm.embd.tobytes()))
+    add("out", hm.out.nbytes, lambda f: f.write(hm.out.tobytes()))
+    add("out_norm", hm.out_norm.nbytes, lambda f: f.write(hm.out_norm.tobytes()))
+    for li, L in enumerate(hm.layers):
+        def blob_writer(f, L=L):
+            start = f.tell()
+            for i, name in enumerate(LAYER):
+                f.seek(start + offsets[i])
+                f.write(np.ascontiguousarray(L[name]).tobytes())
+        add(f"blob.{li}", blob_bytes, blob_writer)
+        add(f"attn_norm.{li}", L["attn_norm"].nbytes, lambda f, L=L: f.write(L["attn_norm"].tobytes()))
+        add(f"ffn_norm.{li}", L["ffn_norm"].nbytes, lambda f, L=L: f.write(L["ffn_norm"].tobytes()))
+    fields = asdict(spec) if hasattr(spec, "__dataclass_fields__") else dict(vars(spec))
+    header = json.dumps({"spec": fields, "blob_offsets": list(offsets), "blob_bytes": blob_bytes,
+                         "entries": entries}).encode()
+    data0 = _up(16 + len(header))
+    with open(path, "wb") as f:
+        f.write(MAGIC + struct.pack("<IQ", VERSION, len(header)) + header)
+        for off, fill in pieces:
+            f.seek(data0 + off)
+            fill(f)
+        f.truncate(data0 + pos)
+
+
+class ModelFile:
+    """A model file mapped read-only: ``spec``, and numpy views of every entry
+    (``layers`` as synth.HostModel lays them out, ``embd``, ``out``,
+    ``out_norm``)."""
+
+    def __init__(self, path: str):
+        self.path = path
+        self._fd = os.open(path, os.O_RDONLY)
+        size = os.fstat(self._fd).st_size
+        self._mm = mmap.mmap(self._fd, size, prot=mmap.PROT_READ)
+        buf = np.frombuffer(self._mm, dtype=np.uint8)
+        if bytes(buf[:4]) != MAGIC:
+            raise ValueError(f"{path}: not a model file")
+        version, hlen = struct.unpack("<IQ", bytes(buf[4:16]))
+        if version != VERSION:
+            raise ValueError(f"{path}: version {version}")
+        meta = json.loads(bytes(buf[16:16 + hlen]).decode())
+        self.spec = FileSpec(meta["spec"])
+        self.blob_offsets, self.blob_bytes = meta["blob_offsets"], meta["blob_bytes"]
+        self.data0 = _up(16 + hlen)
+        self._buf = buf
+        self.entries = {k: (self.data0 + v[0], v[1]) for k, v in meta["entries"].items()}
+        s = self.spec
+
+        def view(name, dtype=np.uint8, shape=None):
+            off, n = self.entries[name]
+            a = buf[off:off + n].view(dtype)
+            return a.reshape(shape) if shape is not None else a
+
+        def mat_shape(name):
+            r, c = s.tensor_shape(name)
+            return r, _row_bytes(s.fmt[name], c)
+
+        self.embd = view("embd", shape=mat_shape("embd"))
+        self.out = view("out", shape=mat_shape("out"))
+        self.out_norm = view("out_norm", np.float32)
+        self.layers = []
+        for li in range(s.n_layers):
+            off, _ = self.entries[f"blob.{li}"]
+            d = {}
+            for i, name in enumerate(LAYER):
+                r, rb = mat_shape(name)
+                o = off + self.blob_offsets[i]
+                d[name] = buf[o:o + r * rb].reshape(r, rb)
+            d["attn_norm"] = view(f"attn_norm.{li}", np.float32)
+            d["ffn_norm"] = view(f"ffn_norm.{li}", np.float32)
+            self.layers.append(d)
+
+    def address(self, name: str) -> int:
+        return self._buf.ctypes.data + self.entries[name][0]
+
+    def close(self):
+        self.embd = self.out = self.out_norm = None
+        self.layers = []
+        self._buf = None
+        try:
+            self._mm.close()
+        except BufferError:
+            pass  # views still alive elsewhere: the mapping closes with them
+        os.close(self._fd)
+
+
+class FileBlobs:
+    """The streamed layers of a mapped model file, page-locked in place: the
+    same interface as engine.HostBlobs (``blob`` maps a layer to its host
+    address, ``embd`` is the embedding table's), so DeviceModel streams from
+    the file mapping."""
+
+    def __init__(self, ctx: nt.Context, mf: ModelFile, n_resident: int, allow_copy: bool = True):
+        self.ctx, self.mf = ctx, mf
+        s = mf.spec
+        self.layers = list(range(n_resident, s.n_layers))
+        self.offsets, self.nbytes = mf.blob_offsets, mf.blob_bytes
+        self._regs = []
+        self._copies = []
+        self.tier = "mmap pinned"
+        self.blob = {}
+        for li in self.layers:
+            self.blob[li] = self._lock(f"blob.{li}", allow_copy)
+        self.embd = self._lock("embd", allow_copy) if self.layers else None
+
+    def _lock(self, name: str, allow_copy: bool) -> int:
+        addr = self.mf.address(name)
+        nbytes = _up(self.mf.entries[name][1])
+        try:
+            nt.nt_host_register(self.ctx, addr, nbytes, read_only=True)
+            self._regs.append(addr)
+            return addr
+        except nt.NtError:
+            if not allow_copy:
+                raise
+        # the pages of this file cannot be locked in place: one CPU copy into page-locked memory
+        import torch
+        self.tier = "CPU memcpy"
+        off = self.mf.entries[name][0]
+        buf = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+        n = self.mf.entries[name][1]
+        buf[:n].numpy()[:] = self.mf._buf[off:off + n]
+        self._copies.append(buf)
+        return buf.data_ptr()
+
+    def close(self):
+        for addr in self._regs:
+            nt.nt_host_unregister(self.ctx, addr)
+        self._regs = []
+        self._copies = []

@@ -99,6 +99,8 @@ class nt_residency_plan(ctypes.Structure):
 
 
 _sig("nt_plan_residency", [ctypes.POINTER(nt_model_desc), _sz, _ci, ctypes.POINTER(nt_residency_plan)])
+_sig("nt_host_register", [_vp, _vp, _sz, _ci])
+_sig("nt_host_unregister", [_vp, _vp])
 _sig("nt_sample", [_vp, _vp, _i64, _cf, _cf, ctypes.c_uint64, ctypes.c_uint64, _vp, _vp])
 _sig("nt_model_set_sampler", [_vp, _vp, _cf, _cf, ctypes.c_uint64])
 _sig("nt_prefill", [_vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp])
@@ -113,7 +115,8 @@ EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "
             "nt_rope_kv_append", "nt_attn_decode", "nt_softmax", "nt_swiglu", "nt_argmax", "nt_cos_sim",
             "nt_model_init", "nt_model_destroy", "nt_decode_step", "nt_layer_skip_calibrate",
             "nt_attn_decode_static", "nt_layer_blob_layout", "nt_stream_layer", "nt_model_slot", "nt_spec_step",
-            "nt_gemm_q", "nt_attn_verify", "nt_plan_residency", "nt_prefill", "nt_sample", "nt_model_set_sampler"]
+            "nt_gemm_q", "nt_attn_verify", "nt_plan_residency", "nt_prefill", "nt_sample", "nt_model_set_sampler",
+            "nt_host_register", "nt_host_unregister"]
 
 
 def lib():
@@ -258,6 +261,14 @@ def nt_gemm_q(ctx, fmt, W, X, Y, rows, cols, M, residual=None, norm_g=None, eps=
 def nt_attn_verify(ctx, q, kcache, vcache, out, n_qh, n_kvh, head_dim, n_pos0, n_query, kv_stride, stream=None):
     return ctx.check(_lib.nt_attn_verify(ctx.handle, _ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), n_qh, n_kvh,
                                          head_dim, n_pos0, n_query, kv_stride, _stream(stream, out)))
+
+
+def nt_host_register(ctx, host_ptr: int, nbytes: int, read_only: bool = True):
+    return ctx.check(_lib.nt_host_register(ctx.handle, host_ptr, nbytes, int(bool(read_only))))
+
+
+def nt_host_unregister(ctx, host_ptr: int):
+    return ctx.check(_lib.nt_host_unregister(ctx.handle, host_ptr))
 
 
 def nt_sample(ctx, logits, n: int, temperature: float, top_p: float, seed: int, counter: int, out, stream=None):

@@ -319,6 +319,16 @@ typedef struct {
 nt_status nt_plan_residency(const nt_model_desc* desc, size_t hbm_weight_budget, int embd_in_hbm,
                             nt_residency_plan* plan_out);
 
+/* Host-file tier [about] (3-tier adaptive caching: NVMe/mmap fallback;
+ * "mmap pinned" data path): page-lock bytes [host_ptr, host_ptr + bytes) of
+ * host memory — typically a read-only mmap of a model file — so streamed
+ * layers (nt_layer_ptrs.host_blob) and the embedding table can point into
+ * it and copy like pinned RAM.  host_ptr and bytes must be multiples of 4096;
+ * read_only != 0 registers read-only (what a PROT_READ mapping needs).
+ * nt_host_unregister releases it; the caller unregisters before unmapping. */
+nt_status nt_host_register(nt_ctx* ctx, const void* host_ptr, size_t bytes, int read_only);
+nt_status nt_host_unregister(nt_ctx* ctx, const void* host_ptr);
+
 /* Streaming-engine copy step [feat] (SLEP double buffering), [cache]
  * (pinned-RAM H2D tier): enqueue on copy_stream the host-to-HBM copy of one
  * layer blob of `bytes` (= the model's blob size) from page-locked

@@ -212,3 +212,34 @@ def test_planned_residency_decodes_like_resident(ctx):
         assert torch.equal(x, y)
     gs.close()
     gr.close()
+
+
+@pytest.mark.parametrize("where", ["tmp", "shm"])
+def test_model_file_streams_like_resident(ctx, tmp_path, where):
+    """The host-file tier: a model written to a file, mapped read-only, its
+    streamed layers page-locked in the mapping (or, where the OS refuses,
+    copied once into page-locked memory), decodes bit-identically to the
+    same model held resident."""
+    import os
+    from block_quantized_gemv_nt_gb300 import engine, modelfile
+    spec = synth.model_spec("small_q4_k_m_r1")
+    hm = synth.make_host_model(spec)
+    d = str(tmp_path) if where == "tmp" or not os.path.isdir("/dev/shm") else "/dev/shm"
+    path = os.path.join(d, f"nt_test_{os.getpid()}.ntq")
+    modelfile.write_model(path, spec, hm)
+    try:
+        mf = modelfile.ModelFile(path)
+        fb = modelfile.FileBlobs(ctx, mf, spec.n_resident)
+        print("tier:", fb.tier)
+        hf = synth.HostModel(mf.spec, mf.layers, mf.embd, mf.out, mf.out_norm, hm.kcache, hm.vcache)
+        gf = engine.DeviceModel(ctx, mf.spec, hf, blobs=fb)
+        base = synth.model_spec("small_q4_k_m")
+        gr = engine.DeviceModel(ctx, base, hm)
+        for x, y in zip(_greedy(gf, spec, 4), _greedy(gr, base, 4)):
+            assert torch.equal(x, y)
+        gf.close()
+        gr.close()
+        fb.close()
+        mf.close()
+    finally:
+        os.unlink(path)
