@@ -97,6 +97,14 @@ def lib():
         L.or_sample.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_double, ctypes.c_double, ctypes.c_double,
                                 ctypes.POINTER(ctypes.c_int64)]
         L.or_sample.restype = ctypes.c_int64
+        u64, u32 = ctypes.c_uint64, ctypes.c_uint32
+        L.or_sample_weights.argtypes = [vp, i64, cd, cd, vp]
+        L.or_sample_weights.restype = u64
+        L.or_spec_uniforms.argtypes = [u64, u64, ctypes.POINTER(u32), ctypes.POINTER(u32)]
+        L.or_spec_accept.argtypes = [u64, u64, u64, u64, u32]
+        L.or_spec_accept.restype = ci
+        L.or_spec_residual.argtypes = [vp, u64, vp, u64, i64, u32]
+        L.or_spec_residual.restype = i64
         _lib = L
     return _lib
 
@@ -223,6 +231,63 @@ def sample(logits, temperature: float, top_p: float, u: float):
     if t < 0:
         raise RuntimeError("or_sample failed")
     return t, int(k.value)
+
+
+def sample_weights(logits, temperature: float, top_p: float):
+    """The sampler's distribution as integer weights: (w uint64 [n], W) with
+    w[i] = token i's weight inside the nucleus, else 0, and W = sum w."""
+    z = np.ascontiguousarray(np.asarray(logits, dtype=np.float32))
+    w = np.zeros(z.size, dtype=np.uint64)
+    W = int(lib().or_sample_weights(z.ctypes.data, z.size, float(temperature), float(top_p), w.ctypes.data))
+    if W == 0:
+        raise RuntimeError("or_sample_weights failed")
+    return w, W
+
+
+def spec_uniforms(seed: int, counter: int) -> tuple[int, int]:
+    """The two 24-bit uniforms (k_acc, k_res) of speculative sampling at
+    (seed, counter)."""
+    a, r = ctypes.c_uint32(), ctypes.c_uint32()
+    lib().or_spec_uniforms(ctypes.c_uint64(seed), ctypes.c_uint64(counter), ctypes.byref(a), ctypes.byref(r))
+    return int(a.value), int(r.value)
+
+
+def spec_accept(wq_d: int, Wq: int, wp_d: int, Wp: int, k_acc: int) -> bool:
+    """Speculative sampling's acceptance test u < p(d) / q(d), u = k_acc / 2^24."""
+    return bool(lib().or_spec_accept(wq_d, Wq, wp_d, Wp, k_acc))
+
+
+def spec_residual(wp, Wp: int, wq, Wq: int, k_res: int) -> int:
+    """Token drawn from max(0, p - q) with uniform k_res / 2^24 (-1: empty)."""
+    wp = np.ascontiguousarray(wp, dtype=np.uint64)
+    wq = np.ascontiguousarray(wq, dtype=np.uint64)
+    return int(lib().or_spec_residual(wp.ctypes.data, Wp, wq.ctypes.data, Wq, wp.size, k_res))
+
+
+def spec_sample(draft_logits, verify_logits, temperature: float, top_p: float, seed: int, pos: int):
+    """Speculative sampling over one step, teacher-forced on given logits.
+
+    draft_logits [k][vocab]: the draft model's logits at positions pos .. pos+k-1
+    (row i is the distribution of draft token i + 1); verify_logits [k+1][vocab]:
+    the target's at pos .. pos+k.  Draft i + 1 is the sampler's pick from row i
+    with the sampler's uniform at counter pos + i.  Returns (tokens, drafts):
+    the accepted drafts, then the residual draw at the first rejection or,
+    with every draft accepted, the sampler's pick from the last target row
+    (counter pos + k)."""
+    k = len(draft_logits)
+    drafts = [sample(draft_logits[i], temperature, top_p, sample_uniform(seed, pos + i))[0] for i in range(k)]
+    out = []
+    for i, d in enumerate(drafts):
+        wq, Wq = sample_weights(draft_logits[i], temperature, top_p)
+        wp, Wp = sample_weights(verify_logits[i], temperature, top_p)
+        k_acc, k_res = spec_uniforms(seed, pos + i)
+        if spec_accept(int(wq[d]), Wq, int(wp[d]), Wp, k_acc):
+            out.append(d)
+            continue
+        out.append(spec_residual(wp, Wp, wq, Wq, k_res))
+        return out, drafts
+    out.append(sample(verify_logits[k], temperature, top_p, sample_uniform(seed, pos + k))[0])
+    return out, drafts
 
 
 def cos_sim(a, b) -> float:

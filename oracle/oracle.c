@@ -347,6 +347,35 @@ static int cmp_desc(const void* a, const void* b) {
   return (i > j) - (i < j);
 }
 
+/* the nucleus of the definition above: w[i] = token i's weight, in[i] = 1
+ * for the nucleus tokens, *size = their count; returns the nucleus weight
+ * sum_{N} w (0 when out of memory) */
+static uint64_t nucleus(const float* z, int64_t n, double temperature, double top_p, uint64_t* w, uint8_t* in,
+                        int64_t* size) {
+  double mx = z[0];
+  for (int64_t i = 1; i < n; ++i)
+    if (z[i] > mx) mx = z[i];
+  int64_t* idx = (int64_t*)malloc(sizeof(int64_t) * (size_t)n);
+  if (!idx) return 0;
+  uint64_t Z = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    w[i] = (uint64_t)nearbyint(exp(((double)z[i] - mx) / temperature) * 0x1.0p40);
+    Z += w[i];
+    idx[i] = i;
+    in[i] = 0;
+  }
+  double t = ceil(top_p * (double)Z);
+  uint64_t target = t < 1.0 ? 1 : (t > (double)Z ? Z : (uint64_t)t);
+  g_sort_z = z;
+  qsort(idx, (size_t)n, sizeof(int64_t), cmp_desc);
+  uint64_t M = 0;
+  int64_t k = 0;
+  while (k < n && M < target) { M += w[idx[k]]; in[idx[k]] = 1; ++k; }
+  free(idx);
+  *size = k;
+  return M;
+}
+
 int64_t or_sample(const float* z, int64_t n, double temperature, double top_p, double u, int64_t* nucleus_out) {
   if (n <= 0) return -1;
   if (temperature <= 0.0) {
@@ -356,26 +385,12 @@ int64_t or_sample(const float* z, int64_t n, double temperature, double top_p, d
     if (nucleus_out) *nucleus_out = 1;
     return best;
   }
-  double mx = z[0];
-  for (int64_t i = 1; i < n; ++i)
-    if (z[i] > mx) mx = z[i];
   uint64_t* w = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)n);
-  int64_t* idx = (int64_t*)malloc(sizeof(int64_t) * (size_t)n);
-  uint8_t* in = (uint8_t*)calloc((size_t)n, 1);
-  if (!w || !idx || !in) { free(w); free(idx); free(in); return -2; }
-  uint64_t Z = 0;
-  for (int64_t i = 0; i < n; ++i) {
-    w[i] = (uint64_t)nearbyint(exp(((double)z[i] - mx) / temperature) * 0x1.0p40);
-    Z += w[i];
-    idx[i] = i;
-  }
-  double t = ceil(top_p * (double)Z);
-  uint64_t target = t < 1.0 ? 1 : (t > (double)Z ? Z : (uint64_t)t);
-  g_sort_z = z;
-  qsort(idx, (size_t)n, sizeof(int64_t), cmp_desc);
-  uint64_t M = 0;
+  uint8_t* in = (uint8_t*)malloc((size_t)n);
+  if (!w || !in) { free(w); free(in); return -2; }
   int64_t k = 0;
-  while (k < n && M < target) { M += w[idx[k]]; in[idx[k]] = 1; ++k; }
+  const uint64_t M = nucleus(z, n, temperature, top_p, w, in, &k);
+  if (!M) { free(w); free(in); return -2; }
   uint64_t r = (uint64_t)floor(u * (double)M);
   uint64_t acc = 0;
   int64_t pick = -1;
@@ -385,8 +400,79 @@ int64_t or_sample(const float* z, int64_t n, double temperature, double top_p, d
     if (acc > r) { pick = i; break; }
   }
   if (nucleus_out) *nucleus_out = k;
-  free(w); free(idx); free(in);
+  free(w); free(in);
   return pick;
+}
+
+/* The sampler's distribution as integer weights: w_out[i] = token i's weight
+ * when it is in the nucleus, else 0.  Returns the nucleus weight (the sum of
+ * w_out), 0 on bad arguments. */
+uint64_t or_sample_weights(const float* z, int64_t n, double temperature, double top_p, uint64_t* w_out) {
+  if (n <= 0 || !(temperature > 0.0)) return 0;
+  uint8_t* in = (uint8_t*)malloc((size_t)n);
+  if (!in) return 0;
+  int64_t k = 0;
+  const uint64_t M = nucleus(z, n, temperature, top_p, w_out, in, &k);
+  for (int64_t i = 0; i < n; ++i)
+    if (!in[i]) w_out[i] = 0;
+  free(in);
+  return M;
+}
+
+/* ---- speculative sampling with sampled drafts ------------------------------
+ * [P-feat] names self-speculative decoding and [P-code] a sampler; the pages
+ * say nothing of how a sampled draft is accepted.  Reading: the published
+ * speculative sampling rule (Leviathan, Kalman & Matias, ICML 2023, section
+ * 2.3; Chen et al. 2023, algorithm 2), which keeps the output distribution
+ * exactly the target's.  With q the draft's and p the target's sampler
+ * distribution at a position (integer weights wq, wp with sums Wq, Wp):
+ *   - draft token d is accepted when u < p(d) / q(d), u uniform;
+ *   - otherwise the position's token is drawn from the residual
+ *     max(0, p - q), renormalised;
+ *   - after k accepted drafts one more token is drawn from p at the next
+ *     position.
+ * Exactness: with u = k_acc / 2^24 the test is
+ *   k_acc * wq(d) * Wp < 2^24 * wp(d) * Wq,
+ * and the residual weights R_t = max(0, wp_t * Wq - wq_t * Wp) are integers;
+ * the pick is the token, in index order, whose cumulative R first exceeds
+ * floor(k_res * sum R / 2^24).  Weights are below 2^40 and their sums below
+ * 2^57, so every product fits in 128 bits.
+ * The two 24-bit uniforms of a position come from one splitmix64 output,
+ * h = splitmix64(seed xor (2 counter + 1)) — the odd counters, disjoint from
+ * the sampler's even ones: k_acc = bits 40..63 of h, k_res = bits 16..39. */
+typedef unsigned __int128 u128;
+
+void or_spec_uniforms(uint64_t seed, uint64_t counter, uint32_t* k_acc, uint32_t* k_res) {
+  const uint64_t h = or_splitmix64(seed ^ ((counter << 1) | 1u));
+  *k_acc = (uint32_t)(h >> 40);
+  *k_res = (uint32_t)((h >> 16) & 0xFFFFFFu);
+}
+
+/* 1 when draft token d (weights wq_d of Wq under the draft, wp_d of Wp under
+ * the target) is accepted with uniform k_acc / 2^24 */
+int or_spec_accept(uint64_t wq_d, uint64_t Wq, uint64_t wp_d, uint64_t Wp, uint32_t k_acc) {
+  return (u128)k_acc * wq_d * Wp < (((u128)wp_d * Wq) << 24);
+}
+
+/* the residual draw: index of the token picked from max(0, p - q) with
+ * uniform k_res / 2^24; -1 when the residual is empty (p == q) */
+int64_t or_spec_residual(const uint64_t* wp, uint64_t Wp, const uint64_t* wq, uint64_t Wq, int64_t n,
+                         uint32_t k_res) {
+  u128 total = 0;
+  for (int64_t t = 0; t < n; ++t) {
+    const u128 a = (u128)wp[t] * Wq, b = (u128)wq[t] * Wp;
+    if (a > b) total += a - b;
+  }
+  if (total == 0) return -1;
+  /* floor(k_res * total / 2^24), split so that no product exceeds 128 bits */
+  const u128 r = (u128)k_res * (total >> 24) + (((u128)k_res * (uint64_t)(total & 0xFFFFFFu)) >> 24);
+  u128 acc = 0;
+  for (int64_t t = 0; t < n; ++t) {
+    const u128 a = (u128)wp[t] * Wq, b = (u128)wq[t] * Wp;
+    if (a > b) acc += a - b;
+    if (acc > r) return t;
+  }
+  return -1;
 }
 
 /* cosine similarity <a,b> / (|a| |b|)   ([P-cache] layer skip) */
