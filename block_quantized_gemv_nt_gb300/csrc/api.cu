@@ -305,7 +305,7 @@ nt_status attn_entry(nt_ctx* ctx, const float* q, const void* kc, const void* vc
   NT_REQUIRE(aligned(kc, 16) && aligned(vc, 16), NT_ERR_ALIGNMENT, "caches must be 16-byte aligned");
   const int S = attn_splits(ctx, n_kvh, kv_stride);
   const size_t need = attn_scratch_bytes(n_qh, n_kvh, S, nq);
-  NT_REQUIRE(kScratchAttn + need <= kScratchTune && kScratchAttn + need <= ctx->scratch_bytes, NT_ERR_OOM,
+  NT_REQUIRE(kScratchAttn + need <= kScratchSample && kScratchAttn + need <= ctx->scratch_bytes, NT_ERR_OOM,
              "attention needs %zu scratch bytes", need);
   float* part = reinterpret_cast<float*>(ctx->scratch + kScratchAttn + kAttnCounterBytes);
   unsigned* counters = reinterpret_cast<unsigned*>(ctx->scratch + kScratchAttn);
@@ -352,11 +352,14 @@ nt_status nt_argmax(nt_ctx* ctx, const float* v, int64_t n, int32_t* out, void* 
 nt_status nt_sample(nt_ctx* ctx, const float* z, int64_t n, float T, float P, uint64_t seed, uint64_t counter,
                     int32_t* out, void* stream) {
   NT_TRY(pre_call(ctx));
-  NT_REQUIRE(z && out && n >= 1 && n <= (int64_t(1) << 31) - 1, NT_ERR_INVALID_ARG, "null pointer or bad n");
+  NT_REQUIRE(z && out && n >= 1 && n <= kSampMaxN, NT_ERR_INVALID_ARG, "null pointer or n outside 1..%lld",
+             (long long)kSampMaxN);
   NT_REQUIRE(aligned(z, 4) && aligned(out, 4), NT_ERR_ALIGNMENT, "logits and out must be 4-byte aligned");
   NT_REQUIRE(P > 0.f && P <= 1.f && !(T != T) && T < 3.0e38f, NT_ERR_INVALID_ARG, "top_p in (0, 1], finite temperature");
+  NT_REQUIRE(ctx->scratch_bytes >= kScratchSample + kSampRowBytes, NT_ERR_OOM, "the context scratch has no room for the sampler");
   DeviceGuard g(ctx->device);
-  return launch_sample(ctx, z, n, T, P, seed, nullptr, int64_t(counter), out, as_stream(stream));
+  return launch_sample(ctx, z, n, 1, T, P, seed, nullptr, int64_t(counter), out, ctx->scratch + kScratchSample,
+                       as_stream(stream));
 }
 
 nt_status nt_host_register(nt_ctx* ctx, const void* p, size_t bytes, int read_only) {

@@ -71,6 +71,10 @@ struct nt_model {
   size_t gpart_bytes = 0;
   float temperature = 0.f, top_p = 1.f;  // decode-step sampler (temperature <= 0: greedy)
   uint64_t seed = 0;
+  char* samp = nullptr;                  // sampler state, kMaxVerify rows of kSampRowBytes
+  // speculative sampling: nucleus weights of the draft rows and of the verify rows
+  unsigned long long *sw_q = nullptr, *sW_q = nullptr;  // [kMaxVerify - 1][vocab], [kMaxVerify]
+  unsigned long long *sw_p = nullptr, *sW_p = nullptr;  // [kMaxVerify][vocab], [kMaxVerify]
 };
 
 namespace nt {
@@ -197,6 +201,9 @@ struct StepIO {
   float* logits;
   int32_t* next_tok;   // nullable: receives the argmax
   bool advance;        // the argmax also moves the model state: tok = argmax, pos += 1
+  // sampled drafts (model sampler set): the draft row's nucleus weights and their sum
+  unsigned long long* w_out = nullptr;
+  unsigned long long* W_out = nullptr;
 };
 
 // all kernels of one decode step, enqueued on st
@@ -274,9 +281,9 @@ nt_status enqueue_step(Ctx* c, nt_model* m, const uint8_t* skip, const StepIO& i
     s = launch_gemv(c, d.fmt_out, &j, 1, nullptr, m->x, m->out_norm, d.eps, d.d_model, false, st);
     if (s) return s;
   }
-  if (io.advance && m->temperature > 0.f)  // counter: the position of this step's input token
-    return launch_sample(c, io.logits, d.vocab, m->temperature, m->top_p, m->seed, io.pos, 0, io.next_tok, st, m->tok,
-                         m->pos);
+  if ((io.advance || io.w_out) && m->temperature > 0.f)  // counter: the position of this step's input token
+    return launch_sample(c, io.logits, d.vocab, 1, m->temperature, m->top_p, m->seed, io.pos, 0, io.next_tok, m->samp,
+                         st, io.advance ? m->tok : nullptr, io.advance ? m->pos : nullptr, io.w_out, io.W_out);
   return launch_argmax(c, io.logits, d.vocab, io.next_tok, m->amax_key, m->amax_cnt, st,
                        io.advance ? m->tok : nullptr, io.advance ? m->pos : nullptr);
 }
@@ -394,6 +401,109 @@ __global__ void spec_accept_kernel(const int32_t* spec_tok, const int32_t* vtok,
   *pos = spec_pos[0] + n + 1;
 }
 
+// end of a sampled speculative step (speculative sampling: Leviathan, Kalman
+// & Matias 2023, section 2.3): draft i + 1, drawn from the draft's nucleus
+// distribution q_i, is kept when u < p_i(d) / q_i(d), p_i the target's
+// (verify row i); at the first rejection the step's last token is drawn from
+// max(0, p_i - q_i) renormalised; with every draft kept, the last token is the
+// sampler's pick from verify row k.  All in integers: weights below 2^40,
+// sums below 2^57, products in 128 bits.  Uniforms: h = splitmix64(seed xor
+// (2 (pos + i) + 1)), u = bits 40..63 of h / 2^24 for the test, bits 16..39
+// for the residual draw.  One CTA.
+typedef unsigned __int128 u128;
+constexpr int kAccThreads = 1024;
+
+__device__ __forceinline__ uint64_t spec_splitmix64(uint64_t z) {
+  z += 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// exclusive prefix sum of 128-bit values over the block; total in *total
+__device__ u128 scan128(u128 v, u128* total) {
+  __shared__ unsigned long long slo[kAccThreads / 32], shi[kAccThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  u128 x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long lo = __shfl_up_sync(0xffffffffu, static_cast<unsigned long long>(x), o);
+    const unsigned long long hi = __shfl_up_sync(0xffffffffu, static_cast<unsigned long long>(x >> 64), o);
+    if (lane >= o) x += (u128(hi) << 64) | lo;
+  }
+  if (lane == 31) {
+    slo[warp] = static_cast<unsigned long long>(x);
+    shi[warp] = static_cast<unsigned long long>(x >> 64);
+  }
+  __syncthreads();
+  u128 before = x - v, all = 0;
+  for (int w = 0; w < kAccThreads / 32; ++w) {
+    const u128 t = (u128(shi[w]) << 64) | slo[w];
+    if (w < warp) before += t;
+    all += t;
+  }
+  *total = all;
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(kAccThreads)
+    spec_accept_sampled_kernel(const int32_t* spec_tok, const int32_t* vtok, int k, int64_t n,
+                               const unsigned long long* wq, const unsigned long long* Wq,
+                               const unsigned long long* wp, const unsigned long long* Wp, uint64_t seed,
+                               int32_t* out, int32_t* n_out, int32_t* tok, int64_t* pos, const int64_t* spec_pos) {
+  __shared__ int s_pick;
+  pdl_wait();
+  pdl_trigger();
+  const int64_t per = (n + kAccThreads - 1) / kAccThreads;
+  const int64_t i0 = min(n, int64_t(threadIdx.x) * per), i1 = min(n, i0 + per);
+  int e = k + 1;  // tokens the step emits
+  for (int i = 0; i < k; ++i) {
+    const int32_t d = spec_tok[i + 1];
+    const unsigned long long* q = wq + int64_t(i) * n;
+    const unsigned long long* p = wp + int64_t(i) * n;
+    const unsigned long long Wqi = Wq[i], Wpi = Wp[i];
+    const uint64_t h = spec_splitmix64(seed ^ ((uint64_t(spec_pos[i]) << 1) | 1u));
+    const uint32_t kacc = uint32_t(h >> 40), kres = uint32_t((h >> 16) & 0xFFFFFFu);
+    if (u128(kacc) * q[d] * Wpi < ((u128(p[d]) * Wqi) << 24)) {
+      if (threadIdx.x == 0) out[i] = d;
+      continue;
+    }
+    // rejected: the residual draw, R_t = max(0, p_t Wq - q_t Wp), pick at floor(kres * sum R / 2^24)
+    u128 mass = 0;
+    for (int64_t t = i0; t < i1; ++t) {
+      const u128 a = u128(p[t]) * Wqi, b = u128(q[t]) * Wpi;
+      if (a > b) mass += a - b;
+    }
+    u128 total;
+    const u128 base = scan128(mass, &total);
+    const u128 r = u128(kres) * (total >> 24) + ((u128(kres) * static_cast<unsigned long long>(total & 0xFFFFFFu)) >> 24);
+    if (threadIdx.x == 0) s_pick = -1;
+    __syncthreads();
+    if (mass && base <= r && r < base + mass) {
+      u128 acc = base;
+      for (int64_t t = i0; t < i1; ++t) {
+        const u128 a = u128(p[t]) * Wqi, b = u128(q[t]) * Wpi;
+        if (a > b) acc += a - b;
+        if (acc > r) {
+          s_pick = int(t);
+          break;
+        }
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) out[i] = s_pick >= 0 ? s_pick : vtok[i];  // the residual is never empty after a rejection
+    e = i + 1;
+    break;
+  }
+  if (threadIdx.x == 0) {
+    if (e == k + 1) out[k] = vtok[k];
+    *n_out = e;
+    *tok = out[e - 1];
+    *pos = spec_pos[0] + e;
+  }
+}
+
 // draft layers: [0, n_draft) when n_draft > 0, else every resident layer
 std::vector<uint8_t> draft_mask(const nt_model* m, int n_draft) {
   std::vector<uint8_t> mask(m->d.n_layers, 0);
@@ -416,16 +526,36 @@ nt_status enqueue_spec(Ctx* c, nt_model* m, int k, int n_draft, int32_t* out, in
   bool drafts_stream = false;
   for (int l = 0; l < m->d.n_layers; ++l) drafts_stream = drafts_stream || (!mask[l] && m->host_blob[l]);
   Streamer sm{c, m, st};
+  const bool sampled = m->temperature > 0.f;
+  const int64_t V = m->d.vocab;
   if (!drafts_stream) s = sm.begin(nullptr);
-  for (int i = 0; i < k && !s; ++i)
-    s = enqueue_step(c, m, mask.data(), StepIO{m->spec_tok + i, m->spec_pos + i, m->dlogits, m->spec_tok + i + 1, false},
-                     st, false);
+  for (int i = 0; i < k && !s; ++i) {
+    StepIO io{m->spec_tok + i, m->spec_pos + i, m->dlogits, m->spec_tok + i + 1, false};
+    if (sampled) {  // drafts drawn by the sampler, their distributions kept for the acceptance test
+      if (logits) io.logits = logits + (M + i) * V;
+      io.w_out = m->sw_q + i * V;
+      io.W_out = m->sW_q + i;
+    }
+    s = enqueue_step(c, m, mask.data(), io, st, false);
+  }
   if (!s && drafts_stream) s = sm.begin(nullptr);
-  if (!s) s = enqueue_multi(c, m, M, m->spec_tok, m->spec_pos, logits ? logits : m->lv, true, sm, st);
+  float* vl = logits ? logits : m->lv;
+  if (!s) s = enqueue_multi(c, m, M, m->spec_tok, m->spec_pos, vl, !sampled, sm, st);
+  if (!s && sampled)
+    s = launch_sample(c, vl, V, M, m->temperature, m->top_p, m->seed, m->spec_pos, 0, m->vtok, m->samp, st, nullptr,
+                      nullptr, m->sw_p, m->sW_p);
   if (!s && !c->dry)
-    s = cuda_check(c, launch_k(c, spec_accept_kernel, dim3(1), dim3(32), 0, st, m->spec_tok, m->vtok, k, out, n_out,
-                               m->tok, m->pos, m->spec_pos),
-                   "spec accept launch");
+    s = sampled ? cuda_check(c, launch_k(c, spec_accept_sampled_kernel, dim3(1), dim3(kAccThreads), 0, st,
+                                         static_cast<const int32_t*>(m->spec_tok), static_cast<const int32_t*>(m->vtok),
+                                         k, V, static_cast<const unsigned long long*>(m->sw_q),
+                                         static_cast<const unsigned long long*>(m->sW_q),
+                                         static_cast<const unsigned long long*>(m->sw_p),
+                                         static_cast<const unsigned long long*>(m->sW_p), m->seed, out, n_out, m->tok,
+                                         m->pos, static_cast<const int64_t*>(m->spec_pos)),
+                             "spec accept launch")
+                : cuda_check(c, launch_k(c, spec_accept_kernel, dim3(1), dim3(32), 0, st, m->spec_tok, m->vtok, k, out,
+                                         n_out, m->tok, m->pos, m->spec_pos),
+                             "spec accept launch");
   return s;
 }
 
@@ -566,7 +696,8 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
                npart = up256(attn_scratch_bytes(d.n_qh, d.n_kvh, m->S, kMaxVerify)), nspec = 1024,
                nvx = up256(fl * kMaxVerify * d.d_model), nvq = up256(fl * kMaxVerify * nq),
                nvh = up256(fl * kMaxVerify * d.ffn), nvl = up256(fl * kMaxVerify * d.vocab), ndl = up256(fl * d.vocab),
-               nprompt = up256(sizeof(int32_t) * size_t(d.kv_cap));
+               nprompt = up256(sizeof(int32_t) * size_t(d.kv_cap)), nsamp = kSampRowBytes * kMaxVerify,
+               nsw = up256(8 * size_t(d.vocab)), nsW = up256(8 * kMaxVerify);
   {
     // partial sums of the largest verify GEMM
     const int64_t nkv = int64_t(d.n_kvh) * d.head_dim;
@@ -579,7 +710,7 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
     m->gpart_bytes = up256(m->gpart_bytes);
   }
   const size_t total = 2 * nx + nqb * 2 + nkb * 2 + nh + ncos + nst + npart + nfreq + nspec + nvx + 2 * nvq + nvh +
-                       nvl + ndl + nprompt + m->gpart_bytes;
+                       nvl + ndl + nprompt + m->gpart_bytes + nsamp + nsw * (2 * kMaxVerify - 1) + 2 * nsW;
   int dev_prev = 0;
   cudaGetDevice(&dev_prev);
   cudaSetDevice(ctx->device);
@@ -639,6 +770,11 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   m->dlogits = reinterpret_cast<float*>(take(ndl));
   m->prompt = reinterpret_cast<int32_t*>(take(nprompt));
   m->gpart = reinterpret_cast<float*>(take(m->gpart_bytes));
+  m->samp = take(nsamp);
+  m->sw_q = reinterpret_cast<unsigned long long*>(take(nsw * (kMaxVerify - 1)));
+  m->sw_p = reinterpret_cast<unsigned long long*>(take(nsw * kMaxVerify));
+  m->sW_q = reinterpret_cast<unsigned long long*>(take(nsW));
+  m->sW_p = reinterpret_cast<unsigned long long*>(take(nsW));
   cudaSetDevice(ctx->device);
   nt_status st = launch_inv_freq(ctx, m->inv_freq, d.head_dim, d.theta, nullptr);
   if (!st) st = cuda_check(ctx, cudaDeviceSynchronize(), "model init");
@@ -762,6 +898,9 @@ nt_status nt_spec_step(nt_ctx* ctx, nt_model* m, int32_t token, int64_t pos, int
     key_append(key, tokens_out);
     key_append(key, n_out);
     key_append(key, logits);
+    key_append(key, m->temperature);
+    key_append(key, m->top_p);
+    key_append(key, m->seed);
     s = run_graph(ctx, m, key, st,
                   [&](cudaStream_t cs) { return enqueue_spec(ctx, m, k, n_draft_layers, tokens_out, n_out, logits, cs); });
   }
@@ -826,6 +965,8 @@ nt_status nt_model_set_sampler(nt_ctx* ctx, nt_model* m, float T, float P, uint6
   if (!ctx) return NT_ERR_INVALID_ARG;
   NT_REQUIRE(m, NT_ERR_INVALID_ARG, "null model");
   NT_REQUIRE(P > 0.f && P <= 1.f && !(T != T) && T < 3.0e38f, NT_ERR_INVALID_ARG, "top_p in (0, 1], finite temperature");
+  NT_REQUIRE(!(T > 0.f) || m->d.vocab <= kSampMaxN, NT_ERR_INVALID_ARG, "the sampler takes at most %lld logits",
+             (long long)kSampMaxN);
   m->temperature = T > 0.f ? T : 0.f;
   m->top_p = P;
   m->seed = seed;

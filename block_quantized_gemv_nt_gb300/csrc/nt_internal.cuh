@@ -60,6 +60,9 @@ constexpr size_t kScratchErr = 0;            // unsigned err flag (also ctx->err
 constexpr size_t kScratchArgmax = 256;       // unsigned long long key + unsigned counter
 constexpr size_t kScratchAttn = 4096;        // attention counters (kAttnCounterBytes), then partials
 constexpr size_t kAttnCounterBytes = 2048;   // [queries <= 8][KV heads <= 64] unsigned
+constexpr size_t kScratchSample = size_t(20) << 20;  // sampler state (one row of kSampRowBytes)
+constexpr size_t kSampRowBytes = 32768;             // sampler state per logits row
+constexpr int64_t kSampMaxN = 256 * 4000;           // longest row the sampler takes
 constexpr size_t kScratchTune = size_t(24) << 20;  // GEMV plan tuning outputs (8 MiB)
 constexpr size_t kScratchGemm = size_t(32) << 20;  // verify-GEMM partial sums, to the end of the scratch
 

@@ -479,13 +479,53 @@ __global__ void argmax_kernel(const float* v, int64_t n, unsigned long long* key
 // Token weights are integers, w = rint(exp((z - max z) / T) * 2^40), so every
 // sum is exact and independent of the order of addition.  The nucleus is the
 // shortest prefix of the tokens ordered by logit (descending, ties by lower
-// index) whose weight reaches ceil(top_p * sum w), found by a 4-round radix
-// select on the order-preserving 32-bit key of the logit; the token is the
-// one of the nucleus, in index order, whose cumulative weight first exceeds
-// floor(u * nucleus weight), u from SplitMix64 (Steele, Lea & Flood 2014) of
-// (seed, counter).  One CTA of 1024 threads, each owning a contiguous index
-// range; T <= 0 is greedy.
-constexpr int kSampThreads = 1024;
+// index) whose weight reaches ceil(top_p * sum w), found by a radix select on
+// the order-preserving 32-bit key of the logit (digits of 11, 11 and 10
+// bits); the token is the one of the nucleus, in index order, whose
+// cumulative weight first exceeds floor(u * nucleus weight), u from
+// SplitMix64 (Steele, Lea & Flood 2014) of (seed, counter).  T <= 0 is greedy.
+//
+// Work split: each row (blockIdx.y) is cut into G contiguous CTA ranges of at
+// most kSampPer logits, each thread owning a contiguous run.  Six launches:
+// max, three histogram rounds, a count of ties and of the weight above the
+// threshold key, and the pick.  In every launch the last CTA to finish (an
+// arrival counter, no waiting) does the row-wide step: reduce the maxima,
+// select the digit, place the pick in a CTA range.  Histograms are summed in
+// shared memory as two 32-bit halves of the weight (20 low bits, 21 high
+// bits), then added once per non-empty bin into the row's 64-bit histogram.
+constexpr int kSampThreads = 256;
+constexpr int kSampMaxCtas = 256;
+constexpr int64_t kSampPer = 4000;  // logits per CTA at most: 4000 * 2^20 keeps each 32-bit half below 2^32
+constexpr int kSampBins = 2048;
+
+struct SampRow {
+  unsigned cnt;  // CTAs of the current launch that arrived; the last resets it
+  float M;       // largest logit
+  int arg;       // lowest index holding it
+  uint32_t prefix;
+  unsigned long long Z, target, above, wt, j, Mn, r, cbase;
+  int cstar, pad;
+  unsigned long long hist[kSampBins];
+  float part_max[kSampMaxCtas];
+  int part_arg[kSampMaxCtas];
+  unsigned long long part_ties[kSampMaxCtas], part_mass[kSampMaxCtas], tie0[kSampMaxCtas];
+};
+static_assert(sizeof(SampRow) <= kSampRowBytes, "sampler state row");
+
+struct SampArgs {
+  const float* z;
+  int64_t n, per;
+  float T, P;
+  uint64_t seed;
+  const int64_t* ctr_dev;  // per-row counters, or null: ctr + row
+  int64_t ctr;
+  int32_t* out;             // [rows]
+  int32_t* tok_state;       // nullable (one row): the pick also becomes the model's token ...
+  int64_t* pos_state;       // ... and its position advances
+  unsigned long long* w_out;  // nullable: [rows][n] each token's weight inside the nucleus, else 0
+  unsigned long long* W_out;  // nullable: [rows] the nucleus weight
+  SampRow* st;              // [rows]
+};
 
 __device__ __forceinline__ uint64_t splitmix64(uint64_t z) {
   z += 0x9E3779B97F4A7C15ull;
@@ -501,182 +541,350 @@ __device__ __forceinline__ uint32_t logit_key(float v) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// exclusive prefix sum over the block (1024 threads); total in *total
-__device__ __forceinline__ unsigned long long block_excl_scan(unsigned long long v, unsigned long long* sm,
-                                                              unsigned long long* total) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+__device__ __forceinline__ unsigned long long samp_weight(float v, float M, float T) {
+  if (!(v >= -3.0e38f)) return 0ull;  // NaN and -inf weigh nothing
+  return __float2ull_rn(expf((v - M) / T) * 1099511627776.0f);  // 2^40
+}
+
+// exclusive prefix sum over a block of kSampThreads threads; total in *total
+__device__ __forceinline__ unsigned long long samp_scan(unsigned long long v, unsigned long long* total) {
+  __shared__ unsigned long long sw[kSampThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned long long x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) sm[warp] = x;
+  if (lane == 31) sw[warp] = x;
   __syncthreads();
-  if (warp == 0) {
-    unsigned long long w = sm[lane];
+  unsigned long long before = x - v, all = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    sm[lane] = w;  // inclusive over warps
+  for (int w = 0; w < kSampThreads / 32; ++w) {
+    const unsigned long long t = sw[w];
+    if (w < warp) before += t;
+    all += t;
   }
-  __syncthreads();
-  const unsigned long long before = (warp ? sm[warp - 1] : 0ull) + x - v;
-  *total = sm[31];
+  *total = all;
   __syncthreads();
   return before;
 }
 
-__global__ void __launch_bounds__(kSampThreads) sample_kernel(const float* z, int64_t n, float T, float P,
-                                                              uint64_t seed, const int64_t* ctr_dev, int64_t ctr,
-                                                              int32_t* out, int32_t* tok_state, int64_t* pos_state) {
+// the thread's contiguous run of its CTA's range of row `z`
+struct SampRange {
+  int64_t i0, i1;
+  __device__ SampRange(const SampArgs& a) {
+    const int64_t lo = int64_t(blockIdx.x) * a.per, hi = min(a.n, lo + a.per);
+    const int64_t tper = (a.per + kSampThreads - 1) / kSampThreads;
+    i0 = min(hi, lo + int64_t(threadIdx.x) * tper);
+    i1 = min(hi, i0 + tper);
+  }
+};
+
+// true in the last CTA of the launch to arrive (after every other CTA's
+// global writes are visible to it); resets the counter for the next launch
+__device__ __forceinline__ bool samp_arrive(SampRow* s) {
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(&s->cnt, 1u);
+    last = prev == gridDim.x - 1;
+    if (last) s->cnt = 0;
+  }
+  __syncthreads();
+  if (last) __threadfence();
+  return last;
+}
+
+__device__ __forceinline__ void samp_finish(const SampArgs& a, int row, int pick, unsigned long long Mn) {
+  const int32_t t = pick < 0 ? 0 : pick;
+  if (a.out) a.out[row] = t;
+  if (a.tok_state) *a.tok_state = t;
+  if (a.pos_state) *a.pos_state += 1;
+  if (a.W_out) a.W_out[row] = Mn;
+}
+
+// (max, lowest index) pairs: the larger value, then the lower index
+__device__ __forceinline__ void maxarg_merge(float& m, int64_t& i, float m2, int64_t i2) {
+  if (m2 > m || (m2 == m && i2 < i)) {
+    m = m2;
+    i = i2;
+  }
+}
+
+__device__ __forceinline__ void block_maxarg(float& m, int64_t& i) {
+  __shared__ float sm_m[kSampThreads / 32];
+  __shared__ int64_t sm_i[kSampThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) maxarg_merge(m, i, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, i, o));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    sm_m[warp] = m;
+    sm_i[warp] = i;
+  }
+  __syncthreads();
+  for (int w = 0; w < kSampThreads / 32; ++w) maxarg_merge(m, i, sm_m[w], sm_i[w]);
+  __syncthreads();
+}
+
+// launch 1: the row's largest logit and the lowest index holding it; greedy
+// rows finish here
+__global__ void __launch_bounds__(kSampThreads) samp_max_kernel(SampArgs a) {
   pdl_wait();
   pdl_trigger();
-  __shared__ unsigned long long sm[32];
-  __shared__ unsigned long long hist[256];
-  __shared__ unsigned long long s_above;
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_pick;
-  __shared__ float s_max;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t per = (n + kSampThreads - 1) / kSampThreads;
-  const int64_t i0 = min(n, int64_t(tid) * per), i1 = min(n, i0 + per);
-  const uint64_t counter = ctr_dev ? uint64_t(*ctr_dev) : uint64_t(ctr);
+  const int row = blockIdx.y;
+  SampRow* s = a.st + row;
+  const float* z = a.z + int64_t(row) * a.n;
+  const SampRange r(a);
+  float m = -INFINITY;
+  int64_t idx = a.n;
+  for (int64_t i = r.i0; i < r.i1; ++i) {
+    const float v = z[i];
+    if (v > m || (idx == a.n && v == m)) {  // NaN never enters
+      m = v;
+      idx = i;
+    }
+  }
+  block_maxarg(m, idx);
+  if (threadIdx.x == 0) {
+    s->part_max[blockIdx.x] = m;
+    s->part_arg[blockIdx.x] = int(idx);
+  }
+  if (!samp_arrive(s)) return;
+  m = -INFINITY;
+  idx = a.n;
+  for (int c = threadIdx.x; c < gridDim.x; c += kSampThreads) maxarg_merge(m, idx, __ldcg(&s->part_max[c]), __ldcg(&s->part_arg[c]));
+  block_maxarg(m, idx);
+  if (threadIdx.x == 0) {
+    s->M = m;
+    s->arg = int(idx < a.n ? idx : 0);
+    if (!(a.T > 0.f)) samp_finish(a, row, s->arg, 0ull);
+  }
+}
 
-  // largest logit (NaN never wins)
-  float mx = -INFINITY;
-  for (int64_t i = i0; i < i1; ++i) mx = fmaxf(mx, z[i]);  // fmaxf ignores a NaN operand
-  mx = warp_max(mx);
-  if (lane == 0) reinterpret_cast<float*>(sm)[warp] = mx;
+// launches 2-4: histogram of digit `round` (bits 31..21, 20..10, 9..0) of the
+// keys that match the digits already selected, weighted; the last CTA selects
+// the digit at which the weight, counted from the top, reaches the target
+__global__ void __launch_bounds__(kSampThreads) samp_round_kernel(SampArgs a, int round) {
+  __shared__ uint32_t hlo[kSampBins], hhi[kSampBins];
+  __shared__ int s_d;
+  __shared__ unsigned long long s_above, s_h0;
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.y;
+  SampRow* s = a.st + row;
+  const float* z = a.z + int64_t(row) * a.n;
+  const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
+  const int nb = round == 2 ? 1024 : 2048;
+  const int sel = shift + (round == 2 ? 10 : 11);  // the bits at and above `sel` are already selected
+  for (int b = threadIdx.x; b < nb; b += kSampThreads) hlo[b] = hhi[b] = 0u;
   __syncthreads();
-  if (warp == 0) {
-    float v = reinterpret_cast<float*>(sm)[lane];
-    v = warp_max(v);
-    if (lane == 0) s_max = v;
+  const float M = s->M;
+  const uint32_t prefix = round == 0 ? 0u : s->prefix;
+  const SampRange r(a);
+  unsigned long long zp = 0;
+  for (int64_t i = r.i0; i < r.i1; ++i) {
+    const float v = z[i];
+    const uint32_t k = logit_key(v);
+    if (round > 0 && (k >> sel) != (prefix >> sel)) continue;
+    const unsigned long long w = samp_weight(v, M, a.T);
+    zp += w;
+    if (w) {
+      const uint32_t d = (k >> shift) & uint32_t(nb - 1);
+      atomicAdd(&hlo[d], uint32_t(w & 0xFFFFFu));
+      atomicAdd(&hhi[d], uint32_t(w >> 20));
+    }
   }
   __syncthreads();
-  const float M = s_max;
-  int64_t pick = -1;
+  for (int b = threadIdx.x; b < nb; b += kSampThreads) {
+    const unsigned long long v = (static_cast<unsigned long long>(hhi[b]) << 20) + hlo[b];
+    if (v) atomicAdd(&s->hist[b], v);
+  }
+  if (round == 0) {
+    unsigned long long tot;
+    samp_scan(zp, &tot);
+    if (threadIdx.x == 0 && tot) atomicAdd(&s->Z, tot);
+  }
+  if (!samp_arrive(s)) return;
 
-  if (!(T > 0.f)) {
-    // greedy: lowest index holding the maximum
-    int64_t first = n;
-    for (int64_t i = i0; i < i1; ++i)
-      if (z[i] == M) {
-        first = i;
+  if (round == 0 && threadIdx.x == 0) {
+    const unsigned long long Z = __ldcg(&s->Z);
+    const double tgt = ceil(double(a.P) * double(Z));
+    s->target = tgt < 1.0 ? 1ull : (tgt > double(Z) ? Z : static_cast<unsigned long long>(tgt));
+    s->above = 0ull;
+    s->Z = 0ull;
+  }
+  __syncthreads();
+  const unsigned long long target = s->target, above = s->above;
+  // thread t holds bins nb-1-t*g .. nb-g-t*g, highest first
+  const int g = nb / kSampThreads;
+  unsigned long long h[kSampBins / kSampThreads], sum = 0;
+#pragma unroll
+  for (int q = 0; q < kSampBins / kSampThreads; ++q) {
+    h[q] = 0ull;
+    if (q >= g) continue;
+    const int b = nb - 1 - threadIdx.x * g - q;
+    h[q] = __ldcg(&s->hist[b]);
+    s->hist[b] = 0ull;
+    sum += h[q];
+    if (b == 0) s_h0 = h[q];
+  }
+  unsigned long long total;
+  unsigned long long cum = above + samp_scan(sum, &total);
+  if (threadIdx.x == 0) {
+    s_d = -1;
+    s_above = 0;
+  }
+  __syncthreads();
+  if (cum < target && cum + sum >= target) {
+#pragma unroll
+    for (int q = 0; q < kSampBins / kSampThreads; ++q) {
+      if (q < g && cum + h[q] >= target) {
+        s_d = nb - 1 - threadIdx.x * g - q;
+        s_above = cum;
         break;
       }
-    unsigned long long f = static_cast<unsigned long long>(first);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long t = __shfl_xor_sync(0xffffffffu, f, o);
-      f = t < f ? t : f;
+      cum += h[q];
     }
-    if (lane == 0) sm[warp] = f;
-    __syncthreads();
-    if (tid == 0) {
-      unsigned long long b = sm[0];
-      for (int w = 1; w < 32; ++w) b = sm[w] < b ? sm[w] : b;
-      s_pick = int(b < static_cast<unsigned long long>(n) ? b : 0ull);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int d = s_d;
+    unsigned long long ab = s_above;
+    if (d < 0) {  // the target is not reached above digit 0: take digit 0
+      d = 0;
+      ab = above + total - s_h0;
     }
-    __syncthreads();
-    pick = s_pick;
-  } else {
-    auto weight = [&](float v) -> unsigned long long {
-      if (!(v >= -3.0e38f)) return 0ull;  // NaN and -inf weigh nothing
-      return __float2ull_rn(expf((v - M) / T) * 1099511627776.0f);  // 2^40
-    };
-    unsigned long long part = 0;
-    for (int64_t i = i0; i < i1; ++i) part += weight(z[i]);
-    unsigned long long Z;
-    block_excl_scan(part, sm, &Z);
-    const double tgt = ceil(double(P) * double(Z));
-    const unsigned long long target = tgt < 1.0 ? 1ull : (tgt > double(Z) ? Z : static_cast<unsigned long long>(tgt));
+    const uint32_t pre = prefix | (uint32_t(d) << shift);
+    s->prefix = pre;
+    s->above = ab;
+    if (round == 2) {
+      // pre is the key of the last token the nucleus needs; the nucleus takes
+      // the first j of the tokens holding it (index order)
+      const unsigned long long wt = samp_weight(key_value(pre), M, a.T);
+      const unsigned long long need = target - ab;
+      const unsigned long long j = wt ? (need + wt - 1) / wt : 0ull;
+      const unsigned long long Mn = ab + j * wt;
+      const uint64_t counter = a.ctr_dev ? uint64_t(a.ctr_dev[row]) : uint64_t(a.ctr + row);
+      const double u = double(splitmix64(a.seed ^ (counter << 1)) >> 40) * 0x1.0p-24;
+      s->wt = wt;
+      s->j = j;
+      s->Mn = Mn;
+      s->r = static_cast<unsigned long long>(u * double(Mn));
+    }
+  }
+}
 
-    // radix select: the key tau of the last token the nucleus needs, and the
-    // weight of all keys above it
-    uint32_t prefix = 0, mask = 0;
-    unsigned long long above = 0;
-    for (int round = 0; round < 4; ++round) {
-      const int shift = 24 - 8 * round;
-      if (tid < 256) hist[tid] = 0ull;
-      __syncthreads();
-      for (int64_t i = i0; i < i1; ++i) {
-        const uint32_t k = logit_key(z[i]);
-        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], weight(z[i]));
-      }
-      __syncthreads();
-      if (tid == 0) {
-        unsigned long long cum = above;
-        int d = 255;
-        for (; d > 0; --d) {
-          if (cum + hist[d] >= target) break;
-          cum += hist[d];
-        }
-        s_above = cum;
-        s_prefix = prefix | (uint32_t(d) << shift);
-      }
-      __syncthreads();
-      above = s_above;
-      prefix = s_prefix;
-      mask |= 0xFFu << shift;
-      __syncthreads();
-    }
-    const uint32_t tau = prefix;
-    // the weight of one token at the threshold key, and how many of those ties the nucleus takes
-    float tv = 0.f;
-    {
-      const uint32_t b = (tau & 0x80000000u) ? (tau & 0x7FFFFFFFu) : ~tau;
-      tv = __uint_as_float(b);
-    }
-    const unsigned long long wt = weight(tv);
-    const unsigned long long need = target - above;
-    const unsigned long long j = wt ? (need + wt - 1) / wt : 0ull;
-    const unsigned long long Mn = above + j * wt;
-    const double u = double(splitmix64(seed ^ (counter << 1)) >> 40) * 0x1.0p-24;
-    const unsigned long long r = static_cast<unsigned long long>(u * double(Mn));
+// launch 5: per CTA, the tokens at the threshold key and the weight above it;
+// the last CTA ranks the ties across CTAs and finds the CTA whose nucleus
+// weight holds r
+__global__ void __launch_bounds__(kSampThreads) samp_count_kernel(SampArgs a) {
+  __shared__ int s_c;
+  __shared__ unsigned long long s_base;
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.y;
+  SampRow* s = a.st + row;
+  const float* z = a.z + int64_t(row) * a.n;
+  const float M = s->M;
+  const uint32_t tau = s->prefix;
+  const SampRange r(a);
+  unsigned long long ties = 0, mass = 0;
+  for (int64_t i = r.i0; i < r.i1; ++i) {
+    const float v = z[i];
+    const uint32_t k = logit_key(v);
+    if (k > tau) mass += samp_weight(v, M, a.T);
+    ties += k == tau;
+  }
+  unsigned long long tt, tm;
+  samp_scan(ties, &tt);
+  samp_scan(mass, &tm);
+  if (threadIdx.x == 0) {
+    s->part_ties[blockIdx.x] = tt;
+    s->part_mass[blockIdx.x] = tm;
+  }
+  if (!samp_arrive(s)) return;
+  const int c = threadIdx.x;  // gridDim.x <= kSampThreads
+  const bool has = c < int(gridDim.x);
+  const unsigned long long t = has ? __ldcg(&s->part_ties[c]) : 0ull, ma = has ? __ldcg(&s->part_mass[c]) : 0ull;
+  unsigned long long tot;
+  const unsigned long long t0 = samp_scan(t, &tot);
+  const unsigned long long j = s->j, wt = s->wt, rr = s->r;
+  const unsigned long long take = j > t0 ? (j - t0 < t ? j - t0 : t) : 0ull;
+  const unsigned long long nm = ma + take * wt;
+  const unsigned long long base = samp_scan(nm, &tot);
+  if (threadIdx.x == 0) s_c = -1;
+  __syncthreads();
+  if (has) s->tie0[c] = t0;
+  if (has && nm && base <= rr && rr < base + nm) {
+    s_c = c;
+    s_base = base;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    s->cstar = s_c;
+    s->cbase = s_c >= 0 ? s_base : 0ull;
+  }
+}
 
-    // tie ranks in index order, then the nucleus weight of each thread's range
-    unsigned long long ties = 0;
-    for (int64_t i = i0; i < i1; ++i) ties += logit_key(z[i]) == tau;
-    unsigned long long tmp;
-    const unsigned long long tie0 = block_excl_scan(ties, sm, &tmp);
-    unsigned long long mass = 0, seen = tie0;
-    for (int64_t i = i0; i < i1; ++i) {
-      const uint32_t k = logit_key(z[i]);
+// launch 6: the pick, in the CTA holding r; with w_out every CTA also writes
+// its tokens' nucleus weights
+__global__ void __launch_bounds__(kSampThreads) samp_pick_kernel(SampArgs a) {
+  __shared__ int s_pick;
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.y;
+  SampRow* s = a.st + row;
+  const int cstar = s->cstar;
+  const bool mine = int(blockIdx.x) == cstar || (cstar < 0 && blockIdx.x == 0);
+  if (!mine && !a.w_out) return;
+  const float* z = a.z + int64_t(row) * a.n;
+  const float M = s->M;
+  const uint32_t tau = s->prefix;
+  const unsigned long long j = s->j, rr = s->r;
+  const SampRange r(a);
+  unsigned long long ties = 0;
+  for (int64_t i = r.i0; i < r.i1; ++i) ties += logit_key(z[i]) == tau;
+  unsigned long long tmp;
+  const unsigned long long tie_first = s->tie0[blockIdx.x] + samp_scan(ties, &tmp);
+  unsigned long long mass = 0, seen = tie_first;
+  unsigned long long* wo = a.w_out ? a.w_out + int64_t(row) * a.n : nullptr;
+  for (int64_t i = r.i0; i < r.i1; ++i) {
+    const float v = z[i];
+    const uint32_t k = logit_key(v);
+    const bool in = k > tau || (k == tau && seen < j);
+    seen += k == tau;
+    const unsigned long long w = in ? samp_weight(v, M, a.T) : 0ull;
+    mass += w;
+    if (wo) wo[i] = w;
+  }
+  if (!mine) return;
+  const unsigned long long base = s->cbase + samp_scan(mass, &tmp);
+  if (threadIdx.x == 0) s_pick = -1;
+  __syncthreads();
+  if (cstar >= 0 && mass && base <= rr && rr < base + mass) {
+    unsigned long long acc = base;
+    seen = tie_first;
+    for (int64_t i = r.i0; i < r.i1; ++i) {
+      const float v = z[i];
+      const uint32_t k = logit_key(v);
       const bool in = k > tau || (k == tau && seen < j);
       seen += k == tau;
-      if (in) mass += weight(z[i]);
-    }
-    const unsigned long long base = block_excl_scan(mass, sm, &tmp);
-    if (tid == 0) s_pick = -1;
-    __syncthreads();
-    if (mass && base <= r && r < base + mass) {
-      unsigned long long acc = base;
-      seen = tie0;
-      for (int64_t i = i0; i < i1; ++i) {
-        const uint32_t k = logit_key(z[i]);
-        const bool in = k > tau || (k == tau && seen < j);
-        seen += k == tau;
-        if (!in) continue;
-        acc += weight(z[i]);
-        if (acc > r) {
-          s_pick = int(i);
-          break;
-        }
+      if (!in) continue;
+      acc += samp_weight(v, M, a.T);
+      if (acc > rr) {
+        s_pick = int(i);
+        break;
       }
     }
-    __syncthreads();
-    pick = s_pick;
   }
-  if (tid == 0) {
-    const int32_t t = pick < 0 ? 0 : int32_t(pick);
-    if (out) *out = t;
-    if (tok_state) *tok_state = t;
-    if (pos_state) *pos_state += 1;
-  }
+  __syncthreads();
+  if (threadIdx.x == 0) samp_finish(a, row, s_pick, s->Mn);
 }
 
 // ---- cosine similarity --------------------------------------------------------------
@@ -835,12 +1043,29 @@ nt_status launch_argmax(Ctx* c, const float* v, int64_t n, int32_t* out, unsigne
                     "argmax launch");
 }
 
-nt_status launch_sample(Ctx* c, const float* z, int64_t n, float T, float P, uint64_t seed, const int64_t* ctr_dev,
-                        int64_t ctr, int32_t* out, cudaStream_t st, int32_t* tok_state, int64_t* pos_state) {
+int sample_ctas(int64_t n) {
+  const int64_t g = (n + 1023) / 1024;
+  return int(g < 1 ? 1 : (g > kSampMaxCtas ? kSampMaxCtas : g));
+}
+
+nt_status launch_sample(Ctx* c, const float* z, int64_t n, int rows, float T, float P, uint64_t seed,
+                        const int64_t* ctr_dev, int64_t ctr, int32_t* out, void* state, cudaStream_t st,
+                        int32_t* tok_state, int64_t* pos_state, unsigned long long* w_out,
+                        unsigned long long* W_out) {
   if (c->dry) return NT_OK;
-  return cuda_check(c, launch_k(c, sample_kernel, dim3(1), dim3(kSampThreads), 0, st, z, n, T, P, seed, ctr_dev, ctr, out,
-                                tok_state, pos_state),
-                    "sample launch");
+  const int G = sample_ctas(n);
+  const int64_t per = (n + G - 1) / G;
+  if (per > kSampPer || rows < 1) return set_err(c, NT_ERR_INVALID_ARG, "sampler: n %lld too large", (long long)n);
+  const SampArgs a{z, n, per, T, P, seed, ctr_dev, ctr, out, tok_state, pos_state, w_out, W_out,
+                   static_cast<SampRow*>(state)};
+  const dim3 grid(G, rows), block(kSampThreads);
+  nt_status s = cuda_check(c, launch_k(c, samp_max_kernel, grid, block, 0, st, a), "sample launch");
+  if (s || !(T > 0.f)) return s;
+  for (int round = 0; round < 3 && !s; ++round)
+    s = cuda_check(c, launch_k(c, samp_round_kernel, grid, block, 0, st, a, round), "sample launch");
+  if (!s) s = cuda_check(c, launch_k(c, samp_count_kernel, grid, block, 0, st, a), "sample launch");
+  if (!s) s = cuda_check(c, launch_k(c, samp_pick_kernel, grid, block, 0, st, a), "sample launch");
+  return s;
 }
 
 nt_status launch_cos(Ctx* c, const float* a, const float* b, int64_t n, float* out, cudaStream_t st) {

@@ -30,11 +30,17 @@ nt_status launch_softmax(Ctx* c, const float* x, float* y, int64_t n, cudaStream
 nt_status launch_swiglu(Ctx* c, const float* g, const float* u, float* h, int64_t n, cudaStream_t st);
 nt_status launch_argmax(Ctx* c, const float* v, int64_t n, int32_t* out, unsigned long long* key, unsigned* counter,
                         cudaStream_t st, int32_t* tok_state = nullptr, int64_t* pos_state = nullptr);
-// nucleus sample of z[0..n): temperature T (<= 0: greedy), top-p P, uniform from (seed, counter),
-// counter = *ctr_dev when ctr_dev is set, else ctr
-nt_status launch_sample(Ctx* c, const float* z, int64_t n, float T, float P, uint64_t seed, const int64_t* ctr_dev,
-                        int64_t ctr, int32_t* out, cudaStream_t st, int32_t* tok_state = nullptr,
-                        int64_t* pos_state = nullptr);
+// nucleus sample of rows z[row][0..n), row < rows: temperature T (<= 0:
+// greedy), top-p P, uniform from (seed, counter), counter = ctr_dev[row] when
+// ctr_dev is set, else ctr + row; state: rows x kSampRowBytes, zero at rest
+// (the launches leave it so).  tok_state / pos_state (one row): the pick also
+// becomes the model's token and its position advances.  w_out [rows][n] /
+// W_out [rows] (nullable, T > 0): each token's weight inside the nucleus
+// (else 0) and the nucleus weight.
+nt_status launch_sample(Ctx* c, const float* z, int64_t n, int rows, float T, float P, uint64_t seed,
+                        const int64_t* ctr_dev, int64_t ctr, int32_t* out, void* state, cudaStream_t st,
+                        int32_t* tok_state = nullptr, int64_t* pos_state = nullptr,
+                        unsigned long long* w_out = nullptr, unsigned long long* W_out = nullptr);
 nt_status configure_gemv(Ctx* c);
 nt_status configure_gemm(Ctx* c);
 int gemm_parts(int fmt, int64_t cols);

@@ -121,9 +121,11 @@ class DeviceModel:
             dev = self.logits.device
             self.spec_tokens = torch.zeros(8, dtype=torch.int32, device=dev)
             self.spec_count = torch.zeros(1, dtype=torch.int32, device=dev)
-            self.spec_logits = torch.empty(8, self.spec.vocab, dtype=torch.float32, device=dev)
+            self.spec_logits = torch.empty(16, self.spec.vocab, dtype=torch.float32, device=dev)
         nt.nt_spec_step(self.ctx, self.handle, token, pos, k, n_draft_layers, self.spec_tokens, self.spec_count,
                         self.spec_logits, stream)
+        # with the sampler set, the draft logits follow the verify rows
+        self.draft_logits = self.spec_logits[k + 1:2 * k + 1]
         return self.spec_tokens, self.spec_count, self.spec_logits[:k + 1]
 
     def calibrate(self, token: int, pos: int, n_skip: int, stream=None):

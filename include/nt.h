@@ -199,7 +199,9 @@ nt_status nt_argmax(nt_ctx* ctx, const float* v_dev, int64_t n, int32_t* out_dev
  * 2^-24 (SplitMix64 output function: Steele, Lea & Flood 2014) and
  * r = floor(u * nucleus weight), the pick is the nucleus token, in index
  * order, whose cumulative weight first exceeds r.  temperature <= 0 is
- * greedy (nt_argmax).  top_p in (0, 1]. */
+ * greedy (nt_argmax).  top_p in (0, 1]; n 1..1,024,000.  Six launches over
+ * up to 256 CTAs (one for greedy); the state between them lives in context
+ * scratch at 20 MiB, so calls on one context must not overlap on the GPU. */
 nt_status nt_sample(nt_ctx* ctx, const float* logits_dev, int64_t n, float temperature, float top_p, uint64_t seed,
                     uint64_t counter, int32_t* out_dev, void* stream);
 
@@ -277,7 +279,8 @@ nt_status nt_decode_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t po
  * token stays greedy): every later step draws its next token with nt_sample's
  * definition, counter = the position of the step's input token, so a
  * sequence is reproducible from (seed, start).  temperature <= 0 restores
- * greedy decoding.  nt_spec_step always decodes greedily. */
+ * greedy decoding.  nt_spec_step then samples too (speculative sampling).
+ * With temperature > 0 the vocabulary must be at most 1,024,000. */
 nt_status nt_model_set_sampler(nt_ctx* ctx, nt_model* model, float temperature, float top_p, uint64_t seed);
 
 /* Layer-skip calibration [cache]: one full decode step (all layers) at
@@ -360,7 +363,24 @@ nt_status nt_model_slot(nt_ctx* ctx, nt_model* model, int slot, void** slot_dev_
  * KV entries written past the accepted ones are overwritten by later steps.
  * logits_dev (nullable) receives the verify logits [k + 1][vocab].  k is
  * 1..7; pos + k < kv_cap.  Streamed layers stream in the verify pass as in
- * nt_decode_step.  One CUDA graph per (k, n_draft_layers, outputs). */
+ * nt_decode_step.  One CUDA graph per (k, n_draft_layers, outputs, sampler).
+ *
+ * With the model's sampler set (nt_model_set_sampler, temperature > 0) the
+ * step is speculative sampling (Leviathan, Kalman & Matias 2023, section
+ * 2.3), whose output follows the target model's sampler distribution:
+ *  - draft d_{i+1} is nt_sample's pick from the draft logits at position
+ *    pos + i (counter pos + i); q_i, p_i are the nucleus distributions of the
+ *    draft row and of verify row i, as integer weights w and their sum W;
+ *  - d_{i+1} is accepted when k_acc * wq(d) * Wp < 2^24 * wp(d) * Wq, i.e.
+ *    u < p_i(d) / q_i(d); at the first rejection the step's last token is the
+ *    index-order pick at floor(k_res * sum R / 2^24) of the residual
+ *    R_t = max(0, wp_t * Wq - wq_t * Wp); with all k accepted it is
+ *    nt_sample's pick from verify row k (counter pos + k);
+ *  - k_acc = bits 40..63 and k_res = bits 16..39 of
+ *    splitmix64(seed ^ (2 (pos + i) + 1)).
+ * tokens_out_dev gets the accepted drafts then that last token, *n_out_dev
+ * their count, and logits_dev (when given) must hold 2k + 1 rows: the k + 1
+ * verify rows, then the k draft rows. */
 nt_status nt_spec_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos, int k, int n_draft_layers,
                        int32_t* tokens_out_dev, int32_t* n_out_dev, float* logits_dev, void* stream);
 
