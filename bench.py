@@ -398,19 +398,27 @@ def bench_prefill(args, rank, world):
             "gpu_launches": None, "clocks": clk.summary()}
 
 
+SAMPLER = (0.8, 0.9)  # temperature, top-p of the "_sample" workloads
+
+
 def parse_decode(name):
-    """<model>[_skip<N>][_spec<K>]: a synthetic model, optionally decoding with
-    the N layers of highest calibration cosine skipped, or self-speculatively
-    with K drafted tokens per step.  Returns (spec, n_skip, k)."""
+    """<model>[_skip<N>][_spec<K>][_sample]: a synthetic model, optionally
+    decoding with the N layers of highest calibration cosine skipped, or
+    self-speculatively with K drafted tokens per step; "_sample" draws tokens
+    with the sampler (SAMPLER) instead of the argmax (speculative sampling
+    with _spec).  Returns (spec, n_skip, k, sampled)."""
     import synth
     n_skip = k = 0
+    sampled = name.endswith("_sample")
+    if sampled:
+        name = name[:-len("_sample")]
     if "_spec" in name:
         name, n = name.rsplit("_spec", 1)
         k = int(n)
     if "_skip" in name:
         name, n = name.rsplit("_skip", 1)
         n_skip = int(n)
-    return synth.model_spec(name), n_skip, k
+    return synth.model_spec(name), n_skip, k, sampled
 
 
 def bench_decode(args, rank, world):
@@ -419,12 +427,14 @@ def bench_decode(args, rank, world):
     import synth
     from block_quantized_gemv_nt_gb300 import engine, nt
 
-    spec, n_skip, _ = parse_decode(args.workload)
+    spec, n_skip, _, sampled = parse_decode(args.workload)
     t0 = time.perf_counter()
     hm = synth.make_host_model(spec)
     t_gen = time.perf_counter() - t0
     ctx = nt.Context(torch.cuda.current_device())
     gm = engine.DeviceModel(ctx, spec, hm)
+    if sampled:
+        gm.set_sampler(*SAMPLER, seed=spec.seed)
     st = torch.cuda.Stream()
     P = spec.n_prefill
     window = spec.n_gen
@@ -525,7 +535,7 @@ def bench_decode(args, rank, world):
 
     per_step_bytes = step_bytes(spec, skip)
     n_exec = spec.n_layers - (int(np.sum(skip)) if skip is not None else 0)
-    kernels_per_step = 2 + n_exec * (4 + len({spec.fmt[t] for t in ("wq", "wk", "wv")})) + 1
+    kernels_per_step = 2 + n_exec * (4 + len({spec.fmt[t] for t in ("wq", "wk", "wv")})) + (6 if sampled else 1)
     line = {
         "metric": METRIC, "value": round(tok_s * world, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
@@ -535,6 +545,7 @@ def bench_decode(args, rank, world):
                    "d_model": spec.d_model, "ffn": spec.ffn,
                    "vocab": spec.vocab, "kv_prefill": P, "batch": 1, "seed": spec.seed,
                    "weights": {k: synth.FMT_NAMES[v] for k, v in spec.fmt.items()},
+                   "decode": "sampled (temperature %g, top-p %g)" % SAMPLER if sampled else "greedy",
                    "l2": f"inputs larger than L2 ({per_step_bytes / 1e9:.2f} GB read per token)",
                    "step_bytes": per_step_bytes,
                    "step_hbm_gbs": round(per_step_bytes * tok_s / 1e9, 1),
@@ -583,7 +594,7 @@ def bench_streamed(args, rank, world):
     import synth
     from block_quantized_gemv_nt_gb300 import engine, nt
 
-    spec, n_skip, k = parse_decode(args.workload)
+    spec, n_skip, k, sampled = parse_decode(args.workload)
     assert n_skip == 0, "layer skip is not combined with streaming here"
     t0 = time.perf_counter()
     blobs = engine.HostBlobs(spec)
@@ -599,6 +610,8 @@ def bench_streamed(args, rank, world):
         fixed = spec.n_resident * spec.layer_bytes() + r * synth.row_bytes(spec.fmt["out"], c)
         slots = int(max(2, min(8, (args.hbm_weight_cap * 1e9 - fixed) // blobs.nbytes))) if k else 2
     gm = engine.DeviceModel(ctx, spec, hm, blobs=blobs, stream_slots=slots)
+    if sampled:
+        gm.set_sampler(*SAMPLER, seed=spec.seed)
     st = torch.cuda.Stream()
     P = spec.n_prefill
     n_streamed = len(blobs.layers)
@@ -678,7 +691,8 @@ def bench_streamed(args, rank, world):
                    "hbm_weight_bytes": hbm_w, "hbm_weight_cap_gb": args.hbm_weight_cap, "d_model": spec.d_model, "ffn": spec.ffn, "vocab": spec.vocab,
                    "kv_prefill": P, "batch": 1, "seed": spec.seed,
                    "weights": {kk: synth.FMT_NAMES[v] for kk, v in spec.fmt.items()},
-                   "decode": f"self-speculative, k={k} drafts by the resident layers" if k else "greedy",
+                   "decode": (f"self-speculative, k={k} drafts by the resident layers" if k else "greedy")
+                   + (", sampled (temperature %g, top-p %g)" % SAMPLER if sampled else ""),
                    "tokens_per_pass": round(per_pass, 3),
                    "draft_acceptance": round((per_pass - 1) / k, 4) if k else None,
                    "l2": f"inputs larger than L2 ({link_bytes / 1e9:.1f} GB streamed per pass)"},
@@ -697,11 +711,12 @@ def bench_streamed(args, rank, world):
     if k:
         # per pass: setup, k drafts (resident layers), verify (GEMM + epilogue per GEMV, attention), accept
         n_res = spec.n_resident
-        draft = 2 + n_res * per_layer + 1
-        verify = 1 + n_exec * (2 * (per_layer - 1) + 1) + 2 + k + 1
+        draft = 2 + n_res * per_layer + (6 if sampled else 1)
+        verify = 1 + n_exec * (2 * (per_layer - 1) + 1) + 2 + (6 if sampled else k + 1)
         line["gpu_launches"] = args.steps * (2 + k * draft + verify)
     else:
-        line["gpu_launches"] = args.steps * (3 + n_exec * per_layer) + (args.steps + window - 1) // window
+        line["gpu_launches"] = (args.steps * (2 + n_exec * per_layer + (6 if sampled else 1))
+                                + (args.steps + window - 1) // window)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_decode(spec, hm, budget_s=args.cpu_budget)
     gm.close()
@@ -781,12 +796,12 @@ def reference_arm(args, rank, world):
                 "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                                  "sample": f"{args.steps} full oracle GEMVs"},
                 "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    prefill_n = 0
+    prefill_n, sampled = 0, False
     if "_prefill" in args.workload:
         base, n = args.workload.rsplit("_prefill", 1)
         spec, n_skip, prefill_n = synth.model_spec(base), 0, int(n)
     else:
-        spec, n_skip, _ = parse_decode(args.workload)
+        spec, n_skip, _, sampled = parse_decode(args.workload)
     hm = synth.make_host_model(spec)
     import oracle
     om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
@@ -803,7 +818,13 @@ def reference_arm(args, rank, world):
     for _ in range(n):
         logits = om.step(tok, pos, skip)
         # a prompt is fed token by token (teacher-forced); decoding feeds back the argmax
-        tok, pos = (int(np.argmax(logits)) if not prefill_n else (tok * 7 + 3) % spec.vocab), pos + 1
+        if prefill_n:
+            nxt = (tok * 7 + 3) % spec.vocab
+        elif sampled:
+            nxt = oracle.sample(logits, *SAMPLER, oracle.sample_uniform(spec.seed, pos))[0]
+        else:
+            nxt = int(np.argmax(logits))
+        tok, pos = nxt, pos + 1
     dt = (time.perf_counter() - t0) / n
     v = round(1.0 / dt, 4)
     return {"metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world, "steps": n, "warmup": args.warmup,

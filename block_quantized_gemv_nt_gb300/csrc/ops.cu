@@ -667,6 +667,31 @@ __global__ void __launch_bounds__(kSampThreads) samp_max_kernel(SampArgs a) {
   }
 }
 
+// add each lane's weight w (when `has`) to bin d of the split histogram:
+// lanes holding the same bin are summed first (up to 4 distinct bins per
+// call, the usual case when the logits crowd a few bins), the rest add alone
+__device__ __forceinline__ void hist_add(uint32_t* hlo, uint32_t* hhi, bool has, uint32_t d, unsigned long long w) {
+  const unsigned lane = threadIdx.x & 31;
+  const uint32_t lo = uint32_t(w & 0xFFFFFu), hi = uint32_t(w >> 20);
+  unsigned todo = __ballot_sync(0xffffffffu, has);
+  for (int it = 0; todo && it < 4; ++it) {
+    const int leader = __ffs(todo) - 1;
+    const uint32_t dl = __shfl_sync(0xffffffffu, d, leader);
+    const bool mine = ((todo >> lane) & 1u) && d == dl;
+    const uint32_t slo = __reduce_add_sync(0xffffffffu, mine ? lo : 0u);
+    const uint32_t shi = __reduce_add_sync(0xffffffffu, mine ? hi : 0u);
+    if (int(lane) == leader) {
+      atomicAdd(&hlo[dl], slo);
+      atomicAdd(&hhi[dl], shi);
+    }
+    todo &= ~__ballot_sync(0xffffffffu, mine);
+  }
+  if ((todo >> lane) & 1u) {
+    atomicAdd(&hlo[d], lo);
+    atomicAdd(&hhi[d], hi);
+  }
+}
+
 // launches 2-4: histogram of digit `round` (bits 31..21, 20..10, 9..0) of the
 // keys that match the digits already selected, weighted; the last CTA selects
 // the digit at which the weight, counted from the top, reaches the target
@@ -688,17 +713,15 @@ __global__ void __launch_bounds__(kSampThreads) samp_round_kernel(SampArgs a, in
   const uint32_t prefix = round == 0 ? 0u : s->prefix;
   const SampRange r(a);
   unsigned long long zp = 0;
-  for (int64_t i = r.i0; i < r.i1; ++i) {
-    const float v = z[i];
+  const int64_t tper = (a.per + kSampThreads - 1) / kSampThreads;  // the same trip count in every lane
+  for (int64_t e = 0; e < tper; ++e) {
+    const int64_t i = r.i0 + e;
+    const float v = i < r.i1 ? z[i] : -INFINITY;
     const uint32_t k = logit_key(v);
-    if (round > 0 && (k >> sel) != (prefix >> sel)) continue;
-    const unsigned long long w = samp_weight(v, M, a.T);
+    const bool match = round == 0 || (k >> sel) == (prefix >> sel);
+    const unsigned long long w = match ? samp_weight(v, M, a.T) : 0ull;
     zp += w;
-    if (w) {
-      const uint32_t d = (k >> shift) & uint32_t(nb - 1);
-      atomicAdd(&hlo[d], uint32_t(w & 0xFFFFFu));
-      atomicAdd(&hhi[d], uint32_t(w >> 20));
-    }
+    hist_add(hlo, hhi, w != 0ull, (k >> shift) & uint32_t(nb - 1), w);
   }
   __syncthreads();
   for (int b = threadIdx.x; b < nb; b += kSampThreads) {
