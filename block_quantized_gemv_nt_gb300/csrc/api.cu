@@ -149,6 +149,7 @@ nt_status nt_ctx_destroy(nt_ctx* ctx) {
     DeviceGuard g(ctx->device);
     cudaDeviceSynchronize();
     cudaFree(ctx->scratch);
+    if (ctx->flush) cudaFree(ctx->flush);
   }
   delete ctx;
   return NT_OK;

@@ -47,6 +47,8 @@ struct Ctx {
   bool gemv_tune = true;         // time candidate plans on a shape's first eager launch
   bool dry = false;              // enqueue nothing: launchers only tune (a dry pass before a capture)
   std::map<std::string, PlanChoice> gemv_plans;  // tuned plan per launch shape
+  char* flush = nullptr;         // read before each timed tuning launch so its weights come from HBM
+  size_t flush_bytes = 0;
 };
 
 // host-side status helpers ----------------------------------------------------
