@@ -1,7 +1,7 @@
 // qformats.cuh — the GGUF block formats as seen by the quant-GEMV kernels:
 // per-format dot products of one block unit against x held in shared memory
-// as 24-bit fixed point in three byte planes, and the x prologue that builds
-// those planes.  Formats and element values ("Ntransformer" (en.unwiki.net),
+// as fixed point in byte planes (24-bit in three planes by default, 16-bit
+// in two with NT_X_PLANES=2), and the x prologue that builds those planes.  Formats and element values ("Ntransformer" (en.unwiki.net),
 // About; GGUF layouts): Q8_0 d*q; Q4_0 d*(q-8); Q4_K/Q5_K d*sc*q - dmin*m;
 // Q6_K d*sc*(q-32).
 #pragma once
@@ -48,33 +48,59 @@ __device__ __forceinline__ void ld4(const uint8_t* p, uint32_t* w) {
 }
 
 // ---------------------------------------------------------------------------
-// Shared x.  Each 32-column group g holds x as 24-bit fixed point,
-// x24 = rint(x * 2^sh_g), split into three byte planes
-//   x24 = p2 * 2^16 + p1 * 2^8 + p0   (p2 signed, p1 and p0 unsigned)
-// stored as [p0: 32 B][p1: 32 B][p2: 32 B][16 B pad] at goff(g), plus
-// scale[g] = 2^-sh_g and psum[col/16] = sum of x24 over 16 columns (for the
+// Shared x.  Each 32-column group g holds x as B-bit fixed point (B = 8 *
+// kPlanes: 24 by default, 16 with NT_X_PLANES=2), xq = rint(x * 2^sh_g),
+// split into kPlanes byte planes
+//   xq = sum_k p_k 256^k   (the top plane signed, the others unsigned)
+// stored as [p0: 32 B][p1: 32 B]([p2: 32 B])[16 B pad] at goff(g), plus
+// scale[g] = 2^-sh_g and psum[col/16] = sum of xq over 16 columns (for the
 // constant offsets of Q4_0 and Q6_K and the mins of the K formats; at most
-// 2^27 in magnitude).  |x - x24 2^-sh| is at most 2^-23 of the group's
-// largest |x|.
+// 2^(B+4) in magnitude).  sh_g puts the group's largest |x| just below
+// 2^(B-1), so |x - xq 2^-sh| is at most 2^-B of it: 2^-24 with three planes,
+// the order of fp32 rounding.  Two planes (2^-16) save a third of the dp4a
+// work — 12-15% faster on the ALU-bound K formats — but a dot product that
+// cancels (|y| far below sum |w x|) can then miss a 1e-3 relative bound, so
+// the library is built with three.
+#ifndef NT_X_PLANES
+#define NT_X_PLANES 3
+#endif
+constexpr int kPlanes = NT_X_PLANES;
+static_assert(kPlanes == 2 || kPlanes == 3, "x is held in two or three byte planes");
+constexpr int kXBits = 8 * kPlanes;
+constexpr int kGroupPitch = 32 * kPlanes + 16;  // shared bytes per 32-column group (planes + pad)
+
 struct XS {
   const uint8_t* x;
   const float* scale;
   const int* psum;
 };
 
-// sum of the three planes' integer dot products: 65536 a2 + 256 a1 + a0.
-// 256 a1 + a0 is formed in int32 (every format keeps |a1|, |a0| below 2^22,
-// so it cannot overflow), then one fp32 rounding per step.
-__device__ __forceinline__ float planes(int a2, int a1, int a0) {
-  return fmaf(float(a2), 65536.0f, float(a1 * 256 + a0));
+// sum of the planes' integer dot products: sum_k 256^k a[k].  256 a1 + a0 is
+// formed in int32 (every format keeps |a1|, |a0| below 2^22, so it cannot
+// overflow), then one fp32 rounding per step.
+__device__ __forceinline__ float planes(const int (&a)[kPlanes]) {
+  if constexpr (kPlanes == 3) return fmaf(float(a[2]), 65536.0f, float(a[1] * 256 + a[0]));
+  else return float(a[1] * 256 + a[0]);
 }
 
-// -c * S split over the planes (S = 65536 (S >> 16) + 256 ((S >> 8) & 255) +
-// (S & 255)), so the constant offset folds exactly into the integer sums
-__device__ __forceinline__ void plane_offsets(int S, int c, int off[3]) {
+// -c * S split over the planes (S = sum_k 256^k s_k, the top digit signed),
+// so the constant offset folds exactly into the integer sums
+__device__ __forceinline__ void plane_offsets(int S, int c, int (&off)[kPlanes]) {
   off[0] = -c * (S & 255);
-  off[1] = -c * ((S >> 8) & 255);
-  off[2] = -c * (S >> 16);
+  if constexpr (kPlanes == 3) {
+    off[1] = -c * ((S >> 8) & 255);
+    off[2] = -c * (S >> 16);
+  } else {
+    off[1] = -c * (S >> 8);
+  }
+}
+
+// a + (x plane word xw) . (weight word w): plane `top` is the signed plane;
+// WS: the weight bytes are signed
+template <bool WS>
+__device__ __forceinline__ int dp(bool top, uint32_t xw, uint32_t w, int a) {
+  if (WS) return top ? dp4_ss(xw, w, a) : dp4_us(xw, w, a);
+  return top ? dp4_su(xw, w, a) : dp4_uu(xw, w, a);
 }
 
 template <int FMT>
@@ -84,14 +110,14 @@ struct Q;
 template <>
 struct Q<NT_Q8_0> {
   static constexpr int BE = 32, BB = 34, ALIGN = 32, UPB = 1, PB = 0;
-  static constexpr bool FLOATX = false;  // x as 24-bit byte planes
+  static constexpr bool FLOATX = false;  // x as fixed-point byte planes
   struct X {
-    uint32_t v[3][8];
+    uint32_t v[kPlanes][8];
     float s;
   };
   __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int) {
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
+    for (int k = 0; k < kPlanes; ++k) {
       ld4(g + 32 * k, x.v[k]);
       ld4(g + 32 * k + 16, x.v[k] + 4);
     }
@@ -107,14 +133,12 @@ struct Q<NT_Q8_0> {
     w.d = __half2float(*reinterpret_cast<const __half*>(blk));
   }
   __device__ static float dotw(const W& w, int, const X& x) {
-    int a0 = 0, a1 = 0, a2 = 0;
+    int a[kPlanes] = {};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      a0 = dp4_us(x.v[0][i], w.q[i], a0);
-      a1 = dp4_us(x.v[1][i], w.q[i], a1);
-      a2 = dp4_ss(x.v[2][i], w.q[i], a2);
-    }
-    return planes(a2, a1, a0) * (w.d * x.s);
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int k = 0; k < kPlanes; ++k) a[k] = dp<true>(k == kPlanes - 1, x.v[k][i], w.q[i], a[k]);
+    return planes(a) * (w.d * x.s);
   }
   __device__ static float dot(const uint8_t* blk, int u, const X& x) {
     W w;
@@ -128,15 +152,15 @@ struct Q<NT_Q8_0> {
 template <>
 struct Q<NT_Q4_0> {
   static constexpr int BE = 32, BB = 18, ALIGN = 32, UPB = 1, PB = 0;
-  static constexpr bool FLOATX = false;  // x as 24-bit byte planes
+  static constexpr bool FLOATX = false;  // x as fixed-point byte planes
   struct X {
-    uint32_t v[3][8];
+    uint32_t v[kPlanes][8];
     float s;
-    int off[3];  // -8 * sum(x24) over the block, split over the planes
+    int off[kPlanes];  // -8 * sum(xq) over the block, split over the planes
   };
   __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int) {
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
+    for (int k = 0; k < kPlanes; ++k) {
       ld4(g + 32 * k, x.v[k]);
       ld4(g + 32 * k + 16, x.v[k] + 4);
     }
@@ -159,14 +183,17 @@ struct Q<NT_Q4_0> {
     w.d = __half2float(*reinterpret_cast<const __half*>(blk));
   }
   __device__ static float dotw(const W& w, int, const X& x) {
-    int a0 = x.off[0], a1 = x.off[1], a2 = x.off[2];
+    int a[kPlanes];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      a0 = dp4_uu(x.v[0][4 + i], w.hi[i], dp4_uu(x.v[0][i], w.lo[i], a0));
-      a1 = dp4_uu(x.v[1][4 + i], w.hi[i], dp4_uu(x.v[1][i], w.lo[i], a1));
-      a2 = dp4_su(x.v[2][4 + i], w.hi[i], dp4_su(x.v[2][i], w.lo[i], a2));
-    }
-    return planes(a2, a1, a0) * (w.d * x.s);
+    for (int k = 0; k < kPlanes; ++k) a[k] = x.off[k];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int k = 0; k < kPlanes; ++k) {
+        const bool top = k == kPlanes - 1;
+        a[k] = dp<false>(top, x.v[k][4 + i], w.hi[i], dp<false>(top, x.v[k][i], w.lo[i], a[k]));
+      }
+    return planes(a) * (w.d * x.s);
   }
   __device__ static float dot(const uint8_t* blk, int u, const X& x) {
     W w;
@@ -198,13 +225,13 @@ __device__ __forceinline__ void kq_scales(uint32_t h1, uint32_t h2, uint32_t h3,
 // X of the 4/5-bit K formats: unit c = 64 columns = sub-blocks 2c, 2c+1 =
 // groups A (low nibbles) and B (high nibbles).
 struct XK {
-  uint32_t a[3][8], b[3][8];
+  uint32_t a[kPlanes][8], b[kPlanes][8];
   float s0, s1;  // group scales
   float t0, t1;  // sum(x) over each sub-block
 };
 __device__ __forceinline__ void load_xk(XK& x, const uint8_t* g, const uint8_t* g2, const XS& xs, int col0, int c) {
 #pragma unroll
-  for (int k = 0; k < 3; ++k) {
+  for (int k = 0; k < kPlanes; ++k) {
     ld4(g + 32 * k, x.a[k]);
     ld4(g + 32 * k + 16, x.a[k] + 4);
     ld4(g2 + 32 * k, x.b[k]);
@@ -231,35 +258,30 @@ __device__ __forceinline__ void kq_header(const uint8_t* blk, int c, WK& w) {
   w.dmin = h2f(hdr.x >> 16);
 }
 
-// nibble bytes lo/hi of one qs word against plane words of groups A and B
-#define NT_KQ_MAC(i, lo, hi)                                          \
-  do {                                                                \
-    A0 = dp4_uu(x.a[0][i], lo, A0);                                   \
-    A1 = dp4_uu(x.a[1][i], lo, A1);                                   \
-    A2 = dp4_su(x.a[2][i], lo, A2);                                   \
-    B0 = dp4_uu(x.b[0][i], hi, B0);                                   \
-    B1 = dp4_uu(x.b[1][i], hi, B1);                                   \
-    B2 = dp4_su(x.b[2][i], hi, B2);                                   \
-  } while (0)
-
+// the quant bytes lo (sub-block 2c) and hi (2c+1) against the plane words
+// of groups A and B
 __device__ __forceinline__ float kq_dotw(const WK& w, const XK& x) {
-  int A0 = 0, A1 = 0, A2 = 0, B0 = 0, B1 = 0, B2 = 0;
+  int A[kPlanes] = {}, B[kPlanes] = {};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) NT_KQ_MAC(i, w.lo[i], w.hi[i]);
-  const float qa = planes(A2, A1, A0), qb = planes(B2, B1, B0);
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int k = 0; k < kPlanes; ++k) {
+      A[k] = dp<false>(k == kPlanes - 1, x.a[k][i], w.lo[i], A[k]);
+      B[k] = dp<false>(k == kPlanes - 1, x.b[k][i], w.hi[i], B[k]);
+    }
+  const float qa = planes(A), qb = planes(B);
   // sum_j (d sc_j q - dmin m_j) x = d (sc0 s0 qa + sc1 s1 qb) - dmin (m0 t0 + m1 t1)
   return w.d * fmaf(w.sc0 * x.s0, qa, w.sc1 * x.s1 * qb) - w.dmin * fmaf(w.m0, x.t0, w.m1 * x.t1);
 }
-#undef NT_KQ_MAC
 
 // Q4_K: d | dmin | scales[12] | qs[128].  value d*sc*q - dmin*m.
 template <>
 struct Q<NT_Q4_K> {
   static constexpr int BE = 256, BB = 144, ALIGN = 8, UPB = 4, PB = 1;
-  static constexpr bool FLOATX = false;  // x as 24-bit byte planes
+  static constexpr bool FLOATX = false;  // x as fixed-point byte planes
   using X = XK;
   __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int c) {
-    load_xk(x, g, g + 112, xs, col0, c);
+    load_xk(x, g, g + kGroupPitch, xs, col0, c);
   }
   using W = WK;
   __device__ static void unpack(const uint8_t* blk, int c, W& w) {
@@ -287,10 +309,10 @@ struct Q<NT_Q4_K> {
 template <>
 struct Q<NT_Q5_K> {
   static constexpr int BE = 256, BB = 176, ALIGN = 8, UPB = 4, PB = 1;
-  static constexpr bool FLOATX = false;  // x as 24-bit byte planes
+  static constexpr bool FLOATX = false;  // x as fixed-point byte planes
   using X = XK;
   __device__ static void load_x(X& x, const uint8_t* g, const XS& xs, int col0, int c) {
-    load_xk(x, g, g + 112, xs, col0, c);
+    load_xk(x, g, g + kGroupPitch, xs, col0, c);
   }
   using W = WK;
   __device__ static void unpack(const uint8_t* blk, int c, W& w) {
@@ -322,19 +344,19 @@ struct Q<NT_Q5_K> {
 template <>
 struct Q<NT_Q6_K> {
   static constexpr int BE = 256, BB = 210, ALIGN = 8, UPB = 4, PB = 2;
-  static constexpr bool FLOATX = false;  // x as 24-bit byte planes
+  static constexpr bool FLOATX = false;  // x as fixed-point byte planes
   struct X {
-    uint32_t v[4][3][4];  // chunk g, plane k, 4 words (16 columns)
-    float s[4];           // group scales
-    int off[4][3];        // -32 * sum(x24) over the chunk, split over the planes
+    uint32_t v[4][kPlanes][4];  // chunk g, plane k, 4 words (16 columns)
+    float s[4];                 // group scales
+    int off[4][kPlanes];        // -32 * sum(xq) over the chunk, split over the planes
   };
   __device__ static void load_x(X& x, const uint8_t* g0, const XS& xs, int col0, int u) {
     const int h = u >> 1, s = u & 1;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      const uint8_t* p = g0 + 112 * (4 * h + g) + 16 * s;
+      const uint8_t* p = g0 + kGroupPitch * (4 * h + g) + 16 * s;
 #pragma unroll
-      for (int k = 0; k < 3; ++k) ld4(p + 32 * k, x.v[g][k]);
+      for (int k = 0; k < kPlanes; ++k) ld4(p + 32 * k, x.v[g][k]);
       const int col = col0 + 128 * h + 32 * g + 16 * s;
       x.s[g] = xs.scale[col / 32];
       plane_offsets(xs.psum[col / 16], 32, x.off[g]);
@@ -369,23 +391,21 @@ struct Q<NT_Q6_K> {
     w.d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
   }
   __device__ static float dotw(const W& w, int, const X& x) {
-    int a[4][3];
+    int a[4][kPlanes];
 #pragma unroll
     for (int g = 0; g < 4; ++g)
 #pragma unroll
-      for (int k = 0; k < 3; ++k) a[g][k] = x.off[g][k];
+      for (int k = 0; k < kPlanes; ++k) a[g][k] = x.off[g][k];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        a[g][0] = dp4_uu(x.v[g][0][i], w.q[i][g], a[g][0]);
-        a[g][1] = dp4_uu(x.v[g][1][i], w.q[i][g], a[g][1]);
-        a[g][2] = dp4_su(x.v[g][2][i], w.q[i][g], a[g][2]);
-      }
-    float t = w.sc[0] * x.s[0] * planes(a[0][2], a[0][1], a[0][0]);
-    t = fmaf(w.sc[1] * x.s[1], planes(a[1][2], a[1][1], a[1][0]), t);
-    t = fmaf(w.sc[2] * x.s[2], planes(a[2][2], a[2][1], a[2][0]), t);
-    t = fmaf(w.sc[3] * x.s[3], planes(a[3][2], a[3][1], a[3][0]), t);
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int k = 0; k < kPlanes; ++k) a[g][k] = dp<false>(k == kPlanes - 1, x.v[g][k][i], w.q[i][g], a[g][k]);
+    float t = w.sc[0] * x.s[0] * planes(a[0]);
+    t = fmaf(w.sc[1] * x.s[1], planes(a[1]), t);
+    t = fmaf(w.sc[2] * x.s[2], planes(a[2]), t);
+    t = fmaf(w.sc[3] * x.s[3], planes(a[3]), t);
     return w.d * t;
   }
   __device__ static float dot(const uint8_t* blk, int u, const X& x) {
@@ -465,13 +485,13 @@ struct Q<NT_F32> {
   }
 };
 
-// byte offset of 32-column group g: 112 bytes per group, plus PB*16 bytes
-// per 8 groups (one K block), chosen per format so that the 16-byte plane
-// reads of a quarter-warp fall into 8 distinct bank groups; 144 bytes per
-// group for fp32 x
+// byte offset of 32-column group g: kGroupPitch bytes per group (80 with two
+// planes, 112 with three), plus PB*16 bytes per 8 groups (one K block),
+// chosen per format so that the 16-byte plane reads of a quarter-warp fall
+// into 8 distinct bank groups; 144 bytes per group for fp32 x
 template <int FMT>
 __host__ __device__ constexpr int goff(int g) {
-  return Q<FMT>::FLOATX ? 144 * g : 112 * g + 16 * Q<FMT>::PB * (g / 8);
+  return Q<FMT>::FLOATX ? 144 * g : kGroupPitch * g + 16 * Q<FMT>::PB * (g / 8);
 }
 
 template <int FMT>
@@ -482,9 +502,9 @@ __host__ __device__ constexpr int x_bytes(int cols) {
 
 // One pass of the x prologue for one warp: 8 lanes per 32-column group, 4
 // columns (x4) per lane, lane `sub` = lane & 7 of group `grp`.  Converts the
-// group to 24-bit fixed point with scale 2^-sh (sh from the exponent of the
-// group's largest |x|), writes its three byte planes, the sum of x24 over
-// each 16 columns and the scale.  Every lane of the warp must call it (shuffles);
+// group to kXBits-bit fixed point with scale 2^-sh (sh from the exponent of
+// the group's largest |x|), writes its byte planes, the sum of xq over each
+// 16 columns and the scale.  Every lane of the warp must call it (shuffles);
 // `live` = grp is a real group.
 template <int FMT>
 __device__ __forceinline__ void put_x4(float4 x4, bool live, int grp, int sub, uint8_t* xsm, int* psum,
@@ -497,22 +517,20 @@ __device__ __forceinline__ void put_x4(float4 x4, bool live, int grp, int sub, u
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-  // m = f * 2^e with f in [0.5, 1): e from the exponent field; scale = 2^(23 - e)
+  // m = f * 2^e with f in [0.5, 1): e from the exponent field; scale = 2^(kXBits - 1 - e)
   const int e = int((__float_as_uint(m) >> 23) & 0xFFu) - 126;
-  const int sh = min(126, max(-126, 23 - e));
+  const int sh = min(126, max(-126, kXBits - 1 - e));
   const float scl = __uint_as_float(uint32_t(127 + sh) << 23);
-  constexpr int kLim = (1 << 23) - 1;
+  constexpr int kLim = (1 << (kXBits - 1)) - 1;
   const int q0 = max(-kLim, min(kLim, __float2int_rn(x4.x * scl)));
   const int q1 = max(-kLim, min(kLim, __float2int_rn(x4.y * scl)));
   const int q2 = max(-kLim, min(kLim, __float2int_rn(x4.z * scl)));
   const int q3 = max(-kLim, min(kLim, __float2int_rn(x4.w * scl)));
-  // byte planes: plane k holds byte k of the four 24-bit values
+  // byte planes: plane k holds byte k of the four values (the top one signed)
   const uint32_t lo01 = __byte_perm(q0, q1, 0x5410), lo23 = __byte_perm(q2, q3, 0x5410);  // bytes 0,1 of each
-  const uint32_t hi01 = __byte_perm(q0, q1, 0x7632), hi23 = __byte_perm(q2, q3, 0x7632);  // bytes 2,3 of each
   const uint32_t pw0 = __byte_perm(lo01, lo23, 0x6420);
   const uint32_t pw1 = __byte_perm(lo01, lo23, 0x7531);
-  const uint32_t pw2 = __byte_perm(hi01, hi23, 0x6420);
-  // sum of x24 over the 16 columns of this lane's quarter-group (4 lanes)
+  // sum of xq over the 16 columns of this lane's quarter-group (4 lanes)
   int ps = (q0 + q1) + (q2 + q3);
   ps += __shfl_xor_sync(0xffffffffu, ps, 1);
   ps += __shfl_xor_sync(0xffffffffu, ps, 2);
@@ -520,7 +538,10 @@ __device__ __forceinline__ void put_x4(float4 x4, bool live, int grp, int sub, u
     uint8_t* gp = xsm + goff<FMT>(grp) + 4 * sub;
     *reinterpret_cast<uint32_t*>(gp) = pw0;
     *reinterpret_cast<uint32_t*>(gp + 32) = pw1;
-    *reinterpret_cast<uint32_t*>(gp + 64) = pw2;
+    if constexpr (kPlanes == 3) {
+      const uint32_t hi01 = __byte_perm(q0, q1, 0x7632), hi23 = __byte_perm(q2, q3, 0x7632);  // bytes 2,3 of each
+      *reinterpret_cast<uint32_t*>(gp + 64) = __byte_perm(hi01, hi23, 0x6420);
+    }
     if ((sub & 3) == 0) psum[2 * grp + (sub >> 2)] = ps;
     if (sub == 0) gscale[grp] = __uint_as_float(uint32_t(127 - sh) << 23);
   }
