@@ -309,9 +309,8 @@ nt_status attn_entry(nt_ctx* ctx, const float* q, const void* kc, const void* vc
   NT_REQUIRE(kScratchAttn + need <= kScratchSample && kScratchAttn + need <= ctx->scratch_bytes, NT_ERR_OOM,
              "attention needs %zu scratch bytes", need);
   float* part = reinterpret_cast<float*>(ctx->scratch + kScratchAttn + kAttnCounterBytes);
-  unsigned* counters = reinterpret_cast<unsigned*>(ctx->scratch + kScratchAttn);
   DeviceGuard g(ctx->device);
-  return launch_attn(ctx, q, kc, vc, out, n_qh, n_kvh, n_pos, nullptr, kv_stride, part, counters, S,
+  return launch_attn(ctx, q, kc, vc, out, n_qh, n_kvh, n_pos, nullptr, kv_stride, part, S,
                      as_stream(stream), nq);
 }
 }  // namespace

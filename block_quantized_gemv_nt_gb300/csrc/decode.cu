@@ -46,7 +46,6 @@ struct nt_model {
   unsigned long long* amax_key = nullptr;
   unsigned* amax_cnt = nullptr;
   float* attn_part = nullptr;
-  unsigned* attn_cnt = nullptr;
   int S = 0;
   cudaStream_t cap = nullptr;
   std::map<std::string, cudaGraphExec_t> graphs;
@@ -250,7 +249,7 @@ nt_status enqueue_step(Ctx* c, nt_model* m, const uint8_t* skip, const StepIO& i
       }
     }
     s = launch_attn(c, m->q, L.kcache, L.vcache, m->ao, d.n_qh, d.n_kvh, 0, io.pos, d.kv_cap, m->attn_part,
-                    m->attn_cnt, m->S, st);
+                    m->S, st);
     if (s) return s;
     {
       nt_gemv_job j{L.wo, m->x, m->x, d.d_model};
@@ -328,7 +327,7 @@ nt_status enqueue_multi(Ctx* c, nt_model* m, int M, const int32_t* tok_dev, cons
       }
     }
     s = launch_attn(c, m->qv, L.kcache, L.vcache, m->aov, d.n_qh, d.n_kvh, 0, pos_dev, d.kv_cap, m->attn_part,
-                    m->attn_cnt, m->S, st, M);
+                    m->S, st, M);
     if (s) return s;
     {
       const GemmJobEx j{L.wo, d.d_model, m->xv, d.d_model, m->xv, nullptr, kEpiPlain};
@@ -754,7 +753,6 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   m->amax_cnt = reinterpret_cast<unsigned*>(stt + 24);
   m->inv_freq = reinterpret_cast<double*>(take(nfreq));
   char* part = take(npart);
-  m->attn_cnt = reinterpret_cast<unsigned*>(part);
   m->attn_part = reinterpret_cast<float*>(part + kAttnCounterBytes);
   char* sp = take(nspec);
   m->spec_tok = reinterpret_cast<int32_t*>(sp);

@@ -60,8 +60,8 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 // scratch layout (bytes from ctx->scratch) ------------------------------------
 constexpr size_t kScratchErr = 0;            // unsigned err flag (also ctx->err_flag)
 constexpr size_t kScratchArgmax = 256;       // unsigned long long key + unsigned counter
-constexpr size_t kScratchAttn = 4096;        // attention counters (kAttnCounterBytes), then partials
-constexpr size_t kAttnCounterBytes = 2048;   // [queries <= 8][KV heads <= 64] unsigned
+constexpr size_t kScratchAttn = 4096;        // attention: a reserved head (kAttnCounterBytes), then partials
+constexpr size_t kAttnCounterBytes = 2048;
 constexpr size_t kScratchSample = size_t(20) << 20;  // sampler state (one row of kSampRowBytes)
 constexpr size_t kSampRowBytes = 32768;             // sampler state per logits row
 constexpr int64_t kSampMaxN = 256 * 4000;           // longest row the sampler takes

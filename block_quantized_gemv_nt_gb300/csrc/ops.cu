@@ -115,7 +115,6 @@ __global__ void rope_append_kernel(float* q, const float* k, const float* v, __h
 // memory; partials (m, l, o[128]) go to scratch; the last CTA of a KV head
 // combines the S partials.
 constexpr int kAttnThreads = 256;
-constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kTiles = 4;  // 32-position tiles per chunk (kMaxChunk / 32)
 constexpr int kHD = 128;
 constexpr int kMaxGroup = 16;
@@ -130,8 +129,7 @@ struct AttnArgs {
   int64_t n_pos;
   const int64_t* pos_dev;  // nullable: n_pos = *pos_dev + 1
   int64_t kv_stride;
-  float* part;             // [nq][n_kvh][S][G][2 + 128]
-  unsigned* counters;      // [nq][n_kvh]
+  float* part;             // [nq][n_kvh][S][G][kPS]
   unsigned* err;
   int64_t q_stride;        // floats between the q (and out) vectors of consecutive queries
   int64_t part_stride;     // floats between the partials of consecutive queries
@@ -143,10 +141,9 @@ constexpr int kWpStride = kHD + 4;
 constexpr int kWpM = kHD, kWpL = kHD + 1;
 constexpr int kPS = kWpStride;  // floats per (split, head) partial in scratch
 
-// shared memory: K and V chunks, q (scaled), combine weights, warp partials
+// shared memory: K and V chunks, q (scaled), warp partials
 __host__ __device__ constexpr size_t attn_smem_bytes(int G) {
-  return size_t(2) * kMaxChunk * kHD * 2 + size_t(G) * kHD * 4 + size_t(G) * kMaxChunk * 4 +
-         size_t(kTiles) * G * kWpStride * 4 + 16;
+  return size_t(2) * kMaxChunk * kHD * 2 + size_t(G) * kHD * 4 + size_t(kTiles) * G * kWpStride * 4 + 16;
 }
 
 __device__ __forceinline__ float4 h4(uint2 raw) {
@@ -156,15 +153,13 @@ __device__ __forceinline__ float4 h4(uint2 raw) {
 }
 
 template <int G>
-__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kAttnThreads, (G >= 16 ? 1 : 2)) attn_kernel(const AttnArgs a) {
   extern __shared__ __align__(128) uint8_t asmem[];
   __half* Ks = reinterpret_cast<__half*>(asmem);                  // [kMaxChunk][128]
   __half* Vs = Ks + kMaxChunk * kHD;                               // [kMaxChunk][128]
   float* qs = reinterpret_cast<float*>(Vs + kMaxChunk * kHD);      // [G][128], pre-scaled by 1/sqrt(128)
-  float* wts = qs + G * kHD;                                       // [G][kMaxChunk] combine weights
-  float* wp = wts + G * kMaxChunk;                                 // [warps][G][kWpStride] warp partials
+  float* wp = qs + G * kHD;                                        // [warps][G][kWpStride] warp partials
   uint64_t* bar = reinterpret_cast<uint64_t*>(wp + kTiles * G * kWpStride);
-  __shared__ bool last;
 
   const int g = blockIdx.x, s = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -172,9 +167,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   // attention of consecutive tokens (the verify pass); one query in decode
   const int qi = blockIdx.z;
   const float* qv = a.q + int64_t(qi) * a.q_stride;
-  float* outv = a.out + int64_t(qi) * a.q_stride;
   float* partv = a.part + int64_t(qi) * a.part_stride;
-  unsigned* cnt = a.counters + qi * a.n_kvh;
   pdl_trigger();
   // In the decode step (pos_dev set) the cached positions before pos were
   // written by earlier tokens and are stable, so their K/V chunk streams in
@@ -326,74 +319,61 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     }
   }
 
-  // the last CTA of this KV head combines the S partials
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned prev = atomicAdd(cnt + g, 1u);
-    last = (prev == unsigned(a.S - 1));
+}
+
+// The split partials of one (KV head g, head h of its group, query qi) into
+// the attention output: with the splits' maxima m_t and sums l_t,
+// M = max m_t, w_t = e^(m_t - M) / sum_t l_t e^(m_t - M), out = sum_t w_t o_t.
+// One CTA of kHD threads, one per output dimension.  Launched right behind
+// the attention kernel (a dependent launch: its CTAs wait for that grid to
+// finish, which orders the partials' writes before the reads here).
+__global__ void __launch_bounds__(kHD) attn_combine_kernel(const AttnArgs a) {
+  __shared__ float wts[kMaxChunk];
+  __shared__ float red[kHD / 32];
+  pdl_trigger();
+  pdl_wait();
+  const int g = blockIdx.x, h = blockIdx.y, qi = blockIdx.z, d = threadIdx.x, lane = d & 31, warp = d >> 5;
+  const int G = a.G, S = a.S;
+  const float* base = a.part + int64_t(qi) * a.part_stride + (int64_t(g) * S * G + h) * kPS;
+  const int64_t stride = int64_t(G) * kPS;  // floats between consecutive splits
+  // split d's (max, sum), and this dimension of the first 32 splits, all in flight together
+  float mt = -INFINITY, lt = 0.f;
+  if (d < S) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + d * stride + kWpM));
+    mt = ml.x;
+    lt = ml.y;
   }
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  // stage every split's (max, sum) in shared memory, turn them into per-split
-  // weights w_t = e^(m_t - M) / L, then each output element is an independent
-  // sum over the splits
-  const float* base = partv + int64_t(g) * a.S * G * kPS;
-  float* lsum = wp;  // the warp partials are merged: their space holds each split's sum
-  for (int i = tid; i < G * a.S; i += kAttnThreads) {
-    const int h = i / a.S, t = i % a.S;
-    const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + (int64_t(t) * G + h) * kPS + kWpM));
-    wts[h * kMaxChunk + t] = ml.x;
-    lsum[h * kMaxChunk + t] = ml.y;
-  }
-  __syncthreads();
-  for (int h = warp; h < G; h += kAttnWarps) {
-    float M = -INFINITY;
-    for (int t = lane; t < a.S; t += 32) M = fmaxf(M, wts[h * kMaxChunk + t]);
-    M = warp_max(M);
-    float L = 0.f;
-    for (int t = lane; t < a.S; t += 32) {
-      const float mt = wts[h * kMaxChunk + t];
-      const float w = mt == -INFINITY ? 0.f : __expf(mt - M);
-      L = fmaf(lsum[h * kMaxChunk + t], w, L);
-      wts[h * kMaxChunk + t] = w;
-    }
-    L = warp_sum(L);
-    const float inv = 1.0f / L;
-    for (int t = lane; t < a.S; t += 32) wts[h * kMaxChunk + t] *= inv;
-  }
-  __syncthreads();
-  // each thread: 4 dims of one head, 16-byte loads, two splits per round
-  for (int it = tid; it < G * (kHD / 4); it += kAttnThreads) {
-    const int h = it / (kHD / 4), d4 = 4 * (it % (kHD / 4));
-    const float* pp = base + int64_t(h) * kPS + d4;
-    const int64_t stride = int64_t(G) * kPS;
-    const float* w = wts + h * kMaxChunk;
-    float4 A = make_float4(0.f, 0.f, 0.f, 0.f), B = A;
-    int t = 0;
-    // eight splits' loads in flight before their sums
-    for (; t + 8 <= a.S; t += 8) {
-      float4 u[8];
+  float v[32];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) u[j] = __ldcg(reinterpret_cast<const float4*>(pp + (t + j) * stride));
+  for (int j = 0; j < 32; ++j) v[j] = j < S ? __ldcg(base + j * stride + d) : 0.f;
+  float M = warp_max(mt);
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = red[0];
 #pragma unroll
-      for (int j = 0; j < 8; j += 2) {
-        const float wu = w[t + j], wv = w[t + j + 1];
-        A = make_float4(fmaf(u[j].x, wu, A.x), fmaf(u[j].y, wu, A.y), fmaf(u[j].z, wu, A.z), fmaf(u[j].w, wu, A.w));
-        B = make_float4(fmaf(u[j + 1].x, wv, B.x), fmaf(u[j + 1].y, wv, B.y), fmaf(u[j + 1].z, wv, B.z),
-                        fmaf(u[j + 1].w, wv, B.w));
-      }
-    }
-    for (; t < a.S; ++t) {
-      const float4 u = __ldcg(reinterpret_cast<const float4*>(pp + t * stride));
-      const float wu = w[t];
-      A = make_float4(fmaf(u.x, wu, A.x), fmaf(u.y, wu, A.y), fmaf(u.z, wu, A.z), fmaf(u.w, wu, A.w));
-    }
-    *reinterpret_cast<float4*>(outv + (int64_t(g) * G + h) * kHD + d4) =
-        make_float4(A.x + B.x, A.y + B.y, A.z + B.z, A.w + B.w);
+  for (int w = 1; w < kHD / 32; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
+  const float w = (d < S && mt != -INFINITY) ? __expf(mt - M) : 0.f;
+  float L = warp_sum(lt * w);
+  if (lane == 0) red[warp] = L;
+  __syncthreads();
+  L = red[0];
+#pragma unroll
+  for (int k = 1; k < kHD / 32; ++k) L += red[k];
+  if (d < S) wts[d] = w * (1.0f / L);
+  __syncthreads();
+  float acc = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (j < S) acc = fmaf(v[j], wts[j], acc);
+  for (int t0 = 32; t0 < S; t0 += 32) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = t0 + j < S ? __ldcg(base + (t0 + j) * stride + d) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (t0 + j < S) acc = fmaf(v[j], wts[t0 + j], acc);
   }
-  if (tid == 0) cnt[g] = 0u;  // ready for the next launch
+  a.out[int64_t(qi) * a.q_stride + (int64_t(g) * G + h) * kHD + d] = acc;
 }
 
 using AttnKernel = void (*)(AttnArgs);
@@ -991,8 +971,8 @@ size_t attn_scratch_bytes(int n_qh, int n_kvh, int S, int nq) {
 size_t attn_part_floats(int n_qh, int n_kvh, int S) { return size_t(n_kvh) * S * (n_qh / n_kvh) * kPS; }
 
 nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, float* out, int n_qh, int n_kvh,
-                      int64_t n_pos, const int64_t* pos_dev, int64_t kv_stride, float* part, unsigned* counters,
-                      int S, cudaStream_t st, int nq) {
+                      int64_t n_pos, const int64_t* pos_dev, int64_t kv_stride, float* part, int S, cudaStream_t st,
+                      int nq) {
   if (c->dry) return NT_OK;
   AttnArgs a{};
   a.q_stride = int64_t(n_qh) * kHD;
@@ -1009,12 +989,14 @@ nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, floa
   a.pos_dev = pos_dev;
   a.kv_stride = kv_stride;
   a.part = part;
-  a.counters = counters;
   a.err = c->err_flag;
   const size_t smem = attn_smem_bytes(a.G);
   AttnKernel k = attn_kernel_for(a.G);
   if (!k) return set_err(c, NT_ERR_INVALID_ARG, "attention: group size %d not in {1,2,4,8,16}", a.G);
-  return cuda_check(c, launch_k(c, k, dim3(n_kvh, S, nq), dim3(kAttnThreads), smem, st, a), "attention launch");
+  nt_status s = cuda_check(c, launch_k(c, k, dim3(n_kvh, S, nq), dim3(kAttnThreads), smem, st, a), "attention launch");
+  if (s) return s;
+  return cuda_check(c, launch_k(c, attn_combine_kernel, dim3(n_kvh, a.G, nq), dim3(kHD), 0, st, a),
+                    "attention combine launch");
 }
 
 cudaError_t configure_attn(size_t optin) {
@@ -1099,14 +1081,13 @@ nt_status launch_cos(Ctx* c, const float* a, const float* b, int64_t n, float* o
 
 // ---------------------------------------------------------------------------
 // Allocation-free variant of the decode attention.  Its scratch (split
-// partials, combine counters, error word) is this file-scope array instead
+// partials, error word) is this file-scope array instead
 // of context memory, so the entry point needs no nt_ctx and calls neither
 // cudaMalloc nor cudaFree.  Every GPU that loads the library holds the array
 // until the process exits.
 namespace {
 constexpr size_t kAttnStaticBytes = size_t(4) << 20;  // 4 MiB
-constexpr size_t kAttnStaticCounters = 0;             // 64 unsigned
-constexpr size_t kAttnStaticErr = 256;                // unsigned error word
+constexpr size_t kAttnStaticErr = 256;                // unsigned error word (bytes 0..255 unused)
 constexpr size_t kAttnStaticPart = 512;               // split partials
 static __device__ __align__(256) unsigned char g_attn_static_scratch[kAttnStaticBytes];
 
@@ -1162,8 +1143,6 @@ extern "C" nt_status nt_attn_decode_static(const float* q, const void* kc, const
   const size_t part_bytes = size_t(n_kvh) * S * (n_qh / n_kvh) * kPS * sizeof(float);
   if (kAttnStaticPart + part_bytes > kAttnStaticBytes) return NT_ERR_INVALID_ARG;  // beyond the fixed scratch
   cudaStream_t st = as_stream(stream);
-  // the combine counters must start at zero; a call cut short may have left them set
-  if (cudaMemsetAsync(sd->scratch + kAttnStaticCounters, 0, kAttnStaticPart, st) != cudaSuccess) return NT_ERR_CUDA;
   AttnArgs a{};
   a.q = q;
   a.K = static_cast<const __half*>(kc);
@@ -1177,11 +1156,11 @@ extern "C" nt_status nt_attn_decode_static(const float* q, const void* kc, const
   a.pos_dev = nullptr;
   a.kv_stride = kv_stride;
   a.part = reinterpret_cast<float*>(sd->scratch + kAttnStaticPart);
-  a.counters = reinterpret_cast<unsigned*>(sd->scratch + kAttnStaticCounters);
   a.err = reinterpret_cast<unsigned*>(sd->scratch + kAttnStaticErr);
   AttnKernel k = attn_kernel_for(a.G);
   if (!k) return NT_ERR_INVALID_ARG;
   k<<<dim3(n_kvh, S), kAttnThreads, attn_smem_bytes(a.G), st>>>(a);
+  attn_combine_kernel<<<dim3(n_kvh, a.G), kHD, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? NT_OK : NT_ERR_CUDA;
 }
 

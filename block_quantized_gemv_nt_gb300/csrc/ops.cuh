@@ -22,10 +22,11 @@ int64_t attn_max_stride();
 size_t attn_scratch_bytes(int n_qh, int n_kvh, int S, int nq = 1);
 size_t attn_part_floats(int n_qh, int n_kvh, int S);
 // nq queries: query i sees n_pos + i positions (pos_dev set: *pos_dev + 1 + i);
-// q, out [nq][n_qh * 128]; part [nq][attn_part_floats]; counters [nq][n_kvh], zero
+// q, out [nq][n_qh * 128]; part [nq][attn_part_floats].  Two launches: the
+// split kernel, then the combine of its partials.
 nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, float* out, int n_qh, int n_kvh,
-                      int64_t n_pos, const int64_t* pos_dev, int64_t kv_stride, float* part, unsigned* counters,
-                      int S, cudaStream_t st, int nq = 1);
+                      int64_t n_pos, const int64_t* pos_dev, int64_t kv_stride, float* part, int S, cudaStream_t st,
+                      int nq = 1);
 nt_status launch_softmax(Ctx* c, const float* x, float* y, int64_t n, cudaStream_t st);
 nt_status launch_swiglu(Ctx* c, const float* g, const float* u, float* h, int64_t n, cudaStream_t st);
 nt_status launch_argmax(Ctx* c, const float* v, int64_t n, int32_t* out, unsigned long long* key, unsigned* counter,

@@ -148,9 +148,10 @@ nt_status nt_rope_kv_append(nt_ctx* ctx, float* q_dev, const float* k_dev, const
 /* Decode attention with grouped KV heads [feat] GQA over the F16 KV cache:
  * for q head h, KV head g = h / (n_qh / n_kvh):
  *   out_h = softmax_j(q_h . K_g[j] / sqrt(head_dim)) . V_g[j],  j < n_pos.
- * Split over positions (flash-decoding), partials combined in the same
- * launch through context scratch.  head_dim must be 128, n_qh / n_kvh one of
- * 1, 2, 4, 8, 16, kv_stride at most 16384 positions. */
+ * Split over positions (flash-decoding): one launch writes each split's
+ * partial (max, sum, unnormalised output) to context scratch, a second
+ * combines them.  head_dim must be 128, n_qh / n_kvh one of 1, 2, 4, 8, 16,
+ * kv_stride at most 16384 positions. */
 nt_status nt_attn_decode(nt_ctx* ctx, const float* q_dev, const void* kcache_dev, const void* vcache_dev,
                          float* out_dev, int n_qh, int n_kvh, int head_dim, int64_t n_pos, int64_t kv_stride,
                          void* stream);
@@ -394,8 +395,8 @@ nt_status nt_spec_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos,
  * callers cannot create one).
  *
  * Same operation, arguments and result as nt_attn_decode, on the calling
- * thread's current device.  The split partials, the combine counters and the
- * error word live in one fixed 4 MiB array compiled into the library
+ * thread's current device.  The split partials and the error word live in
+ * one fixed 4 MiB array compiled into the library
  * (every GPU that loads the library holds it until the process exits);
  * n_kvh * S * (n_qh / n_kvh) * 132 * 4 + 512 bytes must fit in it, where
  * S = min(128, max(ceil(SMs / n_kvh), ceil(kv_stride / 128))) — e.g. 64 q
@@ -404,9 +405,9 @@ nt_status nt_spec_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos,
  *  - The first call on a device looks up the array's device address and sets
  *    the kernel's shared-memory limit; make that first call before any stream
  *    capture.
- *  - Every call shares the array and clears its counters on `stream` first;
- *    calls whose work overlaps on the GPU (different streams, or devices
- *    sharing nothing but the symbol) race on it — serialize them.
+ *  - Every call shares the array; calls whose work overlaps on the GPU
+ *    (different streams, or devices sharing nothing but the symbol) race on
+ *    it — serialize them.
  *  - Returns NT_OK once the work is enqueued; a device-side wait that runs out
  *    is recorded only in the array, not reported. */
 nt_status nt_attn_decode_static(const float* q_dev, const void* kcache_dev, const void* vcache_dev, float* out_dev,
