@@ -760,11 +760,14 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """The largest of every rank's v (the slowest rank's time); the tensor
+    lives where the process group's backend reduces (GPU for NCCL)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
