@@ -400,6 +400,12 @@ def bench_prefill(args, rank, world):
 
 SAMPLER = (0.8, 0.9)  # temperature, top-p of the "_sample" workloads
 
+# The pages' own decode throughput for a workload, where they print one: Llama
+# 8B Q8_0 with custom CUDA kernels on an RTX 3090 ("Ntransformer",
+# en.unwiki.net, roadmap: phase 1).  Another machine's number, so vs_baseline
+# is context, not a target.
+PAGE_TOK_S = {"llama8b_q8_0": 48.9}
+
 
 def parse_decode(name):
     """<model>[_skip<N>][_spec<K>][_sample]: a synthetic model, optionally
@@ -536,10 +542,12 @@ def bench_decode(args, rank, world):
     per_step_bytes = step_bytes(spec, skip)
     n_exec = spec.n_layers - (int(np.sum(skip)) if skip is not None else 0)
     kernels_per_step = 2 + n_exec * (4 + len({spec.fmt[t] for t in ("wq", "wk", "wv")})) + (6 if sampled else 1)
+    page = PAGE_TOK_S.get(args.workload)
     line = {
         "metric": METRIC, "value": round(tok_s * world, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (block-quantized weights, f16 KV)",
+        "scaling": "weak", "vs_baseline": round(tok_s * world / page, 3) if page else None,
+        "dtype": "f32 (block-quantized weights, f16 KV)",
         "data": "synthetic: random weights of the named shape, seeded", "impl": "ours",
         "config": {"workload": args.workload, "layers": spec.n_layers, "layers_executed": n_exec,
                    "d_model": spec.d_model, "ffn": spec.ffn,
