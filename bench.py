@@ -541,7 +541,9 @@ def bench_decode(args, rank, world):
 
     per_step_bytes = step_bytes(spec, skip)
     n_exec = spec.n_layers - (int(np.sum(skip)) if skip is not None else 0)
-    kernels_per_step = 2 + n_exec * (4 + len({spec.fmt[t] for t in ("wq", "wk", "wv")})) + (6 if sampled else 1)
+    # embedding + LM head, per layer Q/K/V (one per format) + attention (split, combine) + O + gate/up + down,
+    # then the argmax (or the six sampler launches)
+    kernels_per_step = 2 + n_exec * (5 + len({spec.fmt[t] for t in ("wq", "wk", "wv")})) + (6 if sampled else 1)
     page = PAGE_TOK_S.get(args.workload)
     line = {
         "metric": METRIC, "value": round(tok_s * world, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
@@ -715,12 +717,13 @@ def bench_streamed(args, rank, world):
         "host_generation_s": round(t_gen, 1),
     }
     n_exec = spec.n_layers
-    per_layer = 4 + len({spec.fmt[t] for t in ("wq", "wk", "wv")})
+    per_layer = 5 + len({spec.fmt[t] for t in ("wq", "wk", "wv")})  # Q/K/V, attention (2), O, gate/up, down
     if k:
         # per pass: setup, k drafts (resident layers), verify (GEMM + epilogue per GEMV, attention), accept
         n_res = spec.n_resident
         draft = 2 + n_res * per_layer + (6 if sampled else 1)
-        verify = 1 + n_exec * (2 * (per_layer - 1) + 1) + 2 + (6 if sampled else k + 1)
+        # every verify GEMM is two launches (the GEMM and its epilogue); attention is split + combine
+        verify = 1 + n_exec * (2 * (per_layer - 2) + 2) + 2 + (6 if sampled else k + 1)
         line["gpu_launches"] = args.steps * (2 + k * draft + verify)
     else:
         line["gpu_launches"] = (args.steps * (2 + n_exec * per_layer + (6 if sampled else 1))
