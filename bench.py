@@ -324,7 +324,7 @@ def bench_attn(args, rank, world):
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4), "peak_kind": kind, "traffic": None,
                          "algo_bytes_per_launch": kv_bytes},
-            "gpu_launches": args.steps, "clocks": clk.summary()}
+            "gpu_launches": 2 * args.steps, "clocks": clk.summary()}  # split + combine per call
 
 
 # ---------------------------------------------------------------------------
