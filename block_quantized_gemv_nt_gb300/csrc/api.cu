@@ -4,6 +4,9 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <chrono>
+#include <thread>
+
 #include "nt_internal.cuh"
 #include "ops.cuh"
 
@@ -155,13 +158,10 @@ nt_status nt_ctx_destroy(nt_ctx* ctx) {
   return NT_OK;
 }
 
-nt_status nt_ctx_sync(nt_ctx* ctx) {
-  if (!ctx) return NT_ERR_INVALID_ARG;
-  DeviceGuard g(ctx->device);
-  cudaError_t e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) return cuda_check(ctx, e, "device synchronize");
+// the device error flag, read and cleared after the work that may set it has finished
+static nt_status take_device_flag(nt_ctx* ctx) {
   unsigned flag = 0;
-  e = cudaMemcpy(&flag, ctx->err_flag, sizeof flag, cudaMemcpyDeviceToHost);
+  cudaError_t e = cudaMemcpy(&flag, ctx->err_flag, sizeof flag, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_check(ctx, e, "read device error flag");
   if (flag) {
     cudaMemset(ctx->err_flag, 0, sizeof(unsigned));
@@ -170,6 +170,53 @@ nt_status nt_ctx_sync(nt_ctx* ctx) {
     return set_err(ctx, NT_ERR_INVALID_ARG, "a device-side position ran past the KV cache (flag 0x%x)", flag);
   }
   return NT_OK;
+}
+
+nt_status nt_ctx_sync(nt_ctx* ctx) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_check(ctx, e, "device synchronize");
+  return take_device_flag(ctx);
+}
+
+nt_status nt_stream_sync(nt_ctx* ctx, void* stream, int64_t timeout_us) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  NT_REQUIRE(timeout_us >= 0, NT_ERR_INVALID_ARG, "negative timeout");
+  DeviceGuard g(ctx->device);
+  const cudaStream_t st = as_stream(stream);
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    const cudaError_t e = cudaStreamQuery(st);
+    if (e == cudaSuccess) break;
+    if (e != cudaErrorNotReady) return cuda_check(ctx, e, "stream query");
+    const auto us = std::chrono::duration_cast<std::chrono::microseconds>(std::chrono::steady_clock::now() - t0);
+    if (us.count() >= timeout_us) {
+      cudaGetLastError();
+      return set_err(ctx, NT_ERR_TIMEOUT, "stream still busy after %lld us", (long long)timeout_us);
+    }
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+  return take_device_flag(ctx);
+}
+
+nt_status nt_debug_fail_copy(nt_ctx* ctx, int nth) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  NT_REQUIRE(nth >= -1, NT_ERR_INVALID_ARG, "nth must be -1 (off) or >= 0");
+  ctx->copy_fail_in = nth;
+  return NT_OK;
+}
+
+static void CUDART_CB host_delay_fn(void* us) {
+  std::this_thread::sleep_for(std::chrono::microseconds(reinterpret_cast<intptr_t>(us)));
+}
+
+nt_status nt_debug_host_delay(nt_ctx* ctx, void* stream, int64_t us) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  NT_REQUIRE(us >= 0 && us <= 10000000, NT_ERR_INVALID_ARG, "delay outside 0..10 s");
+  DeviceGuard g(ctx->device);
+  return cuda_check(ctx, cudaLaunchHostFunc(as_stream(stream), host_delay_fn, reinterpret_cast<void*>(intptr_t(us))),
+                    "host delay");
 }
 
 const char* nt_last_error(const nt_ctx* ctx) { return ctx ? ctx->last_error.c_str() : g_create_error.c_str(); }

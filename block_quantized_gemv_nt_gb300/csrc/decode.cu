@@ -125,6 +125,8 @@ void bind_slot(const nt_model* m, int slot, nt_layer_ptrs& L) {
 
 // the copy step of the streaming engine: layer blob host -> HBM slot on st
 nt_status copy_layer(Ctx* c, nt_model* m, int layer, const void* src, int slot, cudaStream_t st) {
+  if (c->copy_fail_in >= 0 && c->copy_fail_in-- == 0)  // fault injection (host side): nothing is enqueued
+    return set_err(c, NT_ERR_CUDA, "layer %d copy into slot %d: injected failure", layer, slot);
   nt_status s = cuda_check(c, cudaMemcpyAsync(slot_ptr(m, slot), src, m->blob_bytes, cudaMemcpyHostToDevice, st),
                            "stream layer copy");
   if (!s) m->slot_layer[slot] = layer;
@@ -142,7 +144,17 @@ struct Streamer {
   nt_model* m;
   cudaStream_t st;
   std::vector<int> sl;
-  int si = 0;  // ordinal of the next streamed layer
+  int si = 0;           // ordinal of the next streamed layer
+  bool forked = false;  // the copy stream waits on st and must be joined back
+
+  // a pass cut short by an error still joins the copy stream, so a stream
+  // capture in progress ends cleanly
+  ~Streamer() {
+    if (forked) {
+      cudaEventRecord(m->ev_join, m->copy_st);
+      cudaStreamWaitEvent(st, m->ev_join, 0);
+    }
+  }
 
   nt_status copy(int i) {
     if (c->dry) return NT_OK;
@@ -159,6 +171,7 @@ struct Streamer {
     if (sl.empty() || c->dry) return NT_OK;
     nt_status s = cuda_check(c, cudaEventRecord(m->ev_fork, st), "fork copy stream");
     if (!s) s = cuda_check(c, cudaStreamWaitEvent(m->copy_st, m->ev_fork, 0), "fork copy stream");
+    forked = !s;
     for (int i = 0; i < m->n_slots && i < int(sl.size()) && !s; ++i) s = copy(i);
     return s;
   }
@@ -187,6 +200,7 @@ struct Streamer {
   }
   nt_status end() {
     if (sl.empty() || c->dry) return NT_OK;
+    forked = false;
     nt_status s = cuda_check(c, cudaEventRecord(m->ev_join, m->copy_st), "join copy stream");
     if (!s) s = cuda_check(c, cudaStreamWaitEvent(st, m->ev_join, 0), "join copy stream");
     return s;
@@ -591,15 +605,20 @@ nt_status run_graph(Ctx* c, nt_model* m, const std::string& key, cudaStream_t st
     }
     cudaGraph_t g = nullptr;
     cudaGraphExec_t ge = nullptr;
+    const std::vector<int> slots_before = m->slot_layer;  // a failed capture copies nothing
     s = cuda_check(c, cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeThreadLocal), "begin capture");
     if (!s) {
       nt_status s2 = enqueue(m->cap);
       cudaError_t e = cudaStreamEndCapture(m->cap, &g);
+      if (s2 && e != cudaSuccess) cudaGetLastError();  // the first error is the one reported
       s = s2 ? s2 : cuda_check(c, e, "end capture");
     }
     if (!s) s = cuda_check(c, cudaGraphInstantiate(&ge, g, 0), "graph instantiate");
     if (g) cudaGraphDestroy(g);
-    if (s) return s;
+    if (s) {
+      m->slot_layer = slots_before;
+      return s;
+    }
     it = m->graphs.emplace(key, ge).first;
   }
   return cuda_check(c, cudaGraphLaunch(it->second, st), "graph launch");

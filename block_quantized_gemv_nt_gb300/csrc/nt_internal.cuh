@@ -36,6 +36,7 @@ struct Ctx {
   unsigned* err_flag = nullptr; // device word, set by kernels whose bounded wait ran out
   bool pdl = true;               // launch with programmatic stream serialization
   mutable bool pdl_hold = false; // the next launch waits for everything before it (set after an event wait)
+  int copy_fail_in = -1;         // fault injection: the copy_fail_in-th following layer copy fails (-1: none)
   int gemv_warps = 16;           // quant-GEMV launch shape (tuning knobs, env NT_GEMV_*)
   int gemv_stages = 2;
   int gemv_stage_max = 12288;

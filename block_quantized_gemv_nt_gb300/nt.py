@@ -109,6 +109,9 @@ _sig("nt_gemm_q", [_vp, _ci, _vp, _vp, _vp, _i64, _i64, _ci, _vp, _vp, _cf, _vp]
 _sig("nt_attn_verify", [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _i64, _ci, _i64, _vp])
 _sig("nt_stream_layer", [_vp, _vp, _ci, _vp, _sz, _ci, _vp])
 _sig("nt_model_slot", [_vp, _vp, _ci, ctypes.POINTER(_vp), ctypes.POINTER(_sz), ctypes.POINTER(_ci)])
+_sig("nt_stream_sync", [_vp, _vp, _i64])
+_sig("nt_debug_fail_copy", [_vp, _ci])
+_sig("nt_debug_host_delay", [_vp, _vp, _i64])
 
 EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "nt_block_bytes", "nt_block_elems",
             "nt_dequant_rows", "nt_gemv_q", "nt_gemv_q_swiglu", "nt_gemv_q_multi", "nt_rmsnorm", "nt_rope",
@@ -116,7 +119,7 @@ EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "
             "nt_model_init", "nt_model_destroy", "nt_decode_step", "nt_layer_skip_calibrate",
             "nt_attn_decode_static", "nt_layer_blob_layout", "nt_stream_layer", "nt_model_slot", "nt_spec_step",
             "nt_gemm_q", "nt_attn_verify", "nt_plan_residency", "nt_prefill", "nt_sample", "nt_model_set_sampler",
-            "nt_host_register", "nt_host_unregister"]
+            "nt_host_register", "nt_host_unregister", "nt_stream_sync", "nt_debug_fail_copy", "nt_debug_host_delay"]
 
 
 def lib():
@@ -269,6 +272,21 @@ def nt_host_register(ctx, host_ptr: int, nbytes: int, read_only: bool = True):
 
 def nt_host_unregister(ctx, host_ptr: int):
     return ctx.check(_lib.nt_host_unregister(ctx.handle, host_ptr))
+
+
+def nt_stream_sync(ctx, stream, timeout_us: int):
+    """Wait at most timeout_us for `stream`; NtError(NT_ERR_TIMEOUT) when it stays busy."""
+    return ctx.check(_lib.nt_stream_sync(ctx.handle, _stream(stream), timeout_us))
+
+
+def nt_debug_fail_copy(ctx, nth: int):
+    """Fault injection (host side): the nth following layer copy fails; -1 disarms."""
+    return ctx.check(_lib.nt_debug_fail_copy(ctx.handle, nth))
+
+
+def nt_debug_host_delay(ctx, stream, us: int):
+    """A host callback that keeps `stream` busy for `us` microseconds."""
+    return ctx.check(_lib.nt_debug_host_delay(ctx.handle, _stream(stream), us))
 
 
 def nt_sample(ctx, logits, n: int, temperature: float, top_p: float, seed: int, counter: int, out, stream=None):

@@ -83,6 +83,23 @@ nt_status nt_ctx_destroy(nt_ctx* ctx);
  * held on the device (a decode step continued with token < 0) ran past the
  * KV cache — the kernels then wrote nothing outside the caches. */
 nt_status nt_ctx_sync(nt_ctx* ctx);
+/* Wait at most timeout_us for the work enqueued on `stream` to finish (a
+ * host-side poll with a deadline), then report like nt_ctx_sync:
+ * NT_ERR_TIMEOUT when the deadline passes first (the work is not
+ * cancelled; call again to keep waiting), else the device-side error flag
+ * (bounded-wait timeout or position out of range), cleared when read. */
+nt_status nt_stream_sync(nt_ctx* ctx, void* stream, int64_t timeout_us);
+/* Fault injection for the streaming engine's tests (host side only; nothing
+ * is ever made to fail on the GPU): the nth following request to copy a
+ * layer blob into an HBM slot (nth = 0: the next one; counted over
+ * nt_stream_layer and the copies a decode step enqueues) returns
+ * NT_ERR_CUDA with nothing enqueued.  A decode step whose capture hits it
+ * returns the error, keeps no graph and leaves the slot bookkeeping as it
+ * was; the next call captures again.  nth = -1 disarms it. */
+nt_status nt_debug_fail_copy(nt_ctx* ctx, int nth);
+/* Test helper: a host callback on `stream` that sleeps `us` microseconds
+ * (0..10 s), so that the stream stays busy without any GPU work. */
+nt_status nt_debug_host_delay(nt_ctx* ctx, void* stream, int64_t us);
 const char* nt_last_error(const nt_ctx* ctx);
 /* Bytes per block / elements per block of a format (0 for an unknown id). */
 int nt_block_bytes(int fmt);
