@@ -256,12 +256,14 @@ nt_status nt_gemv_q_multi(nt_ctx* ctx, int fmt, const nt_gemv_job* jobs, int njo
 
 nt_status nt_gemv_q(nt_ctx* ctx, int fmt, const void* W, const float* x, float* y, int64_t rows, int64_t cols,
                     const float* residual, void* stream) {
+  NvtxRange nvtx_range("nt_gemv_q");
   nt_gemv_job j{W, y, residual, rows};
   return nt_gemv_q_multi(ctx, fmt, &j, 1, x, nullptr, 0.f, cols, stream);
 }
 
 nt_status nt_gemm_q(nt_ctx* ctx, int fmt, const void* W, const float* X, float* Y, int64_t rows, int64_t cols, int M,
                     const float* residual, const float* norm_g, float eps, void* stream) {
+  NvtxRange nvtx_range("nt_gemm_q");
   NT_TRY(pre_call(ctx));
   NT_TRY(check_fmt_cols(ctx, fmt, cols));
   NT_REQUIRE(M >= 1 && M <= kMaxVerify, NT_ERR_INVALID_ARG, "M must be 1..%d", kMaxVerify);
@@ -364,6 +366,7 @@ nt_status attn_entry(nt_ctx* ctx, const float* q, const void* kc, const void* vc
 
 nt_status nt_attn_decode(nt_ctx* ctx, const float* q, const void* kc, const void* vc, float* out, int n_qh,
                          int n_kvh, int head_dim, int64_t n_pos, int64_t kv_stride, void* stream) {
+  NvtxRange nvtx_range("nt_attn_decode");
   return attn_entry(ctx, q, kc, vc, out, n_qh, n_kvh, head_dim, n_pos, 1, kv_stride, stream);
 }
 
@@ -398,6 +401,7 @@ nt_status nt_argmax(nt_ctx* ctx, const float* v, int64_t n, int32_t* out, void* 
 
 nt_status nt_sample(nt_ctx* ctx, const float* z, int64_t n, float T, float P, uint64_t seed, uint64_t counter,
                     int32_t* out, void* stream) {
+  NvtxRange nvtx_range("nt_sample");
   NT_TRY(pre_call(ctx));
   NT_REQUIRE(z && out && n >= 1 && n <= kSampMaxN, NT_ERR_INVALID_ARG, "null pointer or n outside 1..%lld",
              (long long)kSampMaxN);

@@ -229,8 +229,11 @@ nt_status enqueue_step(Ctx* c, nt_model* m, const uint8_t* skip, const StepIO& i
   if (s) return s;
   s = launch_embed(c, d.fmt_embd, m->embd, d.d_model, io.tok, m->x, st);
   if (s) return s;
+  char lname[24];
   for (int l = 0; l < d.n_layers; ++l) {
     if (skip && skip[l]) continue;
+    snprintf(lname, sizeof lname, "layer %d", l);
+    NvtxRange layer_range(lname);
     nt_layer_ptrs L;
     int slot;
     s = sm.before(l, L, slot);
@@ -638,6 +641,7 @@ extern "C" {
 
 nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_ptrs* layers, const void* embd,
                         const void* out, const float* out_norm, nt_model** res) {
+  NvtxRange nvtx_range("nt_model_init");
   if (!ctx) return NT_ERR_INVALID_ARG;
   NT_REQUIRE(desc && layers && embd && out && out_norm && res, NT_ERR_INVALID_ARG, "null pointer");
   const nt_model_desc& d = *desc;
@@ -828,6 +832,7 @@ nt_status nt_model_destroy(nt_ctx* ctx, nt_model* m) {
 
 nt_status nt_decode_step(nt_ctx* ctx, nt_model* m, int32_t token, int64_t pos, const uint8_t* skip, float* logits,
                          int32_t* next_tok, void* stream) {
+  NvtxRange nvtx_range("nt_decode_step");
   if (!ctx) return NT_ERR_INVALID_ARG;
   NT_REQUIRE(m && logits, NT_ERR_INVALID_ARG, "null model or logits");
   NT_REQUIRE(aligned(logits, 16), NT_ERR_ALIGNMENT, "logits must be 16-byte aligned");
@@ -856,6 +861,7 @@ nt_status nt_decode_step(nt_ctx* ctx, nt_model* m, int32_t token, int64_t pos, c
 
 nt_status nt_layer_skip_calibrate(nt_ctx* ctx, nt_model* m, int32_t token, int64_t pos, int n_skip, uint8_t* mask,
                                   float* cos_host, float* logits, int32_t* next_tok, void* stream) {
+  NvtxRange nvtx_range("nt_layer_skip_calibrate");
   if (!ctx) return NT_ERR_INVALID_ARG;
   NT_REQUIRE(m && mask && logits, NT_ERR_INVALID_ARG, "null pointer");
   NT_REQUIRE(n_skip >= 0 && n_skip <= m->d.n_layers, NT_ERR_INVALID_ARG, "n_skip outside 0..n_layers");
@@ -887,6 +893,7 @@ nt_status nt_layer_skip_calibrate(nt_ctx* ctx, nt_model* m, int32_t token, int64
 
 nt_status nt_spec_step(nt_ctx* ctx, nt_model* m, int32_t token, int64_t pos, int k, int n_draft_layers,
                        int32_t* tokens_out, int32_t* n_out, float* logits, void* stream) {
+  NvtxRange nvtx_range("nt_spec_step");
   if (!ctx) return NT_ERR_INVALID_ARG;
   NT_REQUIRE(m && tokens_out && n_out, NT_ERR_INVALID_ARG, "null model or outputs");
   NT_REQUIRE(k >= 1 && k < kMaxVerify, NT_ERR_INVALID_ARG, "k must be 1..%d", kMaxVerify - 1);
@@ -937,6 +944,7 @@ nt_status nt_layer_blob_layout(const nt_model_desc* d, size_t* off, size_t* byte
 
 nt_status nt_prefill(nt_ctx* ctx, nt_model* m, const int32_t* tokens_host, int64_t n, int64_t pos0, float* logits,
                      int32_t* next_tok, void* stream) {
+  NvtxRange nvtx_range("nt_prefill");
   if (!ctx) return NT_ERR_INVALID_ARG;
   NT_REQUIRE(m && tokens_host && logits, NT_ERR_INVALID_ARG, "null model, tokens or logits");
   NT_REQUIRE(aligned(logits, 16), NT_ERR_ALIGNMENT, "logits must be 16-byte aligned");
@@ -1025,6 +1033,7 @@ nt_status nt_plan_residency(const nt_model_desc* d, size_t budget, int embd_in_h
 
 nt_status nt_stream_layer(nt_ctx* ctx, nt_model* m, int layer, const void* src, size_t bytes, int slot,
                           void* copy_stream) {
+  NvtxRange nvtx_range("nt_stream_layer");
   if (!ctx) return NT_ERR_INVALID_ARG;
   NT_REQUIRE(m && src, NT_ERR_INVALID_ARG, "null model or source");
   NT_REQUIRE(m->n_slots > 0, NT_ERR_INVALID_ARG, "the model streams no layer");

@@ -2,6 +2,7 @@
 // helpers, and the inline-PTX wrappers for mbarriers and TMA bulk copies.
 #pragma once
 
+#include <nvtx3/nvToolsExt.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -50,6 +51,15 @@ struct Ctx {
   std::map<std::string, PlanChoice> gemv_plans;  // tuned plan per launch shape
   char* flush = nullptr;         // read before each timed tuning launch so its weights come from HBM
   size_t flush_bytes = 0;
+};
+
+// an NVTX range over a host-side call (visible in a profiler timeline; next to
+// free when no tool is attached)
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
 // host-side status helpers ----------------------------------------------------
