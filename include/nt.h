@@ -32,6 +32,11 @@
  *    are host pointers.  The caller owns every weight, activation, KV-cache
  *    and output buffer; the context owns only its scratch, events, side
  *    streams and captured graphs.
+ *  - A context, and every model made on it, is used from one host thread at
+ *    a time (its tuning state, scratch and per-call settings are shared);
+ *    separate contexts are independent.  Work from calls on one context that
+ *    share scratch (the standalone kernels, the sampler) must not overlap
+ *    on the GPU: keep it on one stream or order the streams.
  *  - Block-quantized matrices are row-major: row r is cols/block_elems
  *    consecutive blocks.  cols must be a multiple of the format's block size
  *    (32 for Q8_0/Q4_0/F16/F32, 256 for Q4_K/Q5_K/Q6_K).  Block bytes: Q8_0
