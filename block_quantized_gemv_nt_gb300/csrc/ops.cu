@@ -117,7 +117,6 @@ __global__ void rope_append_kernel(float* q, const float* k, const float* v, __h
 constexpr int kAttnThreads = 256;
 constexpr int kTiles = 4;  // 32-position tiles per chunk (kMaxChunk / 32)
 constexpr int kHD = 128;
-constexpr int kMaxGroup = 16;
 constexpr int kMaxChunk = 128;
 
 struct AttnArgs {
