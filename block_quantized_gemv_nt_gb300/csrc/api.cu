@@ -70,7 +70,8 @@ nt_status check_vec(nt_ctx* ctx, const void* p, const char* name) {
   return NT_OK;
 }
 
-// surface a pending device error flag / sticky CUDA error before new work
+// every entry point's first check: a context is required (device error flags
+// are read by nt_ctx_sync / nt_stream_sync, after the work that sets them)
 nt_status pre_call(nt_ctx* ctx) {
   if (!ctx) return NT_ERR_INVALID_ARG;
   return NT_OK;
@@ -315,6 +316,7 @@ nt_status nt_rope(nt_ctx* ctx, float* q, float* k, int n_qh, int n_kvh, int head
   NT_REQUIRE(q && n_qh > 0 && (!k || n_kvh > 0), NT_ERR_INVALID_ARG, "bad q/k or head counts");
   NT_REQUIRE(head_dim > 0 && head_dim % 2 == 0 && head_dim <= 512, NT_ERR_INVALID_ARG, "head_dim must be even, <= 512");
   NT_REQUIRE(pos >= 0 && theta > 0.f, NT_ERR_INVALID_ARG, "pos must be >= 0 and theta > 0");
+  NT_REQUIRE(aligned(q, 4) && aligned(k, 4), NT_ERR_ALIGNMENT, "q and k must be 4-byte aligned");
   DeviceGuard g(ctx->device);
   return launch_rope(ctx, q, k, n_qh, n_kvh, head_dim, pos, theta, as_stream(stream));
 }
@@ -328,6 +330,7 @@ nt_status nt_rope_kv_append(nt_ctx* ctx, float* q, const float* k, const float* 
   NT_REQUIRE(pos >= 0 && pos < kv_stride, NT_ERR_INVALID_ARG, "pos=%lld outside the cache (stride %lld)",
              (long long)pos, (long long)kv_stride);
   NT_REQUIRE(aligned(kc, 2) && aligned(vc, 2), NT_ERR_ALIGNMENT, "caches must be 2-byte aligned");
+  NT_REQUIRE(aligned(q, 4) && aligned(k, 4) && aligned(v, 4), NT_ERR_ALIGNMENT, "q, k and v must be 4-byte aligned");
   DeviceGuard g(ctx->device);
   return launch_rope_append(ctx, q, k, v, kc, vc, n_qh, n_kvh, head_dim, pos, nullptr, kv_stride, theta,
                             as_stream(stream));
@@ -378,6 +381,7 @@ nt_status nt_attn_verify(nt_ctx* ctx, const float* q, const void* kc, const void
 nt_status nt_softmax(nt_ctx* ctx, const float* x, float* y, int64_t n, void* stream) {
   NT_TRY(pre_call(ctx));
   NT_REQUIRE(x && y && n > 0, NT_ERR_INVALID_ARG, "null pointer or n <= 0");
+  NT_REQUIRE(aligned(x, 4) && aligned(y, 4), NT_ERR_ALIGNMENT, "vectors must be 4-byte aligned");
   DeviceGuard g(ctx->device);
   return launch_softmax(ctx, x, y, n, as_stream(stream));
 }
@@ -385,6 +389,7 @@ nt_status nt_softmax(nt_ctx* ctx, const float* x, float* y, int64_t n, void* str
 nt_status nt_swiglu(nt_ctx* ctx, const float* gate, const float* up, float* h, int64_t n, void* stream) {
   NT_TRY(pre_call(ctx));
   NT_REQUIRE(gate && up && h && n >= 0, NT_ERR_INVALID_ARG, "null pointer or n < 0");
+  NT_REQUIRE(aligned(gate, 4) && aligned(up, 4) && aligned(h, 4), NT_ERR_ALIGNMENT, "vectors must be 4-byte aligned");
   if (n == 0) return NT_OK;
   DeviceGuard g(ctx->device);
   return launch_swiglu(ctx, gate, up, h, n, as_stream(stream));
@@ -437,6 +442,7 @@ nt_status nt_host_unregister(nt_ctx* ctx, const void* p) {
 nt_status nt_cos_sim(nt_ctx* ctx, const float* a, const float* b, int64_t n, float* out, void* stream) {
   NT_TRY(pre_call(ctx));
   NT_REQUIRE(a && b && out && n > 0, NT_ERR_INVALID_ARG, "null pointer or n <= 0");
+  NT_REQUIRE(aligned(a, 4) && aligned(b, 4) && aligned(out, 4), NT_ERR_ALIGNMENT, "vectors must be 4-byte aligned");
   DeviceGuard g(ctx->device);
   return launch_cos(ctx, a, b, n, out, as_stream(stream));
 }

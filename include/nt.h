@@ -25,9 +25,10 @@
  *    a call that fails its checks launches nothing and leaves outputs as they
  *    were.  nt_last_error(ctx) then holds a one-line reason.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
- *    stream).  Calls only enqueue work; device-side faults and the device
- *    error flag (a bounded wait inside a kernel that ran out) surface at
- *    nt_ctx_sync() or at the next call on the context.
+ *    stream).  Calls only enqueue work.  The device error flag (a bounded
+ *    wait inside a kernel that ran out, a device-held position past the KV
+ *    cache) is read and cleared by nt_ctx_sync() and nt_stream_sync(); a
+ *    CUDA fault also fails the next launch on the context.
  *  - Pointers named *_dev are device (HBM) pointers; pointers named *_host
  *    are host pointers.  The caller owns every weight, activation, KV-cache
  *    and output buffer; the context owns only its scratch, events, side
@@ -45,7 +46,8 @@
  *  - Weight pointers must be 2-byte aligned.  When the weight pointer is
  *    16-byte aligned and each row is a multiple of 16 bytes, weights stream
  *    through TMA bulk copies; otherwise a slower plain-load path runs.
- *  - fp32 vectors must be 16-byte aligned.
+ *  - fp32 vectors must be 4-byte aligned; the GEMV / GEMM inputs (x, X),
+ *    the norm gains and the attention q and out 16-byte aligned.
  */
 #ifndef NT_H
 #define NT_H
