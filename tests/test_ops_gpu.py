@@ -164,3 +164,28 @@ def test_cos_sim(ctx):
     nt.nt_cos_sim(ctx, dev(a), dev(b), 8192, out)
     torch.cuda.synchronize()
     assert abs(float(host(out)[0]) - oracle.cos_sim(a, b)) <= 1e-6
+
+
+def test_small_ops_reject_misaligned_vectors(ctx):
+    """A float pointer off its 4-byte boundary is refused on the host with
+    NT_ERR_ALIGNMENT; nothing is launched and the output keeps its bytes."""
+    nt = _nt()
+    buf = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    good, bad = buf.data_ptr(), buf.data_ptr() + 2
+    calls = [
+        lambda p: nt.nt_softmax(ctx, p, good, 16),
+        lambda p: nt.nt_softmax(ctx, good, p, 16),
+        lambda p: nt.nt_swiglu(ctx, p, good, good + 1024, 16),
+        lambda p: nt.nt_swiglu(ctx, good, good, p, 16),
+        lambda p: nt.nt_cos_sim(ctx, p, good, 16, good + 1024),
+        lambda p: nt.nt_cos_sim(ctx, good, good, 16, p),
+        lambda p: nt.nt_rmsnorm(ctx, p, good, good + 1024, 16, 1e-5),
+        lambda p: nt.nt_rope(ctx, p, None, 1, 1, 128, 3, 10000.0),
+        lambda p: nt.nt_rope(ctx, good, p, 1, 1, 128, 3, 10000.0),
+    ]
+    for call in calls:
+        with pytest.raises(nt.NtError) as ei:
+            call(bad)
+        assert ei.value.status == nt.NT_ERR_ALIGNMENT
+    torch.cuda.synchronize()
+    assert int(buf.count_nonzero().item()) == 0
