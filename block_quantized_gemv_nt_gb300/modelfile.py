@@ -114,22 +114,38 @@ class ModelFile:
 
     def __init__(self, path: str):
         self.path = path
-        self._fd = os.open(path, os.O_RDONLY)
-        size = os.fstat(self._fd).st_size
-        self._mm = mmap.mmap(self._fd, size, prot=mmap.PROT_READ)
-        buf = np.frombuffer(self._mm, dtype=np.uint8)
-        if bytes(buf[:4]) != MAGIC:
+        with open(path, "rb") as f:
+            head = f.read(16)
+        if len(head) < 16 or head[:4] != MAGIC:
             raise ValueError(f"{path}: not a model file")
-        version, hlen = struct.unpack("<IQ", bytes(buf[4:16]))
+        version, hlen = struct.unpack("<IQ", head[4:16])
         if version != VERSION:
             raise ValueError(f"{path}: version {version}")
-        meta = json.loads(bytes(buf[16:16 + hlen]).decode())
+        self._fd = os.open(path, os.O_RDONLY)
+        try:
+            self._open(path, hlen)
+        except Exception:
+            self.close()
+            raise
+
+    def _open(self, path: str, hlen: int) -> None:
+        size = os.fstat(self._fd).st_size
+        if 16 + hlen > size:
+            raise ValueError(f"{path}: header runs past the end of the file")
+        self._mm = mmap.mmap(self._fd, size, prot=mmap.PROT_READ)
+        meta = json.loads(self._mm[16:16 + hlen].decode())
         self.spec = FileSpec(meta["spec"])
         self.blob_offsets, self.blob_bytes = meta["blob_offsets"], meta["blob_bytes"]
         self.data0 = _up(16 + hlen)
-        self._buf = buf
         self.entries = {k: (self.data0 + v[0], v[1]) for k, v in meta["entries"].items()}
+        # every entry page-aligned and, rounded up to whole pages (what page-locking covers), inside the file
+        for name, (off, n) in self.entries.items():
+            if off % ALIGN or n < 0 or off + _up(n) > size:
+                raise ValueError(f"{path}: entry {name} ({off}, {n} bytes) is misaligned or past the end")
         s = self.spec
+        if any(self.entries[f"blob.{li}"][1] < self.blob_bytes for li in range(s.n_layers)):
+            raise ValueError(f"{path}: a layer blob is shorter than the blob layout")
+        self._buf = buf = np.frombuffer(self._mm, dtype=np.uint8)
 
         def view(name, dtype=np.uint8, shape=None):
             off, n = self.entries[name]
@@ -163,7 +179,8 @@ class ModelFile:
         self.layers = []
         self._buf = None
         try:
-            self._mm.close()
+            if hasattr(self, "_mm"):
+                self._mm.close()
         except BufferError:
             pass  # views still alive elsewhere: the mapping closes with them
         os.close(self._fd)

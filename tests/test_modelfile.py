@@ -34,3 +34,20 @@ def test_rejects_other_files(tmp_path):
     p.write_bytes(b"GGUF" + bytes(60))
     with pytest.raises(ValueError):
         modelfile.ModelFile(str(p))
+
+
+def test_rejects_truncated_files(tmp_path):
+    """A file cut short (past its header, inside its data) is refused before
+    any entry is viewed or page-locked."""
+    from block_quantized_gemv_nt_gb300 import modelfile
+    spec = synth.model_spec("tiny_q8_0")
+    hm = synth.make_host_model(spec, with_kv=False)
+    path = tmp_path / "m.ntq"
+    modelfile.write_model(str(path), spec, hm)
+    data = path.read_bytes()
+    for cut in (10, 40, len(data) - 4096):
+        p = tmp_path / f"cut{cut}.ntq"
+        p.write_bytes(data[:cut])
+        with pytest.raises(ValueError):
+            modelfile.ModelFile(str(p))
+    modelfile.ModelFile(str(path)).close()
