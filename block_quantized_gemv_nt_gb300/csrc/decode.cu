@@ -63,6 +63,8 @@ struct nt_model {
   int64_t* spec_pos = nullptr;         // [kMaxVerify]: pos + i
   int32_t* vtok = nullptr;             // [kMaxVerify]: argmax of each verify row
   int32_t* prompt = nullptr;           // [kv_cap]: prefill tokens
+  std::vector<int32_t> prompt_host;    // the host side of the prompt upload (see nt_prefill)
+  cudaEvent_t ev_prompt = nullptr;     // recorded after that upload
   unsigned long long* vkey = nullptr;  // [kMaxVerify] argmax keys and counters
   unsigned* vcnt = nullptr;
   float *xv = nullptr, *qv = nullptr, *aov = nullptr, *hv = nullptr, *lv = nullptr, *dlogits = nullptr;
@@ -739,6 +741,7 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   cudaError_t e = cudaMalloc(&m->buf, total);
   if (e == cudaSuccess) e = cudaMemset(m->buf, 0, total);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->cap, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_prompt, cudaEventDisableTiming);
   if (e == cudaSuccess && m->n_slots) {
     e = cudaMalloc(&m->slots, size_t(m->n_slots) * m->blob_bytes);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->copy_st, cudaStreamNonBlocking);
@@ -817,7 +820,7 @@ nt_status nt_model_destroy(nt_ctx* ctx, nt_model* m) {
   for (auto& kv : m->graphs) cudaGraphExecDestroy(kv.second);
   if (m->cap) cudaStreamDestroy(m->cap);
   if (m->copy_st) cudaStreamDestroy(m->copy_st);
-  for (cudaEvent_t ev : {m->ev_fork, m->ev_join})
+  for (cudaEvent_t ev : {m->ev_fork, m->ev_join, m->ev_prompt})
     if (ev) cudaEventDestroy(ev);
   for (int i = 0; i < kMaxSlots; ++i) {
     if (m->ev_ready[i]) cudaEventDestroy(m->ev_ready[i]);
@@ -957,9 +960,16 @@ nt_status nt_prefill(nt_ctx* ctx, nt_model* m, const int32_t* tokens_host, int64
   cudaGetDevice(&dev_prev);
   if (dev_prev != ctx->device) cudaSetDevice(ctx->device);
   cudaStream_t st = as_stream(stream);
-  nt_status s = cuda_check(ctx, cudaMemcpyAsync(m->prompt, tokens_host, sizeof(int32_t) * size_t(n),
-                                                cudaMemcpyHostToDevice, st),
-                           "prompt upload");
+  // the upload reads the model's own host copy of the tokens, so the caller's array is free once this call
+  // returns; that copy is rewritten only after the previous upload from it has completed
+  nt_status s = cuda_check(ctx, cudaEventSynchronize(m->ev_prompt), "previous prompt upload");
+  if (!s) {
+    m->prompt_host.assign(tokens_host, tokens_host + n);
+    s = cuda_check(ctx, cudaMemcpyAsync(m->prompt, m->prompt_host.data(), sizeof(int32_t) * size_t(n),
+                                        cudaMemcpyHostToDevice, st),
+                   "prompt upload");
+  }
+  if (!s) s = cuda_check(ctx, cudaEventRecord(m->ev_prompt, st), "prompt upload event");
   for (int64_t base = 0; base < n && !s; base += kMaxVerify) {
     const int M = int(std::min<int64_t>(kMaxVerify, n - base));
     const bool last = base + M == n;

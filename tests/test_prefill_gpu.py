@@ -81,3 +81,39 @@ def test_prefill_bad_args(ctx):
             nt.nt_prefill(ctx, gm.handle, toks, pos0, gm.logits)
         assert ei.value.status == nt.NT_ERR_INVALID_ARG
     gm.close()
+
+
+def test_prefill_tokens_free_on_return(ctx):
+    """The prompt is read before nt_prefill returns, from page-locked memory
+    too: overwriting the caller's array right after the call (the GPU still
+    busy on the stream) changes nothing, and two prefills enqueued back to back
+    on one stream each see their own tokens."""
+    from block_quantized_gemv_nt_gb300 import engine, nt
+    spec = synth.model_spec("tiny_q8_0")
+    hm = synth.make_host_model(spec)
+    a, b = _prompt(spec, 12, 5), _prompt(spec, 12, 6)
+    st = torch.cuda.Stream()
+    ref = []
+    for p in (a, b):
+        g = engine.DeviceModel(ctx, spec, hm)
+        torch.cuda.synchronize()
+        g.prefill(p, 30, stream=st)
+        st.synchronize()
+        ref.append(g.logits.clone())
+        g.close()
+    gm = engine.DeviceModel(ctx, spec, hm)
+    pinned = torch.from_numpy(a.copy()).pin_memory()
+    torch.cuda.synchronize()
+    out = []
+    with torch.cuda.stream(st):
+        nt.nt_debug_host_delay(ctx, st, 100_000)  # keep the stream busy so the upload cannot have run yet
+        for p in (a, b):
+            pinned.numpy()[:] = p
+            ctx.check(nt._lib.nt_prefill(ctx.handle, gm.handle, pinned.data_ptr(), len(p), 30, gm.logits.data_ptr(),
+                                         None, st.cuda_stream))
+            pinned.numpy()[:] = 0
+            out.append(gm.logits.clone())
+    st.synchronize()
+    for g, r in zip(out, ref):
+        assert torch.equal(g, r)
+    gm.close()
