@@ -18,7 +18,8 @@ nt_status launch_rope_append(Ctx* c, float* q, const float* k, const float* v, v
                              cudaStream_t st);
 int attn_splits(const Ctx* c, int n_kvh, int64_t kv_stride);
 int64_t attn_max_stride();
-// counters (kAttnCounterBytes) followed by the partials of nq queries
+// a reserved head of kAttnCounterBytes (unused since the combine became its own
+// launch) followed by the partials of nq queries
 size_t attn_scratch_bytes(int n_qh, int n_kvh, int S, int nq = 1);
 size_t attn_part_floats(int n_qh, int n_kvh, int S);
 // nq queries: query i sees n_pos + i positions (pos_dev set: *pos_dev + 1 + i);
