@@ -779,7 +779,7 @@ def cpu_decode(spec, hm, budget_s=15.0, skip=None):
     dt = time.perf_counter() - t0
     what = "the full model" if skip is None else f"the model with {int(np.sum(skip))} layers skipped"
     return {"value": round(n / dt, 4), "unit": "tok/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} greedy oracle decode steps of {what} in {dt:.1f} s"}
+            "sample": f"{n} greedy oracle decode step{'' if n == 1 else 's'} of {what} in {dt:.1f} s"}
 
 
 # ---------------------------------------------------------------------------
@@ -865,7 +865,7 @@ def reference_arm(args, rank, world):
             "dtype": "f64", "data": "synthetic: random weights of the named shape, seeded", "impl": "reference",
             "config": {"workload": args.workload, "batch": 1},
             "cpu_baseline": {"value": v, "unit": "tok/s", "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": f"{n} greedy oracle decode steps (bounded sample of the workload)"},
+                             "sample": f"{n} greedy oracle decode step{'' if n == 1 else 's'} (bounded sample of the workload)"},
             "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
