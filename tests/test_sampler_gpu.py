@@ -32,7 +32,7 @@ def _valid(z, T, P, u, tok, delta):
     return tok in {oracle.sample(z, T, P, min(max(u + d, 0.0), 1 - 2**-24))[0] for d in (-delta, 0.0, delta)}
 
 
-@pytest.mark.parametrize("n", [7, 1000, 32000, 128256])
+@pytest.mark.parametrize("n", [1, 7, 1000, 32000, 128256])
 def test_sample_matches_oracle(ctx, n):
     from block_quantized_gemv_nt_gb300 import nt
     z = synth.normal_f32(n, seed=3, stream=n % 1000) * 3.0

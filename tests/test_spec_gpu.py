@@ -149,7 +149,7 @@ def _run_spec_vs_oracle(ctx, name, k, n_draft, n_steps):
 
 
 @pytest.mark.parametrize("name,k,n_draft", [("tiny_q8_0", 4, 2), ("tiny_q4_k_m", 4, 3), ("small_q4_k_m", 3, 3),
-                                            ("tiny_q6_k", 7, 1)])
+                                            ("tiny_q6_k", 7, 1), ("tiny_q8_0", 1, 2)])
 def test_spec_step_matches_oracle(ctx, name, k, n_draft):
     emitted, counts, worst, agree, total = _run_spec_vs_oracle(ctx, name, k, n_draft, 4)
     print(f"{name}: tokens/step {counts}, worst max|err|/std {worst:.2e}, agree {agree}/{total}")
