@@ -684,6 +684,7 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
                  "layer %d: set all seven weight pointers, or none and a host blob", l);
       cudaPointerAttributes pa{};
       const cudaError_t pe = cudaPointerGetAttributes(&pa, L.host_blob);
+      if (pe != cudaSuccess) cudaGetLastError();  // a refused query leaves no error behind for later launches
       NT_REQUIRE(pe == cudaSuccess && pa.type == cudaMemoryTypeHost, NT_ERR_INVALID_ARG,
                  "layer %d: host_blob must be page-locked host memory", l);
       ++n_streamed;
