@@ -93,6 +93,8 @@ _sig("nt_decode_step", [_vp, _vp, ctypes.c_int32, _i64, _vp, _vp, _vp, _vp])
 _sig("nt_layer_skip_calibrate", [_vp, _vp, ctypes.c_int32, _i64, _ci, _vp, _vp, _vp, _vp, _vp])
 _sig("nt_attn_decode_static", [_vp, _vp, _vp, _vp, _ci, _ci, _ci, _i64, _i64, _vp])
 _sig("nt_layer_blob_layout", [ctypes.POINTER(nt_model_desc), ctypes.POINTER(_sz), ctypes.POINTER(_sz)])
+
+
 class nt_residency_plan(ctypes.Structure):
     _fields_ = [("n_resident", _ci), ("stream_slots", _ci), ("layer_bytes", _sz), ("fixed_bytes", _sz),
                 ("total_bytes", _sz)]
