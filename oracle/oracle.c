@@ -31,7 +31,10 @@
  * below (each product exact, at most one rounding), every other quantity is
  * fp64.  The KV cache is stored as binary16: fp64 -> fp32 -> f16 (RNE).
  *
- * Parity pins for every function live in tests/test_oracle_*.py.
+ * Parity pins for every function live in tests/test_oracle_*.py.  Parity
+ * unpinned: that the block layouts match real GGUF files byte for byte (no
+ * such file is available; the golden blocks pin the reading, not the files),
+ * and the quality of layer skip (the pages give no measure of it).
  */
 #include <math.h>
 #include <stdint.h>
