@@ -426,6 +426,14 @@ SAMPLER = (0.8, 0.9)  # temperature, top-p of the "_sample" workloads
 PAGE_TOK_S = {"llama8b_q8_0": 48.9}
 
 
+def decode_kernels_per_step(spec, n_exec, sampled=False):
+    """Kernel launches of one decode step: the embedding row and the LM head;
+    per executed layer one Q/K/V GEMV per distinct format, attention (split,
+    combine), O, gate/up and down; then the argmax, or the six sampler
+    launches."""
+    return 2 + n_exec * (5 + len({spec.fmt[t] for t in ("wq", "wk", "wv")})) + (6 if sampled else 1)
+
+
 def parse_decode(name):
     """<model>[_skip<N>][_spec<K>][_sample]: a synthetic model, optionally
     decoding with the N layers of highest calibration cosine skipped, or
@@ -560,9 +568,7 @@ def bench_decode(args, rank, world):
 
     per_step_bytes = step_bytes(spec, skip)
     n_exec = spec.n_layers - (int(np.sum(skip)) if skip is not None else 0)
-    # embedding + LM head, per layer Q/K/V (one per format) + attention (split, combine) + O + gate/up + down,
-    # then the argmax (or the six sampler launches)
-    kernels_per_step = 2 + n_exec * (5 + len({spec.fmt[t] for t in ("wq", "wk", "wv")})) + (6 if sampled else 1)
+    kernels_per_step = decode_kernels_per_step(spec, n_exec, sampled)
     page = PAGE_TOK_S.get(args.workload)
     line = {
         "metric": METRIC, "value": round(tok_s * world, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
