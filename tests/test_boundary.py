@@ -48,3 +48,24 @@ def test_no_gpu_context_fails_loudly():
         pytest.skip("a GPU is present")
     with pytest.raises(nt.NtError):
         nt.Context(0)
+
+
+def test_every_context_call_refuses_a_null_context():
+    """Each entry point that takes a context checks it first: with a NULL
+    context (and every other argument zero or NULL) it returns
+    NT_ERR_INVALID_ARG without touching CUDA, so this runs without a GPU."""
+    from block_quantized_gemv_nt_gb300 import nt
+    no_ctx = {"nt_ctx_create", "nt_last_error", "nt_block_bytes", "nt_block_elems", "nt_attn_decode_static",
+              "nt_layer_blob_layout", "nt_plan_residency"}
+    L = nt.lib()
+    checked = 0
+    for name in nt.EXPORTED:
+        if name in no_ctx:
+            continue
+        f = getattr(L, name)
+        args = [0.0 if t is ctypes.c_float else (0 if t in (ctypes.c_int, ctypes.c_int32, ctypes.c_int64,
+                                                          ctypes.c_uint64, ctypes.c_size_t) else None)
+                for t in f.argtypes]
+        assert f(*args) == nt.NT_ERR_INVALID_ARG, name
+        checked += 1
+    assert checked >= 25
