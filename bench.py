@@ -835,6 +835,28 @@ def reference_arm(args, rank, world):
                 "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                                  "sample": f"{args.steps} full oracle GEMVs"},
                 "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    if args.workload.startswith("attn_"):
+        import oracle
+        H, G, P = (int(v) for v in args.workload.split("_")[1].split("x"))
+        hd = 128
+        K = synth.normal_f16(G * P * hd, 5, 1)
+        V = synth.normal_f16(G * P * hd, 5, 2)
+        q = synth.normal_f32(H * hd, 5, 3).astype(np.float64)
+        kv_bytes = 2 * G * P * hd * 2
+        oracle.attn_decode(q, K, V, H, G, hd, P, P)
+        n = max(1, min(args.steps, args.ref_max_steps))
+        t0 = time.perf_counter()
+        for _ in range(n):
+            oracle.attn_decode(q, K, V, H, G, hd, P, P)
+        dt = (time.perf_counter() - t0) / n
+        v = round(kv_bytes / dt / 1e9, 3)
+        return {"metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world, "steps": n,
+                "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic N(0,1) KV",
+                "impl": "reference", "config": {"workload": args.workload},
+                "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                                 "sample": f"{n} full oracle attention calls"},
+                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     prefill_n, sampled = 0, False
     if "_prefill" in args.workload:
         base, n = args.workload.rsplit("_prefill", 1)
@@ -866,13 +888,16 @@ def reference_arm(args, rank, world):
         tok, pos = nxt, pos + 1
     dt = (time.perf_counter() - t0) / n
     v = round(1.0 / dt, 4)
-    return {"metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world, "steps": n, "warmup": args.warmup,
+    unit = "prompt tok/s" if prefill_n else "tok/s"
+    what = ("prompt tokens fed to the oracle one by one" if prefill_n else
+            "sampled oracle decode steps" if sampled else "greedy oracle decode steps")
+    return {"metric": METRIC, "value": v, "unit": unit, "n_gpus": world, "steps": n, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3, 1), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic: random weights of the named shape, seeded", "impl": "reference",
             "config": {"workload": args.workload, "batch": 1},
-            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": f"{n} greedy oracle decode step{'' if n == 1 else 's'} (bounded sample of the workload)"},
-            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": v, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{n} {what} (bounded sample of the workload)"},
+            "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def main():
