@@ -75,28 +75,22 @@ def pack_qs128(q4):
     return qs
 
 
-def q4_k():
-    d, dmin = 1.0, 0.5
-    q = kq_nibbles()
-    b = le16(HALF[d]) + le16(HALF[dmin]) + pack_scales12(SC, MN) + pack_qs128(q)
-    vals = [d * SC[i // 32] * q[i] - dmin * MN[i // 32] for i in range(256)]
-    return dict(fmt="Q4_K", bytes=b, d=d, dmin=dmin, sc=SC, m=MN, q=q, values=vals)
+def pack_q4_k(d_bits, dmin_bits, sc, mn, q):
+    """Q4_K block bytes: d | dmin (f16 bits) | scales[12] | qs[128]; q[256] 4-bit."""
+    return le16(d_bits) + le16(dmin_bits) + pack_scales12(sc, mn) + pack_qs128(q)
 
 
-def q5_k():
-    d, dmin = 1.0, 0.5
-    lo = kq_nibbles()
-    qh = [(l * 37 + 11) & 0xFF for l in range(32)]   # bit j of qh[l] = 5th bit of element l of sub-block j
-    q = [lo[i] | (((qh[i % 32] >> (i // 32)) & 1) << 4) for i in range(256)]
-    b = le16(HALF[d]) + le16(HALF[dmin]) + pack_scales12(SC, MN) + qh + pack_qs128(lo)
-    vals = [d * SC[i // 32] * q[i] - dmin * MN[i // 32] for i in range(256)]
-    return dict(fmt="Q5_K", bytes=b, d=d, dmin=dmin, sc=SC, m=MN, q=q, values=vals)
+def pack_q5_k(d_bits, dmin_bits, sc, mn, q):
+    """Q5_K block bytes: d | dmin | scales[12] | qh[32] | qs[128]; q[256] 5-bit, the fifth bit of
+    element l of sub-block j is bit j of qh[l]."""
+    qh = [0] * 32
+    for i in range(256):
+        qh[i % 32] |= ((q[i] >> 4) & 1) << (i // 32)
+    return le16(d_bits) + le16(dmin_bits) + pack_scales12(sc, mn) + qh + pack_qs128([x & 15 for x in q])
 
 
-def q6_k():
-    d = 0.25
-    sc = [-128, -7, 0, 1, 5, 127, -1, 64, 2, -3, 9, -50, 33, 100, -100, 17]
-    q = [(7 * i + (i // 16)) % 64 for i in range(256)]  # 6-bit quants
+def pack_q6_k(d_bits, sc, q):
+    """Q6_K block bytes: ql[128] | qh[64] | scales[16] (int8) | d; q[256] 6-bit."""
     ql = [0] * 128
     qh = [0] * 64
     for h in range(2):
@@ -108,7 +102,33 @@ def q6_k():
             ql[64 * h + l + 32] = (e1 & 15) | ((e3 & 15) << 4)
             # qh[32h + l]: bits 2g..2g+1 = top two bits of element l + 32g
             qh[32 * h + l] = (e0 >> 4) | ((e1 >> 4) << 2) | ((e2 >> 4) << 4) | ((e3 >> 4) << 6)
-    b = ql + qh + [x & 0xFF for x in sc] + le16(HALF[d])
+    return ql + qh + [x & 0xFF for x in sc] + le16(d_bits)
+
+
+def q4_k():
+    d, dmin = 1.0, 0.5
+    q = kq_nibbles()
+    b = pack_q4_k(HALF[d], HALF[dmin], SC, MN, q)
+    vals = [d * SC[i // 32] * q[i] - dmin * MN[i // 32] for i in range(256)]
+    return dict(fmt="Q4_K", bytes=b, d=d, dmin=dmin, sc=SC, m=MN, q=q, values=vals)
+
+
+def q5_k():
+    d, dmin = 1.0, 0.5
+    lo = kq_nibbles()
+    qh = [(l * 37 + 11) & 0xFF for l in range(32)]   # bit j of qh[l] = 5th bit of element l of sub-block j
+    q = [lo[i] | (((qh[i % 32] >> (i // 32)) & 1) << 4) for i in range(256)]
+    b = pack_q5_k(HALF[d], HALF[dmin], SC, MN, q)
+    assert b[16:48] == qh
+    vals = [d * SC[i // 32] * q[i] - dmin * MN[i // 32] for i in range(256)]
+    return dict(fmt="Q5_K", bytes=b, d=d, dmin=dmin, sc=SC, m=MN, q=q, values=vals)
+
+
+def q6_k():
+    d = 0.25
+    sc = [-128, -7, 0, 1, 5, 127, -1, 64, 2, -3, 9, -50, 33, 100, -100, 17]
+    q = [(7 * i + (i // 16)) % 64 for i in range(256)]  # 6-bit quants
+    b = pack_q6_k(HALF[d], sc, q)
     vals = [d * sc[(i // 128) * 8 + (i % 128) // 16] * (q[i] - 32) for i in range(256)]
     return dict(fmt="Q6_K", bytes=b, d=d, sc=sc, q=q, values=vals)
 

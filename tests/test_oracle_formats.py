@@ -2,9 +2,12 @@
 
 Each check ties the oracle to something other than itself: hand-packed golden
 blocks (tests/golden/blocks.json, fields chosen by hand, values from the
-closed forms), IEEE binary16 as implemented by numpy, the sizes the pages
-print, and brute force / special cases of the dot product.
+closed forms), K-quant blocks packed from random fields by the same golden
+encoder, IEEE binary16 as implemented by numpy, the sizes the pages print, and
+brute force / special cases of the dot product.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -213,3 +216,50 @@ def test_gemv_rejects_ragged_cols():
     W = np.zeros(34 * 4, np.uint8)
     with pytest.raises(ValueError):
         oracle.gemv(0, W, np.zeros(40), 4, 40)
+
+
+def _golden_packers():
+    import importlib.util
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "make_golden.py")
+    spec = importlib.util.spec_from_file_location("make_golden", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _f16(bits):
+    return float(np.array([bits], dtype=np.uint16).view(np.float16)[0])
+
+
+@pytest.mark.parametrize("fmt", [2, 3, 4])
+def test_kquant_random_fields_roundtrip(fmt):
+    """K-quant blocks packed from random fields by the golden encoder (its own
+    code, written from the GGUF layout) decode in the oracle to those fields
+    and to the closed forms: d*sc*q - dmin*m (Q4_K, Q5_K), d*sc*(q-32)
+    (Q6_K), each the fp32 rounding of the exact value.  d and dmin are
+    normal f16 values of either sign in [2^-10, 2^5), so the exact value fits
+    an fp64."""
+    mg = _golden_packers()
+    rng = np.random.default_rng(20 + fmt)
+    for _ in range(60):
+        def rand_half():
+            return int(rng.integers(0, 2)) << 15 | int(rng.integers(5, 20)) << 10 | int(rng.integers(0, 1024))
+        d_bits, dmin_bits = rand_half(), rand_half()
+        d, dmin = _f16(d_bits), _f16(dmin_bits)
+        if fmt == 4:
+            sc = [int(v) for v in rng.integers(-128, 128, 16)]
+            q = [int(v) for v in rng.integers(0, 64, 256)]
+            raw = bytes(mg.pack_q6_k(d_bits, sc, q))
+            exact = [d * sc[(i // 128) * 8 + (i % 128) // 16] * (q[i] - 32) for i in range(256)]
+        else:
+            sc = [int(v) for v in rng.integers(0, 64, 8)]
+            mn = [int(v) for v in rng.integers(0, 64, 8)]
+            q = [int(v) for v in rng.integers(0, 16 if fmt == 2 else 32, 256)]
+            raw = bytes((mg.pack_q4_k if fmt == 2 else mg.pack_q5_k)(d_bits, dmin_bits, sc, mn, q))
+            for j in range(8):
+                assert oracle.kquant_scale_min(raw[4:16], j) == (sc[j], mn[j])
+            exact = [d * sc[i // 32] * q[i] - dmin * mn[i // 32] for i in range(256)]
+        assert len(raw) == oracle.block_bytes(fmt)
+        assert list(oracle.quants(fmt, raw)) == q
+        got = oracle.dequant(fmt, np.frombuffer(raw, np.uint8), 1, 256)[0]
+        assert np.array_equal(got, np.array(exact, dtype=np.float64).astype(np.float32))
