@@ -79,36 +79,37 @@ typedef struct nt_model nt_model;
 
 /* ---- context ------------------------------------------------------------ */
 
-/* Create a context on CUDA device `device`.  scratch_bytes = 0 picks the
- * default (64 MiB).  The context allocates its scratch on the device. */
+/* Context [road] (the planned public C API): create one on CUDA device
+ * `device`.  scratch_bytes = 0 picks the default (64 MiB).  The context
+ * allocates its scratch on the device. */
 nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes);
 nt_status nt_ctx_destroy(nt_ctx* ctx);
 /* nt_last_error(NULL) describes the last failed nt_ctx_create of this thread. */
-/* Wait for all work of this context's device, then report any asynchronous
+/* [road] Wait for all work of this context's device, then report any asynchronous
  * CUDA error or device-side flag and clear the flag: NT_ERR_TIMEOUT when a
  * bounded wait inside a kernel ran out; NT_ERR_INVALID_ARG when a position
  * held on the device (a decode step continued with token < 0) ran past the
  * KV cache — the kernels then wrote nothing outside the caches. */
 nt_status nt_ctx_sync(nt_ctx* ctx);
-/* Wait at most timeout_us for the work enqueued on `stream` to finish (a
+/* [road] Wait at most timeout_us for the work enqueued on `stream` to finish (a
  * host-side poll with a deadline), then report like nt_ctx_sync:
  * NT_ERR_TIMEOUT when the deadline passes first (the work is not
  * cancelled; call again to keep waiting), else the device-side error flag
  * (bounded-wait timeout or position out of range), cleared when read. */
 nt_status nt_stream_sync(nt_ctx* ctx, void* stream, int64_t timeout_us);
-/* Fault injection for the streaming engine's tests (host side only; nothing
- * is ever made to fail on the GPU): the nth following request to copy a
- * layer blob into an HBM slot (nth = 0: the next one; counted over
- * nt_stream_layer and the copies a decode step enqueues) returns
+/* Fault injection for the streaming engine's tests ([feat] SLEP streaming;
+ * host side only; nothing is ever made to fail on the GPU): the nth following
+ * request to copy a layer blob into an HBM slot (nth = 0: the next one;
+ * counted over nt_stream_layer and the copies a decode step enqueues) returns
  * NT_ERR_CUDA with nothing enqueued.  A decode step whose capture hits it
  * returns the error, keeps no graph and leaves the slot bookkeeping as it
  * was; the next call captures again.  nth = -1 disarms it. */
 nt_status nt_debug_fail_copy(nt_ctx* ctx, int nth);
-/* Test helper: a host callback on `stream` that sleeps `us` microseconds
+/* [road] Test helper: a host callback on `stream` that sleeps `us` microseconds
  * (0..10 s), so that the stream stays busy without any GPU work. */
 nt_status nt_debug_host_delay(nt_ctx* ctx, void* stream, int64_t us);
 const char* nt_last_error(const nt_ctx* ctx);
-/* Bytes per block / elements per block of a format (0 for an unknown id). */
+/* [about] Bytes per block / elements per block of a format (0 for an unknown id). */
 int nt_block_bytes(int fmt);
 int nt_block_elems(int fmt);
 
@@ -263,18 +264,20 @@ typedef struct {
   const void* host_blob;
 } nt_layer_ptrs;
 
-/* Byte layout of one layer's weights as one contiguous blob (the unit the
- * streaming engine copies): offsets_out[0..6] = offsets of wq, wk, wv, wo,
- * wg, wu, wd, each a multiple of 256; *blob_bytes_out = total size (a
- * multiple of 256).  Pure host computation from the descriptor. */
+/* [feat] (SLEP layer streaming) Byte layout of one layer's weights as one
+ * contiguous blob (the unit the streaming engine copies): offsets_out[0..6] =
+ * offsets of wq, wk, wv, wo, wg, wu, wd, each a multiple of 256;
+ * *blob_bytes_out = total size (a multiple of 256).  Pure host computation
+ * from the descriptor. */
 nt_status nt_layer_blob_layout(const nt_model_desc* desc, size_t offsets_out[7], size_t* blob_bytes_out);
 
-/* Bind a model: copies the descriptor and the pointer table (the buffers stay
- * the caller's) and allocates the model's activations and step state on the
- * device, plus, when a layer is streamed, desc->stream_slots HBM slots of
- * one blob each, a copy stream and its events.  embd [vocab x d] and out
- * [vocab x d] are block matrices, out_norm fp32 [d].  embd may live in
- * page-locked host memory: the step reads one row of it per token. */
+/* [code] (model/: transformer composition) Bind a model: copies the
+ * descriptor and the pointer table (the buffers stay the caller's) and
+ * allocates the model's activations and step state on the device, plus, when
+ * a layer is streamed, desc->stream_slots HBM slots of one blob each, a copy
+ * stream and its events.  embd [vocab x d] and out [vocab x d] are block
+ * matrices, out_norm fp32 [d].  embd may live in page-locked host memory: the
+ * step reads one row of it per token. */
 nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_ptrs* layers, const void* embd_dev,
                         const void* out_dev, const float* out_norm_dev, nt_model** out);
 nt_status nt_model_destroy(nt_ctx* ctx, nt_model* model);
@@ -300,12 +303,13 @@ nt_status nt_model_destroy(nt_ctx* ctx, nt_model* model);
 nt_status nt_decode_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos, const uint8_t* skip_mask_host,
                          float* logits_dev, int32_t* next_token_dev, void* stream);
 
-/* Sampling for the model's decode steps (nt_decode_step, nt_prefill's next
- * token stays greedy): every later step draws its next token with nt_sample's
- * definition, counter = the position of the step's input token, so a
- * sequence is reproducible from (seed, start).  temperature <= 0 restores
- * greedy decoding.  nt_spec_step then samples too (speculative sampling).
- * With temperature > 0 the vocabulary must be at most 1,024,000. */
+/* [code] (inference/: sampler) Sampling for the model's decode steps
+ * (nt_decode_step, nt_prefill's next token stays greedy): every later step
+ * draws its next token with nt_sample's definition, counter = the position of
+ * the step's input token, so a sequence is reproducible from (seed, start).
+ * temperature <= 0 restores greedy decoding.  nt_spec_step then samples too
+ * (speculative sampling). With temperature > 0 the vocabulary must be at most
+ * 1,024,000. */
 nt_status nt_model_set_sampler(nt_ctx* ctx, nt_model* model, float temperature, float top_p, uint64_t seed);
 
 /* Layer-skip calibration [cache]: one full decode step (all layers) at
@@ -369,9 +373,9 @@ nt_status nt_host_unregister(nt_ctx* ctx, const void* host_ptr);
 nt_status nt_stream_layer(nt_ctx* ctx, nt_model* model, int layer, const void* host_pinned_src, size_t bytes,
                           int slot, void* copy_stream);
 
-/* HBM address and size of streaming slot `slot`, and the layer last copied
- * into it (-1: none yet).  NT_ERR_INVALID_ARG when the model streams no
- * layer or slot is out of range. */
+/* [feat] (SLEP double buffering) HBM address and size of streaming slot
+ * `slot`, and the layer last copied into it (-1: none yet).
+ * NT_ERR_INVALID_ARG when the model streams no layer or slot is out of range. */
 nt_status nt_model_slot(nt_ctx* ctx, nt_model* model, int slot, void** slot_dev_out, size_t* bytes_out,
                         int* layer_out);
 
@@ -411,8 +415,8 @@ nt_status nt_spec_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos,
 
 /* ---- allocation-free attention ------------------------------------------------ */
 
-/* nt_attn_decode without a context and without any device allocation: the
- * pages have no counterpart; it exists for callers that cannot call
+/* [feat] GQA, [road] F16 KV cache: nt_attn_decode without a context and
+ * without any device allocation.  The pages have no counterpart for this form; it exists for callers that cannot call
  * cudaMalloc — code running while a stream is captured into a CUDA graph in
  * a mode that forbids allocation, and hosts whose device memory is handed
  * out only by their own pool (an nt_ctx allocates its scratch, so such
