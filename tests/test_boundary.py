@@ -69,3 +69,13 @@ def test_every_context_call_refuses_a_null_context():
         assert f(*args) == nt.NT_ERR_INVALID_ARG, name
         checked += 1
     assert checked >= 25
+
+
+def test_every_declaration_cites_a_passage():
+    """Each entry point's comment in include/nt.h names the page passage it
+    serves (one of the tags the header's preamble defines)."""
+    src = open(os.path.join(ROOT, "include", "nt.h")).read()
+    decls = re.finditer(r"(/\*(?:(?!\*/).)*\*/)\s*((?:typedef[^;]*;\s*)?)(?:nt_status|const char\*|int)\s+(nt_\w+)\s*\(",
+                        src, flags=re.S)
+    missing = [m.group(3) for m in decls if not re.search(r"\[(about|code|feat|cache|road)\]", m.group(1))]
+    assert not missing, missing
