@@ -4,6 +4,7 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <atomic>
 #include <chrono>
 #include <thread>
 
@@ -31,6 +32,22 @@ nt_status cuda_check(Ctx* c, cudaError_t e, const char* what) {
 
 // failures of nt_ctx_create have no context to hold their message
 thread_local std::string g_create_error;
+
+// launches still to be armed by nt_debug_stall_waits (process-wide)
+std::atomic<int> g_stall_waits{0};
+
+bool take_stall(cudaStream_t st) {
+  if (g_stall_waits.load(std::memory_order_relaxed) <= 0) return false;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return false;  // a captured launch would stall at every replay
+  }
+  int n = g_stall_waits.load();
+  while (n > 0 && !g_stall_waits.compare_exchange_weak(n, n - 1)) {
+  }
+  return n > 0;
+}
 
 }  // namespace nt
 
@@ -205,6 +222,12 @@ nt_status nt_debug_fail_copy(nt_ctx* ctx, int nth) {
   if (!ctx) return NT_ERR_INVALID_ARG;
   NT_REQUIRE(nth >= -1, NT_ERR_INVALID_ARG, "nth must be -1 (off) or >= 0");
   ctx->copy_fail_in = nth;
+  return NT_OK;
+}
+
+nt_status nt_debug_stall_waits(int n) {
+  if (n < 0 || n > 1000) return NT_ERR_INVALID_ARG;
+  g_stall_waits.store(n);
   return NT_OK;
 }
 

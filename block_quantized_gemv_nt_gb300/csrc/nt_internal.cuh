@@ -19,6 +19,7 @@
 namespace nt {
 
 constexpr int kMaxSpin = 1 << 16;   // iteration cap of every device-side wait
+constexpr int kStallSpin = 8;       // the cap of a launch armed by nt_debug_stall_waits
 constexpr unsigned kWaitHintNs = 50000;  // each try_wait may sleep this long (cap ~3 s in all)
 constexpr unsigned kErrWaitTimeout = 1u;
 constexpr unsigned kErrPosRange = 2u;  // a device-side position fell outside the KV cache: nothing written there
@@ -64,6 +65,11 @@ struct NvtxRange {
 
 // host-side status helpers ----------------------------------------------------
 nt_status set_err(Ctx* c, nt_status s, const char* fmt, ...);
+// Test hook (nt_debug_stall_waits): true when the launch about to be made on
+// st takes one of the armed stalls (never while st is being captured).  An
+// armed launch issues no bulk copies, so its waits run out after kStallSpin
+// tries and take the kernel's timeout path.
+bool take_stall(cudaStream_t st);
 nt_status cuda_check(Ctx* c, cudaError_t e, const char* what);
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -112,8 +118,8 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 
 // Bounded wait on phase `parity` of an mbarrier; false if the cap ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (int i = 0; i < kMaxSpin; ++i) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int max_spin = kMaxSpin) {
+  for (int i = 0; i < max_spin; ++i) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"

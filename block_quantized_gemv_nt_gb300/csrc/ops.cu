@@ -132,6 +132,8 @@ struct AttnArgs {
   unsigned* err;
   int64_t q_stride;        // floats between the q (and out) vectors of consecutive queries
   int64_t part_stride;     // floats between the partials of consecutive queries
+  int stall;               // test hook: issue no bulk copies; the wait gives up after kStallSpin tries
+  int nan_on_err;          // the combine writes NaN when *err holds a timed-out wait
 };
 
 // a partial row (a warp's in shared memory, a CTA's in scratch): o[128]
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(kAttnThreads, (G >= 16 ? 1 : 2)) attn_kernel(c
     fence_barrier_init();
     if (np > 0) {
       mbar_arrive_expect_tx(b, uint32_t(np) * kHD * 2 * 2);
-      if (np_early > 0) {
+      if (np_early > 0 && !a.stall) {
         const uint32_t bytes = uint32_t(np_early) * kHD * 2;
         const uint64_t pol = policy_evict_first();
         bulk_g2s(smem_u32(Ks), Kg + p0 * kHD, bytes, b, pol);
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kAttnThreads, (G >= 16 ? 1 : 2)) attn_kernel(c
   }
   if (a.pos_dev) {
     pdl_wait();
-    if (tid == 0 && np > np_early) {
+    if (tid == 0 && np > np_early && !a.stall) {
       // the rest (the new position pos) after the producer has finished
       const uint32_t off = uint32_t(np_early) * kHD, bytes = uint32_t(np - np_early) * kHD * 2;
       const uint64_t pol = policy_evict_first();
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(kAttnThreads, (G >= 16 ? 1 : 2)) attn_kernel(c
   for (int i = tid; i < G * kHD; i += kAttnThreads) qs[i] = qv[int64_t(g) * G * kHD + i] * scale;
   __syncthreads();
   bool ok = true;
-  if (np > 0) ok = mbar_wait(b, 0);
+  if (np > 0) ok = mbar_wait(b, 0, a.stall ? kStallSpin : kMaxSpin);
   if (!__syncthreads_and(ok)) {
     if (tid == 0) flag_error(a.err, kErrWaitTimeout);
     return;
@@ -372,6 +374,8 @@ __global__ void __launch_bounds__(kHD) attn_combine_kernel(const AttnArgs a) {
     for (int j = 0; j < 32; ++j)
       if (t0 + j < S) acc = fmaf(v[j], wts[t0 + j], acc);
   }
+  // a split whose wait ran out left its partial unwritten: no plausible-looking output
+  if (a.nan_on_err && (__ldcg(a.err) & kErrWaitTimeout)) acc = __int_as_float(0x7fc00000);
   a.out[int64_t(qi) * a.q_stride + (int64_t(g) * G + h) * kHD + d] = acc;
 }
 
@@ -992,6 +996,7 @@ nt_status launch_attn(Ctx* c, const float* q, const void* K, const void* V, floa
   const size_t smem = attn_smem_bytes(a.G);
   AttnKernel k = attn_kernel_for(a.G);
   if (!k) return set_err(c, NT_ERR_INVALID_ARG, "attention: group size %d not in {1,2,4,8,16}", a.G);
+  a.stall = take_stall(st);
   nt_status s = cuda_check(c, launch_k(c, k, dim3(n_kvh, S, nq), dim3(kAttnThreads), smem, st, a), "attention launch");
   if (s) return s;
   return cuda_check(c, launch_k(c, attn_combine_kernel, dim3(n_kvh, a.G, nq), dim3(kHD), 0, st, a),
@@ -1156,10 +1161,18 @@ extern "C" nt_status nt_attn_decode_static(const float* q, const void* kc, const
   a.kv_stride = kv_stride;
   a.part = reinterpret_cast<float*>(sd->scratch + kAttnStaticPart);
   a.err = reinterpret_cast<unsigned*>(sd->scratch + kAttnStaticErr);
+  a.nan_on_err = 1;  // no context to report a timed-out wait: the output says it
   AttnKernel k = attn_kernel_for(a.G);
   if (!k) return NT_ERR_INVALID_ARG;
-  k<<<dim3(n_kvh, S), kAttnThreads, attn_smem_bytes(a.G), st>>>(a);
-  attn_combine_kernel<<<dim3(n_kvh, a.G), kHD, 0, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? NT_OK : NT_ERR_CUDA;
+  a.stall = take_stall(st);
+  // the error word starts every call clear (an earlier call may have left it
+  // set); each enqueue below returns its own status, so an error left by
+  // unrelated earlier work is not reported as this call's
+  if (cudaMemsetAsync(a.err, 0, sizeof(unsigned), st) != cudaSuccess) return NT_ERR_CUDA;
+  if (launch_k(nullptr, k, dim3(n_kvh, S), dim3(kAttnThreads), attn_smem_bytes(a.G), st, a) != cudaSuccess)
+    return NT_ERR_CUDA;
+  if (launch_k(nullptr, attn_combine_kernel, dim3(n_kvh, a.G), dim3(kHD), 0, st, a) != cudaSuccess)
+    return NT_ERR_CUDA;
+  return NT_OK;
 }
 

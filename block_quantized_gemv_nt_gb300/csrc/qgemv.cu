@@ -67,6 +67,7 @@ struct GemvArgs {
   RopeArgs rope;
   int ks;             // warps sharing a row group, each over a column part
   int pblk[5];        // part p covers blocks [pblk[p], pblk[p+1])
+  int stall;          // test hook: issue no bulk copies; waits give up after kStallSpin tries
 };
 
 // the R per-lane partial sums of a row group, summed over the warp: lane
@@ -176,13 +177,14 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
         if (lane == 0) {
           const uint32_t tot = uint32_t(g_nr) * uint32_t(a.rowB);
           mbar_arrive_expect_tx(bar, tot);
-          bulk_g2s(smem_u32(st), a.job[g_j].W + g_r0 * a.rowB, tot, bar, pol);
+          if (!a.stall) bulk_g2s(smem_u32(st), a.job[g_j].W + g_r0 * a.rowB, tot, bar, pol);
         }
       } else {
         const int nvalid = a.swiglu ? 2 * g_nr : g_nr;
         if (lane == 0) mbar_arrive_expect_tx(bar, uint32_t(nvalid) * bytes_row);
         __syncwarp();
-        if (my_row) bulk_g2s(smem_u32(st + lane * a.segStride), my_row + size_t(blk0) * F::BB, bytes_row, bar, pol);
+        if (my_row && !a.stall)
+          bulk_g2s(smem_u32(st + lane * a.segStride), my_row + size_t(blk0) * F::BB, bytes_row, bar, pol);
       }
     } else {
       // plain-load path for weights that break the bulk-copy alignment rules
@@ -294,7 +296,8 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
     if (dead) {
     } else if (a.tma) {
       if (k + kStages - 1 < n_items) issue_next();
-      const bool ok = mbar_wait(bar0 + 8 * uint32_t(cs), cph);
+      const int cap = a.stall ? kStallSpin : kMaxSpin;
+      const bool ok = mbar_wait(bar0 + 8 * uint32_t(cs), cph, cap);
       if (!__all_sync(0xffffffffu, ok)) {
         // flag it, wait (bounded) for the copies still in flight, stream no more
         if (lane == 0) flag_error(a.err, kErrWaitTimeout);
@@ -305,7 +308,7 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
             q = 0;
             ph ^= 1u;
           }
-          mbar_wait(bar0 + 8 * uint32_t(q), ph);
+          mbar_wait(bar0 + 8 * uint32_t(q), ph, cap);
         }
         dead = true;
       }
@@ -757,6 +760,7 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
       ok = make_plan(c, fmt, jobsx, njobs, W2, x, norm_g, eps, cols, swiglu, rope, PlanChoice{nw, pc.stage_max, 0}, P);
   if (!ok)
     return set_err(c, NT_ERR_INVALID_ARG, "gemv: cols=%lld too large for the shared-memory plan", (long long)cols);
+  P.a.stall = P.a.tma && take_stall(st);
   return cuda_check(c, launch_plan(c, fmt, P, st), "qgemv launch");
 }
 

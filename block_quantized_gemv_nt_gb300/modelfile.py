@@ -14,11 +14,17 @@ streamed layer is one contiguous, page-aligned range of the file:
                "attn_norm.l", "ffn_norm.l"
 
 ``ModelFile`` maps the file read-only.  Resident layers are uploaded from
-the mapping; the streamed layers' blobs (and the embedding table) stay in the
-mapping, page-locked with nt_host_register ("mmap pinned"), so the streaming
-engine copies them to HBM exactly as it copies pinned RAM.  Where the
-operating system refuses to page-lock file-backed memory, ``FileBlobs`` falls
-back to one CPU copy of those ranges into page-locked buffers ("CPU memcpy").
+the mapping; the streamed layers' blobs (and the embedding table) are
+page-locked where they lie, so the streaming engine copies them to HBM
+exactly as it copies pinned RAM.  ``FileBlobs`` takes the first rung that
+the operating system and driver accept, in the pages' order of preference:
+
+  "mmap pinned"          the read-only shared mapping, registered read-only;
+  "mmap pinned private"  a private, writable, pre-faulted mapping of the
+                         range (copy-on-write: the file is never written),
+                         registered without the read-only flag;
+  "CPU memcpy"           one CPU copy of the range into page-locked memory.
+
 The KV cache is runtime state, not part of the file.
 """
 from __future__ import annotations
@@ -199,11 +205,25 @@ class FileBlobs:
         self.offsets, self.nbytes = mf.blob_offsets, mf.blob_bytes
         self._regs = []
         self._copies = []
-        self.tier = "mmap pinned"
+        self._maps = []
+        self.rungs = []   # the rung each locked range took
+        self.rung_of = {}  # entry name -> rung
         self.blob = {}
         for li in self.layers:
             self.blob[li] = self._lock(f"blob.{li}", allow_copy)
         self.embd = self._lock("embd", allow_copy) if self.layers else None
+        order = ("CPU memcpy", "mmap pinned private", "mmap pinned")
+        self.tier = next((t for t in order if t in self.rungs), "mmap pinned")  # the lowest rung taken
+
+    def _private_map(self, name: str):
+        """A private, writable, pre-faulted mapping of entry `name`: (mapping, address)."""
+        off, n = self.mf.entries[name]
+        gran = mmap.ALLOCATIONGRANULARITY
+        base = off // gran * gran
+        length = _up(off - base + _up(n), mmap.PAGESIZE)
+        flags = mmap.MAP_PRIVATE | getattr(mmap, "MAP_POPULATE", 0)
+        mm = mmap.mmap(self.mf._fd, length, flags=flags, prot=mmap.PROT_READ | mmap.PROT_WRITE, offset=base)
+        return mm, np.frombuffer(mm, dtype=np.uint8).ctypes.data + (off - base)
 
     def _lock(self, name: str, allow_copy: bool) -> int:
         addr = self.mf.address(name)
@@ -211,13 +231,31 @@ class FileBlobs:
         try:
             nt.nt_host_register(self.ctx, addr, nbytes, read_only=True)
             self._regs.append(addr)
+            self.rungs.append("mmap pinned")
+            self.rung_of[name] = "mmap pinned"
             return addr
         except nt.NtError:
-            if not allow_copy:
-                raise
+            pass
+        try:
+            mm, paddr = self._private_map(name)
+        except (OSError, ValueError):
+            mm = None
+        if mm is not None:
+            try:
+                nt.nt_host_register(self.ctx, paddr, nbytes, read_only=False)
+                self._regs.append(paddr)
+                self._maps.append(mm)
+                self.rungs.append("mmap pinned private")
+                self.rung_of[name] = "mmap pinned private"
+                return paddr
+            except nt.NtError:
+                mm.close()
+        if not allow_copy:
+            raise nt.NtError(nt.NT_ERR_CUDA, f"{name}: the file's pages cannot be page-locked in place")
         # the pages of this file cannot be locked in place: one CPU copy into page-locked memory
         import torch
-        self.tier = "CPU memcpy"
+        self.rungs.append("CPU memcpy")
+        self.rung_of[name] = "CPU memcpy"
         off = self.mf.entries[name][0]
         buf = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
         n = self.mf.entries[name][1]
@@ -230,3 +268,9 @@ class FileBlobs:
             nt.nt_host_unregister(self.ctx, addr)
         self._regs = []
         self._copies = []
+        for mm in self._maps:
+            try:
+                mm.close()
+            except BufferError:
+                pass  # a view still alive elsewhere: the mapping closes with it
+        self._maps = []

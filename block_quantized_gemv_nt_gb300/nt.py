@@ -114,6 +114,7 @@ _sig("nt_model_slot", [_vp, _vp, _ci, ctypes.POINTER(_vp), ctypes.POINTER(_sz), 
 _sig("nt_stream_sync", [_vp, _vp, _i64])
 _sig("nt_debug_fail_copy", [_vp, _ci])
 _sig("nt_debug_host_delay", [_vp, _vp, _i64])
+_sig("nt_debug_stall_waits", [_ci])
 
 EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "nt_block_bytes", "nt_block_elems",
             "nt_dequant_rows", "nt_gemv_q", "nt_gemv_q_swiglu", "nt_gemv_q_multi", "nt_rmsnorm", "nt_rope",
@@ -121,7 +122,8 @@ EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "
             "nt_model_init", "nt_model_destroy", "nt_decode_step", "nt_layer_skip_calibrate",
             "nt_attn_decode_static", "nt_layer_blob_layout", "nt_stream_layer", "nt_model_slot", "nt_spec_step",
             "nt_gemm_q", "nt_attn_verify", "nt_plan_residency", "nt_prefill", "nt_sample", "nt_model_set_sampler",
-            "nt_host_register", "nt_host_unregister", "nt_stream_sync", "nt_debug_fail_copy", "nt_debug_host_delay"]
+            "nt_host_register", "nt_host_unregister", "nt_stream_sync", "nt_debug_fail_copy", "nt_debug_host_delay",
+            "nt_debug_stall_waits"]
 
 
 def lib():
@@ -289,6 +291,15 @@ def nt_debug_fail_copy(ctx, nth: int):
 def nt_debug_host_delay(ctx, stream, us: int):
     """A host callback that keeps `stream` busy for `us` microseconds."""
     return ctx.check(_lib.nt_debug_host_delay(ctx.handle, _stream(stream), us))
+
+
+def nt_debug_stall_waits(n: int):
+    """Test hook: the next n eager launches of the copy-waiting kernels take
+    their bounded-wait timeout path (no GPU fault or hang); 0 disarms."""
+    st = _lib.nt_debug_stall_waits(n)
+    if st != NT_OK:
+        raise NtError(st, "nt_debug_stall_waits failed")
+    return st
 
 
 def nt_sample(ctx, logits, n: int, temperature: float, top_p: float, seed: int, counter: int, out, stream=None):

@@ -105,6 +105,16 @@ nt_status nt_stream_sync(nt_ctx* ctx, void* stream, int64_t timeout_us);
  * returns the error, keeps no graph and leaves the slot bookkeeping as it
  * was; the next call captures again.  nth = -1 disarms it. */
 nt_status nt_debug_fail_copy(nt_ctx* ctx, int nth);
+/* [road] Test hook for the device-side bounded waits (failure detection; no
+ * GPU is made to fault or hang): the next n eager launches in this process
+ * of the kernels that wait on bulk copies — the quant GEMV (nt_gemv_q,
+ * nt_gemv_q_multi, nt_gemv_swiglu), nt_attn_decode and
+ * nt_attn_decode_static — issue no copies, so their waits run out after a
+ * few tries and take the timeout path: the context flag that nt_ctx_sync
+ * reports as NT_ERR_TIMEOUT, or NaN output from nt_attn_decode_static.
+ * Launches on a stream being captured are never armed.  n = 0 disarms;
+ * n outside 0..1000 is NT_ERR_INVALID_ARG. */
+nt_status nt_debug_stall_waits(int n);
 /* [road] Test helper: a host callback on `stream` that sleeps `us` microseconds
  * (0..10 s), so that the stream stays busy without any GPU work. */
 nt_status nt_debug_host_delay(nt_ctx* ctx, void* stream, int64_t us);
@@ -415,10 +425,10 @@ nt_status nt_spec_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos,
 
 /* ---- allocation-free attention ------------------------------------------------ */
 
-/* [feat] GQA, [road] F16 KV cache: nt_attn_decode without a context and
- * without any device allocation.  The pages have no counterpart for this form; it exists for callers that cannot call
- * cudaMalloc — code running while a stream is captured into a CUDA graph in
- * a mode that forbids allocation, and hosts whose device memory is handed
+/* nt_attn_decode without a context and without any device allocation.  The
+ * pages have no counterpart for this form; it exists for callers that cannot
+ * call cudaMalloc — code running while a stream is captured into a CUDA graph
+ * in a mode that forbids allocation, and hosts whose device memory is handed
  * out only by their own pool (an nt_ctx allocates its scratch, so such
  * callers cannot create one).
  *
@@ -433,11 +443,15 @@ nt_status nt_spec_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos,
  *  - The first call on a device looks up the array's device address and sets
  *    the kernel's shared-memory limit; make that first call before any stream
  *    capture.
- *  - Every call shares the array; calls whose work overlaps on the GPU
- *    (different streams, or devices sharing nothing but the symbol) race on
- *    it — serialize them.
- *  - Returns NT_OK once the work is enqueued; a device-side wait that runs out
- *    is recorded only in the array, not reported. */
+ *  - Each device has its own copy of the array, shared by every call on that
+ *    device: calls whose work overlaps on one device (different streams, or
+ *    threads sharing the device) race on it — serialize them.  Calls on
+ *    different devices do not interact.
+ *  - Returns NT_OK once the work is enqueued (each enqueue's own status, not
+ *    an error left by earlier unrelated work).  There is no context to carry
+ *    an asynchronous error: a device-side wait that runs out makes this
+ *    call's output NaN.  The array's error word is cleared at the start of
+ *    every call, so a later call is unaffected. */
 nt_status nt_attn_decode_static(const float* q_dev, const void* kcache_dev, const void* vcache_dev, float* out_dev,
                                 int n_qh, int n_kvh, int head_dim, int64_t n_pos, int64_t kv_stride, void* stream);
 

@@ -7,13 +7,21 @@ fault, trap or hang is ever induced.
   decode step whose graph capture hits the failure).
 - A deadline-bounded stream wait returns NT_ERR_TIMEOUT while a host
   callback keeps the stream busy, and NT_OK once it is done; the context
-  stays usable."""
+  stays usable.
+- The device-side bounded waits themselves: a test hook makes the next
+  launch of the quant GEMV or the decode attention issue no bulk copies, so
+  its mbarrier is never completed (nothing is in flight, nothing faults); the
+  wait gives up after a few tries, the kernel raises the context's flag and
+  returns, nt_ctx_sync reports NT_ERR_TIMEOUT, and the next launch on the
+  same context is correct."""
 import time
 
+import numpy as np
 import pytest
 
+import oracle
 import synth
-from gpu_util import need_gpu, torch
+from gpu_util import dev, host, need_gpu, rel_l2, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -108,3 +116,46 @@ def test_stream_sync_deadline(ctx):
     with pytest.raises(nt.NtError) as ei:
         nt.nt_stream_sync(ctx, st, -1)
     assert ei.value.status == nt.NT_ERR_INVALID_ARG
+
+
+def _stalled_then_clean(ctx, launch):
+    """launch() once armed (the wait runs out), then once clean."""
+    from block_quantized_gemv_nt_gb300 import nt
+    ctx.sync()
+    nt.nt_debug_stall_waits(1)
+    try:
+        launch()
+    finally:
+        nt.nt_debug_stall_waits(0)
+    with pytest.raises(nt.NtError) as ei:
+        ctx.sync()
+    assert ei.value.status == nt.NT_ERR_TIMEOUT
+    launch()
+    ctx.sync()   # the flag was taken: a clean launch reports nothing
+
+
+def test_attention_wait_timeout_is_reported(ctx):
+    from block_quantized_gemv_nt_gb300 import nt
+    H, G, hd, stride, n_pos = 32, 8, 128, 1100, 1088
+    Kh = synth.normal_f16(G * stride * hd, 31, 1).reshape(G, stride, hd)
+    Vh = synth.normal_f16(G * stride * hd, 31, 2).reshape(G, stride, hd)
+    qh = synth.normal_f32(H * hd, 31, 3)
+    K, V, q = dev(Kh), dev(Vh), dev(qh)
+    out = torch.zeros(H * hd, dtype=torch.float32, device="cuda")
+    _stalled_then_clean(ctx, lambda: nt.nt_attn_decode(ctx, q, K, V, out, H, G, hd, n_pos, stride))
+    want = oracle.attn_decode(qh.astype(np.float64), Kh, Vh, H, G, hd, n_pos, stride)
+    assert rel_l2(host(out), want) <= 1e-4
+
+
+@pytest.mark.parametrize("fmt", [0, 2, 4])
+def test_gemv_wait_timeout_is_reported(ctx, fmt):
+    from block_quantized_gemv_nt_gb300 import nt
+    rows, cols = 3000, 4096
+    W = synth.quant_matrix(fmt, rows, cols, seed=32, stream=fmt)
+    x = synth.normal_f32(cols, seed=32, stream=99)
+    Wd, xd = dev(W), dev(x)
+    y = torch.zeros(rows, dtype=torch.float32, device="cuda")
+    nt.nt_gemv_q(ctx, fmt, Wd, xd, y, rows, cols)   # plan tuning happens on this first call, unarmed
+    _stalled_then_clean(ctx, lambda: nt.nt_gemv_q(ctx, fmt, Wd, xd, y, rows, cols))
+    want = oracle.gemv(fmt, W, x.astype(np.float64), rows, cols)
+    assert rel_l2(host(y), want) <= 1e-3

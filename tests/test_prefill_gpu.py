@@ -53,7 +53,9 @@ def test_prefill_matches_oracle(ctx, name, n, pos0):
     assert int(gm.next_token.item()) == int(np.argmax(got)) == int(np.argmax(ref))
     # the K/V of every prompt position, every layer
     torch.cuda.synchronize()
+    worst = []   # per layer: the largest |delta| / (head RMS), K and V together
     for li in range(spec.n_layers):
+        w = 0.0
         for which in ("kcache", "vcache"):
             g = gm.layers[li][which].cpu().numpy().astype(np.float64)[:, pos0:pos0 + n]
             o = getattr(om, which)[li].astype(np.float64)[:, pos0:pos0 + n]
@@ -62,6 +64,9 @@ def test_prefill_matches_oracle(ctx, name, n, pos0):
             ratio = np.abs(g - o) / bar
             where = np.unravel_index(np.argmax(ratio), ratio.shape)
             assert ratio.max() <= 1.0, (li, which, float(ratio.max()), where, float(g[where]), float(o[where]))
+            w = max(w, float(np.max(np.abs(g - o) / scale)))
+        worst.append(w)
+    print(f"prefill K/V {name} n={n}: worst |delta|/rms per layer", " ".join(f"{v:.2e}" for v in worst))
     # decoding continues from the prefilled state
     tok = int(np.argmax(got))
     for step in range(3):

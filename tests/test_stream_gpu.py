@@ -217,9 +217,10 @@ def test_planned_residency_decodes_like_resident(ctx):
 @pytest.mark.parametrize("where", ["tmp", "shm"])
 def test_model_file_streams_like_resident(ctx, tmp_path, where):
     """The host-file tier: a model written to a file, mapped read-only, its
-    streamed layers page-locked in the mapping (or, where the OS refuses,
-    copied once into page-locked memory), decodes bit-identically to the
-    same model held resident."""
+    streamed layers page-locked in the mapping (else in a private mapping of
+    it, else copied once into page-locked memory), decodes bit-identically to
+    the same model held resident, and matches the fp64 oracle reading the
+    file's own mapped bytes (teacher-forced on the GPU's tokens)."""
     import os
     from block_quantized_gemv_nt_gb300 import engine, modelfile
     spec = synth.model_spec("small_q4_k_m_r1")
@@ -230,13 +231,25 @@ def test_model_file_streams_like_resident(ctx, tmp_path, where):
     try:
         mf = modelfile.ModelFile(path)
         fb = modelfile.FileBlobs(ctx, mf, spec.n_resident)
-        print("tier:", fb.tier)
+        print("tier:", fb.tier, "rungs:", fb.rung_of)
+        assert fb.tier in ("mmap pinned", "mmap pinned private", "CPU memcpy")
         hf = synth.HostModel(mf.spec, mf.layers, mf.embd, mf.out, mf.out_norm, hm.kcache, hm.vcache)
         gf = engine.DeviceModel(ctx, mf.spec, hf, blobs=fb)
         base = synth.model_spec("small_q4_k_m")
         gr = engine.DeviceModel(ctx, base, hm)
-        for x, y in zip(_greedy(gf, spec, 4), _greedy(gr, base, 4)):
+        got = _greedy(gf, spec, 4)
+        for x, y in zip(got, _greedy(gr, base, 4)):
             assert torch.equal(x, y)
+        # the oracle on the bytes the file holds (its own mapping), fed the GPU's tokens
+        om = oracle.Model(mf.spec, mf.layers, mf.embd, mf.out, mf.out_norm, hm.kcache, hm.vcache)
+        tok, pos = spec.first_token, spec.n_prefill
+        for lg in got:
+            g = lg.cpu().numpy().astype(np.float64)
+            ref = om.step(tok, pos)
+            assert np.max(np.abs(g - ref)) <= 2e-2 * ref.std()
+            assert int(np.argmax(g)) == int(np.argmax(ref))
+            tok, pos = int(np.argmax(g)), pos + 1
+        del om
         gf.close()
         gr.close()
         fb.close()
