@@ -4,6 +4,7 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <thread>
@@ -241,6 +242,29 @@ nt_status nt_debug_host_delay(nt_ctx* ctx, void* stream, int64_t us) {
   DeviceGuard g(ctx->device);
   return cuda_check(ctx, cudaLaunchHostFunc(as_stream(stream), host_delay_fn, reinterpret_cast<void*>(intptr_t(us))),
                     "host delay");
+}
+
+nt_status nt_ctx_gemv_plans(nt_ctx* ctx, char* out, size_t cap, size_t* len) {
+  NT_TRY(pre_call(ctx));
+  NT_REQUIRE(len && (out || cap == 0), NT_ERR_INVALID_ARG, "null length or buffer");
+  std::string text;
+  {
+    std::lock_guard<std::mutex> lk(ctx->mu);
+    for (const auto& kv : ctx->gemv_plans) {
+      // key: fmt/cols/swiglu/tma/rows0/rows1/rows2
+      char line[256];
+      snprintf(line, sizeof line, "%s -> warps=%d stage_max=%d R=%d ks=%d\n", kv.first.c_str(), kv.second.warps,
+               kv.second.stage_max, kv.second.R, kv.second.ks);
+      text += line;
+    }
+  }
+  *len = text.size() + 1;
+  if (cap) {
+    const size_t n = std::min(cap - 1, text.size());
+    std::memcpy(out, text.data(), n);
+    out[n] = 0;
+  }
+  return NT_OK;
 }
 
 const char* nt_last_error(const nt_ctx* ctx) { return ctx ? ctx->last_error.c_str() : g_create_error.c_str(); }

@@ -48,7 +48,25 @@ struct nt_model {
   float* attn_part = nullptr;
   int S = 0;
   cudaStream_t cap = nullptr;
-  std::map<std::string, cudaGraphExec_t> graphs;
+  // captured steps, keyed on what changes their kernels (skip mask, sampler,
+  // draft shape), never on the caller's output pointers: each graph writes
+  // its outputs into the model's own buffers and ends with copy nodes to the
+  // caller's, re-pointed on the executable graph when they change
+  struct OutCopy {
+    const void* src;
+    size_t bytes;
+    void* dst;
+    cudaGraphNode_t node;
+  };
+  struct Graph {
+    cudaGraph_t g = nullptr;
+    cudaGraphExec_t ge = nullptr;
+    std::vector<OutCopy> outs;
+  };
+  std::map<std::string, Graph> graphs;
+  float* out_logits = nullptr;   // [2 kMaxVerify - 1][vocab]: the step's logits before the copy out
+  int32_t* out_tok = nullptr;    // [kMaxVerify]: next token / emitted tokens
+  int32_t* out_n = nullptr;      // emitted-token count of a speculative step
   // streaming: layers whose weights stay in page-locked host memory
   std::vector<const void*> host_blob;  // per layer; null = resident
   int n_slots = 0;
@@ -582,10 +600,9 @@ void key_append(std::string& k, const T& v) {
   k.append(reinterpret_cast<const char*>(&v), sizeof v);
 }
 
-std::string graph_key(const nt_model* m, const uint8_t* skip, const float* logits, const int32_t* next_tok) {
+std::string graph_key(const nt_model* m, const uint8_t* skip, const int32_t* next_tok) {
   std::string k("d");
-  key_append(k, logits);
-  key_append(k, next_tok);
+  key_append(k, next_tok != nullptr);
   key_append(k, m->temperature);
   key_append(k, m->top_p);
   key_append(k, m->seed);
@@ -593,10 +610,19 @@ std::string graph_key(const nt_model* m, const uint8_t* skip, const float* logit
   return k;
 }
 
+// one output of a step: the model buffer the step writes, its size, and
+// the caller's buffer it is copied to at the end of the graph
+struct Out {
+  const void* src;
+  size_t bytes;
+  void* dst;
+};
+
 // replay the graph under `key`, capturing it first with `enqueue` on the
-// model's capture stream
+// model's capture stream, followed by the copies `outs`
 template <typename F>
-nt_status run_graph(Ctx* c, nt_model* m, const std::string& key, cudaStream_t st, F enqueue) {
+nt_status run_graph(Ctx* c, nt_model* m, const std::string& key, cudaStream_t st, const std::vector<Out>& outs,
+                    F enqueue) {
   auto it = m->graphs.find(key);
   nt_status s = NT_OK;
   if (it == m->graphs.end()) {
@@ -614,19 +640,55 @@ nt_status run_graph(Ctx* c, nt_model* m, const std::string& key, cudaStream_t st
     s = cuda_check(c, cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeThreadLocal), "begin capture");
     if (!s) {
       nt_status s2 = enqueue(m->cap);
+      for (const Out& o : outs)
+        if (!s2)
+          s2 = cuda_check(c, cudaMemcpyAsync(o.dst, o.src, o.bytes, cudaMemcpyDeviceToDevice, m->cap), "copy out");
       cudaError_t e = cudaStreamEndCapture(m->cap, &g);
       if (s2 && e != cudaSuccess) cudaGetLastError();  // the first error is the one reported
       s = s2 ? s2 : cuda_check(c, e, "end capture");
     }
+    nt_model::Graph gr;
+    gr.g = g;
+    if (!s) {
+      // the copy-out nodes, found by their source buffers
+      size_t n = 0;
+      s = cuda_check(c, cudaGraphGetNodes(g, nullptr, &n), "graph nodes");
+      std::vector<cudaGraphNode_t> nodes(n);
+      if (!s && n) s = cuda_check(c, cudaGraphGetNodes(g, nodes.data(), &n), "graph nodes");
+      for (const Out& o : outs) {
+        nt_model::OutCopy oc{o.src, o.bytes, o.dst, nullptr};
+        for (size_t i = 0; i < n && !s && !oc.node; ++i) {
+          cudaGraphNodeType t;
+          if (cudaGraphNodeGetType(nodes[i], &t) != cudaSuccess || t != cudaGraphNodeTypeMemcpy) continue;
+          cudaMemcpy3DParms p{};
+          if (cudaGraphMemcpyNodeGetParams(nodes[i], &p) == cudaSuccess && p.srcPtr.ptr == o.src) oc.node = nodes[i];
+        }
+        if (!s && !oc.node) s = set_err(c, NT_ERR_CUDA, "copy-out node not found in the captured step");
+        gr.outs.push_back(oc);
+      }
+    }
     if (!s) s = cuda_check(c, cudaGraphInstantiate(&ge, g, 0), "graph instantiate");
-    if (g) cudaGraphDestroy(g);
     if (s) {
+      if (g) cudaGraphDestroy(g);
+      cudaGetLastError();
       m->slot_layer = slots_before;
       return s;
     }
-    it = m->graphs.emplace(key, ge).first;
+    gr.ge = ge;
+    it = m->graphs.emplace(key, gr).first;
   }
-  return cuda_check(c, cudaGraphLaunch(it->second, st), "graph launch");
+  // point the copy-out nodes at this call's buffers
+  nt_model::Graph& gr = it->second;
+  for (size_t i = 0; i < gr.outs.size() && i < outs.size() && !s; ++i) {
+    nt_model::OutCopy& oc = gr.outs[i];
+    if (oc.dst == outs[i].dst) continue;
+    s = cuda_check(c, cudaGraphExecMemcpyNodeSetParams1D(gr.ge, oc.node, outs[i].dst, oc.src, oc.bytes,
+                                                         cudaMemcpyDeviceToDevice),
+                   "re-point the step's output copy");
+    if (!s) oc.dst = outs[i].dst;
+  }
+  if (s) return s;
+  return cuda_check(c, cudaGraphLaunch(gr.ge, st), "graph launch");
 }
 
 }  // namespace
@@ -722,7 +784,8 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
                nvx = up256(fl * kMaxVerify * d.d_model), nvq = up256(fl * kMaxVerify * nq),
                nvh = up256(fl * kMaxVerify * d.ffn), nvl = up256(fl * kMaxVerify * d.vocab), ndl = up256(fl * d.vocab),
                nprompt = up256(sizeof(int32_t) * size_t(d.kv_cap)), nsamp = kSampRowBytes * kMaxVerify,
-               nsw = up256(8 * size_t(d.vocab)), nsW = up256(8 * kMaxVerify);
+               nsw = up256(8 * size_t(d.vocab)), nsW = up256(8 * kMaxVerify),
+               nout = up256(fl * size_t(2 * kMaxVerify - 1) * size_t(d.vocab)), nouttok = 256;
   {
     // partial sums of the largest verify GEMM
     const int64_t nkv = int64_t(d.n_kvh) * d.head_dim;
@@ -735,7 +798,8 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
     m->gpart_bytes = up256(m->gpart_bytes);
   }
   const size_t total = 2 * nx + nqb * 2 + nkb * 2 + nh + ncos + nst + npart + nfreq + nspec + nvx + 2 * nvq + nvh +
-                       nvl + ndl + nprompt + m->gpart_bytes + nsamp + nsw * (2 * kMaxVerify - 1) + 2 * nsW;
+                       nvl + ndl + nprompt + m->gpart_bytes + nsamp + nsw * (2 * kMaxVerify - 1) + 2 * nsW + nout +
+                       nouttok;
   int dev_prev = 0;
   cudaGetDevice(&dev_prev);
   cudaSetDevice(ctx->device);
@@ -798,6 +862,12 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   m->samp = take(nsamp);
   m->sw_q = reinterpret_cast<unsigned long long*>(take(nsw * (kMaxVerify - 1)));
   m->sw_p = reinterpret_cast<unsigned long long*>(take(nsw * kMaxVerify));
+  m->out_logits = reinterpret_cast<float*>(take(nout));
+  {
+    char* ot = take(nouttok);
+    m->out_tok = reinterpret_cast<int32_t*>(ot);
+    m->out_n = reinterpret_cast<int32_t*>(ot + 64);
+  }
   m->sW_q = reinterpret_cast<unsigned long long*>(take(nsW));
   m->sW_p = reinterpret_cast<unsigned long long*>(take(nsW));
   cudaSetDevice(ctx->device);
@@ -818,7 +888,10 @@ nt_status nt_model_destroy(nt_ctx* ctx, nt_model* m) {
   cudaGetDevice(&dev_prev);
   cudaSetDevice(ctx->device);
   cudaDeviceSynchronize();
-  for (auto& kv : m->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : m->graphs) {
+    cudaGraphExecDestroy(kv.second.ge);
+    cudaGraphDestroy(kv.second.g);
+  }
   if (m->cap) cudaStreamDestroy(m->cap);
   if (m->copy_st) cudaStreamDestroy(m->copy_st);
   for (cudaEvent_t ev : {m->ev_fork, m->ev_join, m->ev_prompt})
@@ -855,8 +928,10 @@ nt_status nt_decode_step(nt_ctx* ctx, nt_model* m, int32_t token, int64_t pos, c
     s = cuda_check(ctx, cudaGetLastError(), "set step state");
   }
   if (!s) {
-    const StepIO io{m->tok, m->pos, logits, next_tok, true};
-    s = run_graph(ctx, m, graph_key(m, skip, logits, next_tok), st,
+    const StepIO io{m->tok, m->pos, m->out_logits, next_tok ? m->out_tok : nullptr, true};
+    std::vector<Out> outs{{m->out_logits, sizeof(float) * size_t(m->d.vocab), logits}};
+    if (next_tok) outs.push_back({m->out_tok, sizeof(int32_t), next_tok});
+    s = run_graph(ctx, m, graph_key(m, skip, next_tok), st, outs,
                   [&](cudaStream_t cs) { return enqueue_step(ctx, m, skip, io, cs, false); });
   }
   if (dev_prev != ctx->device) cudaSetDevice(dev_prev);
@@ -923,17 +998,27 @@ nt_status nt_spec_step(nt_ctx* ctx, nt_model* m, int32_t token, int64_t pos, int
     std::string key("s");
     key_append(key, k);
     key_append(key, n_draft_layers);
-    key_append(key, tokens_out);
-    key_append(key, n_out);
-    key_append(key, logits);
+    key_append(key, logits != nullptr);
     key_append(key, m->temperature);
     key_append(key, m->top_p);
     key_append(key, m->seed);
-    s = run_graph(ctx, m, key, st,
-                  [&](cudaStream_t cs) { return enqueue_spec(ctx, m, k, n_draft_layers, tokens_out, n_out, logits, cs); });
+    std::vector<Out> outs{{m->out_tok, sizeof(int32_t) * size_t(k + 1), tokens_out},
+                          {m->out_n, sizeof(int32_t), n_out}};
+    if (logits) outs.push_back({m->out_logits, sizeof(float) * size_t(2 * k + 1) * size_t(m->d.vocab), logits});
+    float* own_logits = logits ? m->out_logits : nullptr;
+    s = run_graph(ctx, m, key, st, outs, [&](cudaStream_t cs) {
+      return enqueue_spec(ctx, m, k, n_draft_layers, m->out_tok, m->out_n, own_logits, cs);
+    });
   }
   if (dev_prev != ctx->device) cudaSetDevice(dev_prev);
   return s;
+}
+
+nt_status nt_model_graph_count(nt_ctx* ctx, nt_model* m, int* n) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  NT_REQUIRE(m && n, NT_ERR_INVALID_ARG, "null model or output");
+  *n = int(m->graphs.size());
+  return NT_OK;
 }
 
 nt_status nt_layer_blob_layout(const nt_model_desc* d, size_t* off, size_t* bytes) {

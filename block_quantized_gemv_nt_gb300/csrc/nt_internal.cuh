@@ -24,9 +24,12 @@ constexpr unsigned kWaitHintNs = 50000;  // each try_wait may sleep this long (c
 constexpr unsigned kErrWaitTimeout = 1u;
 constexpr unsigned kErrPosRange = 2u;  // a device-side position fell outside the KV cache: nothing written there
 
-// a GEMV launch configuration: warps per CTA, stage-size cap, split-K (0 = by balance)
+// a GEMV launch configuration: warps per CTA and stage-size cap (what the
+// tuner chooses), and, for the record, the shape's arithmetic: column parts
+// KS and rows per lane group R (fixed by the shape alone)
 struct PlanChoice {
   int warps, stage_max, ks;
+  int R = 0;
 };
 
 struct Ctx {

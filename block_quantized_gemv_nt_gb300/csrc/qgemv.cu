@@ -33,6 +33,7 @@ namespace {
 using namespace qf;
 
 constexpr int kMaxWarps = 32;
+constexpr int kMaxChunks = 512;  // 128-column chunks of a normalised x (cols <= 65536)
 
 struct JobDev {
   const uint8_t* W;
@@ -223,7 +224,9 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
   // per pass.  All of a lane's x loads are issued first (one memory round
   // trip), the RMSNorm sum of squares comes from the same registers.
   {
-    __shared__ float red[kMaxWarps];
+    // sum of squares of x per 128-column chunk, then over the chunks in
+    // index order: the same additions whatever the warp count
+    __shared__ float red[kMaxChunks];
     constexpr int kPF = 16;  // passes held in registers
     const int sub = lane & 7;
     const int pass_stride = nwarps * 4;
@@ -241,22 +244,30 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
     if (whole) load_passes(0);
     float inv = 1.f;
     if (a.norm_g) {
-      float ss = 0.f;
+      const int nchunk = (ng + 3) / 4;  // a warp's pass covers chunk warp + pass * nwarps
       if (whole) {
 #pragma unroll
-        for (int k = 0; k < kPF; ++k)
-          ss = fmaf(v[k].x, v[k].x, fmaf(v[k].y, v[k].y, fmaf(v[k].z, v[k].z, fmaf(v[k].w, v[k].w, ss))));
+        for (int k = 0; k < kPF; ++k) {
+          if (k >= npass) break;  // warp-uniform
+          float ss = fmaf(v[k].x, v[k].x, fmaf(v[k].y, v[k].y, fmaf(v[k].z, v[k].z, v[k].w * v[k].w)));
+          ss = warp_sum(ss);
+          if (lane == 0) red[warp + k * nwarps] = ss;
+        }
       } else {
-        for (int i = tid * 4; i < a.cols; i += blockDim.x * 4) {
-          const float4 t = *reinterpret_cast<const float4*>(a.x + i);
-          ss = fmaf(t.x, t.x, fmaf(t.y, t.y, fmaf(t.z, t.z, fmaf(t.w, t.w, ss))));
+        for (int ch = warp; ch < nchunk; ch += nwarps) {
+          const int grp = 4 * ch + (lane >> 3);
+          float ss = 0.f;
+          if (grp < ng) {
+            const float4 t = *reinterpret_cast<const float4*>(a.x + 32 * grp + 4 * sub);
+            ss = fmaf(t.x, t.x, fmaf(t.y, t.y, fmaf(t.z, t.z, t.w * t.w)));
+          }
+          ss = warp_sum(ss);
+          if (lane == 0) red[ch] = ss;
         }
       }
-      ss = warp_sum(ss);
-      if (lane == 0) red[warp] = ss;
       __syncthreads();
       float tot = 0.f;
-      for (int w = 0; w < nwarps; ++w) tot += red[w];
+      for (int ch = 0; ch < nchunk; ++ch) tot += red[ch];
       inv = rsqrtf(tot / float(a.cols) + a.eps);
     }
     for (int p0 = 0; p0 < npass; p0 += kPF) {
@@ -473,6 +484,54 @@ struct Plan {
   size_t smem = 0;
 };
 
+// blocks per segment granule: a multiple of the format's alignment unit that
+// also holds a multiple of 32 lane units, so that lane l always takes the
+// units l, l + 32, ... of a row part, in that order, whatever the segment size
+int seg_granule(int fmt, int align) { return (fmt == NT_F16 || fmt == NT_F32) ? 32 : align; }
+
+// The arithmetic of a launch shape: rows per lane group R and column parts
+// KS.  Together with the granule above they fix every addition a row's sum
+// goes through, so they are a function of the shape (and the device's SM
+// count and shared memory) alone: the plans the tuner times differ only in
+// warps per CTA and stage size, and never change a result bit.
+struct Arith {
+  int R, ks;
+};
+Arith arith_plan(const Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, int64_t cols, bool swiglu) {
+  const int BB = block_bytes(fmt);
+  const int64_t nb = cols / block_elems(fmt);
+  const int64_t rowB = nb * BB;
+  const FmtInfo fi = fmt_info(fmt, int(cols));
+  const int al = seg_granule(fmt, fi.align);
+  const int ng = int(cols / 32);
+  const int nw = 16, ns = 2;  // the default launch
+  const int head = ((fi.xbytes + 12 * ng + 8 + nw * ns * 8 + 127) / 128) * 128;
+  const long avail = long(c->smem_optin) - head - 16 - c->gemv_static_smem;
+  long stb = avail / (nw * ns) / 16 * 16;
+  if (stb > 12288) stb = 12288;
+  Arith r{4, 1};
+  if (!(4 * rowB <= stb || 4L * al * BB <= stb)) r.R = 2;
+  const int rpg = swiglu ? r.R / 2 : r.R;
+  int64_t g = 0;
+  for (int j = 0; j < njobs; ++j) g += (jobsx[j].j.rows + rpg - 1) / rpg;
+  // split a row over KS warps when there are too few row groups to give every
+  // warp of every SM the same amount of work
+  const int units = int(nb / al);
+  const int64_t T = int64_t(c->num_sms) * nw;
+  double best = 0.0;
+  for (int cand : {1, 2, 4}) {
+    if (cand > 1 && units < cand) continue;
+    const int64_t u = g * cand;
+    const int64_t per = (u + T - 1) / T;
+    const double eff = double(u) / double(T * per);
+    if (eff > best + 0.02) {
+      best = eff;
+      r.ks = cand;
+    }
+  }
+  return r;
+}
+
 // the launch plan for `pc` (warps, stage size cap, split-K: 0 = by balance);
 // false when x leaves no shared-memory room for it
 bool make_plan(const Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, const void* W2, const float* x,
@@ -488,18 +547,20 @@ bool make_plan(const Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, const v
   const FmtInfo fi = fmt_info(fmt, int(cols));
   const int ng = int(cols / 32);
   const int pad = 16;  // the unaligned readers may touch 4 bytes past a stage
+  if (norm_g && (ng + 3) / 4 > kMaxChunks) return false;
   GemvArgs& a = P.a;
   a = GemvArgs{};
   int R = 0, kStages = 0, kWarps = 0, head = 0, stb = 0;
-  const int al = fi.align;
+  const int al = seg_granule(fmt, fi.align);
   const int nw = pc.warps;
+  const Arith ar = arith_plan(c, fmt, jobsx, njobs, cols, swiglu);
   for (int ns = c->gemv_stages; ns >= 2 && R == 0; --ns) {
     head = ((fi.xbytes + 12 * ng + 8 + nw * ns * 8 + 127) / 128) * 128;
     const long avail = long(c->smem_optin) - head - pad - c->gemv_static_smem;
     stb = int(avail / (nw * ns)) / 16 * 16;
     if (stb > pc.stage_max) stb = pc.stage_max;
     if (stb < 256) continue;
-    for (int r : {4, 2}) {
+    for (int r : {ar.R}) {
       // whole rows when R of them fit a stage
       if (int64_t(r) * (tma ? rowB : ((rowB + 15) / 16) * 16) <= stb) {
         R = r;
@@ -543,26 +604,10 @@ bool make_plan(const Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, const v
   }
   if (rope) a.rope = *rope;
 
-  // split row groups over KS warps (column parts) when there are too few
-  // groups to give every warp of every SM the same amount of work
-  int ks = pc.ks;
-  const int units = int(nb / al);  // ALIGN-block units per row
-  if (ks > 1 && (kWarps % ks || units < ks)) return false;
-  if (ks == 0) {
-    ks = 1;
-    const int64_t T = int64_t(c->num_sms) * kWarps;
-    double best = 0.0;
-    for (int cand : {1, 2, 4}) {
-      if (kWarps % cand || (cand > 1 && units < cand)) continue;
-      const int64_t u = g * cand;
-      const int64_t per = (u + T - 1) / T;
-      const double eff = double(u) / double(T * per);
-      if (eff > best + 0.02) {
-        best = eff;
-        ks = cand;
-      }
-    }
-  }
+  // the column parts of the shape's arithmetic (arith_plan)
+  const int ks = ar.ks;
+  const int units = int(nb / al);  // granule units per row
+  if (kWarps % ks || (ks > 1 && units < ks)) return false;
   a.ks = ks;
   if (ks == 1) {
     a.pblk[0] = 0;
@@ -655,13 +700,13 @@ nt_status tune(Ctx* c, const std::string& key, int fmt, const GemvJobEx* jobsx, 
     off += (size_t(jobsx[j].j.rows) * 4 + 255) / 256 * 256;
   }
   if (kScratchTune + off > kScratchGemm || kScratchGemm > c->scratch_bytes) {
+    const Arith ar = arith_plan(c, fmt, jobsx, njobs, cols, swiglu);
     std::lock_guard<std::mutex> lk(c->mu);  // no room to tune: keep the default
-    c->gemv_plans[key] = PlanChoice{c->gemv_warps, c->gemv_stage_max, 0};
+    c->gemv_plans[key] = PlanChoice{c->gemv_warps, c->gemv_stage_max, ar.ks, ar.R};
     return NT_OK;
   }
-  const PlanChoice cands[] = {{c->gemv_warps, c->gemv_stage_max, 0}, {12, 16384, 0}, {8, 24576, 0},
-                              {16, 12288, 1},  {12, 12288, 0},      {16, 16384, 0}, {12, 16384, 1},
-                              {8, 16384, 0},   {16, 8192, 0}};
+  const PlanChoice cands[] = {{c->gemv_warps, c->gemv_stage_max, 0}, {12, 16384, 0}, {8, 24576, 0}, {12, 12288, 0},
+                              {16, 16384, 0}, {8, 16384, 0}, {16, 8192, 0}};
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   cudaError_t ce = cudaEventCreate(&e0);
   if (ce == cudaSuccess) ce = cudaEventCreate(&e1);
@@ -716,6 +761,9 @@ nt_status tune(Ctx* c, const std::string& key, int fmt, const GemvJobEx* jobsx, 
   if (e0) cudaEventDestroy(e0);
   if (e1) cudaEventDestroy(e1);
   if (ce != cudaSuccess) return cuda_check(c, ce, "gemv plan tuning");
+  const Arith ar = arith_plan(c, fmt, jobsx, njobs, cols, swiglu);
+  best.R = ar.R;
+  best.ks = ar.ks;
   std::lock_guard<std::mutex> lk(c->mu);
   c->gemv_plans[key] = best;
   return NT_OK;
@@ -750,6 +798,11 @@ nt_status launch_gemv_ex(Ctx* c, int fmt, const GemvJobEx* jobsx, int njobs, con
       pc = c->gemv_plans[key];
     }
     cudaGetLastError();
+  }
+  if (!known && !c->gemv_tune) {
+    const Arith ar = arith_plan(c, fmt, jobsx, njobs, cols, swiglu);
+    std::lock_guard<std::mutex> lk(c->mu);
+    c->gemv_plans[key] = PlanChoice{pc.warps, pc.stage_max, ar.ks, ar.R};
   }
   if (c->dry) return NT_OK;
   // the chosen plan, else fewer warps when x leaves too little shared memory

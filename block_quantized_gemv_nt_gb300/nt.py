@@ -115,6 +115,8 @@ _sig("nt_stream_sync", [_vp, _vp, _i64])
 _sig("nt_debug_fail_copy", [_vp, _ci])
 _sig("nt_debug_host_delay", [_vp, _vp, _i64])
 _sig("nt_debug_stall_waits", [_ci])
+_sig("nt_ctx_gemv_plans", [_vp, _vp, _sz, ctypes.POINTER(_sz)])
+_sig("nt_model_graph_count", [_vp, _vp, ctypes.POINTER(_ci)])
 
 EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "nt_block_bytes", "nt_block_elems",
             "nt_dequant_rows", "nt_gemv_q", "nt_gemv_q_swiglu", "nt_gemv_q_multi", "nt_rmsnorm", "nt_rope",
@@ -123,7 +125,7 @@ EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "
             "nt_attn_decode_static", "nt_layer_blob_layout", "nt_stream_layer", "nt_model_slot", "nt_spec_step",
             "nt_gemm_q", "nt_attn_verify", "nt_plan_residency", "nt_prefill", "nt_sample", "nt_model_set_sampler",
             "nt_host_register", "nt_host_unregister", "nt_stream_sync", "nt_debug_fail_copy", "nt_debug_host_delay",
-            "nt_debug_stall_waits"]
+            "nt_debug_stall_waits", "nt_ctx_gemv_plans", "nt_model_graph_count"]
 
 
 def lib():
@@ -291,6 +293,21 @@ def nt_debug_fail_copy(ctx, nth: int):
 def nt_debug_host_delay(ctx, stream, us: int):
     """A host callback that keeps `stream` busy for `us` microseconds."""
     return ctx.check(_lib.nt_debug_host_delay(ctx.handle, _stream(stream), us))
+
+
+def nt_ctx_gemv_plans(ctx) -> list:
+    """The quant-GEMV plans the context has chosen, one string per launch shape."""
+    n = _sz()
+    ctx.check(_lib.nt_ctx_gemv_plans(ctx.handle, None, 0, ctypes.byref(n)))
+    buf = ctypes.create_string_buffer(n.value)
+    ctx.check(_lib.nt_ctx_gemv_plans(ctx.handle, buf, n.value, ctypes.byref(n)))
+    return [ln for ln in buf.value.decode().splitlines() if ln]
+
+
+def nt_model_graph_count(ctx, model: int) -> int:
+    n = _ci()
+    ctx.check(_lib.nt_model_graph_count(ctx.handle, model, ctypes.byref(n)))
+    return n.value
 
 
 def nt_debug_stall_waits(n: int):

@@ -118,6 +118,17 @@ nt_status nt_debug_stall_waits(int n);
 /* [road] Test helper: a host callback on `stream` that sleeps `us` microseconds
  * (0..10 s), so that the stream stays busy without any GPU work. */
 nt_status nt_debug_host_delay(nt_ctx* ctx, void* stream, int64_t us);
+/* [road] The quant-GEMV launch plans this context has chosen, one line per
+ * launch shape: "fmt/cols/swiglu/tma/rows0/rows1/rows2 -> warps=W
+ * stage_max=B R=r ks=k".  A shape's arithmetic (R rows per lane group, ks
+ * column parts, the segment granule) is fixed by the shape and the device's
+ * SM count and shared memory alone; the first eager launch of a shape times
+ * only launch shapes (warps, stage size) that leave every addition
+ * unchanged, so results are bit-identical across processes and runs on the
+ * same kind of GPU whichever plan the timing picks.  Writes at most cap
+ * bytes (NUL-terminated) to out and the full size, NUL included, to *len;
+ * out may be NULL when cap is 0. */
+nt_status nt_ctx_gemv_plans(nt_ctx* ctx, char* out, size_t cap, size_t* len);
 const char* nt_last_error(const nt_ctx* ctx);
 /* [about] Bytes per block / elements per block of a format (0 for an unknown id). */
 int nt_block_bytes(int fmt);
@@ -300,8 +311,12 @@ nt_status nt_model_destroy(nt_ctx* ctx, nt_model* model);
  * token >= 0: start from (token, pos).  token < 0: continue on the device
  * from the previous step (token = its argmax, pos = its pos + 1) with no host
  * round trip.  next_token_dev (nullable) receives the argmax.  Each distinct
- * (skip mask, logits, next_token) is captured once into a CUDA graph and
- * replayed.  skip_mask_host is n_layers bytes or NULL.  Before the first
+ * (skip mask, sampler setting, next_token given or not) is captured once
+ * into a CUDA graph and replayed; the graph computes into the model's own
+ * buffers and ends by copying the logits (and the token) to the caller's,
+ * so fresh logits_dev / next_token_dev pointers on every call re-point those
+ * copies and capture nothing new (nt_model_graph_count stays constant).
+ * skip_mask_host is n_layers bytes or NULL.  Before the first
  * capture of a graph, a dry pass tunes the GEMV plans of its shapes on
  * `stream` (see nt_gemv_q), which synchronizes that stream once.
  * Streamed layers: inside the same graph, executed streamed layer i (in layer
@@ -312,6 +327,9 @@ nt_status nt_model_destroy(nt_ctx* ctx, nt_model* model);
  * copy (double buffering with 2 slots).  Skipped layers are not copied. */
 nt_status nt_decode_step(nt_ctx* ctx, nt_model* model, int32_t token, int64_t pos, const uint8_t* skip_mask_host,
                          float* logits_dev, int32_t* next_token_dev, void* stream);
+/* [road] The number of step graphs the model holds (decode and speculative
+ * steps): one per distinct skip mask, sampler setting and output shape. */
+nt_status nt_model_graph_count(nt_ctx* ctx, nt_model* model, int* n);
 
 /* [code] (inference/: sampler) Sampling for the model's decode steps
  * (nt_decode_step, nt_prefill's next token stays greedy): every later step
@@ -402,7 +420,9 @@ nt_status nt_model_slot(nt_ctx* ctx, nt_model* model, int slot, void** slot_dev_
  * KV entries written past the accepted ones are overwritten by later steps.
  * logits_dev (nullable) receives the verify logits [k + 1][vocab].  k is
  * 1..7; pos + k < kv_cap.  Streamed layers stream in the verify pass as in
- * nt_decode_step.  One CUDA graph per (k, n_draft_layers, outputs, sampler).
+ * nt_decode_step.  One CUDA graph per (k, n_draft_layers, logits given or
+ * not, sampler); the outputs are copied to the caller's buffers at the end
+ * of the graph, so new output pointers capture nothing new.
  *
  * With the model's sampler set (nt_model_set_sampler, temperature > 0) the
  * step is speculative sampling (Leviathan, Kalman & Matias 2023, section
