@@ -17,6 +17,22 @@
 //    parts in a fixed order (results do not depend on scheduling) and
 //    applies the epilogue: residual add, SwiGLU, RoPE at position pos + m,
 //    or the f16 KV-cache append at pos + m.
+//
+// Tensor-core form (Q8_0, Q4_K, Q6_K; qgemm_mma_kernel below).  The dp4a
+// form pays 3 byte-plane dp4a per weight for every one of the M vectors; an
+// MMA multiplies a 16-row tile of weights by all 8 vector slots at once, so
+// each weight is unpacked once and the per-vector cost nearly vanishes:
+//  * the quants are small integers, exact in f16 (Q8_0 q, Q4_K q, Q6_K
+//    q - 32); they go straight from the staged block bytes into the A
+//    fragments of mma.sync m16n8k16 (f16 in, fp32 accumulate);
+//  * x is split into two f16 terms, hi = f16(x s) and lo = f16(x s - hi),
+//    with a power-of-two s per vector and part, so hi + lo carries x to
+//    about 2^-22; two MMAs per k-step, one per term;
+//  * the MMA's 16 k-indices are mapped to the physical columns so that
+//    each thread's four weights of a row are one contiguous 4-byte word;
+//  * block (and sub-block) scales multiply the fp32 accumulator fragment
+//    once per block; the K-quant mins subtract dmin m_j sum(x) per
+//    sub-block from precomputed sums of x.
 #include "nt_internal.cuh"
 #include "ops.cuh"
 #include "qformats.cuh"
@@ -337,6 +353,397 @@ __global__ void qgemm_epi_kernel(const EpiArgs e) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core form: mma.sync m16n8k16 (f16 x f16 -> f32), 16-row tiles.
+constexpr int kMmaWarps = 8;
+constexpr int kMmaThreads = kMmaWarps * 32;
+constexpr int kMmaRows = 16;                      // rows per tile (the MMA's m)
+constexpr int kMmaSlice = 256;                    // columns per warp (2048 per CTA part)
+constexpr int kXPitch = 2048 + 16;                // f16 per vector row: +32 B keeps the B loads conflict-free
+constexpr int kMmaGroups = 2048 / 32;             // 32-column groups per part
+
+struct MmaArgs {
+  GemmJobDev job[3];  // g0: first 16-row tile of the job; rb: first row in the row space
+  int njobs;
+  int64_t total_tiles;
+  int64_t total_rows;
+  const float* X;
+  int64_t ldx;
+  const float* norm_g;
+  float eps;
+  int M;
+  int cols, nb, cwb, nparts;
+  int64_t rowB;
+  int segB;  // stage bytes per row (the part's blocks, rounded up to 16)
+  int SB;    // bytes per stage (16 rows)
+  int NS;    // stages
+  float* part;
+  unsigned* err;
+  int stall;
+};
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// bytes 0,1 (lo) or 2,3 (hi) of w, each an unsigned value u < 1024, as the
+// f16 pair (u - bias): f16(1024 + u) is exact, built by placing u in the
+// mantissa under the exponent of 1024
+__device__ __forceinline__ uint32_t u8lo_f16(uint32_t w, uint32_t bias2) { return hsub2(__byte_perm(w, 0x64646464u, 0x4140), bias2); }
+__device__ __forceinline__ uint32_t u8hi_f16(uint32_t w, uint32_t bias2) { return hsub2(__byte_perm(w, 0x64646464u, 0x4342), bias2); }
+constexpr uint32_t kBias1024 = 0x64006400u;  // f16 pair (1024, 1024)
+constexpr uint32_t kBias1056 = 0x64206420u;  // (1056, 1056): 1024 + the Q6_K offset 32
+constexpr uint32_t kBias1152 = 0x64806480u;  // (1152, 1152): 1024 + 128 for sign-flipped int8
+
+// a little-endian word at a 2-byte-aligned shared address
+__device__ __forceinline__ uint32_t lds32_a2(const uint8_t* p) {
+  const uint32_t mis = smem_u32(p) & 2u;
+  const uint32_t* b = reinterpret_cast<const uint32_t*>(p - mis);
+  return mis ? __funnelshift_r(b[0], b[1], 16) : b[0];
+}
+
+template <int FMT>
+struct MmaRows;
+
+// Q8_0: per block (32 columns, 2 k-steps) the 4-byte words of qs for rows
+// g and g + 8, signed -> f16; one scale d per row and block.
+template <>
+struct MmaRows<NT_Q8_0> {
+  __device__ static void block(const uint8_t* r0, const uint8_t* r1, int b, int t, int c0, const uint32_t* xh,
+                               const uint32_t* xl, const float*, float (&acc)[4]) {
+    const uint8_t* p0 = r0 + b * 34;
+    const uint8_t* p1 = r1 + b * 34;
+    const float d0 = __half2float(*reinterpret_cast<const __half*>(p0));
+    const float d1 = __half2float(*reinterpret_cast<const __half*>(p1));
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub) {
+      const uint32_t w0 = lds32_a2(p0 + 2 + 16 * sub + 4 * t) ^ 0x80808080u;
+      const uint32_t w1 = lds32_a2(p1 + 2 + 16 * sub + 4 * t) ^ 0x80808080u;
+      const uint32_t a[4] = {u8lo_f16(w0, kBias1152), u8lo_f16(w1, kBias1152), u8hi_f16(w0, kBias1152),
+                             u8hi_f16(w1, kBias1152)};
+      const int col = c0 + 16 * sub;
+      const uint2 bh = *reinterpret_cast<const uint2*>(xh + col / 2);
+      const uint2 bl = *reinterpret_cast<const uint2*>(xl + col / 2);
+      mma16816(c, a, bh.x, bh.y);
+      mma16816(c, a, bl.x, bl.y);
+    }
+    acc[0] = fmaf(d0, c[0], acc[0]);
+    acc[1] = fmaf(d0, c[1], acc[1]);
+    acc[2] = fmaf(d1, c[2], acc[2]);
+    acc[3] = fmaf(d1, c[3], acc[3]);
+  }
+  static constexpr int BPS = kMmaSlice / 32;  // blocks per warp slice
+};
+
+// Q4_K: per block (256 columns): for each pair of sub-blocks (2c, 2c+1) the
+// words of qs[32c..32c+31] give both sub-blocks' quants (low / high
+// nibbles); scale d sc_j and min dmin m_j per row and sub-block.
+template <>
+struct MmaRows<NT_Q4_K> {
+  __device__ static void block(const uint8_t* r0, const uint8_t* r1, int b, int t, int c0, const uint32_t* xh,
+                               const uint32_t* xl, const float* xs, float (&acc)[4]) {
+    const uint8_t* p0 = r0 + b * 144;
+    const uint8_t* p1 = r1 + b * 144;
+    const uint4 h0 = *reinterpret_cast<const uint4*>(p0);
+    const uint4 h1 = *reinterpret_cast<const uint4*>(p1);
+    const float d0 = qf::h2f(h0.x & 0xFFFFu), dm0 = qf::h2f(h0.x >> 16);
+    const float d1 = qf::h2f(h1.x & 0xFFFFu), dm1 = qf::h2f(h1.x >> 16);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float sa0, sb0, ma0, mb0, sa1, sb1, ma1, mb1;
+      qf::kq_scales(h0.y, h0.z, h0.w, c, sa0, sb0, ma0, mb0);
+      qf::kq_scales(h1.y, h1.z, h1.w, c, sa1, sb1, ma1, mb1);
+      float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(p0 + 16 + 32 * c + 16 * s + 4 * t);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(p1 + 16 + 32 * c + 16 * s + 4 * t);
+        const uint32_t l0 = w0 & 0x0F0F0F0Fu, l1 = w1 & 0x0F0F0F0Fu;
+        const uint32_t u0 = (w0 >> 4) & 0x0F0F0F0Fu, u1 = (w1 >> 4) & 0x0F0F0F0Fu;
+        const uint32_t al[4] = {u8lo_f16(l0, kBias1024), u8lo_f16(l1, kBias1024), u8hi_f16(l0, kBias1024),
+                                u8hi_f16(l1, kBias1024)};
+        const uint32_t au[4] = {u8lo_f16(u0, kBias1024), u8lo_f16(u1, kBias1024), u8hi_f16(u0, kBias1024),
+                                u8hi_f16(u1, kBias1024)};
+        const int colA = c0 + 64 * c + 16 * s, colB = colA + 32;
+        const uint2 bha = *reinterpret_cast<const uint2*>(xh + colA / 2);
+        const uint2 bla = *reinterpret_cast<const uint2*>(xl + colA / 2);
+        const uint2 bhb = *reinterpret_cast<const uint2*>(xh + colB / 2);
+        const uint2 blb = *reinterpret_cast<const uint2*>(xl + colB / 2);
+        mma16816(ca, al, bha.x, bha.y);
+        mma16816(ca, al, bla.x, bla.y);
+        mma16816(cb, au, bhb.x, bhb.y);
+        mma16816(cb, au, blb.x, blb.y);
+      }
+      // sums of x over the two sub-blocks for this thread's vectors 2t, 2t + 1
+      const int grp = (c0 + 64 * c) / 32;
+      const float2 xa = *reinterpret_cast<const float2*>(xs + grp * 8 + 2 * t);
+      const float2 xb = *reinterpret_cast<const float2*>(xs + (grp + 1) * 8 + 2 * t);
+      const float ka0 = d0 * sa0, kb0 = d0 * sb0, ka1 = d1 * sa1, kb1 = d1 * sb1;
+      const float na0 = dm0 * ma0, nb0 = dm0 * mb0, na1 = dm1 * ma1, nb1 = dm1 * mb1;
+      acc[0] += fmaf(ka0, ca[0], fmaf(kb0, cb[0], -fmaf(na0, xa.x, nb0 * xb.x)));
+      acc[1] += fmaf(ka0, ca[1], fmaf(kb0, cb[1], -fmaf(na0, xa.y, nb0 * xb.y)));
+      acc[2] += fmaf(ka1, ca[2], fmaf(kb1, cb[2], -fmaf(na1, xa.x, nb1 * xb.x)));
+      acc[3] += fmaf(ka1, ca[3], fmaf(kb1, cb[3], -fmaf(na1, xa.y, nb1 * xb.y)));
+    }
+  }
+  static constexpr int BPS = kMmaSlice / 256;
+};
+
+// Q6_K: per block (256 columns) and half h, step s: the words of ql (two
+// runs) and qh give the 6-bit quants of the four 16-column sub-blocks
+// (g = 0..3); q - 32 as f16; scale d sc per row and sub-block.
+template <>
+struct MmaRows<NT_Q6_K> {
+  __device__ static void block(const uint8_t* r0, const uint8_t* r1, int b, int t, int c0, const uint32_t* xh,
+                               const uint32_t* xl, const float*, float (&acc)[4]) {
+    const uint8_t* p0 = r0 + b * 210;
+    const uint8_t* p1 = r1 + b * 210;
+    const float d0 = __half2float(*reinterpret_cast<const __half*>(p0 + 208));
+    const float d1 = __half2float(*reinterpret_cast<const __half*>(p1 + 208));
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const int lo = 64 * h + 16 * s + 4 * t, qh = 128 + 32 * h + 16 * s + 4 * t;
+        const uint32_t A0 = lds32_a2(p0 + lo), B0 = lds32_a2(p0 + lo + 32), H0 = lds32_a2(p0 + qh);
+        const uint32_t A1 = lds32_a2(p1 + lo), B1 = lds32_a2(p1 + lo + 32), H1 = lds32_a2(p1 + qh);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t L0 = (g & 1) ? B0 : A0, L1 = (g & 1) ? B1 : A1;
+          const int nib = 4 * (g >> 1);
+          const uint32_t q0 = ((L0 >> nib) & 0x0F0F0F0Fu) | (((H0 >> (2 * g)) & 0x03030303u) << 4);
+          const uint32_t q1 = ((L1 >> nib) & 0x0F0F0F0Fu) | (((H1 >> (2 * g)) & 0x03030303u) << 4);
+          const uint32_t a[4] = {u8lo_f16(q0, kBias1056), u8lo_f16(q1, kBias1056), u8hi_f16(q0, kBias1056),
+                                 u8hi_f16(q1, kBias1056)};
+          const int col = c0 + 128 * h + 32 * g + 16 * s;
+          const uint2 bh = *reinterpret_cast<const uint2*>(xh + col / 2);
+          const uint2 bl = *reinterpret_cast<const uint2*>(xl + col / 2);
+          float c[4] = {0.f, 0.f, 0.f, 0.f};
+          mma16816(c, a, bh.x, bh.y);
+          mma16816(c, a, bl.x, bl.y);
+          const int j = 8 * h + 2 * g + s;  // sub-block: scales[j]
+          const float k0 = d0 * float(*reinterpret_cast<const int8_t*>(p0 + 192 + j));
+          const float k1 = d1 * float(*reinterpret_cast<const int8_t*>(p1 + 192 + j));
+          acc[0] = fmaf(k0, c[0], acc[0]);
+          acc[1] = fmaf(k0, c[1], acc[1]);
+          acc[2] = fmaf(k1, c[2], acc[2]);
+          acc[3] = fmaf(k1, c[3], acc[3]);
+        }
+      }
+    }
+  }
+  static constexpr int BPS = kMmaSlice / 256;
+};
+
+__device__ __forceinline__ void mma_locate(const MmaArgs& a, int64_t tile, int& j, int64_t& r0, int& nr) {
+  j = 0;
+  while (j + 1 < a.njobs && tile >= a.job[j + 1].g0) ++j;
+  r0 = (tile - a.job[j].g0) * kMmaRows;
+  const int64_t left = a.job[j].rows - r0;
+  nr = left < kMmaRows ? int(left) : kMmaRows;
+}
+
+// shared layout: x hi [8][kXPitch] f16, x lo [8][kXPitch] f16, sums of x
+// [kMmaGroups][8] f32, vector scales [8], tile reductions [2][warps][16][8]
+// f32, stage barriers, then the ring of NS stages of 16 rows
+constexpr size_t kMmaXh = 0;
+constexpr size_t kMmaXl = kMmaXh + size_t(8) * kXPitch * 2;
+constexpr size_t kMmaXs = kMmaXl + size_t(8) * kXPitch * 2;
+constexpr size_t kMmaSc = kMmaXs + size_t(kMmaGroups) * 8 * 4;
+constexpr size_t kMmaRed = kMmaSc + 8 * 4 + 32;
+constexpr size_t kMmaBar = kMmaRed + size_t(2) * kMmaWarps * kMmaRows * 8 * 4;
+__host__ __device__ constexpr size_t mma_ring_off(int NS) { return ((kMmaBar + size_t(NS) * 8 + 127) / 128) * 128; }
+
+template <int FMT>
+__global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs a) {
+  using F = Q<FMT>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __half* xh = reinterpret_cast<__half*>(smem + kMmaXh);
+  __half* xl = reinterpret_cast<__half*>(smem + kMmaXl);
+  float* xs = reinterpret_cast<float*>(smem + kMmaXs);
+  float* xsc = reinterpret_cast<float*>(smem + kMmaSc);
+  float* red = reinterpret_cast<float*>(smem + kMmaRed);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kMmaBar);
+  uint8_t* ring = smem + mma_ring_off(a.NS);
+  const int NS = a.NS;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int p = blockIdx.y;
+  const int blk_lo = p * a.cwb;
+  const int blk_hi = min(a.nb, blk_lo + a.cwb);
+  const int pcols = (blk_hi - blk_lo) * F::BE;  // columns of this part
+  const int64_t nct = gridDim.x;
+  const int n_items = blockIdx.x < a.total_tiles ? int((a.total_tiles - blockIdx.x + nct - 1) / nct) : 0;
+  const uint64_t pol = policy_evict_first();
+  const int cap = a.stall ? kStallSpin : kMaxSpin;
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(smem_u32(full + s), 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  // warp 0 loads item i (tile blockIdx.x + i * gridDim.x) into stage i % NS
+  auto issue = [&](int i) {
+    int j, nr;
+    int64_t r0;
+    mma_locate(a, blockIdx.x + int64_t(i) * nct, j, r0, nr);
+    const int st = i % NS;
+    const uint32_t bar = smem_u32(full + st);
+    const uint32_t bytes_row = uint32_t(blk_hi - blk_lo) * F::BB;
+    if (lane == 0) mbar_arrive_expect_tx(bar, uint32_t(nr) * bytes_row);
+    __syncwarp();
+    if (lane < nr && !a.stall)
+      bulk_g2s(smem_u32(ring + size_t(st) * a.SB + size_t(lane) * a.segB),
+               a.job[j].W + (r0 + lane) * a.rowB + size_t(blk_lo) * F::BB, bytes_row, bar, pol);
+    __syncwarp();
+  };
+  if (warp == 0) {
+    const int pre = n_items < NS ? n_items : NS;
+    for (int i = 0; i < pre; ++i) issue(i);
+  }
+  pdl_trigger();
+  pdl_wait();
+
+  // ---- prologue: warp m holds vector m (zeros for m >= M): the part's columns,
+  // RMS-normalised when asked, scaled by a power of two, split into f16 hi + lo,
+  // and the sums of x over each 32 columns (scaled likewise)
+  {
+    const int m = warp;
+    float inv = 1.f;
+    const float* xr = a.X + int64_t(m) * a.ldx;
+    if (m < a.M && a.norm_g) {
+      // sum of squares per 128-column chunk, then over the chunks in order
+      float tot = 0.f;
+      for (int c = 0; c < a.cols; c += 128) {
+        float ss = 0.f;
+        if (c + 4 * lane < a.cols) {
+          const float4 v = *reinterpret_cast<const float4*>(xr + c + 4 * lane);
+          ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, v.w * v.w)));
+        }
+        tot += warp_sum(ss);
+      }
+      inv = rsqrtf(tot / float(a.cols) + a.eps);
+    }
+    // lane l holds columns 64 l .. 64 l + 63 of the part: 16 float4
+    float4 v[16];
+    float mx = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int col = 64 * lane + 4 * k;
+      float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (m < a.M && col < pcols) {
+        const int gc = blk_lo * F::BE + col;
+        x4 = *reinterpret_cast<const float4*>(xr + gc);
+        if (a.norm_g) {
+          const float4 gg = *reinterpret_cast<const float4*>(a.norm_g + gc);
+          x4.x = x4.x * inv * gg.x;
+          x4.y = x4.y * inv * gg.y;
+          x4.z = x4.z * inv * gg.z;
+          x4.w = x4.w * inv * gg.w;
+        }
+      }
+      v[k] = x4;
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    // scale 2^sh puts the vector's largest |x| in [2^13, 2^14): far inside the f16 range
+    int sh = 0;
+    if (mx > 0.f) sh = min(100, max(-100, 13 - (int((__float_as_uint(mx) >> 23) & 0xFFu) - 127)));
+    const float scl = ldexpf(1.f, sh);
+    if (lane == 0) xsc[m] = m < a.M ? ldexpf(1.f, -sh) : 0.f;
+    __half* hr = xh + m * kXPitch;
+    __half* lr = xl + m * kXPitch;
+    float gs0 = 0.f, gs1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float e[4] = {v[k].x * scl, v[k].y * scl, v[k].z * scl, v[k].w * scl};
+      __half hi[4], lo[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        hi[i] = __float2half_rn(e[i]);
+        lo[i] = __float2half_rn(e[i] - __half2float(hi[i]));
+      }
+      const int col = 64 * lane + 4 * k;
+      *reinterpret_cast<uint2*>(hr + col) = make_uint2(
+          uint32_t(__half_as_ushort(hi[0])) | (uint32_t(__half_as_ushort(hi[1])) << 16),
+          uint32_t(__half_as_ushort(hi[2])) | (uint32_t(__half_as_ushort(hi[3])) << 16));
+      *reinterpret_cast<uint2*>(lr + col) = make_uint2(
+          uint32_t(__half_as_ushort(lo[0])) | (uint32_t(__half_as_ushort(lo[1])) << 16),
+          uint32_t(__half_as_ushort(lo[2])) | (uint32_t(__half_as_ushort(lo[3])) << 16));
+      const float s4 = (e[0] + e[1]) + (e[2] + e[3]);
+      if (k < 8) gs0 += s4;
+      else gs1 += s4;
+    }
+    xs[(2 * lane) * 8 + m] = gs0;
+    xs[(2 * lane + 1) * 8 + m] = gs1;
+    __syncthreads();
+  }
+
+  float* redw = red;  // [2][warps][16][8]
+  for (int i = 0; i < n_items; ++i) {
+    const int st = i % NS;
+    const uint8_t* stage = ring + size_t(st) * a.SB;
+    const bool ok = mbar_wait(smem_u32(full + st), uint32_t(i / NS) & 1u, cap);
+    const bool dead = !__all_sync(0xffffffffu, ok);
+    if (dead && lane == 0) flag_error(a.err, kErrWaitTimeout);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (!dead) {
+      const uint8_t* r0p = stage + size_t(g) * a.segB;
+      const uint8_t* r1p = stage + size_t(g + 8) * a.segB;
+      const uint32_t* xh32 = reinterpret_cast<const uint32_t*>(xh + g * kXPitch) + 2 * t;
+      const uint32_t* xl32 = reinterpret_cast<const uint32_t*>(xl + g * kXPitch) + 2 * t;
+      // this warp's slice: kMmaSlice columns = BPS blocks
+      const int b0 = warp * MmaRows<FMT>::BPS;
+#pragma unroll 1
+      for (int bb = 0; bb < MmaRows<FMT>::BPS; ++bb) {
+        const int b = b0 + bb;
+        if (b >= blk_hi - blk_lo) break;  // warp-uniform
+        MmaRows<FMT>::block(r0p, r1p, b, t, b * F::BE, xh32, xl32, xs, acc);
+      }
+    }
+    // the 8 warps' partial tiles meet in shared memory, in warp order
+    float* rw = redw + (size_t(i & 1) * kMmaWarps + warp) * kMmaRows * 8;
+    rw[g * 8 + 2 * t] = acc[0];
+    rw[g * 8 + 2 * t + 1] = acc[1];
+    rw[(g + 8) * 8 + 2 * t] = acc[2];
+    rw[(g + 8) * 8 + 2 * t + 1] = acc[3];
+    __syncthreads();
+    if (warp == 0 && i + NS < n_items) issue(i + NS);  // every warp is done with this stage
+    if (tid >= 32 && tid < 32 + kMmaRows * 8) {
+      const int e = tid - 32, row = e >> 3, n = e & 7;
+      int j, nr;
+      int64_t r0;
+      mma_locate(a, blockIdx.x + int64_t(i) * nct, j, r0, nr);
+      if (row < nr && n < a.M) {
+        const float* rb = redw + size_t(i & 1) * kMmaWarps * kMmaRows * 8 + row * 8 + n;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMmaWarps; ++w) v += rb[w * kMmaRows * 8];
+        a.part[(int64_t(p) * a.M + n) * a.total_rows + a.job[j].rb + r0 + row] = v * xsc[n];
+      }
+    }
+  }
+}
+
+size_t mma_smem(int fmt, int NS) {
+  const int cwb = 2048 / block_elems(fmt);
+  const int segB = ((cwb * block_bytes(fmt) + 15) / 16) * 16;
+  return mma_ring_off(NS) + size_t(NS) * kMmaRows * segB + 16;  // the unaligned readers may touch 4 bytes past a row
+}
+
+bool mma_format(int fmt) { return fmt == NT_Q8_0 || fmt == NT_Q4_K || fmt == NT_Q6_K; }
+
 template <int FMT>
 cudaError_t gemm_launch_t(const Ctx* c, const GemmArgs& a, dim3 grid, size_t smem, cudaStream_t st) {
   return launch_k(c, qgemm_kernel<FMT>, grid, dim3(kGemmThreads), smem, st, a);
@@ -396,6 +803,9 @@ nt_status configure_gemm(Ctx* c) {
   allow(qgemm_kernel<NT_Q6_K>);
   allow(qgemm_kernel<NT_F16>);
   allow(qgemm_kernel<NT_F32>);
+  allow(qgemm_mma_kernel<NT_Q8_0>);
+  allow(qgemm_mma_kernel<NT_Q4_K>);
+  allow(qgemm_mma_kernel<NT_Q6_K>);
   c->gemm_static_smem = st;
   return cuda_check(c, e, "gemm shared-memory attribute");
 }
@@ -432,6 +842,53 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
   if (need > part_bytes)
     return set_err(c, NT_ERR_OOM, "gemm: %zu scratch bytes needed for the partial sums, %zu available", need,
                    part_bytes);
+  // the tensor-core form: its formats, bulk-copy alignment (every part's row
+  // bytes a multiple of 16), and 2048-column parts (the dp4a form's too)
+  const bool mma = c->gemm_mma && mma_format(fmt) && tma && part_cols(fmt) == 2048 &&
+                   (int64_t(cwb) * BB) % 16 == 0 && ((nb % cwb) * BB) % 16 == 0;
+  if (mma) {
+    MmaArgs ma{};
+    int64_t tiles = 0;
+    for (int j = 0; j < njobs; ++j) {
+      ma.job[j] = a.job[j];
+      ma.job[j].g0 = tiles;
+      tiles += (jobs[j].rows + kMmaRows - 1) / kMmaRows;
+    }
+    ma.njobs = njobs;
+    ma.total_tiles = tiles;
+    ma.total_rows = rb;
+    ma.X = X;
+    ma.ldx = ldx;
+    ma.norm_g = norm_g;
+    ma.eps = eps;
+    ma.M = M;
+    ma.cols = int(cols);
+    ma.nb = int(nb);
+    ma.cwb = cwb;
+    ma.nparts = nparts;
+    ma.rowB = rowB;
+    ma.segB = ((cwb * BB + 15) / 16) * 16;
+    ma.NS = 8;
+    while (ma.NS > 2 && mma_smem(fmt, ma.NS) + size_t(c->gemm_static_smem) > c->smem_optin) --ma.NS;
+    ma.SB = kMmaRows * ma.segB;
+    ma.part = part;
+    ma.err = c->err_flag;
+    ma.stall = take_stall(st);
+    const size_t msmem = mma_smem(fmt, ma.NS);
+    if (msmem + size_t(c->gemm_static_smem) > c->smem_optin)
+      return set_err(c, NT_ERR_INVALID_ARG, "gemm: no shared-memory plan for the tensor-core form");
+    int gx = (c->num_sms + nparts - 1) / nparts;
+    if (gx > tiles) gx = int(tiles);
+    const dim3 grid(gx, nparts);
+    cudaError_t err;
+    switch (fmt) {
+      case NT_Q8_0: err = launch_k(c, qgemm_mma_kernel<NT_Q8_0>, grid, dim3(kMmaThreads), msmem, st, ma); break;
+      case NT_Q4_K: err = launch_k(c, qgemm_mma_kernel<NT_Q4_K>, grid, dim3(kMmaThreads), msmem, st, ma); break;
+      default: err = launch_k(c, qgemm_mma_kernel<NT_Q6_K>, grid, dim3(kMmaThreads), msmem, st, ma); break;
+    }
+    nt_status s = cuda_check(c, err, "qgemm (tensor-core) launch");
+    if (s) return s;
+  }
   a.njobs = njobs;
   a.total_groups = g;
   a.total_rows = rb;
@@ -451,26 +908,28 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
   a.tma = tma;
   a.part = part;
   a.err = c->err_flag;
-  const size_t smem = gemm_smem(fmt, M);
-  if (smem + size_t(c->gemm_static_smem) > c->smem_optin)
-    return set_err(c, NT_ERR_INVALID_ARG, "gemm: no shared-memory plan for M=%d", M);
-  // one CTA per SM in all: the parts side by side
-  int gx = (c->num_sms + nparts - 1) / nparts;
-  const int64_t need_x = (g + kGemmWarps - 1) / kGemmWarps;
-  if (gx > need_x) gx = int(need_x);
-  const dim3 grid(gx, nparts);
-  cudaError_t err;
-  switch (fmt) {
-    case NT_Q8_0: err = gemm_launch_t<NT_Q8_0>(c, a, grid, smem, st); break;
-    case NT_Q4_0: err = gemm_launch_t<NT_Q4_0>(c, a, grid, smem, st); break;
-    case NT_Q4_K: err = gemm_launch_t<NT_Q4_K>(c, a, grid, smem, st); break;
-    case NT_Q5_K: err = gemm_launch_t<NT_Q5_K>(c, a, grid, smem, st); break;
-    case NT_Q6_K: err = gemm_launch_t<NT_Q6_K>(c, a, grid, smem, st); break;
-    case NT_F16: err = gemm_launch_t<NT_F16>(c, a, grid, smem, st); break;
-    default: err = gemm_launch_t<NT_F32>(c, a, grid, smem, st); break;
+  if (!mma) {
+    const size_t smem = gemm_smem(fmt, M);
+    if (smem + size_t(c->gemm_static_smem) > c->smem_optin)
+      return set_err(c, NT_ERR_INVALID_ARG, "gemm: no shared-memory plan for M=%d", M);
+    // one CTA per SM in all: the parts side by side
+    int gx = (c->num_sms + nparts - 1) / nparts;
+    const int64_t need_x = (g + kGemmWarps - 1) / kGemmWarps;
+    if (gx > need_x) gx = int(need_x);
+    const dim3 grid(gx, nparts);
+    cudaError_t err;
+    switch (fmt) {
+      case NT_Q8_0: err = gemm_launch_t<NT_Q8_0>(c, a, grid, smem, st); break;
+      case NT_Q4_0: err = gemm_launch_t<NT_Q4_0>(c, a, grid, smem, st); break;
+      case NT_Q4_K: err = gemm_launch_t<NT_Q4_K>(c, a, grid, smem, st); break;
+      case NT_Q5_K: err = gemm_launch_t<NT_Q5_K>(c, a, grid, smem, st); break;
+      case NT_Q6_K: err = gemm_launch_t<NT_Q6_K>(c, a, grid, smem, st); break;
+      case NT_F16: err = gemm_launch_t<NT_F16>(c, a, grid, smem, st); break;
+      default: err = gemm_launch_t<NT_F32>(c, a, grid, smem, st); break;
+    }
+    nt_status s = cuda_check(c, err, "qgemm launch");
+    if (s) return s;
   }
-  nt_status s = cuda_check(c, err, "qgemm launch");
-  if (s) return s;
 
   e.njobs = njobs;
   e.total_pairs = pb;
