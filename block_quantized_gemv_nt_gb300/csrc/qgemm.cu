@@ -355,10 +355,10 @@ __global__ void qgemm_epi_kernel(const EpiArgs e) {
 
 // ---------------------------------------------------------------------------
 // Tensor-core form: mma.sync m16n8k16 (f16 x f16 -> f32), 16-row tiles.
-constexpr int kMmaWarps = 8;
+constexpr int kMmaWarps = 16;
 constexpr int kMmaThreads = kMmaWarps * 32;
 constexpr int kMmaRows = 16;                      // rows per tile (the MMA's m)
-constexpr int kMmaSlice = 256;                    // columns per warp (2048 per CTA part)
+constexpr int kMmaSlice = 128;                    // columns per warp (2048 per CTA part)
 constexpr int kXPitch = 2048 + 16;                // f16 per vector row: +32 B keeps the B loads conflict-free
 constexpr int kMmaGroups = 2048 / 32;             // 32-column groups per part
 
@@ -442,7 +442,14 @@ struct MmaRows<NT_Q8_0> {
     acc[2] = fmaf(d1, c[2], acc[2]);
     acc[3] = fmaf(d1, c[3], acc[3]);
   }
-  static constexpr int BPS = kMmaSlice / 32;  // blocks per warp slice
+  // a warp's slice: blocks b0 .. b0 + 3 of the part (32 columns each)
+  __device__ static void slice(const uint8_t* r0, const uint8_t* r1, int warp, int nblk, int t, const uint32_t* xh,
+                               const uint32_t* xl, const float* xs, float (&acc)[4]) {
+    const int b0 = 4 * warp;
+#pragma unroll
+    for (int bb = 0; bb < 4; ++bb)
+      if (b0 + bb < nblk) block(r0, r1, b0 + bb, t, (b0 + bb) * 32, xh, xl, xs, acc);
+  }
 };
 
 // Q4_K: per block (256 columns): for each pair of sub-blocks (2c, 2c+1) the
@@ -450,16 +457,21 @@ struct MmaRows<NT_Q8_0> {
 // nibbles); scale d sc_j and min dmin m_j per row and sub-block.
 template <>
 struct MmaRows<NT_Q4_K> {
-  __device__ static void block(const uint8_t* r0, const uint8_t* r1, int b, int t, int c0, const uint32_t* xh,
+  // a warp's slice: the half `half` (sub-block pairs 2 half, 2 half + 1) of block b
+  __device__ static void slice(const uint8_t* r0, const uint8_t* r1, int warp, int nblk, int t, const uint32_t* xh,
                                const uint32_t* xl, const float* xs, float (&acc)[4]) {
+    const int b = warp >> 1, half = warp & 1;
+    if (b >= nblk) return;
     const uint8_t* p0 = r0 + b * 144;
     const uint8_t* p1 = r1 + b * 144;
+    const int c0 = b * 256;
     const uint4 h0 = *reinterpret_cast<const uint4*>(p0);
     const uint4 h1 = *reinterpret_cast<const uint4*>(p1);
     const float d0 = qf::h2f(h0.x & 0xFFFFu), dm0 = qf::h2f(h0.x >> 16);
     const float d1 = qf::h2f(h1.x & 0xFFFFu), dm1 = qf::h2f(h1.x >> 16);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = 2 * half + cc;
       float sa0, sb0, ma0, mb0, sa1, sb1, ma1, mb1;
       qf::kq_scales(h0.y, h0.z, h0.w, c, sa0, sb0, ma0, mb0);
       qf::kq_scales(h1.y, h1.z, h1.w, c, sa1, sb1, ma1, mb1);
@@ -496,7 +508,6 @@ struct MmaRows<NT_Q4_K> {
       acc[3] += fmaf(ka1, ca[3], fmaf(kb1, cb[3], -fmaf(na1, xa.y, nb1 * xb.y)));
     }
   }
-  static constexpr int BPS = kMmaSlice / 256;
 };
 
 // Q6_K: per block (256 columns) and half h, step s: the words of ql (two
@@ -504,14 +515,17 @@ struct MmaRows<NT_Q4_K> {
 // (g = 0..3); q - 32 as f16; scale d sc per row and sub-block.
 template <>
 struct MmaRows<NT_Q6_K> {
-  __device__ static void block(const uint8_t* r0, const uint8_t* r1, int b, int t, int c0, const uint32_t* xh,
+  // a warp's slice: the half h = warp & 1 (128 columns) of block warp >> 1
+  __device__ static void slice(const uint8_t* r0, const uint8_t* r1, int warp, int nblk, int t, const uint32_t* xh,
                                const uint32_t* xl, const float*, float (&acc)[4]) {
+    const int b = warp >> 1, h = warp & 1;
+    if (b >= nblk) return;
     const uint8_t* p0 = r0 + b * 210;
     const uint8_t* p1 = r1 + b * 210;
+    const int c0 = b * 256;
     const float d0 = __half2float(*reinterpret_cast<const __half*>(p0 + 208));
     const float d1 = __half2float(*reinterpret_cast<const __half*>(p1 + 208));
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    {
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         const int lo = 64 * h + 16 * s + 4 * t, qh = 128 + 32 * h + 16 * s + 4 * t;
@@ -542,7 +556,6 @@ struct MmaRows<NT_Q6_K> {
       }
     }
   }
-  static constexpr int BPS = kMmaSlice / 256;
 };
 
 __device__ __forceinline__ void mma_locate(const MmaArgs& a, int64_t tile, int& j, int64_t& r0, int& nr) {
@@ -566,6 +579,7 @@ __host__ __device__ constexpr size_t mma_ring_off(int NS) { return ((kMmaBar + s
 
 template <int FMT>
 __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs a) {
+  static_assert(kMmaWarps * kMmaSlice == 2048, "a CTA's warps cover one 2048-column part");
   using F = Q<FMT>;
   extern __shared__ __align__(128) uint8_t smem[];
   __half* xh = reinterpret_cast<__half*>(smem + kMmaXh);
@@ -614,10 +628,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
   pdl_trigger();
   pdl_wait();
 
-  // ---- prologue: warp m holds vector m (zeros for m >= M): the part's columns,
-  // RMS-normalised when asked, scaled by a power of two, split into f16 hi + lo,
-  // and the sums of x over each 32 columns (scaled likewise)
-  {
+  // ---- prologue: warp m < 8 holds vector m (zeros for m >= M): the part's
+  // columns, RMS-normalised when asked, scaled by a power of two, split into
+  // f16 hi + lo, and the sums of x over each 32 columns (scaled likewise)
+  if (warp < 8) {
     const int m = warp;
     float inv = 1.f;
     const float* xr = a.X + int64_t(m) * a.ldx;
@@ -634,11 +648,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
       }
       inv = rsqrtf(tot / float(a.cols) + a.eps);
     }
-    // lane l holds columns 64 l .. 64 l + 63 of the part: 16 float4
-    float4 v[16];
-    float mx = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    // lane l holds columns 64 l .. 64 l + 63 of the part: 16 float4, read
+    // twice (the largest |x| first, then the conversion) to stay in registers
+    auto load4 = [&](int k) {
       const int col = 64 * lane + 4 * k;
       float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
       if (m < a.M && col < pcols) {
@@ -652,7 +664,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
           x4.w = x4.w * inv * gg.w;
         }
       }
-      v[k] = x4;
+      return x4;
+    };
+    float mx = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float4 x4 = load4(k);
       mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w))));
     }
 #pragma unroll
@@ -665,14 +682,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
     __half* hr = xh + m * kXPitch;
     __half* lr = xl + m * kXPitch;
     float gs0 = 0.f, gs1 = 0.f;
-#pragma unroll
+#pragma unroll 4
     for (int k = 0; k < 16; ++k) {
-      const float e[4] = {v[k].x * scl, v[k].y * scl, v[k].z * scl, v[k].w * scl};
+      const float4 x4 = load4(k);
+      const float e[4] = {x4.x * scl, x4.y * scl, x4.z * scl, x4.w * scl};
       __half hi[4], lo[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        hi[i] = __float2half_rn(e[i]);
-        lo[i] = __float2half_rn(e[i] - __half2float(hi[i]));
+      for (int q = 0; q < 4; ++q) {
+        hi[q] = __float2half_rn(e[q]);
+        lo[q] = __float2half_rn(e[q] - __half2float(hi[q]));
       }
       const int col = 64 * lane + 4 * k;
       *reinterpret_cast<uint2*>(hr + col) = make_uint2(
@@ -687,8 +705,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
     }
     xs[(2 * lane) * 8 + m] = gs0;
     xs[(2 * lane + 1) * 8 + m] = gs1;
-    __syncthreads();
   }
+  __syncthreads();
 
   float* redw = red;  // [2][warps][16][8]
   for (int i = 0; i < n_items; ++i) {
@@ -703,16 +721,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
       const uint8_t* r1p = stage + size_t(g + 8) * a.segB;
       const uint32_t* xh32 = reinterpret_cast<const uint32_t*>(xh + g * kXPitch) + 2 * t;
       const uint32_t* xl32 = reinterpret_cast<const uint32_t*>(xl + g * kXPitch) + 2 * t;
-      // this warp's slice: kMmaSlice columns = BPS blocks
-      const int b0 = warp * MmaRows<FMT>::BPS;
-#pragma unroll 1
-      for (int bb = 0; bb < MmaRows<FMT>::BPS; ++bb) {
-        const int b = b0 + bb;
-        if (b >= blk_hi - blk_lo) break;  // warp-uniform
-        MmaRows<FMT>::block(r0p, r1p, b, t, b * F::BE, xh32, xl32, xs, acc);
-      }
+      // this warp's slice of kMmaSlice columns
+      MmaRows<FMT>::slice(r0p, r1p, warp, blk_hi - blk_lo, t, xh32, xl32, xs, acc);
     }
-    // the 8 warps' partial tiles meet in shared memory, in warp order
+    // the warps' partial tiles meet in shared memory, in warp order
     float* rw = redw + (size_t(i & 1) * kMmaWarps + warp) * kMmaRows * 8;
     rw[g * 8 + 2 * t] = acc[0];
     rw[g * 8 + 2 * t + 1] = acc[1];
@@ -736,9 +748,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
   }
 }
 
-size_t mma_smem(int fmt, int NS) {
+// bytes between the staged rows: a multiple of 16 (bulk copies) holding an
+// odd number of 16-byte units, so the eight row groups of a warp read eight
+// different bank quads
+int mma_segB(int fmt) {
   const int cwb = 2048 / block_elems(fmt);
-  const int segB = ((cwb * block_bytes(fmt) + 15) / 16) * 16;
+  int u = (cwb * block_bytes(fmt) + 15) / 16;
+  if (!(u & 1)) ++u;
+  return 16 * u;
+}
+
+size_t mma_smem(int fmt, int NS) {
+  const int segB = mma_segB(fmt);
   return mma_ring_off(NS) + size_t(NS) * kMmaRows * segB + 16;  // the unaligned readers may touch 4 bytes past a row
 }
 
@@ -867,7 +888,7 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
     ma.cwb = cwb;
     ma.nparts = nparts;
     ma.rowB = rowB;
-    ma.segB = ((cwb * BB + 15) / 16) * 16;
+    ma.segB = mma_segB(fmt);
     ma.NS = 8;
     while (ma.NS > 2 && mma_smem(fmt, ma.NS) + size_t(c->gemm_static_smem) > c->smem_optin) --ma.NS;
     ma.SB = kMmaRows * ma.segB;
