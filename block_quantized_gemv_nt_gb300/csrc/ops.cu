@@ -246,16 +246,26 @@ __global__ void __launch_bounds__(kAttnThreads, (G >= 16 ? 1 : 2)) attn_kernel(c
     for (int h = 0; h < HS; ++h) sc[h] = 0.f;
     if (valid) {
       const __half* krow = Ks + j * kHD;
-#pragma unroll 4
-      for (int c = 0; c < 32; ++c) {
-        const int cc = (c + lane) & 31;  // lane-rotated 4-dim chunk: distinct banks across the warp
-        const float4 k = h4(*reinterpret_cast<const uint2*>(krow + 4 * cc));
+      // four partial sums per head (4-dim chunks c = 4i + r go to sum r): four
+      // short dependency chains instead of one of 128 FMAs
+      float sp[HS][4];
 #pragma unroll
-        for (int h = 0; h < HS; ++h) {
-          const float4 qv = *reinterpret_cast<const float4*>(qh + h * kHD + 4 * cc);
-          sc[h] = fmaf(qv.x, k.x, fmaf(qv.y, k.y, fmaf(qv.z, k.z, fmaf(qv.w, k.w, sc[h]))));
+      for (int h = 0; h < HS; ++h) sp[h][0] = sp[h][1] = sp[h][2] = sp[h][3] = 0.f;
+#pragma unroll 2
+      for (int c4 = 0; c4 < 32; c4 += 4) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int cc = (c4 + r + lane) & 31;  // lane-rotated 4-dim chunk: distinct banks across the warp
+          const float4 k = h4(*reinterpret_cast<const uint2*>(krow + 4 * cc));
+#pragma unroll
+          for (int h = 0; h < HS; ++h) {
+            const float4 qv = *reinterpret_cast<const float4*>(qh + h * kHD + 4 * cc);
+            sp[h][r] = fmaf(qv.x, k.x, fmaf(qv.y, k.y, fmaf(qv.z, k.z, fmaf(qv.w, k.w, sp[h][r]))));
+          }
         }
       }
+#pragma unroll
+      for (int h = 0; h < HS; ++h) sc[h] = (sp[h][0] + sp[h][1]) + (sp[h][2] + sp[h][3]);
     }
     float pj[HS];
 #pragma unroll
@@ -272,6 +282,7 @@ __global__ void __launch_bounds__(kAttnThreads, (G >= 16 ? 1 : 2)) attn_kernel(c
       m[h] = mn;
     }
     const int nt = min(32, np - t0);
+#pragma unroll 4
     for (int jj = 0; jj < nt; ++jj) {
       const float4 v = h4(*reinterpret_cast<const uint2*>(Vs + (t0 + jj) * kHD + 4 * lane));
 #pragma unroll

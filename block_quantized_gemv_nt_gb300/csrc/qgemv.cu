@@ -219,10 +219,13 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
   pdl_trigger();
   pdl_wait();
 
-  // ---- prologue: x (optionally RMS-normalised) -> 24-bit fixed point per 32-column group.
-  // 8 lanes per group of 32 columns, 4 columns per lane; a warp covers 4 groups
-  // per pass.  All of a lane's x loads are issued first (one memory round
-  // trip), the RMSNorm sum of squares comes from the same registers.
+  // ---- prologue: x (times the RMSNorm gain when asked) -> 24-bit fixed point
+  // per 32-column group.  8 lanes per group of 32 columns, 4 columns per lane;
+  // a warp covers 4 groups per pass.  All of a lane's x loads are issued first
+  // (one memory round trip); the RMSNorm sum of squares comes from the same
+  // registers, and its scalar rsqrt(mean x^2 + eps) multiplies the row sums in
+  // the epilogue, so the quantization waits for no CTA-wide reduction.
+  float inv = 1.f;
   {
     // sum of squares of x per 128-column chunk, then over the chunks in
     // index order: the same additions whatever the warp count
@@ -242,9 +245,8 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
       }
     };
     if (whole) load_passes(0);
-    float inv = 1.f;
+    const int nchunk = (ng + 3) / 4;  // a warp's pass covers chunk warp + pass * nwarps
     if (a.norm_g) {
-      const int nchunk = (ng + 3) / 4;  // a warp's pass covers chunk warp + pass * nwarps
       if (whole) {
 #pragma unroll
         for (int k = 0; k < kPF; ++k) {
@@ -265,10 +267,6 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
           if (lane == 0) red[ch] = ss;
         }
       }
-      __syncthreads();
-      float tot = 0.f;
-      for (int ch = 0; ch < nchunk; ++ch) tot += red[ch];
-      inv = rsqrtf(tot / float(a.cols) + a.eps);
     }
     for (int p0 = 0; p0 < npass; p0 += kPF) {
       if (!whole) load_passes(p0);
@@ -281,15 +279,20 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
         float4 x4 = v[k];
         if (a.norm_g && live) {
           const float4 g = *reinterpret_cast<const float4*>(a.norm_g + col);
-          x4.x = x4.x * inv * g.x;
-          x4.y = x4.y * inv * g.y;
-          x4.z = x4.z * inv * g.z;
-          x4.w = x4.w * inv * g.w;
+          x4.x *= g.x;
+          x4.y *= g.y;
+          x4.z *= g.z;
+          x4.w *= g.w;
         }
         put_x4<FMT>(x4, live, grp, sub, xsm, psum, gscale);
       }
     }
     __syncthreads();
+    if (a.norm_g) {
+      float tot = 0.f;
+      for (int ch = 0; ch < nchunk; ++ch) tot += red[ch];
+      inv = rsqrtf(tot / float(a.cols) + a.eps);
+    }
   }
   if (my_groups == 0) return;
   const XS xs{xsm, gscale, psum};
@@ -355,6 +358,7 @@ __global__ void __launch_bounds__(MAXT, 1) qgemv_kernel(const GemvArgs a) {
           for (int p = 1; p < KS; ++p) mine += xb[p * R + lane];
       }
       if (part == 0) {
+        mine *= inv;  // the RMSNorm scalar (1 without a norm)
         const float other = __shfl_down_sync(0xffffffffu, mine, R / 2);  // lane i: row i + R/2
         int j, nr;
         int64_t r0;
