@@ -141,6 +141,8 @@ nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes) {
   c->gemv_tune = env_int("NT_GEMV_TUNE", 0, 1, 1) != 0;
   c->attn_fill = env_int("NT_ATTN_FILL", 0, 1, 1) != 0;
   c->gemm_mma = env_int("NT_GEMM_MMA", 0, 1, 1) != 0;
+  c->gemm_warps = env_int("NT_GEMM_WARPS", 8, 16, 16) / 4 * 4;
+  c->gemm_stages = env_int("NT_GEMM_STAGES", 2, 8, 4);
   c->scratch_bytes = scratch_bytes ? scratch_bytes : (size_t(64) << 20);
   if (c->scratch_bytes < (size_t(1) << 20)) c->scratch_bytes = size_t(1) << 20;
   if (cudaMalloc(&c->scratch, c->scratch_bytes) != cudaSuccess) {

@@ -47,7 +47,9 @@ struct Ctx {
   int gemv_stage_max = 12288;
   int gemv_static_smem = 2048;   // largest static shared memory of the GEMV kernels
   int gemm_static_smem = 1024;   // same for the verify-GEMM kernels
-  bool gemm_mma = true;          // verify GEMM: the tensor-core form for Q8_0 / Q4_K / Q6_K
+  bool gemm_mma = true;
+  int gemm_warps = 16;           // tensor-core verify GEMM: warps per CTA, stages per warp at most
+  int gemm_stages = 4;          // verify GEMM: the tensor-core form for Q8_0 / Q4_K / Q6_K
   std::string last_error;
   std::mutex mu;
   bool attn_fill = true;         // attention splits: also one CTA per SM (else by positions only)

@@ -3,11 +3,11 @@
 // principales": the VRAM-resident layers draft, the whole model verifies):
 // Y[m] = W X[m] for M <= 8 activation vectors, every weight byte read once.
 //
-// GB300 design.  M = 5 is still far from a tensor-core shape (an MMA tile is
-// 64 or 128 rows of one operand), and the block formats carry one scale per
-// 16 or 32 weights, so the contraction stays on the integer pipes: the same
-// 24-bit fixed-point x planes and dp4a dot products as the M = 1 GEMV, with
-// the weights staged once per CTA and reused for all M vectors.
+// GB300 design.  Two forms.  The integer form (every format) keeps the
+// contraction on the integer pipes: the same 24-bit fixed-point x planes and
+// dp4a dot products as the M = 1 GEMV, with the weights staged once per CTA
+// and reused for all M vectors.  The tensor-core form (below) serves Q8_0,
+// Q4_K and Q6_K whenever the part rows meet the bulk-copy alignment.
 //  * grid (X, P): the columns are cut into P parts (2048 columns; 1024 /
 //    512 for F16 / F32) so that M vectors of x fit in shared memory; CTA
 //    (x, p) holds part p of every vector and walks row groups of R = 2 rows.
@@ -32,7 +32,11 @@
 //    each thread's four weights of a row are one contiguous 4-byte word;
 //  * block (and sub-block) scales multiply the fp32 accumulator fragment
 //    once per block; the K-quant mins subtract dmin m_j sum(x) per
-//    sub-block from precomputed sums of x.
+//    sub-block from precomputed sums of x;
+//  * each warp owns whole 16-row tiles of its CTA's column part and streams
+//    them through a private ring of bulk copies, so no barrier or reduction
+//    joins the warps; the parts are narrowed for small matrices (a
+//    function of the shape alone) so that every SM has tiles to work on.
 #include "nt_internal.cuh"
 #include "ops.cuh"
 #include "qformats.cuh"
@@ -355,10 +359,9 @@ __global__ void qgemm_epi_kernel(const EpiArgs e) {
 
 // ---------------------------------------------------------------------------
 // Tensor-core form: mma.sync m16n8k16 (f16 x f16 -> f32), 16-row tiles.
-constexpr int kMmaWarps = 16;
+constexpr int kMmaWarps = 16;                     // warps per CTA at most
 constexpr int kMmaThreads = kMmaWarps * 32;
 constexpr int kMmaRows = 16;                      // rows per tile (the MMA's m)
-constexpr int kMmaSlice = 128;                    // columns per warp (2048 per CTA part)
 constexpr int kXPitch = 2048 + 16;                // f16 per vector row: +32 B keeps the B loads conflict-free
 constexpr int kMmaGroups = 2048 / 32;             // 32-column groups per part
 
@@ -418,17 +421,38 @@ struct MmaRows;
 // g and g + 8, signed -> f16; one scale d per row and block.
 template <>
 struct MmaRows<NT_Q8_0> {
-  __device__ static void block(const uint8_t* r0, const uint8_t* r1, int b, int t, int c0, const uint32_t* xh,
-                               const uint32_t* xl, const float*, float (&acc)[4]) {
-    const uint8_t* p0 = r0 + b * 34;
-    const uint8_t* p1 = r1 + b * 34;
-    const float d0 = __half2float(*reinterpret_cast<const __half*>(p0));
-    const float d1 = __half2float(*reinterpret_cast<const __half*>(p1));
+  // block b of a staged row whose first byte is 4-byte aligned (R0, R1: rows
+  // g and g + 8 as words).  Blocks come in pairs of 68 bytes = 17 words: the
+  // even block's quants sit 2 bytes off a word boundary (one funnel shift by
+  // 16 per word), the odd block's are word-aligned.
+  __device__ static void block_w(const uint32_t* R0, const uint32_t* R1, int b, int t, int c0, const uint32_t* xh,
+                                 const uint32_t* xl, float (&acc)[4]) {
+    const int pw = 17 * (b >> 1);
+    float d0, d1;
+    uint32_t w[2][2];  // [sub][row]
+    if ((b & 1) == 0) {
+      d0 = qf::h2f(R0[pw] & 0xFFFFu);
+      d1 = qf::h2f(R1[pw] & 0xFFFFu);
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        const int k = pw + 4 * sub + t;
+        w[sub][0] = __funnelshift_r(R0[k], R0[k + 1], 16);
+        w[sub][1] = __funnelshift_r(R1[k], R1[k + 1], 16);
+      }
+    } else {
+      d0 = qf::h2f(R0[pw + 8] >> 16);
+      d1 = qf::h2f(R1[pw + 8] >> 16);
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        const int k = pw + 9 + 4 * sub + t;
+        w[sub][0] = R0[k];
+        w[sub][1] = R1[k];
+      }
+    }
     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int sub = 0; sub < 2; ++sub) {
-      const uint32_t w0 = lds32_a2(p0 + 2 + 16 * sub + 4 * t) ^ 0x80808080u;
-      const uint32_t w1 = lds32_a2(p1 + 2 + 16 * sub + 4 * t) ^ 0x80808080u;
+      const uint32_t w0 = w[sub][0] ^ 0x80808080u, w1 = w[sub][1] ^ 0x80808080u;
       const uint32_t a[4] = {u8lo_f16(w0, kBias1152), u8lo_f16(w1, kBias1152), u8hi_f16(w0, kBias1152),
                              u8hi_f16(w1, kBias1152)};
       const int col = c0 + 16 * sub;
@@ -442,14 +466,6 @@ struct MmaRows<NT_Q8_0> {
     acc[2] = fmaf(d1, c[2], acc[2]);
     acc[3] = fmaf(d1, c[3], acc[3]);
   }
-  // a warp's slice: blocks b0 .. b0 + 3 of the part (32 columns each)
-  __device__ static void slice(const uint8_t* r0, const uint8_t* r1, int warp, int nblk, int t, const uint32_t* xh,
-                               const uint32_t* xl, const float* xs, float (&acc)[4]) {
-    const int b0 = 4 * warp;
-#pragma unroll
-    for (int bb = 0; bb < 4; ++bb)
-      if (b0 + bb < nblk) block(r0, r1, b0 + bb, t, (b0 + bb) * 32, xh, xl, xs, acc);
-  }
 };
 
 // Q4_K: per block (256 columns): for each pair of sub-blocks (2c, 2c+1) the
@@ -457,10 +473,10 @@ struct MmaRows<NT_Q8_0> {
 // nibbles); scale d sc_j and min dmin m_j per row and sub-block.
 template <>
 struct MmaRows<NT_Q4_K> {
-  // a warp's slice: the half `half` (sub-block pairs 2 half, 2 half + 1) of block b
-  __device__ static void slice(const uint8_t* r0, const uint8_t* r1, int warp, int nblk, int t, const uint32_t* xh,
-                               const uint32_t* xl, const float* xs, float (&acc)[4]) {
-    const int b = warp >> 1, half = warp & 1;
+  // half-block hb: the half `half` (sub-block pairs 2 half, 2 half + 1) of block b = hb / 2
+  __device__ static void half_block(const uint8_t* r0, const uint8_t* r1, int hb, int nblk, int t,
+                                    const uint32_t* xh, const uint32_t* xl, const float* xs, float (&acc)[4]) {
+    const int b = hb >> 1, half = hb & 1;
     if (b >= nblk) return;
     const uint8_t* p0 = r0 + b * 144;
     const uint8_t* p1 = r1 + b * 144;
@@ -515,10 +531,10 @@ struct MmaRows<NT_Q4_K> {
 // (g = 0..3); q - 32 as f16; scale d sc per row and sub-block.
 template <>
 struct MmaRows<NT_Q6_K> {
-  // a warp's slice: the half h = warp & 1 (128 columns) of block warp >> 1
-  __device__ static void slice(const uint8_t* r0, const uint8_t* r1, int warp, int nblk, int t, const uint32_t* xh,
-                               const uint32_t* xl, const float*, float (&acc)[4]) {
-    const int b = warp >> 1, h = warp & 1;
+  // half-block hb: the half h = hb & 1 (128 columns) of block hb / 2
+  __device__ static void half_block(const uint8_t* r0, const uint8_t* r1, int hb, int nblk, int t,
+                                    const uint32_t* xh, const uint32_t* xl, const float*, float (&acc)[4]) {
+    const int b = hb >> 1, h = hb & 1;
     if (b >= nblk) return;
     const uint8_t* p0 = r0 + b * 210;
     const uint8_t* p1 = r1 + b * 210;
@@ -567,64 +583,120 @@ __device__ __forceinline__ void mma_locate(const MmaArgs& a, int64_t tile, int& 
 }
 
 // shared layout: x hi [8][kXPitch] f16, x lo [8][kXPitch] f16, sums of x
-// [kMmaGroups][8] f32, vector scales [8], tile reductions [2][warps][16][8]
-// f32, stage barriers, then the ring of NS stages of 16 rows
+// [kMmaGroups][8] f32, vector scales [8], stage barriers [warps][NS], then
+// each warp's ring of NS stages of 16 staged rows
 constexpr size_t kMmaXh = 0;
 constexpr size_t kMmaXl = kMmaXh + size_t(8) * kXPitch * 2;
 constexpr size_t kMmaXs = kMmaXl + size_t(8) * kXPitch * 2;
 constexpr size_t kMmaSc = kMmaXs + size_t(kMmaGroups) * 8 * 4;
-constexpr size_t kMmaRed = kMmaSc + 8 * 4 + 32;
-constexpr size_t kMmaBar = kMmaRed + size_t(2) * kMmaWarps * kMmaRows * 8 * 4;
-__host__ __device__ constexpr size_t mma_ring_off(int NS) { return ((kMmaBar + size_t(NS) * 8 + 127) / 128) * 128; }
+constexpr size_t kMmaBar = kMmaSc + 8 * 4 + 32;
+__host__ __device__ constexpr size_t mma_ring_off(int warps, int NS) {
+  return ((kMmaBar + size_t(warps) * NS * 8 + 127) / 128) * 128;
+}
 
+// blocks per staged segment of a row: about 256 bytes of weights per row
+__host__ __device__ constexpr int mma_seg_blocks(int fmt) { return fmt == NT_Q8_0 ? 8 : fmt == NT_Q4_K ? 2 : 1; }
+
+// one segment of 16 rows: the blocks [0, nbk) of each staged row, every
+// row's data starting at byte `o` of its pitch
+template <int FMT>
+__device__ __forceinline__ void mma_segment(const uint8_t* r0, const uint8_t* r1, int nbk, int t, const uint32_t* xh,
+                                            const uint32_t* xl, const float* xs, float (&acc)[4]) {
+  constexpr int S = mma_seg_blocks(FMT);
+  // a whole segment is straight-line code (every offset a constant); a
+  // part's ragged last segment takes the loop
+  if constexpr (FMT == NT_Q8_0) {
+    // a segment starts at a multiple of 8 blocks (272 bytes) from a 16-byte
+    // aligned row start: word-aligned
+    const uint32_t* R0 = reinterpret_cast<const uint32_t*>(r0);
+    const uint32_t* R1 = reinterpret_cast<const uint32_t*>(r1);
+    if (nbk == S) {
+#pragma unroll
+      for (int b = 0; b < S; ++b) MmaRows<FMT>::block_w(R0, R1, b, t, b * 32, xh, xl, acc);
+    } else {
+#pragma unroll 1
+      for (int b = 0; b < nbk; ++b) MmaRows<FMT>::block_w(R0, R1, b, t, b * 32, xh, xl, acc);
+    }
+  } else {
+    if (nbk == S) {
+#pragma unroll
+      for (int h = 0; h < 2 * S; ++h) MmaRows<FMT>::half_block(r0, r1, h, S, t, xh, xl, xs, acc);
+    } else {
+#pragma unroll 1
+      for (int h = 0; h < 2 * nbk; ++h) MmaRows<FMT>::half_block(r0, r1, h, nbk, t, xh, xl, xs, acc);
+    }
+  }
+}
+
+// Each warp owns whole 16-row tiles of its CTA's column part: it walks the
+// part in segments through its own ring of bulk copies (16 row copies per
+// stage, mbarrier completion), accumulates the MMA results of every segment
+// in registers, and writes the tile's partial sums itself.  No two warps
+// share a tile, so there is no barrier and no reduction between warps.
 template <int FMT>
 __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs a) {
-  static_assert(kMmaWarps * kMmaSlice == 2048, "a CTA's warps cover one 2048-column part");
   using F = Q<FMT>;
+  constexpr int S = mma_seg_blocks(FMT);
   extern __shared__ __align__(128) uint8_t smem[];
   __half* xh = reinterpret_cast<__half*>(smem + kMmaXh);
   __half* xl = reinterpret_cast<__half*>(smem + kMmaXl);
   float* xs = reinterpret_cast<float*>(smem + kMmaXs);
   float* xsc = reinterpret_cast<float*>(smem + kMmaSc);
-  float* red = reinterpret_cast<float*>(smem + kMmaRed);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kMmaBar);
-  uint8_t* ring = smem + mma_ring_off(a.NS);
   const int NS = a.NS;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kMmaBar) + warp * NS;
+  uint8_t* ring = smem + mma_ring_off(nwarps, NS) + size_t(warp) * NS * a.SB;
   const int g = lane >> 2, t = lane & 3;
   const int p = blockIdx.y;
   const int blk_lo = p * a.cwb;
   const int blk_hi = min(a.nb, blk_lo + a.cwb);
   const int pcols = (blk_hi - blk_lo) * F::BE;  // columns of this part
-  const int64_t nct = gridDim.x;
-  const int n_items = blockIdx.x < a.total_tiles ? int((a.total_tiles - blockIdx.x + nct - 1) / nct) : 0;
+  const int nseg = (blk_hi - blk_lo + S - 1) / S;
+  // this warp's tiles: ws, ws + stride, ...
+  const int64_t ws = int64_t(blockIdx.x) * nwarps + warp, stride = int64_t(gridDim.x) * nwarps;
+  const int ntiles = ws < a.total_tiles ? int((a.total_tiles - ws + stride - 1) / stride) : 0;
+  const int n_items = ntiles * nseg;
   const uint64_t pol = policy_evict_first();
   const int cap = a.stall ? kStallSpin : kMaxSpin;
 
-  if (tid == 0) {
+  if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(smem_u32(full + s), 1);
     fence_barrier_init();
   }
   __syncwarp();
-  // warp 0 loads item i (tile blockIdx.x + i * gridDim.x) into stage i % NS
-  auto issue = [&](int i) {
-    int j, nr;
-    int64_t r0;
-    mma_locate(a, blockIdx.x + int64_t(i) * nct, j, r0, nr);
-    const int st = i % NS;
-    const uint32_t bar = smem_u32(full + st);
-    const uint32_t bytes_row = uint32_t(blk_hi - blk_lo) * F::BB;
-    if (lane == 0) mbar_arrive_expect_tx(bar, uint32_t(nr) * bytes_row);
+  // item i = (tile ws + (i / nseg) stride, segment i % nseg) into stage i % NS.
+  // Each row's segment is copied as the 16-byte-aligned range around it
+  // (rows start 16-byte aligned, so the range stays inside the row); the
+  // segment's bytes start `o` bytes into the staged row.
+  auto seg_off = [&](int sg) { return int((int64_t(blk_lo + sg * S) * F::BB) & 15); };
+  // issue cursor: tile ordinal, segment, stage slot; the tile's rows cached
+  int it_t = 0, it_sg = 0, it_slot = 0, it_nr = 0;
+  const uint8_t* it_row = nullptr;  // lane < 16: its row of the issue tile (null past the tile's rows)
+  auto issue_next = [&]() {
+    if (it_sg == 0) {
+      int j;
+      int64_t r0;
+      mma_locate(a, ws + int64_t(it_t) * stride, j, r0, it_nr);
+      it_row = lane < it_nr ? a.job[j].W + (r0 + lane) * a.rowB : nullptr;
+    }
+    const int b0 = blk_lo + it_sg * S, nbk = min(S, blk_hi - b0);
+    const int64_t lo = int64_t(b0) * F::BB, hi = lo + int64_t(nbk) * F::BB;
+    const int64_t lo16 = lo & ~int64_t(15), hi16 = (hi + 15) & ~int64_t(15);
+    const uint32_t bytes = uint32_t(hi16 - lo16);
+    const uint32_t bar = smem_u32(full + it_slot);
+    if (lane == 0) mbar_arrive_expect_tx(bar, uint32_t(it_nr) * bytes);
     __syncwarp();
-    if (lane < nr && !a.stall)
-      bulk_g2s(smem_u32(ring + size_t(st) * a.SB + size_t(lane) * a.segB),
-               a.job[j].W + (r0 + lane) * a.rowB + size_t(blk_lo) * F::BB, bytes_row, bar, pol);
-    __syncwarp();
+    if (it_row && !a.stall)
+      bulk_g2s(smem_u32(ring + size_t(it_slot) * a.SB + size_t(lane) * a.segB), it_row + lo16, bytes, bar, pol);
+    if (++it_sg == nseg) {
+      it_sg = 0;
+      ++it_t;
+    }
+    if (++it_slot == NS) it_slot = 0;
   };
-  if (warp == 0) {
-    const int pre = n_items < NS ? n_items : NS;
-    for (int i = 0; i < pre; ++i) issue(i);
-  }
+  // weights do not depend on x: start streaming before waiting for its producer
+  const int pre = n_items < NS - 1 ? n_items : NS - 1;
+  for (int i = 0; i < pre; ++i) issue_next();
   pdl_trigger();
   pdl_wait();
 
@@ -707,60 +779,80 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
     xs[(2 * lane + 1) * 8 + m] = gs1;
   }
   __syncthreads();
+  if (n_items == 0) return;
 
-  float* redw = red;  // [2][warps][16][8]
+  const uint32_t* xh32 = reinterpret_cast<const uint32_t*>(xh + g * kXPitch) + 2 * t;
+  const uint32_t* xl32 = reinterpret_cast<const uint32_t*>(xl + g * kXPitch) + 2 * t;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  bool dead = false;
+  // consume cursor: stage slot and phase, segment, tile ordinal
+  int cs = 0, csg = 0, ct = 0;
+  uint32_t cph = 0;
   for (int i = 0; i < n_items; ++i) {
-    const int st = i % NS;
-    const uint8_t* stage = ring + size_t(st) * a.SB;
-    const bool ok = mbar_wait(smem_u32(full + st), uint32_t(i / NS) & 1u, cap);
-    const bool dead = !__all_sync(0xffffffffu, ok);
-    if (dead && lane == 0) flag_error(a.err, kErrWaitTimeout);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (!dead) {
-      const uint8_t* r0p = stage + size_t(g) * a.segB;
-      const uint8_t* r1p = stage + size_t(g + 8) * a.segB;
-      const uint32_t* xh32 = reinterpret_cast<const uint32_t*>(xh + g * kXPitch) + 2 * t;
-      const uint32_t* xl32 = reinterpret_cast<const uint32_t*>(xl + g * kXPitch) + 2 * t;
-      // this warp's slice of kMmaSlice columns
-      MmaRows<FMT>::slice(r0p, r1p, warp, blk_hi - blk_lo, t, xh32, xl32, xs, acc);
+      if (i + NS - 1 < n_items) issue_next();  // into the stage consumed last
+      const bool ok = mbar_wait(smem_u32(full + cs), cph, cap);
+      if (!__all_sync(0xffffffffu, ok)) {
+        // flag it, wait (bounded) for the copies still in flight, stream no more
+        if (lane == 0) flag_error(a.err, kErrWaitTimeout);
+        int q = cs;
+        uint32_t ph = cph;
+        for (int n = i + 1; n < min(n_items, i + NS); ++n) {
+          if (++q == NS) {
+            q = 0;
+            ph ^= 1u;
+          }
+          mbar_wait(smem_u32(full + q), ph, cap);
+        }
+        dead = true;
+      }
     }
-    // the warps' partial tiles meet in shared memory, in warp order
-    float* rw = redw + (size_t(i & 1) * kMmaWarps + warp) * kMmaRows * 8;
-    rw[g * 8 + 2 * t] = acc[0];
-    rw[g * 8 + 2 * t + 1] = acc[1];
-    rw[(g + 8) * 8 + 2 * t] = acc[2];
-    rw[(g + 8) * 8 + 2 * t + 1] = acc[3];
-    __syncthreads();
-    if (warp == 0 && i + NS < n_items) issue(i + NS);  // every warp is done with this stage
-    if (tid >= 32 && tid < 32 + kMmaRows * 8) {
-      const int e = tid - 32, row = e >> 3, n = e & 7;
+    if (!dead) {
+      const int b0 = csg * S, nbk = min(S, blk_hi - blk_lo - b0);
+      const uint8_t* stage = ring + size_t(cs) * a.SB + seg_off(csg);
+      const int c0 = b0 * F::BE;  // first column of the segment in the part
+      mma_segment<FMT>(stage + size_t(g) * a.segB, stage + size_t(g + 8) * a.segB, nbk, t, xh32 + c0 / 2,
+                       xl32 + c0 / 2, xs + (c0 / 32) * 8, acc);
+    }
+    __syncwarp();
+    if (++csg == nseg) {
+      // the tile's partial sums: rows g, g + 8 and vectors 2t, 2t + 1 of this thread
+      csg = 0;
       int j, nr;
       int64_t r0;
-      mma_locate(a, blockIdx.x + int64_t(i) * nct, j, r0, nr);
-      if (row < nr && n < a.M) {
-        const float* rb = redw + size_t(i & 1) * kMmaWarps * kMmaRows * 8 + row * 8 + n;
-        float v = 0.f;
+      mma_locate(a, ws + int64_t(ct) * stride, j, r0, nr);
+      const int64_t rbase = a.job[j].rb + r0;
 #pragma unroll
-        for (int w = 0; w < kMmaWarps; ++w) v += rb[w * kMmaRows * 8];
-        a.part[(int64_t(p) * a.M + n) * a.total_rows + a.job[j].rb + r0 + row] = v * xsc[n];
+      for (int e = 0; e < 4; ++e) {
+        const int row = g + 8 * (e >> 1), n = 2 * t + (e & 1);
+        if (!dead && row < nr && n < a.M) a.part[(int64_t(p) * a.M + n) * a.total_rows + rbase + row] = acc[e] * xsc[n];
+        acc[e] = 0.f;
       }
+      ++ct;
+    }
+    if (++cs == NS) {
+      cs = 0;
+      cph ^= 1u;
     }
   }
 }
 
-// bytes between the staged rows: a multiple of 16 (bulk copies) holding an
-// odd number of 16-byte units, so the eight row groups of a warp read eight
-// different bank quads
+// bytes between the staged rows: room for a segment's 16-byte-aligned range,
+// a multiple of 16 holding an odd number of 16-byte units, so the eight row
+// groups of a warp read eight different bank quads
 int mma_segB(int fmt) {
-  const int cwb = 2048 / block_elems(fmt);
-  int u = (cwb * block_bytes(fmt) + 15) / 16;
+  const int sb = mma_seg_blocks(fmt) * block_bytes(fmt);
+  // segments of a multiple of 16 bytes start 16-byte aligned; otherwise the
+  // range may start up to 14 bytes before the segment
+  int u = sb % 16 == 0 ? sb / 16 : (sb + 14 + 15) / 16;
   if (!(u & 1)) ++u;
   return 16 * u;
 }
 
-size_t mma_smem(int fmt, int NS) {
+size_t mma_smem(int fmt, int warps, int NS) {
   const int segB = mma_segB(fmt);
-  return mma_ring_off(NS) + size_t(NS) * kMmaRows * segB + 16;  // the unaligned readers may touch 4 bytes past a row
+  // + 16: the unaligned readers may touch 4 bytes past a row
+  return mma_ring_off(warps, NS) + size_t(warps) * NS * kMmaRows * segB + 16;
 }
 
 bool mma_format(int fmt) { return fmt == NT_Q8_0 || fmt == NT_Q4_K || fmt == NT_Q6_K; }
@@ -800,8 +892,26 @@ size_t gemm_smem(int fmt, int M) {
 
 int gemm_parts(int fmt, int64_t cols) { return int((cols + part_cols(fmt) - 1) / part_cols(fmt)); }
 
+// Blocks per column part of the tensor-core form: 2048 columns, halved (down
+// to one staged segment) while the 16-row tiles times the parts give fewer
+// than 4096 warp tasks, so that small matrices still occupy every SM.  A
+// function of the shape alone: the parts fix the order of the additions.
+static int mma_part_blocks(int fmt, int64_t tiles, int64_t nb) {
+  int cwb = 2048 / block_elems(fmt);
+  const int S = mma_seg_blocks(fmt);
+  while (cwb > S && tiles * ((nb + cwb - 1) / cwb) < 4096) cwb /= 2;
+  return cwb;
+}
+
 size_t gemm_scratch_bytes(int fmt, int64_t total_rows, int64_t cols, int M) {
-  return size_t(gemm_parts(fmt, cols)) * size_t(M) * size_t(total_rows) * sizeof(float);
+  int64_t parts = gemm_parts(fmt, cols);
+  if (mma_format(fmt)) {
+    // fewer tiles than ceil(rows / 16) summed per job never occur, and more tiles never ask for more parts
+    const int64_t nb = cols / block_elems(fmt);
+    const int cwb = mma_part_blocks(fmt, (total_rows + kMmaRows - 1) / kMmaRows, nb);
+    parts = std::max<int64_t>(parts, (nb + cwb - 1) / cwb);
+  }
+  return size_t(parts) * size_t(M) * size_t(total_rows) * sizeof(float);
 }
 
 nt_status configure_gemm(Ctx* c) {
@@ -857,19 +967,20 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
     pb += (J.rows + 1) / 2;
   }
   if (g == 0) return NT_OK;
-  const int cwb = part_cols(fmt) / BE;
+  // the tensor-core form: its formats and bulk-copy alignment (rows of a
+  // multiple of 16 bytes at 16-byte-aligned addresses)
+  const bool mma = c->gemm_mma && mma_format(fmt) && tma;
+  int64_t tiles = 0;
+  for (int j = 0; j < njobs; ++j) tiles += (jobs[j].rows + kMmaRows - 1) / kMmaRows;
+  const int cwb = mma ? mma_part_blocks(fmt, tiles, nb) : part_cols(fmt) / BE;
   const int nparts = int((nb + cwb - 1) / cwb);
   const size_t need = size_t(nparts) * M * size_t(rb) * sizeof(float);
   if (need > part_bytes)
     return set_err(c, NT_ERR_OOM, "gemm: %zu scratch bytes needed for the partial sums, %zu available", need,
                    part_bytes);
-  // the tensor-core form: its formats, bulk-copy alignment (every part's row
-  // bytes a multiple of 16), and 2048-column parts (the dp4a form's too)
-  const bool mma = c->gemm_mma && mma_format(fmt) && tma && part_cols(fmt) == 2048 &&
-                   (int64_t(cwb) * BB) % 16 == 0 && ((nb % cwb) * BB) % 16 == 0;
   if (mma) {
     MmaArgs ma{};
-    int64_t tiles = 0;
+    tiles = 0;
     for (int j = 0; j < njobs; ++j) {
       ma.job[j] = a.job[j];
       ma.job[j].g0 = tiles;
@@ -889,23 +1000,31 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
     ma.nparts = nparts;
     ma.rowB = rowB;
     ma.segB = mma_segB(fmt);
-    ma.NS = 8;
-    while (ma.NS > 2 && mma_smem(fmt, ma.NS) + size_t(c->gemm_static_smem) > c->smem_optin) --ma.NS;
     ma.SB = kMmaRows * ma.segB;
     ma.part = part;
     ma.err = c->err_flag;
     ma.stall = take_stall(st);
-    const size_t msmem = mma_smem(fmt, ma.NS);
-    if (msmem + size_t(c->gemm_static_smem) > c->smem_optin)
-      return set_err(c, NT_ERR_INVALID_ARG, "gemm: no shared-memory plan for the tensor-core form");
-    int gx = (c->num_sms + nparts - 1) / nparts;
-    if (gx > tiles) gx = int(tiles);
+    // warps per CTA and stages per warp: the most warps whose rings of at
+    // least two stages fit beside x, then as many stages as fit
+    const size_t room = c->smem_optin - size_t(c->gemm_static_smem);
+    int warps = c->gemm_warps;
+    while (warps > 8 && mma_smem(fmt, warps, 2) > room) warps -= 4;  // 8 at least: warp m converts vector m
+    ma.NS = 2;
+    while (ma.NS < c->gemm_stages && mma_smem(fmt, warps, ma.NS + 1) <= room) ++ma.NS;
+    const size_t msmem = mma_smem(fmt, warps, ma.NS);
+    if (msmem > room) return set_err(c, NT_ERR_INVALID_ARG, "gemm: no shared-memory plan for the tensor-core form");
+    // CTAs side by side over the parts, at most one per SM in all (one wave);
+    // no more warps than tiles
+    int gx = c->num_sms / nparts;
+    if (gx < 1) gx = 1;
+    const int64_t need_x = (tiles + warps - 1) / warps;
+    if (gx > need_x) gx = int(need_x);
     const dim3 grid(gx, nparts);
     cudaError_t err;
     switch (fmt) {
-      case NT_Q8_0: err = launch_k(c, qgemm_mma_kernel<NT_Q8_0>, grid, dim3(kMmaThreads), msmem, st, ma); break;
-      case NT_Q4_K: err = launch_k(c, qgemm_mma_kernel<NT_Q4_K>, grid, dim3(kMmaThreads), msmem, st, ma); break;
-      default: err = launch_k(c, qgemm_mma_kernel<NT_Q6_K>, grid, dim3(kMmaThreads), msmem, st, ma); break;
+      case NT_Q8_0: err = launch_k(c, qgemm_mma_kernel<NT_Q8_0>, grid, dim3(32 * warps), msmem, st, ma); break;
+      case NT_Q4_K: err = launch_k(c, qgemm_mma_kernel<NT_Q4_K>, grid, dim3(32 * warps), msmem, st, ma); break;
+      default: err = launch_k(c, qgemm_mma_kernel<NT_Q6_K>, grid, dim3(32 * warps), msmem, st, ma); break;
     }
     nt_status s = cuda_check(c, err, "qgemm (tensor-core) launch");
     if (s) return s;
@@ -934,7 +1053,8 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
     if (smem + size_t(c->gemm_static_smem) > c->smem_optin)
       return set_err(c, NT_ERR_INVALID_ARG, "gemm: no shared-memory plan for M=%d", M);
     // one CTA per SM in all: the parts side by side
-    int gx = (c->num_sms + nparts - 1) / nparts;
+    int gx = c->num_sms / nparts;  // one wave
+    if (gx < 1) gx = 1;
     const int64_t need_x = (g + kGemmWarps - 1) / kGemmWarps;
     if (gx > need_x) gx = int(need_x);
     const dim3 grid(gx, nparts);
