@@ -307,6 +307,7 @@ __global__ void qgemm_epi_kernel(const EpiArgs e) {
   const int m = blockIdx.y;
   auto sum_row = [&](int64_t row) {
     float v = 0.f;
+#pragma unroll 8
     for (int p = 0; p < e.nparts; ++p) v += __ldcg(e.part + (int64_t(p) * e.M + m) * e.total_rows + row);
     return v;
   };
@@ -362,8 +363,6 @@ __global__ void qgemm_epi_kernel(const EpiArgs e) {
 constexpr int kMmaWarps = 16;                     // warps per CTA at most
 constexpr int kMmaThreads = kMmaWarps * 32;
 constexpr int kMmaRows = 16;                      // rows per tile (the MMA's m)
-constexpr int kXPitch = 2048 + 16;                // f16 per vector row: +32 B keeps the B loads conflict-free
-constexpr int kMmaGroups = 2048 / 32;             // 32-column groups per part
 
 struct MmaArgs {
   GemmJobDev job[3];  // g0: first 16-row tile of the job; rb: first row in the row space
@@ -582,20 +581,27 @@ __device__ __forceinline__ void mma_locate(const MmaArgs& a, int64_t tile, int& 
   nr = left < kMmaRows ? int(left) : kMmaRows;
 }
 
-// shared layout: x hi [8][kXPitch] f16, x lo [8][kXPitch] f16, sums of x
-// [kMmaGroups][8] f32, vector scales [8], stage barriers [warps][NS], then
-// each warp's ring of NS stages of 16 staged rows
-constexpr size_t kMmaXh = 0;
-constexpr size_t kMmaXl = kMmaXh + size_t(8) * kXPitch * 2;
-constexpr size_t kMmaXs = kMmaXl + size_t(8) * kXPitch * 2;
-constexpr size_t kMmaSc = kMmaXs + size_t(kMmaGroups) * 8 * 4;
-constexpr size_t kMmaBar = kMmaSc + 8 * 4 + 32;
-__host__ __device__ constexpr size_t mma_ring_off(int warps, int NS) {
-  return ((kMmaBar + size_t(warps) * NS * 8 + 127) / 128) * 128;
+// shared layout, sized by the part's columns pc: x hi [8][pc + 16] f16, x lo
+// [8][pc + 16] f16 (the extra 32 bytes per vector keep the B loads free of
+// bank conflicts), sums of x [pc / 32][8] f32, vector scales [8], stage
+// barriers [warps][NS], then each warp's ring of NS stages of 16 staged rows
+struct MmaLayout {
+  size_t xl, xs, sc, bar, ring;
+};
+__host__ __device__ inline MmaLayout mma_layout(int pc, int warps, int NS) {
+  MmaLayout L;
+  const size_t pitch = size_t(pc) + 16;
+  L.xl = 8 * pitch * 2;
+  L.xs = L.xl + 8 * pitch * 2;
+  L.sc = L.xs + size_t(pc / 32) * 8 * 4;
+  L.bar = L.sc + 8 * 4 + 32;
+  L.ring = ((L.bar + size_t(warps) * NS * 8 + 127) / 128) * 128;
+  return L;
 }
 
-// blocks per staged segment of a row: about 256 bytes of weights per row
-__host__ __device__ constexpr int mma_seg_blocks(int fmt) { return fmt == NT_Q8_0 ? 8 : fmt == NT_Q4_K ? 2 : 1; }
+// blocks per staged segment of a row: about 512 bytes of weights per row
+// (each row copy moves that much; halving it cost 15-20%)
+__host__ __device__ constexpr int mma_seg_blocks(int fmt) { return fmt == NT_Q8_0 ? 16 : fmt == NT_Q4_K ? 4 : 2; }
 
 // one segment of 16 rows: the blocks [0, nbk) of each staged row, every
 // row's data starting at byte `o` of its pitch
@@ -606,7 +612,7 @@ __device__ __forceinline__ void mma_segment(const uint8_t* r0, const uint8_t* r1
   // a whole segment is straight-line code (every offset a constant); a
   // part's ragged last segment takes the loop
   if constexpr (FMT == NT_Q8_0) {
-    // a segment starts at a multiple of 8 blocks (272 bytes) from a 16-byte
+    // a segment starts at a multiple of 16 blocks (544 bytes) from a 16-byte
     // aligned row start: word-aligned
     const uint32_t* R0 = reinterpret_cast<const uint32_t*>(r0);
     const uint32_t* R1 = reinterpret_cast<const uint32_t*>(r1);
@@ -638,14 +644,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
   using F = Q<FMT>;
   constexpr int S = mma_seg_blocks(FMT);
   extern __shared__ __align__(128) uint8_t smem[];
-  __half* xh = reinterpret_cast<__half*>(smem + kMmaXh);
-  __half* xl = reinterpret_cast<__half*>(smem + kMmaXl);
-  float* xs = reinterpret_cast<float*>(smem + kMmaXs);
-  float* xsc = reinterpret_cast<float*>(smem + kMmaSc);
   const int NS = a.NS;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kMmaBar) + warp * NS;
-  uint8_t* ring = smem + mma_ring_off(nwarps, NS) + size_t(warp) * NS * a.SB;
+  const int xpitch = a.cwb * F::BE + 16;  // f16 per staged x vector
+  const MmaLayout L = mma_layout(a.cwb * F::BE, nwarps, NS);
+  __half* xh = reinterpret_cast<__half*>(smem);
+  __half* xl = reinterpret_cast<__half*>(smem + L.xl);
+  float* xs = reinterpret_cast<float*>(smem + L.xs);
+  float* xsc = reinterpret_cast<float*>(smem + L.sc);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar) + warp * NS;
+  uint8_t* ring = smem + L.ring + size_t(warp) * NS * a.SB;
   const int g = lane >> 2, t = lane & 3;
   const int p = blockIdx.y;
   const int blk_lo = p * a.cwb;
@@ -708,21 +716,31 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
     float inv = 1.f;
     const float* xr = a.X + int64_t(m) * a.ldx;
     if (m < a.M && a.norm_g) {
-      // sum of squares per 128-column chunk, then over the chunks in order
+      // sum of squares per 128-column chunk, then over the chunks in order;
+      // eight chunks' loads in flight at a time
       float tot = 0.f;
-      for (int c = 0; c < a.cols; c += 128) {
-        float ss = 0.f;
-        if (c + 4 * lane < a.cols) {
-          const float4 v = *reinterpret_cast<const float4*>(xr + c + 4 * lane);
-          ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, v.w * v.w)));
+      for (int c0 = 0; c0 < a.cols; c0 += 8 * 128) {
+        float ss[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int c = c0 + 128 * k + 4 * lane;
+          ss[k] = 0.f;
+          if (c < a.cols) {
+            const float4 v = *reinterpret_cast<const float4*>(xr + c);
+            ss[k] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, v.w * v.w)));
+          }
         }
-        tot += warp_sum(ss);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (c0 + 128 * k < a.cols) tot += warp_sum(ss[k]);
       }
       inv = rsqrtf(tot / float(a.cols) + a.eps);
     }
-    // lane l holds columns 64 l .. 64 l + 63 of the part: 16 float4, read
-    // twice (the largest |x| first, then the conversion) to stay in registers
-    auto load4 = [&](int k) {
+    // lane l holds columns 64 l .. 64 l + 63 of the part: 16 float4, loaded
+    // together (one memory round trip)
+    float4 xv[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
       const int col = 64 * lane + 4 * k;
       float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
       if (m < a.M && col < pcols) {
@@ -736,14 +754,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
           x4.w = x4.w * inv * gg.w;
         }
       }
-      return x4;
-    };
+      xv[k] = x4;
+    }
     float mx = 0.f;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float4 x4 = load4(k);
-      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x4.x), fabsf(x4.y)), fmaxf(fabsf(x4.z), fabsf(x4.w))));
-    }
+    for (int k = 0; k < 16; ++k)
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(xv[k].x), fabsf(xv[k].y)), fmaxf(fabsf(xv[k].z), fabsf(xv[k].w))));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     // scale 2^sh puts the vector's largest |x| in [2^13, 2^14): far inside the f16 range
@@ -751,13 +767,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
     if (mx > 0.f) sh = min(100, max(-100, 13 - (int((__float_as_uint(mx) >> 23) & 0xFFu) - 127)));
     const float scl = ldexpf(1.f, sh);
     if (lane == 0) xsc[m] = m < a.M ? ldexpf(1.f, -sh) : 0.f;
-    __half* hr = xh + m * kXPitch;
-    __half* lr = xl + m * kXPitch;
+    __half* hr = xh + m * xpitch;
+    __half* lr = xl + m * xpitch;
     float gs0 = 0.f, gs1 = 0.f;
-#pragma unroll 4
+#pragma unroll
     for (int k = 0; k < 16; ++k) {
-      const float4 x4 = load4(k);
-      const float e[4] = {x4.x * scl, x4.y * scl, x4.z * scl, x4.w * scl};
+      const float e[4] = {xv[k].x * scl, xv[k].y * scl, xv[k].z * scl, xv[k].w * scl};
       __half hi[4], lo[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -765,24 +780,28 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
         lo[q] = __float2half_rn(e[q] - __half2float(hi[q]));
       }
       const int col = 64 * lane + 4 * k;
-      *reinterpret_cast<uint2*>(hr + col) = make_uint2(
-          uint32_t(__half_as_ushort(hi[0])) | (uint32_t(__half_as_ushort(hi[1])) << 16),
-          uint32_t(__half_as_ushort(hi[2])) | (uint32_t(__half_as_ushort(hi[3])) << 16));
-      *reinterpret_cast<uint2*>(lr + col) = make_uint2(
-          uint32_t(__half_as_ushort(lo[0])) | (uint32_t(__half_as_ushort(lo[1])) << 16),
-          uint32_t(__half_as_ushort(lo[2])) | (uint32_t(__half_as_ushort(lo[3])) << 16));
+      if (col < a.cwb * F::BE) {  // inside the layout's part width
+        *reinterpret_cast<uint2*>(hr + col) = make_uint2(
+            uint32_t(__half_as_ushort(hi[0])) | (uint32_t(__half_as_ushort(hi[1])) << 16),
+            uint32_t(__half_as_ushort(hi[2])) | (uint32_t(__half_as_ushort(hi[3])) << 16));
+        *reinterpret_cast<uint2*>(lr + col) = make_uint2(
+            uint32_t(__half_as_ushort(lo[0])) | (uint32_t(__half_as_ushort(lo[1])) << 16),
+            uint32_t(__half_as_ushort(lo[2])) | (uint32_t(__half_as_ushort(lo[3])) << 16));
+      }
       const float s4 = (e[0] + e[1]) + (e[2] + e[3]);
       if (k < 8) gs0 += s4;
       else gs1 += s4;
     }
-    xs[(2 * lane) * 8 + m] = gs0;
-    xs[(2 * lane + 1) * 8 + m] = gs1;
+    if (64 * lane < a.cwb * F::BE) {  // the groups of the layout's part width
+      xs[(2 * lane) * 8 + m] = gs0;
+      xs[(2 * lane + 1) * 8 + m] = gs1;
+    }
   }
   __syncthreads();
   if (n_items == 0) return;
 
-  const uint32_t* xh32 = reinterpret_cast<const uint32_t*>(xh + g * kXPitch) + 2 * t;
-  const uint32_t* xl32 = reinterpret_cast<const uint32_t*>(xl + g * kXPitch) + 2 * t;
+  const uint32_t* xh32 = reinterpret_cast<const uint32_t*>(xh + g * xpitch) + 2 * t;
+  const uint32_t* xl32 = reinterpret_cast<const uint32_t*>(xl + g * xpitch) + 2 * t;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   bool dead = false;
   // consume cursor: stage slot and phase, segment, tile ordinal
@@ -849,10 +868,10 @@ int mma_segB(int fmt) {
   return 16 * u;
 }
 
-size_t mma_smem(int fmt, int warps, int NS) {
+size_t mma_smem(int fmt, int cwb, int warps, int NS) {
   const int segB = mma_segB(fmt);
   // + 16: the unaligned readers may touch 4 bytes past a row
-  return mma_ring_off(warps, NS) + size_t(warps) * NS * kMmaRows * segB + 16;
+  return mma_layout(cwb * block_elems(fmt), warps, NS).ring + size_t(warps) * NS * kMmaRows * segB + 16;
 }
 
 bool mma_format(int fmt) { return fmt == NT_Q8_0 || fmt == NT_Q4_K || fmt == NT_Q6_K; }
@@ -1008,10 +1027,10 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
     // least two stages fit beside x, then as many stages as fit
     const size_t room = c->smem_optin - size_t(c->gemm_static_smem);
     int warps = c->gemm_warps;
-    while (warps > 8 && mma_smem(fmt, warps, 2) > room) warps -= 4;  // 8 at least: warp m converts vector m
+    while (warps > 8 && mma_smem(fmt, cwb, warps, 2) > room) warps -= 4;  // 8 at least: warp m converts vector m
     ma.NS = 2;
-    while (ma.NS < c->gemm_stages && mma_smem(fmt, warps, ma.NS + 1) <= room) ++ma.NS;
-    const size_t msmem = mma_smem(fmt, warps, ma.NS);
+    while (ma.NS < c->gemm_stages && mma_smem(fmt, cwb, warps, ma.NS + 1) <= room) ++ma.NS;
+    const size_t msmem = mma_smem(fmt, cwb, warps, ma.NS);
     if (msmem > room) return set_err(c, NT_ERR_INVALID_ARG, "gemm: no shared-memory plan for the tensor-core form");
     // CTAs side by side over the parts, at most one per SM in all (one wave);
     // no more warps than tiles
