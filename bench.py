@@ -39,7 +39,9 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms; each line is
+    stamped with the host time it arrived, so the summary can keep the samples
+    taken inside the timed region (mark_start / mark_end around it)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -48,13 +50,14 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host time, csv line)
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except (FileNotFoundError, OSError):
@@ -63,7 +66,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def wait_first(self, timeout=5.0):
         t0 = time.time()
@@ -88,7 +97,10 @@ class ClockSampler:
     def summary(self):
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        inside = [ln for t, ln in self.lines if self.t0 is not None and self.t1 is not None and self.t0 <= t <= self.t1]
+        # the samples taken inside the timed region; the ones around it when the region is shorter than a sample
+        use = inside if inside else [ln for _, ln in self.lines]
+        for ln in use:
             p = [x.strip() for x in ln.split(",")]
             if len(p) < 9:
                 continue
@@ -102,7 +114,8 @@ class ClockSampler:
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm),
+                "samples_in_timed_region": len(inside), "sample_ms": 50}
 
 
 def kernel_source_sha() -> str:
@@ -193,10 +206,12 @@ def bench_gemv(args, rank, world):
         with ClockSampler(torch.cuda.current_device()) as clk:
             clk.wait_first()
             torch.cuda.synchronize()
+            clk.mark_start()
             e0.record(st)
             g.replay()
             e1.record(st)
             e1.synchronize()
+            clk.mark_end()
             clk.wait_one_more()
         ms = e0.elapsed_time(e1)
     ms = max_over_ranks(ms, world)
@@ -308,10 +323,12 @@ def bench_attn(args, rank, world):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(torch.cuda.current_device()) as clk:
             clk.wait_first()
+            clk.mark_start()
             e0.record(st)
             g.replay()
             e1.record(st)
             e1.synchronize()
+            clk.mark_end()
             clk.wait_one_more()
     per = e0.elapsed_time(e1) / 1e3 / args.steps
     gbs = kv_bytes / per / 1e9
@@ -373,11 +390,13 @@ def bench_prefill(args, rank, world):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(torch.cuda.current_device()) as clk:
             clk.wait_first()
+            clk.mark_start()
             e0.record(st)
             for _ in range(args.steps):
                 gm.prefill(prompt, pos0, stream=st)
             e1.record(st)
             e1.synchronize()
+            clk.mark_end()
             clk.wait_one_more()
     ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
     chunks = -(-n // 8)
@@ -485,6 +504,7 @@ def bench_decode(args, rank, world):
         with ClockSampler(torch.cuda.current_device()) as clk:
             clk.wait_first()
             torch.cuda.synchronize()
+            clk.mark_start()
             e0.record(st)
             for i in range(args.steps):
                 if i % window == 0:
@@ -493,6 +513,7 @@ def bench_decode(args, rank, world):
                     gm.step(-1, 0, skip, stream=st)
             e1.record(st)
             e1.synchronize()
+            clk.mark_end()
             clk.wait_one_more()
         ms = e0.elapsed_time(e1)
     ms = max_over_ranks(ms, world)
@@ -672,11 +693,13 @@ def bench_streamed(args, rank, world):
         with ClockSampler(torch.cuda.current_device()) as clk:
             clk.wait_first()
             torch.cuda.synchronize()
+            clk.mark_start()
             e0.record(st)
             for i in range(args.steps):
                 one(i, True)
             e1.record(st)
             e1.synchronize()
+            clk.mark_end()
             clk.wait_one_more()
         ms = e0.elapsed_time(e1)
     ms = max_over_ranks(ms, world)
