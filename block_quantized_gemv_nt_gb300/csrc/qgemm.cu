@@ -600,11 +600,12 @@ __host__ __device__ inline MmaLayout mma_layout(int pc, int warps, int NS) {
 }
 
 // blocks per staged segment of a row: about 512 bytes of weights per row
-// (each row copy moves that much; halving it cost 15-20%)
+// (each row copy moves that much; segments half this size measured up to
+// 19% slower)
 __host__ __device__ constexpr int mma_seg_blocks(int fmt) { return fmt == NT_Q8_0 ? 16 : fmt == NT_Q4_K ? 4 : 2; }
 
-// one segment of 16 rows: the blocks [0, nbk) of each staged row, every
-// row's data starting at byte `o` of its pitch
+// one segment of 16 rows: the blocks [0, nbk) of the segment, r0 and r1
+// pointing at its first byte in the staged rows g and g + 8
 template <int FMT>
 __device__ __forceinline__ void mma_segment(const uint8_t* r0, const uint8_t* r1, int nbk, int t, const uint32_t* xh,
                                             const uint32_t* xl, const float* xs, float (&acc)[4]) {
