@@ -141,7 +141,7 @@ nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes) {
   c->gemv_tune = env_int("NT_GEMV_TUNE", 0, 1, 1) != 0;
   c->attn_fill = env_int("NT_ATTN_FILL", 0, 1, 1) != 0;
   c->gemm_mma = env_int("NT_GEMM_MMA", 0, 1, 1) != 0;
-  c->gemm_warps = env_int("NT_GEMM_WARPS", 8, 16, 16) / 4 * 4;
+  c->gemm_warps = env_int("NT_GEMM_WARPS", 8, 12, 12) / 4 * 4;
   c->gemm_stages = env_int("NT_GEMM_STAGES", 2, 8, 4);
   c->scratch_bytes = scratch_bytes ? scratch_bytes : (size_t(64) << 20);
   if (c->scratch_bytes < (size_t(1) << 20)) c->scratch_bytes = size_t(1) << 20;
@@ -317,7 +317,7 @@ nt_status nt_gemm_q(nt_ctx* ctx, int fmt, const void* W, const float* X, float* 
   NvtxRange nvtx_range("nt_gemm_q");
   NT_TRY(pre_call(ctx));
   NT_TRY(check_fmt_cols(ctx, fmt, cols));
-  NT_REQUIRE(M >= 1 && M <= kMaxVerify, NT_ERR_INVALID_ARG, "M must be 1..%d", kMaxVerify);
+  NT_REQUIRE(M >= 1 && M <= kMaxGemmM, NT_ERR_INVALID_ARG, "M must be 1..%d", kMaxGemmM);
   NT_REQUIRE(rows >= 0, NT_ERR_INVALID_ARG, "negative rows");
   if (rows == 0) return NT_OK;
   NT_REQUIRE(W && Y, NT_ERR_INVALID_ARG, "null W or Y");

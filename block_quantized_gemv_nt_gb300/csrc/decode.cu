@@ -780,9 +780,9 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   const size_t fl = sizeof(float);
   const size_t nx = up256(fl * d.d_model), nqb = up256(fl * nq), nkb = up256(fl * d.n_kvh * d.head_dim),
                nh = up256(fl * d.ffn), ncos = up256(fl * d.n_layers), nst = 256, nfreq = up256(8 * d.head_dim),
-               npart = up256(attn_scratch_bytes(d.n_qh, d.n_kvh, m->S, kMaxVerify)), nspec = 1024,
-               nvx = up256(fl * kMaxVerify * d.d_model), nvq = up256(fl * kMaxVerify * nq),
-               nvh = up256(fl * kMaxVerify * d.ffn), nvl = up256(fl * kMaxVerify * d.vocab), ndl = up256(fl * d.vocab),
+               npart = up256(attn_scratch_bytes(d.n_qh, d.n_kvh, m->S, kMaxGemmM)), nspec = 1024,
+               nvx = up256(fl * kMaxGemmM * d.d_model), nvq = up256(fl * kMaxGemmM * nq),
+               nvh = up256(fl * kMaxGemmM * d.ffn), nvl = up256(fl * kMaxGemmM * d.vocab), ndl = up256(fl * d.vocab),
                nprompt = up256(sizeof(int32_t) * size_t(d.kv_cap)), nsamp = kSampRowBytes * kMaxVerify,
                nsw = up256(8 * size_t(d.vocab)), nsW = up256(8 * kMaxVerify),
                nout = up256(fl * size_t(2 * kMaxVerify - 1) * size_t(d.vocab)), nouttok = 256;
@@ -794,7 +794,7 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
                               {2 * int64_t(d.ffn), d.d_model, d.fmt_gate}, {d.d_model, d.ffn, d.fmt_down},
                               {d.vocab, d.d_model, d.fmt_out}};
     for (auto& x : rc)
-      m->gpart_bytes = std::max(m->gpart_bytes, gemm_scratch_bytes(int(x[2]), x[0], x[1], kMaxVerify));
+      m->gpart_bytes = std::max(m->gpart_bytes, gemm_scratch_bytes(int(x[2]), x[0], x[1], kMaxGemmM));
     m->gpart_bytes = up256(m->gpart_bytes);
   }
   const size_t total = 2 * nx + nqb * 2 + nkb * 2 + nh + ncos + nst + npart + nfreq + nspec + nvx + 2 * nvq + nvh +
@@ -846,11 +846,11 @@ nt_status nt_model_init(nt_ctx* ctx, const nt_model_desc* desc, const nt_layer_p
   char* part = take(npart);
   m->attn_part = reinterpret_cast<float*>(part + kAttnCounterBytes);
   char* sp = take(nspec);
-  m->spec_tok = reinterpret_cast<int32_t*>(sp);
-  m->spec_pos = reinterpret_cast<int64_t*>(sp + 64);
-  m->vtok = reinterpret_cast<int32_t*>(sp + 128);
-  m->vkey = reinterpret_cast<unsigned long long*>(sp + 192);
-  m->vcnt = reinterpret_cast<unsigned*>(sp + 256);
+  m->spec_tok = reinterpret_cast<int32_t*>(sp);         // [kMaxGemmM]
+  m->spec_pos = reinterpret_cast<int64_t*>(sp + 64);     // [kMaxGemmM]
+  m->vtok = reinterpret_cast<int32_t*>(sp + 192);        // [kMaxVerify]
+  m->vkey = reinterpret_cast<unsigned long long*>(sp + 256);
+  m->vcnt = reinterpret_cast<unsigned*>(sp + 320);
   m->xv = reinterpret_cast<float*>(take(nvx));
   m->qv = reinterpret_cast<float*>(take(nvq));
   m->aov = reinterpret_cast<float*>(take(nvq));
@@ -1031,6 +1031,23 @@ nt_status nt_layer_blob_layout(const nt_model_desc* d, size_t* off, size_t* byte
   return NT_OK;
 }
 
+// prompt tokens per prefill pass: 16 when every GEMM of the step takes the
+// tensor-core form (formats, row widths, 16-byte-aligned resident weights;
+// streamed weights sit in aligned slots), else the verify size
+static int prefill_chunk(const Ctx* c, const nt_model* m) {
+  const nt_model_desc& d = m->d;
+  const int64_t nq = int64_t(d.n_qh) * d.head_dim;
+  const bool fmts = gemm_wide_ok(c, d.fmt_q, d.d_model) && gemm_wide_ok(c, d.fmt_k, d.d_model) &&
+                    gemm_wide_ok(c, d.fmt_v, d.d_model) && gemm_wide_ok(c, d.fmt_o, nq) &&
+                    gemm_wide_ok(c, d.fmt_gate, d.d_model) && gemm_wide_ok(c, d.fmt_down, d.ffn) &&
+                    gemm_wide_ok(c, d.fmt_out, d.d_model);
+  if (!fmts || !aligned(m->out, 16)) return kMaxVerify;
+  for (const nt_layer_ptrs& L : m->layers)
+    for (const void* w : {L.wq, L.wk, L.wv, L.wo, L.wg, L.wu, L.wd})
+      if (w && !aligned(w, 16)) return kMaxVerify;
+  return kMaxGemmM;
+}
+
 nt_status nt_prefill(nt_ctx* ctx, nt_model* m, const int32_t* tokens_host, int64_t n, int64_t pos0, float* logits,
                      int32_t* next_tok, void* stream) {
   NvtxRange nvtx_range("nt_prefill");
@@ -1056,8 +1073,12 @@ nt_status nt_prefill(nt_ctx* ctx, nt_model* m, const int32_t* tokens_host, int64
                    "prompt upload");
   }
   if (!s) s = cuda_check(ctx, cudaEventRecord(m->ev_prompt, st), "prompt upload event");
-  for (int64_t base = 0; base < n && !s; base += kMaxVerify) {
-    const int M = int(std::min<int64_t>(kMaxVerify, n - base));
+  // chunks of 16 prompt tokens when every GEMM of the model takes the
+  // tensor-core form (its time hardly depends on the vector count, so each
+  // weight pass serves twice the tokens); 8 otherwise
+  const int chunk = prefill_chunk(ctx, m);
+  for (int64_t base = 0; base < n && !s; base += chunk) {
+    const int M = int(std::min<int64_t>(chunk, n - base));
     const bool last = base + M == n;
     s = cuda_check(ctx, launch_k(ctx, prefill_setup_kernel, dim3(1), dim3(32), 0, st, m->prompt + base, pos0 + base,
                                  m->spec_tok, m->spec_pos, M),

@@ -48,7 +48,7 @@ struct Ctx {
   int gemv_static_smem = 2048;   // largest static shared memory of the GEMV kernels
   int gemm_static_smem = 1024;   // same for the verify-GEMM kernels
   bool gemm_mma = true;
-  int gemm_warps = 16;           // tensor-core verify GEMM: warps per CTA, stages per warp at most
+  int gemm_warps = 12;           // tensor-core verify GEMM: warps per CTA, stages per warp at most
   int gemm_stages = 4;          // verify GEMM: the tensor-core form for Q8_0 / Q4_K / Q6_K
   std::string last_error;
   std::mutex mu;
@@ -234,6 +234,7 @@ struct GemvJobEx {
 // one job of the M-vector verify GEMM: Y[m] = W X[m], with the epilogue applied
 // per vector m (RoPE and the cache append at position pos + m)
 constexpr int kMaxVerify = 8;  // vectors per verify GEMM (draft length + 1)
+constexpr int kMaxGemmM = 16;  // vectors per GEMM in the tensor-core form (prompt chunks)
 struct GemmJobEx {
   const void* W;
   int64_t rows;

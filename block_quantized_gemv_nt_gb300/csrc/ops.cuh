@@ -47,6 +47,9 @@ nt_status configure_gemv(Ctx* c);
 nt_status configure_gemm(Ctx* c);
 int gemm_parts(int fmt, int64_t cols);
 size_t gemm_scratch_bytes(int fmt, int64_t total_rows, int64_t cols, int M);
+// whether launch_gemm takes more than kMaxVerify vectors for this format and
+// width (the tensor-core form, with rows at 16-byte-aligned addresses)
+bool gemm_wide_ok(const Ctx* c, int fmt, int64_t cols);
 nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool swiglu, const float* X, int64_t ldx,
                       int M, const float* norm_g, float eps, int64_t cols, const RopeArgs* rope, float* part,
                       size_t part_bytes, cudaStream_t st);

@@ -360,7 +360,7 @@ __global__ void qgemm_epi_kernel(const EpiArgs e) {
 
 // ---------------------------------------------------------------------------
 // Tensor-core form: mma.sync m16n8k16 (f16 x f16 -> f32), 16-row tiles.
-constexpr int kMmaWarps = 16;                     // warps per CTA at most
+constexpr int kMmaWarps = 12;                     // warps per CTA at most (the rings of more do not fit)
 constexpr int kMmaThreads = kMmaWarps * 32;
 constexpr int kMmaRows = 16;                      // rows per tile (the MMA's m)
 
@@ -416,6 +416,10 @@ __device__ __forceinline__ uint32_t lds32_a2(const uint8_t* p) {
 template <int FMT>
 struct MmaRows;
 
+// The vectors come in N-tiles of 8 (the MMA's n): NT tiles, the x of tile
+// nt at xh + nt * xt (and xl + nt * xt), the sums of x of vector n at
+// xs[group * 8 NT + n]; acc[nt] holds the fragment of tile nt.
+
 // Q8_0: per block (32 columns, 2 k-steps) the 4-byte words of qs for rows
 // g and g + 8, signed -> f16; one scale d per row and block.
 template <>
@@ -424,8 +428,9 @@ struct MmaRows<NT_Q8_0> {
   // g and g + 8 as words).  Blocks come in pairs of 68 bytes = 17 words: the
   // even block's quants sit 2 bytes off a word boundary (one funnel shift by
   // 16 per word), the odd block's are word-aligned.
+  template <int NT>
   __device__ static void block_w(const uint32_t* R0, const uint32_t* R1, int b, int t, int c0, const uint32_t* xh,
-                                 const uint32_t* xl, float (&acc)[4]) {
+                                 const uint32_t* xl, int xt, float (&acc)[NT][4]) {
     const int pw = 17 * (b >> 1);
     float d0, d1;
     uint32_t w[2][2];  // [sub][row]
@@ -448,22 +453,30 @@ struct MmaRows<NT_Q8_0> {
         w[sub][1] = R1[k];
       }
     }
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    float c[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
 #pragma unroll
     for (int sub = 0; sub < 2; ++sub) {
       const uint32_t w0 = w[sub][0] ^ 0x80808080u, w1 = w[sub][1] ^ 0x80808080u;
       const uint32_t a[4] = {u8lo_f16(w0, kBias1152), u8lo_f16(w1, kBias1152), u8hi_f16(w0, kBias1152),
                              u8hi_f16(w1, kBias1152)};
       const int col = c0 + 16 * sub;
-      const uint2 bh = *reinterpret_cast<const uint2*>(xh + col / 2);
-      const uint2 bl = *reinterpret_cast<const uint2*>(xl + col / 2);
-      mma16816(c, a, bh.x, bh.y);
-      mma16816(c, a, bl.x, bl.y);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint2 bh = *reinterpret_cast<const uint2*>(xh + nt * xt + col / 2);
+        const uint2 bl = *reinterpret_cast<const uint2*>(xl + nt * xt + col / 2);
+        mma16816(c[nt], a, bh.x, bh.y);
+        mma16816(c[nt], a, bl.x, bl.y);
+      }
     }
-    acc[0] = fmaf(d0, c[0], acc[0]);
-    acc[1] = fmaf(d0, c[1], acc[1]);
-    acc[2] = fmaf(d1, c[2], acc[2]);
-    acc[3] = fmaf(d1, c[3], acc[3]);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      acc[nt][0] = fmaf(d0, c[nt][0], acc[nt][0]);
+      acc[nt][1] = fmaf(d0, c[nt][1], acc[nt][1]);
+      acc[nt][2] = fmaf(d1, c[nt][2], acc[nt][2]);
+      acc[nt][3] = fmaf(d1, c[nt][3], acc[nt][3]);
+    }
   }
 };
 
@@ -473,8 +486,11 @@ struct MmaRows<NT_Q8_0> {
 template <>
 struct MmaRows<NT_Q4_K> {
   // half-block hb: the half `half` (sub-block pairs 2 half, 2 half + 1) of block b = hb / 2
+  template <int NT>
   __device__ static void half_block(const uint8_t* r0, const uint8_t* r1, int hb, int nblk, int t,
-                                    const uint32_t* xh, const uint32_t* xl, const float* xs, float (&acc)[4]) {
+                                    const uint32_t* xh, const uint32_t* xl, int xt, const float* xs,
+                                    float (&acc)[NT][4]) {
+    constexpr int MV = 8 * NT;
     const int b = hb >> 1, half = hb & 1;
     if (b >= nblk) return;
     const uint8_t* p0 = r0 + b * 144;
@@ -484,13 +500,18 @@ struct MmaRows<NT_Q4_K> {
     const uint4 h1 = *reinterpret_cast<const uint4*>(p1);
     const float d0 = qf::h2f(h0.x & 0xFFFFu), dm0 = qf::h2f(h0.x >> 16);
     const float d1 = qf::h2f(h1.x & 0xFFFFu), dm1 = qf::h2f(h1.x >> 16);
-#pragma unroll
+    // with two N-tiles the sub-block pairs go one at a time (register room)
+#pragma unroll(3 - NT)
     for (int cc = 0; cc < 2; ++cc) {
       const int c = 2 * half + cc;
       float sa0, sb0, ma0, mb0, sa1, sb1, ma1, mb1;
       qf::kq_scales(h0.y, h0.z, h0.w, c, sa0, sb0, ma0, mb0);
       qf::kq_scales(h1.y, h1.z, h1.w, c, sa1, sb1, ma1, mb1);
-      float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+      float ca[NT][4], cb[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ca[nt][e] = cb[nt][e] = 0.f;
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         const uint32_t w0 = *reinterpret_cast<const uint32_t*>(p0 + 16 + 32 * c + 16 * s + 4 * t);
@@ -502,25 +523,31 @@ struct MmaRows<NT_Q4_K> {
         const uint32_t au[4] = {u8lo_f16(u0, kBias1024), u8lo_f16(u1, kBias1024), u8hi_f16(u0, kBias1024),
                                 u8hi_f16(u1, kBias1024)};
         const int colA = c0 + 64 * c + 16 * s, colB = colA + 32;
-        const uint2 bha = *reinterpret_cast<const uint2*>(xh + colA / 2);
-        const uint2 bla = *reinterpret_cast<const uint2*>(xl + colA / 2);
-        const uint2 bhb = *reinterpret_cast<const uint2*>(xh + colB / 2);
-        const uint2 blb = *reinterpret_cast<const uint2*>(xl + colB / 2);
-        mma16816(ca, al, bha.x, bha.y);
-        mma16816(ca, al, bla.x, bla.y);
-        mma16816(cb, au, bhb.x, bhb.y);
-        mma16816(cb, au, blb.x, blb.y);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint2 bha = *reinterpret_cast<const uint2*>(xh + nt * xt + colA / 2);
+          const uint2 bla = *reinterpret_cast<const uint2*>(xl + nt * xt + colA / 2);
+          const uint2 bhb = *reinterpret_cast<const uint2*>(xh + nt * xt + colB / 2);
+          const uint2 blb = *reinterpret_cast<const uint2*>(xl + nt * xt + colB / 2);
+          mma16816(ca[nt], al, bha.x, bha.y);
+          mma16816(ca[nt], al, bla.x, bla.y);
+          mma16816(cb[nt], au, bhb.x, bhb.y);
+          mma16816(cb[nt], au, blb.x, blb.y);
+        }
       }
-      // sums of x over the two sub-blocks for this thread's vectors 2t, 2t + 1
+      // sums of x over the two sub-blocks for this thread's vectors 8 nt + 2t, 8 nt + 2t + 1
       const int grp = (c0 + 64 * c) / 32;
-      const float2 xa = *reinterpret_cast<const float2*>(xs + grp * 8 + 2 * t);
-      const float2 xb = *reinterpret_cast<const float2*>(xs + (grp + 1) * 8 + 2 * t);
       const float ka0 = d0 * sa0, kb0 = d0 * sb0, ka1 = d1 * sa1, kb1 = d1 * sb1;
       const float na0 = dm0 * ma0, nb0 = dm0 * mb0, na1 = dm1 * ma1, nb1 = dm1 * mb1;
-      acc[0] += fmaf(ka0, ca[0], fmaf(kb0, cb[0], -fmaf(na0, xa.x, nb0 * xb.x)));
-      acc[1] += fmaf(ka0, ca[1], fmaf(kb0, cb[1], -fmaf(na0, xa.y, nb0 * xb.y)));
-      acc[2] += fmaf(ka1, ca[2], fmaf(kb1, cb[2], -fmaf(na1, xa.x, nb1 * xb.x)));
-      acc[3] += fmaf(ka1, ca[3], fmaf(kb1, cb[3], -fmaf(na1, xa.y, nb1 * xb.y)));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float2 xa = *reinterpret_cast<const float2*>(xs + grp * MV + 8 * nt + 2 * t);
+        const float2 xb = *reinterpret_cast<const float2*>(xs + (grp + 1) * MV + 8 * nt + 2 * t);
+        acc[nt][0] += fmaf(ka0, ca[nt][0], fmaf(kb0, cb[nt][0], -fmaf(na0, xa.x, nb0 * xb.x)));
+        acc[nt][1] += fmaf(ka0, ca[nt][1], fmaf(kb0, cb[nt][1], -fmaf(na0, xa.y, nb0 * xb.y)));
+        acc[nt][2] += fmaf(ka1, ca[nt][2], fmaf(kb1, cb[nt][2], -fmaf(na1, xa.x, nb1 * xb.x)));
+        acc[nt][3] += fmaf(ka1, ca[nt][3], fmaf(kb1, cb[nt][3], -fmaf(na1, xa.y, nb1 * xb.y)));
+      }
     }
   }
 };
@@ -531,8 +558,10 @@ struct MmaRows<NT_Q4_K> {
 template <>
 struct MmaRows<NT_Q6_K> {
   // half-block hb: the half h = hb & 1 (128 columns) of block hb / 2
+  template <int NT>
   __device__ static void half_block(const uint8_t* r0, const uint8_t* r1, int hb, int nblk, int t,
-                                    const uint32_t* xh, const uint32_t* xl, const float*, float (&acc)[4]) {
+                                    const uint32_t* xh, const uint32_t* xl, int xt, const float*,
+                                    float (&acc)[NT][4]) {
     const int b = hb >> 1, h = hb & 1;
     if (b >= nblk) return;
     const uint8_t* p0 = r0 + b * 210;
@@ -540,33 +569,34 @@ struct MmaRows<NT_Q6_K> {
     const int c0 = b * 256;
     const float d0 = __half2float(*reinterpret_cast<const __half*>(p0 + 208));
     const float d1 = __half2float(*reinterpret_cast<const __half*>(p1 + 208));
-    {
 #pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        const int lo = 64 * h + 16 * s + 4 * t, qh = 128 + 32 * h + 16 * s + 4 * t;
-        const uint32_t A0 = lds32_a2(p0 + lo), B0 = lds32_a2(p0 + lo + 32), H0 = lds32_a2(p0 + qh);
-        const uint32_t A1 = lds32_a2(p1 + lo), B1 = lds32_a2(p1 + lo + 32), H1 = lds32_a2(p1 + qh);
+    for (int s = 0; s < 2; ++s) {
+      const int lo = 64 * h + 16 * s + 4 * t, qh = 128 + 32 * h + 16 * s + 4 * t;
+      const uint32_t A0 = lds32_a2(p0 + lo), B0 = lds32_a2(p0 + lo + 32), H0 = lds32_a2(p0 + qh);
+      const uint32_t A1 = lds32_a2(p1 + lo), B1 = lds32_a2(p1 + lo + 32), H1 = lds32_a2(p1 + qh);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const uint32_t L0 = (g & 1) ? B0 : A0, L1 = (g & 1) ? B1 : A1;
-          const int nib = 4 * (g >> 1);
-          const uint32_t q0 = ((L0 >> nib) & 0x0F0F0F0Fu) | (((H0 >> (2 * g)) & 0x03030303u) << 4);
-          const uint32_t q1 = ((L1 >> nib) & 0x0F0F0F0Fu) | (((H1 >> (2 * g)) & 0x03030303u) << 4);
-          const uint32_t a[4] = {u8lo_f16(q0, kBias1056), u8lo_f16(q1, kBias1056), u8hi_f16(q0, kBias1056),
-                                 u8hi_f16(q1, kBias1056)};
-          const int col = c0 + 128 * h + 32 * g + 16 * s;
-          const uint2 bh = *reinterpret_cast<const uint2*>(xh + col / 2);
-          const uint2 bl = *reinterpret_cast<const uint2*>(xl + col / 2);
+      for (int g = 0; g < 4; ++g) {
+        const uint32_t L0 = (g & 1) ? B0 : A0, L1 = (g & 1) ? B1 : A1;
+        const int nib = 4 * (g >> 1);
+        const uint32_t q0 = ((L0 >> nib) & 0x0F0F0F0Fu) | (((H0 >> (2 * g)) & 0x03030303u) << 4);
+        const uint32_t q1 = ((L1 >> nib) & 0x0F0F0F0Fu) | (((H1 >> (2 * g)) & 0x03030303u) << 4);
+        const uint32_t a[4] = {u8lo_f16(q0, kBias1056), u8lo_f16(q1, kBias1056), u8hi_f16(q0, kBias1056),
+                               u8hi_f16(q1, kBias1056)};
+        const int col = c0 + 128 * h + 32 * g + 16 * s;
+        const int j = 8 * h + 2 * g + s;  // sub-block: scales[j]
+        const float k0 = d0 * float(*reinterpret_cast<const int8_t*>(p0 + 192 + j));
+        const float k1 = d1 * float(*reinterpret_cast<const int8_t*>(p1 + 192 + j));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint2 bh = *reinterpret_cast<const uint2*>(xh + nt * xt + col / 2);
+          const uint2 bl = *reinterpret_cast<const uint2*>(xl + nt * xt + col / 2);
           float c[4] = {0.f, 0.f, 0.f, 0.f};
           mma16816(c, a, bh.x, bh.y);
           mma16816(c, a, bl.x, bl.y);
-          const int j = 8 * h + 2 * g + s;  // sub-block: scales[j]
-          const float k0 = d0 * float(*reinterpret_cast<const int8_t*>(p0 + 192 + j));
-          const float k1 = d1 * float(*reinterpret_cast<const int8_t*>(p1 + 192 + j));
-          acc[0] = fmaf(k0, c[0], acc[0]);
-          acc[1] = fmaf(k0, c[1], acc[1]);
-          acc[2] = fmaf(k1, c[2], acc[2]);
-          acc[3] = fmaf(k1, c[3], acc[3]);
+          acc[nt][0] = fmaf(k0, c[0], acc[nt][0]);
+          acc[nt][1] = fmaf(k0, c[1], acc[nt][1]);
+          acc[nt][2] = fmaf(k1, c[2], acc[nt][2]);
+          acc[nt][3] = fmaf(k1, c[3], acc[nt][3]);
         }
       }
     }
@@ -581,20 +611,21 @@ __device__ __forceinline__ void mma_locate(const MmaArgs& a, int64_t tile, int& 
   nr = left < kMmaRows ? int(left) : kMmaRows;
 }
 
-// shared layout, sized by the part's columns pc: x hi [8][pc + 16] f16, x lo
-// [8][pc + 16] f16 (the extra 32 bytes per vector keep the B loads free of
-// bank conflicts), sums of x [pc / 32][8] f32, vector scales [8], stage
-// barriers [warps][NS], then each warp's ring of NS stages of 16 staged rows
+// shared layout for MV vector slots, sized by the part's columns pc: x hi
+// [MV][pc + 16] f16, x lo [MV][pc + 16] f16 (the extra 32 bytes per vector
+// keep the B loads free of bank conflicts), sums of x [pc / 32][MV] f32,
+// vector scales [MV], stage barriers [warps][NS], then each warp's ring of NS
+// stages of 16 staged rows
 struct MmaLayout {
   size_t xl, xs, sc, bar, ring;
 };
-__host__ __device__ inline MmaLayout mma_layout(int pc, int warps, int NS) {
+__host__ __device__ inline MmaLayout mma_layout(int pc, int MV, int warps, int NS) {
   MmaLayout L;
   const size_t pitch = size_t(pc) + 16;
-  L.xl = 8 * pitch * 2;
-  L.xs = L.xl + 8 * pitch * 2;
-  L.sc = L.xs + size_t(pc / 32) * 8 * 4;
-  L.bar = L.sc + 8 * 4 + 32;
+  L.xl = size_t(MV) * pitch * 2;
+  L.xs = L.xl + size_t(MV) * pitch * 2;
+  L.sc = L.xs + size_t(pc / 32) * MV * 4;
+  L.bar = L.sc + size_t(MV) * 4 + 32;
   L.ring = ((L.bar + size_t(warps) * NS * 8 + 127) / 128) * 128;
   return L;
 }
@@ -606,9 +637,9 @@ __host__ __device__ constexpr int mma_seg_blocks(int fmt) { return fmt == NT_Q8_
 
 // one segment of 16 rows: the blocks [0, nbk) of the segment, r0 and r1
 // pointing at its first byte in the staged rows g and g + 8
-template <int FMT>
+template <int FMT, int NT>
 __device__ __forceinline__ void mma_segment(const uint8_t* r0, const uint8_t* r1, int nbk, int t, const uint32_t* xh,
-                                            const uint32_t* xl, const float* xs, float (&acc)[4]) {
+                                            const uint32_t* xl, int xt, const float* xs, float (&acc)[NT][4]) {
   constexpr int S = mma_seg_blocks(FMT);
   // a whole segment is straight-line code (every offset a constant); a
   // part's ragged last segment takes the loop
@@ -619,18 +650,19 @@ __device__ __forceinline__ void mma_segment(const uint8_t* r0, const uint8_t* r1
     const uint32_t* R1 = reinterpret_cast<const uint32_t*>(r1);
     if (nbk == S) {
 #pragma unroll
-      for (int b = 0; b < S; ++b) MmaRows<FMT>::block_w(R0, R1, b, t, b * 32, xh, xl, acc);
+      for (int b = 0; b < S; ++b) MmaRows<FMT>::template block_w<NT>(R0, R1, b, t, b * 32, xh, xl, xt, acc);
     } else {
 #pragma unroll 1
-      for (int b = 0; b < nbk; ++b) MmaRows<FMT>::block_w(R0, R1, b, t, b * 32, xh, xl, acc);
+      for (int b = 0; b < nbk; ++b) MmaRows<FMT>::template block_w<NT>(R0, R1, b, t, b * 32, xh, xl, xt, acc);
     }
   } else {
     if (nbk == S) {
 #pragma unroll
-      for (int h = 0; h < 2 * S; ++h) MmaRows<FMT>::half_block(r0, r1, h, S, t, xh, xl, xs, acc);
+      for (int h = 0; h < 2 * S; ++h) MmaRows<FMT>::template half_block<NT>(r0, r1, h, S, t, xh, xl, xt, xs, acc);
     } else {
 #pragma unroll 1
-      for (int h = 0; h < 2 * nbk; ++h) MmaRows<FMT>::half_block(r0, r1, h, nbk, t, xh, xl, xs, acc);
+      for (int h = 0; h < 2 * nbk; ++h)
+        MmaRows<FMT>::template half_block<NT>(r0, r1, h, nbk, t, xh, xl, xt, xs, acc);
     }
   }
 }
@@ -640,15 +672,16 @@ __device__ __forceinline__ void mma_segment(const uint8_t* r0, const uint8_t* r1
 // stage, mbarrier completion), accumulates the MMA results of every segment
 // in registers, and writes the tile's partial sums itself.  No two warps
 // share a tile, so there is no barrier and no reduction between warps.
-template <int FMT>
+template <int FMT, int NT>
 __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs a) {
   using F = Q<FMT>;
   constexpr int S = mma_seg_blocks(FMT);
+  constexpr int MV = 8 * NT;  // vector slots
   extern __shared__ __align__(128) uint8_t smem[];
   const int NS = a.NS;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int xpitch = a.cwb * F::BE + 16;  // f16 per staged x vector
-  const MmaLayout L = mma_layout(a.cwb * F::BE, nwarps, NS);
+  const MmaLayout L = mma_layout(a.cwb * F::BE, MV, nwarps, NS);
   __half* xh = reinterpret_cast<__half*>(smem);
   __half* xl = reinterpret_cast<__half*>(smem + L.xl);
   float* xs = reinterpret_cast<float*>(smem + L.xs);
@@ -709,11 +742,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
   pdl_trigger();
   pdl_wait();
 
-  // ---- prologue: warp m < 8 holds vector m (zeros for m >= M): the part's
-  // columns, RMS-normalised when asked, scaled by a power of two, split into
-  // f16 hi + lo, and the sums of x over each 32 columns (scaled likewise)
-  if (warp < 8) {
-    const int m = warp;
+  // ---- prologue: warp w converts vectors w, w + warps, ... < MV (zeros for
+  // m >= M): the part's columns, RMS-normalised when asked, scaled by a power
+  // of two, split into f16 hi + lo, and the sums of x over each 32 columns
+  // (scaled likewise)
+  for (int m = warp; m < MV; m += nwarps) {
     float inv = 1.f;
     const float* xr = a.X + int64_t(m) * a.ldx;
     if (m < a.M && a.norm_g) {
@@ -794,8 +827,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
       else gs1 += s4;
     }
     if (64 * lane < a.cwb * F::BE) {  // the groups of the layout's part width
-      xs[(2 * lane) * 8 + m] = gs0;
-      xs[(2 * lane + 1) * 8 + m] = gs1;
+      xs[(2 * lane) * MV + m] = gs0;
+      xs[(2 * lane + 1) * MV + m] = gs1;
     }
   }
   __syncthreads();
@@ -803,7 +836,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
 
   const uint32_t* xh32 = reinterpret_cast<const uint32_t*>(xh + g * xpitch) + 2 * t;
   const uint32_t* xl32 = reinterpret_cast<const uint32_t*>(xl + g * xpitch) + 2 * t;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const int xt = 4 * xpitch;  // uint32 words between the x of N-tiles (8 vectors)
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
   bool dead = false;
   // consume cursor: stage slot and phase, segment, tile ordinal
   int cs = 0, csg = 0, ct = 0;
@@ -831,23 +867,26 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
       const int b0 = csg * S, nbk = min(S, blk_hi - blk_lo - b0);
       const uint8_t* stage = ring + size_t(cs) * a.SB + seg_off(csg);
       const int c0 = b0 * F::BE;  // first column of the segment in the part
-      mma_segment<FMT>(stage + size_t(g) * a.segB, stage + size_t(g + 8) * a.segB, nbk, t, xh32 + c0 / 2,
-                       xl32 + c0 / 2, xs + (c0 / 32) * 8, acc);
+      mma_segment<FMT, NT>(stage + size_t(g) * a.segB, stage + size_t(g + 8) * a.segB, nbk, t, xh32 + c0 / 2,
+                           xl32 + c0 / 2, xt, xs + (c0 / 32) * MV, acc);
     }
     __syncwarp();
     if (++csg == nseg) {
-      // the tile's partial sums: rows g, g + 8 and vectors 2t, 2t + 1 of this thread
+      // the tile's partial sums: rows g, g + 8 and vectors 8 nt + 2t, 8 nt + 2t + 1 of this thread
       csg = 0;
       int j, nr;
       int64_t r0;
       mma_locate(a, ws + int64_t(ct) * stride, j, r0, nr);
       const int64_t rbase = a.job[j].rb + r0;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int row = g + 8 * (e >> 1), n = 2 * t + (e & 1);
-        if (!dead && row < nr && n < a.M) a.part[(int64_t(p) * a.M + n) * a.total_rows + rbase + row] = acc[e] * xsc[n];
-        acc[e] = 0.f;
-      }
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int row = g + 8 * (e >> 1), n = 8 * nt + 2 * t + (e & 1);
+          if (!dead && row < nr && n < a.M)
+            a.part[(int64_t(p) * a.M + n) * a.total_rows + rbase + row] = acc[nt][e] * xsc[n];
+          acc[nt][e] = 0.f;
+        }
       ++ct;
     }
     if (++cs == NS) {
@@ -869,10 +908,10 @@ int mma_segB(int fmt) {
   return 16 * u;
 }
 
-size_t mma_smem(int fmt, int cwb, int warps, int NS) {
+size_t mma_smem(int fmt, int cwb, int MV, int warps, int NS) {
   const int segB = mma_segB(fmt);
   // + 16: the unaligned readers may touch 4 bytes past a row
-  return mma_layout(cwb * block_elems(fmt), warps, NS).ring + size_t(warps) * NS * kMmaRows * segB + 16;
+  return mma_layout(cwb * block_elems(fmt), MV, warps, NS).ring + size_t(warps) * NS * kMmaRows * segB + 16;
 }
 
 bool mma_format(int fmt) { return fmt == NT_Q8_0 || fmt == NT_Q4_K || fmt == NT_Q6_K; }
@@ -916,11 +955,16 @@ int gemm_parts(int fmt, int64_t cols) { return int((cols + part_cols(fmt) - 1) /
 // to one staged segment) while the 16-row tiles times the parts give fewer
 // than 4096 warp tasks, so that small matrices still occupy every SM.  A
 // function of the shape alone: the parts fix the order of the additions.
-static int mma_part_blocks(int fmt, int64_t tiles, int64_t nb) {
-  int cwb = 2048 / block_elems(fmt);
+static int mma_part_blocks(int fmt, int64_t tiles, int64_t nb, int MV) {
+  int cwb = (MV > 8 ? 1024 : 2048) / block_elems(fmt);  // the x of 16 vectors fits for 1024 columns
   const int S = mma_seg_blocks(fmt);
   while (cwb > S && tiles * ((nb + cwb - 1) / cwb) < 4096) cwb /= 2;
   return cwb;
+}
+
+bool gemm_wide_ok(const Ctx* c, int fmt, int64_t cols) {
+  return c->gemm_mma && mma_format(fmt) && cols % block_elems(fmt) == 0 &&
+         (cols / block_elems(fmt) * block_bytes(fmt)) % 16 == 0;
 }
 
 size_t gemm_scratch_bytes(int fmt, int64_t total_rows, int64_t cols, int M) {
@@ -928,7 +972,7 @@ size_t gemm_scratch_bytes(int fmt, int64_t total_rows, int64_t cols, int M) {
   if (mma_format(fmt)) {
     // fewer tiles than ceil(rows / 16) summed per job never occur, and more tiles never ask for more parts
     const int64_t nb = cols / block_elems(fmt);
-    const int cwb = mma_part_blocks(fmt, (total_rows + kMmaRows - 1) / kMmaRows, nb);
+    const int cwb = mma_part_blocks(fmt, (total_rows + kMmaRows - 1) / kMmaRows, nb, M > 8 ? 16 : 8);
     parts = std::max<int64_t>(parts, (nb + cwb - 1) / cwb);
   }
   return size_t(parts) * size_t(M) * size_t(total_rows) * sizeof(float);
@@ -954,9 +998,12 @@ nt_status configure_gemm(Ctx* c) {
   allow(qgemm_kernel<NT_Q6_K>);
   allow(qgemm_kernel<NT_F16>);
   allow(qgemm_kernel<NT_F32>);
-  allow(qgemm_mma_kernel<NT_Q8_0>);
-  allow(qgemm_mma_kernel<NT_Q4_K>);
-  allow(qgemm_mma_kernel<NT_Q6_K>);
+  allow(qgemm_mma_kernel<NT_Q8_0, 1>);
+  allow(qgemm_mma_kernel<NT_Q4_K, 1>);
+  allow(qgemm_mma_kernel<NT_Q6_K, 1>);
+  allow(qgemm_mma_kernel<NT_Q8_0, 2>);
+  allow(qgemm_mma_kernel<NT_Q4_K, 2>);
+  allow(qgemm_mma_kernel<NT_Q6_K, 2>);
   c->gemm_static_smem = st;
   return cuda_check(c, e, "gemm shared-memory attribute");
 }
@@ -965,7 +1012,7 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
                       int M, const float* norm_g, float eps, int64_t cols, const RopeArgs* rope, float* part,
                       size_t part_bytes, cudaStream_t st) {
   if (c->dry) return NT_OK;
-  if (M < 1 || M > kMaxVerify) return set_err(c, NT_ERR_INVALID_ARG, "gemm: M must be 1..%d", kMaxVerify);
+  if (M < 1 || M > kMaxGemmM) return set_err(c, NT_ERR_INVALID_ARG, "gemm: M must be 1..%d", kMaxGemmM);
   const int BB = block_bytes(fmt), BE = block_elems(fmt);
   const int64_t nb = cols / BE;
   const int64_t rowB = nb * BB;
@@ -990,9 +1037,13 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
   // the tensor-core form: its formats and bulk-copy alignment (rows of a
   // multiple of 16 bytes at 16-byte-aligned addresses)
   const bool mma = c->gemm_mma && mma_format(fmt) && tma;
+  if (M > kMaxVerify && !mma)
+    return set_err(c, NT_ERR_INVALID_ARG, "gemm: M > %d needs the tensor-core form (Q8_0, Q4_K, Q6_K; aligned rows)",
+                   kMaxVerify);
+  const int MV = M > 8 ? 16 : 8;  // vector slots: one or two MMA N-tiles
   int64_t tiles = 0;
   for (int j = 0; j < njobs; ++j) tiles += (jobs[j].rows + kMmaRows - 1) / kMmaRows;
-  const int cwb = mma ? mma_part_blocks(fmt, tiles, nb) : part_cols(fmt) / BE;
+  const int cwb = mma ? mma_part_blocks(fmt, tiles, nb, MV) : part_cols(fmt) / BE;
   const int nparts = int((nb + cwb - 1) / cwb);
   const size_t need = size_t(nparts) * M * size_t(rb) * sizeof(float);
   if (need > part_bytes)
@@ -1027,11 +1078,11 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
     // warps per CTA and stages per warp: the most warps whose rings of at
     // least two stages fit beside x, then as many stages as fit
     const size_t room = c->smem_optin - size_t(c->gemm_static_smem);
-    int warps = c->gemm_warps;
-    while (warps > 8 && mma_smem(fmt, cwb, warps, 2) > room) warps -= 4;  // 8 at least: warp m converts vector m
+    int warps = std::min(c->gemm_warps, kMmaWarps);
+    while (warps > 8 && mma_smem(fmt, cwb, MV, warps, 2) > room) warps -= 4;
     ma.NS = 2;
-    while (ma.NS < c->gemm_stages && mma_smem(fmt, cwb, warps, ma.NS + 1) <= room) ++ma.NS;
-    const size_t msmem = mma_smem(fmt, cwb, warps, ma.NS);
+    while (ma.NS < c->gemm_stages && mma_smem(fmt, cwb, MV, warps, ma.NS + 1) <= room) ++ma.NS;
+    const size_t msmem = mma_smem(fmt, cwb, MV, warps, ma.NS);
     if (msmem > room) return set_err(c, NT_ERR_INVALID_ARG, "gemm: no shared-memory plan for the tensor-core form");
     // CTAs side by side over the parts, at most one per SM in all (one wave);
     // no more warps than tiles
@@ -1041,10 +1092,19 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
     if (gx > need_x) gx = int(need_x);
     const dim3 grid(gx, nparts);
     cudaError_t err;
-    switch (fmt) {
-      case NT_Q8_0: err = launch_k(c, qgemm_mma_kernel<NT_Q8_0>, grid, dim3(32 * warps), msmem, st, ma); break;
-      case NT_Q4_K: err = launch_k(c, qgemm_mma_kernel<NT_Q4_K>, grid, dim3(32 * warps), msmem, st, ma); break;
-      default: err = launch_k(c, qgemm_mma_kernel<NT_Q6_K>, grid, dim3(32 * warps), msmem, st, ma); break;
+    const dim3 blk(32 * warps);
+    if (MV == 8) {
+      switch (fmt) {
+        case NT_Q8_0: err = launch_k(c, qgemm_mma_kernel<NT_Q8_0, 1>, grid, blk, msmem, st, ma); break;
+        case NT_Q4_K: err = launch_k(c, qgemm_mma_kernel<NT_Q4_K, 1>, grid, blk, msmem, st, ma); break;
+        default: err = launch_k(c, qgemm_mma_kernel<NT_Q6_K, 1>, grid, blk, msmem, st, ma); break;
+      }
+    } else {
+      switch (fmt) {
+        case NT_Q8_0: err = launch_k(c, qgemm_mma_kernel<NT_Q8_0, 2>, grid, blk, msmem, st, ma); break;
+        case NT_Q4_K: err = launch_k(c, qgemm_mma_kernel<NT_Q4_K, 2>, grid, blk, msmem, st, ma); break;
+        default: err = launch_k(c, qgemm_mma_kernel<NT_Q6_K, 2>, grid, blk, msmem, st, ma); break;
+      }
     }
     nt_status s = cuda_check(c, err, "qgemm (tensor-core) launch");
     if (s) return s;

@@ -226,9 +226,14 @@ nt_status nt_swiglu(nt_ctx* ctx, const float* gate_dev, const float* up_dev, flo
  * else X_dev[m].  X_dev fp32 [M][cols] (16-byte aligned, cols a multiple of
  * 4), Y_dev and residual_dev fp32 [M][rows] (residual may equal Y).  Every
  * weight byte is read once for all M vectors.  Precision and layout rules
- * as nt_gemv_q.  M 1..8.  Uses the context scratch beyond its first 32 MiB
- * for partial sums: NT_ERR_OOM when 4 * M * rows * ceil(cols / P) bytes do
- * not fit (P = 2048 columns; 1024 for F16, 512 for F32). */
+ * as nt_gemv_q.  M 1..8 for every format; M 1..16 for Q8_0, Q4_K and Q6_K
+ * with rows of a multiple of 16 bytes at a 16-byte-aligned W_dev (the
+ * tensor-core form; NT_ERR_INVALID_ARG otherwise, and under NT_GEMM_MMA=0).
+ * Uses the context scratch beyond its first 32 MiB for partial sums:
+ * NT_ERR_OOM when 4 * M * rows * P bytes do not fit, P the column parts
+ * (ceil(cols / 2048) for the integer form, 1024 for F16, 512 for F32; the
+ * tensor-core form narrows its parts for small matrices, at most to one
+ * staged segment: 512 columns for Q8_0 and Q6_K, 1024 for Q4_K). */
 nt_status nt_gemm_q(nt_ctx* ctx, int fmt, const void* W_dev, const float* X_dev, float* Y_dev, int64_t rows,
                     int64_t cols, int M, const float* residual_dev, const float* norm_g_dev, float eps,
                     void* stream);
@@ -351,9 +356,11 @@ nt_status nt_layer_skip_calibrate(nt_ctx* ctx, nt_model* model, int32_t token, i
 
 /* Prompt prefill [feat] (KV cache): run tokens_host[0..n) at positions
  * pos0 .. pos0 + n - 1 through every layer, writing their K/V into the
- * caches, in chunks of up to 8 tokens — each chunk one pass of the M-vector
- * GEMMs and the causal multi-query attention of the verify step (weights
- * read once per chunk).  logits_dev receives the logits after the last
+ * caches, in chunks of up to 16 tokens (8 when a GEMM of the model cannot
+ * take the tensor-core form: a format other than Q8_0 / Q4_K / Q6_K, rows
+ * not a multiple of 16 bytes, or a resident weight not 16-byte aligned) —
+ * each chunk one pass of the M-vector GEMMs and the causal multi-query
+ * attention of the verify step (weights read once per chunk).  logits_dev receives the logits after the last
  * token, next_token_dev (nullable) their argmax, and the device state
  * becomes (that argmax, pos0 + n): nt_decode_step with token < 0 continues
  * from there.  Runs eagerly on `stream` (no graph); streamed layers stream

@@ -1,7 +1,8 @@
 """Prompt prefill on the GPU (the step before decoding: "ntransformer - moteur
 d'inférence NVMe-to-GPU…", "Fonctionnalités principales", KV cache): chunks of
-up to 8 prompt tokens through the M-vector GEMMs and causal multi-query
-attention, against the fp64 oracle run token by token (teacher-forced).
+up to 16 prompt tokens (8 when a GEMM of the model takes the integer form)
+through the M-vector GEMMs and causal multi-query attention, against the fp64
+oracle run token by token (teacher-forced).
 
 Pins: the K/V the prefill writes for every prompt position match the
 oracle's — layer 0 to one f16 ulp plus the fp32 GEMV rounding; deeper layers
@@ -37,7 +38,7 @@ def _prompt(spec, n, stream):
 
 @pytest.mark.parametrize("name,n,pos0", [("tiny_q4_k_m", 20, 37), ("tiny_q8_0", 8, 0), ("small_q6_k", 13, 300),
                                          ("tiny_f16", 3, 40), ("small_q4_k_m_r1", 11, 290),
-                                         ("tiny_q8_0", 1, 0)])
+                                         ("tiny_q8_0", 1, 0), ("tiny_q8_0", 37, 5)])
 def test_prefill_matches_oracle(ctx, name, n, pos0):
     from block_quantized_gemv_nt_gb300 import engine
     spec = synth.model_spec(name)

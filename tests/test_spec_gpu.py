@@ -77,15 +77,45 @@ def test_gemm_q_one_vector_equals_gemv(ctx):
     assert rel_l2(host(b[0]), host(a).astype(np.float64)) <= 1e-6
 
 
+@pytest.mark.parametrize("fmt", [synth.Q8_0, synth.Q4_K, synth.Q6_K])
+@pytest.mark.parametrize("rows,cols,M", [(300, 2304, 16), (257, 4608, 9), (64, 2048, 12), (1000, 512, 16),
+                                         (4096, 4096, 16)])
+def test_gemm_q_sixteen_vectors(ctx, fmt, rows, cols, M):
+    """M 9..16 (two MMA N-tiles of 8 vectors, the prompt-chunk width) against
+    the oracle, with the fused RMSNorm on half the cases; ragged parts, row
+    tiles and vector counts.  The tensor-core form needs rows of a multiple of
+    16 bytes: Q6_K's 210-byte blocks take column counts of a multiple of 2048."""
+    from block_quantized_gemv_nt_gb300 import nt
+    if fmt == synth.Q6_K:
+        cols = max(2048, cols // 2048 * 2048)
+    W = synth.quant_matrix(fmt, rows, cols, seed=24, stream=fmt)
+    X = synth.normal_f32(M * cols, seed=24, stream=80 + M).reshape(M, cols) * 3
+    g = synth.normal_f32(cols, seed=24, stream=81, mean=1.0, std=0.02)
+    norm = (rows + M) % 2 == 0
+    Y = torch.empty(M, rows, dtype=torch.float32, device="cuda")
+    nt.nt_gemm_q(ctx, fmt, dev(W), dev(X), Y, rows, cols, M, norm_g=dev(g) if norm else None, eps=1e-5)
+    torch.cuda.synchronize()
+    for m in range(M):
+        x = X[m].astype(np.float64)
+        if norm:
+            x = oracle.rmsnorm(x, g, 1e-5)
+        assert rel_l2(host(Y[m]), oracle.gemv(fmt, W, x, rows, cols)) <= 1e-3, m
+
+
 def test_gemm_q_bad_args(ctx):
     from block_quantized_gemv_nt_gb300 import nt
     W = torch.zeros(64 * 34 * 8, dtype=torch.uint8, device="cuda")
-    X = torch.zeros(9 * 256, device="cuda")
-    Y = torch.zeros(9 * 64, device="cuda")
-    for M, cols in [(0, 256), (9, 256), (2, 100)]:
+    X = torch.zeros(17 * 256, device="cuda")
+    Y = torch.zeros(17 * 64, device="cuda")
+    for M, cols in [(0, 256), (17, 256), (2, 100)]:
         with pytest.raises(nt.NtError) as ei:
             nt.nt_gemm_q(ctx, synth.Q8_0, W, X, Y, 64, cols, M)
         assert ei.value.status == nt.NT_ERR_INVALID_ARG
+    # more than 8 vectors only in the tensor-core form: not for Q4_0
+    W4 = torch.zeros(64 * 18 * 8, dtype=torch.uint8, device="cuda")
+    with pytest.raises(nt.NtError) as ei:
+        nt.nt_gemm_q(ctx, synth.Q4_0, W4, X, Y, 64, 256, 9)
+    assert ei.value.status == nt.NT_ERR_INVALID_ARG
 
 
 # ---- causal multi-query attention -------------------------------------------
