@@ -364,6 +364,8 @@ constexpr int kMmaWarps = 12;                     // warps per CTA at most (the 
 constexpr int kMmaThreads = kMmaWarps * 32;
 constexpr int kMmaRows = 16;                      // rows per tile (the MMA's m)
 
+constexpr int kMaxChunksRms = 1024;  // 128-column chunks: vectors of up to 131072 columns
+
 struct MmaArgs {
   GemmJobDev job[3];  // g0: first 16-row tile of the job; rb: first row in the row space
   int njobs;
@@ -382,7 +384,36 @@ struct MmaArgs {
   float* part;
   unsigned* err;
   int stall;
+  const float* inv;  // with norm_g: rsqrt(mean x_m^2 + eps) per vector, from rms_inv_kernel
 };
+
+// The RMSNorm scalar of each of the M vectors, once per launch instead of in
+// every CTA: block m sums x_m^2 per 128-column chunk (one warp per chunk),
+// then over the chunks in index order, and writes rsqrt(mean + eps).
+__global__ void __launch_bounds__(256) rms_inv_kernel(const float* X, int64_t ldx, int cols, float eps, float* inv) {
+  __shared__ float red[kMaxChunksRms];
+  pdl_wait();
+  pdl_trigger();
+  const int m = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const float* xr = X + int64_t(m) * ldx;
+  const int nchunk = (cols + 127) / 128;
+  for (int ch = warp; ch < nchunk; ch += nwarps) {
+    const int c = 128 * ch + 4 * lane;
+    float ss = 0.f;
+    if (c < cols) {
+      const float4 v = *reinterpret_cast<const float4*>(xr + c);
+      ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, v.w * v.w)));
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[ch] = ss;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int ch = 0; ch < nchunk; ++ch) tot += red[ch];
+    inv[m] = rsqrtf(tot / float(cols) + eps);
+  }
+}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -749,27 +780,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) qgemm_mma_kernel(const MmaArgs
   for (int m = warp; m < MV; m += nwarps) {
     float inv = 1.f;
     const float* xr = a.X + int64_t(m) * a.ldx;
-    if (m < a.M && a.norm_g) {
-      // sum of squares per 128-column chunk, then over the chunks in order;
-      // eight chunks' loads in flight at a time
-      float tot = 0.f;
-      for (int c0 = 0; c0 < a.cols; c0 += 8 * 128) {
-        float ss[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int c = c0 + 128 * k + 4 * lane;
-          ss[k] = 0.f;
-          if (c < a.cols) {
-            const float4 v = *reinterpret_cast<const float4*>(xr + c);
-            ss[k] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, v.w * v.w)));
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (c0 + 128 * k < a.cols) tot += warp_sum(ss[k]);
-      }
-      inv = rsqrtf(tot / float(a.cols) + a.eps);
-    }
+    if (m < a.M && a.norm_g) inv = a.inv[m];
     // lane l holds columns 64 l .. 64 l + 63 of the part: 16 float4, loaded
     // together (one memory round trip)
     float4 xv[16];
@@ -955,6 +966,9 @@ int gemm_parts(int fmt, int64_t cols) { return int((cols + part_cols(fmt) - 1) /
 // to one staged segment) while the 16-row tiles times the parts give fewer
 // than 4096 warp tasks, so that small matrices still occupy every SM.  A
 // function of the shape alone: the parts fix the order of the additions.
+// bytes after the partial sums for the M RMSNorm scalars (and alignment)
+constexpr size_t kInvBytes = 512;
+
 static int mma_part_blocks(int fmt, int64_t tiles, int64_t nb, int MV) {
   int cwb = (MV > 8 ? 1024 : 2048) / block_elems(fmt);  // the x of 16 vectors fits for 1024 columns
   const int S = mma_seg_blocks(fmt);
@@ -975,7 +989,8 @@ size_t gemm_scratch_bytes(int fmt, int64_t total_rows, int64_t cols, int M) {
     const int cwb = mma_part_blocks(fmt, (total_rows + kMmaRows - 1) / kMmaRows, nb, M > 8 ? 16 : 8);
     parts = std::max<int64_t>(parts, (nb + cwb - 1) / cwb);
   }
-  return size_t(parts) * size_t(M) * size_t(total_rows) * sizeof(float);
+  // + the RMSNorm scalars of the tensor-core form, after the partials
+  return size_t(parts) * size_t(M) * size_t(total_rows) * sizeof(float) + kInvBytes;
 }
 
 nt_status configure_gemm(Ctx* c) {
@@ -1045,7 +1060,7 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
   for (int j = 0; j < njobs; ++j) tiles += (jobs[j].rows + kMmaRows - 1) / kMmaRows;
   const int cwb = mma ? mma_part_blocks(fmt, tiles, nb, MV) : part_cols(fmt) / BE;
   const int nparts = int((nb + cwb - 1) / cwb);
-  const size_t need = size_t(nparts) * M * size_t(rb) * sizeof(float);
+  const size_t need = size_t(nparts) * M * size_t(rb) * sizeof(float) + (mma && norm_g ? kInvBytes : 0);
   if (need > part_bytes)
     return set_err(c, NT_ERR_OOM, "gemm: %zu scratch bytes needed for the partial sums, %zu available", need,
                    part_bytes);
@@ -1075,6 +1090,17 @@ nt_status launch_gemm(Ctx* c, int fmt, const GemmJobEx* jobs, int njobs, bool sw
     ma.part = part;
     ma.err = c->err_flag;
     ma.stall = take_stall(st);
+    if (norm_g) {
+      // the M RMSNorm scalars, once, right after the partial sums (256-byte aligned)
+      if ((cols + 127) / 128 > kMaxChunksRms)
+        return set_err(c, NT_ERR_INVALID_ARG, "gemm: cols=%lld too large for the fused RMSNorm", (long long)cols);
+      const size_t off = (size_t(nparts) * M * size_t(rb) * sizeof(float) + 255) / 256 * 256;
+      float* inv = reinterpret_cast<float*>(reinterpret_cast<char*>(part) + off);
+      nt_status s0 = cuda_check(c, launch_k(c, rms_inv_kernel, dim3(M), dim3(256), 0, st, X, ldx, int(cols), eps, inv),
+                                "gemm RMSNorm launch");
+      if (s0) return s0;
+      ma.inv = inv;
+    }
     // warps per CTA and stages per warp: the most warps whose rings of at
     // least two stages fit beside x, then as many stages as fit
     const size_t room = c->smem_optin - size_t(c->gemm_static_smem);
