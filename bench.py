@@ -11,12 +11,14 @@ independent replicas ("scaling": "weak"): the path has no exchange step.
 from __future__ import annotations
 
 import argparse
+import atexit
 import hashlib
 import json
 import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import threading
 import time
 
@@ -365,9 +367,28 @@ def gemv_plan(spec, skip=None):
     return plan
 
 
+def gemm_launches(fmt, cols, normed):
+    """Kernel launches of one verify GEMM: the GEMM and its epilogue, plus the
+    RMSNorm scalars' kernel when a normed launch takes the tensor-core form
+    (Q8_0 / Q4_K / Q6_K rows of a multiple of 16 bytes)."""
+    import synth
+    wide = (os.environ.get("NT_GEMM_MMA", "1") != "0" and fmt in (synth.Q8_0, synth.Q4_K, synth.Q6_K)
+            and synth.row_bytes(fmt, cols) % 16 == 0)
+    return 2 + (1 if normed and wide else 0)
+
+
+def verify_layer_launches(spec):
+    """Launches of one layer of a verify (or prefill) pass: the Q/K/V GEMMs (one
+    per format), attention (split, combine), O, gate/up and down."""
+    nq = spec.n_qh * spec.head_dim
+    qkv = sum(gemm_launches(f, spec.d_model, True) for f in {spec.fmt[t] for t in ("wq", "wk", "wv")})
+    return (qkv + 2 + gemm_launches(spec.fmt["wo"], nq, False) + gemm_launches(spec.fmt["wg"], spec.d_model, True)
+            + gemm_launches(spec.fmt["wd"], spec.ffn, False))
+
+
 def bench_prefill(args, rank, world):
-    """<model>_prefill<N>: one N-token prompt through nt_prefill (chunks of 8
-    tokens through the verify GEMMs), repeated; tokens/s of prompt."""
+    """<model>_prefill<N>: one N-token prompt through nt_prefill (chunks of 16
+    tokens, or 8, through the verify GEMMs), repeated; tokens/s of prompt."""
     import torch
 
     import synth
@@ -399,7 +420,8 @@ def bench_prefill(args, rank, world):
             clk.mark_end()
             clk.wait_one_more()
     ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
-    chunks = -(-n // 8)
+    chunk = nt.nt_model_prefill_chunk(ctx, gm.handle)
+    chunks = -(-n // chunk)
     wbytes = spec.layer_bytes() * spec.n_layers
     gbs = chunks * wbytes / (ms / 1e3) / 1e9
     peak, kind = measured_peaks()
@@ -416,18 +438,18 @@ def bench_prefill(args, rank, world):
         e2e_s = max_over_ranks((time.perf_counter() - h0) / n_e2e, world)
     ctx.sync()
     gm.close()
-    # launches per prompt: per chunk its setup, the embedding rows, and per layer the Q/K/V GEMMs (GEMM +
-    # epilogue per format), attention (split, combine), O, gate/up and down; after the last chunk the LM head
-    # (GEMM + epilogue), the state update and the argmax
-    per_layer = 2 * len({spec.fmt[t] for t in ("wq", "wk", "wv")}) + 8
-    launches = chunks * (2 + spec.n_layers * per_layer) + 4
+    # launches per prompt: per chunk its setup, the embedding rows and the layers; after the last chunk the
+    # LM head, the state update and the argmax
+    launches = (chunks * (2 + spec.n_layers * verify_layer_launches(spec))
+                + gemm_launches(spec.fmt["out"], spec.d_model, True) + 2)
     return {"metric": METRIC, "value": round(n / (ms / 1e3) * world, 2), "unit": "prompt tok/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32 (block-quantized weights, f16 KV)",
             "data": "synthetic: random weights of the named shape, seeded", "impl": "ours",
-            "config": {"workload": args.workload, "prompt_tokens": n, "chunks_of_8": chunks, "pos0": pos0,
+            "config": {"workload": args.workload, "prompt_tokens": n, "chunk_tokens": chunk, "chunks": chunks,
+                       "pos0": pos0,
                        "l2": f"inputs larger than L2 ({wbytes / 1e9:.2f} GB of weights per chunk)"},
-            "roofline": {"bound": "hbm", "kernel": "qgemm (M = 8; integer-issue-bound, far from the HBM bound)",
+            "roofline": {"bound": "hbm", "kernel": f"qgemm (M <= {chunk}; issue-bound, far from the HBM bound)",
                          "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
                          "peak_kind": kind, "traffic": None,
                          "algo_bytes_per_launch": wbytes},
@@ -454,13 +476,16 @@ def decode_kernels_per_step(spec, n_exec, sampled=False):
 
 
 def parse_decode(name):
-    """<model>[_skip<N>][_spec<K>][_sample]: a synthetic model, optionally
+    """<model>[_skip<N>][_spec<K>][_sample][_file]: a synthetic model, optionally
     decoding with the N layers of highest calibration cosine skipped, or
     self-speculatively with K drafted tokens per step; "_sample" draws tokens
     with the sampler (SAMPLER) instead of the argmax (speculative sampling
-    with _spec).  Returns (spec, n_skip, k, sampled)."""
+    with _spec); "_file" streams a streamed model's layers from a model file
+    (bench_streamed).  Returns (spec, n_skip, k, sampled)."""
     import synth
     n_skip = k = 0
+    if name.endswith("_file"):
+        name = name[:-len("_file")]
     sampled = name.endswith("_sample")
     if sampled:
         name = name[:-len("_sample")]
@@ -652,11 +677,25 @@ def bench_streamed(args, rank, world):
 
     spec, n_skip, k, sampled = parse_decode(args.workload)
     assert n_skip == 0, "layer skip is not combined with streaming here"
+    from_file = args.workload.endswith("_file")
     t0 = time.perf_counter()
     blobs = engine.HostBlobs(spec)
     hm = synth.make_host_model(spec, out_view=blobs.view)
     t_gen = time.perf_counter() - t0
     ctx = nt.Context(torch.cuda.current_device())
+    mf = fpath = None
+    ram_blobs = blobs  # the pinned-RAM copy of the streamed layers: also the copy-peak reference
+    if from_file:
+        # the host-file tier: the model written to a file (RAM-backed /dev/shm when present), its
+        # streamed layers page-locked in the mapping where the OS allows, else copied once
+        from block_quantized_gemv_nt_gb300 import modelfile
+        fdir = "/dev/shm" if os.path.isdir("/dev/shm") else tempfile.gettempdir()
+        fpath = os.path.join(fdir, f"nt_bench_{os.getpid()}_{rank}.ntq")
+        atexit.register(lambda p=fpath: os.path.exists(p) and os.unlink(p))  # removed however the run ends
+        modelfile.write_model(fpath, spec, hm)
+        mf = modelfile.ModelFile(fpath)
+        hm = synth.HostModel(mf.spec, mf.layers, mf.embd, mf.out, mf.out_norm, hm.kcache, hm.vcache)
+        blobs = modelfile.FileBlobs(ctx, mf, spec.n_resident)
     slots = args.stream_slots
     if slots <= 0:
         # greedy: double buffering (per-layer compute is far below a layer copy);
@@ -665,7 +704,7 @@ def bench_streamed(args, rank, world):
         r, c = spec.tensor_shape("out")
         fixed = spec.n_resident * spec.layer_bytes() + r * synth.row_bytes(spec.fmt["out"], c)
         slots = int(max(2, min(8, (args.hbm_weight_cap * 1e9 - fixed) // blobs.nbytes))) if k else 2
-    gm = engine.DeviceModel(ctx, spec, hm, blobs=blobs, stream_slots=slots)
+    gm = engine.DeviceModel(ctx, mf.spec if from_file else spec, hm, blobs=blobs, stream_slots=slots)
     if sampled:
         gm.set_sampler(*SAMPLER, seed=spec.seed)
     st = torch.cuda.Stream()
@@ -707,7 +746,7 @@ def bench_streamed(args, rank, world):
     tok_s = n_tok / (ms / 1e3)
     pass_s = ms / 1e3 / args.steps
     link_bytes = n_streamed * blobs.nbytes          # host -> HBM bytes of one pass
-    b_h2d = h2d_peak(blobs.blob[blobs.layers[0]], blobs.nbytes)
+    b_h2d = h2d_peak(ram_blobs.blob[ram_blobs.layers[0]], ram_blobs.nbytes)
     link_gbs = link_bytes / pass_s / 1e9
 
     # e2e: host-driven loop through the C ABI, results back to pinned host memory each step
@@ -770,15 +809,25 @@ def bench_streamed(args, rank, world):
         # per pass: setup, k drafts (resident layers), verify (GEMM + epilogue per GEMV, attention), accept
         n_res = spec.n_resident
         draft = 2 + n_res * per_layer + (6 if sampled else 1)
-        # every verify GEMM is two launches (the GEMM and its epilogue); attention is split + combine
-        verify = 1 + n_exec * (2 * (per_layer - 2) + 2) + 2 + (6 if sampled else k + 1)
+        verify = (1 + n_exec * verify_layer_launches(spec) + gemm_launches(spec.fmt["out"], spec.d_model, True)
+                  + (6 if sampled else k + 1))
         line["gpu_launches"] = args.steps * (2 + k * draft + verify)
     else:
         line["gpu_launches"] = (args.steps * (2 + n_exec * per_layer + (6 if sampled else 1))
                                 + (args.steps + window - 1) // window)
+    if from_file:
+        rungs = {}
+        for r in blobs.rung_of.values():
+            rungs[r] = rungs.get(r, 0) + 1
+        line["config"]["host_source"] = {"model_file": fpath, "tier": blobs.tier, "ranges_by_rung": rungs}
+        line["roofline"]["peak_kind"] = "measured in this run: best pinned-RAM copy of one layer blob"
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_decode(spec, hm, budget_s=args.cpu_budget)
     gm.close()
+    if from_file:
+        blobs.close()
+        mf.close()
+        os.unlink(fpath)
     return line
 
 

@@ -1048,6 +1048,13 @@ static int prefill_chunk(const Ctx* c, const nt_model* m) {
   return kMaxGemmM;
 }
 
+nt_status nt_model_prefill_chunk(nt_ctx* ctx, nt_model* m, int* chunk) {
+  if (!ctx) return NT_ERR_INVALID_ARG;
+  NT_REQUIRE(m && chunk, NT_ERR_INVALID_ARG, "null model or chunk");
+  *chunk = prefill_chunk(ctx, m);
+  return NT_OK;
+}
+
 nt_status nt_prefill(nt_ctx* ctx, nt_model* m, const int32_t* tokens_host, int64_t n, int64_t pos0, float* logits,
                      int32_t* next_tok, void* stream) {
   NvtxRange nvtx_range("nt_prefill");

@@ -117,6 +117,7 @@ _sig("nt_debug_host_delay", [_vp, _vp, _i64])
 _sig("nt_debug_stall_waits", [_ci])
 _sig("nt_ctx_gemv_plans", [_vp, _vp, _sz, ctypes.POINTER(_sz)])
 _sig("nt_model_graph_count", [_vp, _vp, ctypes.POINTER(_ci)])
+_sig("nt_model_prefill_chunk", [_vp, _vp, ctypes.POINTER(_ci)])
 
 EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "nt_block_bytes", "nt_block_elems",
             "nt_dequant_rows", "nt_gemv_q", "nt_gemv_q_swiglu", "nt_gemv_q_multi", "nt_rmsnorm", "nt_rope",
@@ -125,7 +126,7 @@ EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "
             "nt_attn_decode_static", "nt_layer_blob_layout", "nt_stream_layer", "nt_model_slot", "nt_spec_step",
             "nt_gemm_q", "nt_attn_verify", "nt_plan_residency", "nt_prefill", "nt_sample", "nt_model_set_sampler",
             "nt_host_register", "nt_host_unregister", "nt_stream_sync", "nt_debug_fail_copy", "nt_debug_host_delay",
-            "nt_debug_stall_waits", "nt_ctx_gemv_plans", "nt_model_graph_count"]
+            "nt_debug_stall_waits", "nt_ctx_gemv_plans", "nt_model_graph_count", "nt_model_prefill_chunk"]
 
 
 def lib():
@@ -307,6 +308,12 @@ def nt_ctx_gemv_plans(ctx) -> list:
 def nt_model_graph_count(ctx, model: int) -> int:
     n = _ci()
     ctx.check(_lib.nt_model_graph_count(ctx.handle, model, ctypes.byref(n)))
+    return n.value
+
+
+def nt_model_prefill_chunk(ctx, model: int) -> int:
+    n = ctypes.c_int(0)
+    ctx.check(_lib.nt_model_prefill_chunk(ctx.handle, model, ctypes.byref(n)))
     return n.value
 
 

@@ -368,6 +368,11 @@ nt_status nt_layer_skip_calibrate(nt_ctx* ctx, nt_model* model, int32_t token, i
 nt_status nt_prefill(nt_ctx* ctx, nt_model* model, const int32_t* tokens_host, int64_t n, int64_t pos0,
                      float* logits_dev, int32_t* next_token_dev, void* stream);
 
+/* Prompt tokens per nt_prefill pass [feat] (KV cache): 16 when every GEMM of
+ * the model's step takes the tensor-core form, else 8 (the rule above).
+ * Writes it to *chunk; NT_ERR_INVALID_ARG for a NULL model or chunk. */
+nt_status nt_model_prefill_chunk(nt_ctx* ctx, nt_model* model, int* chunk);
+
 /* Resident-layer planner [about] (3-tier adaptive caching: VRAM-resident
  * layers first, the rest from pinned RAM) [cache] (the format decides how
  * many layers fit: "36 vs 26" for Q4_K_M vs Q6_K on the pages' card): how

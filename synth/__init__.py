@@ -186,6 +186,10 @@ def model_spec(name: str) -> ModelSpec:
     if name == "llama8b_q8_0":
         return ModelSpec(name, 32, 4096, 32, 8, 128, 14336, 128256, 1e-5, 500000.0, seed=1,
                          n_prefill=1024, n_gen=128, fmt=_uniform_fmt(Q8_0))
+    if name == "llama8b_q8_0_streamed":
+        # the 8B workload's weights (same seed) with layers 16..31 streamed from host memory
+        return ModelSpec(name, 32, 4096, 32, 8, 128, 14336, 128256, 1e-5, 500000.0, seed=1,
+                         n_prefill=1024, n_gen=128, fmt=_uniform_fmt(Q8_0), n_resident=16)
     if name == "llama70b_q4_k_m":
         return ModelSpec(name, 80, 8192, 64, 8, 128, 28672, 128256, 1e-5, 500000.0, seed=2,
                          n_prefill=4096, n_gen=64, fmt=_q4_k_m())

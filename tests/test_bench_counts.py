@@ -33,3 +33,15 @@ def test_step_bytes_8b():
     got = bench.step_bytes(spec)
     # the step also reads one embedding row and the KV cache; the weights are all but a few percent
     assert weights <= got <= weights * 1.03, (got, weights)
+
+
+def test_verify_layer_launches():
+    """A verify or prefill layer: every GEMM is its kernel and the epilogue that
+    adds the column parts; a normed GEMM in the tensor-core form (Q8_0 / Q4_K /
+    Q6_K) has the RMSNorm scalars' kernel in front; attention is split +
+    combine."""
+    assert bench.verify_layer_launches(synth.model_spec("llama8b_q8_0")) == 3 + 2 + 2 + 3 + 2
+    # Q/K in Q4_K and V in Q6_K: two normed Q/K/V launches
+    assert bench.verify_layer_launches(synth.model_spec("llama70b_q4_k_m")) == 2 * 3 + 2 + 2 + 3 + 2
+    # F16 takes the integer form: no RMSNorm kernel
+    assert bench.verify_layer_launches(synth.model_spec("tiny_f16")) == 2 + 2 + 2 + 2 + 2
