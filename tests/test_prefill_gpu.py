@@ -79,6 +79,21 @@ def test_prefill_matches_oracle(ctx, name, n, pos0):
     gm.close()
 
 
+@pytest.mark.parametrize("name,chunk", [("tiny_q8_0", 16), ("tiny_q4_k_m", 16), ("small_q6_k", 16),
+                                        ("tiny_f16", 8), ("tiny_q4_0", 8), ("small_q4_k_m_r1", 16)])
+def test_prefill_chunk(ctx, name, chunk):
+    """16 prompt tokens per pass when every GEMM of the model takes the
+    tensor-core form (Q8_0 / Q4_K / Q6_K, streamed layers in aligned slots
+    included), 8 when one takes the integer form."""
+    from block_quantized_gemv_nt_gb300 import engine, nt
+    spec = synth.model_spec(name)
+    blobs = engine.HostBlobs(spec) if spec.n_resident >= 0 else None
+    hm = synth.make_host_model(spec, out_view=blobs.view if blobs else None)
+    gm = engine.DeviceModel(ctx, spec, hm, blobs=blobs)
+    assert nt.nt_model_prefill_chunk(ctx, gm.handle) == chunk
+    gm.close()
+
+
 def test_prefill_bad_args(ctx):
     from block_quantized_gemv_nt_gb300 import engine, nt
     spec = synth.model_spec("tiny_q8_0")
