@@ -38,7 +38,7 @@ def _prompt(spec, n, stream):
 
 @pytest.mark.parametrize("name,n,pos0", [("tiny_q4_k_m", 20, 37), ("tiny_q8_0", 8, 0), ("small_q6_k", 13, 300),
                                          ("tiny_f16", 3, 40), ("small_q4_k_m_r1", 11, 290),
-                                         ("tiny_q8_0", 1, 0), ("tiny_q8_0", 37, 5)])
+                                         ("tiny_q8_0", 1, 0), ("tiny_q8_0", 37, 5), ("small_q4_k_m_r1", 20, 270)])
 def test_prefill_matches_oracle(ctx, name, n, pos0):
     from block_quantized_gemv_nt_gb300 import engine
     spec = synth.model_spec(name)

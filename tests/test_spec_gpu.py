@@ -92,14 +92,20 @@ def test_gemm_q_sixteen_vectors(ctx, fmt, rows, cols, M):
     X = synth.normal_f32(M * cols, seed=24, stream=80 + M).reshape(M, cols) * 3
     g = synth.normal_f32(cols, seed=24, stream=81, mean=1.0, std=0.02)
     norm = (rows + M) % 2 == 0
+    res = synth.normal_f32(M * rows, seed=24, stream=82).reshape(M, rows)
     Y = torch.empty(M, rows, dtype=torch.float32, device="cuda")
+    Yr = dev(res)
     nt.nt_gemm_q(ctx, fmt, dev(W), dev(X), Y, rows, cols, M, norm_g=dev(g) if norm else None, eps=1e-5)
+    nt.nt_gemm_q(ctx, fmt, dev(W), dev(X), Yr, rows, cols, M, residual=Yr, norm_g=dev(g) if norm else None,
+                 eps=1e-5)
     torch.cuda.synchronize()
     for m in range(M):
         x = X[m].astype(np.float64)
         if norm:
             x = oracle.rmsnorm(x, g, 1e-5)
-        assert rel_l2(host(Y[m]), oracle.gemv(fmt, W, x, rows, cols)) <= 1e-3, m
+        ref = oracle.gemv(fmt, W, x, rows, cols)
+        assert rel_l2(host(Y[m]), ref) <= 1e-3, m
+        assert rel_l2(host(Yr[m]), ref + res[m]) <= 1e-3, m
 
 
 def test_gemm_q_bad_args(ctx):
