@@ -437,12 +437,6 @@ constexpr uint32_t kBias1024 = 0x64006400u;  // f16 pair (1024, 1024)
 constexpr uint32_t kBias1056 = 0x64206420u;  // (1056, 1056): 1024 + the Q6_K offset 32
 constexpr uint32_t kBias1152 = 0x64806480u;  // (1152, 1152): 1024 + 128 for sign-flipped int8
 
-// a little-endian word at a 2-byte-aligned shared address
-__device__ __forceinline__ uint32_t lds32_a2(const uint8_t* p) {
-  const uint32_t mis = smem_u32(p) & 2u;
-  const uint32_t* b = reinterpret_cast<const uint32_t*>(p - mis);
-  return mis ? __funnelshift_r(b[0], b[1], 16) : b[0];
-}
 
 template <int FMT>
 struct MmaRows;
@@ -600,11 +594,26 @@ struct MmaRows<NT_Q6_K> {
     const int c0 = b * 256;
     const float d0 = __half2float(*reinterpret_cast<const __half*>(p0 + 208));
     const float d1 = __half2float(*reinterpret_cast<const __half*>(p1 + 208));
+    // a segment's first block starts 4-byte aligned (a multiple of 420 bytes
+    // plus the 16-byte-aligned copy's offset, a multiple of 4): block 0 of a
+    // pair is word-aligned, block 1 sits 2 bytes off (a funnel shift by 16)
+    // (with two N-tiles the runtime-checked form measured faster: register room)
+    auto ldw = [&](const uint8_t* p, int off) -> uint32_t {
+      if constexpr (NT == 1) {
+        if (b % 2 == 0) return *reinterpret_cast<const uint32_t*>(p + off);
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(p + off - 2);
+        return __funnelshift_r(w[0], w[1], 16);
+      } else {
+        const uint32_t mis = smem_u32(p + off) & 2u;
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(p + off - mis);
+        return mis ? __funnelshift_r(w[0], w[1], 16) : w[0];
+      }
+    };
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const int lo = 64 * h + 16 * s + 4 * t, qh = 128 + 32 * h + 16 * s + 4 * t;
-      const uint32_t A0 = lds32_a2(p0 + lo), B0 = lds32_a2(p0 + lo + 32), H0 = lds32_a2(p0 + qh);
-      const uint32_t A1 = lds32_a2(p1 + lo), B1 = lds32_a2(p1 + lo + 32), H1 = lds32_a2(p1 + qh);
+      const uint32_t A0 = ldw(p0, lo), B0 = ldw(p0, lo + 32), H0 = ldw(p0, qh);
+      const uint32_t A1 = ldw(p1, lo), B1 = ldw(p1, lo + 32), H1 = ldw(p1, qh);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         const uint32_t L0 = (g & 1) ? B0 : A0, L1 = (g & 1) ? B1 : A1;
