@@ -138,7 +138,9 @@ nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes) {
   c->gemv_stages = env_int("NT_GEMV_STAGES", 2, 8, 2);
   c->gemv_stage_max = env_int("NT_GEMV_STAGE_MAX", 1024, 65536, 12288) / 16 * 16;
   c->pdl = env_int("NT_PDL", 0, 1, 1) != 0;
-  c->gemv_tune = env_int("NT_GEMV_TUNE", 0, 1, 1) != 0;
+  // timing candidate launch shapes picks the fastest alone, which is not
+  // always the fastest inside a decode step: off unless asked for
+  c->gemv_tune = env_int("NT_GEMV_TUNE", 0, 1, 0) != 0;
   c->attn_fill = env_int("NT_ATTN_FILL", 0, 1, 1) != 0;
   c->gemm_mma = env_int("NT_GEMM_MMA", 0, 1, 1) != 0;
   c->gemm_warps = env_int("NT_GEMM_WARPS", 8, 12, 12) / 4 * 4;

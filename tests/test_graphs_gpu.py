@@ -128,7 +128,8 @@ def test_processes_decode_bit_identically(tmp_path):
     shapes (8 warps, 24 KB stages, no tuning).  Every logit is
     bit-identical: the plans differ only in how the work is launched."""
     need_gpu()
-    envs = [{}, {}, {"NT_GEMV_TUNE": "0", "NT_GEMV_WARPS": "8", "NT_GEMV_STAGE_MAX": "24576"}]
+    envs = [{"NT_GEMV_TUNE": "1"}, {"NT_GEMV_TUNE": "1"},
+            {"NT_GEMV_TUNE": "0", "NT_GEMV_WARPS": "8", "NT_GEMV_STAGE_MAX": "24576"}]
     outs = []
     for i, extra in enumerate(envs):
         path = str(tmp_path / f"logits{i}.npy")
