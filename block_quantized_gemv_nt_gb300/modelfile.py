@@ -13,11 +13,14 @@ streamed layer is one contiguous, page-aligned range of the file:
                matrices in the library's blob layout, nt_layer_blob_layout),
                "attn_norm.l", "ffn_norm.l"
 
-``ModelFile`` maps the file read-only.  Resident layers are uploaded from
-the mapping; the streamed layers' blobs (and the embedding table) are
-page-locked where they lie, so the streaming engine copies them to HBM
-exactly as it copies pinned RAM.  ``FileBlobs`` takes the first rung that
-the operating system and driver accept, in the pages' order of preference:
+``write_model`` writes it; reading is native (libnt.so: nt_file_open,
+nt_file_entry, nt_file_lock), so a C caller has the whole tier too.
+``ModelFile`` opens the file through that reader.  Resident layers are
+uploaded from the mapping; the streamed layers' blobs (and the embedding
+table) are page-locked where they lie, so the streaming engine copies them
+to HBM exactly as it copies pinned RAM.  ``FileBlobs`` (nt_file_lock) takes
+the first rung that the operating system and driver accept, in the pages'
+order of preference:
 
   "mmap pinned"          the read-only shared mapping, registered read-only;
   "mmap pinned private"  a private, writable, pre-faulted mapping of the
@@ -31,7 +34,6 @@ from __future__ import annotations
 
 import json
 import mmap
-import os
 import struct
 from dataclasses import asdict
 
@@ -114,44 +116,38 @@ def write_model(path: str, spec, hm) -> None:
 
 
 class ModelFile:
-    """A model file mapped read-only: ``spec``, and numpy views of every entry
-    (``layers`` as synth.HostModel lays them out, ``embd``, ``out``,
-    ``out_norm``)."""
+    """A model file opened through the native reader (nt_file_open: the
+    container, the header, the blob layout and every entry are checked
+    there): ``spec``, ``handle`` (the nt_file), and numpy views of every
+    entry (``layers`` as synth.HostModel lays them out, ``embd``, ``out``,
+    ``out_norm``).  The views read a second read-only mapping of the same
+    file (the same page-cache pages), so their lifetime follows Python's
+    references rather than nt_file_close.  A file the reader refuses raises
+    ValueError with its reason."""
 
     def __init__(self, path: str):
         self.path = path
-        with open(path, "rb") as f:
-            head = f.read(16)
-        if len(head) < 16 or head[:4] != MAGIC:
-            raise ValueError(f"{path}: not a model file")
-        version, hlen = struct.unpack("<IQ", head[4:16])
-        if version != VERSION:
-            raise ValueError(f"{path}: version {version}")
-        self._fd = os.open(path, os.O_RDONLY)
+        self.handle = None
+        self._mm = None
         try:
-            self._open(path, hlen)
+            self.handle = nt.nt_file_open(path)
+        except nt.NtError as e:
+            raise ValueError(str(e)) from None
+        try:
+            self._open(path)
         except Exception:
             self.close()
             raise
 
-    def _open(self, path: str, hlen: int) -> None:
-        size = os.fstat(self._fd).st_size
-        if 16 + hlen > size:
-            raise ValueError(f"{path}: header runs past the end of the file")
-        self._mm = mmap.mmap(self._fd, size, prot=mmap.PROT_READ)
-        meta = json.loads(self._mm[16:16 + hlen].decode())
+    def _open(self, path: str) -> None:
+        meta = json.loads(nt.nt_file_header(self.handle))
         self.spec = FileSpec(meta["spec"])
         self.blob_offsets, self.blob_bytes = meta["blob_offsets"], meta["blob_bytes"]
-        self.data0 = _up(16 + hlen)
-        self.entries = {k: (self.data0 + v[0], v[1]) for k, v in meta["entries"].items()}
-        # every entry page-aligned and, rounded up to whole pages (what page-locking covers), inside the file
-        for name, (off, n) in self.entries.items():
-            if off % ALIGN or n < 0 or off + _up(n) > size:
-                raise ValueError(f"{path}: entry {name} ({off}, {n} bytes) is misaligned or past the end")
-        s = self.spec
-        if any(self.entries[f"blob.{li}"][1] < self.blob_bytes for li in range(s.n_layers)):
-            raise ValueError(f"{path}: a layer blob is shorter than the blob layout")
+        self.entries = {k: nt.nt_file_entry(self.handle, k)[1:] for k in meta["entries"]}  # name -> (offset, bytes)
+        with open(path, "rb") as f:
+            self._mm = mmap.mmap(f.fileno(), 0, prot=mmap.PROT_READ)
         self._buf = buf = np.frombuffer(self._mm, dtype=np.uint8)
+        s = self.spec
 
         def view(name, dtype=np.uint8, shape=None):
             off, n = self.entries[name]
@@ -177,100 +173,51 @@ class ModelFile:
             d["ffn_norm"] = view(f"ffn_norm.{li}", np.float32)
             self.layers.append(d)
 
-    def address(self, name: str) -> int:
-        return self._buf.ctypes.data + self.entries[name][0]
-
     def close(self):
         self.embd = self.out = self.out_norm = None
         self.layers = []
         self._buf = None
-        try:
-            if hasattr(self, "_mm"):
+        if self._mm is not None:
+            try:
                 self._mm.close()
-        except BufferError:
-            pass  # views still alive elsewhere: the mapping closes with them
-        os.close(self._fd)
+            except BufferError:
+                pass  # views still alive elsewhere: the mapping closes with them
+            self._mm = None
+        if self.handle:
+            nt.nt_file_close(self.handle)  # refused while a FileBlobs still holds page-locked entries
+            self.handle = None
 
 
 class FileBlobs:
-    """The streamed layers of a mapped model file, page-locked in place: the
-    same interface as engine.HostBlobs (``blob`` maps a layer to its host
-    address, ``embd`` is the embedding table's), so DeviceModel streams from
-    the file mapping."""
+    """The streamed layers of a model file, page-locked through the native
+    reader (nt_file_lock): the same interface as engine.HostBlobs (``blob``
+    maps a layer to its page-locked host address, ``embd`` is the embedding
+    table's), so DeviceModel streams from the file.  ``rung_of`` records the
+    rung each range took, ``tier`` the lowest taken."""
 
     def __init__(self, ctx: nt.Context, mf: ModelFile, n_resident: int, allow_copy: bool = True):
         self.ctx, self.mf = ctx, mf
         s = mf.spec
         self.layers = list(range(n_resident, s.n_layers))
         self.offsets, self.nbytes = mf.blob_offsets, mf.blob_bytes
-        self._regs = []
-        self._copies = []
-        self._maps = []
-        self.rungs = []   # the rung each locked range took
         self.rung_of = {}  # entry name -> rung
         self.blob = {}
-        for li in self.layers:
-            self.blob[li] = self._lock(f"blob.{li}", allow_copy)
-        self.embd = self._lock("embd", allow_copy) if self.layers else None
+        try:
+            for li in self.layers:
+                self.blob[li] = self._lock(f"blob.{li}", allow_copy)
+            self.embd = self._lock("embd", allow_copy) if self.layers else None
+        except Exception:
+            self.close()
+            raise
         order = ("CPU memcpy", "mmap pinned private", "mmap pinned")
-        self.tier = next((t for t in order if t in self.rungs), "mmap pinned")  # the lowest rung taken
-
-    def _private_map(self, name: str):
-        """A private, writable, pre-faulted mapping of entry `name`: (mapping, address)."""
-        off, n = self.mf.entries[name]
-        gran = mmap.ALLOCATIONGRANULARITY
-        base = off // gran * gran
-        length = _up(off - base + _up(n), mmap.PAGESIZE)
-        flags = mmap.MAP_PRIVATE | getattr(mmap, "MAP_POPULATE", 0)
-        mm = mmap.mmap(self.mf._fd, length, flags=flags, prot=mmap.PROT_READ | mmap.PROT_WRITE, offset=base)
-        return mm, np.frombuffer(mm, dtype=np.uint8).ctypes.data + (off - base)
+        self.tier = next((t for t in order if t in self.rung_of.values()), "mmap pinned")  # the lowest rung taken
 
     def _lock(self, name: str, allow_copy: bool) -> int:
-        addr = self.mf.address(name)
-        nbytes = _up(self.mf.entries[name][1])
-        try:
-            nt.nt_host_register(self.ctx, addr, nbytes, read_only=True)
-            self._regs.append(addr)
-            self.rungs.append("mmap pinned")
-            self.rung_of[name] = "mmap pinned"
-            return addr
-        except nt.NtError:
-            pass
-        try:
-            mm, paddr = self._private_map(name)
-        except (OSError, ValueError):
-            mm = None
-        if mm is not None:
-            try:
-                nt.nt_host_register(self.ctx, paddr, nbytes, read_only=False)
-                self._regs.append(paddr)
-                self._maps.append(mm)
-                self.rungs.append("mmap pinned private")
-                self.rung_of[name] = "mmap pinned private"
-                return paddr
-            except nt.NtError:
-                mm.close()
-        if not allow_copy:
-            raise nt.NtError(nt.NT_ERR_CUDA, f"{name}: the file's pages cannot be page-locked in place")
-        # the pages of this file cannot be locked in place: one CPU copy into page-locked memory
-        import torch
-        self.rungs.append("CPU memcpy")
-        self.rung_of[name] = "CPU memcpy"
-        off = self.mf.entries[name][0]
-        buf = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
-        n = self.mf.entries[name][1]
-        buf[:n].numpy()[:] = self.mf._buf[off:off + n]
-        self._copies.append(buf)
-        return buf.data_ptr()
+        addr, rung = nt.nt_file_lock(self.ctx, self.mf.handle, name, allow_copy)
+        self.rung_of[name] = nt.FILE_RUNGS[rung]
+        return addr
 
     def close(self):
-        for addr in self._regs:
-            nt.nt_host_unregister(self.ctx, addr)
-        self._regs = []
-        self._copies = []
-        for mm in self._maps:
-            try:
-                mm.close()
-            except BufferError:
-                pass  # a view still alive elsewhere: the mapping closes with it
-        self._maps = []
+        for name in list(self.rung_of):
+            nt.nt_file_unlock(self.ctx, self.mf.handle, name)
+            del self.rung_of[name]

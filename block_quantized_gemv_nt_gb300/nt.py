@@ -118,6 +118,13 @@ _sig("nt_debug_stall_waits", [_ci])
 _sig("nt_ctx_gemv_plans", [_vp, _vp, _sz, ctypes.POINTER(_sz)])
 _sig("nt_model_graph_count", [_vp, _vp, ctypes.POINTER(_ci)])
 _sig("nt_model_prefill_chunk", [_vp, _vp, ctypes.POINTER(_ci)])
+_sig("nt_file_open", [ctypes.c_char_p, ctypes.POINTER(_vp)])
+_sig("nt_file_close", [_vp])
+_sig("nt_file_desc", [_vp, ctypes.POINTER(nt_model_desc)])
+_sig("nt_file_header", [_vp, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(_sz)])
+_sig("nt_file_entry", [_vp, ctypes.c_char_p, ctypes.POINTER(_vp), ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_sz)])
+_sig("nt_file_lock", [_vp, _vp, ctypes.c_char_p, _ci, ctypes.POINTER(_vp), ctypes.POINTER(_ci)])
+_sig("nt_file_unlock", [_vp, _vp, ctypes.c_char_p])
 
 EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "nt_block_bytes", "nt_block_elems",
             "nt_dequant_rows", "nt_gemv_q", "nt_gemv_q_swiglu", "nt_gemv_q_multi", "nt_rmsnorm", "nt_rope",
@@ -126,7 +133,9 @@ EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "
             "nt_attn_decode_static", "nt_layer_blob_layout", "nt_stream_layer", "nt_model_slot", "nt_spec_step",
             "nt_gemm_q", "nt_attn_verify", "nt_plan_residency", "nt_prefill", "nt_sample", "nt_model_set_sampler",
             "nt_host_register", "nt_host_unregister", "nt_stream_sync", "nt_debug_fail_copy", "nt_debug_host_delay",
-            "nt_debug_stall_waits", "nt_ctx_gemv_plans", "nt_model_graph_count", "nt_model_prefill_chunk"]
+            "nt_debug_stall_waits", "nt_ctx_gemv_plans", "nt_model_graph_count", "nt_model_prefill_chunk",
+            "nt_file_open", "nt_file_close", "nt_file_desc", "nt_file_header", "nt_file_entry", "nt_file_lock",
+            "nt_file_unlock"]
 
 
 def lib():
@@ -279,6 +288,61 @@ def nt_host_register(ctx, host_ptr: int, nbytes: int, read_only: bool = True):
 
 def nt_host_unregister(ctx, host_ptr: int):
     return ctx.check(_lib.nt_host_unregister(ctx.handle, host_ptr))
+
+
+# rungs of nt_file_lock, in the order of preference
+FILE_RUNGS = ("mmap pinned", "mmap pinned private", "CPU memcpy")
+
+
+def _no_ctx_check(status: int, what: str):
+    """Raise for a failed call made without a context (its reason is the thread's nt_last_error(NULL))."""
+    if status != NT_OK:
+        raise NtError(status, what + ": " + (_lib.nt_last_error(None) or b"").decode())
+    return status
+
+
+def nt_file_open(path: str) -> int:
+    """Open and check a model file; returns the nt_file handle."""
+    h = _vp()
+    _no_ctx_check(_lib.nt_file_open(os.fsencode(path), ctypes.byref(h)), "nt_file_open")
+    return h.value
+
+
+def nt_file_close(f: int):
+    return _no_ctx_check(_lib.nt_file_close(f), "nt_file_close")
+
+
+def nt_file_desc(f: int) -> nt_model_desc:
+    d = nt_model_desc()
+    _no_ctx_check(_lib.nt_file_desc(f, ctypes.byref(d)), "nt_file_desc")
+    return d
+
+
+def nt_file_header(f: int) -> str:
+    t, n = ctypes.c_char_p(), _sz()
+    _no_ctx_check(_lib.nt_file_header(f, ctypes.byref(t), ctypes.byref(n)), "nt_file_header")
+    return ctypes.string_at(t, n.value).decode()
+
+
+def nt_file_entry(f: int, name: str):
+    """Returns (address in the read-only mapping, offset in the file, bytes) of entry `name`."""
+    p, off, n = _vp(), ctypes.c_uint64(), _sz()
+    st = _lib.nt_file_entry(f, name.encode(), ctypes.byref(p), ctypes.byref(off), ctypes.byref(n))
+    if st != NT_OK:
+        raise NtError(st, f"nt_file_entry: no entry {name}")
+    return p.value, off.value, n.value
+
+
+def nt_file_lock(ctx, f: int, name: str, allow_copy: bool = True):
+    """Page-lock entry `name`; returns (page-locked address, rung index into FILE_RUNGS)."""
+    p, rung = _vp(), _ci()
+    ctx.check(_lib.nt_file_lock(ctx.handle, f, name.encode(), int(bool(allow_copy)), ctypes.byref(p),
+                                ctypes.byref(rung)))
+    return p.value, rung.value
+
+
+def nt_file_unlock(ctx, f: int, name: str):
+    return ctx.check(_lib.nt_file_unlock(ctx.handle, f, name.encode()))
 
 
 def nt_stream_sync(ctx, stream, timeout_us: int):

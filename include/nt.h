@@ -84,7 +84,8 @@ typedef struct nt_model nt_model;
  * allocates its scratch on the device. */
 nt_status nt_ctx_create(nt_ctx** out, int device, size_t scratch_bytes);
 nt_status nt_ctx_destroy(nt_ctx* ctx);
-/* nt_last_error(NULL) describes the last failed nt_ctx_create of this thread. */
+/* nt_last_error(NULL) describes this thread's last failed nt_ctx_create,
+ * nt_file_open or nt_file_close (the calls made without a context). */
 /* [road] Wait for all work of this context's device, then report any asynchronous
  * CUDA error or device-side flag and clear the flag: NT_ERR_TIMEOUT when a
  * bounded wait inside a kernel ran out; NT_ERR_INVALID_ARG when a position
@@ -400,6 +401,73 @@ nt_status nt_plan_residency(const nt_model_desc* desc, size_t hbm_weight_budget,
  * nt_host_unregister releases it; the caller unregisters before unmapping. */
 nt_status nt_host_register(nt_ctx* ctx, const void* host_ptr, size_t bytes, int read_only);
 nt_status nt_host_unregister(nt_ctx* ctx, const void* host_ptr);
+
+/* ---- host-file tier: model files ----------------------------------------- */
+
+/* A model file [about] (3-tier adaptive caching: NVMe/mmap fallback), the
+ * GGUF-style container of one model's weights:
+ *   offset 0   "NTQF", u32 version (1), u64 header length H (little-endian)
+ *   offset 16  H bytes of JSON: {"spec": {n_layers, d_model, n_qh, n_kvh,
+ *              head_dim, ffn, vocab, eps, theta, fmt: {wq, wk, wv, wo, wg,
+ *              wu, wd, embd, out: nt_fmt ids}, ...}, "blob_offsets": [7],
+ *              "blob_bytes": N, "entries": {name: [offset, bytes], ...}}
+ *   data       from the first multiple of 4096 after the header, entries at
+ *              4096-aligned offsets (relative to it): "embd", "out",
+ *              "out_norm" (fp32 [d]), and per layer l "blob.l" (its seven
+ *              weight matrices in the layout of nt_layer_blob_layout, so a
+ *              streamed layer is one contiguous range), "attn_norm.l",
+ *              "ffn_norm.l" (fp32 [d]).
+ * The KV cache is runtime state, not part of the file. */
+typedef struct nt_file nt_file;
+
+/* Rungs of nt_file_lock, in the pages' order of preference
+ * [feat] ("mmap pinned > CPU memcpy"). */
+enum { NT_FILE_MMAP_PINNED = 0, NT_FILE_MMAP_PINNED_PRIVATE = 1, NT_FILE_CPU_MEMCPY = 2 };
+
+/* [about] (NVMe/mmap fallback) Open a model file: map it read-only (shared)
+ * and check it before anything is handed out — the preamble, the header's
+ * JSON, every field the descriptor needs, the blob layout against this
+ * library's, and every entry a model needs, with the size its shape gives,
+ * 4096-aligned and (rounded up to 4096 bytes) inside the file.  A file that
+ * fails a check is refused with NT_ERR_INVALID_ARG; nt_last_error(NULL) then
+ * holds the reason on the calling thread.  Host-only: needs no GPU and no
+ * context.  The caller owns *out and closes it with nt_file_close. */
+nt_status nt_file_open(const char* path, nt_file** out);
+/* [about] (NVMe/mmap fallback) Unmap and free.  Refused (NT_ERR_INVALID_ARG, reason in nt_last_error(NULL))
+ * while an entry is still page-locked: nt_file_unlock each first. */
+nt_status nt_file_close(nt_file* f);
+/* [about] The descriptor stored in the file; kv_cap and stream_slots are 0 (runtime
+ * choices the caller sets before nt_model_init). */
+nt_status nt_file_desc(const nt_file* f, nt_model_desc* desc);
+/* [about] The header's JSON text (NUL-terminated, owned by f, valid until
+ * nt_file_close); *len (nullable) gets its length. */
+nt_status nt_file_header(const nt_file* f, const char** text, size_t* len);
+/* [about] Entry `name`: its address in the read-only mapping (*host_ptr; reading it
+ * faults the pages in from the file), its offset from the start of the file
+ * and its size.  Each output is nullable.  NT_ERR_INVALID_ARG for an unknown
+ * name.  Resident weights are uploaded from here by the caller. */
+nt_status nt_file_entry(const nt_file* f, const char* name, const void** host_ptr, uint64_t* offset,
+                        size_t* bytes);
+/* [feat] ("mmap pinned" data path) Page-lock entry `name` (its size rounded
+ * up to 4096 bytes) for streaming, taking the first rung the operating
+ * system and driver accept:
+ *   NT_FILE_MMAP_PINNED          the read-only mapping itself, registered read-only;
+ *   NT_FILE_MMAP_PINNED_PRIVATE  a private, writable, pre-faulted mapping of the
+ *                                range (copy-on-write: the file is never written),
+ *                                registered without the read-only flag;
+ *   NT_FILE_CPU_MEMCPY           (only when allow_copy) one CPU copy into
+ *                                page-locked memory (tail bytes zero).
+ * *pinned_out gets the page-locked address to stream from (a layer's
+ * nt_layer_ptrs.host_blob, the embedding table of nt_model_init), *rung_out
+ * (nullable) the rung.  Locking a locked entry returns the same address.
+ * NT_ERR_CUDA when neither mapping can be locked and allow_copy is 0;
+ * NT_ERR_OOM when the copy cannot be allocated. */
+nt_status nt_file_lock(nt_ctx* ctx, nt_file* f, const char* name, int allow_copy, const void** pinned_out,
+                       int* rung_out);
+/* [feat] ("mmap pinned" data path) Release what nt_file_lock took for `name` (unregister, unmap the private
+ * mapping or free the copy).  Call it with the context the entry was locked
+ * with, before destroying that context, once no stream still copies from it. */
+nt_status nt_file_unlock(nt_ctx* ctx, nt_file* f, const char* name);
 
 /* Streaming-engine copy step [feat] (SLEP double buffering), [cache]
  * (pinned-RAM H2D tier): enqueue on copy_stream the host-to-HBM copy of one

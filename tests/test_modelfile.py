@@ -51,3 +51,155 @@ def test_rejects_truncated_files(tmp_path):
         with pytest.raises(ValueError):
             modelfile.ModelFile(str(p))
     modelfile.ModelFile(str(path)).close()
+
+
+# ---- the native reader (nt_file_*), host-only --------------------------------
+
+def _written(tmp_path, name="tiny_q4_k_m"):
+    from block_quantized_gemv_nt_gb300 import modelfile
+    spec = synth.model_spec(name)
+    hm = synth.make_host_model(spec, with_kv=False)
+    path = tmp_path / "m.ntq"
+    modelfile.write_model(str(path), spec, hm)
+    return spec, hm, path
+
+
+def _split(data: bytes):
+    """(header dict, data section) of a file's bytes."""
+    import json
+    import struct
+    hlen = struct.unpack("<Q", data[8:16])[0]
+    data0 = (16 + hlen + 4095) // 4096 * 4096
+    return json.loads(data[16:16 + hlen]), data[data0:]
+
+
+def _join(header, body: bytes, version=1, raw=None) -> bytes:
+    """A file with header `header` (or the literal text `raw`) in front of data section `body`."""
+    import json
+    import struct
+    h = raw if raw is not None else json.dumps(header).encode()
+    pre = b"NTQF" + struct.pack("<IQ", version, len(h)) + h
+    return pre + bytes((-len(pre)) % 4096) + body
+
+
+@pytest.mark.parametrize("name", ["tiny_q4_k_m", "tiny_f16"])
+def test_native_reader_matches_writer(tmp_path, name):
+    """nt_file_open reads back what the writer laid out: the descriptor (the
+    runtime fields zero), the header text, and every entry's offset, size and
+    bytes in the mapping."""
+    import ctypes
+    from block_quantized_gemv_nt_gb300 import engine, modelfile, nt
+    spec, hm, path = _written(tmp_path, name)
+    f = nt.nt_file_open(str(path))
+    try:
+        d, want = nt.nt_file_desc(f), engine.model_desc(spec)
+        for fld, _ in nt.nt_model_desc._fields_:
+            if fld in ("kv_cap", "stream_slots"):
+                assert getattr(d, fld) == 0
+            else:
+                assert getattr(d, fld) == getattr(want, fld), fld
+        data = path.read_bytes()
+        header, _ = _split(data)
+        assert nt.nt_file_header(f) == data[16:16 + len(nt.nt_file_header(f))].decode()
+        data0 = (16 + len(nt.nt_file_header(f)) + 4095) // 4096 * 4096
+        for ename, (rel, n) in header["entries"].items():
+            addr, off, nbytes = nt.nt_file_entry(f, ename)
+            assert (off, nbytes) == (data0 + rel, n), ename
+            assert ctypes.string_at(addr, n) == data[off:off + n], ename
+        addr, off, n = nt.nt_file_entry(f, "blob.1")
+        wq = np.ascontiguousarray(hm.layers[1]["wq"])
+        assert ctypes.string_at(addr, wq.nbytes) == wq.tobytes()
+        with pytest.raises(nt.NtError):
+            nt.nt_file_entry(f, "blob.999")
+    finally:
+        nt.nt_file_close(f)
+    mf = modelfile.ModelFile(str(path))   # the Python views agree with the native offsets
+    assert np.array_equal(mf.layers[1]["wq"], hm.layers[1]["wq"])
+    mf.close()
+
+
+def test_native_reader_json(tmp_path):
+    """The header's JSON reader takes what RFC 8259 allows (escapes, a
+    surrogate pair, nested values, literals, exponents) and refuses what it
+    does not, each with a reason on the calling thread."""
+    from block_quantized_gemv_nt_gb300 import nt
+    _, _, path = _written(tmp_path)
+    header, body = _split(path.read_bytes())
+    ok = dict(header)
+    ok["note"] = ["café \U0001F600 \"q\" \\ /\t", {"a": [True, False, None, -0.5e-3, 12, []]}, {}]
+    p = tmp_path / "ok.ntq"
+    p.write_bytes(_join(ok, body))
+    f = nt.nt_file_open(str(p))
+    import json
+    assert json.loads(nt.nt_file_header(f))["note"] == ok["note"]
+    nt.nt_file_close(f)
+    text = path.read_bytes()[16:16 + len(json.dumps(header).encode())]
+    bad = {
+        "trailing comma": text[:-1] + b",}",
+        "unterminated string": b'{"spec": "abc',
+        "lone low surrogate": text[:-1] + b', "x": "\\udc00"}',
+        "bare control char": text[:-1] + b', "x": "a\x01b"}',
+        "leading zero": text[:-1] + b', "x": 012}',
+        "not an object": b"[1, 2]",
+        "nested too deep": text[:-1] + b', "x": ' + b"[" * 100 + b"]" * 100 + b"}",
+        "trailing garbage": text + b" x",
+    }
+    for why, raw in bad.items():
+        p = tmp_path / "bad.ntq"
+        p.write_bytes(_join(None, body, raw=raw))
+        with pytest.raises(nt.NtError) as ei:
+            nt.nt_file_open(str(p))
+        assert ei.value.status == nt.NT_ERR_INVALID_ARG, why
+        assert str(p) in str(ei.value), why
+        assert ("not a JSON object" if why == "not an object" else "not valid JSON") in str(ei.value), why
+
+
+def test_native_reader_refusals(tmp_path):
+    """Each check of nt_file_open refuses a file that breaks it, before any
+    entry is handed out: version, blob layout, entry alignment, a missing or
+    wrongly sized entry, a duplicate, an entry past the end, a format id."""
+    import copy
+    from block_quantized_gemv_nt_gb300 import nt
+    _, _, path = _written(tmp_path)
+    header, body = _split(path.read_bytes())
+
+    def edited(fn):
+        h = copy.deepcopy(header)
+        fn(h)
+        return _join(h, body)
+
+    cases = {
+        "version": _join(header, body, version=2),
+        "blob layout": edited(lambda h: h["blob_offsets"].__setitem__(1, h["blob_offsets"][1] + 256)),
+        "blob bytes": edited(lambda h: h.__setitem__("blob_bytes", h["blob_bytes"] + 256)),
+        "misaligned": edited(lambda h: h["entries"]["out"].__setitem__(0, h["entries"]["out"][0] + 16)),
+        "missing": edited(lambda h: h["entries"].pop("ffn_norm.1")),
+        "norm size": edited(lambda h: h["entries"]["attn_norm.0"].__setitem__(1, 4)),
+        "embd size": edited(lambda h: h["entries"]["embd"].__setitem__(1, h["entries"]["embd"][1] - 1)),
+        "short blob": edited(lambda h: h["entries"]["blob.0"].__setitem__(1, h["blob_bytes"] - 1)),
+        "past the end": edited(lambda h: h["entries"]["out"].__setitem__(0, len(body))),
+        "negative": edited(lambda h: h["entries"]["out"].__setitem__(0, -4096)),
+        "format id": edited(lambda h: h["spec"]["fmt"].__setitem__("wq", 7)),
+        "ragged": edited(lambda h: h["spec"].__setitem__("d_model", h["spec"]["d_model"] + 32)),
+        "gqa": edited(lambda h: h["spec"].__setitem__("n_kvh", h["spec"]["n_qh"] + 1)),
+        "no eps": edited(lambda h: h["spec"].pop("eps")),
+        "float dim": edited(lambda h: h["spec"].__setitem__("n_layers", 2.0)),
+    }
+    raw_dup = _join(header, body).replace(b'"entries": {', b'"entries": {"out": [0, 4], ', 1)
+    import struct
+    hl = struct.unpack("<Q", raw_dup[8:16])[0] + len(b'"out": [0, 4], ')
+    cases["duplicate"] = _join(None, body, raw=raw_dup[16:16 + hl])
+    for why, data in cases.items():
+        p = tmp_path / "bad.ntq"
+        p.write_bytes(data)
+        with pytest.raises(nt.NtError) as ei:
+            nt.nt_file_open(str(p))
+        assert ei.value.status == nt.NT_ERR_INVALID_ARG, why
+    p = tmp_path / "good.ntq"
+    p.write_bytes(_join(header, body))
+    nt.nt_file_close(nt.nt_file_open(str(p)))   # the unedited header still opens
+    with pytest.raises(nt.NtError):
+        nt.nt_file_open(str(tmp_path / "absent.ntq"))
+    with pytest.raises(nt.NtError):
+        nt.nt_file_open(str(tmp_path))          # a directory
+    assert nt.lib().nt_file_close(None) == nt.NT_ERR_INVALID_ARG

@@ -256,3 +256,47 @@ def test_model_file_streams_like_resident(ctx, tmp_path, where):
         mf.close()
     finally:
         os.unlink(path)
+
+
+def test_model_file_lock(ctx, tmp_path):
+    """nt_file_lock hands out page-locked ranges holding the entry's bytes
+    (in place, or NT_ERR_CUDA when in-place locking is refused and no copy
+    is allowed); locking again returns the same range; the file cannot be
+    closed while a range is locked; unlocking twice or locking an unknown
+    entry is refused."""
+    import ctypes
+    import os
+    from block_quantized_gemv_nt_gb300 import modelfile, nt
+    spec = synth.model_spec("tiny_q8_0")
+    path = os.path.join(str(tmp_path), "m.ntq")
+    modelfile.write_model(path, spec, synth.make_host_model(spec, with_kv=False))
+    data = open(path, "rb").read()
+    f = nt.nt_file_open(path)
+    held = []
+    try:
+        try:
+            a, rung = nt.nt_file_lock(ctx, f, "blob.0", allow_copy=False)
+            held.append("blob.0")
+            assert nt.FILE_RUNGS[rung] in ("mmap pinned", "mmap pinned private")
+        except nt.NtError as e:
+            assert e.status == nt.NT_ERR_CUDA
+        a, rung = nt.nt_file_lock(ctx, f, "blob.1")
+        held.append("blob.1")
+        print("rung:", nt.FILE_RUNGS[rung])
+        assert nt.nt_file_lock(ctx, f, "blob.1") == (a, rung)
+        _, off, n = nt.nt_file_entry(f, "blob.1")
+        assert a % 4096 == 0 and ctypes.string_at(a, n) == data[off:off + n]
+        with pytest.raises(nt.NtError) as ei:
+            nt.nt_file_lock(ctx, f, "blob.99")
+        assert ei.value.status == nt.NT_ERR_INVALID_ARG
+        with pytest.raises(nt.NtError):
+            nt.nt_file_close(f)
+        nt.nt_file_unlock(ctx, f, "blob.1")
+        held.remove("blob.1")
+        with pytest.raises(nt.NtError) as ei:
+            nt.nt_file_unlock(ctx, f, "blob.1")
+        assert ei.value.status == nt.NT_ERR_INVALID_ARG
+    finally:
+        for name in held:
+            nt.nt_file_unlock(ctx, f, name)
+        nt.nt_file_close(f)
