@@ -417,7 +417,8 @@ nt_status nt_host_unregister(nt_ctx* ctx, const void* host_ptr);
  *              weight matrices in the layout of nt_layer_blob_layout, so a
  *              streamed layer is one contiguous range), "attn_norm.l",
  *              "ffn_norm.l" (fp32 [d]).
- * The KV cache is runtime state, not part of the file. */
+ * The KV cache is runtime state, not part of the file.  An nt_file, like a
+ * context, is used from one host thread at a time. */
 typedef struct nt_file nt_file;
 
 /* Rungs of nt_file_lock, in the pages' order of preference
