@@ -21,6 +21,7 @@
 #include <sys/stat.h>
 #include <unistd.h>
 
+#include <atomic>
 #include <charconv>
 #include <cstring>
 #include <map>
@@ -38,6 +39,10 @@ namespace {
 
 constexpr uint64_t kFileAlign = 4096;  // entry alignment in the file, and the page-lock granule
 constexpr int kMaxJsonDepth = 32;
+
+// test hook (nt_debug_file_refuse_in_place): treat both in-place rungs as
+// refused, so nt_file_lock takes the CPU copy (process-wide)
+std::atomic<int> g_refuse_in_place{0};
 
 uint64_t up(uint64_t n, uint64_t a) { return (n + a - 1) / a * a; }
 
@@ -477,8 +482,9 @@ nt_status nt_file_lock(nt_ctx* ctx, nt_file* f, const char* name, int allow_copy
   const size_t n = size_t(up(e.bytes, kFileAlign));
   void* addr = f->base + e.off;
   Lock L;
+  const bool in_place = g_refuse_in_place.load(std::memory_order_relaxed) == 0;
   // rung 0, "mmap pinned": the read-only shared mapping itself, registered read-only
-  if (nt_host_register(ctx, addr, n, 1) == NT_OK) {
+  if (in_place && nt_host_register(ctx, addr, n, 1) == NT_OK) {
     L.rung = 0, L.ptr = addr;
   } else {
     // rung 1, "mmap pinned private": a private, writable, pre-faulted mapping of the range
@@ -491,7 +497,7 @@ nt_status nt_file_lock(nt_ctx* ctx, nt_file* f, const char* name, int allow_copy
 #ifdef MAP_POPULATE
     flags |= MAP_POPULATE;
 #endif
-    void* m = mmap(nullptr, mlen, PROT_READ | PROT_WRITE, flags, f->fd, off_t(mbase));
+    void* m = in_place ? mmap(nullptr, mlen, PROT_READ | PROT_WRITE, flags, f->fd, off_t(mbase)) : MAP_FAILED;
     if (m != MAP_FAILED) {
       void* p = static_cast<uint8_t*>(m) + (e.off - mbase);
       if (nt_host_register(ctx, p, n, 0) == NT_OK) {
@@ -522,6 +528,12 @@ nt_status nt_file_lock(nt_ctx* ctx, nt_file* f, const char* name, int allow_copy
   f->locks.emplace(name, L);
   *pinned_out = L.ptr;
   if (rung_out) *rung_out = L.rung;
+  return NT_OK;
+}
+
+nt_status nt_debug_file_refuse_in_place(int on) {
+  if (on != 0 && on != 1) return NT_ERR_INVALID_ARG;
+  g_refuse_in_place.store(on);
   return NT_OK;
 }
 

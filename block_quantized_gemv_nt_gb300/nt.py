@@ -125,6 +125,7 @@ _sig("nt_file_header", [_vp, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(_sz
 _sig("nt_file_entry", [_vp, ctypes.c_char_p, ctypes.POINTER(_vp), ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_sz)])
 _sig("nt_file_lock", [_vp, _vp, ctypes.c_char_p, _ci, ctypes.POINTER(_vp), ctypes.POINTER(_ci)])
 _sig("nt_file_unlock", [_vp, _vp, ctypes.c_char_p])
+_sig("nt_debug_file_refuse_in_place", [_ci])
 
 EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "nt_block_bytes", "nt_block_elems",
             "nt_dequant_rows", "nt_gemv_q", "nt_gemv_q_swiglu", "nt_gemv_q_multi", "nt_rmsnorm", "nt_rope",
@@ -135,7 +136,7 @@ EXPORTED = ["nt_ctx_create", "nt_ctx_destroy", "nt_ctx_sync", "nt_last_error", "
             "nt_host_register", "nt_host_unregister", "nt_stream_sync", "nt_debug_fail_copy", "nt_debug_host_delay",
             "nt_debug_stall_waits", "nt_ctx_gemv_plans", "nt_model_graph_count", "nt_model_prefill_chunk",
             "nt_file_open", "nt_file_close", "nt_file_desc", "nt_file_header", "nt_file_entry", "nt_file_lock",
-            "nt_file_unlock"]
+            "nt_file_unlock", "nt_debug_file_refuse_in_place"]
 
 
 def lib():
@@ -343,6 +344,14 @@ def nt_file_lock(ctx, f: int, name: str, allow_copy: bool = True):
 
 def nt_file_unlock(ctx, f: int, name: str):
     return ctx.check(_lib.nt_file_unlock(ctx.handle, f, name.encode()))
+
+
+def nt_debug_file_refuse_in_place(on: bool):
+    """Test hook: nt_file_lock treats both in-place rungs as refused (host side only)."""
+    st = _lib.nt_debug_file_refuse_in_place(int(bool(on)))
+    if st != NT_OK:
+        raise NtError(st, "nt_debug_file_refuse_in_place failed")
+    return st
 
 
 def nt_stream_sync(ctx, stream, timeout_us: int):

@@ -469,6 +469,12 @@ nt_status nt_file_lock(nt_ctx* ctx, nt_file* f, const char* name, int allow_copy
  * mapping or free the copy).  Call it with the context the entry was locked
  * with, before destroying that context, once no stream still copies from it. */
 nt_status nt_file_unlock(nt_ctx* ctx, nt_file* f, const char* name);
+/* [feat] ("mmap pinned > CPU memcpy") Test hook for the rung order, host
+ * side only: on = 1 makes every following nt_file_lock in this process treat
+ * both in-place rungs as refused, so it takes NT_FILE_CPU_MEMCPY (or fails
+ * with NT_ERR_CUDA when the copy is not allowed); on = 0 restores the order.
+ * Any other value is NT_ERR_INVALID_ARG. */
+nt_status nt_debug_file_refuse_in_place(int on);
 
 /* Streaming-engine copy step [feat] (SLEP double buffering), [cache]
  * (pinned-RAM H2D tier): enqueue on copy_stream the host-to-HBM copy of one

@@ -56,7 +56,7 @@ def test_every_context_call_refuses_a_null_context():
     NT_ERR_INVALID_ARG without touching CUDA, so this runs without a GPU."""
     from block_quantized_gemv_nt_gb300 import nt
     no_ctx = {"nt_ctx_create", "nt_last_error", "nt_block_bytes", "nt_block_elems", "nt_attn_decode_static",
-              "nt_layer_blob_layout", "nt_plan_residency", "nt_debug_stall_waits"}
+              "nt_layer_blob_layout", "nt_plan_residency", "nt_debug_stall_waits", "nt_debug_file_refuse_in_place"}
     L = nt.lib()
     checked = 0
     for name in nt.EXPORTED:

@@ -259,3 +259,12 @@ def test_native_reader_survives_mutated_headers(tmp_path):
         os.close(fd)
     print(f"mutated headers: {opened} opened, {refused} refused")
     assert opened > 0 and refused > 0
+
+
+def test_refuse_in_place_hook_arguments():
+    """The rung-order test hook takes 0 or 1 only (host-side state, no GPU)."""
+    from block_quantized_gemv_nt_gb300 import nt
+    assert nt.lib().nt_debug_file_refuse_in_place(2) == nt.NT_ERR_INVALID_ARG
+    assert nt.lib().nt_debug_file_refuse_in_place(-1) == nt.NT_ERR_INVALID_ARG
+    nt.nt_debug_file_refuse_in_place(True)
+    nt.nt_debug_file_refuse_in_place(False)

@@ -258,6 +258,41 @@ def test_model_file_streams_like_resident(ctx, tmp_path, where):
         os.unlink(path)
 
 
+def test_model_file_cpu_copy_rung(ctx, tmp_path):
+    """The third rung on the hardware: with both in-place rungs refused (the
+    host-side hook), every streamed range takes one CPU copy into page-locked
+    memory, or the lock fails with NT_ERR_CUDA when no copy is allowed; the
+    model streamed from those copies decodes bit-identically to the same
+    model held resident."""
+    import os
+    from block_quantized_gemv_nt_gb300 import engine, modelfile, nt
+    spec = synth.model_spec("small_q4_k_m_r1")
+    hm = synth.make_host_model(spec)
+    path = os.path.join(str(tmp_path), "m.ntq")
+    modelfile.write_model(path, spec, hm)
+    mf = modelfile.ModelFile(path)
+    nt.nt_debug_file_refuse_in_place(True)
+    try:
+        with pytest.raises(nt.NtError) as ei:
+            modelfile.FileBlobs(ctx, mf, spec.n_resident, allow_copy=False)
+        assert ei.value.status == nt.NT_ERR_CUDA
+        fb = modelfile.FileBlobs(ctx, mf, spec.n_resident)
+    finally:
+        nt.nt_debug_file_refuse_in_place(False)
+    assert fb.tier == "CPU memcpy" and set(fb.rung_of.values()) == {"CPU memcpy"}
+    assert len(fb.rung_of) == spec.n_layers - spec.n_resident + 1   # the streamed layers and the embedding table
+    hf = synth.HostModel(mf.spec, mf.layers, mf.embd, mf.out, mf.out_norm, hm.kcache, hm.vcache)
+    gf = engine.DeviceModel(ctx, mf.spec, hf, blobs=fb)
+    base = synth.model_spec("small_q4_k_m")
+    gr = engine.DeviceModel(ctx, base, hm)
+    for x, y in zip(_greedy(gf, spec, 3), _greedy(gr, base, 3)):
+        assert torch.equal(x, y)
+    gf.close()
+    gr.close()
+    fb.close()
+    mf.close()
+
+
 def test_model_file_lock(ctx, tmp_path):
     """nt_file_lock hands out page-locked ranges holding the entry's bytes
     (in place, or NT_ERR_CUDA when in-place locking is refused and no copy
