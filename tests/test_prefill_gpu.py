@@ -141,3 +141,41 @@ def test_prefill_tokens_free_on_return(ctx):
     for g, r in zip(out, ref):
         assert torch.equal(g, r)
     gm.close()
+
+
+@pytest.mark.slow
+def test_prefill_llama8b_q8_0_full_size(ctx):
+    """The 8B Q8_0 prefill workload at full size: the first 17 tokens of its
+    prompt (one chunk of 16 and a ragged one) at the position it starts from,
+    against the oracle run token by token — the logits after the prompt, the
+    K/V the prefill wrote in the first and the last layer, and one decode
+    step continued from the prefilled state."""
+    from block_quantized_gemv_nt_gb300 import engine, nt
+    spec = synth.model_spec("llama8b_q8_0")
+    n, n_bench = 17, 256
+    hm = synth.make_host_model(spec)
+    om = oracle.Model(spec, hm.layers, hm.embd, hm.out, hm.out_norm, hm.kcache, hm.vcache)
+    gm = engine.DeviceModel(ctx, spec, hm)
+    assert nt.nt_model_prefill_chunk(ctx, gm.handle) == 16
+    raw = synth.random_bytes(4 * n_bench, seed=spec.seed, stream=777).view(np.uint32)
+    prompt = (raw % spec.vocab).astype(np.int32)[:n]
+    pos0 = max(0, min(spec.n_prefill, spec.kv_cap - n_bench))
+    got = gm.prefill(prompt, pos0).cpu().numpy().astype(np.float64)
+    for i, t in enumerate(prompt):
+        ref = om.step(int(t), pos0 + i)
+    assert np.max(np.abs(got - ref)) <= 2e-2 * ref.std()
+    assert int(np.argmax(got)) == int(np.argmax(ref))
+    torch.cuda.synchronize()
+    for li in (0, spec.n_layers - 1):
+        for which in ("kcache", "vcache"):
+            g = gm.layers[li][which].cpu().numpy().astype(np.float64)[:, pos0:pos0 + n]
+            o = getattr(om, which)[li].astype(np.float64)[:, pos0:pos0 + n]
+            scale = np.sqrt(np.mean(o ** 2, axis=-1, keepdims=True))
+            bar = np.abs(o) * 2 ** -10 + 1e-4 * scale if li == 0 else 2e-2 * scale
+            assert np.all(np.abs(g - o) <= bar), (li, which)
+    tok = int(np.argmax(got))
+    g = gm.step(-1, 0).cpu().numpy().astype(np.float64)
+    r = om.step(tok, pos0 + n)
+    assert np.max(np.abs(g - r)) <= 2e-2 * r.std()
+    assert int(np.argmax(g)) == int(np.argmax(r))
+    gm.close()
