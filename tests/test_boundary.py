@@ -89,3 +89,52 @@ def test_every_declaration_cites_a_passage():
     for m in decls:
         if m.group(3) in NO_PASSAGE:
             assert "no counterpart" in m.group(1), m.group(3)
+
+
+def _prototypes():
+    """name -> (return type, [parameter types]) of every function nt.h declares."""
+    src = open(os.path.join(ROOT, "include", "nt.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    protos = {}
+    for m in re.finditer(r"^\s*(nt_status|const char\*|int)\s+(nt_\w+)\s*\(([^;]*?)\)\s*;", src, flags=re.M | re.S):
+        params = [p.strip() for p in " ".join(m.group(3).split()).split(",") if p.strip()]
+        if params == ["void"]:
+            params = []
+        types = []
+        for p in params:
+            p = re.sub(r"\[\s*\d*\s*\]$", "*", p)              # an array parameter is a pointer
+            p = re.sub(r"\s*\b\w+\s*(\*?)$", r"\1", p)        # drop the parameter's name
+            types.append(" ".join(p.replace("*", " * ").split()))
+        protos[m.group(2)] = (m.group(1), types)
+    return protos
+
+
+def _ctype_of(c_type: str):
+    """The ctypes classes a C parameter type may be bound as."""
+    if "*" in c_type:
+        return "pointer"
+    base = c_type.replace("const ", "").strip()
+    return {"int": ctypes.c_int, "int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64, "uint64_t": ctypes.c_uint64,
+            "size_t": ctypes.c_size_t, "float": ctypes.c_float}[base]
+
+
+def test_binding_matches_header_prototypes():
+    """The ctypes binding declares every entry point with the header's
+    parameter count and types (pointers as pointers, each integer and float
+    width as itself) and its return type: a mismatch would pass arguments
+    in the wrong registers."""
+    from block_quantized_gemv_nt_gb300 import nt
+    lib = nt.lib()
+    protos = _prototypes()
+    assert set(protos) == set(_declared())
+    for name, (ret, params) in protos.items():
+        f = getattr(lib, name)
+        assert f.argtypes is not None, name
+        assert len(f.argtypes) == len(params), (name, params, f.argtypes)
+        for c_type, py in zip(params, f.argtypes):
+            want = _ctype_of(c_type)
+            if want == "pointer":
+                assert py in (ctypes.c_void_p, ctypes.c_char_p) or issubclass(py, ctypes._Pointer), (name, c_type, py)
+            else:
+                assert py is want, (name, c_type, py)
+        assert f.restype is (ctypes.c_char_p if ret == "const char*" else ctypes.c_int), name
